@@ -1,0 +1,246 @@
+"""CPU oracle for MiniMax-M3 block-sparse attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never touches it, and it never touches the product path.
+
+The arithmetic lives in ``msa_oracle.c`` (plain C, fp64, OpenMP over queries);
+this module compiles it with gcc and wraps it with ctypes over numpy arrays.
+Inputs are raw element bits (bf16 as uint16, E4M3 as uint8) so the oracle
+decodes every element itself.
+
+Which statement on the pages each function follows:
+  * ``select_prefill`` / ``select_decode`` -- block scores (max over causal,
+    document-local keys of the unscaled index dot product) and top-k with forced
+    init/local blocks: TensorRT-LLM "MiniMaxM3SparseAttentionConfig" (class
+    description; fields sparse_topk_blocks, sparse_init_blocks,
+    sparse_local_blocks, sparse_score_type, indexer_kv_dtype) and NeMo AutoModel
+    "...minimax_m3_vl.msa" (MSAMicrobatch.select_blocks, _SelectionPlan).
+  * ``attend_prefill`` / ``attend_decode`` -- sparse GQA attention over the
+    selected blocks: the TensorRT-LLM class description and NeMo
+    ``sparse_attention`` / ``_SparseAttention.forward``.
+  * ``pack_metadata`` / ``pack`` / ``unpack`` -- NeMo layout-from-doc_ids
+    constructor, ``_contiguous_runs``, ``MSAMicrobatch.pack`` / ``unpack``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+H, G, D, DI, BLOCK = 64, 4, 128, 128, 128
+PACK_ERRORS = {
+    1: "negative document id",
+    2: "interrupted document",
+    3: "no real token",
+    4: "empty map",
+    5: "coordinates past int32",
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (-O2, OpenMP, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+             "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            Dbl = ctypes.c_double
+            lib.oracle_select_prefill.argtypes = [P, P, I, P, I, P, I64, I, I, I, P, P, P, I]
+            lib.oracle_attend_prefill.argtypes = [P, P, P, P, I, P, I64, P, I, Dbl, P]
+            lib.oracle_select_decode.argtypes = [P, P, I, P, P, P, I, P, I64, I, I, I, P, P]
+            lib.oracle_attend_decode.argtypes = [P, P, P, P, P, P, I, P, I64, P, I, Dbl, P]
+            lib.oracle_pack_metadata.argtypes = [P, I64, I64, P, P, P, P, P, P]
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = Dbl
+            for f in (lib.oracle_select_prefill, lib.oracle_attend_prefill,
+                      lib.oracle_select_decode, lib.oracle_attend_decode,
+                      lib.oracle_pack_metadata):
+                f.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(x):
+    """numpy view of raw element bits: bf16 -> uint16, e4m3 -> uint8."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16)
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy()
+            return x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x)
+
+
+def _dtype_code(a):
+    if a.dtype == np.uint16:
+        return 0
+    if a.dtype == np.uint8:
+        return 1
+    raise TypeError("index tensors must be bf16 (uint16 bits) or e4m3 (uint8 bits)")
+
+
+def _i32(x):
+    return np.ascontiguousarray(_bits(x), dtype=np.int32)
+
+
+def _i64(x):
+    return np.ascontiguousarray(_bits(x), dtype=np.int64)
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().oracle_e4m3_value(byte)
+
+
+def select_prefill(index_q, index_k, cu_seqlens, tokens, topk=16, init=0, local=1,
+                   return_scores=False):
+    """q2k int32 [G, n, topk] and relative top-k gap [G, n] for compact tokens."""
+    lib = _load()
+    iq, ik = _bits(index_q), _bits(index_k)
+    code = _dtype_code(iq)
+    cu = _i32(cu_seqlens)
+    tok = _i64(tokens)
+    n = tok.shape[0]
+    q2k = np.full((G, n, topk), -7, dtype=np.int32)
+    gap = np.zeros((G, n), dtype=np.float64)
+    scores = None
+    max_nb = 0
+    if return_scores:
+        lens = np.diff(cu.astype(np.int64))
+        max_nb = int((lens.max() + BLOCK - 1) // BLOCK)
+        scores = np.full((n, G, max_nb), np.nan)
+    rc = lib.oracle_select_prefill(_ptr(iq), _ptr(ik), code, _ptr(cu), cu.shape[0] - 1, _ptr(tok), n,
+                                   topk, init, local, _ptr(q2k), _ptr(gap), _ptr(scores), max_nb)
+    if rc:
+        raise ValueError("oracle_select_prefill failed")
+    return (q2k, gap, scores) if return_scores else (q2k, gap)
+
+
+def attend_prefill(q, k, v, cu_seqlens, tokens, q2k, scale):
+    """fp64 out [n, H, D] for compact tokens, given their q2k rows [G, n, topk]."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    cu = _i32(cu_seqlens)
+    tok = _i64(tokens)
+    n = tok.shape[0]
+    q2k = _i32(q2k)
+    topk = q2k.shape[2]
+    out = np.zeros((n, H, D), dtype=np.float64)
+    lib.oracle_attend_prefill(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), cu.shape[0] - 1, _ptr(tok), n,
+                              _ptr(q2k), topk, float(scale), _ptr(out))
+    return out
+
+
+def select_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None,
+                  requests=None, topk=16, init=0, local=1):
+    """q2k int32 [G, n, topk] and gap [G, n] for the listed requests."""
+    lib = _load()
+    iq, ik = _bits(index_q), _bits(index_k_cache)
+    code = _dtype_code(iq)
+    sl = _i32(seq_lens)
+    pt = None if page_table is None else _i32(page_table)
+    cuk = None if cu_seqlens_k is None else _i64(cu_seqlens_k)
+    if pt is None and cuk is None:
+        raise ValueError("need page_table or cu_seqlens_k")
+    req = _i64(np.arange(sl.shape[0]) if requests is None else requests)
+    n = req.shape[0]
+    max_pages = 0 if pt is None else pt.shape[1]
+    q2k = np.full((G, n, topk), -7, dtype=np.int32)
+    gap = np.zeros((G, n), dtype=np.float64)
+    rc = lib.oracle_select_decode(_ptr(iq), _ptr(ik), code, _ptr(sl), _ptr(pt), _ptr(cuk), max_pages,
+                                  _ptr(req), n, topk, init, local, _ptr(q2k), _ptr(gap))
+    if rc:
+        raise ValueError("oracle_select_decode failed")
+    return q2k, gap
+
+
+def attend_decode(q, k_cache, v_cache, seq_lens, q2k, scale, page_table=None, cu_seqlens_k=None,
+                  requests=None):
+    """fp64 out [n, H, D] for the listed requests, given their q2k rows [G, n, topk]."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    sl = _i32(seq_lens)
+    pt = None if page_table is None else _i32(page_table)
+    cuk = None if cu_seqlens_k is None else _i64(cu_seqlens_k)
+    req = _i64(np.arange(sl.shape[0]) if requests is None else requests)
+    n = req.shape[0]
+    q2k = _i32(q2k)
+    topk = q2k.shape[2]
+    max_pages = 0 if pt is None else pt.shape[1]
+    out = np.zeros((n, H, D), dtype=np.float64)
+    lib.oracle_attend_decode(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sl), _ptr(pt), _ptr(cuk), max_pages,
+                             _ptr(req), n, _ptr(q2k), topk, float(scale), _ptr(out))
+    return out
+
+
+def pack_metadata(doc_ids):
+    """(cu_seqlens int32 [docs+1], token_rows int64 [tokens], max_seqlen) or ValueError."""
+    lib = _load()
+    ids = _i64(doc_ids)
+    if ids.ndim != 2:
+        raise ValueError("doc_ids must be [batch, seq]")
+    b, s = ids.shape
+    n = max(b * s, 1)
+    cu = np.zeros(n + 1, dtype=np.int32)
+    rows = np.zeros(n, dtype=np.int64)
+    nd, nt, mx, bad = (np.zeros(1, dtype=np.int64) for _ in range(4))
+    rc = lib.oracle_pack_metadata(_ptr(ids), b, s, _ptr(cu), _ptr(rows), _ptr(nd), _ptr(nt),
+                                  _ptr(mx), _ptr(bad))
+    if rc:
+        err = ValueError(PACK_ERRORS[rc])
+        err.code = rc
+        err.bad_row = int(bad[0])
+        raise err
+    return cu[: nd[0] + 1].copy(), rows[: nt[0]].copy(), int(mx[0])
+
+
+def pack(external, token_rows):
+    """Gather external[batch, seq, ...] -> [tokens, ...] (NeMo MSAMicrobatch.pack)."""
+    x = np.asarray(external)
+    flat = x.reshape((-1,) + x.shape[2:])
+    return flat[np.asarray(token_rows)]
+
+
+def unpack(packed, token_rows, batch, seq):
+    """Scatter packed[tokens, ...] -> [batch, seq, ...], zeros elsewhere (NeMo unpack)."""
+    p = np.asarray(packed)
+    out = np.zeros((batch * seq,) + p.shape[1:], dtype=p.dtype)
+    out[np.asarray(token_rows)] = p
+    return out.reshape((batch, seq) + p.shape[1:])
+
+
+def exempt_rows(gap, rel=1e-5):
+    """Boolean [G, n]: rows whose k-th / (k+1)-th non-forced scores are a near tie."""
+    return np.asarray(gap) < rel

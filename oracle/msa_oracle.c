@@ -1,0 +1,415 @@
+/*
+ * msa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct CPU statement of what MiniMax-M3 two-step
+ * block-sparse attention computes: block scoring, top-k block selection and
+ * sparse GQA attention over the selected blocks, for the packed-document
+ * prefill layout and for the paged / contiguous decode cache.  Only the tests,
+ * the smoke check and the CPU-baseline leg of the benchmark may load it.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (three web pages on the method):
+ *   [TRT] TensorRT-LLM, "MiniMaxM3SparseAttentionConfig": class description
+ *         (index branch scores blocks, top-k per (kv_head, q_token), init blocks
+ *         forced at the head and local blocks at the tail; sparse GQA attention
+ *         over the selected blocks), fields sparse_block_size,
+ *         sparse_topk_blocks, sparse_init_blocks, sparse_local_blocks,
+ *         sparse_score_type ('max'), indexer_kv_dtype ('fp8' = unscaled E4M3
+ *         with FP32 score accumulation), paged index-K cache [num_slots,1,dim].
+ *   [NEMO] NeMo AutoModel, "nemo_automodel.components.models.minimax_m3_vl.msa":
+ *         MSAMicrobatch.select_blocks (hard top-k over unnormalised QK maxima,
+ *         document-local block ids, int32 [4, tokens, 16] padded with -1),
+ *         _SelectionPlan (candidate and forced [tokens, blocks] masks),
+ *         sparse_attention / _SparseAttention.forward (bf16 q[tokens,64,128],
+ *         k/v[tokens,4,128] -> out[tokens,64,128]), the layout-from-doc_ids
+ *         constructor and _contiguous_runs (document map rules).
+ *
+ * Precision: index scores are summed in fp64 (exact for E4M3 operands, exact
+ * to far below fp32 resolution for bf16) and the selection decision is taken
+ * on the fp32 rounding of that sum, because the pages fix FP32 as the score
+ * precision ([TRT] indexer_kv_dtype).  Attention is computed in fp64.
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ * forced blocks occupy top-k slots; q2k rows list block ids ascending then -1;
+ * equal scores prefer the lower block id; no scale on index scores; the
+ * diagonal block takes its max over causal keys only; blocks restart at each
+ * document (request) start; query head h uses kv/index head h / (H / G);
+ * softmax scale is a caller argument (1/sqrt(128) in the workloads); a decode
+ * query sits at position len-1 and sees its own key.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_HEADS 64
+#define OR_KV 4
+#define OR_DIM 128
+#define OR_IDIM 128
+#define OR_BLOCK 128
+#define OR_MAXTOPK 64
+
+/* ---- element decoding -------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 ("fn": no infinities): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+ * m/8 * 2^-6; S.1111.111 is NaN. */
+double oracle_e4m3_value(uint8_t byte) {
+  int sign = byte >> 7;
+  int e = (byte >> 3) & 15;
+  int m = byte & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+static double index_elem(const void* base, int dtype, int64_t i) {
+  if (dtype == 0) return bf16_value(((const uint16_t*)base)[i]);
+  return oracle_e4m3_value(((const uint8_t*)base)[i]);
+}
+
+/* ---- step 1: block scores ---------------------------------------------
+ * score(g, b) = max over causal keys p in block b (128b <= p <= min(128b+127,
+ * pos)) of <index_q[g], index_k[key p]>  ([TRT] sparse_score_type 'max';
+ * [NEMO] select_blocks "unnormalized QK maxima").  key_row[p] maps a document-
+ * local key position to its row in the index-K array. */
+static void block_scores(const void* iq_row /* [G][IDIM] of this query */,
+                         const void* ik /* [rows][IDIM] */, int dtype,
+                         const int64_t* key_row, int64_t pos, int nb,
+                         double* s64 /* [G][nb] */) {
+  for (int g = 0; g < OR_KV; ++g)
+    for (int b = 0; b < nb; ++b) s64[g * nb + b] = -INFINITY;
+  for (int64_t p = 0; p <= pos; ++p) {
+    int b = (int)(p / OR_BLOCK);
+    int64_t row = key_row[p];
+    for (int g = 0; g < OR_KV; ++g) {
+      double acc = 0.0;
+      for (int c = 0; c < OR_IDIM; ++c)
+        acc += index_elem(iq_row, dtype, (int64_t)g * OR_IDIM + c) *
+               index_elem(ik, dtype, row * OR_IDIM + c);
+      if (acc > s64[g * nb + b]) s64[g * nb + b] = acc;
+    }
+  }
+}
+
+/* ---- step 2: top-k selection with forced blocks -------------------------
+ * F = [0, init) u [nb-local, nb) restricted to [0, nb) ([TRT]
+ * sparse_init_blocks / sparse_local_blocks: forced "into the top-k regardless
+ * of score"; [NEMO] _SelectionPlan forced mask).  If nb <= topk every candidate
+ * is kept.  Otherwise the non-forced candidates are ordered by (score desc,
+ * id asc) and the first topk-|F| join F.  Output: ascending ids, then -1.
+ * Returns the relative gap between the last kept and first rejected
+ * non-forced score (INFINITY when nothing was decided by score). */
+static double select_row(const float* s32 /* [nb] */, int nb, int topk,
+                         int init, int local, int32_t* out /* [topk] */) {
+  char* keep = (char*)calloc((size_t)nb, 1);
+  int* cand = (int*)malloc(sizeof(int) * (size_t)nb);
+  double gap = INFINITY;
+  int n_keep = 0, n_cand = 0;
+  if (nb <= topk) {
+    for (int b = 0; b < nb; ++b) keep[b] = 1;
+    n_keep = nb;
+  } else {
+    for (int b = 0; b < nb; ++b) {
+      int forced = (b < init) || (b >= nb - local);
+      if (forced) {
+        keep[b] = 1;
+        ++n_keep;
+      } else {
+        cand[n_cand++] = b;
+      }
+    }
+    int need = topk - n_keep;
+    /* selection sort by (score desc, id asc): slow and plain */
+    for (int i = 0; i < n_cand && i <= need; ++i) {
+      int best = i;
+      for (int j = i + 1; j < n_cand; ++j) {
+        float sj = s32[cand[j]], sb = s32[cand[best]];
+        if (sj > sb || (sj == sb && cand[j] < cand[best])) best = j;
+      }
+      int tmp = cand[i];
+      cand[i] = cand[best];
+      cand[best] = tmp;
+    }
+    for (int i = 0; i < need && i < n_cand; ++i) {
+      keep[cand[i]] = 1;
+      ++n_keep;
+    }
+    if (need > 0 && n_cand > need) {
+      double a = s32[cand[need - 1]], c = s32[cand[need]];
+      double den = fmax(fabs(a), fabs(c));
+      gap = den > 0 ? fabs(a - c) / den : 0.0;
+    }
+  }
+  int w = 0;
+  for (int b = 0; b < nb; ++b)
+    if (keep[b]) out[w++] = b;
+  while (w < topk) out[w++] = -1;
+  free(keep);
+  free(cand);
+  return gap;
+}
+
+/* ---- step 3: sparse GQA attention over the selected blocks --------------
+ * For query head h (kv head g = h / (H/G)): keys J = { p <= pos : p / 128 is
+ * one of the ids in q2k[g] }; z_p = scale * <q[h], k[key p, g]>;
+ * out[h] = sum_p softmax(z)_p v[key p, g]   ([TRT] class description, sparse
+ * GQA over the selected blocks; [NEMO] sparse_attention).  No keys -> zeros. */
+static void attend_query(const uint16_t* q_row /* [H][D] */,
+                         const uint16_t* k /* [rows][G][D] */,
+                         const uint16_t* v, const int64_t* key_row, int64_t pos,
+                         const int32_t* q2k_g /* q2k_g[g * stride + i] */,
+                         int64_t q2k_stride, int topk, double scale,
+                         double* out /* [H][D] */) {
+  int64_t nkeys_max = (int64_t)topk * OR_BLOCK;
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)nkeys_max);
+  double* z = (double*)malloc(sizeof(double) * (size_t)nkeys_max);
+  for (int g = 0; g < OR_KV; ++g) {
+    int64_t nk = 0;
+    for (int i = 0; i < topk; ++i) {
+      int32_t b = q2k_g[g * q2k_stride + i];
+      if (b < 0) continue;
+      for (int64_t p = (int64_t)b * OR_BLOCK; p < (int64_t)(b + 1) * OR_BLOCK && p <= pos; ++p)
+        keys[nk++] = p;
+    }
+    for (int hh = 0; hh < OR_HEADS / OR_KV; ++hh) {
+      int h = g * (OR_HEADS / OR_KV) + hh;
+      double* o = out + (int64_t)h * OR_DIM;
+      for (int c = 0; c < OR_DIM; ++c) o[c] = 0.0;
+      if (nk == 0) continue;
+      double zmax = -INFINITY;
+      for (int64_t j = 0; j < nk; ++j) {
+        int64_t row = key_row[keys[j]];
+        double acc = 0.0;
+        for (int c = 0; c < OR_DIM; ++c)
+          acc += bf16_value(q_row[h * OR_DIM + c]) *
+                 bf16_value(k[(row * OR_KV + g) * OR_DIM + c]);
+        z[j] = scale * acc;
+        if (z[j] > zmax) zmax = z[j];
+      }
+      double denom = 0.0;
+      for (int64_t j = 0; j < nk; ++j) {
+        z[j] = exp(z[j] - zmax);
+        denom += z[j];
+      }
+      for (int64_t j = 0; j < nk; ++j) {
+        int64_t row = key_row[keys[j]];
+        double w = z[j] / denom;
+        for (int c = 0; c < OR_DIM; ++c)
+          o[c] += w * bf16_value(v[(row * OR_KV + g) * OR_DIM + c]);
+      }
+    }
+  }
+  free(keys);
+  free(z);
+}
+
+/* ---- geometry ------------------------------------------------------------ */
+
+/* Document of compact token t: the d with cu[d] <= t < cu[d+1]. */
+static int doc_of(const int32_t* cu, int num_docs, int64_t t) {
+  int lo = 0, hi = num_docs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (cu[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+/* Decode: key position p of request r lives at slot page*128 + p%128 with
+ * page = page_table[r][p/128] (paged, [TRT] paged index-K cache parallel to
+ * the K/V cache) or at row cu_seqlens_k[r] + p (contiguous). */
+static void decode_rows(const int32_t* page_table, const int64_t* cu_k,
+                        int max_pages, int r, int64_t len, int64_t* rows) {
+  for (int64_t p = 0; p < len; ++p) {
+    if (page_table)
+      rows[p] = (int64_t)page_table[(int64_t)r * max_pages + p / OR_BLOCK] * OR_BLOCK + p % OR_BLOCK;
+    else
+      rows[p] = cu_k[r] + p;
+  }
+}
+
+/* ---- exported drivers ---------------------------------------------------- */
+
+/* Prefill selection for a list of compact query tokens.
+ * q2k: [G][n][topk]; gap: [G][n]; s64_out (optional): [n][G][max_nb]. */
+int oracle_select_prefill(const void* index_q, const void* index_k, int dtype,
+                          const int32_t* cu_seqlens, int num_docs,
+                          const int64_t* tokens, int64_t n, int topk, int init,
+                          int local, int32_t* q2k, double* gap,
+                          double* s64_out, int max_nb) {
+  if (topk < 1 || topk > OR_MAXTOPK) return 1;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t t = tokens[i];
+    int d = doc_of(cu_seqlens, num_docs, t);
+    int64_t start = cu_seqlens[d];
+    int64_t pos = t - start;
+    int nb = (int)(pos / OR_BLOCK) + 1;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(pos + 1));
+    double* s64 = (double*)malloc(sizeof(double) * OR_KV * (size_t)nb);
+    float* s32 = (float*)malloc(sizeof(float) * (size_t)nb);
+    for (int64_t p = 0; p <= pos; ++p) rows[p] = start + p;
+    const void* iq_row = (dtype == 0) ? (const void*)((const uint16_t*)index_q + t * OR_KV * OR_IDIM)
+                                      : (const void*)((const uint8_t*)index_q + t * OR_KV * OR_IDIM);
+    block_scores(iq_row, index_k, dtype, rows, pos, nb, s64);
+    for (int g = 0; g < OR_KV; ++g) {
+      for (int b = 0; b < nb; ++b) s32[b] = (float)s64[g * nb + b];
+      gap[g * n + i] = select_row(s32, nb, topk, init, local, q2k + ((int64_t)g * n + i) * topk);
+      if (s64_out && nb <= max_nb)
+        for (int b = 0; b < nb; ++b) s64_out[(i * OR_KV + g) * max_nb + b] = s64[g * nb + b];
+    }
+    free(rows);
+    free(s64);
+    free(s32);
+  }
+  return err;
+}
+
+/* Prefill attention for a list of compact query tokens, given q2k rows for
+ * those tokens ([G][n][topk]).  out: [n][H][D] fp64. */
+int oracle_attend_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const int32_t* cu_seqlens, int num_docs,
+                          const int64_t* tokens, int64_t n, const int32_t* q2k,
+                          int topk, double scale, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t t = tokens[i];
+    int d = doc_of(cu_seqlens, num_docs, t);
+    int64_t start = cu_seqlens[d];
+    int64_t pos = t - start;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(pos + 1));
+    for (int64_t p = 0; p <= pos; ++p) rows[p] = start + p;
+    attend_query(q + t * OR_HEADS * OR_DIM, k, v, rows, pos, q2k + i * topk,
+                 n * topk, topk, scale, out + i * OR_HEADS * OR_DIM);
+    free(rows);
+  }
+  return 0;
+}
+
+/* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n]. */
+int oracle_select_decode(const void* index_q, const void* index_k_cache, int dtype,
+                         const int32_t* seq_lens, const int32_t* page_table,
+                         const int64_t* cu_seqlens_k, int max_pages,
+                         const int64_t* requests, int64_t n, int topk, int init,
+                         int local, int32_t* q2k, double* gap) {
+  if (topk < 1 || topk > OR_MAXTOPK) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int r = (int)requests[i];
+    int64_t len = seq_lens[r];
+    int64_t pos = len - 1;
+    int nb = (int)(pos / OR_BLOCK) + 1;
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)len);
+    double* s64 = (double*)malloc(sizeof(double) * OR_KV * (size_t)nb);
+    float* s32 = (float*)malloc(sizeof(float) * (size_t)nb);
+    decode_rows(page_table, cu_seqlens_k, max_pages, r, len, rows);
+    const void* iq_row = (dtype == 0) ? (const void*)((const uint16_t*)index_q + (int64_t)r * OR_KV * OR_IDIM)
+                                      : (const void*)((const uint8_t*)index_q + (int64_t)r * OR_KV * OR_IDIM);
+    block_scores(iq_row, index_k_cache, dtype, rows, pos, nb, s64);
+    for (int g = 0; g < OR_KV; ++g) {
+      for (int b = 0; b < nb; ++b) s32[b] = (float)s64[g * nb + b];
+      gap[g * n + i] = select_row(s32, nb, topk, init, local, q2k + ((int64_t)g * n + i) * topk);
+    }
+    free(rows);
+    free(s64);
+    free(s32);
+  }
+  return 0;
+}
+
+/* Decode attention for a list of requests given q2k rows ([G][n][topk]).
+ * out: [n][H][D] fp64. */
+int oracle_attend_decode(const uint16_t* q, const uint16_t* k_cache,
+                         const uint16_t* v_cache, const int32_t* seq_lens,
+                         const int32_t* page_table, const int64_t* cu_seqlens_k,
+                         int max_pages, const int64_t* requests, int64_t n,
+                         const int32_t* q2k, int topk, double scale, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int r = (int)requests[i];
+    int64_t len = seq_lens[r];
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)len);
+    decode_rows(page_table, cu_seqlens_k, max_pages, r, len, rows);
+    attend_query(q + (int64_t)r * OR_HEADS * OR_DIM, k_cache, v_cache, rows, len - 1,
+                 q2k + i * topk, n * topk, topk, scale, out + i * OR_HEADS * OR_DIM);
+    free(rows);
+  }
+  return 0;
+}
+
+/* Packed layout of a document map ([NEMO] layout-from-doc_ids constructor and
+ * _contiguous_runs): ids [batch][seq], 0 = padding, each positive id one
+ * contiguous run within its row.  Documents are the runs in row-major order;
+ * token_rows lists the flat index of every real token in that order.
+ * Returns 0 on success, 1 negative id, 2 interrupted document (bad_row set to
+ * the flat index where the id reappears), 3 no real token, 4 empty map,
+ * 5 coordinates past int32. */
+int oracle_pack_metadata(const int64_t* ids, int64_t batch, int64_t seq,
+                         int32_t* cu_seqlens /* [batch*seq+1] */,
+                         int64_t* token_rows /* [batch*seq] */, int64_t* num_docs,
+                         int64_t* total_tokens, int64_t* max_seqlen,
+                         int64_t* bad_row) {
+  *bad_row = -1;
+  if (batch <= 0 || seq <= 0) return 4;
+  if (batch * seq > INT32_MAX) return 5;
+  for (int64_t i = 0; i < batch * seq; ++i)
+    if (ids[i] < 0) {
+      *bad_row = i;
+      return 1;
+    }
+  /* interrupted: an id whose run is followed, later in the same row, by
+   * another run of the same id */
+  for (int64_t r = 0; r < batch; ++r) {
+    const int64_t* row = ids + r * seq;
+    for (int64_t i = 0; i < seq; ++i) {
+      if (row[i] == 0) continue;
+      int starts_run = (i == 0) || (row[i - 1] != row[i]);
+      if (!starts_run) continue;
+      for (int64_t j = 0; j < i; ++j)
+        if (row[j] == row[i]) {
+          *bad_row = r * seq + i;
+          return 2;
+        }
+    }
+  }
+  int64_t nd = 0, nt = 0, mx = 0, cur = 0;
+  cu_seqlens[0] = 0;
+  for (int64_t r = 0; r < batch; ++r) {
+    for (int64_t i = 0; i < seq; ++i) {
+      int64_t id = ids[r * seq + i];
+      if (id == 0) continue;
+      int starts_run = (i == 0) || (ids[r * seq + i - 1] != id);
+      if (starts_run) {
+        if (nd > 0) cu_seqlens[nd] = (int32_t)nt;
+        ++nd;
+        cur = 0;
+      }
+      token_rows[nt++] = r * seq + i;
+      ++cur;
+      if (cur > mx) mx = cur;
+    }
+  }
+  if (nt == 0) return 3;
+  cu_seqlens[nd] = (int32_t)nt;
+  *num_docs = nd;
+  *total_tokens = nt;
+  *max_seqlen = mx;
+  return 0;
+}
