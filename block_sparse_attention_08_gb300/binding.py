@@ -1,0 +1,327 @@
+"""Thin ctypes binding of libmsa (include/msa.h).
+
+Argument marshalling only: shapes, dtypes and devices are checked, raw
+pointers and the current CUDA stream are passed to the C ABI, and a non-OK
+status raises :class:`MsaError`.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback path.  Output and workspace
+tensors are allocated with torch when the caller does not pass them.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+H, G, D, DI, BLOCK = 64, 4, 128, 128, 128
+MODE_DECODE, MODE_PREFILL, MODE_PACK = 0, 1, 2
+INDEX_DTYPES = {"bf16": 0, "e4m3": 1}
+DEVICE_ERRORS = {0: "none", 1: "page id outside the pool", 2: "block id outside the query's range",
+                 3: "sequence length out of range", 4: "bounded on-chip wait gave up"}
+
+
+class MsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn}: {text} (status {status})")
+        self.status = status
+        self.bad_index = -1
+
+
+class msa_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "num_q_heads", "num_kv_heads", "head_dim", "num_index_heads", "index_dim", "block_size",
+        "topk", "init_blocks", "local_blocks", "index_dtype")]
+
+
+_lib = None
+_lock = threading.Lock()
+P, I, I64, SZ, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+CFG = ctypes.POINTER(msa_config)
+_SIGS = {
+    "msa_config_default": [CFG],
+    "msa_config_check": [CFG],
+    "msa_workspace_size": [CFG, I, I64, I, ctypes.POINTER(SZ)],
+    "msa_workspace_init": [P, SZ, P],
+    "msa_read_device_error": [P, P, ctypes.POINTER(I), ctypes.POINTER(I64)],
+    "msa_select_blocks_decode": [CFG, P, P, P, P, P, I, I, I64, P, P, SZ, P],
+    "msa_sparse_attend_decode": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, SZ, P],
+    "msa_select_blocks_prefill": [CFG, P, P, P, I, I64, I, P, P, SZ, P],
+    "msa_sparse_attend_prefill": [CFG, P, P, P, P, P, I, I64, I, F, P, P, SZ, P],
+    "msa_pack_metadata": [P, I, I, P, P, ctypes.POINTER(I), ctypes.POINTER(I64), ctypes.POINTER(I),
+                          ctypes.POINTER(I64), P, SZ, P],
+    "msa_pack": [P, P, I64, I64, P, P],
+    "msa_unpack": [P, P, I64, I64, I64, P, P],
+}
+EXPORTS = tuple(_SIGS) + ("msa_status_string",)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libmsa.so (building it first when it is missing or stale).  Raises
+    when the library cannot be built or loaded: there is no other path."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_missing else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libmsa not built: {path} is missing")
+            lib = ctypes.CDLL(path)
+            for name, args in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            lib.msa_status_string.argtypes = [ctypes.c_int]
+            lib.msa_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _call(name: str, *args):
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != 0:
+        raise MsaError(name, st, lib.msa_status_string(st).decode())
+    return st
+
+
+def make_config(topk: int = 16, init_blocks: int = 0, local_blocks: int = 1, index_dtype="bf16",
+                **overrides) -> msa_config:
+    cfg = msa_config()
+    _call("msa_config_default", ctypes.byref(cfg))
+    cfg.topk, cfg.init_blocks, cfg.local_blocks = topk, init_blocks, local_blocks
+    cfg.index_dtype = INDEX_DTYPES[index_dtype] if isinstance(index_dtype, str) else int(index_dtype)
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None:
+        if t.dim() != len(shape) or any(b is not None and a != b for a, b in zip(t.shape, shape)):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    return t
+
+
+def _index_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return "bf16"
+    if t.dtype == torch.float8_e4m3fn:
+        return "e4m3"
+    raise ValueError(f"index tensors must be bf16 or float8_e4m3fn, got {t.dtype}")
+
+
+def workspace_size(cfg: msa_config, mode: int, n: int, max_blocks: int) -> int:
+    out = ctypes.c_size_t()
+    _call("msa_workspace_size", ctypes.byref(cfg), mode, n, max_blocks, ctypes.byref(out))
+    return out.value
+
+
+class Workspace:
+    """Caller-owned scratch for the library's calls; zeroed once at creation."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.nbytes = int(nbytes)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _call("msa_workspace_init", _ptr(self.buf), self.nbytes, _stream(self.buf.device))
+
+    def grow(self, nbytes: int):
+        if nbytes > self.nbytes:
+            self.__init__(nbytes, self.buf.device)
+        return self
+
+    def read_device_error(self):
+        code, detail = ctypes.c_int(), ctypes.c_int64()
+        _call("msa_read_device_error", _ptr(self.buf), _stream(self.buf.device), ctypes.byref(code),
+              ctypes.byref(detail))
+        return code.value, detail.value
+
+
+_WS: dict = {}
+
+
+def _workspace(key, nbytes, device, ws):
+    if ws is not None:
+        if ws.nbytes < nbytes:
+            raise ValueError(f"workspace too small: {ws.nbytes} < {nbytes}")
+        return ws
+    w = _WS.get((key, str(device)))
+    if w is None:
+        w = _WS[(key, str(device))] = Workspace(nbytes, device)
+    return w.grow(nbytes)
+
+
+# ---- decode -----------------------------------------------------------------------
+
+def msa_select_blocks_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None, *,
+                             max_blocks=None, topk=16, init_blocks=0, local_blocks=1, q2k=None,
+                             workspace=None):
+    """q2k int32 [4, batch, topk] for one decode query per request (C: msa_select_blocks_decode)."""
+    B = index_q.shape[0]
+    dt = _index_dtype(index_q)
+    _need(index_q, "index_q", (torch.bfloat16, torch.float8_e4m3fn), (B, G, DI))
+    _need(index_k_cache, "index_k_cache", index_q.dtype, (None, 1, DI))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32, (B, None))
+        mb = page_table.shape[1]
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int64, (B + 1,))
+        mb = max_blocks
+    if mb is None:
+        raise ValueError("max_blocks is required with a contiguous cache")
+    cfg = make_config(topk, init_blocks, local_blocks, dt)
+    dev = index_q.device
+    if q2k is None:
+        q2k = torch.empty((G, B, topk), dtype=torch.int32, device=dev)
+    _need(q2k, "q2k", torch.int32, (G, B, topk))
+    ws = _workspace("decode", workspace_size(cfg, MODE_DECODE, B, mb), dev, workspace)
+    _call("msa_select_blocks_decode", ctypes.byref(cfg), _ptr(index_q), _ptr(index_k_cache), _ptr(seq_lens),
+          _ptr(page_table), _ptr(cu_seqlens_k if page_table is None else None), B, mb,
+          index_k_cache.shape[0], _ptr(q2k), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return q2k
+
+
+def msa_sparse_attend_decode(q, k_cache, v_cache, q2k, seq_lens, page_table=None, cu_seqlens_k=None, *,
+                             max_blocks=None, scale=None, out=None, workspace=None):
+    """bf16 out [batch, 64, 128] (C: msa_sparse_attend_decode)."""
+    B = q.shape[0]
+    _need(q, "q", torch.bfloat16, (B, H, D))
+    _need(k_cache, "k_cache", torch.bfloat16, (None, G, D))
+    _need(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape))
+    _need(q2k, "q2k", torch.int32, (G, B, None))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32, (B, None))
+        mb = page_table.shape[1]
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int64, (B + 1,))
+        mb = max_blocks
+    if mb is None:
+        raise ValueError("max_blocks is required with a contiguous cache")
+    cfg = make_config(q2k.shape[2], 0, 0)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, H, D))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws = _workspace("decode", workspace_size(cfg, MODE_DECODE, B, mb), dev, workspace)
+    _call("msa_sparse_attend_decode", ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(q2k),
+          _ptr(seq_lens), _ptr(page_table), _ptr(cu_seqlens_k if page_table is None else None), B, mb,
+          k_cache.shape[0], scale, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return out
+
+
+# ---- prefill ----------------------------------------------------------------------
+
+def msa_select_blocks_prefill(index_q, index_k, cu_seqlens, max_seqlen, *, topk=16, init_blocks=0,
+                              local_blocks=1, q2k=None, workspace=None):
+    """q2k int32 [4, tokens, topk] for packed documents (C: msa_select_blocks_prefill)."""
+    T = index_q.shape[0]
+    _need(index_q, "index_q", torch.bfloat16, (T, G, DI))
+    _need(index_k, "index_k", torch.bfloat16, (T, 1, DI))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (None,))
+    cfg = make_config(topk, init_blocks, local_blocks, "bf16")
+    dev = index_q.device
+    if q2k is None:
+        q2k = torch.empty((G, T, topk), dtype=torch.int32, device=dev)
+    _need(q2k, "q2k", torch.int32, (G, T, topk))
+    mt = (int(max_seqlen) + BLOCK - 1) // BLOCK
+    ws = _workspace("prefill", workspace_size(cfg, MODE_PREFILL, T, mt), dev, workspace)
+    _call("msa_select_blocks_prefill", ctypes.byref(cfg), _ptr(index_q), _ptr(index_k), _ptr(cu_seqlens),
+          cu_seqlens.shape[0] - 1, T, int(max_seqlen), _ptr(q2k), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return q2k
+
+
+def msa_sparse_attend_prefill(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=None, out=None, workspace=None):
+    """bf16 out [tokens, 64, 128] for packed documents (C: msa_sparse_attend_prefill)."""
+    T = q.shape[0]
+    _need(q, "q", torch.bfloat16, (T, H, D))
+    _need(k, "k", torch.bfloat16, (T, G, D))
+    _need(v, "v", torch.bfloat16, (T, G, D))
+    _need(q2k, "q2k", torch.int32, (G, T, None))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (None,))
+    cfg = make_config(q2k.shape[2], 0, 0)
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, H, D))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    mt = (int(max_seqlen) + BLOCK - 1) // BLOCK
+    ws = _workspace("prefill", workspace_size(cfg, MODE_PREFILL, T, mt), dev, workspace)
+    _call("msa_sparse_attend_prefill", ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q2k), _ptr(cu_seqlens),
+          cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return out
+
+
+# ---- packing ----------------------------------------------------------------------
+
+def msa_pack_metadata(doc_ids, *, workspace=None):
+    """(cu_seqlens int32 [docs+1], token_rows int64 [tokens], max_seqlen) of a [batch, seq]
+    int64 document map (C: msa_pack_metadata; one device-to-host synchronisation)."""
+    _need(doc_ids, "doc_ids", torch.int64)
+    if doc_ids.dim() != 2:
+        raise ValueError("doc_ids must be [batch, seq]")
+    b, s = doc_ids.shape
+    dev = doc_ids.device
+    n = max(b * s, 1)
+    cu = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    rows = torch.empty(n, dtype=torch.int64, device=dev)
+    nd, nt, mx, bad = ctypes.c_int(), ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64()
+    wsp, wsn = None, 0
+    if b > 0 and s > 0:
+        ws = _workspace("pack", workspace_size(make_config(), MODE_PACK, b * s, b), dev, workspace)
+        wsp, wsn = _ptr(ws.buf), ws.nbytes
+    st = load().msa_pack_metadata(_ptr(doc_ids), b, s, _ptr(cu), _ptr(rows), ctypes.byref(nd), ctypes.byref(nt),
+                                  ctypes.byref(mx), ctypes.byref(bad), wsp, wsn, _stream(dev))
+    if st != 0:
+        err = MsaError("msa_pack_metadata", st, load().msa_status_string(st).decode())
+        err.bad_index = bad.value
+        raise err
+    return cu[: nd.value + 1], rows[: nt.value], mx.value
+
+
+def msa_pack(external, token_rows):
+    """Gather external[batch, seq, ...] -> [tokens, ...] (C: msa_pack)."""
+    _need(external, "external")
+    _need(token_rows, "token_rows", torch.int64, (None,))
+    feat = tuple(external.shape[2:])
+    row_bytes = external[0, 0].numel() * external.element_size()
+    out = torch.empty((token_rows.shape[0],) + feat, dtype=external.dtype, device=external.device)
+    _call("msa_pack", _ptr(external), _ptr(token_rows), token_rows.shape[0], row_bytes, _ptr(out),
+          _stream(external.device))
+    return out
+
+
+def msa_unpack(packed, token_rows, batch, seq):
+    """Scatter packed[tokens, ...] -> [batch, seq, ...] with zero padding (C: msa_unpack)."""
+    _need(packed, "packed")
+    _need(token_rows, "token_rows", torch.int64, (packed.shape[0],))
+    feat = tuple(packed.shape[1:])
+    row_bytes = packed[0].numel() * packed.element_size() if packed.shape[0] else 16
+    out = torch.empty((batch, seq) + feat, dtype=packed.dtype, device=packed.device)
+    _call("msa_unpack", _ptr(packed), _ptr(token_rows), packed.shape[0], batch * seq, row_bytes, _ptr(out),
+          _stream(packed.device))
+    return out

@@ -1,0 +1,277 @@
+// abi.cu -- the extern "C" entry points of libmsa: argument validation,
+// workspace layout and kernel launches.  Declarations and contracts are in
+// include/msa.h.
+#include <mutex>
+
+#include "launch.h"
+
+namespace msa {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace layout, shared by msa_workspace_size and the calls.  Completion
+// counters come first, right after the error-word header.
+struct Layout {
+  size_t scores = 0, sel_tickets = 0, att_tickets = 0, partials = 0, plan = 0, total = 0;
+};
+static Layout layout(int mode, long long n, int max_blocks) {
+  Layout L;
+  size_t off = kHeaderBytes;
+  if (mode == MSA_MODE_DECODE) {
+    L.sel_tickets = off;
+    off += up256(static_cast<size_t>(n) * sizeof(int));
+    L.att_tickets = off;
+    off += up256(static_cast<size_t>(n) * kKvHeads * sizeof(int));
+    L.scores = off;
+    off += up256(static_cast<size_t>(n) * kKvHeads * max_blocks * sizeof(float));
+    L.partials = off;
+    off += up256(attend_partials_bytes());
+  } else if (mode == MSA_MODE_PREFILL) {
+    L.att_tickets = off;
+    off += up256(static_cast<size_t>(n) * kKvHeads * sizeof(int));
+    L.partials = off;
+    off += up256(attend_partials_bytes());
+    L.plan = off;
+    off += up256(prefill_plan_ints(static_cast<int>(n), max_blocks) * sizeof(int));
+  }
+  L.total = off;
+  return L;
+}
+
+// The completion counters of a call start at zero whatever an earlier call
+// with other sizes left in the same workspace.
+static cudaError_t clear_counters(uint8_t* ws, size_t off, size_t bytes, cudaStream_t s) {
+  return cudaMemsetAsync(ws + off, 0, bytes, s);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+msa_status msa_config_default(msa_config* cfg) {
+  if (!cfg) return MSA_ERR_NULL;
+  *cfg = msa_config{64, 4, 128, 4, 128, 128, 16, 0, 1, MSA_INDEX_BF16};
+  return MSA_OK;
+}
+
+msa_status msa_config_check(const msa_config* cfg) {
+  if (!cfg) return MSA_ERR_NULL;
+  if (cfg->num_q_heads != kHeads || cfg->num_kv_heads != kKvHeads || cfg->head_dim != kDim ||
+      cfg->num_index_heads != kKvHeads || cfg->index_dim != kIdxDim || cfg->block_size != kBlock)
+    return MSA_ERR_SHAPE;
+  if (cfg->topk < 1 || cfg->topk > kMaxTopk || cfg->init_blocks < 0 || cfg->local_blocks < 0 ||
+      cfg->init_blocks + cfg->local_blocks > cfg->topk)
+    return MSA_ERR_SHAPE;
+  if (cfg->index_dtype != MSA_INDEX_BF16 && cfg->index_dtype != MSA_INDEX_E4M3) return MSA_ERR_DTYPE;
+  return MSA_OK;
+}
+
+msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int max_blocks, size_t* bytes) {
+  if (!cfg || !bytes) return MSA_ERR_NULL;
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (n < 1 || max_blocks < 1) return MSA_ERR_SHAPE;
+  if (mode == MSA_MODE_PACK) {
+    // n = batch * seq, max_blocks = batch
+    if (n % max_blocks || n / max_blocks > 0x7fffffffLL) return MSA_ERR_SHAPE;
+    *bytes = kHeaderBytes + pack_workspace_bytes(max_blocks, static_cast<int>(n / max_blocks));
+    return MSA_OK;
+  }
+  if (mode != MSA_MODE_DECODE && mode != MSA_MODE_PREFILL) return MSA_ERR_SHAPE;
+  *bytes = layout(mode, n, max_blocks).total;
+  return MSA_OK;
+}
+
+msa_status msa_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace) return MSA_ERR_NULL;
+  return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK
+                                                                                                  : MSA_ERR_CUDA;
+}
+
+msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64_t* detail) {
+  if (!workspace || !code) return MSA_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevError h{};
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(DevError), s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  *code = h.code;
+  if (detail) *detail = h.detail;
+  return MSA_OK;
+}
+
+const char* msa_status_string(msa_status s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_NULL: return "null pointer";
+    case MSA_ERR_SHAPE: return "unsupported topology or inconsistent sizes";
+    case MSA_ERR_DTYPE: return "unsupported dtype";
+    case MSA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MSA_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_DOC_MAP: return "malformed document map";
+  }
+  return "unknown status";
+}
+
+static msa_status check_ws(void* ws, size_t have, size_t need) {
+  if (!ws) return MSA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return MSA_ERR_WORKSPACE;
+  if (have < need) return MSA_ERR_WORKSPACE;
+  return MSA_OK;
+}
+
+static msa_status check_decode_geom(const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
+                                    int batch, int max_blocks, int64_t num_slots) {
+  if (!seq_lens || (!page_table && !cu_k)) return MSA_ERR_NULL;
+  if (batch < 1 || max_blocks < 1 || num_slots < 1 || num_slots >= (1LL << 31)) return MSA_ERR_SHAPE;
+  if (page_table && num_slots % kBlock) return MSA_ERR_SHAPE;
+  return MSA_OK;
+}
+
+msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, const void* index_k_cache,
+                                    const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                    int batch, int max_blocks, int64_t num_slots, int32_t* q2k, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!index_q || !index_k_cache || !q2k) return MSA_ERR_NULL;
+  if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
+  if (!aligned16(index_q) || !aligned16(index_k_cache)) return MSA_ERR_ALIGN;
+  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks);
+  if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (clear_counters(ws, L.sel_tickets, static_cast<size_t>(batch) * sizeof(int), s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  cudaError_t e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch,
+                                       max_blocks, num_slots, q2k, reinterpret_cast<float*>(ws + L.scores),
+                                       reinterpret_cast<int*>(ws + L.sel_tickets), reinterpret_cast<DevError*>(ws), s);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* q2k, const int32_t* seq_lens, const int32_t* page_table,
+                                    const int64_t* cu_seqlens_k, int batch, int max_blocks, int64_t num_slots,
+                                    float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!q || !k_cache || !v_cache || !q2k || !out) return MSA_ERR_NULL;
+  if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return MSA_ERR_ALIGN;
+  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks);
+  if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  AttnGeom geo{0, batch, seq_lens, page_table, cu_seqlens_k, max_blocks, nullptr, 0, num_slots};
+  cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out,
+                                       reinterpret_cast<float*>(ws + L.partials),
+                                       reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+static msa_status check_prefill_geom(const int32_t* cu_seqlens, int num_docs, int64_t total_tokens, int max_seqlen) {
+  if (!cu_seqlens) return MSA_ERR_NULL;
+  if (num_docs < 1 || total_tokens < 1 || total_tokens >= (1LL << 31) || max_seqlen < 1 ||
+      max_seqlen > total_tokens || num_docs > total_tokens)
+    return MSA_ERR_SHAPE;
+  return MSA_OK;
+}
+
+msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q, const void* index_k,
+                                     const int32_t* cu_seqlens, int num_docs, int64_t total_tokens, int max_seqlen,
+                                     int32_t* q2k, void* workspace, size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (cfg->index_dtype != MSA_INDEX_BF16) return MSA_ERR_DTYPE;
+  if (!index_q || !index_k || !q2k) return MSA_ERR_NULL;
+  if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
+  if (!aligned16(index_q) || !aligned16(index_k) || !aligned16(q2k)) return MSA_ERR_ALIGN;
+  const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
+  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles);
+  if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_prefill_select(*cfg, index_q, index_k, cu_seqlens, num_docs, total_tokens, max_seqlen, q2k,
+                                        reinterpret_cast<int*>(ws + L.plan), reinterpret_cast<DevError*>(ws),
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
+                                     const int32_t* q2k, const int32_t* cu_seqlens, int num_docs,
+                                     int64_t total_tokens, int max_seqlen, float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!q || !k || !v || !q2k || !out) return MSA_ERR_NULL;
+  if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return MSA_ERR_ALIGN;
+  const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
+  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles);
+  if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (clear_counters(ws, L.att_tickets, static_cast<size_t>(total_tokens) * kKvHeads * sizeof(int), s) !=
+      cudaSuccess)
+    return MSA_ERR_CUDA;
+  AttnGeom geo{1, static_cast<int>(total_tokens), nullptr, nullptr, nullptr, max_tiles, cu_seqlens, num_docs,
+               total_tokens};
+  cudaError_t e = launch_sparse_attend(geo, q, k, v, q2k, cfg->topk, scale, out,
+                                       reinterpret_cast<float*>(ws + L.partials),
+                                       reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_pack_metadata(const int64_t* doc_ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
+                             int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (bad_index) *bad_index = -1;
+  if (!doc_ids || !cu_seqlens || !token_rows || !num_docs || !total_tokens || !max_seqlen) return MSA_ERR_NULL;
+  if (batch < 1 || seq < 1) return MSA_ERR_DOC_MAP;                                // empty map
+  if (static_cast<long long>(batch) * seq > 0x7fffffffLL) return MSA_ERR_DOC_MAP;  // past int32
+  msa_status st = check_ws(workspace, workspace_bytes, kHeaderBytes + pack_workspace_bytes(batch, seq));
+  if (st != MSA_OK) return st;
+  return run_pack_metadata(doc_ids, batch, seq, cu_seqlens, token_rows, num_docs, total_tokens, max_seqlen, bad_index,
+                           static_cast<uint8_t*>(workspace) + kHeaderBytes, static_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_pack(const void* external, const int64_t* token_rows, int64_t total_tokens, int64_t row_bytes,
+                    void* packed, void* stream) {
+  if (!external || !token_rows || !packed) return MSA_ERR_NULL;
+  if (total_tokens < 0 || row_bytes < 16 || row_bytes % 16) return MSA_ERR_SHAPE;
+  if (!aligned16(external) || !aligned16(packed)) return MSA_ERR_ALIGN;
+  return run_gather(external, token_rows, total_tokens, row_bytes, packed, static_cast<cudaStream_t>(stream), false);
+}
+
+msa_status msa_unpack(const void* packed, const int64_t* token_rows, int64_t total_tokens, int64_t batch_seq,
+                      int64_t row_bytes, void* external, void* stream) {
+  if (!external || !token_rows || !packed) return MSA_ERR_NULL;
+  if (total_tokens < 0 || batch_seq < total_tokens || row_bytes < 16 || row_bytes % 16) return MSA_ERR_SHAPE;
+  if (!aligned16(external) || !aligned16(packed)) return MSA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(external, 0, static_cast<size_t>(batch_seq) * row_bytes, s) != cudaSuccess) return MSA_ERR_CUDA;
+  return run_gather(packed, token_rows, total_tokens, row_bytes, external, s, true);
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// launch.h -- host-side launcher declarations shared by the libmsa sources.
+#pragma once
+
+#include "common.cuh"
+
+namespace msa {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+// Geometry of the queries of one attention call.
+struct AttnGeom {
+  int prefill;  // 0 decode, 1 prefill
+  int nq;       // requests (decode) or compact tokens (prefill)
+  // decode
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  const int64_t* cu_k;
+  int max_blocks;
+  // prefill
+  const int32_t* cu_seqlens;
+  int num_docs;
+  long long num_rows;  // rows of the K/V arrays (slots or tokens)
+};
+
+cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
+                                 const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
+                                 int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
+                                 int* tickets, DevError* err, cudaStream_t stream);
+cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
+                                 const int32_t* q2k, int topk, float scale, void* out, float* partials,
+                                 int* tickets, DevError* err, cudaStream_t stream);
+size_t attend_partials_bytes();
+size_t prefill_plan_ints(int num_docs, int max_tiles);
+cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, const void* index_k,
+                                  const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
+                                  int32_t* q2k, int* plan_ints, DevError* err, cudaStream_t stream);
+size_t pack_workspace_bytes(int batch, int seq);
+msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
+                             int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,
+                             uint8_t* ws, cudaStream_t stream);
+msa_status run_gather(const void* src, const int64_t* rows, long long n, long long row_bytes, void* dst,
+                      cudaStream_t stream, bool scatter);
+
+}  // namespace msa

@@ -1,0 +1,424 @@
+// prefill_select.cu -- block scoring and top-k selection for packed documents,
+// fused into one tensor-core kernel.
+//
+// NeMo "...minimax_m3_vl.msa", MSAMicrobatch.select_blocks and
+// _SelectionPlan.select: bf16 index_q [tokens, 4, 128] against index_k
+// [tokens, 1, 128] -> int32 q2k [4, tokens, 16], a hard top-k over the
+// unnormalised QK maxima of each causal, document-local 128-key block, with the
+// candidate / forced [tokens, blocks] masks of the plan; TensorRT-LLM
+// "MiniMaxM3SparseAttentionConfig" fields sparse_score_type 'max',
+// sparse_init_blocks, sparse_local_blocks.
+//
+// GB300 design.  One work unit is (document, 128-token query block, pair of
+// index heads).  A TMA producer warp loads the two 128x128 index-Q tiles once
+// and then streams the document's causal key blocks (128 keys x 128 dims of
+// index_k each) through a 3-deep shared-memory ring; an MMA warp issues
+// tcgen05.mma (M=128 tokens, N=128 keys, K=128, bf16 -> fp32) into a
+// double-buffered tensor-memory accumulator (2 heads x 2 buffers x 128
+// columns = all 512 columns); four epilogue warps read the scores back with
+// tcgen05.ld (one token row per thread), take the causal block max and insert
+// it into a per-thread top-k list held in registers.  The score matrix never
+// reaches global memory: each thread writes its token's q2k row when the unit
+// ends.  Query blocks whose candidates all fit in top-k (nb <= topk) need no
+// scores and are written directly.  Units are ordered by decreasing cost by a
+// one-CTA plan kernel (counting sort of documents by block count) and dealt to
+// the persistent CTAs in snake order.
+#include "launch.h"
+
+namespace msa {
+
+constexpr int kPsStages = 3;
+constexpr int kPsTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-dim boxes)
+constexpr int kPsBox = 128 * 128;       // 128 rows x 128 bytes
+constexpr int kPsThreads = 192;         // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr uint32_t kPsIdesc = tc::idesc_bf16_f32(128, 128);
+
+struct PsSmem {
+  alignas(1024) uint8_t a[2][kPsTile];          // index-Q tiles of the head pair
+  alignas(1024) uint8_t b[kPsStages][kPsTile];  // index-K key blocks
+  uint64_t a_full, a_empty;
+  uint64_t b_full[kPsStages], b_empty[kPsStages];
+  uint64_t t_full[2], t_empty[2];
+  uint32_t tmem_base;
+};
+
+struct PsPlan {
+  const int32_t* cu_seqlens;
+  int num_docs;
+  int max_tiles;           // ceil(max_seqlen / 128)
+  const int* sorted_docs;  // documents by decreasing tile count
+  const int* level_base;   // [max_tiles]: first tile index of query-block level qb
+  const int* level_cnt;    // [max_tiles]: documents having query block qb
+  const int* n_tiles;      // total tiles
+};
+
+struct Unit {
+  int doc, qb, hp;
+  int start, len;  // document rows
+};
+
+__device__ __forceinline__ Unit unit_of(const PsPlan& p, int u) {
+  Unit x;
+  const int ut = u >> 1;
+  x.hp = u & 1;
+  // level qb holds tiles [level_base[qb], level_base[qb] + level_cnt[qb]); bases grow as qb falls
+  int lo = 0, hi = p.max_tiles - 1;
+  while (lo < hi) {  // smallest qb with level_base[qb] <= ut
+    const int mid = (lo + hi) >> 1;
+    if (p.level_base[mid] <= ut) hi = mid; else lo = mid + 1;
+  }
+  x.qb = lo;
+  x.doc = p.sorted_docs[ut - p.level_base[lo]];
+  x.start = p.cu_seqlens[x.doc];
+  x.len = p.cu_seqlens[x.doc + 1] - x.start;
+  return x;
+}
+
+// snake order over rows of gridDim.x units
+__device__ __forceinline__ int snake(int k, int c, int G) { return (k & 1) ? (k + 1) * G - 1 - c : k * G + c; }
+
+// One-CTA plan: documents sorted by tile count (descending), level bases.
+__global__ void prefill_plan_kernel(const int32_t* __restrict__ cu, int num_docs, int max_tiles,
+                                    int* __restrict__ hist /*[max_tiles+2]*/, int* __restrict__ sorted_docs,
+                                    int* __restrict__ level_base, int* __restrict__ level_cnt,
+                                    int* __restrict__ n_tiles, DevError* err) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < max_tiles + 2; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int d = tid; d < num_docs; d += blockDim.x) {
+    const int len = cu[d + 1] - cu[d];
+    int nt = (len + kBlock - 1) / kBlock;
+    if (len < 1 || nt > max_tiles) {
+      record_error(err, MSA_DEVERR_LENGTH, d);
+      nt = len < 1 ? 0 : max_tiles;
+    }
+    atomicAdd(&hist[nt], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // level_cnt[qb] = #docs with tile count > qb ; level_base: levels in decreasing qb
+    int above = 0;
+    for (int n = max_tiles; n >= 1; --n) {
+      above += hist[n];
+      level_cnt[n - 1] = above;
+    }
+    int base = 0;
+    for (int qb = max_tiles - 1; qb >= 0; --qb) {
+      level_base[qb] = base;
+      base += level_cnt[qb];
+    }
+    *n_tiles = base;
+    // scatter cursors: docs with tile count n start after all docs with more tiles
+    int run = 0;
+    for (int n = max_tiles; n >= 0; --n) {
+      const int c = hist[n];
+      hist[n] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int d = tid; d < num_docs; d += blockDim.x) {
+    const int len = cu[d + 1] - cu[d];
+    const int nt = len < 1 ? 0 : min((len + kBlock - 1) / kBlock, max_tiles);
+    sorted_docs[atomicAdd(&hist[nt], 1)] = d;
+  }
+}
+
+// Sorted top-k list (score desc, id asc) of up to 16 entries in registers.
+struct TopList {
+  float v[kMaxTopk];
+  int id[kMaxTopk];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < kMaxTopk; ++i) {
+      v[i] = -INFINITY;
+      id[i] = 0x7fffffff;
+    }
+  }
+  // ids arrive in increasing order, so an equal score never moves up
+  __device__ __forceinline__ void insert(float s, int b) {
+    if (s > v[kMaxTopk - 1]) {
+      v[kMaxTopk - 1] = s;
+      id[kMaxTopk - 1] = b;
+#pragma unroll
+      for (int i = kMaxTopk - 1; i > 0; --i) {
+        const bool up = v[i] > v[i - 1];
+        const float tv = v[i];
+        const int ti = id[i];
+        v[i] = up ? v[i - 1] : v[i];
+        id[i] = up ? id[i - 1] : id[i];
+        v[i - 1] = up ? tv : v[i - 1];
+        id[i - 1] = up ? ti : id[i - 1];
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ void cswap(int& a, int& b) {
+  const int lo = min(a, b), hi = max(a, b);
+  a = lo;
+  b = hi;
+}
+
+// Writes the q2k row: [0, init) ++ ascending(top `need` ids) ++ [nb-local, nb).
+__device__ __forceinline__ void write_row(int32_t* row, const TopList& L, int need, int nb, int topk, int init,
+                                          int local) {
+  int ids[kMaxTopk];
+#pragma unroll
+  for (int i = 0; i < kMaxTopk; ++i) ids[i] = i < need ? L.id[i] : 0x7fffffff;
+  // bitonic sort of 16 ints, ascending
+#pragma unroll
+  for (int k = 2; k <= kMaxTopk; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < kMaxTopk; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0) cswap(ids[i], ids[l]);
+          else cswap(ids[l], ids[i]);
+        }
+      }
+  int outv[kMaxTopk];
+#pragma unroll
+  for (int i = 0; i < kMaxTopk; ++i) {
+    int v;
+    if (i < init) v = i;
+    else if (i < init + need) v = ids[i - init];
+    else if (i < topk) v = nb - local + (i - init - need);
+    else v = -1;
+    outv[i] = v;
+  }
+  if (topk == kMaxTopk) {
+    int4* o = reinterpret_cast<int4*>(row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_int4(outv[4 * i], outv[4 * i + 1], outv[4 * i + 2], outv[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kMaxTopk; ++i)
+      if (i < topk) row[i] = outv[i];
+  }
+}
+
+__global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, PsPlan plan,
+    long long total_tokens, int32_t* __restrict__ q2k, int topk, int init, int local, DevError* err) {
+  extern __shared__ uint8_t smem_raw[];
+  PsSmem& sm = *reinterpret_cast<PsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int U = 2 * (*plan.n_tiles);
+
+  if (tid == 0) {
+    mbar_init(&sm.a_full, 1);
+    mbar_init(&sm.a_empty, 1);
+    for (int s = 0; s < kPsStages; ++s) {
+      mbar_init(&sm.b_full[s], 1);
+      mbar_init(&sm.b_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.t_full[i], 1);
+      mbar_init(&sm.t_empty[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::alloc(&sm.tmem_base, 512);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&qmap);
+      prefetch_tmap(&kmap);
+      uint32_t nunit = 0, bc = 0;
+      for (int k = 0; k * G < U; ++k) {
+        const int u = snake(k, c, G);
+        if (u >= U) continue;
+        const Unit x = unit_of(plan, u);
+        if (x.qb + 1 <= topk) continue;
+        mbar_wait(&sm.a_empty, (nunit & 1) ^ 1, err, 400);
+        mbar_expect_tx(&sm.a_full, 2 * kPsTile);
+        const int row = x.start + x.qb * kBlock;
+        for (int hh = 0; hh < 2; ++hh) {
+          tma_load_3d(sm.a[hh], &qmap, 0, 2 * x.hp + hh, row, &sm.a_full);
+          tma_load_3d(sm.a[hh] + kPsBox, &qmap, 64, 2 * x.hp + hh, row, &sm.a_full);
+        }
+        for (int b = 0; b <= x.qb; ++b, ++bc) {
+          const int s = bc % kPsStages;
+          mbar_wait(&sm.b_empty[s], ((bc / kPsStages) & 1) ^ 1, err, 401);
+          mbar_expect_tx(&sm.b_full[s], kPsTile);
+          tma_load_2d(sm.b[s], &kmap, 0, x.start + b * kBlock, &sm.b_full[s]);
+          tma_load_2d(sm.b[s] + kPsBox, &kmap, 64, x.start + b * kBlock, &sm.b_full[s]);
+        }
+        ++nunit;
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t nunit = 0, bc = 0, kc = 0;
+      for (int k = 0; k * G < U; ++k) {
+        const int u = snake(k, c, G);
+        if (u >= U) continue;
+        const Unit x = unit_of(plan, u);
+        if (x.qb + 1 <= topk) continue;
+        mbar_wait(&sm.a_full, nunit & 1, err, 500);
+        tc::fence_after();
+        for (int b = 0; b <= x.qb; ++b, ++bc, ++kc) {
+          const int s = bc % kPsStages, buf = kc & 1;
+          mbar_wait(&sm.b_full[s], (bc / kPsStages) & 1, err, 501);
+          mbar_wait(&sm.t_empty[buf], ((kc >> 1) & 1) ^ 1, err, 502);
+          tc::fence_after();
+          const uint32_t bsm = smem_u32(sm.b[s]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t asm_ = smem_u32(sm.a[hh]);
+            const uint32_t d = tmem + static_cast<uint32_t>((buf * 2 + hh) * 128);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kPsBox + (kk & 3) * 32;
+              tc::mma_bf16(d, tc::desc_k_sw128(asm_ + off), tc::desc_k_sw128(bsm + off), kPsIdesc, kk > 0);
+            }
+          }
+          tc::commit(&sm.b_empty[s]);
+          tc::commit(&sm.t_full[buf]);
+        }
+        tc::commit(&sm.a_empty);
+        ++nunit;
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 0-3: one token row per thread ----------------
+    const int r = warp * 32 + lane;
+    uint32_t kc = 0;
+    for (int k = 0; k * G < U; ++k) {
+      const int u = snake(k, c, G);
+      if (u >= U) continue;
+      const Unit x = unit_of(plan, u);
+      const int nb = x.qb + 1;
+      const int p = x.qb * kBlock + r;  // position of this row's token
+      const bool row_ok = p < x.len;
+      const long long t = static_cast<long long>(x.start) + p;
+      if (nb <= topk) {
+        if (row_ok)
+          for (int hh = 0; hh < 2; ++hh) {
+            int32_t* row = q2k + (static_cast<long long>(2 * x.hp + hh) * total_tokens + t) * topk;
+            for (int i = 0; i < topk; ++i) row[i] = i < nb ? i : -1;
+          }
+        continue;
+      }
+      TopList L0, L1;
+      L0.reset();
+      L1.reset();
+      for (int b = 0; b <= x.qb; ++b, ++kc) {
+        const int buf = kc & 1;
+        mbar_wait(&sm.t_full[buf], (kc >> 1) & 1, err, 600);
+        tc::fence_after();
+        const bool diag = (b == x.qb);
+        float mx[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float m = -INFINITY;
+          const uint32_t col0 = static_cast<uint32_t>((buf * 2 + hh) * 128);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t v[32];
+            tc::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + col0 + ch * 32, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float f = __uint_as_float(v[j]);
+              const bool ok = !diag || (ch * 32 + j <= r);
+              m = ok ? fmaxf(m, f) : m;
+            }
+          }
+          mx[hh] = m;
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.t_empty[buf]);
+        const bool forced = (b < init) || (b >= nb - local);
+        if (!forced) {
+          L0.insert(mx[0], b);
+          L1.insert(mx[1], b);
+        }
+      }
+      if (row_ok) {
+        const int need = topk - init - local;
+        write_row(q2k + (static_cast<long long>(2 * x.hp) * total_tokens + t) * topk, L0, need, nb, topk, init,
+                  local);
+        write_row(q2k + (static_cast<long long>(2 * x.hp + 1) * total_tokens + t) * topk, L1, need, nb, topk,
+                  init, local);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+size_t prefill_plan_ints(int num_docs, int max_tiles) {
+  return static_cast<size_t>(max_tiles + 2) + num_docs + 2 * static_cast<size_t>(max_tiles) + 1;
+}
+
+cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, const void* index_k,
+                                  const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
+                                  int32_t* q2k, int* plan_ints, DevError* err, cudaStream_t stream) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return cudaErrorInvalidValue;
+  const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
+  int* hist = plan_ints;
+  int* sorted_docs = hist + (max_tiles + 2);
+  int* level_base = sorted_docs + num_docs;
+  int* level_cnt = level_base + max_tiles;
+  int* n_tiles = level_cnt + max_tiles;
+  prefill_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_docs, max_tiles, hist, sorted_docs, level_base,
+                                               level_cnt, n_tiles, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap qmap, kmap;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(kKvHeads),
+                          static_cast<cuuint64_t>(total_tokens)};
+    cuuint64_t strides[2] = {kIdxDim * 2, kKvHeads * kIdxDim * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(index_q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(total_tokens)};
+    cuuint64_t strides[1] = {kIdxDim * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(index_k), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  PsPlan plan{cu_seqlens, num_docs, max_tiles, sorted_docs, level_base, level_cnt, n_tiles};
+  const long long tiles_upper = total_tokens / kBlock + num_docs;
+  int grid = static_cast<int>(2 * tiles_upper < kNumSMs ? 2 * tiles_upper : kNumSMs);
+  if (grid < 1) grid = 1;
+  const size_t smem = sizeof(PsSmem) + 1024;
+  cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  prefill_select_kernel<<<grid, kPsThreads, smem, stream>>>(qmap, kmap, plan, total_tokens, q2k, cfg.topk,
+                                                            cfg.init_blocks, cfg.local_blocks, err);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

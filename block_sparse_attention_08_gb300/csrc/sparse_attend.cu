@@ -1,0 +1,422 @@
+// sparse_attend.cu -- sparse GQA attention over the selected blocks, for a
+// decode step (one query per request over a paged or contiguous K/V cache) and
+// for packed-document prefill (every compact token).
+//
+// TensorRT-LLM "MiniMaxM3SparseAttentionConfig" (class description, second
+// step: a sparse GQA attention over only the selected blocks) and NeMo
+// "...minimax_m3_vl.msa" sparse_attention / _SparseAttention.forward: bf16
+// q [tokens, 64, 128], k / v [tokens, 4, 128], int32 q2k [4, tokens, 16] ->
+// bf16 out [tokens, 64, 128].
+//
+// GB300 design.  The 16 query heads that share a KV head form exactly one
+// 16-row MMA tile, so one (query, KV head, selected block) triple is the unit
+// of work.  All units are split evenly over a persistent grid (stream-K): a
+// producer warp walks the CTA's units and gathers each selected block's K and V
+// in 64-key chunks with tiled TMA copies (3-D tensor map over
+// [rows, 4 heads, 128], 128-byte swizzle) into a 4-deep shared-memory ring;
+// four consumer warps each take 16 keys of a chunk, run S = Q K^T and O += P V
+// on the tensor cores (mma.sync bf16, fp32 accumulate) with an online softmax,
+// and merge their states in shared memory when the (query, KV head) segment
+// ends.  A segment cut by a CTA boundary is written as an fp32 partial
+// (max, sum, unnormalised output); the CTA that completes the segment's last
+// unit (atomic ticket, no waiting) merges the partials and writes bf16.
+#include "launch.h"
+
+namespace msa {
+
+constexpr int kAttStages = 4;
+constexpr int kChunkKeys = 64;
+constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 dims)
+constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
+constexpr int kConsumerWarps = 4;
+constexpr int kAttThreads = (kConsumerWarps + 1) * 32;
+constexpr int kCombStride = kDim + 8;              // padded fp32 row in the merge buffer
+constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
+
+struct QueryGeo {
+  int pos;         // position of the query (keys 0..pos are causal)
+  int nb;          // candidate blocks
+  long long base;  // prefill: first row of the document; decode contiguous: cu_k[r]
+};
+
+__device__ __forceinline__ QueryGeo query_geo(const AttnGeom& geo, int qi) {
+  QueryGeo q;
+  if (geo.prefill) {
+    int lo = 0, hi = geo.num_docs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (geo.cu_seqlens[mid] <= qi) lo = mid; else hi = mid - 1;
+    }
+    q.base = geo.cu_seqlens[lo];
+    q.pos = qi - static_cast<int>(q.base);
+    q.nb = q.pos / kBlock + 1;
+  } else {
+    const int L = geo.seq_lens[qi];
+    q.pos = L - 1;
+    q.nb = L < 1 ? 0 : min((L + kBlock - 1) / kBlock, geo.max_blocks);
+    q.base = geo.page_table ? 0 : geo.cu_k[qi];
+  }
+  return q;
+}
+
+// First K/V row of block b of the query, or -1 when the page is outside the pool.
+__device__ __forceinline__ long long block_row0(const AttnGeom& geo, int qi, const QueryGeo& q, int b) {
+  if (!geo.prefill && geo.page_table) {
+    const int page = geo.page_table[static_cast<long long>(qi) * geo.max_blocks + b];
+    const long long r0 = static_cast<long long>(page) * kBlock;
+    return (page < 0 || r0 + kBlock > geo.num_rows) ? -1 : r0;
+  }
+  return q.base + static_cast<long long>(b) * kBlock;
+}
+
+// Number of causal keys of block b (0 for an empty / invalid entry).
+__device__ __forceinline__ int block_keys(const QueryGeo& q, int b) {
+  if (b < 0 || b >= q.nb) return 0;
+  return min(kBlock, q.pos - b * kBlock + 1);
+}
+
+struct AttSmem {
+  alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
+  float comb[kConsumerWarps][kGroup][kCombStride];
+  float comb_m[kConsumerWarps][kGroup];
+  float comb_l[kConsumerWarps][kGroup];
+  uint64_t full[kAttStages];
+  uint64_t empty[kAttStages];
+  int bcast;
+};
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ long long seg_begin(long long c, long long N, long long G) { return c * N / G; }
+__device__ __forceinline__ long long cta_of(long long i, long long N, long long G) {
+  long long c = i * G / N;
+  while (c + 1 < G && seg_begin(c + 1, N, G) <= i) ++c;
+  while (c > 0 && seg_begin(c, N, G) > i) --c;
+  return c;
+}
+
+__global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
+    float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ partials,
+    int* __restrict__ tickets, DevError* err) {
+  extern __shared__ uint8_t smem_raw[];
+  AttSmem& sm = *reinterpret_cast<AttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
+  const long long G = gridDim.x;
+  const long long lo = seg_begin(blockIdx.x, N, G), hi = seg_begin(blockIdx.x + 1, N, G);
+
+  if (tid == 0) {
+    for (int s = 0; s < kAttStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (lo >= hi) return;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      long long sc = 0;
+      long long it = lo;
+      while (it < hi) {
+        const int qi = static_cast<int>(it / (kKvHeads * topk));
+        const int g = static_cast<int>((it / topk) % kKvHeads);
+        const long long seg_end = min(hi, (static_cast<long long>(qi) * kKvHeads + g + 1) * topk);
+        const QueryGeo qg = query_geo(geo, qi);
+        for (; it < seg_end; ++it) {
+          const int j = static_cast<int>(it % topk);
+          const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j];
+          const int nk = block_keys(qg, b);
+          if (nk == 0) continue;
+          const long long r0 = block_row0(geo, qi, qg, b);
+          if (r0 < 0) continue;
+          const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
+          for (int ch = 0; ch < nch; ++ch, ++sc) {
+            const int s = static_cast<int>(sc % kAttStages);
+            mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kAttStages) & 1) ^ 1), err, 200);
+            mbar_expect_tx(&sm.full[s], kAttStageBytes);
+            const int row = static_cast<int>(r0 + ch * kChunkKeys);
+            uint8_t* st = sm.stage[s];
+            tma_load_3d(st + 0 * kBoxBytes, &kmap, 0, g, row, &sm.full[s]);
+            tma_load_3d(st + 1 * kBoxBytes, &kmap, 64, g, row, &sm.full[s]);
+            tma_load_3d(st + 2 * kBoxBytes, &vmap, 0, g, row, &sm.full[s]);
+            tma_load_3d(st + 3 * kBoxBytes, &vmap, 64, g, row, &sm.full[s]);
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int g8 = lane >> 2, t4 = lane & 3;
+  long long sc = 0;
+  long long it = lo;
+  while (it < hi) {
+    const int qi = static_cast<int>(it / (kKvHeads * topk));
+    const int g = static_cast<int>((it / topk) % kKvHeads);
+    const long long seg_lo = it;
+    const long long range0 = (static_cast<long long>(qi) * kKvHeads + g) * topk;
+    const long long seg_end = min(hi, range0 + topk);
+    const QueryGeo qg = query_geo(geo, qi);
+
+    // Q fragments of the 16 heads of KV head g (A operand, 8 k-steps)
+    uint32_t qa[8][4];
+    {
+      const __nv_bfloat16* qp = q + (static_cast<long long>(qi) * kHeads + g * kGroup) * kDim;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int c = 16 * kk + 2 * t4;
+        qa[kk][0] = *reinterpret_cast<const uint32_t*>(qp + g8 * kDim + c);
+        qa[kk][1] = *reinterpret_cast<const uint32_t*>(qp + (g8 + 8) * kDim + c);
+        qa[kk][2] = *reinterpret_cast<const uint32_t*>(qp + g8 * kDim + c + 8);
+        qa[kk][3] = *reinterpret_cast<const uint32_t*>(qp + (g8 + 8) * kDim + c + 8);
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    for (; it < seg_end; ++it) {
+      const int j = static_cast<int>(it % topk);
+      const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j];
+      if (b >= qg.nb && lane == 0 && warp == 0) record_error(err, MSA_DEVERR_BLOCK, it);
+      const int nk = block_keys(qg, b);
+      if (nk == 0) continue;
+      if (block_row0(geo, qi, qg, b) < 0) {
+        if (lane == 0 && warp == 0) record_error(err, MSA_DEVERR_PAGE, it);
+        continue;
+      }
+      const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
+      for (int ch = 0; ch < nch; ++ch, ++sc) {
+        const int s = static_cast<int>(sc % kAttStages);
+        const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
+        mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kAttStages) & 1), err, 300);
+        const int key0 = 16 * warp;
+        if (key0 < valid) {
+          const uint32_t st = smem_u32(sm.stage[s]);
+          // ---- S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys) ----
+          float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          {
+            const int mi = lane >> 3;
+            const int krow = key0 + 8 * (mi >> 1) + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
+              const uint32_t addr = st + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7);
+              uint32_t kb[4];
+              ldsm_x4(kb, addr);
+              mma_bf16(sacc[0], qa[kk], kb[0], kb[1]);
+              mma_bf16(sacc[1], qa[kk], kb[2], kb[3]);
+            }
+          }
+          // ---- mask, online softmax (base 2, scale folded in) ----
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kidx = key0 + 8 * p + 2 * t4 + e;
+              const bool ok = kidx < valid;
+              sacc[p][e] = ok ? sacc[p][e] * scale_log2 : -INFINITY;
+              sacc[p][2 + e] = ok ? sacc[p][2 + e] * scale_log2 : -INFINITY;
+              mx0 = fmaxf(mx0, sacc[p][e]);
+              mx1 = fmaxf(mx1, sacc[p][2 + e]);
+            }
+          }
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+          m0 = mn0;
+          m1 = mn1;
+          float ps[2][4];
+          float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            ps[p][0] = exp2f(sacc[p][0] - mu0);
+            ps[p][1] = exp2f(sacc[p][1] - mu0);
+            ps[p][2] = exp2f(sacc[p][2] - mu1);
+            ps[p][3] = exp2f(sacc[p][3] - mu1);
+            rs0 += ps[p][0] + ps[p][1];
+            rs1 += ps[p][2] + ps[p][3];
+          }
+          l0 = l0 * al0 + rs0;
+          l1 = l1 * al1 + rs1;
+#pragma unroll
+          for (int nd = 0; nd < 16; ++nd) {
+            o[nd][0] *= al0;
+            o[nd][1] *= al0;
+            o[nd][2] *= al1;
+            o[nd][3] *= al1;
+          }
+          // P = P_hi + P_lo in two bf16 terms (relative error ~2^-17), so the
+          // bf16 rounding of the probabilities does not reach the output
+          uint32_t pa[4], pl[4];
+          split_bf16(ps[0][0], ps[0][1], pa[0], pl[0]);
+          split_bf16(ps[0][2], ps[0][3], pa[1], pl[1]);
+          split_bf16(ps[1][0], ps[1][1], pa[2], pl[2]);
+          split_bf16(ps[1][2], ps[1][3], pa[3], pl[3]);
+          // ---- O += P V (k = this warp's 16 keys, 16 n-tiles of 8 dims) ----
+          {
+            const int mi = lane >> 3;
+            const int vrow = key0 + 8 * (mi & 1) + (lane & 7);
+#pragma unroll
+            for (int nd = 0; nd < 16; nd += 2) {
+              const int chunk = nd + (mi >> 1);
+              const uint32_t addr = st + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7);
+              uint32_t vb[4];
+              ldsm_x4_t(vb, addr);
+              mma_bf16(o[nd], pa, vb[0], vb[1]);
+              mma_bf16(o[nd + 1], pa, vb[2], vb[3]);
+              mma_bf16(o[nd], pl, vb[0], vb[1]);
+              mma_bf16(o[nd + 1], pl, vb[2], vb[3]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+      }
+    }
+
+    // ---- merge the four warps' states ----
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (t4 == 0) {
+      sm.comb_m[warp][g8] = m0;
+      sm.comb_m[warp][g8 + 8] = m1;
+      sm.comb_l[warp][g8] = l0;
+      sm.comb_l[warp][g8 + 8] = l1;
+    }
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      *reinterpret_cast<float2*>(&sm.comb[warp][g8][8 * nd + 2 * t4]) = make_float2(o[nd][0], o[nd][1]);
+      *reinterpret_cast<float2*>(&sm.comb[warp][g8 + 8][8 * nd + 2 * t4]) = make_float2(o[nd][2], o[nd][3]);
+    }
+    consumer_sync();
+    const int row = tid >> 3, d0 = (tid & 7) * 16;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.comb_m[w][row]);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float Lsum = 0.f, acc[16];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) acc[d] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = exp2f(sm.comb_m[w][row] - Mu);
+      Lsum += sm.comb_l[w][row] * f;
+#pragma unroll
+      for (int d = 0; d < 16; ++d) acc[d] += sm.comb[w][row][d0 + d] * f;
+    }
+    const bool complete = (seg_lo == range0) && (seg_end == range0 + topk);
+    __nv_bfloat16* orow = out + (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+    if (complete) {
+      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      uint32_t w8[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(acc[2 * d] * inv, acc[2 * d + 1] * inv);
+      reinterpret_cast<uint4*>(orow)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+      reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+      consumer_sync();
+    } else {
+      // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
+      const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
+      float* pp = partials + slot * kPartialFloats;
+      if ((tid & 7) == 0) {
+        pp[row] = M;
+        pp[16 + row] = Lsum;
+      }
+#pragma unroll
+      for (int d = 0; d < 16; d += 4)
+        *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + d) =
+            make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
+      __threadfence();
+      consumer_sync();
+      if (tid == 0) {
+        const int cnt = static_cast<int>(seg_end - seg_lo);
+        const int old = atomicAdd(&tickets[qi * kKvHeads + g], cnt);
+        sm.bcast = (old + cnt == topk) ? 1 : 0;
+      }
+      consumer_sync();
+      if (sm.bcast) {
+        __threadfence();
+        const long long c_first = cta_of(range0, N, G), c_last = cta_of(range0 + topk - 1, N, G);
+        float Mg = -INFINITY;
+        for (long long c = c_first; c <= c_last; ++c) {
+          const long long sl = 2 * c + (range0 <= seg_begin(c, N, G) ? 0 : 1);
+          Mg = fmaxf(Mg, __ldcg(partials + sl * kPartialFloats + row));
+        }
+        const float Mgu = Mg == -INFINITY ? 0.f : Mg;
+        float Lg = 0.f, ag[16];
+#pragma unroll
+        for (int d = 0; d < 16; ++d) ag[d] = 0.f;
+        for (long long c = c_first; c <= c_last; ++c) {
+          const long long sl = 2 * c + (range0 <= seg_begin(c, N, G) ? 0 : 1);
+          const float* pc = partials + sl * kPartialFloats;
+          const float f = exp2f(__ldcg(pc + row) - Mgu);
+          Lg += __ldcg(pc + 16 + row) * f;
+#pragma unroll
+          for (int d = 0; d < 16; ++d) ag[d] += __ldcg(pc + 32 + row * kDim + d0 + d) * f;
+        }
+        const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
+        uint32_t w8[8];
+#pragma unroll
+        for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(ag[2 * d] * inv, ag[2 * d + 1] * inv);
+        reinterpret_cast<uint4*>(orow)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+        reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+        if (tid == 0) tickets[qi * kKvHeads + g] = 0;
+      }
+      consumer_sync();
+    }
+  }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+// 3-D map over a [rows, 4, 128] bf16 array; box = 64 dims x 1 head x 64 rows, 128-byte swizzle.
+static bool make_kv_map(CUtensorMap* map, const void* base, long long rows) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kKvHeads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {kDim * 2, kKvHeads * kDim * 2};
+  cuuint32_t box[3] = {64, 1, kChunkKeys};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
+
+cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
+                                 const int32_t* q2k, int topk, float scale, void* out, float* partials,
+                                 int* tickets, DevError* err, cudaStream_t stream) {
+  CUtensorMap kmap, vmap;
+  if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows)) return cudaErrorInvalidValue;
+  const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
+  const int grid = static_cast<int>(N < kNumSMs ? (N > 0 ? N : 1) : kNumSMs);
+  const size_t smem = sizeof(AttSmem) + 1024;
+  cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const float scale_log2 = scale * 1.4426950408889634f;
+  sparse_attend_kernel<<<grid, kAttThreads, smem, stream>>>(
+      kmap, vmap, static_cast<const __nv_bfloat16*>(q), q2k, geo, topk, scale_log2,
+      static_cast<__nv_bfloat16*>(out), partials, tickets, err);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

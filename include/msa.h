@@ -1,0 +1,225 @@
+/*
+ * msa.h -- C ABI of libmsa: MiniMax-M3 two-step block-sparse attention on
+ * GB300 (sm_103a).
+ *
+ * The method (TensorRT-LLM "MiniMaxM3SparseAttentionConfig", class
+ * description): an index branch scores the 128-token key blocks of each query
+ * with a per-KV-head index query against one shared index key, keeps the top-k
+ * blocks per (kv_head, q_token) with init blocks forced at the head and local
+ * blocks forced at the tail, and a sparse GQA attention then runs over the
+ * selected blocks only.  The NeMo AutoModel page
+ * "nemo_automodel.components.models.minimax_m3_vl.msa" states the same two
+ * steps for packed documents (MSAMicrobatch.select_blocks, sparse_attention).
+ *
+ * Conventions for every entry point
+ *   - Pointers marked "dev" are device pointers; "host" are host pointers.
+ *     All device buffers are owned by the caller.  The library allocates no
+ *     memory and launches all work on the caller's `stream` (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream).
+ *   - No entry point synchronises the stream except msa_pack_metadata and
+ *     msa_read_device_error, which say so.
+ *   - Tensors are dense row-major with the shapes given; tensor base pointers
+ *     must be 16-byte aligned.
+ *   - Errors are returned synchronously as msa_status; nothing is thrown and
+ *     nothing aborts.  Argument errors are detected before any CUDA call, so a
+ *     call that returns MSA_ERR_NULL / SHAPE / DTYPE / WORKSPACE / ALIGN has
+ *     enqueued no work.  Bad data found on the device (a page id outside the
+ *     pool, a block id outside the query's range, a length outside its bound)
+ *     is skipped and recorded in the workspace's device error word, which
+ *     msa_read_device_error returns.
+ *   - Fixed topology (NeMo msa, require_msa_support): 64 query heads, 4 KV
+ *     heads, head dim 128, 4 index heads of dim 128, block size 128 (the
+ *     TensorRT-LLM field implementation='msa' requires sparse_block_size 128),
+ *     max score reduction.  Query head h reads KV / index head h / 16.
+ *   - q2k rows hold the selected document-local block ids in ascending order,
+ *     then -1 up to topk (NeMo select_blocks: "int32 [4, tokens, 16]
+ *     document-local block ids, padded with -1").
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_NULL = 1,      /* a required pointer is NULL */
+  MSA_ERR_SHAPE = 2,     /* unsupported topology or inconsistent sizes */
+  MSA_ERR_DTYPE = 3,     /* unsupported index dtype */
+  MSA_ERR_WORKSPACE = 4, /* workspace NULL, too small or not 256-byte aligned */
+  MSA_ERR_ALIGN = 5,     /* a tensor pointer is not 16-byte aligned */
+  MSA_ERR_CUDA = 6,      /* a CUDA runtime call or a kernel launch failed */
+  MSA_ERR_DOC_MAP = 7    /* malformed document map (msa_pack_metadata) */
+} msa_status;
+
+/* Index Q/K storage dtype (TensorRT-LLM field indexer_kv_dtype): bf16, or
+ * unscaled E4M3 with FP32 score accumulation. */
+enum { MSA_INDEX_BF16 = 0, MSA_INDEX_E4M3 = 1 };
+
+/* Workspace modes for msa_workspace_size. */
+enum { MSA_MODE_DECODE = 0, MSA_MODE_PREFILL = 1, MSA_MODE_PACK = 2 };
+
+/* Device error codes reported by msa_read_device_error. */
+enum {
+  MSA_DEVERR_NONE = 0,
+  MSA_DEVERR_PAGE = 1,     /* page id outside [0, num_slots/128) */
+  MSA_DEVERR_BLOCK = 2,    /* q2k id outside [0, blocks of the query) */
+  MSA_DEVERR_LENGTH = 3,   /* seq_len < 1, or above max_blocks * 128 */
+  MSA_DEVERR_TIMEOUT = 4   /* a bounded on-chip wait gave up */
+};
+
+/* Layer configuration (TensorRT-LLM MiniMaxM3SparseAttentionConfig fields:
+ * num_attention_heads, num_key_value_heads, sparse_num_index_heads,
+ * sparse_index_dim, sparse_block_size, sparse_topk_blocks,
+ * sparse_init_blocks, sparse_local_blocks, indexer_kv_dtype).
+ * Accepted: 64 / 4 / 128 / 4 / 128 / 128, 1 <= topk <= 16, init >= 0,
+ * local >= 0, init + local <= topk. */
+typedef struct {
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int num_index_heads;
+  int index_dim;
+  int block_size;
+  int topk;
+  int init_blocks;
+  int local_blocks;
+  int index_dtype;
+} msa_config;
+
+/* Fills `cfg` with the MiniMax-M3 defaults: 64/4/128/4/128/128, topk 16,
+ * init 0, local 1, bf16 index. */
+msa_status msa_config_default(msa_config* cfg);
+
+/* Checks `cfg` against the supported topology (NeMo require_msa_support). */
+msa_status msa_config_check(const msa_config* cfg);
+
+/* Bytes of workspace one call of the given mode needs.
+ *   MSA_MODE_DECODE : n = batch, max_blocks = blocks per request row of the
+ *                     page table (or ceil(max context / 128) when contiguous).
+ *   MSA_MODE_PREFILL: n = total compact tokens, max_blocks = ceil(max_seqlen/128).
+ *   MSA_MODE_PACK   : n = batch * seq of the document map, max_blocks = batch.
+ * The workspace must be zero-filled once before its first use (see
+ * msa_workspace_init), which clears the device error word in its first 256
+ * bytes.  Each call clears its own completion counters (a cudaMemsetAsync on
+ * `stream`) and the scorer stores rather than accumulates (NeMo
+ * _score_scratch), so one workspace can serve later calls of any size up to
+ * the one it was sized for.  Calls that share a workspace must not run
+ * concurrently. */
+msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int max_blocks,
+                              size_t* bytes);
+
+/* Zero-fills `bytes` of workspace on `stream` (cudaMemsetAsync). */
+msa_status msa_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Reads the device error word of `workspace` into *code and *detail (the
+ * offending index), then clears it.  Synchronises `stream`. */
+msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64_t* detail);
+
+/* Human-readable name of a status. */
+const char* msa_status_string(msa_status status);
+
+/* ---- step 1+2, decode: block scores + top-k ---------------------------------
+ * One query per request at position seq_lens[r]-1 over keys 0..seq_lens[r]-1
+ * (the query's own key is already in the cache).  Score of block b for index
+ * head g = max over the block's keys of <index_q[r,g,:], index_k[key,:]>,
+ * unscaled, fp32 accumulation (TensorRT-LLM sparse_score_type 'max',
+ * indexer_kv_dtype).  Key position p of request r sits at slot
+ *   page_table[r * max_blocks + p/128] * 128 + p % 128   (paged), or
+ *   cu_seqlens_k[r] + p                                   (page_table == NULL)
+ * of the paged side index-K cache [num_slots, 1, 128] that parallels the main
+ * K/V cache (TensorRT-LLM class description, MiniMaxM3KVCacheManagerV2).
+ *   index_q       dev [batch, 4, 128]  bf16 or e4m3 (cfg->index_dtype)
+ *   index_k_cache dev [num_slots, 1, 128] same dtype
+ *   seq_lens      dev int32 [batch], 1 <= seq_lens[r] <= max_blocks * 128
+ *   page_table    dev int32 [batch, max_blocks] or NULL
+ *   cu_seqlens_k  dev int64 [batch + 1], read only when page_table == NULL
+ *   q2k           dev int32 [4, batch, topk], fully written (ids asc, then -1)
+ *   workspace     >= msa_workspace_size(cfg, MSA_MODE_DECODE, batch, max_blocks)
+ */
+msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q,
+                                    const void* index_k_cache, const int32_t* seq_lens,
+                                    const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                    int batch, int max_blocks, int64_t num_slots, int32_t* q2k,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- step 3, decode: sparse GQA attention over the selected blocks ----------
+ * out[r, h, :] = softmax_j(scale * <q[r,h,:], k[j, h/16, :]>) v[j, h/16, :]
+ * over the keys j <= seq_lens[r]-1 of the blocks listed in q2k[h/16, r, :]
+ * (entries < 0 are ignored).  fp32 accumulation, bf16 output; a row with no
+ * key is written as zeros.  Same geometry arguments as the decode select.
+ *   q        dev [batch, 64, 128] bf16
+ *   k_cache  dev [num_slots, 4, 128] bf16;  v_cache: same
+ *   q2k      dev int32 [4, batch, topk]
+ *   out      dev [batch, 64, 128] bf16
+ */
+msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* q2k,
+                                    const int32_t* seq_lens, const int32_t* page_table,
+                                    const int64_t* cu_seqlens_k, int batch, int max_blocks,
+                                    int64_t num_slots, float scale, void* out, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/* ---- step 1+2, prefill: block scores + top-k on packed documents ------------
+ * NeMo MSAMicrobatch.select_blocks: compact tokens in document order, document
+ * d spanning [cu_seqlens[d], cu_seqlens[d+1]); token t of document d has
+ * position p = t - cu_seqlens[d] and candidate blocks 0..p/128 of its own
+ * document; the diagonal block's score covers keys <= p only.
+ *   index_q    dev [total_tokens, 4, 128] bf16 (post norm and RoPE)
+ *   index_k    dev [total_tokens, 1, 128] bf16
+ *   cu_seqlens dev int32 [num_docs + 1], cu_seqlens[0] = 0, strictly increasing,
+ *              cu_seqlens[num_docs] = total_tokens; max_seqlen = the longest document
+ *   q2k        dev int32 [4, total_tokens, topk]
+ * Only the bf16 index dtype is accepted here (MSA_ERR_DTYPE otherwise). */
+msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
+                                     const void* index_k, const int32_t* cu_seqlens, int num_docs,
+                                     int64_t total_tokens, int max_seqlen, int32_t* q2k,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- step 3, prefill: sparse GQA attention on packed documents ---------------
+ * NeMo sparse_attention / _SparseAttention.forward: bf16 q [tokens, 64, 128],
+ * k / v [tokens, 4, 128], int32 q2k [4, tokens, topk] -> bf16 out
+ * [tokens, 64, 128]; keys are the causal keys (position <= the query's) of the
+ * query's document inside the listed blocks. */
+msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k,
+                                     const void* v, const int32_t* q2k, const int32_t* cu_seqlens,
+                                     int num_docs, int64_t total_tokens, int max_seqlen,
+                                     float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* ---- packed layout of a document map ----------------------------------------
+ * NeMo layout-from-doc_ids constructor and _contiguous_runs: doc_ids is an
+ * int64 [batch, seq] map, 0 = padding, each positive id one contiguous run of
+ * tokens within its row.  Documents are the runs in row-major order.  Writes
+ *   cu_seqlens dev int32 [num_docs + 1]   (capacity batch*seq + 1)
+ *   token_rows dev int64 [total_tokens]   flat index of each real token (capacity batch*seq)
+ * and the host scalars *num_docs, *total_tokens, *max_seqlen.  Synchronises
+ * `stream` exactly once (one device-to-host copy of the scalars).
+ * Returns MSA_ERR_DOC_MAP for an empty map, a negative id, no real token, an
+ * interrupted document, or sizes past int32; *bad_index (host, may be NULL)
+ * then holds the flat index of the first offending token (-1 if none). */
+msa_status msa_pack_metadata(const int64_t* doc_ids, int batch, int seq, int32_t* cu_seqlens,
+                             int64_t* token_rows, int* num_docs, int64_t* total_tokens,
+                             int* max_seqlen, int64_t* bad_index, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* NeMo MSAMicrobatch.pack: packed[i, :] = external[token_rows[i], :] for rows
+ * of `row_bytes` bytes (a multiple of 16).  external dev [batch*seq, row_bytes],
+ * packed dev [total_tokens, row_bytes].  Always copies (never aliases). */
+msa_status msa_pack(const void* external, const int64_t* token_rows, int64_t total_tokens,
+                    int64_t row_bytes, void* packed, void* stream);
+
+/* NeMo MSAMicrobatch.unpack: external[token_rows[i], :] = packed[i, :] and
+ * every other row of external dev [batch_seq, row_bytes] zero-filled. */
+msa_status msa_unpack(const void* packed, const int64_t* token_rows, int64_t total_tokens,
+                      int64_t batch_seq, int64_t row_bytes, void* external, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -1,0 +1,60 @@
+"""Comparison helpers shared by the GPU parity tests."""
+import math
+
+import numpy as np
+import torch
+
+SCALE = 1.0 / math.sqrt(128.0)
+ATOL_MAX = 1e-2    # max-abs error of the bf16 output against the fp64 oracle
+ATOL_MEAN = 1e-3   # mean-abs error
+GAP_REL = 1e-5     # near-tie exemption of the k-th / (k+1)-th score
+
+
+def check_q2k(gpu_q2k, ref_q2k, gap, nb, topk, init, local, label=""):
+    """Bit-exact q2k except rows whose top-k boundary is a near tie (gap < 1e-5
+    relative); those rows are reported and must still be valid selections.
+    gpu_q2k / ref_q2k: [G, n, topk]; nb: [n] candidate blocks per query.
+    Returns (rows that differ, exempt rows)."""
+    gpu = np.asarray(gpu_q2k)
+    ref = np.asarray(ref_q2k)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    diff = (gpu != ref).any(axis=2)
+    exempt = np.asarray(gap) < GAP_REL
+    bad = diff & ~exempt
+    if bad.any():
+        g, i = np.argwhere(bad)[0]
+        raise AssertionError(f"{label}: q2k mismatch at head {g} row {i}: gpu {gpu[g, i]} ref {ref[g, i]} "
+                             f"(nb={nb[i]}, gap={gap[g, i]:.3g}); {bad.sum()} bad rows")
+    for g, i in np.argwhere(diff):
+        row = gpu[g, i]
+        sel = [b for b in row if b >= 0]
+        n = int(nb[i])
+        assert row.tolist() == sel + [-1] * (topk - len(sel))
+        assert sel == sorted(set(sel)) and len(sel) == min(topk, n)
+        forced = {b for b in range(n) if b < init or b >= n - local} if n > topk else set()
+        assert forced <= set(sel)
+    return int(diff.sum()), int(exempt.sum())
+
+
+def check_out(gpu_out, ref_out, label=""):
+    g = gpu_out.float().cpu().double().numpy() if isinstance(gpu_out, torch.Tensor) else np.asarray(gpu_out)
+    r = np.asarray(ref_out)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{label}: non-finite output"
+    err = np.abs(g - r)
+    mx, mean = float(err.max()), float(err.mean())
+    assert mx <= ATOL_MAX and mean <= ATOL_MEAN, f"{label}: max-abs {mx:.3g} mean-abs {mean:.3g}"
+    return mx, mean
+
+
+def decode_nb(seq_lens, max_blocks=None):
+    L = np.asarray(seq_lens.cpu() if isinstance(seq_lens, torch.Tensor) else seq_lens, dtype=np.int64)
+    nb = (L + 127) // 128
+    return nb if max_blocks is None else np.minimum(nb, max_blocks)
+
+
+def prefill_nb(cu_seqlens, tokens):
+    cu = np.asarray(cu_seqlens.cpu() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens, dtype=np.int64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    d = np.searchsorted(cu, tokens, side="right") - 1
+    return (tokens - cu[d]) // 128 + 1

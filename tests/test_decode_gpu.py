@@ -1,0 +1,105 @@
+"""Decode path on the GPU (through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_08_gb300 as msa
+import msa_synth
+import oracle
+from _parity import SCALE, check_out, check_q2k, decode_nb
+
+pytestmark = pytest.mark.gpu
+
+SMALL_LENS = [1, 2, 127, 128, 129, 300, 1000, 2048, 2049, 2050, 4095, 5000, 8191]
+
+
+def _run(d, topk, init, local):
+    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+    q2k = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, topk=topk, init_blocks=init,
+                                       local_blocks=local, **kw)
+    torch.cuda.synchronize()
+    ref_q2k, gap = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
+                                        cu_seqlens_k=d.cu_seqlens_k, topk=topk, init=init, local=local)
+    nb = decode_nb(d.seq_lens, d.max_blocks)
+    check_q2k(q2k.cpu().numpy(), ref_q2k, gap, nb, topk, init, local, "decode q2k")
+    # attention on the oracle's selection (identical q2k on both sides)
+    out = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, torch.from_numpy(ref_q2k).cuda(), d.seq_lens,
+                                       scale=SCALE, **kw)
+    torch.cuda.synchronize()
+    ref_out = oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, ref_q2k, SCALE,
+                                   page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k)
+    check_out(out, ref_out, "decode out")
+    return q2k, out
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (4, 1, 1), (3, 0, 0), (16, 2, 3), (1, 0, 1)])
+def test_decode_small(paged, topk, init, local):
+    d = msa_synth.decode_inputs(SMALL_LENS, paged=paged, seed=topk * 7 + init, device="cuda")
+    _run(d, topk, init, local)
+
+
+def test_decode_e4m3_small():
+    d = msa_synth.decode_inputs(SMALL_LENS, paged=True, index_dtype="e4m3", seed=3, device="cuda")
+    _run(d, 16, 0, 1)
+
+
+def test_decode_paged_equals_contiguous():
+    lens = [700, 4097, 129, 9000]
+    a = msa_synth.decode_inputs(lens, paged=True, seed=5, device="cuda")
+    pt = a.page_table.cpu().numpy()
+    rows = np.concatenate([pt[r, np.arange(L) // 128] * 128 + np.arange(L) % 128 for r, L in enumerate(lens)])
+    rows = torch.from_numpy(rows).cuda()
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int64, device="cuda")
+    q2k_a = msa.msa_select_blocks_decode(a.index_q, a.index_k_cache, a.seq_lens, page_table=a.page_table)
+    q2k_b = msa.msa_select_blocks_decode(a.index_q, a.index_k_cache[rows].contiguous(), a.seq_lens,
+                                         cu_seqlens_k=cu, max_blocks=a.max_blocks)
+    assert torch.equal(q2k_a, q2k_b)
+    oa = msa.msa_sparse_attend_decode(a.q, a.k_cache, a.v_cache, q2k_a, a.seq_lens, page_table=a.page_table)
+    ob = msa.msa_sparse_attend_decode(a.q, a.k_cache[rows].contiguous(), a.v_cache[rows].contiguous(), q2k_a,
+                                      a.seq_lens, cu_seqlens_k=cu, max_blocks=a.max_blocks)
+    assert torch.equal(oa, ob)
+
+
+def test_decode_repeated_calls_reuse_workspace():
+    """Each call clears its own counters, so one workspace serves repeated calls
+    of different sizes with identical results."""
+    d = msa_synth.decode_inputs([3000, 70, 9000, 128 * 20 + 1], paged=True, seed=9, device="cuda")
+    e = msa_synth.decode_inputs([50000, 20000], paged=True, seed=10, device="cuda")
+    kw = dict(page_table=d.page_table)
+    first = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, **kw)
+    o1 = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, first, d.seq_lens, **kw)
+    for _ in range(3):
+        other = msa.msa_select_blocks_decode(e.index_q, e.index_k_cache, e.seq_lens, page_table=e.page_table)
+        msa.msa_sparse_attend_decode(e.q, e.k_cache, e.v_cache, other, e.seq_lens, page_table=e.page_table)
+        again = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, **kw)
+        o2 = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, again, d.seq_lens, **kw)
+        assert torch.equal(first, again) and torch.equal(o1, o2)
+
+
+def test_decode_bad_page_is_reported_not_faulted():
+    d = msa_synth.decode_inputs([3000, 4000], paged=True, seed=2, device="cuda")
+    pt = d.page_table.clone()
+    pt[1, 3] = 10 ** 6  # outside the pool: the kernel's bounds check skips it
+    ws = msa.Workspace(msa.workspace_size(msa.make_config(), 0, 2, pt.shape[1]))
+    msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=pt, workspace=ws)
+    code, detail = ws.read_device_error()
+    assert code == 1 and detail == 1 * pt.shape[1] + 3
+    assert ws.read_device_error() == (0, 0)
+
+
+def test_decode_workload_b4_ctx8k_contig():
+    d = msa_synth.workload("decode_b4_ctx8k_contig", device="cuda")
+    _run(d, 16, 0, 1)
+
+
+@pytest.mark.slow
+def test_decode_workload_b64_paged():
+    d = msa_synth.workload("decode_b64_ctx4k_64k_paged", device="cuda")
+    _run(d, 16, 0, 1)
+
+
+@pytest.mark.slow
+def test_decode_workload_b16_128k_e4m3():
+    d = msa_synth.workload("decode_b16_ctx128k_paged_e4m3", device="cuda")
+    _run(d, 16, 0, 1)

@@ -1,0 +1,118 @@
+"""Packed-document prefill path on the GPU (through the C ABI) against the CPU oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_08_gb300 as msa
+import msa_synth
+import oracle
+from _parity import SCALE, check_out, check_q2k, prefill_nb
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _check(p, tokens=None, topk=16, init=0, local=1, attend=True):
+    q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=topk,
+                                        init_blocks=init, local_blocks=local)
+    torch.cuda.synchronize()
+    T = p.total_tokens
+    tok = np.arange(T, dtype=np.int64) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    ref_q2k, gap = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=topk, init=init,
+                                         local=local)
+    gq = q2k.cpu().numpy()[:, tok]
+    check_q2k(gq, ref_q2k, gap, prefill_nb(p.cu_seqlens, tok), topk, init, local, "prefill q2k")
+    if not attend:
+        return
+    # attention on the oracle's selection for the checked rows
+    full = q2k.clone()
+    idx = torch.from_numpy(tok).cuda()
+    full[:, idx] = torch.from_numpy(ref_q2k).cuda()
+    out = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, full, p.cu_seqlens, p.max_seqlen, scale=SCALE)
+    torch.cuda.synchronize()
+    ref_out = oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, ref_q2k, SCALE)
+    check_out(out[idx], ref_out, "prefill out")
+
+
+DOCS = [1, 127, 128, 129, 700, 2047, 2048, 2049, 3000, 5000]
+
+
+@pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (16, 1, 1), (4, 1, 1), (3, 0, 0), (2, 0, 2), (1, 1, 0)])
+def test_prefill_small(topk, init, local):
+    p = msa_synth.prefill_inputs(DOCS, seed=11 + topk + init, device="cuda")
+    _check(p, topk=topk, init=init, local=local)
+
+
+def test_prefill_single_short_document():
+    p = msa_synth.prefill_inputs([37], seed=1, device="cuda")
+    _check(p)
+
+
+def _three_block(index_k_vals):
+    T = 384
+    iq = torch.zeros(T, 4, 128)
+    iq[:, :, 0] = 1.0
+    ik = torch.zeros(T, 1, 128)
+    for row, val in index_k_vals.items():
+        ik[int(row), 0, 0] = val
+    v = (torch.arange(T) // 128 + 1).float()[:, None, None].expand(T, 4, 128).contiguous()
+
+    def bf(x):
+        return x.to(torch.bfloat16).cuda()
+    return bf(iq), bf(ik), bf(torch.zeros(T, 64, 128)), bf(torch.zeros(T, 4, 128)), bf(v)
+
+
+def test_hand_worked_three_blocks_on_gpu():
+    with open(os.path.join(GOLDEN, "hand_worked_3block.json")) as f:
+        g = json.load(f)
+    cu = torch.tensor([0, 384], dtype=torch.int32, device="cuda")
+    for case in g["cases"]:
+        topk = case.get("topk_override", g["setup"]["topk"])
+        iq, ik, q, k, v = _three_block(case["index_k"])
+        q2k = msa.msa_select_blocks_prefill(iq, ik, cu, 384, topk=topk, init_blocks=case["init"],
+                                            local_blocks=case["local"])
+        out = msa.msa_sparse_attend_prefill(q, k, v, q2k, cu, 384, scale=SCALE)
+        for t, exp in case["expect"].items():
+            for gg in range(4):
+                assert q2k[gg, int(t)].tolist() == exp["q2k"], (case["name"], t, gg)
+            np.testing.assert_allclose(out[int(t)].float().cpu().numpy(), exp["out"], atol=1e-2)
+
+
+def test_prefill_repeated_calls_are_identical():
+    p = msa_synth.prefill_inputs([3000, 400, 2500], seed=4, device="cuda")
+    o = msa_synth.prefill_inputs([9000], seed=5, device="cuda")
+    a = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
+    oa = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, a, p.cu_seqlens, p.max_seqlen)
+    for _ in range(3):
+        x = msa.msa_select_blocks_prefill(o.index_q, o.index_k, o.cu_seqlens, o.max_seqlen)
+        msa.msa_sparse_attend_prefill(o.q, o.k, o.v, x, o.cu_seqlens, o.max_seqlen)
+        b = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
+        ob = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, b, p.cu_seqlens, p.max_seqlen)
+        assert torch.equal(a, b) and torch.equal(oa, ob)
+
+
+def _sample_tokens(cu, n, seed):
+    cu = np.asarray(cu.cpu(), dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(cu[-1], size=n, replace=False).tolist())
+    for d in range(len(cu) - 1):  # document edges and block edges
+        for off in (0, 1, 127, 128, 129, 2047, 2048):
+            if cu[d] + off < cu[d + 1]:
+                pick.add(int(cu[d] + off))
+        pick.add(int(cu[d + 1] - 1))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+@pytest.mark.slow
+def test_prefill_workload_1doc_16k():
+    p = msa_synth.workload("prefill_1doc_16k", device="cuda")
+    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 0))
+
+
+@pytest.mark.slow
+def test_prefill_workload_packed_2x32k():
+    p = msa_synth.workload("prefill_packed_2x32k", device="cuda")
+    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 1), init=1, local=1)
