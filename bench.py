@@ -1,0 +1,401 @@
+"""Benchmark of one MiniMax-M3 block-sparse attention step (score + select + attend).
+
+Default workload: a decode step of 64 requests with contexts U{4096..65536}
+over paged K/V and index-K caches (bf16), top-16, init 0, local 1.  One step =
+msa_select_blocks_decode + msa_sparse_attend_decode over the whole batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  The device-timed value uses CUDA events on the
+launching stream around each step; L2 is flushed (a 256 MiB write) between
+steps, outside the timed events.  Under torchrun each rank runs its own
+independent batch (weak scaling, no collective on the data path); the time is
+the max over ranks.  ``--impl reference`` times the CPU oracle on this host's
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import msa_synth  # noqa: E402
+
+METRIC = "query tokens/s of score+select+attend; HBM GB/s (decode), TFLOP/s (prefill)"
+DEFAULT_WORKLOAD = "decode_b64_ctx4k_64k_paged"
+SCALE = 1.0 / math.sqrt(128.0)
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---- algorithmic work per step -------------------------------------------------------
+
+def decode_work(d, q2k):
+    """(bytes_select, bytes_attend).  Select: the index-K of every scored context
+    once (contexts with nb <= topk keep every block and read nothing) plus the
+    index queries.  Attend: K and V of every attended key once per KV head, plus
+    q and out."""
+    lens = d.seq_lens.cpu().numpy().astype(np.int64)
+    nb = (lens + 127) // 128
+    scored = nb > d.topk
+    idx_bytes = 128 if d.index_dtype == "e4m3" else 256
+    b_sel = int((lens[scored] * idx_bytes).sum()) + d.batch * 4 * idx_bytes
+    q = q2k.cpu().numpy()
+    keys = 0
+    for g in range(4):
+        blk = q[g]
+        k = np.minimum(128, lens[:, None] - 128 * blk)
+        keys += int(np.where(blk >= 0, k, 0).sum())
+    b_att = keys * 2 * 128 * 2 + 2 * d.batch * 64 * 128 * 2
+    return b_sel, b_att
+
+
+def prefill_work(p, q2k):
+    """(flops_select, flops_attend): causal valid index pairs x 4 heads x 2*128;
+    selected causal keys x 16 heads x 4*128 (QK^T and PV)."""
+    cu = p.cu_seqlens.cpu().numpy().astype(np.int64)
+    lens = np.diff(cu)
+    f_sel = float(sum(4 * 2 * 128 * n * (n + 1) // 2 for n in lens))
+    q = q2k.cpu().numpy()
+    T = p.total_tokens
+    doc = np.searchsorted(cu, np.arange(T), side="right") - 1
+    pos = np.arange(T) - cu[doc]
+    keys = 0
+    for g in range(4):
+        blk = q[g]
+        k = np.minimum(128, pos[:, None] - 128 * blk + 1)
+        keys += int(np.where(blk >= 0, k, 0).sum())
+    return f_sel, float(keys) * 16 * 4 * 128
+
+
+# ---- clocks --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the GPU arm -----------------------------------------------------------------------
+
+def run_gpu(args, rank, world, device):
+    import block_sparse_attention_08_gb300 as msa
+    torch.cuda.set_device(device)
+    name = args.workload
+    inp = msa_synth.workload(name, seed=args.seed + rank, device=device, max_requests=args.requests)
+    decode = name.startswith("decode")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    hbm_peak, tf_peak, peak_src = _peaks()
+
+    if decode:
+        d = inp
+        kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+        q2k = torch.empty((4, d.batch, d.topk), dtype=torch.int32, device=device)
+        out = torch.empty((d.batch, 64, 128), dtype=torch.bfloat16, device=device)
+
+        def sel():
+            msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, topk=d.topk,
+                                         init_blocks=d.init_blocks, local_blocks=d.local_blocks, q2k=q2k, **kw)
+
+        def att():
+            msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE, out=out, **kw)
+        n_queries = d.batch
+    else:
+        p = inp
+        q2k = torch.empty((4, p.total_tokens, p.topk), dtype=torch.int32, device=device)
+        out = torch.empty((p.total_tokens, 64, 128), dtype=torch.bfloat16, device=device)
+
+        def sel():
+            msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=p.topk,
+                                          init_blocks=p.init_blocks, local_blocks=p.local_blocks, q2k=q2k)
+
+        def att():
+            msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE, out=out)
+        n_queries = p.total_tokens
+
+    for _ in range(args.warmup):
+        sel()
+        att()
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    work = decode_work(inp, q2k) if decode else prefill_work(inp, q2k)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 255)
+            ev[i][0].record(stream)
+            sel()
+            ev[i][1].record(stream)
+            att()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    ms = sum(a + b for a, b in zip(t_sel, t_att)) / args.steps
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of the step's inputs, D2H of the output.  Decode: the new queries,
+    # lengths and page table (the K/V and index-K caches are resident state);
+    # prefill: every input tensor.
+    if decode:
+        hosts = [d.q, d.index_q, d.seq_lens, d.page_table if d.page_table is not None else d.cu_seqlens_k]
+    else:
+        hosts = [p.q, p.k, p.v, p.index_q, p.index_k, p.cu_seqlens]
+    h_in = [x.cpu().pin_memory() for x in hosts]
+    d_in = [torch.empty_like(x, device=device) for x in h_in]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for h, dd in zip(h_in, d_in):
+            dd.copy_(h, non_blocking=True)
+        if decode:
+            dq, diq, dsl, dpt = d_in
+            kw2 = dict(page_table=dpt) if d.page_table is not None else dict(cu_seqlens_k=dpt)
+            msa.msa_select_blocks_decode(diq, d.index_k_cache, dsl, topk=d.topk, init_blocks=d.init_blocks,
+                                         local_blocks=d.local_blocks, q2k=q2k, max_blocks=d.max_blocks, **kw2)
+            msa.msa_sparse_attend_decode(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out=out,
+                                         max_blocks=d.max_blocks, **kw2)
+        else:
+            q_, k_, v_, iq_, ik_, cu_ = d_in
+            msa.msa_select_blocks_prefill(iq_, ik_, cu_, p.max_seqlen, topk=p.topk, init_blocks=p.init_blocks,
+                                          local_blocks=p.local_blocks, q2k=q2k)
+            msa.msa_sparse_attend_prefill(q_, k_, v_, q2k, cu_, p.max_seqlen, scale=SCALE, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    return dict(ms=ms, sel_ms=sum(t_sel) / len(t_sel), att_ms=sum(t_att) / len(t_att),
+                e2e_ms=sum(e_ms) / len(e_ms), n_queries=n_queries, work=work, h2d=h2d, d2h=d2h,
+                clocks=clk.summary(), decode=decode, hbm_peak=hbm_peak, tf_peak=tf_peak, peak_src=peak_src)
+
+
+_CPU_INPUTS: dict = {}
+
+
+def cpu_baseline(name, seed, budget_s=15.0):
+    """The oracle, as it stands, on this host's cores over a bounded sample:
+    whole requests (decode) or random query tokens (prefill), until the
+    budget is spent."""
+    import oracle
+    oracle.build()
+    key = (name, seed)
+    if key not in _CPU_INPUTS:
+        _CPU_INPUTS[key] = msa_synth.workload(name, seed=seed, device="cpu")
+    inp = _CPU_INPUTS[key]
+    cores = os.cpu_count()
+    t0 = time.time()
+    done = 0
+    if name.startswith("decode"):
+        d = inp
+        B = d.batch
+        chunk = max(1, min(B, cores))
+        while done < B and time.time() - t0 < budget_s:
+            req = np.arange(done, min(B, done + chunk), dtype=np.int64)
+            q2k, _ = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
+                                          cu_seqlens_k=d.cu_seqlens_k, requests=req, topk=d.topk,
+                                          init=d.init_blocks, local=d.local_blocks)
+            oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, q2k, SCALE, page_table=d.page_table,
+                                 cu_seqlens_k=d.cu_seqlens_k, requests=req)
+            done += len(req)
+        sample = f"{done} of {B} requests of {name}, whole select+attend per request"
+    else:
+        p = inp
+        T = p.total_tokens
+        perm = np.random.default_rng(seed).permutation(T)
+        chunk = max(1, cores)
+        while done < T and time.time() - t0 < budget_s:
+            tok = np.sort(perm[done: done + chunk]).astype(np.int64)
+            q2k, _ = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=p.topk,
+                                           init=p.init_blocks, local=p.local_blocks)
+            oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, q2k, SCALE)
+            done += len(tok)
+        sample = f"{done} random query tokens of {T} of {name}"
+    dt = time.time() - t0
+    return {"value": round(done / dt, 3), "unit": "query tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds": round(dt, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(msa_synth.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="keep only the first N requests of a decode workload (small profiling cases)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    unit = "query tokens/s"
+    config = {"workload": args.workload, "desc": msa_synth.WORKLOADS[args.workload], "seed": args.seed}
+    if args.requests:
+        config["requests"] = args.requests
+
+    if args.impl == "reference":
+        if rank == 0:
+            for _ in range(args.warmup):
+                cpu_baseline(args.workload, args.seed, budget_s=1.0)
+            vals, info = [], None
+            for _ in range(args.steps):
+                info = cpu_baseline(args.workload, args.seed, budget_s=6.0)
+                vals.append(info["value"])
+            v = sum(vals) / len(vals)
+            info["value"] = v
+            line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+                    "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                    "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                    "cpu_baseline": info,
+                    "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line))
+        if world > 1:
+            torch.distributed.barrier()
+        return
+
+    device = torch.device("cuda", local)
+    res = run_gpu(args, rank, world, device)
+    ms, e2e_ms = res["ms"], res["e2e_ms"]
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+    value = res["n_queries"] * world / (ms * 1e-3)
+    e2e = res["n_queries"] * world / (e2e_ms * 1e-3)
+    dom = "select" if res["sel_ms"] >= res["att_ms"] else "attend"
+    if res["decode"]:
+        b_sel, b_att = res["work"]
+        sel_r = b_sel / (res["sel_ms"] * 1e-3) / 1e9
+        att_r = b_att / (res["att_ms"] * 1e-3) / 1e9
+        ach = sel_r if dom == "select" else att_r
+        roof = {"bound": "hbm", "kernel": "decode_select_kernel" if dom == "select" else "sparse_attend_kernel",
+                "achieved": round(ach, 1), "peak": res["hbm_peak"], "unit": "GB/s",
+                "frac": round(ach / res["hbm_peak"], 4), "traffic": None,
+                "peak_source": res["peak_src"] + " hbm_gbs (copy, burst)",
+                "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "bytes": b_sel, "GB/s": round(sel_r, 1)},
+                               "attend": {"ms": round(res["att_ms"], 4), "bytes": b_att, "GB/s": round(att_r, 1)},
+                               "step_GB/s": round((b_sel + b_att) / (ms * 1e-3) / 1e9, 1)}}
+        dtype = "bf16" if "e4m3" not in args.workload else "e4m3-index/bf16"
+    else:
+        f_sel, f_att = res["work"]
+        sel_r = f_sel / (res["sel_ms"] * 1e-3) / 1e12
+        att_r = f_att / (res["att_ms"] * 1e-3) / 1e12
+        ach = sel_r if dom == "select" else att_r
+        roof = {"bound": "tensor", "kernel": "prefill_select_kernel" if dom == "select" else "sparse_attend_kernel",
+                "achieved": round(ach, 2), "peak": res["tf_peak"], "unit": "TFLOP/s",
+                "frac": round(ach / res["tf_peak"], 4), "traffic": None,
+                "peak_source": res["peak_src"] + " bf16_tflops (burst)",
+                "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "flop": f_sel, "TFLOP/s": round(sel_r, 2)},
+                               "attend": {"ms": round(res["att_ms"], 4), "flop": f_att, "TFLOP/s": round(att_r, 2)},
+                               "step_TFLOP/s": round((f_sel + f_att) / (ms * 1e-3) / 1e12, 2)}}
+        dtype = "bf16"
+    config.update({"queries_per_step": res["n_queries"],
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"})
+    line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config, "roofline": roof,
+            "e2e": {"value": round(e2e, 1), "unit": unit, "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": (2 if res["decode"] else 3) * args.steps, "clocks": res["clocks"]}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

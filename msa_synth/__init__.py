@@ -211,16 +211,19 @@ WORKLOADS = {
 }
 
 
-def workload(name: str, *, seed: int = 0, device="cpu", scale_down: int = 1):
-    """Build a named workload.  ``scale_down`` > 1 shrinks the sizes (tests)."""
+def workload(name: str, *, seed: int = 0, device="cpu", scale_down: int = 1, max_requests: int | None = None):
+    """Build a named workload.  ``scale_down`` > 1 shrinks the sizes;
+    ``max_requests`` keeps the first requests of a decode batch (small
+    profiling cases)."""
     rng = np.random.Generator(np.random.PCG64(seed))
+    cut = (lambda x: x[:max_requests]) if max_requests else (lambda x: x)
     if name == "decode_b4_ctx8k_contig":
         L = max(8192 // scale_down, 1)
-        return decode_inputs([L] * 4, paged=False, seed=seed, device=device)
+        return decode_inputs(cut([L] * 4), paged=False, seed=seed, device=device)
     if name == "decode_b64_ctx4k_64k_paged":
         lens = rng.integers(4096, 65536 + 1, size=64)
         lens = np.maximum(lens // scale_down, 1)
-        return decode_inputs(lens, paged=True, seed=seed, device=device,
+        return decode_inputs(cut(lens), paged=True, seed=seed, device=device,
                              max_blocks=(65536 // scale_down + BLOCK - 1) // BLOCK)
     if name == "prefill_1doc_16k":
         return prefill_inputs([max(16384 // scale_down, 1)], seed=seed, device=device)
@@ -233,5 +236,5 @@ def workload(name: str, *, seed: int = 0, device="cpu", scale_down: int = 1):
         return p
     if name == "decode_b16_ctx128k_paged_e4m3":
         L = max(131072 // scale_down, 1)
-        return decode_inputs([L] * 16, paged=True, index_dtype="e4m3", seed=seed, device=device)
+        return decode_inputs(cut([L] * 16), paged=True, index_dtype="e4m3", seed=seed, device=device)
     raise KeyError(name)
