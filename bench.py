@@ -300,6 +300,16 @@ def cpu_baseline(name, seed, budget_s=15.0):
             "sample": sample, "seconds": round(dt, 2)}
 
 
+def max_over_ranks(values, world):
+    """Element-wise max of per-rank timings (host-side gloo collective; the data
+    path itself has no collective)."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -347,11 +357,7 @@ def main():
 
     device = torch.device("cuda", local)
     res = run_gpu(args, rank, world, device)
-    ms, e2e_ms = res["ms"], res["e2e_ms"]
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([res["ms"], res["e2e_ms"]], world)
     if rank != 0:
         return
     value = res["n_queries"] * world / (ms * 1e-3)
