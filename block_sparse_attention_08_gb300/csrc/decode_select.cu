@@ -409,3 +409,73 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
 }
 
 }  // namespace msa
+
+// ---- allocation-free variant of the decode select ---------------------------------
+// Some callers cannot allocate device memory at the point where they select
+// blocks: code that runs inside an allocator-less runtime, plugins handed only
+// their input and output buffers, or hosts whose memory pool is fixed before
+// the model loads.  For them the block scores and completion counters live in
+// one fixed array in the library's own device memory, sized once for every GPU
+// that loads the library.
+#include <mutex>
+
+namespace msa {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[256] = {};  // device address of g_noalloc_scratch, per device ordinal
+
+// Device address of the fixed scratch on the current device (looked up once per
+// device; the host-side name of the array is not a device address).
+static void* noalloc_scratch(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 256) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+static size_t noalloc_up256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace msa
+
+extern "C" msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, const void* index_q,
+                                                      const void* index_k_cache, const int32_t* seq_lens,
+                                                      const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                                      int batch, int max_blocks, int64_t num_slots, int32_t* q2k,
+                                                      void* stream) {
+  using namespace msa;
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!index_q || !index_k_cache || !q2k || !seq_lens || (!page_table && !cu_seqlens_k)) return MSA_ERR_NULL;
+  if (batch < 1 || max_blocks < 1 || num_slots < 1 || num_slots >= (1LL << 31)) return MSA_ERR_SHAPE;
+  if (page_table && num_slots % kBlock) return MSA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(index_q) & 15) || (reinterpret_cast<uintptr_t>(index_k_cache) & 15))
+    return MSA_ERR_ALIGN;
+  const size_t off_tickets = kHeaderBytes;
+  const size_t off_scores = off_tickets + noalloc_up256(static_cast<size_t>(batch) * sizeof(int));
+  const size_t need = off_scores + static_cast<size_t>(batch) * kKvHeads * max_blocks * sizeof(float);
+  if (need > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // sizes beyond the fixed scratch
+  cudaError_t e;
+  auto* base = static_cast<uint8_t*>(noalloc_scratch(&e));
+  if (!base) return MSA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the error word and the counters must start at zero; the scores are stored before they are read
+  if (cudaMemsetAsync(base, 0, off_scores, s) != cudaSuccess) return MSA_ERR_CUDA;
+  e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
+                           num_slots, q2k, reinterpret_cast<float*>(base + off_scores),
+                           reinterpret_cast<int*>(base + off_tickets), reinterpret_cast<DevError*>(base), s);
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}

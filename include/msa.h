@@ -147,6 +147,29 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q,
                                     int batch, int max_blocks, int64_t num_slots, int32_t* q2k,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- decode select without a workspace ---------------------------------------
+ * The same computation and arguments as msa_select_blocks_decode, for callers
+ * that cannot allocate device memory (for example code running inside a
+ * runtime with no allocator of its own, or a plugin that is handed only its
+ * input and output buffers).  The pages have no counterpart: this is a
+ * deployment convenience of this library.
+ *   - Scratch is one fixed 4 MiB array in the library's device memory, held by
+ *     every GPU that loads the library until the process exits.  It must hold
+ *     256 + round_up(4*batch, 256) + 16*batch*max_blocks bytes; larger sizes
+ *     are rejected with MSA_ERR_WORKSPACE before any work is enqueued.
+ *   - The first call on each device looks up the array's device address on
+ *     the current device; make that first call before any stream capture.
+ *   - Every call uses the same array and leaves its contents behind; the call
+ *     clears what must start at zero on `stream`.  Calls whose work overlaps
+ *     on the GPU (other streams, other threads) race on the array.
+ *   - Device-side data errors are recorded in the array, not reported.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library. */
+msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, const void* index_q,
+                                            const void* index_k_cache, const int32_t* seq_lens,
+                                            const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                            int batch, int max_blocks, int64_t num_slots, int32_t* q2k,
+                                            void* stream);
+
 /* ---- step 3, decode: sparse GQA attention over the selected blocks ----------
  * out[r, h, :] = softmax_j(scale * <q[r,h,:], k[j, h/16, :]>) v[j, h/16, :]
  * over the keys j <= seq_lens[r]-1 of the blocks listed in q2k[h/16, r, :]
