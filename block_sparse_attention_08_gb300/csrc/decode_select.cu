@@ -9,23 +9,27 @@
 // blocks forced in.
 //
 // GB300 design: the paged index-K cache is streamed from HBM once.  Each
-// 128-key page (32 KB bf16 / 16 KB E4M3, contiguous) is one work item, brought
-// into shared memory by a single 1-D bulk TMA copy into a 3-deep ring.  The
-// (request, block) items of all requests are split evenly across a persistent
-// grid (stream-K), so every SM streams the same number of bytes.  Four warps
-// score 32 keys each on the tensor cores (mma.sync: keys as A, the 4 index
-// heads as B, fp32 accumulate), reduce the block max across lanes and warps,
-// and store one fp32 score per (request, head, block).  The CTA that finishes
-// the last block of a request (an atomic ticket, no waiting) runs the top-k for
-// that request's 4 heads: a warp per head, a threshold from the 32 lane maxima
-// filters the candidates, then an exact (score desc, id asc) pick.
+// 128-key page (32 KB bf16 / 16 KB E4M3, contiguous) is one work item.  The
+// (request, page) items of all requests are split evenly across a persistent
+// grid of one CTA per SM (stream-K), so every SM streams the same number of
+// bytes.  Inside a CTA a producer warp resolves 32 page ids at a time with
+// one coalesced load and issues one 1-D bulk TMA copy per page into a ring of
+// 192 KB of shared memory (6 bf16 / 12 E4M3 pages in flight); six consumer
+// warps each take whole pages round-robin (stage s always to warp s % 6) and score all 128 keys on the
+// tensor cores (mma.sync: keys as A read straight from the page, the 4 index
+// heads as B, fp32 accumulate), reduce the block max in registers and store
+// one fp32 score per (request, head, page).  No CTA-wide barrier sits in the
+// loop.  Each finished page bumps an atomic per-request counter; the warp that
+// completes a request (no waiting) runs its top-k: per head, the need-th
+// largest of the 32 lane maxima is a threshold that filters the candidates,
+// then an exact (score desc, id asc) pick.
 #include "launch.h"
 
 namespace msa {
 
-constexpr int kSelStages = 3;
-constexpr int kSelStageBytes = kBlock * kIdxDim * 2;  // one bf16 page
-constexpr int kSelThreads = 128;
+constexpr int kSelConsumers = 6;  // a divisor of the stage counts (6 bf16, 12 E4M3)
+constexpr int kSelThreads = 32 * (kSelConsumers + 1);
+constexpr int kSelRingBytes = 192 * 1024;
 constexpr int kCandCap = 64;  // per-warp candidate list of the top-k filter
 
 struct DecodeGeom {
@@ -37,12 +41,17 @@ struct DecodeGeom {
   long long num_slots;
 };
 
+struct SelMeta {
+  int r, b, rows, pad;
+};
+
+template <int kStages>
 struct SelSmem {
-  alignas(1024) uint8_t stage[kSelStages][kSelStageBytes];
-  uint64_t full[kSelStages];
-  int stage_rows[kSelStages];
-  float red[2][4][4];  // [parity][warp][head]
-  unsigned long long cand[4][kCandCap];
+  alignas(1024) uint8_t ring[kSelRingBytes];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  SelMeta meta[kStages];
+  unsigned long long cand[kSelConsumers][kCandCap];
   int scan[kSelThreads / 32];
   int bcast[4];
 };
@@ -156,22 +165,30 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
 }
 
 template <int kE4M3>
-__global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
+__global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     const uint8_t* __restrict__ index_q, const uint8_t* __restrict__ index_k, DecodeGeom geo,
     float* __restrict__ scores, int* __restrict__ tickets, int32_t* __restrict__ q2k, int topk,
     int init, int local, DevError* err) {
-  extern __shared__ uint8_t smem_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g8 = lane >> 2, t4 = lane & 3;
   constexpr int kRowBytes = kE4M3 ? kIdxDim : kIdxDim * 2;
+  constexpr int kPageBytes = kBlock * kRowBytes;
+  constexpr int kStages = kSelRingBytes / kPageBytes;
+  // stage s is always consumed by warp s % kSelConsumers, so a warp never waits
+  // on a stage more than one mbarrier phase ahead
+  static_assert(kStages % kSelConsumers == 0, "stages must be a multiple of the consumer warps");
+  extern __shared__ uint8_t smem_raw[];
+  auto& sm = *reinterpret_cast<SelSmem<kStages>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = geo.batch, mb = geo.max_blocks;
 
   if (tid == 0) {
-    for (int s = 0; s < kSelStages; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
     fence_mbar_init();
   }
-  // total scored blocks; rows of unscored requests are written here
+  // total scored pages; rows of requests that need no scoring are written here
   int total = 0;
   for (int r0 = 0; r0 < B; r0 += kSelThreads) {
     const int r = r0 + tid;
@@ -227,83 +244,105 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
   }
   const int n_items = static_cast<int>(hi - lo);
 
-  // producer cursor (thread 0 only)
-  int pr = r_lo, pb = static_cast<int>(lo - off_lo), pnb = 0;
-  if (tid == 0) pnb = scored_blocks(geo, pr, topk, nullptr);
-  auto issue = [&](int i) {  // thread 0: load item i into its stage
-    const int s = i % kSelStages;
-    const int L = geo.seq_lens[pr];
-    const int rows = min(kBlock, L - pb * kBlock);
-    long long row0;
-    bool ok = rows > 0;
-    if (geo.page_table) {
-      const int page = geo.page_table[static_cast<long long>(pr) * mb + pb];
-      row0 = static_cast<long long>(page) * kBlock;
-      if (page < 0 || row0 + kBlock > geo.num_slots) {
-        record_error(err, MSA_DEVERR_PAGE, static_cast<long long>(pr) * mb + pb);
-        ok = false;
+  if (warp == kSelConsumers) {
+    // ---------------- producer warp ----------------
+    int r = r_lo, b = static_cast<int>(lo - off_lo);
+    int i = 0;
+    while (i < n_items) {
+      const int nbr = scored_blocks(geo, r, topk, nullptr);
+      const int L = geo.seq_lens[r];
+      const int cnt = min(min(nbr - b, n_items - i), 32);
+      // one coalesced load resolves the next (up to) 32 pages of this request
+      long long row0 = 0;
+      int ok = 0;
+      if (lane < cnt) {
+        const int bb = b + lane;
+        const int rows = min(kBlock, L - bb * kBlock);
+        if (geo.page_table) {
+          const int page = geo.page_table[static_cast<long long>(r) * mb + bb];
+          row0 = static_cast<long long>(page) * kBlock;
+          ok = page >= 0 && row0 + kBlock <= geo.num_slots;
+          if (!ok) record_error(err, MSA_DEVERR_PAGE, static_cast<long long>(r) * mb + bb);
+        } else {
+          row0 = geo.cu_k[r] + static_cast<long long>(bb) * kBlock;
+          ok = row0 >= 0 && row0 + rows <= geo.num_slots;
+          if (!ok) record_error(err, MSA_DEVERR_PAGE, r);
+        }
+        ok = ok && rows > 0 ? rows : 0;
       }
-    } else {
-      row0 = geo.cu_k[pr] + static_cast<long long>(pb) * kBlock;
-      if (row0 < 0 || row0 + rows > geo.num_slots) {
-        record_error(err, MSA_DEVERR_PAGE, pr);
-        ok = false;
+      for (int k = 0; k < cnt; ++k, ++i) {
+        const long long pr0 = __shfl_sync(0xffffffffu, row0, k);
+        const int rows = __shfl_sync(0xffffffffu, ok, k);
+        if (lane == 0) {
+          const int s = i % kStages;
+          mbar_wait(&sm.empty[s], ((i / kStages) & 1) ^ 1, err, 101);
+          sm.meta[s] = SelMeta{r, b + k, rows, 0};
+          if (rows > 0) {
+            mbar_expect_tx(&sm.full[s], static_cast<uint32_t>(rows * kRowBytes));
+            tma_bulk_g2s(sm.ring + s * kPageBytes, index_k + pr0 * kRowBytes, static_cast<uint32_t>(rows * kRowBytes),
+                         &sm.full[s]);
+          } else {
+            mbar_arrive(&sm.full[s]);
+          }
+        }
+        __syncwarp();
+      }
+      b += cnt;
+      if (b == nbr && i < n_items) {
+        b = 0;
+        do {
+          ++r;
+        } while (scored_blocks(geo, r, topk, nullptr) == 0);
       }
     }
-    sm.stage_rows[s] = ok ? rows : 0;
-    if (ok) {
-      mbar_expect_tx(&sm.full[s], static_cast<uint32_t>(rows * kRowBytes));
-      tma_bulk_g2s(sm.stage[s], index_k + row0 * kRowBytes, static_cast<uint32_t>(rows * kRowBytes), &sm.full[s]);
-    } else {
-      mbar_arrive(&sm.full[s]);
-    }
-    if (++pb == pnb) {  // advance to the next scored request
-      pb = 0;
-      do {
-        ++pr;
-        pnb = pr < B ? scored_blocks(geo, pr, topk, nullptr) : 1;
-      } while (pnb == 0);
-    }
-  };
-  __syncthreads();
-  if (tid == 0)
-    for (int i = 0; i < kSelStages - 1 && i < n_items; ++i) issue(i);
+    return;
+  }
 
-  // consumer cursor (all threads)
-  int cr = r_lo, cb = static_cast<int>(lo - off_lo), seg_start = cb;
-  int cnb = scored_blocks(geo, cr, topk, nullptr);
+  // ---------------- consumer warps: whole pages, round-robin ----------------
+  const int g8 = lane >> 2, t4 = lane & 3;
+  int cur_r = -1, cur_nb = 0;
   uint32_t qf[4][4];
-  auto load_q = [&](int r) {
-    constexpr int kQChunks = kE4M3 ? 2 : 4;
-    for (int j = 0; j < 4; ++j) qf[j][0] = qf[j][1] = qf[j][2] = qf[j][3] = 0u;
-    if (g8 < kKvHeads)
-      for (int j = 0; j < kQChunks; ++j) {
-        // bf16: dims 32j + 8t .. +8 ; e4m3: dims 64j + 16t .. +16 -- both at byte 64j + 16t
-        const uint8_t* p = index_q + (static_cast<long long>(r) * kKvHeads + g8) * kRowBytes + 64 * j + 16 * t4;
-        const uint4 v = *reinterpret_cast<const uint4*>(p);
-        qf[j][0] = v.x;
-        qf[j][1] = v.y;
-        qf[j][2] = v.z;
-        qf[j][3] = v.w;
+  for (int i = warp; i < n_items; i += kSelConsumers) {
+    const int s = i % kStages;
+    mbar_wait(&sm.full[s], (i / kStages) & 1, err, 100);
+    const SelMeta meta = sm.meta[s];
+    if (meta.r < 0 || meta.r >= B || meta.b < 0 || meta.b >= mb) {  // never expected: guard the stores
+      record_error(err, MSA_DEVERR_TIMEOUT, 1000000 + i);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      continue;
+    }
+    if (meta.r != cur_r) {
+      cur_r = meta.r;
+      cur_nb = scored_blocks(geo, cur_r, topk, nullptr);
+      constexpr int kQChunks = kE4M3 ? 2 : 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) qf[j][0] = qf[j][1] = qf[j][2] = qf[j][3] = 0u;
+      if (g8 < kKvHeads) {
+#pragma unroll
+        for (int j = 0; j < kQChunks; ++j) {
+          // bf16: dims 32j + 8t .. +8 ; e4m3: dims 64j + 16t .. +16 -- both at byte 64j + 16t
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              index_q + (static_cast<long long>(cur_r) * kKvHeads + g8) * kRowBytes + 64 * j + 16 * t4);
+          qf[j][0] = v.x;
+          qf[j][1] = v.y;
+          qf[j][2] = v.z;
+          qf[j][3] = v.w;
+        }
       }
-  };
-  load_q(cr);
-
-  for (int i = 0; i < n_items; ++i) {
-    const int s = i % kSelStages;
-    if (tid == 0 && i + kSelStages - 1 < n_items) issue(i + kSelStages - 1);
-    mbar_wait(&sm.full[s], (i / kSelStages) & 1, err, 100);
-    const int rows = sm.stage_rows[s];
-    const uint32_t base = smem_u32(sm.stage[s]);
+    }
+    const int rows = meta.rows;
+    const uint32_t base = smem_u32(sm.ring + s * kPageBytes);
     float mx0 = -INFINITY, mx1 = -INFINITY;  // heads 2*t4, 2*t4+1
-    for (int m = 0; m < 2; ++m) {
-      const int key0 = 32 * warp + 16 * m;
+#pragma unroll 2
+    for (int m = 0; m < kBlock / 16; ++m) {
+      const int key0 = 16 * m;
       if (key0 >= rows) break;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t ra_addr = base + (key0 + g8) * kRowBytes;
       const uint32_t rb_addr = ra_addr + 8 * kRowBytes;
-      // each thread reads 16 contiguous bytes of a key row; the k slots of the
-      // MMA take them in a fixed permutation that B (index_q) repeats
+      // each thread reads 16 contiguous bytes of a key row; the MMA k slots take
+      // them in a fixed permutation that B (index_q) repeats, so none is moved
       if (!kE4M3) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -334,50 +373,31 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(
         mx1 = fmaxf(mx1, c[3]);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);  // page consumed
     for (int o = 4; o < 32; o <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
     if (lane < 2) {
-      sm.red[i & 1][warp][2 * lane] = mx0;
-      sm.red[i & 1][warp][2 * lane + 1] = mx1;
-    }
-    __syncthreads();  // stage s is free; block maxima visible
-    if (tid < kKvHeads && cb < mb) {
-      const float v = fmaxf(fmaxf(sm.red[i & 1][0][tid], sm.red[i & 1][1][tid]),
-                            fmaxf(sm.red[i & 1][2][tid], sm.red[i & 1][3][tid]));
-      scores[(static_cast<long long>(cr) * kKvHeads + tid) * mb + cb] = v;
+      float* sp = scores + (static_cast<long long>(cur_r) * kKvHeads + 2 * lane) * mb + meta.b;
+      sp[0] = mx0;
+      sp[mb] = mx1;
       __threadfence();
     }
-    const bool seg_end = (cb == cnb - 1) || (i == n_items - 1);
-    if (seg_end) {
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const int cnt = cb - seg_start + 1;
-        const int old = atomicAdd(&tickets[cr], cnt);
-        sm.bcast[2] = (old + cnt == cnb) ? 1 : 0;
-      }
-      __syncthreads();
-      if (sm.bcast[2]) {
-        __threadfence();
-        const float* srow = scores + (static_cast<long long>(cr) * kKvHeads + warp) * mb;
-        topk_row(srow, cnb, topk, init, local, q2k + (static_cast<long long>(warp) * B + cr) * topk,
-                 sm.cand[warp]);
-        if (tid == 0) tickets[cr] = 0;
-      }
-      // advance the consumer cursor to the next scored request
-      if (i + 1 < n_items) {
-        cb = 0;
-        do {
-          ++cr;
-          cnb = scored_blocks(geo, cr, topk, nullptr);
-        } while (cnb == 0);
-        seg_start = 0;
-        load_q(cr);
-      }
-    } else {
-      ++cb;
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      const int old = atomicAdd(&tickets[cur_r], 1);
+      last = (old + 1 == cur_nb) ? 1 : 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      for (int h = 0; h < kKvHeads; ++h)
+        topk_row(scores + (static_cast<long long>(cur_r) * kKvHeads + h) * mb, cur_nb, topk, init, local,
+                 q2k + (static_cast<long long>(h) * B + cur_r) * topk, sm.cand[warp]);
+      if (lane == 0) tickets[cur_r] = 0;
     }
   }
 }
@@ -387,20 +407,21 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
                                  int* tickets, DevError* err, cudaStream_t stream) {
   DecodeGeom geo{seq_lens, page_table, cu_k, batch, max_blocks, num_slots};
-  const size_t smem = sizeof(SelSmem) + 1024;
-  // enough CTAs to keep every SM streaming (two per SM); bounded by the block count
+  // one CTA per SM; never more CTAs than pages
   const long long blocks_upper = static_cast<long long>(batch) * max_blocks;
-  int grid = static_cast<int>(blocks_upper < 2LL * kNumSMs ? blocks_upper : 2LL * kNumSMs);
+  int grid = static_cast<int>(blocks_upper < kNumSMs ? blocks_upper : kNumSMs);
   if (grid < 1) grid = 1;
   const auto* iq = static_cast<const uint8_t*>(index_q);
   const auto* ik = static_cast<const uint8_t*>(index_k);
   if (cfg.index_dtype == MSA_INDEX_E4M3) {
     auto k = decode_select_kernel<1>;
+    const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, tickets, q2k, cfg.topk, cfg.init_blocks,
                                            cfg.local_blocks, err);
   } else {
     auto k = decode_select_kernel<0>;
+    const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim * 2)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, tickets, q2k, cfg.topk, cfg.init_blocks,
                                            cfg.local_blocks, err);

@@ -10,16 +10,20 @@
 //
 // GB300 design.  The 16 query heads that share a KV head form exactly one
 // 16-row MMA tile, so one (query, KV head, selected block) triple is the unit
-// of work.  All units are split evenly over a persistent grid (stream-K): a
-// producer warp walks the CTA's units and gathers each selected block's K and V
-// in 64-key chunks with tiled TMA copies (3-D tensor map over
-// [rows, 4 heads, 128], 128-byte swizzle) into a 4-deep shared-memory ring;
-// four consumer warps each take 16 keys of a chunk, run S = Q K^T and O += P V
-// on the tensor cores (mma.sync bf16, fp32 accumulate) with an online softmax,
-// and merge their states in shared memory when the (query, KV head) segment
-// ends.  A segment cut by a CTA boundary is written as an fp32 partial
-// (max, sum, unnormalised output); the CTA that completes the segment's last
-// unit (atomic ticket, no waiting) merges the partials and writes bf16.
+// of work.  All units are split evenly over a persistent grid of one CTA per
+// SM (stream-K).  A producer warp walks the CTA's units; per (query, KV head)
+// segment its lanes resolve the selected blocks in parallel (q2k entry, then
+// page id) and lane 0 gathers each block's K and V in 64-key chunks with tiled
+// TMA copies (3-D tensor map over [rows, 4 heads, 128], 128-byte swizzle) into
+// a 4-deep shared-memory ring.  Four consumer warps each own one stage and
+// take whole chunks round-robin, so four chunks are in flight on the tensor
+// cores at once: S = Q K^T (ldmatrix B fragments), online softmax in base 2, O += P V
+// (ldmatrix.trans V fragments; P fed as bf16 hi + lo terms), mma.sync bf16 with
+// fp32 accumulation.  At the end of a segment the warps' (max, sum, O) states
+// are merged in two halving rounds through shared memory.  A segment cut by
+// a CTA boundary is written as an fp32 partial (max, sum, unnormalised O); the
+// CTA whose atomic ticket completes the segment (no waiting) merges the
+// partials and writes bf16.
 #include "launch.h"
 
 namespace msa {
@@ -29,8 +33,12 @@ constexpr int kChunkKeys = 64;
 constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 dims)
 constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
 constexpr int kConsumerWarps = 4;
-constexpr int kAttThreads = (kConsumerWarps + 1) * 32;
-constexpr int kCombStride = kDim + 8;              // padded fp32 row in the merge buffer
+// stage s is always consumed by warp s % kConsumerWarps, so a warp never waits
+// on a stage more than one mbarrier phase ahead
+static_assert(kAttStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kAttThreads = kConsumerThreads + 32;
+constexpr int kCombStride = kDim + 8;               // padded fp32 row of the merge buffer
 constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
 
 struct QueryGeo {
@@ -77,9 +85,9 @@ __device__ __forceinline__ int block_keys(const QueryGeo& q, int b) {
 
 struct AttSmem {
   alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
-  float comb[kConsumerWarps][kGroup][kCombStride];
-  float comb_m[kConsumerWarps][kGroup];
-  float comb_l[kConsumerWarps][kGroup];
+  float comb[kConsumerWarps / 2][kGroup][kCombStride];
+  float comb_m[kConsumerWarps / 2][kGroup];
+  float comb_l[kConsumerWarps / 2][kGroup];
   uint64_t full[kAttStages];
   uint64_t empty[kAttStages];
   int bcast;
@@ -93,6 +101,47 @@ __device__ __forceinline__ long long cta_of(long long i, long long N, long long 
   while (c + 1 < G && seg_begin(c + 1, N, G) <= i) ++c;
   while (c > 0 && seg_begin(c, N, G) > i) --c;
   return c;
+}
+
+// Online-softmax state of one warp: rows g8 (m0, l0, o[.][0..1]) and g8+8 (m1, l1, o[.][2..3]).
+struct WarpState {
+  float m0, m1, l0, l1;
+  float o[16][4];
+};
+
+__device__ __forceinline__ void state_to_smem(const WarpState& st, AttSmem& sm, int slot, int g8, int t4) {
+  if (t4 == 0) {
+    sm.comb_m[slot][g8] = st.m0;
+    sm.comb_m[slot][g8 + 8] = st.m1;
+    sm.comb_l[slot][g8] = st.l0;
+    sm.comb_l[slot][g8 + 8] = st.l1;
+  }
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) {
+    *reinterpret_cast<float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]) = make_float2(st.o[nd][0], st.o[nd][1]);
+    *reinterpret_cast<float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]) = make_float2(st.o[nd][2], st.o[nd][3]);
+  }
+}
+
+__device__ __forceinline__ void merge_from_smem(WarpState& st, const AttSmem& sm, int slot, int g8, int t4) {
+  const float mb0 = sm.comb_m[slot][g8], mb1 = sm.comb_m[slot][g8 + 8];
+  const float M0 = fmaxf(st.m0, mb0), M1 = fmaxf(st.m1, mb1);
+  const float u0 = M0 == -INFINITY ? 0.f : M0, u1 = M1 == -INFINITY ? 0.f : M1;
+  const float fa0 = exp2f(st.m0 - u0), fb0 = exp2f(mb0 - u0);
+  const float fa1 = exp2f(st.m1 - u1), fb1 = exp2f(mb1 - u1);
+  st.l0 = st.l0 * fa0 + sm.comb_l[slot][g8] * fb0;
+  st.l1 = st.l1 * fa1 + sm.comb_l[slot][g8 + 8] * fb1;
+  st.m0 = M0;
+  st.m1 = M1;
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) {
+    const float2 x = *reinterpret_cast<const float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]);
+    const float2 y = *reinterpret_cast<const float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]);
+    st.o[nd][0] = st.o[nd][0] * fa0 + x.x * fb0;
+    st.o[nd][1] = st.o[nd][1] * fa0 + x.y * fb0;
+    st.o[nd][2] = st.o[nd][2] * fa1 + y.x * fb1;
+    st.o[nd][3] = st.o[nd][3] * fa1 + y.y * fb1;
+  }
 }
 
 __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
@@ -110,7 +159,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kConsumerWarps);
+      mbar_init(&sm.empty[s], 1);
     }
     fence_mbar_init();
   }
@@ -119,25 +168,37 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
+    // per (query, KV head) segment the lanes resolve up to 16 selected blocks
+    // at once (q2k entry, then page id), and lane 0 issues their chunks
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
-      long long sc = 0;
-      long long it = lo;
-      while (it < hi) {
-        const int qi = static_cast<int>(it / (kKvHeads * topk));
-        const int g = static_cast<int>((it / topk) % kKvHeads);
-        const long long seg_end = min(hi, (static_cast<long long>(qi) * kKvHeads + g + 1) * topk);
-        const QueryGeo qg = query_geo(geo, qi);
-        for (; it < seg_end; ++it) {
-          const int j = static_cast<int>(it % topk);
-          const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j];
-          const int nk = block_keys(qg, b);
-          if (nk == 0) continue;
-          const long long r0 = block_row0(geo, qi, qg, b);
-          if (r0 < 0) continue;
-          const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
-          for (int ch = 0; ch < nch; ++ch, ++sc) {
+    }
+    long long sc = 0;
+    long long it = lo;
+    while (it < hi) {
+      const int qi = static_cast<int>(it / (kKvHeads * topk));
+      const int g = static_cast<int>((it / topk) % kKvHeads);
+      const long long seg_end = min(hi, (static_cast<long long>(qi) * kKvHeads + g + 1) * topk);
+      const QueryGeo qg = query_geo(geo, qi);
+      const int j0 = static_cast<int>(it % topk), jn = static_cast<int>(seg_end - it);
+      int nk_l = 0;
+      long long r0_l = 0;
+      if (lane < jn) {
+        const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j0 + lane];
+        nk_l = block_keys(qg, b);
+        if (nk_l) {
+          r0_l = block_row0(geo, qi, qg, b);
+          if (r0_l < 0) nk_l = 0;
+        }
+      }
+      for (int k = 0; k < jn; ++k) {
+        const int nk = __shfl_sync(0xffffffffu, nk_l, k);
+        const long long r0 = __shfl_sync(0xffffffffu, r0_l, k);
+        if (nk == 0) continue;
+        const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
+        for (int ch = 0; ch < nch; ++ch, ++sc) {
+          if (lane == 0) {
             const int s = static_cast<int>(sc % kAttStages);
             mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kAttStages) & 1) ^ 1), err, 200);
             mbar_expect_tx(&sm.full[s], kAttStageBytes);
@@ -148,15 +209,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             tma_load_3d(st + 2 * kBoxBytes, &vmap, 0, g, row, &sm.full[s]);
             tma_load_3d(st + 3 * kBoxBytes, &vmap, 64, g, row, &sm.full[s]);
           }
+          __syncwarp();
         }
       }
+      it = seg_end;
     }
     return;
   }
 
-  // ---------------- consumer warps ----------------
+  // ---------------- consumer warps: whole 64-key chunks, round-robin ----------------
   const int g8 = lane >> 2, t4 = lane & 3;
-  long long sc = 0;
+  long long sc = 0;  // chunk counter, identical in every consumer warp and the producer
   long long it = lo;
   while (it < hi) {
     const int qi = static_cast<int>(it / (kKvHeads * topk));
@@ -165,6 +228,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const long long range0 = (static_cast<long long>(qi) * kKvHeads + g) * topk;
     const long long seg_end = min(hi, range0 + topk);
     const QueryGeo qg = query_geo(geo, qi);
+    const int j0 = static_cast<int>(it % topk), jn = static_cast<int>(seg_end - it);
+    int nk_l = 0;
+    if (lane < jn) {
+      const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j0 + lane];
+      if (b >= qg.nb && warp == 0) record_error(err, MSA_DEVERR_BLOCK, it + lane);
+      nk_l = block_keys(qg, b);
+      if (nk_l && block_row0(geo, qi, qg, b) < 0) {
+        nk_l = 0;
+        if (warp == 0) record_error(err, MSA_DEVERR_PAGE, it + lane);
+      }
+    }
 
     // Q fragments of the 16 heads of KV head g (A operand, 8 k-steps)
     uint32_t qa[8][4];
@@ -179,158 +253,138 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         qa[kk][3] = *reinterpret_cast<const uint32_t*>(qp + (g8 + 8) * kDim + c + 8);
       }
     }
-    float o[16][4];
+    WarpState st;
+    st.m0 = st.m1 = -INFINITY;
+    st.l0 = st.l1 = 0.f;
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int nd = 0; nd < 16; ++nd) st.o[nd][0] = st.o[nd][1] = st.o[nd][2] = st.o[nd][3] = 0.f;
 
-    for (; it < seg_end; ++it) {
-      const int j = static_cast<int>(it % topk);
-      const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j];
-      if (b >= qg.nb && lane == 0 && warp == 0) record_error(err, MSA_DEVERR_BLOCK, it);
-      const int nk = block_keys(qg, b);
+    for (int k = 0; k < jn; ++k) {
+      const int nk = __shfl_sync(0xffffffffu, nk_l, k);
       if (nk == 0) continue;
-      if (block_row0(geo, qi, qg, b) < 0) {
-        if (lane == 0 && warp == 0) record_error(err, MSA_DEVERR_PAGE, it);
-        continue;
-      }
       const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
       for (int ch = 0; ch < nch; ++ch, ++sc) {
+        if (static_cast<int>(sc % kConsumerWarps) != warp) continue;
         const int s = static_cast<int>(sc % kAttStages);
         const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
         mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kAttStages) & 1), err, 300);
-        const int key0 = 16 * warp;
-        if (key0 < valid) {
-          const uint32_t st = smem_u32(sm.stage[s]);
-          // ---- S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys) ----
-          float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          {
-            const int mi = lane >> 3;
-            const int krow = key0 + 8 * (mi >> 1) + (lane & 7);
+        const uint32_t stg = smem_u32(sm.stage[s]);
+        const int mi = lane >> 3;
+        // ---- S = Q K^T over the chunk's keys (n-tiles of 8 keys, in pairs) ----
+        float sacc[8][4];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
-              const uint32_t addr = st + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7);
-              uint32_t kb[4];
-              ldsm_x4(kb, addr);
-              mma_bf16(sacc[0], qa[kk], kb[0], kb[1]);
-              mma_bf16(sacc[1], qa[kk], kb[2], kb[3]);
-            }
+        for (int p = 0; p < 8; ++p) sacc[p][0] = sacc[p][1] = sacc[p][2] = sacc[p][3] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          if (16 * kp >= valid) break;
+          const int krow = 16 * kp + 8 * (mi >> 1) + (lane & 7);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
+            uint32_t kb[4];
+            ldsm_x4(kb, stg + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7));
+            mma_bf16(sacc[2 * kp], qa[kk], kb[0], kb[1]);
+            mma_bf16(sacc[2 * kp + 1], qa[kk], kb[2], kb[3]);
           }
-          // ---- mask, online softmax (base 2, scale folded in) ----
-          float mx0 = -INFINITY, mx1 = -INFINITY;
+        }
+        // ---- mask, online softmax (base 2, scale folded in) ----
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-          for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < 8; ++p) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int kidx = key0 + 8 * p + 2 * t4 + e;
-              const bool ok = kidx < valid;
-              sacc[p][e] = ok ? sacc[p][e] * scale_log2 : -INFINITY;
-              sacc[p][2 + e] = ok ? sacc[p][2 + e] * scale_log2 : -INFINITY;
-              mx0 = fmaxf(mx0, sacc[p][e]);
-              mx1 = fmaxf(mx1, sacc[p][2 + e]);
-            }
+          for (int e = 0; e < 2; ++e) {
+            const bool ok = 8 * p + 2 * t4 + e < valid;
+            sacc[p][e] = ok ? sacc[p][e] * scale_log2 : -INFINITY;
+            sacc[p][2 + e] = ok ? sacc[p][2 + e] * scale_log2 : -INFINITY;
+            mx0 = fmaxf(mx0, sacc[p][e]);
+            mx1 = fmaxf(mx1, sacc[p][2 + e]);
           }
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-          const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-          m0 = mn0;
-          m1 = mn1;
-          float ps[2][4];
-          float rs0 = 0.f, rs1 = 0.f;
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2f(st.m0 - mu0), al1 = exp2f(st.m1 - mu1);
+        st.m0 = mn0;
+        st.m1 = mn1;
+        float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-          for (int p = 0; p < 2; ++p) {
-            ps[p][0] = exp2f(sacc[p][0] - mu0);
-            ps[p][1] = exp2f(sacc[p][1] - mu0);
-            ps[p][2] = exp2f(sacc[p][2] - mu1);
-            ps[p][3] = exp2f(sacc[p][3] - mu1);
-            rs0 += ps[p][0] + ps[p][1];
-            rs1 += ps[p][2] + ps[p][3];
-          }
-          l0 = l0 * al0 + rs0;
-          l1 = l1 * al1 + rs1;
+        for (int p = 0; p < 8; ++p) {
+          sacc[p][0] = exp2f(sacc[p][0] - mu0);
+          sacc[p][1] = exp2f(sacc[p][1] - mu0);
+          sacc[p][2] = exp2f(sacc[p][2] - mu1);
+          sacc[p][3] = exp2f(sacc[p][3] - mu1);
+          rs0 += sacc[p][0] + sacc[p][1];
+          rs1 += sacc[p][2] + sacc[p][3];
+        }
+        st.l0 = st.l0 * al0 + rs0;
+        st.l1 = st.l1 * al1 + rs1;
 #pragma unroll
-          for (int nd = 0; nd < 16; ++nd) {
-            o[nd][0] *= al0;
-            o[nd][1] *= al0;
-            o[nd][2] *= al1;
-            o[nd][3] *= al1;
-          }
-          // P = P_hi + P_lo in two bf16 terms (relative error ~2^-17), so the
-          // bf16 rounding of the probabilities does not reach the output
+        for (int nd = 0; nd < 16; ++nd) {
+          st.o[nd][0] *= al0;
+          st.o[nd][1] *= al0;
+          st.o[nd][2] *= al1;
+          st.o[nd][3] *= al1;
+        }
+        // ---- O += P V, one k-step per 16 keys; P = P_hi + P_lo in two bf16 terms
+        // (relative error ~2^-17) so the bf16 rounding of probabilities does not
+        // reach the output ----
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          if (16 * kp >= valid) break;
           uint32_t pa[4], pl[4];
-          split_bf16(ps[0][0], ps[0][1], pa[0], pl[0]);
-          split_bf16(ps[0][2], ps[0][3], pa[1], pl[1]);
-          split_bf16(ps[1][0], ps[1][1], pa[2], pl[2]);
-          split_bf16(ps[1][2], ps[1][3], pa[3], pl[3]);
-          // ---- O += P V (k = this warp's 16 keys, 16 n-tiles of 8 dims) ----
-          {
-            const int mi = lane >> 3;
-            const int vrow = key0 + 8 * (mi & 1) + (lane & 7);
+          split_bf16(sacc[2 * kp][0], sacc[2 * kp][1], pa[0], pl[0]);
+          split_bf16(sacc[2 * kp][2], sacc[2 * kp][3], pa[1], pl[1]);
+          split_bf16(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1], pa[2], pl[2]);
+          split_bf16(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3], pa[3], pl[3]);
+          const int vrow = 16 * kp + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
-            for (int nd = 0; nd < 16; nd += 2) {
-              const int chunk = nd + (mi >> 1);
-              const uint32_t addr = st + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7);
-              uint32_t vb[4];
-              ldsm_x4_t(vb, addr);
-              mma_bf16(o[nd], pa, vb[0], vb[1]);
-              mma_bf16(o[nd + 1], pa, vb[2], vb[3]);
-              mma_bf16(o[nd], pl, vb[0], vb[1]);
-              mma_bf16(o[nd + 1], pl, vb[2], vb[3]);
-            }
+          for (int nd = 0; nd < 16; nd += 2) {
+            const int chunk = nd + (mi >> 1);
+            uint32_t vb[4];
+            ldsm_x4_t(vb, stg + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7));
+            mma_bf16(st.o[nd], pa, vb[0], vb[1]);
+            mma_bf16(st.o[nd + 1], pa, vb[2], vb[3]);
+            mma_bf16(st.o[nd], pl, vb[0], vb[1]);
+            mma_bf16(st.o[nd + 1], pl, vb[2], vb[3]);
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);
       }
     }
+    it = seg_end;
 
-    // ---- merge the four warps' states ----
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (t4 == 0) {
-      sm.comb_m[warp][g8] = m0;
-      sm.comb_m[warp][g8 + 8] = m1;
-      sm.comb_l[warp][g8] = l0;
-      sm.comb_l[warp][g8 + 8] = l1;
-    }
+    // ---- merge the four warps' states: 4 -> 2 -> 1 ----
+    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
+    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
+    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
+    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      *reinterpret_cast<float2*>(&sm.comb[warp][g8][8 * nd + 2 * t4]) = make_float2(o[nd][0], o[nd][1]);
-      *reinterpret_cast<float2*>(&sm.comb[warp][g8 + 8][8 * nd + 2 * t4]) = make_float2(o[nd][2], o[nd][3]);
+    for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
+      consumer_sync();
+      if (warp >= half && warp < 2 * half) state_to_smem(st, sm, warp - half, g8, t4);
+      consumer_sync();
+      if (warp < half) merge_from_smem(st, sm, warp, g8, t4);
     }
     consumer_sync();
+    if (warp == 0) state_to_smem(st, sm, 0, g8, t4);
+    consumer_sync();
+    // ---- write: 16 rows x 128 dims, 16 dims per consumer thread ----
     const int row = tid >> 3, d0 = (tid & 7) * 16;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.comb_m[w][row]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float Lsum = 0.f, acc[16];
-#pragma unroll
-    for (int d = 0; d < 16; ++d) acc[d] = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = exp2f(sm.comb_m[w][row] - Mu);
-      Lsum += sm.comb_l[w][row] * f;
-#pragma unroll
-      for (int d = 0; d < 16; ++d) acc[d] += sm.comb[w][row][d0 + d] * f;
-    }
+    const float M = sm.comb_m[0][row], Lsum = sm.comb_l[0][row];
     const bool complete = (seg_lo == range0) && (seg_end == range0 + topk);
     __nv_bfloat16* orow = out + (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+    const float* src = &sm.comb[0][row][d0];
     if (complete) {
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
       uint32_t w8[8];
 #pragma unroll
-      for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(acc[2 * d] * inv, acc[2 * d + 1] * inv);
+      for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(src[2 * d] * inv, src[2 * d + 1] * inv);
       reinterpret_cast<uint4*>(orow)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
       reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
-      consumer_sync();
     } else {
       // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
       const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
@@ -342,7 +396,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
 #pragma unroll
       for (int d = 0; d < 16; d += 4)
         *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + d) =
-            make_float4(acc[d], acc[d + 1], acc[d + 2], acc[d + 3]);
+            make_float4(src[d], src[d + 1], src[d + 2], src[d + 3]);
       __threadfence();
       consumer_sync();
       if (tid == 0) {
@@ -379,7 +433,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
         if (tid == 0) tickets[qi * kKvHeads + g] = 0;
       }
-      consumer_sync();
     }
   }
 }
