@@ -397,7 +397,7 @@ def main():
             "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config, "roofline": roof,
             "e2e": {"value": round(e2e, 1), "unit": unit, "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": (2 if res["decode"] else 3) * args.steps, "clocks": res["clocks"]}
+            "gpu_launches": 3 * args.steps, "clocks": res["clocks"]}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
     print(json.dumps(line))

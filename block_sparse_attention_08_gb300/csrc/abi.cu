@@ -161,8 +161,6 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (clear_counters(ws, L.sel_tickets, static_cast<size_t>(batch) * sizeof(int), s) != cudaSuccess)
-    return MSA_ERR_CUDA;
   cudaError_t e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch,
                                        max_blocks, num_slots, q2k, reinterpret_cast<float*>(ws + L.scores),
                                        reinterpret_cast<int*>(ws + L.sel_tickets), reinterpret_cast<DevError*>(ws), s);

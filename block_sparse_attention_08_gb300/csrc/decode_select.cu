@@ -15,14 +15,15 @@
 // bytes.  Inside a CTA a producer warp resolves 32 page ids at a time with
 // one coalesced load and issues one 1-D bulk TMA copy per page into a ring of
 // 192 KB of shared memory (6 bf16 / 12 E4M3 pages in flight); six consumer
-// warps each take whole pages round-robin (stage s always to warp s % 6) and score all 128 keys on the
-// tensor cores (mma.sync: keys as A read straight from the page, the 4 index
-// heads as B, fp32 accumulate), reduce the block max in registers and store
-// one fp32 score per (request, head, page).  No CTA-wide barrier sits in the
-// loop.  Each finished page bumps an atomic per-request counter; the warp that
-// completes a request (no waiting) runs its top-k: per head, the need-th
-// largest of the 32 lane maxima is a threshold that filters the candidates,
-// then an exact (score desc, id asc) pick.
+// warps each take whole pages round-robin (stage s always to warp s % 6) and
+// score all 128 keys on the tensor cores (mma.sync: keys as A read straight
+// from the page, the 4 index heads as B, fp32 accumulate), reduce the block
+// max in registers and store one fp32 score per (request, head, page).  No
+// CTA-wide barrier sits in the loop.  A second kernel, launched as a
+// programmatic dependent so its launch overlaps the scorer's tail, runs the
+// top-k with one warp per (request, head): the need-th largest of the 32 lane
+// maxima is a threshold that filters the candidates, then an exact
+// (score desc, id asc) pick.
 #include "launch.h"
 
 namespace msa {
@@ -77,7 +78,14 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 }
 
 // Exact top-`need` by (score desc, id asc) over the non-forced blocks of one
-// (request, head) row, then the ascending q2k row.  One warp.
+// (request, head) row, then the ascending q2k row.  One warp.  Rows of up to
+// 32 x 32 candidates are read once into registers with independent loads.
+constexpr int kTopkRegs = 32;
+
+__device__ __forceinline__ unsigned long long score_key(float v, int b) {
+  return (static_cast<unsigned long long>(float_key(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(b));
+}
+
 __device__ void topk_row(const float* s, int nb, int topk, int init, int local, int32_t* out,
                          unsigned long long* cand) {
   const int lane = threadIdx.x & 31;
@@ -86,38 +94,61 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
     return;
   }
   const int need = topk - init - local;
-  // key = (orderable score << 32) | (~id): larger key = better (score desc, id asc)
-  auto key_of = [&](int b) -> unsigned long long {
-    return (static_cast<unsigned long long>(float_key(__ldcg(s + b))) << 32) |
-           (0xffffffffu - static_cast<uint32_t>(b));
-  };
+  const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi)
   int picked = -1;
   if (need > 0) {
+    const bool in_regs = c_hi - c_lo <= 32 * kTopkRegs;
+    float v[kTopkRegs];
     unsigned long long best = 0;
-    for (int b = init + lane; b < nb - local; b += 32) {
-      const unsigned long long k = key_of(b);
-      best = k > best ? k : best;
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < kTopkRegs; ++k) {
+        const int b = c_lo + lane + 32 * k;
+        v[k] = b < c_hi ? __ldcg(s + b) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < kTopkRegs; ++k) {
+        const int b = c_lo + lane + 32 * k;
+        const unsigned long long key = b < c_hi ? score_key(v[k], b) : 0ull;
+        best = key > best ? key : best;
+      }
+    } else {
+      for (int b = c_lo + lane; b < c_hi; b += 32) {
+        const unsigned long long key = score_key(__ldcg(s + b), b);
+        best = key > best ? key : best;
+      }
     }
     // need-th largest lane maximum (bitonic sort of 32 keys, ascending): at
     // least `need` candidates are >= theta, so the top `need` all are
-    unsigned long long v = best;
+    unsigned long long t = best;
     for (int k = 2; k <= 32; k <<= 1)
       for (int j = k >> 1; j > 0; j >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, t, j);
         const bool lower = (lane & j) == 0, asc = (lane & k) == 0;
-        v = (lower == asc) ? (v < o ? v : o) : (v > o ? v : o);
+        t = (lower == asc) ? (t < o ? t : o) : (t > o ? t : o);
       }
-    const unsigned long long theta = __shfl_sync(0xffffffffu, v, 32 - need);
+    const unsigned long long theta = __shfl_sync(0xffffffffu, t, 32 - need);
     int count = 0;
-    for (int b0 = init; b0 < nb - local; b0 += 32) {
-      const int b = b0 + lane;
-      const bool c = b < nb - local && key_of(b) >= theta;
+    auto consider = [&](unsigned long long key) {
+      const bool c = key >= theta && key != 0ull;
       const unsigned m = __ballot_sync(0xffffffffu, c);
       if (c) {
         const int slot = count + __popc(m & ((1u << lane) - 1));
-        if (slot < kCandCap) cand[slot] = key_of(b);
+        if (slot < kCandCap) cand[slot] = key;
       }
       count += __popc(m);
+    };
+    if (in_regs) {
+#pragma unroll
+      for (int k = 0; k < kTopkRegs; ++k) {
+        const int b = c_lo + lane + 32 * k;
+        consider(b < c_hi ? score_key(v[k], b) : 0ull);
+      }
+    } else {
+      for (int b0 = c_lo; b0 < c_hi; b0 += 32) {
+        const int b = b0 + lane;
+        consider(b < c_hi ? score_key(__ldcg(s + b), b) : 0ull);
+      }
     }
     __syncwarp();
     if (count <= kCandCap) {
@@ -134,13 +165,13 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
         if (lane == i) picked = static_cast<int>(0xffffffffu - static_cast<uint32_t>(m));
       }
     } else {
-      // rare: too many candidates above the threshold -- exact rounds
+      // rare: too many candidates at or above the threshold -- exact rounds
       unsigned long long prev = ~0ull;
       for (int i = 0; i < need; ++i) {
         unsigned long long m = 0;
-        for (int b = init + lane; b < nb - local; b += 32) {
-          const unsigned long long k = key_of(b);
-          if (k < prev && k > m) m = k;
+        for (int b = c_lo + lane; b < c_hi; b += 32) {
+          const unsigned long long key = score_key(__ldcg(s + b), b);
+          if (key < prev && key > m) m = key;
         }
         for (int o = 16; o > 0; o >>= 1) {
           const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
@@ -196,13 +227,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     if (r < B) {
       int nb;
       v = scored_blocks(geo, r, topk, &nb);
-      if (r % gridDim.x == blockIdx.x) {
-        const int L = geo.seq_lens[r];
-        if (L < 1 || L > mb * kBlock) record_error(err, MSA_DEVERR_LENGTH, r);
-        if (v == 0)
-          for (int h = 0; h < kKvHeads; ++h)
-            for (int i = 0; i < topk; ++i) q2k[(static_cast<long long>(h) * B + r) * topk + i] = i < nb ? i : -1;
-      }
     }
     total += block_sum(v, sm.scan);
   }
@@ -299,8 +323,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
   }
 
   // ---------------- consumer warps: whole pages, round-robin ----------------
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int g8 = lane >> 2, t4 = lane & 3;
-  int cur_r = -1, cur_nb = 0;
+  int cur_r = -1;
   uint32_t qf[4][4];
   for (int i = warp; i < n_items; i += kSelConsumers) {
     const int s = i % kStages;
@@ -314,7 +339,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     }
     if (meta.r != cur_r) {
       cur_r = meta.r;
-      cur_nb = scored_blocks(geo, cur_r, topk, nullptr);
       constexpr int kQChunks = kE4M3 ? 2 : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) qf[j][0] = qf[j][1] = qf[j][2] = qf[j][3] = 0u;
@@ -334,43 +358,52 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     const int rows = meta.rows;
     const uint32_t base = smem_u32(sm.ring + s * kPageBytes);
     float mx0 = -INFINITY, mx1 = -INFINITY;  // heads 2*t4, 2*t4+1
-#pragma unroll 2
-    for (int m = 0; m < kBlock / 16; ++m) {
-      const int key0 = 16 * m;
+    // two m-tiles (32 keys) per step: all shared loads first, then two
+    // independent MMA chains.  Each thread reads 16 contiguous bytes of a key
+    // row; the MMA k slots take them in a fixed permutation that B (index_q)
+    // repeats, so nothing is moved.
+    constexpr int kJ = kE4M3 ? 2 : 4;
+    for (int mp = 0; mp < kBlock / 32; ++mp) {
+      const int key0 = 32 * mp;
       if (key0 >= rows) break;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t ra_addr = base + (key0 + g8) * kRowBytes;
-      const uint32_t rb_addr = ra_addr + 8 * kRowBytes;
-      // each thread reads 16 contiguous bytes of a key row; the MMA k slots take
-      // them in a fixed permutation that B (index_q) repeats, so none is moved
-      if (!kE4M3) {
+      uint4 ra[2][kJ], rb[2][kJ];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 ra = lds128(ra_addr + (32 * j + 8 * t4) * 2);
-          const uint4 rb = lds128(rb_addr + (32 * j + 8 * t4) * 2);
-          const uint32_t a0[4] = {ra.x, rb.x, ra.y, rb.y};
-          const uint32_t a1[4] = {ra.z, rb.z, ra.w, rb.w};
-          mma_bf16(c, a0, qf[j][0], qf[j][1]);
-          mma_bf16(c, a1, qf[j][2], qf[j][3]);
-        }
-      } else {
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t a_addr = base + (key0 + 16 * h2 + g8) * kRowBytes;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint4 ra = lds128(ra_addr + 64 * j + 16 * t4);
-          const uint4 rb = lds128(rb_addr + 64 * j + 16 * t4);
-          const uint32_t a0[4] = {ra.x, rb.x, ra.y, rb.y};
-          const uint32_t a1[4] = {ra.z, rb.z, ra.w, rb.w};
-          mma_e4m3(c, a0, qf[j][0], qf[j][1]);
-          mma_e4m3(c, a1, qf[j][2], qf[j][3]);
+        for (int j = 0; j < kJ; ++j) {
+          const uint32_t off = kE4M3 ? (64 * j + 16 * t4) : (32 * j + 8 * t4) * 2;
+          ra[h2][j] = lds128(a_addr + off);
+          rb[h2][j] = lds128(a_addr + 8 * kRowBytes + off);
         }
       }
-      if (key0 + g8 < rows) {
-        mx0 = fmaxf(mx0, c[0]);
-        mx1 = fmaxf(mx1, c[1]);
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t a0[4] = {ra[h2][j].x, rb[h2][j].x, ra[h2][j].y, rb[h2][j].y};
+          const uint32_t a1[4] = {ra[h2][j].z, rb[h2][j].z, ra[h2][j].w, rb[h2][j].w};
+          if (!kE4M3) {
+            mma_bf16(c[h2], a0, qf[j][0], qf[j][1]);
+            mma_bf16(c[h2], a1, qf[j][2], qf[j][3]);
+          } else {
+            mma_e4m3(c[h2], a0, qf[j][0], qf[j][1]);
+            mma_e4m3(c[h2], a1, qf[j][2], qf[j][3]);
+          }
+        }
       }
-      if (key0 + g8 + 8 < rows) {
-        mx0 = fmaxf(mx0, c[2]);
-        mx1 = fmaxf(mx1, c[3]);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int k0 = key0 + 16 * h2 + g8;
+        if (k0 < rows) {
+          mx0 = fmaxf(mx0, c[h2][0]);
+          mx1 = fmaxf(mx1, c[h2][1]);
+        }
+        if (k0 + 8 < rows) {
+          mx0 = fmaxf(mx0, c[h2][2]);
+          mx1 = fmaxf(mx1, c[h2][3]);
+        }
       }
     }
     __syncwarp();
@@ -383,23 +416,25 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
       float* sp = scores + (static_cast<long long>(cur_r) * kKvHeads + 2 * lane) * mb + meta.b;
       sp[0] = mx0;
       sp[mb] = mx1;
-      __threadfence();
-    }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      const int old = atomicAdd(&tickets[cur_r], 1);
-      last = (old + 1 == cur_nb) ? 1 : 0;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      for (int h = 0; h < kKvHeads; ++h)
-        topk_row(scores + (static_cast<long long>(cur_r) * kKvHeads + h) * mb, cur_nb, topk, init, local,
-                 q2k + (static_cast<long long>(h) * B + cur_r) * topk, sm.cand[warp]);
-      if (lane == 0) tickets[cur_r] = 0;
     }
   }
+}
+
+// Top-k per (request, head): one warp each, four per CTA (one request).
+// Launched right behind the scorer as a programmatic dependent: its CTAs may
+// start while the scorer drains, and wait for the scores to be complete.
+__global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
+                                                          int32_t* __restrict__ q2k, int topk, int init, int local,
+                                                          DevError* err) {
+  __shared__ unsigned long long cand[kKvHeads][kCandCap];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int r = blockIdx.x, h = threadIdx.x >> 5;
+  const int L = geo.seq_lens[r];
+  if (threadIdx.x == 0 && (L < 1 || L > geo.max_blocks * kBlock)) record_error(err, MSA_DEVERR_LENGTH, r);
+  int nb;
+  scored_blocks(geo, r, topk, &nb);
+  topk_row(scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks, nb, topk, init, local,
+           q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h]);
 }
 
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
@@ -426,7 +461,20 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
     k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, tickets, q2k, cfg.topk, cfg.init_blocks,
                                            cfg.local_blocks, err);
   }
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(batch));
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const float* sc = scores;
+  return cudaLaunchKernelEx(&lc, decode_topk_kernel, sc, geo, q2k, cfg.topk, cfg.init_blocks, cfg.local_blocks, err);
 }
 
 }  // namespace msa
