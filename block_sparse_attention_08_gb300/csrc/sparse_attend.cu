@@ -10,36 +10,41 @@
 //
 // GB300 design.  The 16 query heads that share a KV head form exactly one
 // 16-row MMA tile, so one (query, KV head, selected block) triple is the unit
-// of work.  All units are split evenly over a persistent grid of one CTA per
-// SM (stream-K).  A producer warp walks the CTA's units; per (query, KV head)
-// segment its lanes resolve the selected blocks in parallel (q2k entry, then
-// page id) and lane 0 gathers each block's K and V in 64-key chunks with tiled
-// TMA copies (3-D tensor map over [rows, 4 heads, 128], 128-byte swizzle) into
-// a 4-deep shared-memory ring.  Four consumer warps each own one stage and
-// take whole chunks round-robin, so four chunks are in flight on the tensor
-// cores at once: S = Q K^T (ldmatrix B fragments), online softmax in base 2, O += P V
+// of work and a (query, KV head) pair is a segment of up to topk units.  All
+// units are split evenly over a persistent grid of one CTA per SM (stream-K).
+//
+// A producer warp walks the CTA's segments.  Per segment its lanes resolve the
+// selected blocks in parallel (q2k entry, then page id); it puts the segment's
+// key counts in a 2-slot segment ring together with the 16 x 128 Q tile (a
+// tiled TMA copy), then gathers each block's K and V in 64-key chunks with
+// tiled TMA copies (3-D tensor map over [rows, 4 heads, 128], 128-byte swizzle)
+// into a 6-stage chunk ring.  Three consumer warps each own two stages
+// (stage s always to warp s % 3), so every warp has one chunk landing while it
+// computes on the other, and none reads global memory on its critical path:
+// S = Q K^T (ldmatrix fragments), online softmax in base 2, O += P V
 // (ldmatrix.trans V fragments; P fed as bf16 hi + lo terms), mma.sync bf16 with
-// fp32 accumulation.  At the end of a segment the warps' (max, sum, O) states
-// are merged in two halving rounds through shared memory.  A segment cut by
-// a CTA boundary is written as an fp32 partial (max, sum, unnormalised O); the
-// CTA whose atomic ticket completes the segment (no waiting) merges the
-// partials and writes bf16.
+// fp32 accumulation.  At the end of a segment the three states are merged
+// through shared memory.  A segment cut by a CTA boundary is written as an fp32
+// partial (max, sum, unnormalised O); the CTA whose atomic ticket completes the
+// segment (no waiting) merges the partials and writes bf16.
 #include "launch.h"
 
 namespace msa {
 
-constexpr int kAttStages = 4;
+constexpr int kAttStages = 6;
 constexpr int kChunkKeys = 64;
 constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 dims)
 constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 3;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kAttThreads = kConsumerThreads + 32;
+constexpr int kSegSlots = 2;
+constexpr int kQBoxBytes = kGroup * 128;            // 16 rows x 128 bytes (64 dims)
+constexpr int kCombStride = kDim + 8;               // padded fp32 row of the merge buffer
+constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
 // stage s is always consumed by warp s % kConsumerWarps, so a warp never waits
 // on a stage more than one mbarrier phase ahead
 static_assert(kAttStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kAttThreads = kConsumerThreads + 32;
-constexpr int kCombStride = kDim + 8;               // padded fp32 row of the merge buffer
-constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
 
 struct QueryGeo {
   int pos;         // position of the query (keys 0..pos are causal)
@@ -83,17 +88,25 @@ __device__ __forceinline__ int block_keys(const QueryGeo& q, int b) {
   return min(kBlock, q.pos - b * kBlock + 1);
 }
 
+struct SegInfo {
+  int nk[kMaxTopk];  // causal keys of each of the segment's units (0 = nothing to do)
+};
+
 struct AttSmem {
   alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
-  float comb[kConsumerWarps / 2][kGroup][kCombStride];
-  float comb_m[kConsumerWarps / 2][kGroup];
-  float comb_l[kConsumerWarps / 2][kGroup];
+  alignas(1024) uint8_t qtile[kSegSlots][2 * kQBoxBytes];
+  float comb[kConsumerWarps - 1][kGroup][kCombStride];
+  float comb_m[kConsumerWarps - 1][kGroup];
+  float comb_l[kConsumerWarps - 1][kGroup];
+  SegInfo seg[kSegSlots];
   uint64_t full[kAttStages];
   uint64_t empty[kAttStages];
+  uint64_t seg_full[kSegSlots];
+  uint64_t seg_empty[kSegSlots];
   int bcast;
 };
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
 
 __device__ __forceinline__ long long seg_begin(long long c, long long N, long long G) { return c * N / G; }
 __device__ __forceinline__ long long cta_of(long long i, long long N, long long G) {
@@ -146,7 +159,7 @@ __device__ __forceinline__ void merge_from_smem(WarpState& st, const AttSmem& sm
 
 __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-    const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
+    const __grid_constant__ CUtensorMap qmap, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
     float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ partials,
     int* __restrict__ tickets, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -161,6 +174,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
+    for (int s = 0; s < kSegSlots; ++s) {
+      mbar_init(&sm.seg_full[s], 1);
+      mbar_init(&sm.seg_empty[s], kConsumerWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -168,13 +185,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    // per (query, KV head) segment the lanes resolve up to 16 selected blocks
-    // at once (q2k entry, then page id), and lane 0 issues their chunks
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
+      prefetch_tmap(&qmap);
     }
     long long sc = 0;
+    int nseg = 0;
     long long it = lo;
     while (it < hi) {
       const int qi = static_cast<int>(it / (kKvHeads * topk));
@@ -182,16 +199,36 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       const long long seg_end = min(hi, (static_cast<long long>(qi) * kKvHeads + g + 1) * topk);
       const QueryGeo qg = query_geo(geo, qi);
       const int j0 = static_cast<int>(it % topk), jn = static_cast<int>(seg_end - it);
+      // the lanes resolve the segment's blocks in parallel: q2k entry, then page id
       int nk_l = 0;
       long long r0_l = 0;
       if (lane < jn) {
         const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j0 + lane];
+        if (b >= qg.nb) record_error(err, MSA_DEVERR_BLOCK, it + lane);
         nk_l = block_keys(qg, b);
         if (nk_l) {
           r0_l = block_row0(geo, qi, qg, b);
-          if (r0_l < 0) nk_l = 0;
+          if (r0_l < 0) {
+            nk_l = 0;
+            record_error(err, MSA_DEVERR_PAGE, it + lane);
+          }
         }
       }
+      // segment slot: key counts + the Q tile of the 16 heads
+      const int ss = nseg % kSegSlots;
+      if (lane == 0) mbar_wait(&sm.seg_empty[ss], ((nseg / kSegSlots) & 1) ^ 1, err, 210);
+      for (int j = 0; j < kMaxTopk; ++j) {
+        const int v = __shfl_sync(0xffffffffu, nk_l, j);
+        if (lane == 0) sm.seg[ss].nk[j] = j < jn ? v : 0;
+      }
+      if (lane == 0) {
+        mbar_expect_tx(&sm.seg_full[ss], 2 * kQBoxBytes);
+        const int qrow = qi * kHeads + g * kGroup;
+        tma_load_2d(sm.qtile[ss], &qmap, 0, qrow, &sm.seg_full[ss]);
+        tma_load_2d(sm.qtile[ss] + kQBoxBytes, &qmap, 64, qrow, &sm.seg_full[ss]);
+      }
+      __syncwarp();
+      ++nseg;
       for (int k = 0; k < jn; ++k) {
         const int nk = __shfl_sync(0xffffffffu, nk_l, k);
         const long long r0 = __shfl_sync(0xffffffffu, r0_l, k);
@@ -217,9 +254,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     return;
   }
 
-  // ---------------- consumer warps: whole 64-key chunks, round-robin ----------------
+  // ---------------- consumer warps: whole 64-key chunks, stage s -> warp s % 3 ----------------
   const int g8 = lane >> 2, t4 = lane & 3;
   long long sc = 0;  // chunk counter, identical in every consumer warp and the producer
+  int nseg = 0;
   long long it = lo;
   while (it < hi) {
     const int qi = static_cast<int>(it / (kKvHeads * topk));
@@ -227,32 +265,25 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const long long seg_lo = it;
     const long long range0 = (static_cast<long long>(qi) * kKvHeads + g) * topk;
     const long long seg_end = min(hi, range0 + topk);
-    const QueryGeo qg = query_geo(geo, qi);
-    const int j0 = static_cast<int>(it % topk), jn = static_cast<int>(seg_end - it);
-    int nk_l = 0;
-    if (lane < jn) {
-      const int b = q2k[(static_cast<long long>(g) * geo.nq + qi) * topk + j0 + lane];
-      if (b >= qg.nb && warp == 0) record_error(err, MSA_DEVERR_BLOCK, it + lane);
-      nk_l = block_keys(qg, b);
-      if (nk_l && block_row0(geo, qi, qg, b) < 0) {
-        nk_l = 0;
-        if (warp == 0) record_error(err, MSA_DEVERR_PAGE, it + lane);
-      }
-    }
-
-    // Q fragments of the 16 heads of KV head g (A operand, 8 k-steps)
+    const int jn = static_cast<int>(seg_end - it);
+    const int ss = nseg % kSegSlots;
+    mbar_wait(&sm.seg_full[ss], (nseg / kSegSlots) & 1, err, 310);
+    const int nk_l = lane < kMaxTopk ? sm.seg[ss].nk[lane] : 0;
+    // Q fragments of the 16 heads (A operand, 8 k-steps) from the swizzled Q tile
     uint32_t qa[8][4];
     {
-      const __nv_bfloat16* qp = q + (static_cast<long long>(qi) * kHeads + g * kGroup) * kDim;
+      const uint32_t qt = smem_u32(sm.qtile[ss]);
+      const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const int c = 16 * kk + 2 * t4;
-        qa[kk][0] = *reinterpret_cast<const uint32_t*>(qp + g8 * kDim + c);
-        qa[kk][1] = *reinterpret_cast<const uint32_t*>(qp + (g8 + 8) * kDim + c);
-        qa[kk][2] = *reinterpret_cast<const uint32_t*>(qp + g8 * kDim + c + 8);
-        qa[kk][3] = *reinterpret_cast<const uint32_t*>(qp + (g8 + 8) * kDim + c + 8);
+        const int chunk = 2 * kk + (lane >> 4);
+        ldsm_x4(qa[kk], qt + (chunk >> 3) * kQBoxBytes + sw128(qrow, chunk & 7));
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.seg_empty[ss]);  // the slot may be refilled
+    ++nseg;
+
     WarpState st;
     st.m0 = st.m1 = -INFINITY;
     st.l0 = st.l1 = 0.f;
@@ -264,8 +295,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       if (nk == 0) continue;
       const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
       for (int ch = 0; ch < nch; ++ch, ++sc) {
-        if (static_cast<int>(sc % kConsumerWarps) != warp) continue;
         const int s = static_cast<int>(sc % kAttStages);
+        if (s % kConsumerWarps != warp) continue;
         const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
         mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kAttStages) & 1), err, 300);
         const uint32_t stg = smem_u32(sm.stage[s]);
@@ -357,55 +388,54 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     }
     it = seg_end;
 
-    // ---- merge the four warps' states: 4 -> 2 -> 1 ----
+    // ---- merge the three warps' states into warp 0 ----
     st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
     st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
+    consumer_sync();
+    if (warp > 0) state_to_smem(st, sm, warp - 1, g8, t4);
+    consumer_sync();
+    if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
 #pragma unroll
-    for (int half = kConsumerWarps / 2; half >= 1; half >>= 1) {
-      consumer_sync();
-      if (warp >= half && warp < 2 * half) state_to_smem(st, sm, warp - half, g8, t4);
-      consumer_sync();
-      if (warp < half) merge_from_smem(st, sm, warp, g8, t4);
-    }
-    consumer_sync();
-    if (warp == 0) state_to_smem(st, sm, 0, g8, t4);
-    consumer_sync();
-    // ---- write: 16 rows x 128 dims, 16 dims per consumer thread ----
-    const int row = tid >> 3, d0 = (tid & 7) * 16;
+    for (int w = 0; w < kConsumerWarps - 1; ++w) merge_from_smem(st, sm, w, g8, t4);
+    __syncwarp();
+    state_to_smem(st, sm, 0, g8, t4);  // staging for coalesced stores (slot 0 is read only by warp 0)
+    __syncwarp();
+    // ---- warp 0 writes: lane -> row lane/2, 64 dims ----
+    const int row = lane >> 1, d0 = (lane & 1) * 64;
     const float M = sm.comb_m[0][row], Lsum = sm.comb_l[0][row];
+    const float* src = &sm.comb[0][row][d0];
     const bool complete = (seg_lo == range0) && (seg_end == range0 + topk);
     __nv_bfloat16* orow = out + (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
-    const float* src = &sm.comb[0][row][d0];
     if (complete) {
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-      uint32_t w8[8];
 #pragma unroll
-      for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(src[2 * d] * inv, src[2 * d + 1] * inv);
-      reinterpret_cast<uint4*>(orow)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-      reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+      for (int v = 0; v < 8; ++v)
+        reinterpret_cast<uint4*>(orow)[v] =
+            make_uint4(pack_bf16(src[8 * v] * inv, src[8 * v + 1] * inv), pack_bf16(src[8 * v + 2] * inv, src[8 * v + 3] * inv),
+                       pack_bf16(src[8 * v + 4] * inv, src[8 * v + 5] * inv), pack_bf16(src[8 * v + 6] * inv, src[8 * v + 7] * inv));
     } else {
       // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
       const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
       float* pp = partials + slot * kPartialFloats;
-      if ((tid & 7) == 0) {
+      if ((lane & 1) == 0) {
         pp[row] = M;
         pp[16 + row] = Lsum;
       }
 #pragma unroll
-      for (int d = 0; d < 16; d += 4)
-        *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + d) =
-            make_float4(src[d], src[d + 1], src[d + 2], src[d + 3]);
+      for (int v = 0; v < 16; ++v)
+        *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + 4 * v) =
+            make_float4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
       __threadfence();
-      consumer_sync();
-      if (tid == 0) {
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
         const int cnt = static_cast<int>(seg_end - seg_lo);
-        const int old = atomicAdd(&tickets[qi * kKvHeads + g], cnt);
-        sm.bcast = (old + cnt == topk) ? 1 : 0;
+        last = (atomicAdd(&tickets[qi * kKvHeads + g], cnt) + cnt == topk) ? 1 : 0;
       }
-      consumer_sync();
-      if (sm.bcast) {
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
         __threadfence();
         const long long c_first = cta_of(range0, N, G), c_last = cta_of(range0 + topk - 1, N, G);
         float Mg = -INFINITY;
@@ -414,24 +444,30 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
           Mg = fmaxf(Mg, __ldcg(partials + sl * kPartialFloats + row));
         }
         const float Mgu = Mg == -INFINITY ? 0.f : Mg;
-        float Lg = 0.f, ag[16];
+        float Lg = 0.f, ag[64];
 #pragma unroll
-        for (int d = 0; d < 16; ++d) ag[d] = 0.f;
+        for (int d = 0; d < 64; ++d) ag[d] = 0.f;
         for (long long c = c_first; c <= c_last; ++c) {
           const long long sl = 2 * c + (range0 <= seg_begin(c, N, G) ? 0 : 1);
           const float* pc = partials + sl * kPartialFloats;
           const float f = exp2f(__ldcg(pc + row) - Mgu);
           Lg += __ldcg(pc + 16 + row) * f;
 #pragma unroll
-          for (int d = 0; d < 16; ++d) ag[d] += __ldcg(pc + 32 + row * kDim + d0 + d) * f;
+          for (int d = 0; d < 64; d += 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(pc + 32 + row * kDim + d0 + d));
+            ag[d] += x.x * f;
+            ag[d + 1] += x.y * f;
+            ag[d + 2] += x.z * f;
+            ag[d + 3] += x.w * f;
+          }
         }
         const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
-        uint32_t w8[8];
 #pragma unroll
-        for (int d = 0; d < 8; ++d) w8[d] = pack_bf16(ag[2 * d] * inv, ag[2 * d + 1] * inv);
-        reinterpret_cast<uint4*>(orow)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-        reinterpret_cast<uint4*>(orow)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
-        if (tid == 0) tickets[qi * kKvHeads + g] = 0;
+        for (int v = 0; v < 8; ++v)
+          reinterpret_cast<uint4*>(orow)[v] =
+              make_uint4(pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
+                         pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
+        if (lane == 0) tickets[qi * kKvHeads + g] = 0;
       }
     }
   }
@@ -448,10 +484,22 @@ static bool make_kv_map(CUtensorMap* map, const void* base, long long rows) {
   cuuint64_t strides[2] = {kDim * 2, kKvHeads * kDim * 2};
   cuuint32_t box[3] = {64, 1, kChunkKeys};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over q viewed as [queries * 64, 128] bf16; box = 64 dims x 16 heads, 128-byte swizzle.
+static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(nq * kHeads)};
+  cuuint64_t strides[1] = {kDim * 2};
+  cuuint32_t box[2] = {64, kGroup};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
@@ -459,16 +507,18 @@ size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, float* partials,
                                  int* tickets, DevError* err, cudaStream_t stream) {
-  CUtensorMap kmap, vmap;
-  if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows)) return cudaErrorInvalidValue;
+  CUtensorMap kmap, vmap, qmap;
+  if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows) ||
+      !make_q_map(&qmap, q, geo.nq))
+    return cudaErrorInvalidValue;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const int grid = static_cast<int>(N < kNumSMs ? (N > 0 ? N : 1) : kNumSMs);
   const size_t smem = sizeof(AttSmem) + 1024;
   cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const float scale_log2 = scale * 1.4426950408889634f;
-  sparse_attend_kernel<<<grid, kAttThreads, smem, stream>>>(
-      kmap, vmap, static_cast<const __nv_bfloat16*>(q), q2k, geo, topk, scale_log2,
-      static_cast<__nv_bfloat16*>(out), partials, tickets, err);
+  sparse_attend_kernel<<<grid, kAttThreads, smem, stream>>>(kmap, vmap, qmap, q2k, geo, topk, scale_log2,
+                                                            static_cast<__nv_bfloat16*>(out), partials, tickets,
+                                                            err);
   return cudaGetLastError();
 }
 
