@@ -27,9 +27,9 @@ static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 // Workspace layout, shared by msa_workspace_size and the calls.  Completion
 // counters come first, right after the error-word header.
 struct Layout {
-  size_t scores = 0, sel_tickets = 0, att_tickets = 0, partials = 0, plan = 0, total = 0;
+  size_t scores = 0, sel_tickets = 0, att_tickets = 0, partials = 0, plan = 0, bm = 0, total = 0;
 };
-static Layout layout(int mode, long long n, int max_blocks) {
+static Layout layout(int mode, long long n, int max_blocks, int topk) {
   Layout L;
   size_t off = kHeaderBytes;
   if (mode == MSA_MODE_DECODE) {
@@ -42,12 +42,10 @@ static Layout layout(int mode, long long n, int max_blocks) {
     L.partials = off;
     off += up256(attend_partials_bytes());
   } else if (mode == MSA_MODE_PREFILL) {
-    L.att_tickets = off;
-    off += up256(static_cast<size_t>(n) * kKvHeads * sizeof(int));
-    L.partials = off;
-    off += up256(attend_partials_bytes());
     L.plan = off;
     off += up256(prefill_plan_ints(static_cast<int>(n), max_blocks) * sizeof(int));
+    L.bm = off;
+    off += up256(prefill_attend_bytes(n, max_blocks * kBlock, topk));
   }
   L.total = off;
   return L;
@@ -97,7 +95,8 @@ msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int ma
     return MSA_OK;
   }
   if (mode != MSA_MODE_DECODE && mode != MSA_MODE_PREFILL) return MSA_ERR_SHAPE;
-  *bytes = layout(mode, n, max_blocks).total;
+  if (mode == MSA_MODE_PREFILL && !prefill_attend_fits(n, max_blocks * kBlock, cfg->topk)) return MSA_ERR_SHAPE;
+  *bytes = layout(mode, n, max_blocks, cfg->topk).total;
   return MSA_OK;
 }
 
@@ -157,7 +156,7 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   if (!index_q || !index_k_cache || !q2k) return MSA_ERR_NULL;
   if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
   if (!aligned16(index_q) || !aligned16(index_k_cache)) return MSA_ERR_ALIGN;
-  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks);
+  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -176,7 +175,7 @@ msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const 
   if (!q || !k_cache || !v_cache || !q2k || !out) return MSA_ERR_NULL;
   if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return MSA_ERR_ALIGN;
-  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks);
+  const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -207,7 +206,7 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
   if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
   if (!aligned16(index_q) || !aligned16(index_k) || !aligned16(q2k)) return MSA_ERR_ALIGN;
   const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
-  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles);
+  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = launch_prefill_select(*cfg, index_q, index_k, cu_seqlens, num_docs, total_tokens, max_seqlen, q2k,
@@ -226,18 +225,13 @@ msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const
   if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return MSA_ERR_ALIGN;
   const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
-  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles);
+  const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  if (!prefill_attend_fits(total_tokens, max_seqlen, cfg->topk)) return MSA_ERR_SHAPE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (clear_counters(ws, L.att_tickets, static_cast<size_t>(total_tokens) * kKvHeads * sizeof(int), s) !=
-      cudaSuccess)
-    return MSA_ERR_CUDA;
-  AttnGeom geo{1, static_cast<int>(total_tokens), nullptr, nullptr, nullptr, max_tiles, cu_seqlens, num_docs,
-               total_tokens};
-  cudaError_t e = launch_sparse_attend(geo, q, k, v, q2k, cfg->topk, scale, out,
-                                       reinterpret_cast<float*>(ws + L.partials),
-                                       reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
+  cudaError_t e = launch_prefill_attend(q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, cfg->topk,
+                                        scale, out, ws + L.bm, reinterpret_cast<DevError*>(ws),
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -1,0 +1,782 @@
+// prefill_attend.cu -- block-major sparse attention for packed-document prefill.
+//
+// TensorRT-LLM "MiniMaxM3SparseAttentionConfig" (class description, second
+// step: a sparse GQA attention over only the selected blocks) and NeMo
+// "...minimax_m3_vl.msa" sparse_attention / _SparseAttention.forward: bf16
+// q [tokens, 64, 128], k / v [tokens, 4, 128], int32 q2k [4, tokens, topk] ->
+// bf16 out [tokens, 64, 128]; query t of a document attends, for each KV head,
+// to the causal keys of the blocks its q2k row names.
+//
+// GB300 design.  In prefill a key block is selected by many queries of its
+// document, so the work is turned around: every selected (query, KV head,
+// block) triple -- an "entry" -- is bucketed by (KV head, token window, key
+// block), and each bucket is cut into tiles of 8 entries.  A tile's 8 x 16
+// query rows form one 128-row tcgen05 MMA against the block's 128 keys, so a
+// K / V block is read once per tile run instead of once per query, and the
+// tensor cores see full 128 x 128 x 128 products:
+//
+//   S = Q K^T   (A = gathered Q rows, B = K block; both K-major, 128-byte swizzle)
+//   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 to shared memory)
+//   O = P V     (A = P, B = V read MN-major straight from the TMA tile)
+//
+// with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 4
+// issues TMA (Q rows gathered with a 3-D tensor map, one 16-head box per
+// entry; K and V blocks as 128-row boxes), warp 5 issues the MMAs from one
+// thread, warps 0-3 own one tensor-memory lane (query row) each thread: they
+// run the softmax of tile i and the epilogue of tile i-1.  Each entry's result
+// is written as a partial (row max and sum in fp32, O / sum in fp16); a merge
+// kernel combines the <= topk partials of a (query, KV head) pair into the
+// bf16 output.  Tiles are handed out in chunks of 4, round-robin over the
+// persistent grid, so all CTAs move through the (KV head, window) buckets
+// together and the window's Q rows and K / V blocks stay in L2.
+#include <cuda_fp16.h>
+
+#include "launch.h"
+
+namespace msa {
+
+constexpr int kBmEntries = 8;                     // entries per tile (8 x 16 heads = 128 MMA rows)
+constexpr int kBmHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16) = 16 KB
+constexpr int kBmTile = 2 * kBmHalf;              // a 128 x 128 bf16 operand
+constexpr int kBmQBox = kGroup * 128;             // one entry's 16 rows x 64 dims = 2 KB
+constexpr int kBmThreads = 192;                   // warps 0-3 softmax/epilogue, 4 TMA, 5 MMA
+constexpr int kBmChunk = 4;                       // tiles per scheduling chunk
+constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
+constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
+
+struct BmTile {
+  int row0;  // first K / V row of the block
+  int g;     // KV head
+  int off;   // first entry of the tile in the bucketed entry list
+  int cnt;   // entries in the tile (1..8)
+};
+
+struct BmSmem {
+  alignas(1024) uint8_t q[2][kBmTile];
+  alignas(1024) uint8_t k[2][kBmTile];
+  alignas(1024) uint8_t v[2][kBmTile];
+  alignas(1024) uint8_t p[kBmTile];
+  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
+  uint64_t p_full, p_empty, done;
+  uint32_t tmem_base;
+};
+
+// Sizes of the bucketing problem, fixed by (tokens, longest document, topk).
+struct BmDims {
+  long long T;       // compact tokens
+  int topk;
+  int W;             // token window of a bucket (power of two)
+  int nw;            // windows
+  long long kg_max;  // bound on the keys of one KV head
+  long long entries; // 4 * T * topk
+  long long tiles_max;
+};
+
+static BmDims bm_dims(long long T, int max_seqlen, int topk) {
+  BmDims d;
+  d.T = T;
+  d.topk = topk;
+  d.W = 256;
+  while (d.W < max_seqlen / 16) d.W *= 2;
+  d.nw = static_cast<int>((T + d.W - 1) / d.W);
+  const long long mb = (max_seqlen + kBlock - 1) / kBlock;
+  // A window reaches the blocks of its first document plus blocks that start
+  // inside it.  The bound uses the smallest window (256 tokens) so that it only
+  // grows with T and max_seqlen: a workspace sized for one call serves every
+  // smaller one.
+  d.kg_max = (T + 255) / 256 * mb + T + 1;
+  d.entries = static_cast<long long>(kKvHeads) * T * topk;
+  const long long keys = kKvHeads * d.kg_max;
+  d.tiles_max = d.entries / kBmEntries + (keys < d.entries ? keys : d.entries) + 1;
+  return d;
+}
+
+// Carving of the prefill-attention part of the workspace.
+struct BmPlan {
+  int* meta;       // [0] keys per KV head (Kg), [1] tiles
+  int* counts;     // [4 * kg_max] entries per key
+  int* offs;       // [4 * kg_max + 1] first entry of each key
+  int* toff;       // [4 * kg_max + 1] first tile of each key
+  int* blk_base;   // [T + 1] first global block of each document
+  int* wlo;        // [nw] first global block a window can reach
+  int* wbase;      // [nw + 1] first key of each window (per KV head)
+  int* ekey;       // [entries] key of each q2k entry, -1 when skipped
+  int* erank;      // [entries] rank of the entry inside its key
+  int* elist;      // [entries] bucketed entries: t * topk + j
+  BmTile* tiles;   // [tiles_max]
+  __half* po;      // [entries][16][128] partial O / sum
+  float2* pml;     // [entries][16] partial (row max in log2 units, row sum)
+};
+
+static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+static size_t bm_carve(const BmDims& d, uint8_t* base, BmPlan* p) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* ptr = base ? base + off : nullptr;
+    off += al256(bytes);
+    return ptr;
+  };
+  const size_t keys = static_cast<size_t>(kKvHeads) * d.kg_max;
+  BmPlan q;
+  q.meta = reinterpret_cast<int*>(take(4 * sizeof(int)));
+  q.counts = reinterpret_cast<int*>(take(keys * sizeof(int)));
+  q.offs = reinterpret_cast<int*>(take((keys + 1) * sizeof(int)));
+  q.toff = reinterpret_cast<int*>(take((keys + 1) * sizeof(int)));
+  q.blk_base = reinterpret_cast<int*>(take((d.T + 1) * sizeof(int)));
+  q.wlo = reinterpret_cast<int*>(take(((d.T + 255) / 256) * sizeof(int)));
+  q.wbase = reinterpret_cast<int*>(take(((d.T + 255) / 256 + 1) * sizeof(int)));
+  q.ekey = reinterpret_cast<int*>(take(d.entries * sizeof(int)));
+  q.erank = reinterpret_cast<int*>(take(d.entries * sizeof(int)));
+  q.elist = reinterpret_cast<int*>(take(d.entries * sizeof(int)));
+  q.tiles = reinterpret_cast<BmTile*>(take(d.tiles_max * sizeof(BmTile)));
+  q.po = reinterpret_cast<__half*>(take(d.entries * kGroup * kDim * sizeof(__half)));
+  q.pml = reinterpret_cast<float2*>(take(d.entries * kGroup * sizeof(float2)));
+  if (p) *p = q;
+  return off;
+}
+
+size_t prefill_attend_bytes(long long total_tokens, int max_seqlen, int topk) {
+  return bm_carve(bm_dims(total_tokens, max_seqlen, topk), nullptr, nullptr);
+}
+
+// ---- small device helpers ---------------------------------------------------------
+
+// Index of the document holding compact token t: the last d with cu[d] <= t.
+__device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int num_docs, long long t) {
+  int lo = 0, hi = num_docs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Last index i in [0, n) with a[i] <= x (a ascending, a[0] <= x).
+__device__ __forceinline__ int last_le(const int* __restrict__ a, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Exclusive scan of one value per thread over a 1024-thread block; returns the
+// prefix and writes the block total to *total.  `sh` holds 32 ints.
+__device__ __forceinline__ long long block_scan_1024(long long v, long long* sh, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = sh[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh[lane] = w;
+  }
+  __syncthreads();
+  const long long before = (warp > 0 ? sh[warp - 1] : 0) + x - v;
+  *total = sh[31];
+  __syncthreads();
+  return before;
+}
+
+
+// ---- bucketing ----------------------------------------------------------------------
+
+// One block of 1024 threads: document block bases, window reach and the first
+// key of every window.  Key space of one KV head: window w owns keys
+// [wbase[w], wbase[w+1]), one per global block in [wlo[w], wlo[w] + span).
+__global__ void __launch_bounds__(1024) bm_geom_kernel(const int32_t* __restrict__ cu, int num_docs, long long T,
+                                                       int W, int nw, long long kg_max, BmPlan p, DevError* err) {
+  __shared__ long long sh[32];
+  const int tid = threadIdx.x;
+  {
+    const int per = (num_docs + 1023) / 1024;
+    const int d0 = min(num_docs, tid * per), d1 = min(num_docs, d0 + per);
+    long long s = 0;
+    for (int d = d0; d < d1; ++d) s += (cu[d + 1] - cu[d] + kBlock - 1) / kBlock;
+    long long tot;
+    long long run = block_scan_1024(s, sh, &tot);
+    for (int d = d0; d < d1; ++d) {
+      p.blk_base[d] = static_cast<int>(run);
+      run += (cu[d + 1] - cu[d] + kBlock - 1) / kBlock;
+    }
+    if (tid == 0) p.blk_base[num_docs] = static_cast<int>(tot);
+  }
+  __syncthreads();
+  {
+    const int per = (nw + 1023) / 1024;
+    const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
+    long long s = 0;
+    for (int w = w0; w < w1; ++w) {
+      const long long t0 = static_cast<long long>(w) * W;
+      const long long t1 = (t0 + W < T ? t0 + W : T) - 1;
+      const int da = doc_of(cu, num_docs, t0), db = doc_of(cu, num_docs, t1);
+      const int lo = p.blk_base[da];
+      const int hi = p.blk_base[db] + static_cast<int>((t1 - cu[db]) / kBlock);
+      p.wlo[w] = lo;
+      p.wbase[w] = hi - lo + 1;  // span for now
+      s += hi - lo + 1;
+    }
+    long long tot;
+    long long run = block_scan_1024(s, sh, &tot);
+    for (int w = w0; w < w1; ++w) {
+      const int span = p.wbase[w];
+      p.wbase[w] = static_cast<int>(run);
+      run += span;
+    }
+    if (tid == 0) {
+      if (tot > kg_max) {  // cannot happen for a well-formed cu_seqlens; leave nothing to do
+        record_error(err, MSA_DEVERR_LENGTH, tot);
+        tot = 0;
+      }
+      p.wbase[nw] = static_cast<int>(tot);
+      p.meta[0] = static_cast<int>(tot);
+    }
+  }
+}
+
+// One thread per (KV head, token): the key of each of the token's q2k entries
+// and its rank inside the key (warp-aggregated atomics: the tokens of a warp
+// share their forced blocks).  Entries that name no block (-1) are skipped;
+// ids at or past the query's causal block count are recorded and skipped.
+__global__ void __launch_bounds__(256) bm_count_kernel(const int32_t* __restrict__ q2k,
+                                                       const int32_t* __restrict__ cu, int num_docs, long long T,
+                                                       int topk, int W, BmPlan p, DevError* err) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const bool live = idx < kKvHeads * T;
+  const int Kg = p.meta[0];
+  int g = 0, nb = 0, w = 0, gb0 = 0, kbase = 0;
+  long long t = 0;
+  if (live) {
+    g = static_cast<int>(idx / T);
+    t = idx - static_cast<long long>(g) * T;
+    const int d = doc_of(cu, num_docs, t);
+    const int pos = static_cast<int>(t - cu[d]);
+    nb = pos / kBlock + 1;
+    w = static_cast<int>(t / W);
+    gb0 = p.blk_base[d];
+    kbase = g * Kg + p.wbase[w] - p.wlo[w];
+  }
+  const long long e0 = idx * topk;  // == (g * T + t) * topk
+  const unsigned lt = (1u << lane) - 1u;
+  for (int j = 0; j < topk; ++j) {
+    int key = -1;
+    if (live) {
+      const int b = q2k[e0 + j];
+      if (b >= nb) record_error(err, MSA_DEVERR_BLOCK, e0 + j);
+      else if (b >= 0) key = kbase + gb0 + b;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(grp) - 1;
+    int base = 0;
+    if (key >= 0 && lane == leader) base = atomicAdd(&p.counts[key], __popc(grp));
+    base = __shfl_sync(grp, base, leader);
+    if (live) {
+      p.ekey[e0 + j] = key;
+      p.erank[e0 + j] = base + __popc(grp & lt);
+    }
+  }
+}
+
+// One block of 1024 threads: exclusive scans of the key counts (entry offsets)
+// and of the tiles per key; the tile total goes to meta[1].
+__global__ void __launch_bounds__(1024) bm_scan_kernel(BmPlan p) {
+  __shared__ long long sh[32];
+  const int tid = threadIdx.x;
+  const long long K = static_cast<long long>(kKvHeads) * p.meta[0];
+  const long long per = (K + 1023) / 1024;
+  const long long k0 = min(K, tid * per), k1 = min(K, k0 + per);
+  long long se = 0, st = 0;
+  for (long long k = k0; k < k1; ++k) {
+    const int c = p.counts[k];
+    se += c;
+    st += (c + kBmEntries - 1) / kBmEntries;
+  }
+  long long te, tt;
+  long long re = block_scan_1024(se, sh, &te);
+  long long rt = block_scan_1024(st, sh, &tt);
+  for (long long k = k0; k < k1; ++k) {
+    const int c = p.counts[k];
+    p.offs[k] = static_cast<int>(re);
+    p.toff[k] = static_cast<int>(rt);
+    re += c;
+    rt += (c + kBmEntries - 1) / kBmEntries;
+  }
+  if (tid == 0) {
+    p.offs[K] = static_cast<int>(te);
+    p.toff[K] = static_cast<int>(tt);
+    p.meta[1] = static_cast<int>(tt);
+  }
+}
+
+// One thread per key: the tile descriptors of the key (K / V rows, KV head,
+// entry range).
+__global__ void __launch_bounds__(256) bm_tiles_kernel(const int32_t* __restrict__ cu, int num_docs, int nw,
+                                                       BmPlan p) {
+  const long long key = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int Kg = p.meta[0];
+  if (key >= static_cast<long long>(kKvHeads) * Kg) return;
+  const int c = p.counts[key];
+  if (c == 0) return;
+  const int g = static_cast<int>(key / Kg), kk = static_cast<int>(key - static_cast<long long>(g) * Kg);
+  const int w = last_le(p.wbase, nw, kk);
+  const int gb = p.wlo[w] + kk - p.wbase[w];
+  const int d = last_le(p.blk_base, num_docs, gb);
+  const int row0 = cu[d] + (gb - p.blk_base[d]) * kBlock;
+  const int t0 = p.toff[key], o0 = p.offs[key];
+  for (int i = 0; i * kBmEntries < c; ++i)
+    p.tiles[t0 + i] = BmTile{row0, g, o0 + i * kBmEntries, min(kBmEntries, c - i * kBmEntries)};
+}
+
+// One thread per q2k entry: its place in the bucketed list.
+__global__ void __launch_bounds__(256) bm_scatter_kernel(long long entries, long long per_head, BmPlan p) {
+  const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= entries) return;
+  const int key = p.ekey[e];
+  if (key < 0) return;
+  p.elist[p.offs[key] + p.erank[e]] = static_cast<int>(e % per_head);
+}
+
+
+// ---- the tensor-core kernel ---------------------------------------------------------
+
+// Shared-memory descriptor of V read MN-major (N = head dims contiguous inside a
+// 128-byte swizzled row, K = keys along rows): 64-dim atoms 16 KB apart (LBO),
+// 8-key groups 1024 bytes apart (SBO).
+__device__ __forceinline__ uint64_t desc_v_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(kBmHalf >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// The CTA's tiles: chunks c, c + G, c + 2G, ... of kBmChunk consecutive tiles.
+#define BM_FOR_EACH_TILE(tau)                                                        \
+  for (int ch_ = blockIdx.x; ch_ * kBmChunk < n_tiles; ch_ += gridDim.x)             \
+    for (int tau = ch_ * kBmChunk, te_ = min(n_tiles, ch_ * kBmChunk + kBmChunk); tau < te_; ++tau)
+
+__global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap vmap, BmPlan p, long long T, int topk, float scale_log2, DevError* err) {
+  extern __shared__ uint8_t smem_raw[];
+  BmSmem& sm = *reinterpret_cast<BmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_tiles = p.meta[1];
+  const BmTile* __restrict__ tiles = p.tiles;
+  const int* __restrict__ elist = p.elist;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1);
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.o_full[i], 1);
+      mbar_init(&sm.o_free[i], 4);
+    }
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.p_empty, 1);
+    mbar_init(&sm.done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::alloc(&sm.tmem_base, 512);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  // A wait that gives up (recorded in the error word) marks the role dead: it
+  // stops issuing work, so a broken pipeline ends after one bounded wait per
+  // role instead of one per tile.
+  if (warp == 4) {
+    // ---------------- TMA producer: K / V per new block, Q rows per tile ----------------
+    if (lane == 0) {
+      prefetch_tmap(&qmap);
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+    }
+    int i = 0, prow = -1, pg = -1;
+    int nkf = 0, nvf = 0;  // K and V fills issued (lane 0)
+    bool dead = false;
+    // Per tile: K of a new block, then the tile's Q rows, then V of a new block.
+    // V comes last because its stage is released by the O MMA of the previous
+    // block's first tile, which the MMA warp issues only after this tile's S MMA.
+    BM_FOR_EACH_TILE(tau) {
+      if (dead) break;
+      const BmTile d = tiles[tau];
+      const bool fresh = d.row0 != prow || d.g != pg;
+      const int qs = i & 1;
+      const int ent = lane < d.cnt ? elist[d.off + lane] : 0;
+      bool ok = true;
+      if (lane == 0) {
+        if (fresh) {
+          const int s = nkf & 1;
+          ok = mbar_wait(&sm.k_empty[s], ((nkf >> 1) & 1) ^ 1, err, 700);
+          if (ok) {
+            mbar_expect_tx(&sm.k_full[s], kBmTile);
+            tma_load_3d(sm.k[s], &kmap, 0, d.g, d.row0, &sm.k_full[s]);
+            tma_load_3d(sm.k[s] + kBmHalf, &kmap, 64, d.g, d.row0, &sm.k_full[s]);
+            ++nkf;
+          }
+        }
+        ok = ok && mbar_wait(&sm.q_empty[qs], ((i >> 1) & 1) ^ 1, err, 702);
+        if (ok) mbar_expect_tx(&sm.q_full[qs], d.cnt * 2 * kBmQBox);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        dead = true;
+        break;
+      }
+      if (lane < d.cnt) {
+        const int t = ent / topk;
+        tma_load_3d(sm.q[qs] + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.q_full[qs]);
+        tma_load_3d(sm.q[qs] + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.q_full[qs]);
+      }
+      __syncwarp();
+      ++i;
+      if (fresh) {
+        prow = d.row0;
+        pg = d.g;
+        if (lane == 0) {
+          const int s = nvf & 1;
+          ok = mbar_wait(&sm.v_empty[s], ((nvf >> 1) & 1) ^ 1, err, 701);
+          if (ok) {
+            mbar_expect_tx(&sm.v_full[s], kBmTile);
+            tma_load_3d(sm.v[s], &vmap, 0, d.g, d.row0, &sm.v_full[s]);
+            tma_load_3d(sm.v[s] + kBmHalf, &vmap, 64, d.g, d.row0, &sm.v_full[s]);
+            ++nvf;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          dead = true;
+          break;
+        }
+      }
+    }
+    // no copy may still be landing when the CTA exits: wait for the last fill of every stage
+    if (lane == 0) {
+      for (int q = 0; q < 2; ++q) {
+        const int fq = (i - q + 1) / 2;  // fills of Q stage q
+        if (fq > 0) mbar_wait(&sm.q_full[q], (fq - 1) & 1, err, 703);
+        const int fk = (nkf - q + 1) / 2;
+        if (fk > 0) mbar_wait(&sm.k_full[q], (fk - 1) & 1, err, 704);
+        const int fv = (nvf - q + 1) / 2;
+        if (fv > 0) mbar_wait(&sm.v_full[q], (fv - 1) & 1, err, 705);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer: S(i) then O(i-1) ----------------
+    if (lane == 0) {
+      int i = 0, nk = 0, ks = 0, prow = -1, pg = -1;    // S side
+      int nv = 0, vs = 0, vrow = -1, vg = -1;           // O side
+      bool dead = false;
+      BmTile pend{0, 0, 0, 0};
+      auto issue_o = [&](const BmTile& d, int i2) {
+        if (d.row0 != vrow || d.g != vg) {
+          if (nv > 0) tc::commit(&sm.v_empty[vs]);
+          vs = nv & 1;
+          if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) return false;
+          ++nv;
+          vrow = d.row0;
+          vg = d.g;
+        }
+        const int ob = i2 & 1;
+        if (!mbar_wait(&sm.p_full, i2 & 1, err, 714)) return false;
+        if (!mbar_wait(&sm.o_free[ob], ((i2 >> 1) & 1) ^ 1, err, 715)) return false;
+        tc::fence_after();
+        const uint32_t pa = smem_u32(sm.p), va = smem_u32(sm.v[vs]);
+        const uint32_t dt = tmem + 256 + ob * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(dt, tc::desc_k_sw128(pa + (kk >> 2) * kBmHalf + (kk & 3) * 32),
+                       desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
+        tc::commit(&sm.o_full[ob]);
+        tc::commit(&sm.p_empty);
+        return true;
+      };
+      BM_FOR_EACH_TILE(tau) {
+        if (dead) break;
+        const BmTile d = tiles[tau];
+        if (d.row0 != prow || d.g != pg) {
+          if (nk > 0) tc::commit(&sm.k_empty[ks]);
+          ks = nk & 1;
+          if (!mbar_wait(&sm.k_full[ks], (nk >> 1) & 1, err, 710)) {
+            dead = true;
+            break;
+          }
+          ++nk;
+          prow = d.row0;
+          pg = d.g;
+        }
+        const int qs = i & 1, sb = i & 1;
+        if (!mbar_wait(&sm.q_full[qs], (i >> 1) & 1, err, 711) ||
+            !mbar_wait(&sm.s_free[sb], ((i >> 1) & 1) ^ 1, err, 712)) {
+          dead = true;
+          break;
+        }
+        tc::fence_after();
+        const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k[ks]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + sb * 128, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kBmIdescS, kk > 0);
+        }
+        tc::commit(&sm.s_full[sb]);
+        tc::commit(&sm.q_empty[qs]);
+        if (i > 0 && !issue_o(pend, i - 1)) {
+          dead = true;
+          break;
+        }
+        pend = d;
+        ++i;
+      }
+      if (!dead && i > 0) issue_o(pend, i - 1);
+      // every MMA has finished before tensor memory is released
+      tc::commit(&sm.done);
+      mbar_wait(&sm.done, 0, err, 716);
+    }
+  } else {
+    // ---------------- warps 0-3: softmax of tile i, epilogue of tile i-1 ----------------
+    const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t pbase = smem_u32(sm.p);
+    const long long per_head = T * topk;
+    int i = 0;
+    bool dead = false, pvalid = false;
+    long long pslot = 0;
+    float pm = 0.f, pl = 0.f;
+    auto epilogue = [&](int i2) {
+      const int ob = i2 & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[ob], (i2 >> 1) & 1, err, 722))) return false;
+      tc::fence_after();
+      const float inv = pl > 0.f ? 1.f / pl : 0.f;
+      __half* orow = p.po + (pslot * kGroup + h) * kDim;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(lane_base + 256 + ob * 128 + ch * 32, v);
+        tc::wait_ld();
+        if (pvalid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_half2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+            u.y = pack_half2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+            u.z = pack_half2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+            u.w = pack_half2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) = u;
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      if (pvalid) p.pml[pslot * kGroup + h] = make_float2(pm, pl);
+      return true;
+    };
+    BM_FOR_EACH_TILE(tau) {
+      if (dead) break;
+      const BmTile d = tiles[tau];
+      const bool valid = e < d.cnt;
+      const int ent = valid ? elist[d.off + e] : 0;
+      const long long t = ent / topk;
+      const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - d.row0 + 1)) : 0;
+      const int sb = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, err, 720))) {
+        dead = true;
+        break;
+      }
+      tc::fence_after();
+      float s[128];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(lane_base + sb * 128 + ch * 32, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) s[ch * 32 + q] = __uint_as_float(v[q]);
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 128; ++k) {
+        s[k] = k < nkeys ? s[k] * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      const float mu = mx == -INFINITY ? 0.f : mx;
+      float l = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const float a = exp2f(s[2 * k] - mu), b = exp2f(s[2 * k + 1] - mu);
+        l += a + b;
+        pk[k] = pack_bf16(a, b);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty, (i & 1) ^ 1, err, 721))) {
+        dead = true;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        sts128(pbase + (c >> 3) * kBmHalf + sw128(r, c & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+               pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full);
+      if (i > 0 && !epilogue(i - 1)) {
+        dead = true;
+        break;
+      }
+      pvalid = valid;
+      pslot = static_cast<long long>(d.g) * per_head + ent;
+      pm = mx;
+      pl = l;
+      ++i;
+    }
+    if (!dead && i > 0) epilogue(i - 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+#undef BM_FOR_EACH_TILE
+
+// One 256-thread block per (token, KV head): combines the token's partials.
+// Thread (h, c) owns dims 8c..8c+7 of head h of the group.
+__global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict__ q2k,
+                                                       const int32_t* __restrict__ cu, int num_docs, long long T,
+                                                       int topk, BmPlan p, __nv_bfloat16* __restrict__ out) {
+  const long long t = blockIdx.x;
+  const int g = blockIdx.y;
+  const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
+  const int d = doc_of(cu, num_docs, t);
+  const int nb = static_cast<int>(t - cu[d]) / kBlock + 1;
+  const long long e0 = (static_cast<long long>(g) * T + t) * topk;
+  unsigned ok = 0;
+  for (int j = 0; j < topk; ++j) {
+    const int b = q2k[e0 + j];
+    if (b >= 0 && b < nb) ok |= 1u << j;
+  }
+  float M = -INFINITY;
+  for (unsigned m = ok; m; m &= m - 1) M = fmaxf(M, p.pml[(e0 + __ffs(m) - 1) * kGroup + h].x);
+  const float Mu = M == -INFINITY ? 0.f : M;
+  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (unsigned m = ok; m; m &= m - 1) {
+    const long long slot = e0 + __ffs(m) - 1;
+    const float2 ml = p.pml[slot * kGroup + h];
+    const float w = ml.y * exp2f(ml.x - Mu);
+    L += w;
+    const uint4 u = *reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c);
+    const __half2* hv = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(hv[q]);
+      acc[2 * q] += w * f.x;
+      acc[2 * q + 1] += w * f.y;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint4 o;
+  o.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(out + ((t * kHeads) + g * kGroup + h) * kDim + 8 * c) = o;
+}
+
+
+// ---- host side --------------------------------------------------------------------
+
+static bool encode3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+                     cuuint32_t b0, cuuint32_t b1, cuuint32_t b2) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prefill_attend_fits(long long total_tokens, int max_seqlen, int topk) {
+  const BmDims d = bm_dims(total_tokens, max_seqlen, topk);
+  return d.entries < (1LL << 31) && kKvHeads * d.kg_max < (1LL << 31) && d.tiles_max < (1LL << 31);
+}
+
+cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, const int32_t* q2k,
+                                  const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
+                                  int topk, float scale, void* out, uint8_t* region, DevError* err,
+                                  cudaStream_t stream) {
+  const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
+  BmPlan p;
+  bm_carve(dims, region, &p);
+  CUtensorMap qmap, kmap, vmap;
+  if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
+      !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
+    return cudaErrorInvalidValue;
+  const long long keys = kKvHeads * dims.kg_max;
+  cudaError_t e = cudaMemsetAsync(p.counts, 0, keys * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  bm_geom_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_docs, total_tokens, dims.W, dims.nw, dims.kg_max, p, err);
+  const long long pairs = kKvHeads * total_tokens;
+  bm_count_kernel<<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(q2k, cu_seqlens, num_docs,
+                                                                                 total_tokens, topk, dims.W, p, err);
+  bm_scan_kernel<<<1, 1024, 0, stream>>>(p);
+  bm_tiles_kernel<<<static_cast<unsigned>((keys + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs, dims.nw, p);
+  bm_scatter_kernel<<<static_cast<unsigned>((dims.entries + 255) / 256), 256, 0, stream>>>(
+      dims.entries, total_tokens * topk, p);
+  const size_t smem = sizeof(BmSmem) + 1024;
+  cudaFuncSetAttribute(bm_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
+  const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
+  bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, p, total_tokens, topk,
+                                                       scale * 1.4426950408889634f, err);
+  bm_merge_kernel<<<dim3(static_cast<unsigned>(total_tokens), kKvHeads), 256, 0, stream>>>(
+      q2k, cu_seqlens, num_docs, total_tokens, topk, p, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace msa
