@@ -67,14 +67,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after kWaitLimit polls, records MSA_DEVERR_TIMEOUT
-// with `where` as the detail, and returns false.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// try_wait that may suspend the thread in hardware for up to `ns` nanoseconds
+// (woken early when the phase completes), so waiting warps do not spin.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(1000)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after kWaitNs of wall time (global timer), records
+// MSA_DEVERR_TIMEOUT with `where` as the detail, and returns false.
+constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevError* err, int where) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(32);
-  }
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  do {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+  } while (global_ns() - t0 < kWaitNs);
   record_error(err, MSA_DEVERR_TIMEOUT, where);
   return false;
 }

@@ -20,11 +20,13 @@
 //   O = P V     (A = P, B = V read MN-major straight from the TMA tile)
 //
 // with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 4
-// issues TMA (Q rows gathered with a 3-D tensor map, one 16-head box per
-// entry; K and V blocks as 128-row boxes), warp 5 issues the MMAs from one
-// thread, warps 0-3 own one tensor-memory lane (query row) each thread: they
-// run the softmax of tile i and the epilogue of tile i-1.  Each entry's result
-// is written as a partial (row max and sum in fp32, O / sum in fp16); a merge
+// schedules the tiles (descriptors and entries read ahead from global memory,
+// published in a shared-memory ring) and issues TMA (Q rows gathered with a
+// 3-D tensor map, one 16-head box per entry; K and V blocks as 128-row boxes);
+// warp 5 issues the MMAs from one thread; warps 0-3 run the softmax with one
+// tensor-memory lane (query row) per thread; warps 6-9 move O out of tensor
+// memory.  Each entry's result is written as a partial: row max (log2 units)
+// and row sum of p in fp32, and the unnormalised O / 128 in fp16; a merge
 // kernel combines the <= topk partials of a (query, KV head) pair into the
 // bf16 output.  Tiles are handed out in chunks of 4, round-robin over the
 // persistent grid, so all CTAs move through the (KV head, window) buckets
@@ -39,7 +41,7 @@ constexpr int kBmEntries = 8;                     // entries per tile (8 x 16 he
 constexpr int kBmHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16) = 16 KB
 constexpr int kBmTile = 2 * kBmHalf;              // a 128 x 128 bf16 operand
 constexpr int kBmQBox = kGroup * 128;             // one entry's 16 rows x 64 dims = 2 KB
-constexpr int kBmThreads = 192;                   // warps 0-3 softmax/epilogue, 4 TMA, 5 MMA
+constexpr int kBmThreads = 320;                   // warps 0-3 softmax, 4 TMA, 5 MMA, 6-9 epilogue
 constexpr int kBmChunk = 4;                       // tiles per scheduling chunk
 constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
@@ -51,6 +53,13 @@ struct BmTile {
   int cnt;   // entries in the tile (1..8)
 };
 
+// A tile as the scheduler publishes it to the MMA and softmax warps.
+struct BmInfo {
+  int row0, g, cnt, fresh;  // fresh: first tile of a new K / V block
+  int ent[kBmEntries];
+};
+constexpr int kBmInfo = 8;  // info ring slots
+
 struct BmSmem {
   alignas(1024) uint8_t q[2][kBmTile];
   alignas(1024) uint8_t k[2][kBmTile];
@@ -59,6 +68,8 @@ struct BmSmem {
   uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
   uint64_t p_full, p_empty, done;
+  uint64_t info_full[kBmInfo], info_empty[kBmInfo];
+  BmInfo info[kBmInfo];
   uint32_t tmem_base;
 };
 
@@ -105,8 +116,8 @@ struct BmPlan {
   int* erank;      // [entries] rank of the entry inside its key
   int* elist;      // [entries] bucketed entries: t * topk + j
   BmTile* tiles;   // [tiles_max]
-  __half* po;      // [entries][16][128] partial O / sum
-  float2* pml;     // [entries][16] partial (row max in log2 units, row sum)
+  __half* po;      // [entries][16][128] partial O / 128 (O = sum_k p_k v_k, unnormalised)
+  float2* pml;     // [entries][16] partial (row max in log2 units, row sum of p)
 };
 
 static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -379,10 +390,27 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// The CTA's tiles: chunks c, c + G, c + 2G, ... of kBmChunk consecutive tiles.
-#define BM_FOR_EACH_TILE(tau)                                                        \
-  for (int ch_ = blockIdx.x; ch_ * kBmChunk < n_tiles; ch_ += gridDim.x)             \
-    for (int tau = ch_ * kBmChunk, te_ = min(n_tiles, ch_ * kBmChunk + kBmChunk); tau < te_; ++tau)
+// The CTA's i-th tile: chunks c, c + G, c + 2G, ... of kBmChunk consecutive tiles.
+__device__ __forceinline__ int tile_at(int i) {
+  return (blockIdx.x + gridDim.x * (i / kBmChunk)) * kBmChunk + i % kBmChunk;
+}
+__device__ __forceinline__ int local_tiles(int n_tiles) {
+  int n = 0;
+  for (int k = blockIdx.x; k * kBmChunk < n_tiles; k += gridDim.x) n += min(kBmChunk, n_tiles - k * kBmChunk);
+  return n;
+}
+
+// Single MUFU base-2 exponential (ex2.approx.ftz: relative error about 2^-22;
+// exp2(-inf) = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -390,9 +418,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   extern __shared__ uint8_t smem_raw[];
   BmSmem& sm = *reinterpret_cast<BmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_tiles = p.meta[1];
-  const BmTile* __restrict__ tiles = p.tiles;
-  const int* __restrict__ elist = p.elist;
+  const int n = local_tiles(p.meta[1]);  // tiles of this CTA
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -406,6 +432,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       mbar_init(&sm.s_free[i], 4);
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 4);
+    }
+    for (int i = 0; i < kBmInfo; ++i) {
+      mbar_init(&sm.info_full[i], 1);
+      mbar_init(&sm.info_empty[i], 9);  // four softmax warps, the MMA thread, four epilogue warps
     }
     mbar_init(&sm.p_full, 4);
     mbar_init(&sm.p_empty, 1);
@@ -425,25 +455,46 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   // stops issuing work, so a broken pipeline ends after one bounded wait per
   // role instead of one per tile.
   if (warp == 4) {
-    // ---------------- TMA producer: K / V per new block, Q rows per tile ----------------
+    // ---------------- scheduler + TMA producer ----------------
+    // Reads each tile's descriptor and entries from global memory one and two
+    // tiles ahead, publishes them in the info ring, then issues K of a new
+    // block, the tile's Q rows, and V of a new block.  V comes last because its
+    // stage is released by the O MMA of the previous block's first tile, which
+    // the MMA warp issues only after this tile's S MMA.
     if (lane == 0) {
       prefetch_tmap(&qmap);
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
     }
-    int i = 0, prow = -1, pg = -1;
+    const BmTile none{-1, -1, 0, 0};
+    BmTile d_next = n > 0 ? p.tiles[tile_at(0)] : none;
+    int e_next = lane < d_next.cnt ? p.elist[d_next.off + lane] : 0;
+    BmTile d_after = n > 1 ? p.tiles[tile_at(1)] : none;
+    int prow = -1, pg = -1;
     int nkf = 0, nvf = 0;  // K and V fills issued (lane 0)
-    bool dead = false;
-    // Per tile: K of a new block, then the tile's Q rows, then V of a new block.
-    // V comes last because its stage is released by the O MMA of the previous
-    // block's first tile, which the MMA warp issues only after this tile's S MMA.
-    BM_FOR_EACH_TILE(tau) {
-      if (dead) break;
-      const BmTile d = tiles[tau];
+    int i = 0;
+    for (; i < n; ++i) {
+      const BmTile d = d_next;
+      const int ent = e_next;
+      d_next = d_after;
+      e_next = (i + 1 < n && lane < d_next.cnt) ? p.elist[d_next.off + lane] : 0;
+      d_after = i + 2 < n ? p.tiles[tile_at(i + 2)] : none;
       const bool fresh = d.row0 != prow || d.g != pg;
-      const int qs = i & 1;
-      const int ent = lane < d.cnt ? elist[d.off + lane] : 0;
+      // publish the tile
+      const int is = i % kBmInfo;
       bool ok = true;
+      if (lane == 0) ok = mbar_wait(&sm.info_empty[is], ((i / kBmInfo) & 1) ^ 1, err, 706);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane < kBmEntries) sm.info[is].ent[lane] = ent;
+      if (lane == 0) {
+        sm.info[is].row0 = d.row0;
+        sm.info[is].g = d.g;
+        sm.info[is].cnt = d.cnt;
+        sm.info[is].fresh = fresh ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_full[is]);
+      const int qs = i & 1;
       if (lane == 0) {
         if (fresh) {
           const int s = nkf & 1;
@@ -458,17 +509,13 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         ok = ok && mbar_wait(&sm.q_empty[qs], ((i >> 1) & 1) ^ 1, err, 702);
         if (ok) mbar_expect_tx(&sm.q_full[qs], d.cnt * 2 * kBmQBox);
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        dead = true;
-        break;
-      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (lane < d.cnt) {
         const int t = ent / topk;
         tma_load_3d(sm.q[qs] + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.q_full[qs]);
         tma_load_3d(sm.q[qs] + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.q_full[qs]);
       }
       __syncwarp();
-      ++i;
       if (fresh) {
         prow = d.row0;
         pg = d.g;
@@ -483,7 +530,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) {
-          dead = true;
+          ++i;  // this tile's Q copies were issued
           break;
         }
       }
@@ -502,18 +549,14 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   } else if (warp == 5) {
     // ---------------- MMA issuer: S(i) then O(i-1) ----------------
     if (lane == 0) {
-      int i = 0, nk = 0, ks = 0, prow = -1, pg = -1;    // S side
-      int nv = 0, vs = 0, vrow = -1, vg = -1;           // O side
-      bool dead = false;
-      BmTile pend{0, 0, 0, 0};
-      auto issue_o = [&](const BmTile& d, int i2) {
-        if (d.row0 != vrow || d.g != vg) {
+      int nk = 0, ks = 0, nv = 0, vs = 0;
+      bool dead = false, pend_fresh = false;
+      auto issue_o = [&](bool fresh, int i2) {
+        if (fresh) {
           if (nv > 0) tc::commit(&sm.v_empty[vs]);
           vs = nv & 1;
           if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) return false;
           ++nv;
-          vrow = d.row0;
-          vg = d.g;
         }
         const int ob = i2 & 1;
         if (!mbar_wait(&sm.p_full, i2 & 1, err, 714)) return false;
@@ -529,10 +572,16 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         tc::commit(&sm.p_empty);
         return true;
       };
-      BM_FOR_EACH_TILE(tau) {
-        if (dead) break;
-        const BmTile d = tiles[tau];
-        if (d.row0 != prow || d.g != pg) {
+      int i = 0;
+      for (; i < n; ++i) {
+        const int is = i % kBmInfo;
+        if (!mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 717)) {
+          dead = true;
+          break;
+        }
+        const bool fresh = sm.info[is].fresh != 0;
+        mbar_arrive(&sm.info_empty[is]);
+        if (fresh) {
           if (nk > 0) tc::commit(&sm.k_empty[ks]);
           ks = nk & 1;
           if (!mbar_wait(&sm.k_full[ks], (nk >> 1) & 1, err, 710)) {
@@ -540,8 +589,6 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             break;
           }
           ++nk;
-          prow = d.row0;
-          pg = d.g;
         }
         const int qs = i & 1, sb = i & 1;
         if (!mbar_wait(&sm.q_full[qs], (i >> 1) & 1, err, 711) ||
@@ -558,119 +605,149 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         }
         tc::commit(&sm.s_full[sb]);
         tc::commit(&sm.q_empty[qs]);
-        if (i > 0 && !issue_o(pend, i - 1)) {
+        if (i > 0 && !issue_o(pend_fresh, i - 1)) {
           dead = true;
           break;
         }
-        pend = d;
-        ++i;
+        pend_fresh = fresh;
       }
-      if (!dead && i > 0) issue_o(pend, i - 1);
+      if (!dead && i > 0) issue_o(pend_fresh, i - 1);
       // every MMA has finished before tensor memory is released
       tc::commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 716);
     }
-  } else {
-    // ---------------- warps 0-3: softmax of tile i, epilogue of tile i-1 ----------------
+  } else if (warp < 4) {
+    // ---------------- warps 0-3: softmax, one query row per thread ----------------
     const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const uint32_t pbase = smem_u32(sm.p);
     const long long per_head = T * topk;
-    int i = 0;
-    bool dead = false, pvalid = false;
-    long long pslot = 0;
-    float pm = 0.f, pl = 0.f;
-    auto epilogue = [&](int i2) {
-      const int ob = i2 & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[ob], (i2 >> 1) & 1, err, 722))) return false;
+    for (int i = 0; i < n; ++i) {
+      const int is = i % kBmInfo;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 723))) break;
+      const int cnt = sm.info[is].cnt, row0 = sm.info[is].row0, g = sm.info[is].g;
+      const bool valid = e < cnt;
+      const int ent = valid ? sm.info[is].ent[e] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_empty[is]);
+      const long long t = ent / topk;
+      const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - row0 + 1)) : 0;
+      const int sb = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, err, 720))) break;
       tc::fence_after();
-      const float inv = pl > 0.f ? 1.f / pl : 0.f;
-      __half* orow = p.po + (pslot * kGroup + h) * kDim;
+      const uint32_t srow = lane_base + sb * 128;
+      // pass 1: row max over the causal keys (eight independent chains)
+      float m8[8];
 #pragma unroll
+      for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(srow + ch * 32, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          m8[q & 7] = fmaxf(m8[q & 7], ch * 32 + q < nkeys ? __uint_as_float(v[q]) : -INFINITY);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // scale > 0, so the max of the scaled scores is the scaled max
+      const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
+      // pass 2: p = 2^(s * scale * log2 e - mu), bf16 into the P tile, fp32 row sum
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty, (i & 1) ^ 1, err, 721))) break;
+      float l8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(srow + ch * 32, v);
+        tc::wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int k = ch * 32 + 2 * q;
+          const float a = k < nkeys ? ex2(fmaf(__uint_as_float(v[2 * q]), scale_log2, -mu)) : 0.f;
+          const float b = k + 1 < nkeys ? ex2(fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -mu)) : 0.f;
+          l8[q & 7] += a + b;
+          pk[q] = pack_bf16(a, b);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte P row
+          sts128(pbase + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                 pk[4 * c + 3]);
+        }
+      }
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      tc::fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.s_free[sb]);
+        mbar_arrive(&sm.p_full);
+      }
+      if (valid) p.pml[(static_cast<long long>(g) * per_head + ent) * kGroup + h] = make_float2(mu, l);
+    }
+  } else {
+    // ---------------- warps 6-9: epilogue, O / 128 as fp16 partials ----------------
+    // Lane pairs swap 16-byte pieces so that every store fills whole 32-byte
+    // sectors: the even lane writes the first half of a sector, the odd lane the
+    // second, for both rows of the pair in turn.
+    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter.. are this warp's rows
+    const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
+    const bool odd = lane & 1;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const long long per_head = T * topk;
+    for (int i = 0; i < n; ++i) {
+      const int is = i % kBmInfo;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 724))) break;
+      const int cnt = sm.info[is].cnt, g = sm.info[is].g;
+      const bool valid = e < cnt;
+      const int ent = valid ? sm.info[is].ent[e] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_empty[is]);
+      const int ob = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[ob], (i >> 1) & 1, err, 722))) break;
+      tc::fence_after();
+      // this lane's row, and the even row of its pair
+      __half* own = p.po + ((static_cast<long long>(g) * per_head + ent) * kGroup + h) * kDim;
+      __half* pair_even = odd ? own - kDim : own;
+#pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
         tc::ld_32x32b_x32(lane_base + 256 + ob * 128 + ch * 32, v);
         tc::wait_ld();
-        if (pvalid) {
+        uint32_t u[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_half2(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-            u.y = pack_half2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-            u.z = pack_half2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-            u.w = pack_half2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + ch * 32 + q * 8) = u;
+        for (int k = 0; k < 16; ++k)
+          u[k] = pack_half2(__uint_as_float(v[2 * k]) * (1.f / 128.f), __uint_as_float(v[2 * k + 1]) * (1.f / 128.f));
+        uint32_t x[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          x[q] = __shfl_xor_sync(0xffffffffu, odd ? u[q] : u[4 + q], 1);
+          x[4 + q] = __shfl_xor_sync(0xffffffffu, odd ? u[8 + q] : u[12 + q], 1);
+        }
+        if (valid) {
+          __half* a = pair_even + ch * 32;  // even row of the pair, this chunk
+          __half* b = a + kDim;             // odd row
+          if (!odd) {
+            stg128(a, u[0], u[1], u[2], u[3]);
+            stg128(a + 16, u[8], u[9], u[10], u[11]);
+            stg128(b, x[0], x[1], x[2], x[3]);
+            stg128(b + 16, x[4], x[5], x[6], x[7]);
+          } else {
+            stg128(a + 8, x[0], x[1], x[2], x[3]);
+            stg128(a + 24, x[4], x[5], x[6], x[7]);
+            stg128(b + 8, u[4], u[5], u[6], u[7]);
+            stg128(b + 24, u[12], u[13], u[14], u[15]);
           }
         }
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.o_free[ob]);
-      if (pvalid) p.pml[pslot * kGroup + h] = make_float2(pm, pl);
-      return true;
-    };
-    BM_FOR_EACH_TILE(tau) {
-      if (dead) break;
-      const BmTile d = tiles[tau];
-      const bool valid = e < d.cnt;
-      const int ent = valid ? elist[d.off + e] : 0;
-      const long long t = ent / topk;
-      const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - d.row0 + 1)) : 0;
-      const int sb = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, err, 720))) {
-        dead = true;
-        break;
-      }
-      tc::fence_after();
-      float s[128];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(lane_base + sb * 128 + ch * 32, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; ++q) s[ch * 32 + q] = __uint_as_float(v[q]);
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.s_free[sb]);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        s[k] = k < nkeys ? s[k] * scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[k]);
-      }
-      const float mu = mx == -INFINITY ? 0.f : mx;
-      float l = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float a = exp2f(s[2 * k] - mu), b = exp2f(s[2 * k + 1] - mu);
-        l += a + b;
-        pk[k] = pack_bf16(a, b);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty, (i & 1) ^ 1, err, 721))) {
-        dead = true;
-        break;
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        sts128(pbase + (c >> 3) * kBmHalf + sw128(r, c & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-               pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full);
-      if (i > 0 && !epilogue(i - 1)) {
-        dead = true;
-        break;
-      }
-      pvalid = valid;
-      pslot = static_cast<long long>(d.g) * per_head + ent;
-      pm = mx;
-      pl = l;
-      ++i;
     }
-    if (!dead && i > 0) epilogue(i - 1);
   }
   tc::fence_before();
   __syncthreads();
@@ -679,9 +756,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     tc::dealloc(tmem, 512);
   }
 }
-#undef BM_FOR_EACH_TILE
 
-// One 256-thread block per (token, KV head): combines the token's partials.
+// One 256-thread block per (token, KV head): combines the token's partials
+// out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, M = max_j m_j.
 // Thread (h, c) owns dims 8c..8c+7 of head h of the group.
 __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict__ q2k,
                                                        const int32_t* __restrict__ cu, int num_docs, long long T,
@@ -704,8 +781,9 @@ __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict
   for (unsigned m = ok; m; m &= m - 1) {
     const long long slot = e0 + __ffs(m) - 1;
     const float2 ml = p.pml[slot * kGroup + h];
-    const float w = ml.y * exp2f(ml.x - Mu);
-    L += w;
+    const float f = exp2f(ml.x - Mu);
+    L += ml.y * f;
+    const float w = 128.f * f;  // the partial holds O / 128, O unnormalised
     const uint4 u = *reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c);
     const __half2* hv = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
