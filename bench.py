@@ -397,7 +397,9 @@ def main():
         sel_r = b_sel / (res["sel_ms"] * 1e-3) / 1e9
         att_r = b_att / (res["att_ms"] * 1e-3) / 1e9
         ach = sel_r if dom == "select" else att_r
-        roof = {"bound": "hbm", "kernel": "decode_select_kernel" if dom == "select" else "sparse_attend_kernel",
+        roof = {"bound": "hbm",
+                "kernel": ("msa_select_blocks_decode (decode_select_kernel + decode_topk_kernel)" if dom == "select"
+                           else "msa_sparse_attend_decode (sparse_attend_kernel)"),
                 "achieved": round(ach, 1), "peak": res["hbm_peak"], "unit": "GB/s",
                 "frac": round(ach / res["hbm_peak"], 4), "traffic": None,
                 "peak_source": res["peak_src"] + " hbm_gbs (copy, burst)",
@@ -410,7 +412,9 @@ def main():
         sel_r = f_sel / (res["sel_ms"] * 1e-3) / 1e12
         att_r = f_att / (res["att_ms"] * 1e-3) / 1e12
         ach = sel_r if dom == "select" else att_r
-        roof = {"bound": "tensor", "kernel": "prefill_select_kernel" if dom == "select" else "sparse_attend_kernel",
+        roof = {"bound": "tensor",
+                "kernel": ("msa_select_blocks_prefill (prefill_plan_kernel + prefill_select_kernel)" if dom == "select"
+                           else "msa_sparse_attend_prefill (bucketing, bm_attend_kernel, bm_merge_kernel)"),
                 "achieved": round(ach, 2), "peak": res["tf_peak"], "unit": "TFLOP/s",
                 "frac": round(ach / res["tf_peak"], 4), "traffic": None,
                 "peak_source": res["peak_src"] + " bf16_tflops (burst)",
@@ -427,7 +431,9 @@ def main():
             "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config, "roofline": roof,
             "e2e": {"value": round(e2e, 1), "unit": unit, "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": 3 * args.steps, "clocks": res["clocks"]}
+            # decode: scorer + top-k + attention; prefill: plan + scorer, then geometry, count, scan,
+            # tiles, scatter, tensor-core attention and merge
+            "gpu_launches": (3 if res["decode"] else 9) * args.steps, "clocks": res["clocks"]}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
     print(json.dumps(line))

@@ -19,18 +19,20 @@
 //   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 to shared memory)
 //   O = P V     (A = P, B = V read MN-major straight from the TMA tile)
 //
-// with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 4
+// with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 16
 // schedules the tiles (descriptors and entries read ahead from global memory,
 // published in a shared-memory ring) and issues TMA (Q rows gathered with a
 // 3-D tensor map, one 16-head box per entry; K and V blocks as 128-row boxes);
-// warp 5 issues the MMAs from one thread; warps 0-3 run the softmax with one
-// tensor-memory lane (query row) per thread; warps 6-9 move O out of tensor
-// memory.  Each entry's result is written as a partial: row max (log2 units)
-// and row sum of p in fp32, and the unnormalised O / 128 in fp16; a merge
-// kernel combines the <= topk partials of a (query, KV head) pair into the
-// bf16 output.  Tiles are handed out in chunks of 4, round-robin over the
-// persistent grid, so all CTAs move through the (KV head, window) buckets
-// together and the window's Q rows and K / V blocks stay in L2.
+// warp 17 issues the MMAs from one thread.  Two softmax warpgroups (warps 0-7)
+// and two epilogue warpgroups (warps 8-15) take the even and the odd tiles, so
+// two tiles are in their softmax and two in their epilogue at a time; in each,
+// a thread owns one tensor-memory lane (query row).  Each entry's result is
+// written as a partial: row max (log2 units) and row sum of p in fp32, and the
+// unnormalised O / 128 in fp16; a merge kernel combines the <= topk partials
+// of a (query, KV head) pair into the bf16 output.  Tiles are handed out in
+// chunks of 4, round-robin over the persistent grid, so all CTAs move through
+// the (KV head, window) buckets together and the window's Q rows and K / V
+// blocks stay in L2.
 #include <cuda_fp16.h>
 
 #include "launch.h"
@@ -41,7 +43,11 @@ constexpr int kBmEntries = 8;                     // entries per tile (8 x 16 he
 constexpr int kBmHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16) = 16 KB
 constexpr int kBmTile = 2 * kBmHalf;              // a 128 x 128 bf16 operand
 constexpr int kBmQBox = kGroup * 128;             // one entry's 16 rows x 64 dims = 2 KB
-constexpr int kBmThreads = 320;                   // warps 0-3 softmax, 4 TMA, 5 MMA, 6-9 epilogue
+// warps 0-7 softmax (two warpgroups, even / odd tiles), 8-15 epilogue (two
+// warpgroups), 16 TMA and scheduling, 17 MMA
+constexpr int kBmThreads = 576;
+constexpr int kBmProducerWarp = 16;
+constexpr int kBmMmaWarp = 17;
 constexpr int kBmChunk = 4;                       // tiles per scheduling chunk
 constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
@@ -60,14 +66,16 @@ struct BmInfo {
 };
 constexpr int kBmInfo = 8;  // info ring slots
 
+// Q, V and P double-buffered, K single (a K block is released as soon as the
+// S MMAs of its last tile finish, well before V).
 struct BmSmem {
   alignas(1024) uint8_t q[2][kBmTile];
-  alignas(1024) uint8_t k[2][kBmTile];
+  alignas(1024) uint8_t k[kBmTile];
   alignas(1024) uint8_t v[2][kBmTile];
-  alignas(1024) uint8_t p[kBmTile];
-  uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+  alignas(1024) uint8_t p[2][kBmTile];
+  uint64_t q_full[2], q_empty[2], k_full, k_empty, v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  uint64_t p_full, p_empty, done;
+  uint64_t p_full[2], p_empty[2], done;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -424,25 +432,25 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
-      mbar_init(&sm.k_full[i], 1);
-      mbar_init(&sm.k_empty[i], 1);
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 4);
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 4);
+      mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_empty[i], 1);
     }
+    mbar_init(&sm.k_full, 1);
+    mbar_init(&sm.k_empty, 1);
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
-      mbar_init(&sm.info_empty[i], 9);  // four softmax warps, the MMA thread, four epilogue warps
+      mbar_init(&sm.info_empty[i], 9);  // the tile's softmax and epilogue warpgroups, the MMA thread
     }
-    mbar_init(&sm.p_full, 4);
-    mbar_init(&sm.p_empty, 1);
     mbar_init(&sm.done, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kBmMmaWarp) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
   }
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   // A wait that gives up (recorded in the error word) marks the role dead: it
   // stops issuing work, so a broken pipeline ends after one bounded wait per
   // role instead of one per tile.
-  if (warp == 4) {
+  if (warp == kBmProducerWarp) {
     // ---------------- scheduler + TMA producer ----------------
     // Reads each tile's descriptor and entries from global memory one and two
     // tiles ahead, publishes them in the info ring, then issues K of a new
@@ -497,12 +505,11 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const int qs = i & 1;
       if (lane == 0) {
         if (fresh) {
-          const int s = nkf & 1;
-          ok = mbar_wait(&sm.k_empty[s], ((nkf >> 1) & 1) ^ 1, err, 700);
+          ok = mbar_wait(&sm.k_empty, (nkf & 1) ^ 1, err, 700);
           if (ok) {
-            mbar_expect_tx(&sm.k_full[s], kBmTile);
-            tma_load_3d(sm.k[s], &kmap, 0, d.g, d.row0, &sm.k_full[s]);
-            tma_load_3d(sm.k[s] + kBmHalf, &kmap, 64, d.g, d.row0, &sm.k_full[s]);
+            mbar_expect_tx(&sm.k_full, kBmTile);
+            tma_load_3d(sm.k, &kmap, 0, d.g, d.row0, &sm.k_full);
+            tma_load_3d(sm.k + kBmHalf, &kmap, 64, d.g, d.row0, &sm.k_full);
             ++nkf;
           }
         }
@@ -537,19 +544,18 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
     // no copy may still be landing when the CTA exits: wait for the last fill of every stage
     if (lane == 0) {
+      if (nkf > 0) mbar_wait(&sm.k_full, (nkf - 1) & 1, err, 704);
       for (int q = 0; q < 2; ++q) {
         const int fq = (i - q + 1) / 2;  // fills of Q stage q
         if (fq > 0) mbar_wait(&sm.q_full[q], (fq - 1) & 1, err, 703);
-        const int fk = (nkf - q + 1) / 2;
-        if (fk > 0) mbar_wait(&sm.k_full[q], (fk - 1) & 1, err, 704);
         const int fv = (nvf - q + 1) / 2;
         if (fv > 0) mbar_wait(&sm.v_full[q], (fv - 1) & 1, err, 705);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kBmMmaWarp) {
     // ---------------- MMA issuer: S(i) then O(i-1) ----------------
     if (lane == 0) {
-      int nk = 0, ks = 0, nv = 0, vs = 0;
+      int nk = 0, nv = 0, vs = 0;
       bool dead = false, pend_fresh = false;
       auto issue_o = [&](bool fresh, int i2) {
         if (fresh) {
@@ -558,18 +564,18 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) return false;
           ++nv;
         }
-        const int ob = i2 & 1;
-        if (!mbar_wait(&sm.p_full, i2 & 1, err, 714)) return false;
-        if (!mbar_wait(&sm.o_free[ob], ((i2 >> 1) & 1) ^ 1, err, 715)) return false;
+        const int b = i2 & 1;
+        if (!mbar_wait(&sm.p_full[b], (i2 >> 1) & 1, err, 714)) return false;
+        if (!mbar_wait(&sm.o_free[b], ((i2 >> 1) & 1) ^ 1, err, 715)) return false;
         tc::fence_after();
-        const uint32_t pa = smem_u32(sm.p), va = smem_u32(sm.v[vs]);
-        const uint32_t dt = tmem + 256 + ob * 128;
+        const uint32_t pa = smem_u32(sm.p[b]), va = smem_u32(sm.v[vs]);
+        const uint32_t dt = tmem + 256 + b * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc::mma_bf16(dt, tc::desc_k_sw128(pa + (kk >> 2) * kBmHalf + (kk & 3) * 32),
                        desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
-        tc::commit(&sm.o_full[ob]);
-        tc::commit(&sm.p_empty);
+        tc::commit(&sm.o_full[b]);
+        tc::commit(&sm.p_empty[b]);
         return true;
       };
       int i = 0;
@@ -582,29 +588,28 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         const bool fresh = sm.info[is].fresh != 0;
         mbar_arrive(&sm.info_empty[is]);
         if (fresh) {
-          if (nk > 0) tc::commit(&sm.k_empty[ks]);
-          ks = nk & 1;
-          if (!mbar_wait(&sm.k_full[ks], (nk >> 1) & 1, err, 710)) {
+          if (nk > 0) tc::commit(&sm.k_empty);
+          if (!mbar_wait(&sm.k_full, nk & 1, err, 710)) {
             dead = true;
             break;
           }
           ++nk;
         }
-        const int qs = i & 1, sb = i & 1;
-        if (!mbar_wait(&sm.q_full[qs], (i >> 1) & 1, err, 711) ||
-            !mbar_wait(&sm.s_free[sb], ((i >> 1) & 1) ^ 1, err, 712)) {
+        const int b = i & 1;
+        if (!mbar_wait(&sm.q_full[b], (i >> 1) & 1, err, 711) ||
+            !mbar_wait(&sm.s_free[b], ((i >> 1) & 1) ^ 1, err, 712)) {
           dead = true;
           break;
         }
         tc::fence_after();
-        const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k[ks]);
+        const uint32_t qa = smem_u32(sm.q[b]), ka = smem_u32(sm.k);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + sb * 128, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kBmIdescS, kk > 0);
+          tc::mma_bf16(tmem + b * 128, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kBmIdescS, kk > 0);
         }
-        tc::commit(&sm.s_full[sb]);
-        tc::commit(&sm.q_empty[qs]);
+        tc::commit(&sm.s_full[b]);
+        tc::commit(&sm.q_empty[b]);
         if (i > 0 && !issue_o(pend_fresh, i - 1)) {
           dead = true;
           break;
@@ -616,14 +621,16 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       tc::commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 716);
     }
-  } else if (warp < 4) {
-    // ---------------- warps 0-3: softmax, one query row per thread ----------------
-    const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t pbase = smem_u32(sm.p);
+  } else if (warp < 8) {
+    // ---------------- warps 0-7: softmax, one query row per thread ----------------
+    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (S and P buffer wg).
+    const int wg = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
+    const uint32_t srow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 128;
+    const uint32_t pbase = smem_u32(sm.p[wg]);
     const long long per_head = T * topk;
-    for (int i = 0; i < n; ++i) {
-      const int is = i % kBmInfo;
+    for (int i = wg; i < n; i += 2) {
+      const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 723))) break;
       const int cnt = sm.info[is].cnt, row0 = sm.info[is].row0, g = sm.info[is].g;
       const bool valid = e < cnt;
@@ -632,10 +639,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       const long long t = ent / topk;
       const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - row0 + 1)) : 0;
-      const int sb = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (i >> 1) & 1, err, 720))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, 720))) break;
       tc::fence_after();
-      const uint32_t srow = lane_base + sb * 128;
       // pass 1: row max over the causal keys (eight independent chains)
       float m8[8];
 #pragma unroll
@@ -654,7 +659,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       // scale > 0, so the max of the scaled scores is the scaled max
       const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
       // pass 2: p = 2^(s * scale * log2 e - mu), bf16 into the P tile, fp32 row sum
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty, (i & 1) ^ 1, err, 721))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty[wg], (k & 1) ^ 1, err, 721))) break;
       float l8[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) l8[q] = 0.f;
@@ -666,9 +671,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         uint32_t pk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const int k = ch * 32 + 2 * q;
-          const float a = k < nkeys ? ex2(fmaf(__uint_as_float(v[2 * q]), scale_log2, -mu)) : 0.f;
-          const float b = k + 1 < nkeys ? ex2(fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -mu)) : 0.f;
+          const int kc = ch * 32 + 2 * q;
+          const float a = ex2(kc < nkeys ? fmaf(__uint_as_float(v[2 * q]), scale_log2, -mu) : -INFINITY);
+          const float b = ex2(kc + 1 < nkeys ? fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -mu) : -INFINITY);
           l8[q & 7] += a + b;
           pk[q] = pack_bf16(a, b);
         }
@@ -684,31 +689,31 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sm.s_free[sb]);
-        mbar_arrive(&sm.p_full);
+        mbar_arrive(&sm.s_free[wg]);
+        mbar_arrive(&sm.p_full[wg]);
       }
       if (valid) p.pml[(static_cast<long long>(g) * per_head + ent) * kGroup + h] = make_float2(mu, l);
     }
   } else {
-    // ---------------- warps 6-9: epilogue, O / 128 as fp16 partials ----------------
-    // Lane pairs swap 16-byte pieces so that every store fills whole 32-byte
+    // ---------------- warps 8-15: epilogue, O / 128 as fp16 partials ----------------
+    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Lane
+    // pairs swap 16-byte pieces so that every store fills whole 32-byte
     // sectors: the even lane writes the first half of a sector, the odd lane the
     // second, for both rows of the pair in turn.
-    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter.. are this warp's rows
+    const int wg = (warp - 8) >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
     const bool odd = lane & 1;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
     const long long per_head = T * topk;
-    for (int i = 0; i < n; ++i) {
-      const int is = i % kBmInfo;
+    for (int i = wg; i < n; i += 2) {
+      const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 724))) break;
       const int cnt = sm.info[is].cnt, g = sm.info[is].g;
       const bool valid = e < cnt;
       const int ent = valid ? sm.info[is].ent[e] : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
-      const int ob = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[ob], (i >> 1) & 1, err, 722))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
       tc::fence_after();
       // this lane's row, and the even row of its pair
       __half* own = p.po + ((static_cast<long long>(g) * per_head + ent) * kGroup + h) * kDim;
@@ -716,12 +721,12 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
-        tc::ld_32x32b_x32(lane_base + 256 + ob * 128 + ch * 32, v);
+        tc::ld_32x32b_x32(orow + ch * 32, v);
         tc::wait_ld();
         uint32_t u[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          u[k] = pack_half2(__uint_as_float(v[2 * k]) * (1.f / 128.f), __uint_as_float(v[2 * k + 1]) * (1.f / 128.f));
+        for (int q = 0; q < 16; ++q)
+          u[q] = pack_half2(__uint_as_float(v[2 * q]) * (1.f / 128.f), __uint_as_float(v[2 * q + 1]) * (1.f / 128.f));
         uint32_t x[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -746,12 +751,12 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      if (lane == 0) mbar_arrive(&sm.o_free[wg]);
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBmMmaWarp) {
     tc::fence_after();
     tc::dealloc(tmem, 512);
   }
@@ -769,28 +774,36 @@ __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict
   const int d = doc_of(cu, num_docs, t);
   const int nb = static_cast<int>(t - cu[d]) / kBlock + 1;
   const long long e0 = (static_cast<long long>(g) * T + t) * topk;
-  unsigned ok = 0;
-  for (int j = 0; j < topk; ++j) {
-    const int b = q2k[e0 + j];
-    if (b >= 0 && b < nb) ok |= 1u << j;
+  // all of the token's partials are requested before any is used
+  float2 ml[kMaxTopk];
+  uint4 u[kMaxTopk];
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    const int b = j < topk ? q2k[e0 + j] : -1;
+    ml[j] = make_float2(-INFINITY, 0.f);
+    u[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (b >= 0 && b < nb) {
+      const long long slot = e0 + j;
+      ml[j] = p.pml[slot * kGroup + h];
+      u[j] = __ldcs(reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c));
+    }
   }
   float M = -INFINITY;
-  for (unsigned m = ok; m; m &= m - 1) M = fmaxf(M, p.pml[(e0 + __ffs(m) - 1) * kGroup + h].x);
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) M = fmaxf(M, ml[j].x);
   const float Mu = M == -INFINITY ? 0.f : M;
   float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (unsigned m = ok; m; m &= m - 1) {
-    const long long slot = e0 + __ffs(m) - 1;
-    const float2 ml = p.pml[slot * kGroup + h];
-    const float f = exp2f(ml.x - Mu);
-    L += ml.y * f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    const float f = exp2f(ml[j].x - Mu);  // 0 for a skipped entry
+    L += ml[j].y * f;
     const float w = 128.f * f;  // the partial holds O / 128, O unnormalised
-    const uint4 u = *reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c);
-    const __half2* hv = reinterpret_cast<const __half2*>(&u);
+    const __half2* hv = reinterpret_cast<const __half2*>(&u[j]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float2 f = __half22float2(hv[q]);
-      acc[2 * q] += w * f.x;
-      acc[2 * q + 1] += w * f.y;
+      const float2 x = __half22float2(hv[q]);
+      acc[2 * q] += w * x.x;
+      acc[2 * q + 1] += w * x.y;
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
