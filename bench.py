@@ -69,6 +69,24 @@ def decode_work(d, q2k):
     return b_sel, b_att
 
 
+# DRAM traffic of the dominant kernel(s) per unit of work, from one ncu capture of a
+# smaller case of the same workload (profiles/), scaled by the units of a full launch.
+# Set to None when the kernels change after the capture.
+TRAFFIC = {
+    # decode_select_kernel<bf16> + scores, first 16 requests: 147.1 MB DRAM / 143.7 MB algorithmic
+    "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0235,
+                                   "capture": "profiles/decode_b64_ctx4k_64k_paged.md"},
+    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.10 GB DRAM / 462848 entries
+    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8858.0,
+                         "capture": "profiles/bm_attend_merge_prefill_1doc_8k.md"},
+}
+
+
+def prefill_entries(q2k):
+    """Selected (query, KV head, block) triples: the units of the block-major attention."""
+    return int((q2k >= 0).sum().item())
+
+
 def prefill_work(p, q2k):
     """(flops_select, flops_attend): causal valid index pairs x 4 heads x 2*128;
     selected causal keys x 16 heads x 4*128 (QK^T and PV)."""
@@ -148,7 +166,8 @@ def run_gpu(args, rank, world, device):
     import block_sparse_attention_08_gb300 as msa
     torch.cuda.set_device(device)
     name = args.workload
-    inp = msa_synth.workload(name, seed=args.seed + rank, device=device, max_requests=args.requests)
+    inp = msa_synth.workload(name, seed=args.seed + rank, device=device, max_requests=args.requests,
+                            scale_down=args.scale_down)
     decode = name.startswith("decode")
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
@@ -195,6 +214,7 @@ def run_gpu(args, rank, world, device):
         flush_l2(1)
     torch.cuda.synchronize()
     work = decode_work(inp, q2k) if decode else prefill_work(inp, q2k)
+    entries = 0 if decode else prefill_entries(q2k)
 
     # The timed steps replay CUDA graphs of the two C-ABI calls (captured once,
     # same buffers), so host submission cost does not leak into device time.
@@ -278,7 +298,7 @@ def run_gpu(args, rank, world, device):
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
     return dict(ms=ms, sel_ms=sum(t_sel) / len(t_sel), att_ms=sum(t_att) / len(t_att),
-                e2e_ms=sum(e_ms) / len(e_ms), n_queries=n_queries, work=work, h2d=h2d, d2h=d2h,
+                e2e_ms=sum(e_ms) / len(e_ms), n_queries=n_queries, work=work, entries=entries, h2d=h2d, d2h=d2h,
                 clocks=clk.summary(), decode=decode, hbm_peak=hbm_peak, tf_peak=tf_peak, peak_src=peak_src)
 
 
@@ -348,6 +368,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager C-ABI calls instead of graph replays")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="divide the workload's lengths by this factor (small profiling cases)")
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of a decode workload (small profiling cases)")
     args = ap.parse_args()
@@ -363,6 +385,8 @@ def main():
     config = {"workload": args.workload, "desc": msa_synth.WORKLOADS[args.workload], "seed": args.seed}
     if args.requests:
         config["requests"] = args.requests
+    if args.scale_down > 1:
+        config["scale_down"] = args.scale_down
 
     if args.impl == "reference":
         if rank == 0:
@@ -397,11 +421,16 @@ def main():
         sel_r = b_sel / (res["sel_ms"] * 1e-3) / 1e9
         att_r = b_att / (res["att_ms"] * 1e-3) / 1e9
         ach = sel_r if dom == "select" else att_r
+        tr = TRAFFIC.get(args.workload) if args.requests is None and args.scale_down == 1 else None
+        traffic = None
+        if tr and tr["kernel"] == dom:
+            traffic = round(tr["value"] * (b_sel if dom == "select" else b_att))
         roof = {"bound": "hbm",
                 "kernel": ("msa_select_blocks_decode (decode_select_kernel + decode_topk_kernel)" if dom == "select"
                            else "msa_sparse_attend_decode (sparse_attend_kernel)"),
                 "achieved": round(ach, 1), "peak": res["hbm_peak"], "unit": "GB/s",
-                "frac": round(ach / res["hbm_peak"], 4), "traffic": None,
+                "frac": round(ach / res["hbm_peak"], 4), "traffic": traffic,
+                "traffic_source": tr["capture"] + " (scaled by algorithmic bytes)" if traffic else None,
                 "peak_source": res["peak_src"] + " hbm_gbs (copy, burst)",
                 "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "bytes": b_sel, "GB/s": round(sel_r, 1)},
                                "attend": {"ms": round(res["att_ms"], 4), "bytes": b_att, "GB/s": round(att_r, 1)},
@@ -412,11 +441,16 @@ def main():
         sel_r = f_sel / (res["sel_ms"] * 1e-3) / 1e12
         att_r = f_att / (res["att_ms"] * 1e-3) / 1e12
         ach = sel_r if dom == "select" else att_r
+        tr = TRAFFIC.get(args.workload) if args.scale_down == 1 else None
+        traffic = None
+        if tr and tr["kernel"] == dom:
+            traffic = round(tr["value"] * res["entries"])
         roof = {"bound": "tensor",
                 "kernel": ("msa_select_blocks_prefill (prefill_plan_kernel + prefill_select_kernel)" if dom == "select"
                            else "msa_sparse_attend_prefill (bucketing, bm_attend_kernel, bm_merge_kernel)"),
                 "achieved": round(ach, 2), "peak": res["tf_peak"], "unit": "TFLOP/s",
-                "frac": round(ach / res["tf_peak"], 4), "traffic": None,
+                "frac": round(ach / res["tf_peak"], 4), "traffic": traffic,
+                "traffic_source": tr["capture"] + " (scaled by entries)" if traffic else None,
                 "peak_source": res["peak_src"] + " bf16_tflops (burst)",
                 "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "flop": f_sel, "TFLOP/s": round(sel_r, 2)},
                                "attend": {"ms": round(res["att_ms"], 4), "flop": f_att, "TFLOP/s": round(att_r, 2)},
