@@ -35,6 +35,8 @@
 // blocks stay in L2.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "launch.h"
 
 namespace msa {
@@ -44,10 +46,11 @@ constexpr int kBmHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf
 constexpr int kBmTile = 2 * kBmHalf;              // a 128 x 128 bf16 operand
 constexpr int kBmQBox = kGroup * 128;             // one entry's 16 rows x 64 dims = 2 KB
 // warps 0-7 softmax (two warpgroups, even / odd tiles), 8-15 epilogue (two
-// warpgroups), 16 TMA and scheduling, 17 MMA
-constexpr int kBmThreads = 576;
+// warpgroups), 16 TMA and scheduling, 17 the S MMAs, 18 the O MMAs
+constexpr int kBmThreads = 608;
 constexpr int kBmProducerWarp = 16;
-constexpr int kBmMmaWarp = 17;
+constexpr int kBmMmaSWarp = 17;
+constexpr int kBmMmaOWarp = 18;
 constexpr int kBmChunk = 4;                       // tiles per scheduling chunk
 constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
@@ -75,7 +78,7 @@ struct BmSmem {
   alignas(1024) uint8_t p[2][kBmTile];
   uint64_t q_full[2], q_empty[2], k_full, k_empty, v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  uint64_t p_full[2], p_empty[2], done;
+  uint64_t p_full[2], p_empty[2], done_s, done_o;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -445,12 +448,13 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     mbar_init(&sm.k_empty, 1);
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
-      mbar_init(&sm.info_empty[i], 9);  // the tile's softmax and epilogue warpgroups, the MMA thread
+      mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
     }
-    mbar_init(&sm.done, 1);
+    mbar_init(&sm.done_s, 1);
+    mbar_init(&sm.done_o, 1);
     fence_mbar_init();
   }
-  if (warp == kBmMmaWarp) {
+  if (warp == kBmMmaSWarp) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
   }
@@ -552,55 +556,26 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         if (fv > 0) mbar_wait(&sm.v_full[q], (fv - 1) & 1, err, 705);
       }
     }
-  } else if (warp == kBmMmaWarp) {
-    // ---------------- MMA issuer: S(i) then O(i-1) ----------------
+  } else if (warp == kBmMmaSWarp) {
+    // ---------------- S MMAs: S(i) = Q K^T into tensor-memory buffer i % 2 ----------------
+    // Issued independently of the O MMAs (another warp), so an S tile never
+    // waits behind the P of an earlier tile.
     if (lane == 0) {
-      int nk = 0, nv = 0, vs = 0;
-      bool dead = false, pend_fresh = false;
-      auto issue_o = [&](bool fresh, int i2) {
-        if (fresh) {
-          if (nv > 0) tc::commit(&sm.v_empty[vs]);
-          vs = nv & 1;
-          if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) return false;
-          ++nv;
-        }
-        const int b = i2 & 1;
-        if (!mbar_wait(&sm.p_full[b], (i2 >> 1) & 1, err, 714)) return false;
-        if (!mbar_wait(&sm.o_free[b], ((i2 >> 1) & 1) ^ 1, err, 715)) return false;
-        tc::fence_after();
-        const uint32_t pa = smem_u32(sm.p[b]), va = smem_u32(sm.v[vs]);
-        const uint32_t dt = tmem + 256 + b * 128;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16(dt, tc::desc_k_sw128(pa + (kk >> 2) * kBmHalf + (kk & 3) * 32),
-                       desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
-        tc::commit(&sm.o_full[b]);
-        tc::commit(&sm.p_empty[b]);
-        return true;
-      };
-      int i = 0;
-      for (; i < n; ++i) {
+      int nk = 0;
+      for (int i = 0; i < n; ++i) {
         const int is = i % kBmInfo;
-        if (!mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 717)) {
-          dead = true;
-          break;
-        }
+        if (!mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 717)) break;
         const bool fresh = sm.info[is].fresh != 0;
         mbar_arrive(&sm.info_empty[is]);
         if (fresh) {
           if (nk > 0) tc::commit(&sm.k_empty);
-          if (!mbar_wait(&sm.k_full, nk & 1, err, 710)) {
-            dead = true;
-            break;
-          }
+          if (!mbar_wait(&sm.k_full, nk & 1, err, 710)) break;
           ++nk;
         }
         const int b = i & 1;
         if (!mbar_wait(&sm.q_full[b], (i >> 1) & 1, err, 711) ||
-            !mbar_wait(&sm.s_free[b], ((i >> 1) & 1) ^ 1, err, 712)) {
-          dead = true;
+            !mbar_wait(&sm.s_free[b], ((i >> 1) & 1) ^ 1, err, 712))
           break;
-        }
         tc::fence_after();
         const uint32_t qa = smem_u32(sm.q[b]), ka = smem_u32(sm.k);
 #pragma unroll
@@ -610,16 +585,42 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         }
         tc::commit(&sm.s_full[b]);
         tc::commit(&sm.q_empty[b]);
-        if (i > 0 && !issue_o(pend_fresh, i - 1)) {
-          dead = true;
-          break;
-        }
-        pend_fresh = fresh;
       }
-      if (!dead && i > 0) issue_o(pend_fresh, i - 1);
-      // every MMA has finished before tensor memory is released
-      tc::commit(&sm.done);
-      mbar_wait(&sm.done, 0, err, 716);
+      // every MMA of this thread has finished before tensor memory is released
+      tc::commit(&sm.done_s);
+      mbar_wait(&sm.done_s, 0, err, 716);
+    }
+  } else if (warp == kBmMmaOWarp) {
+    // ---------------- O MMAs: O(i) = P(i) V into tensor-memory buffer 2 + i % 2 ----------------
+    if (lane == 0) {
+      int nv = 0, vs = 0;
+      for (int i = 0; i < n; ++i) {
+        const int is = i % kBmInfo;
+        if (!mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 718)) break;
+        const bool fresh = sm.info[is].fresh != 0;
+        mbar_arrive(&sm.info_empty[is]);
+        if (fresh) {
+          if (nv > 0) tc::commit(&sm.v_empty[vs]);
+          vs = nv & 1;
+          if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) break;
+          ++nv;
+        }
+        const int b = i & 1;
+        if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, err, 714) ||
+            !mbar_wait(&sm.o_free[b], ((i >> 1) & 1) ^ 1, err, 715))
+          break;
+        tc::fence_after();
+        const uint32_t pa = smem_u32(sm.p[b]), va = smem_u32(sm.v[vs]);
+        const uint32_t dt = tmem + 256 + b * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(dt, tc::desc_k_sw128(pa + (kk >> 2) * kBmHalf + (kk & 3) * 32),
+                       desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
+        tc::commit(&sm.o_full[b]);
+        tc::commit(&sm.p_empty[b]);
+      }
+      tc::commit(&sm.done_o);
+      mbar_wait(&sm.done_o, 0, err, 719);
     }
   } else if (warp < 8) {
     // ---------------- warps 0-7: softmax, one query row per thread ----------------
@@ -641,50 +642,71 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - row0 + 1)) : 0;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, 720))) break;
       tc::fence_after();
-      // pass 1: row max over the causal keys (eight independent chains)
-      float m8[8];
+      // Rows whose keys are all causal (every block but the diagonal one) skip
+      // the per-key mask.  P is produced as p / 128 (the exponent is lowered by
+      // 7), so the O MMA writes O / 128 and the epilogue only converts.
+      const bool masked = !__all_sync(0xffffffffu, nkeys >= kBlock);
+      float mx = -INFINITY, l = 0.f;
+      auto softmax_rows = [&](auto mask_tag) -> bool {
+        constexpr bool kMask = decltype(mask_tag)::value;
+        // pass 1: row max (eight independent chains)
+        float m8[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+        for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(srow + ch * 32, v);
-        tc::wait_ld();
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(srow + ch * 32, v);
+          tc::wait_ld();
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          m8[q & 7] = fmaxf(m8[q & 7], ch * 32 + q < nkeys ? __uint_as_float(v[q]) : -INFINITY);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      // scale > 0, so the max of the scaled scores is the scaled max
-      const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
-      // pass 2: p = 2^(s * scale * log2 e - mu), bf16 into the P tile, fp32 row sum
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty[wg], (k & 1) ^ 1, err, 721))) break;
-      float l8[8];
+          for (int q = 0; q < 32; ++q) {
+            const float x = __uint_as_float(v[q]);
+            m8[q & 7] = fmaxf(m8[q & 7], (!kMask || ch * 32 + q < nkeys) ? x : -INFINITY);
+          }
+        }
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // scale > 0, so the max of the scaled scores is the scaled max
+        const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
+        const float shift = mu + 7.f;  // p / 128 = 2^(s * scale * log2 e - mu - 7)
+        // pass 2: bf16 p / 128 into the P tile, fp32 row sum
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty[wg], (k & 1) ^ 1, err, 721))) return false;
+        float l8[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+        for (int q = 0; q < 8; ++q) l8[q] = 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(srow + ch * 32, v);
-        tc::wait_ld();
-        uint32_t pk[16];
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(srow + ch * 32, v);
+          tc::wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int kc = ch * 32 + 2 * q;
-          const float a = ex2(kc < nkeys ? fmaf(__uint_as_float(v[2 * q]), scale_log2, -mu) : -INFINITY);
-          const float b = ex2(kc + 1 < nkeys ? fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -mu) : -INFINITY);
-          l8[q & 7] += a + b;
-          pk[q] = pack_bf16(a, b);
-        }
+          for (int q = 0; q < 16; ++q) {
+            const int kc = ch * 32 + 2 * q;
+            float xa = fmaf(__uint_as_float(v[2 * q]), scale_log2, -shift);
+            float xb = fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -shift);
+            if (kMask) {
+              xa = kc < nkeys ? xa : -INFINITY;
+              xb = kc + 1 < nkeys ? xb : -INFINITY;
+            }
+            const float pa = ex2(xa), pb = ex2(xb);
+            l8[q & 7] += pa + pb;
+            pk[q] = pack_bf16(pa, pb);
+          }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte P row
-          sts128(pbase + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                 pk[4 * c + 3]);
+          for (int c = 0; c < 4; ++c) {
+            const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte P row
+            sts128(pbase + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                   pk[4 * c + 3]);
+          }
         }
-      }
-      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+        l = 128.f * (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        mx = mu;
+        return true;
+      };
+      const bool ok = masked ? softmax_rows(std::true_type{}) : softmax_rows(std::false_type{});
+      if (!ok) break;
+      const float mu = mx;
       tc::fence_before();
       fence_proxy_async_smem();
       __syncwarp();
@@ -695,7 +717,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (valid) p.pml[(static_cast<long long>(g) * per_head + ent) * kGroup + h] = make_float2(mu, l);
     }
   } else {
-    // ---------------- warps 8-15: epilogue, O / 128 as fp16 partials ----------------
+    // ---------------- warps 8-15: epilogue, O / 128 (as the MMA wrote it) to fp16 partials ----------------
     // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Lane
     // pairs swap 16-byte pieces so that every store fills whole 32-byte
     // sectors: the even lane writes the first half of a sector, the odd lane the
@@ -726,7 +748,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         uint32_t u[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q)
-          u[q] = pack_half2(__uint_as_float(v[2 * q]) * (1.f / 128.f), __uint_as_float(v[2 * q + 1]) * (1.f / 128.f));
+          u[q] = pack_half2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
         uint32_t x[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -756,7 +778,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == kBmMmaWarp) {
+  if (warp == kBmMmaSWarp) {
     tc::fence_after();
     tc::dealloc(tmem, 512);
   }
