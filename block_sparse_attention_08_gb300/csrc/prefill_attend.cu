@@ -69,16 +69,17 @@ struct BmInfo {
 };
 constexpr int kBmInfo = 8;  // info ring slots
 
-// Q, V and P double-buffered, K single (a K block is released as soon as the
-// S MMAs of its last tile finish, well before V).
+// Four Q stages (the gather of a tile's 8 x 16 query rows is the longest
+// load), two V stages, one K stage (a K block is released as soon as the S
+// MMAs of its last tile finish, well before V).  P lives in tensor memory.
+constexpr int kBmQStages = 4;
 struct BmSmem {
-  alignas(1024) uint8_t q[2][kBmTile];
+  alignas(1024) uint8_t q[kBmQStages][kBmTile];
   alignas(1024) uint8_t k[kBmTile];
   alignas(1024) uint8_t v[2][kBmTile];
-  alignas(1024) uint8_t p[2][kBmTile];
-  uint64_t q_full[2], q_empty[2], k_full, k_empty, v_full[2], v_empty[2];
+  uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full, k_empty, v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  uint64_t p_full[2], p_empty[2], done_s, done_o;
+  uint64_t p_full[2], done_s, done_o;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -432,17 +433,18 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   const int n = local_tiles(p.meta[1]);  // tiles of this CTA
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBmQStages; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 4);
+      mbar_init(&sm.s_free[i], 1);  // committed by the O MMAs that read P from the same columns
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 4);
       mbar_init(&sm.p_full[i], 4);
-      mbar_init(&sm.p_empty[i], 1);
     }
     mbar_init(&sm.k_full, 1);
     mbar_init(&sm.k_empty, 1);
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_full[is]);
-      const int qs = i & 1;
+      const int qs = i % kBmQStages;
       if (lane == 0) {
         if (fresh) {
           ok = mbar_wait(&sm.k_empty, (nkf & 1) ^ 1, err, 700);
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             ++nkf;
           }
         }
-        ok = ok && mbar_wait(&sm.q_empty[qs], ((i >> 1) & 1) ^ 1, err, 702);
+        ok = ok && mbar_wait(&sm.q_empty[qs], ((i / kBmQStages) & 1) ^ 1, err, 702);
         if (ok) mbar_expect_tx(&sm.q_full[qs], d.cnt * 2 * kBmQBox);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -549,9 +551,11 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     // no copy may still be landing when the CTA exits: wait for the last fill of every stage
     if (lane == 0) {
       if (nkf > 0) mbar_wait(&sm.k_full, (nkf - 1) & 1, err, 704);
-      for (int q = 0; q < 2; ++q) {
-        const int fq = (i - q + 1) / 2;  // fills of Q stage q
+      for (int q = 0; q < kBmQStages; ++q) {
+        const int fq = (i - q + kBmQStages - 1) / kBmQStages;  // fills of Q stage q
         if (fq > 0) mbar_wait(&sm.q_full[q], (fq - 1) & 1, err, 703);
+      }
+      for (int q = 0; q < 2; ++q) {
         const int fv = (nvf - q + 1) / 2;
         if (fv > 0) mbar_wait(&sm.v_full[q], (fv - 1) & 1, err, 705);
       }
@@ -572,19 +576,19 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           if (!mbar_wait(&sm.k_full, nk & 1, err, 710)) break;
           ++nk;
         }
-        const int b = i & 1;
-        if (!mbar_wait(&sm.q_full[b], (i >> 1) & 1, err, 711) ||
+        const int b = i & 1, qs = i % kBmQStages;
+        if (!mbar_wait(&sm.q_full[qs], (i / kBmQStages) & 1, err, 711) ||
             !mbar_wait(&sm.s_free[b], ((i >> 1) & 1) ^ 1, err, 712))
           break;
         tc::fence_after();
-        const uint32_t qa = smem_u32(sm.q[b]), ka = smem_u32(sm.k);
+        const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
           tc::mma_bf16(tmem + b * 128, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kBmIdescS, kk > 0);
         }
         tc::commit(&sm.s_full[b]);
-        tc::commit(&sm.q_empty[b]);
+        tc::commit(&sm.q_empty[qs]);
       }
       // every MMA of this thread has finished before tensor memory is released
       tc::commit(&sm.done_s);
@@ -592,6 +596,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
   } else if (warp == kBmMmaOWarp) {
     // ---------------- O MMAs: O(i) = P(i) V into tensor-memory buffer 2 + i % 2 ----------------
+    // A = P from tensor memory (written by the softmax over the S it came from),
+    // B = V from shared memory; their completion also frees the S / P columns.
     if (lane == 0) {
       int nv = 0, vs = 0;
       for (int i = 0; i < n; ++i) {
@@ -610,14 +616,14 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             !mbar_wait(&sm.o_free[b], ((i >> 1) & 1) ^ 1, err, 715))
           break;
         tc::fence_after();
-        const uint32_t pa = smem_u32(sm.p[b]), va = smem_u32(sm.v[vs]);
+        const uint32_t va = smem_u32(sm.v[vs]);
+        const uint32_t pt = tmem + b * 128;  // P over the first 64 columns of the S buffer
         const uint32_t dt = tmem + 256 + b * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16(dt, tc::desc_k_sw128(pa + (kk >> 2) * kBmHalf + (kk & 3) * 32),
-                       desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
+          tc::mma_bf16_ts(dt, pt + kk * 8, desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
         tc::commit(&sm.o_full[b]);
-        tc::commit(&sm.p_empty[b]);
+        tc::commit(&sm.s_free[b]);
       }
       tc::commit(&sm.done_o);
       mbar_wait(&sm.done_o, 0, err, 719);
@@ -628,7 +634,6 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const int wg = warp >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
     const uint32_t srow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 128;
-    const uint32_t pbase = smem_u32(sm.p[wg]);
     const long long per_head = T * topk;
     for (int i = wg; i < n; i += 2) {
       const int is = i % kBmInfo, k = i >> 1;
@@ -669,8 +674,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         // scale > 0, so the max of the scaled scores is the scaled max
         const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
         const float shift = mu + 7.f;  // p / 128 = 2^(s * scale * log2 e - mu - 7)
-        // pass 2: bf16 p / 128 into the P tile, fp32 row sum
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_empty[wg], (k & 1) ^ 1, err, 721))) return false;
+        // pass 2: bf16 p / 128 written over the S columns already read (P chunk
+        // ch, 16 columns, lands in S chunk ch / 2), fp32 row sum
         float l8[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) l8[q] = 0.f;
@@ -693,12 +698,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             l8[q & 7] += pa + pb;
             pk[q] = pack_bf16(pa, pb);
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte P row
-            sts128(pbase + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                   pk[4 * c + 3]);
-          }
+          tc::st_32x32b_x16(srow + ch * 16, pk);
         }
         l = 128.f * (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         mx = mu;
@@ -707,13 +707,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const bool ok = masked ? softmax_rows(std::true_type{}) : softmax_rows(std::false_type{});
       if (!ok) break;
       const float mu = mx;
+      tc::wait_st();
       tc::fence_before();
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.s_free[wg]);
-        mbar_arrive(&sm.p_full[wg]);
-      }
+      if (lane == 0) mbar_arrive(&sm.p_full[wg]);
       if (valid) p.pml[(static_cast<long long>(g) * per_head + ent) * kGroup + h] = make_float2(mu, l);
     }
   } else {
