@@ -69,21 +69,26 @@ struct BmInfo {
 };
 constexpr int kBmInfo = 8;  // info ring slots
 
-// Four Q stages (the gather of a tile's 8 x 16 query rows is the longest
-// load), two V stages, one K stage (a K block is released as soon as the S
-// MMAs of its last tile finish, well before V).  P lives in tensor memory.
-constexpr int kBmQStages = 4;
+// Two Q stages, two V stages, one K stage (a K block is released as soon as
+// the S MMAs of its last tile finish, well before V), and one fp16 O staging
+// tile per epilogue warpgroup for the TMA stores.  P lives in tensor memory.
+constexpr int kBmQStages = 2;
 struct BmSmem {
   alignas(1024) uint8_t q[kBmQStages][kBmTile];
   alignas(1024) uint8_t k[kBmTile];
   alignas(1024) uint8_t v[2][kBmTile];
+  alignas(1024) uint8_t ostage[2][kBmTile];  // 128 rows x 128 fp16, two 64-dim halves
   uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full, k_empty, v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
   uint64_t p_full[2], done_s, done_o;
+  uint64_t stage_free[2], stage_full[2];  // epilogue warpgroup: staging tile free / written
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
 };
+
+// 1024 bytes of slack align the dynamic shared memory base; 227 KB per CTA at most.
+static_assert(sizeof(BmSmem) + 1024 <= 227 * 1024, "shared memory of the attention kernel");
 
 // Sizes of the bucketing problem, fixed by (tokens, longest document, topk).
 struct BmDims {
@@ -426,7 +431,8 @@ __device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t
 
 __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, BmPlan p, long long T, int topk, float scale_log2, DevError* err) {
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap pmap, BmPlan p, long long T,
+    int topk, float scale_log2, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   BmSmem& sm = *reinterpret_cast<BmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -451,6 +457,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
       mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.stage_free[i], 1);
+      mbar_init(&sm.stage_full[i], 4);
     }
     mbar_init(&sm.done_s, 1);
     mbar_init(&sm.done_o, 1);
@@ -715,28 +725,35 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
   } else {
     // ---------------- warps 8-15: epilogue, O / 128 (as the MMA wrote it) to fp16 partials ----------------
-    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Lane
-    // pairs swap 16-byte pieces so that every store fills whole 32-byte
-    // sectors: the even lane writes the first half of a sector, the odd lane the
-    // second, for both rows of the pair in turn.
+    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Each
+    // thread converts its row to fp16 in a 128-byte-swizzled staging tile;
+    // one thread then writes each entry's 16 rows with two tiled TMA stores.
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
-    const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
-    const bool odd = lane & 1;
+    const int r = quarter * 32 + lane;
     const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
+    const uint32_t stage = smem_u32(sm.ostage[wg]);
     const long long per_head = T * topk;
+    const bool issuer = r == 0;
+    if (issuer) prefetch_tmap(&pmap);
     for (int i = wg; i < n; i += 2) {
       const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 724))) break;
       const int cnt = sm.info[is].cnt, g = sm.info[is].g;
-      const bool valid = e < cnt;
-      const int ent = valid ? sm.info[is].ent[e] : 0;
+      int ents[kBmEntries];
+      if (issuer) {
+#pragma unroll
+        for (int e = 0; e < kBmEntries; ++e) ents[e] = sm.info[is].ent[e];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
       tc::fence_after();
-      // this lane's row, and the even row of its pair
-      __half* own = p.po + ((static_cast<long long>(g) * per_head + ent) * kGroup + h) * kDim;
-      __half* pair_even = odd ? own - kDim : own;
+      // the staging tile is free once the TMA stores of this group's previous tile have read it
+      if (issuer) {
+        bulk_wait_read_all();
+        mbar_arrive(&sm.stage_free[wg]);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[wg], k & 1, err, 725))) break;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -744,34 +761,31 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         tc::wait_ld();
         uint32_t u[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          u[q] = pack_half2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-        uint32_t x[8];
+        for (int q = 0; q < 16; ++q) u[q] = pack_half2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          x[q] = __shfl_xor_sync(0xffffffffu, odd ? u[q] : u[4 + q], 1);
-          x[4 + q] = __shfl_xor_sync(0xffffffffu, odd ? u[8 + q] : u[12 + q], 1);
-        }
-        if (valid) {
-          __half* a = pair_even + ch * 32;  // even row of the pair, this chunk
-          __half* b = a + kDim;             // odd row
-          if (!odd) {
-            stg128(a, u[0], u[1], u[2], u[3]);
-            stg128(a + 16, u[8], u[9], u[10], u[11]);
-            stg128(b, x[0], x[1], x[2], x[3]);
-            stg128(b + 16, x[4], x[5], x[6], x[7]);
-          } else {
-            stg128(a + 8, x[0], x[1], x[2], x[3]);
-            stg128(a + 24, x[4], x[5], x[6], x[7]);
-            stg128(b + 8, u[4], u[5], u[6], u[7]);
-            stg128(b + 24, u[12], u[13], u[14], u[15]);
-          }
+        for (int c = 0; c < 4; ++c) {
+          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte row
+          sts128(stage + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), u[4 * c], u[4 * c + 1], u[4 * c + 2],
+                 u[4 * c + 3]);
         }
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.o_free[wg]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.stage_full[wg]);
+      if (issuer) {
+        if (!mbar_wait(&sm.stage_full[wg], k & 1, err, 726)) break;
+        for (int e = 0; e < cnt; ++e) {
+          const int row = static_cast<int>((static_cast<long long>(g) * per_head + ents[e]) * kGroup);
+          tma_store_2d(&pmap, sm.ostage[wg] + e * kBmQBox, 0, row);
+          tma_store_2d(&pmap, sm.ostage[wg] + kBmHalf + e * kBmQBox, 64, row);
+        }
+        bulk_commit();
+      }
     }
+    if (issuer) bulk_wait_all();
   }
   tc::fence_before();
   __syncthreads();
@@ -850,9 +864,23 @@ static bool encode3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over the fp16 partials viewed as [entries * 16 rows, 128]; box = 64 dims x 16 rows.
+static bool encode_partials(CUtensorMap* map, const void* base, long long rows) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {kDim * 2};
+  cuuint32_t box[2] = {64, kGroup};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool prefill_attend_fits(long long total_tokens, int max_seqlen, int topk) {
   const BmDims d = bm_dims(total_tokens, max_seqlen, topk);
-  return d.entries < (1LL << 31) && kKvHeads * d.kg_max < (1LL << 31) && d.tiles_max < (1LL << 31);
+  // partial rows are addressed by 32-bit TMA coordinates
+  return d.entries * kGroup < (1LL << 31) && kKvHeads * d.kg_max < (1LL << 31) && d.tiles_max < (1LL << 31);
 }
 
 cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, const int32_t* q2k,
@@ -862,8 +890,9 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
   bm_carve(dims, region, &p);
-  CUtensorMap qmap, kmap, vmap;
-  if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+  CUtensorMap qmap, kmap, vmap, pmap;
+  if (!encode_partials(&pmap, p.po, dims.entries * kGroup) ||
+      !encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
       !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
     return cudaErrorInvalidValue;
@@ -882,7 +911,7 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   cudaFuncSetAttribute(bm_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
   const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
-  bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, p, total_tokens, topk,
+  bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, pmap, p, total_tokens, topk,
                                                        scale * 1.4426950408889634f, err);
   bm_merge_kernel<<<dim3(static_cast<unsigned>(total_tokens), kKvHeads), 256, 0, stream>>>(
       q2k, cu_seqlens, num_docs, total_tokens, topk, p, static_cast<__nv_bfloat16*>(out));
