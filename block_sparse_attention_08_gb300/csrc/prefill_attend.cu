@@ -30,7 +30,7 @@
 // written as a partial: row max (log2 units) and row sum of p in fp32, and the
 // unnormalised O / 128 in fp16; a merge kernel combines the <= topk partials
 // of a (query, KV head) pair into the bf16 output.  Tiles are handed out in
-// chunks of 4, round-robin over the persistent grid, so all CTAs move through
+// chunks of 16, round-robin over the persistent grid, so all CTAs move through
 // the (KV head, window) buckets together and the window's Q rows and K / V
 // blocks stay in L2.
 #include <cuda_fp16.h>
@@ -51,7 +51,7 @@ constexpr int kBmThreads = 608;
 constexpr int kBmProducerWarp = 16;
 constexpr int kBmMmaSWarp = 17;
 constexpr int kBmMmaOWarp = 18;
-constexpr int kBmChunk = 4;                       // tiles per scheduling chunk
+constexpr int kBmChunk = 16;                      // tiles per scheduling chunk
 constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
 
@@ -69,19 +69,23 @@ struct BmInfo {
 };
 constexpr int kBmInfo = 8;  // info ring slots
 
-// Two Q stages, two V stages, one K stage (a K block is released as soon as
-// the S MMAs of its last tile finish, well before V), and one fp16 O staging
-// tile per epilogue warpgroup for the TMA stores.  P lives in tensor memory.
+// Two Q stages, two K and two V stages (the next block's K / V load while the
+// current one is in use), and one fp16 O staging tile that the two epilogue
+// warpgroups take in tile order for the TMA stores.  P lives in tensor memory.
 constexpr int kBmQStages = 2;
+constexpr int kBmKStages = 2;
+constexpr int kBmVStages = 2;
 struct BmSmem {
   alignas(1024) uint8_t q[kBmQStages][kBmTile];
-  alignas(1024) uint8_t k[kBmTile];
-  alignas(1024) uint8_t v[2][kBmTile];
-  alignas(1024) uint8_t ostage[2][kBmTile];  // 128 rows x 128 fp16, two 64-dim halves
-  uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full, k_empty, v_full[2], v_empty[2];
+  alignas(1024) uint8_t k[kBmKStages][kBmTile];
+  alignas(1024) uint8_t v[kBmVStages][kBmTile];
+  alignas(1024) uint8_t ostage[kBmTile];  // 128 rows x 128 fp16, two 64-dim halves
+  uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full[kBmKStages], k_empty[kBmKStages];
+  uint64_t v_full[kBmVStages], v_empty[kBmVStages];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
   uint64_t p_full[2], done_s, done_o;
-  uint64_t stage_free[2], stage_full[2];  // epilogue warpgroup: staging tile free / written
+  // staging tile: read by the stores of tile i (stage_free[i % 2]) / written for the current tile
+  uint64_t stage_free[2], stage_full;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -443,25 +447,28 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBmVStages; ++i) {
       mbar_init(&sm.v_full[i], 1);
       mbar_init(&sm.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 1);  // committed by the O MMAs that read P from the same columns
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 4);
       mbar_init(&sm.p_full[i], 4);
     }
-    mbar_init(&sm.k_full, 1);
-    mbar_init(&sm.k_empty, 1);
+    for (int i = 0; i < kBmKStages; ++i) {
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+    }
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
       mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.stage_free[i], 1);
-      mbar_init(&sm.stage_full[i], 4);
-    }
+    mbar_init(&sm.stage_free[0], 1);
+    mbar_init(&sm.stage_free[1], 1);
+    mbar_init(&sm.stage_full, 4);
     mbar_init(&sm.done_s, 1);
     mbar_init(&sm.done_o, 1);
     fence_mbar_init();
@@ -521,11 +528,12 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const int qs = i % kBmQStages;
       if (lane == 0) {
         if (fresh) {
-          ok = mbar_wait(&sm.k_empty, (nkf & 1) ^ 1, err, 700);
+          const int s = nkf % kBmKStages;
+          ok = mbar_wait(&sm.k_empty[s], ((nkf / kBmKStages) & 1) ^ 1, err, 700);
           if (ok) {
-            mbar_expect_tx(&sm.k_full, kBmTile);
-            tma_load_3d(sm.k, &kmap, 0, d.g, d.row0, &sm.k_full);
-            tma_load_3d(sm.k + kBmHalf, &kmap, 64, d.g, d.row0, &sm.k_full);
+            mbar_expect_tx(&sm.k_full[s], kBmTile);
+            tma_load_3d(sm.k[s], &kmap, 0, d.g, d.row0, &sm.k_full[s]);
+            tma_load_3d(sm.k[s] + kBmHalf, &kmap, 64, d.g, d.row0, &sm.k_full[s]);
             ++nkf;
           }
         }
@@ -543,8 +551,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         prow = d.row0;
         pg = d.g;
         if (lane == 0) {
-          const int s = nvf & 1;
-          ok = mbar_wait(&sm.v_empty[s], ((nvf >> 1) & 1) ^ 1, err, 701);
+          const int s = nvf % kBmVStages;
+          ok = mbar_wait(&sm.v_empty[s], ((nvf / kBmVStages) & 1) ^ 1, err, 701);
           if (ok) {
             mbar_expect_tx(&sm.v_full[s], kBmTile);
             tma_load_3d(sm.v[s], &vmap, 0, d.g, d.row0, &sm.v_full[s]);
@@ -560,13 +568,16 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
     // no copy may still be landing when the CTA exits: wait for the last fill of every stage
     if (lane == 0) {
-      if (nkf > 0) mbar_wait(&sm.k_full, (nkf - 1) & 1, err, 704);
+      for (int q = 0; q < kBmKStages; ++q) {
+        const int fk = (nkf - q + kBmKStages - 1) / kBmKStages;
+        if (fk > 0) mbar_wait(&sm.k_full[q], (fk - 1) & 1, err, 704);
+      }
       for (int q = 0; q < kBmQStages; ++q) {
         const int fq = (i - q + kBmQStages - 1) / kBmQStages;  // fills of Q stage q
         if (fq > 0) mbar_wait(&sm.q_full[q], (fq - 1) & 1, err, 703);
       }
-      for (int q = 0; q < 2; ++q) {
-        const int fv = (nvf - q + 1) / 2;
+      for (int q = 0; q < kBmVStages; ++q) {
+        const int fv = (nvf - q + kBmVStages - 1) / kBmVStages;
         if (fv > 0) mbar_wait(&sm.v_full[q], (fv - 1) & 1, err, 705);
       }
     }
@@ -575,15 +586,16 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     // Issued independently of the O MMAs (another warp), so an S tile never
     // waits behind the P of an earlier tile.
     if (lane == 0) {
-      int nk = 0;
+      int nk = 0, ks = 0;
       for (int i = 0; i < n; ++i) {
         const int is = i % kBmInfo;
         if (!mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 717)) break;
         const bool fresh = sm.info[is].fresh != 0;
         mbar_arrive(&sm.info_empty[is]);
         if (fresh) {
-          if (nk > 0) tc::commit(&sm.k_empty);
-          if (!mbar_wait(&sm.k_full, nk & 1, err, 710)) break;
+          if (nk > 0) tc::commit(&sm.k_empty[ks]);
+          ks = nk % kBmKStages;
+          if (!mbar_wait(&sm.k_full[ks], (nk / kBmKStages) & 1, err, 710)) break;
           ++nk;
         }
         const int b = i & 1, qs = i % kBmQStages;
@@ -591,7 +603,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             !mbar_wait(&sm.s_free[b], ((i >> 1) & 1) ^ 1, err, 712))
           break;
         tc::fence_after();
-        const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k);
+        const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k[ks]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
@@ -617,8 +629,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         mbar_arrive(&sm.info_empty[is]);
         if (fresh) {
           if (nv > 0) tc::commit(&sm.v_empty[vs]);
-          vs = nv & 1;
-          if (!mbar_wait(&sm.v_full[vs], (nv >> 1) & 1, err, 713)) break;
+          vs = nv % kBmVStages;
+          if (!mbar_wait(&sm.v_full[vs], (nv / kBmVStages) & 1, err, 713)) break;
           ++nv;
         }
         const int b = i & 1;
@@ -731,7 +743,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
-    const uint32_t stage = smem_u32(sm.ostage[wg]);
+    const uint32_t stage = smem_u32(sm.ostage);
     const long long per_head = T * topk;
     const bool issuer = r == 0;
     if (issuer) prefetch_tmap(&pmap);
@@ -748,12 +760,12 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
       tc::fence_after();
-      // the staging tile is free once the TMA stores of this group's previous tile have read it
-      if (issuer) {
-        bulk_wait_read_all();
-        mbar_arrive(&sm.stage_free[wg]);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[wg], k & 1, err, 725))) break;
+      // the staging tile is free once the TMA stores of the previous tile (the
+      // other warpgroup's) have read it.  One barrier per tile parity: this
+      // group's warps can run a tile ahead of its own store thread, so a single
+      // barrier could be two phases behind and pass on a stale parity.
+      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[(i - 1) & 1], ((i - 1) >> 1) & 1, err, 725)))
+        break;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -774,15 +786,17 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.o_free[wg]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.stage_full[wg]);
+      if (lane == 0) mbar_arrive(&sm.stage_full);
       if (issuer) {
-        if (!mbar_wait(&sm.stage_full[wg], k & 1, err, 726)) break;
+        if (!mbar_wait(&sm.stage_full, i & 1, err, 726)) break;
         for (int e = 0; e < cnt; ++e) {
           const int row = static_cast<int>((static_cast<long long>(g) * per_head + ents[e]) * kGroup);
-          tma_store_2d(&pmap, sm.ostage[wg] + e * kBmQBox, 0, row);
-          tma_store_2d(&pmap, sm.ostage[wg] + kBmHalf + e * kBmQBox, 64, row);
+          tma_store_2d(&pmap, sm.ostage + e * kBmQBox, 0, row);
+          tma_store_2d(&pmap, sm.ostage + kBmHalf + e * kBmQBox, 64, row);
         }
         bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&sm.stage_free[i & 1]);
       }
     }
     if (issuer) bulk_wait_all();
