@@ -69,23 +69,23 @@ struct BmInfo {
 };
 constexpr int kBmInfo = 8;  // info ring slots
 
-// Two Q stages, two K and two V stages (the next block's K / V load while the
-// current one is in use), and one fp16 O staging tile that the two epilogue
-// warpgroups take in tile order for the TMA stores.  P lives in tensor memory.
+// Two Q stages, two K stages (the next block's K loads while the current one
+// is in use), one V stage (a block's V is needed a tile later than its K), and
+// one fp16 O staging tile per epilogue warpgroup for the TMA stores.  P lives
+// in tensor memory.
 constexpr int kBmQStages = 2;
 constexpr int kBmKStages = 2;
-constexpr int kBmVStages = 2;
+constexpr int kBmVStages = 1;
 struct BmSmem {
   alignas(1024) uint8_t q[kBmQStages][kBmTile];
   alignas(1024) uint8_t k[kBmKStages][kBmTile];
   alignas(1024) uint8_t v[kBmVStages][kBmTile];
-  alignas(1024) uint8_t ostage[kBmTile];  // 128 rows x 128 fp16, two 64-dim halves
+  alignas(1024) uint8_t ostage[2][kBmTile];  // per epilogue warpgroup: 128 rows x 128 fp16, two 64-dim halves
   uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full[kBmKStages], k_empty[kBmKStages];
   uint64_t v_full[kBmVStages], v_empty[kBmVStages];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
   uint64_t p_full[2], done_s, done_o;
-  // staging tile: read by the stores of tile i (stage_free[i % 2]) / written for the current tile
-  uint64_t stage_free[2], stage_full;
+  uint64_t stage_free[2], stage_full[2];  // per epilogue warpgroup: staging tile free / written
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -466,9 +466,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       mbar_init(&sm.info_full[i], 1);
       mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
     }
-    mbar_init(&sm.stage_free[0], 1);
-    mbar_init(&sm.stage_free[1], 1);
-    mbar_init(&sm.stage_full, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.stage_free[i], 1);
+      mbar_init(&sm.stage_full[i], 4);
+    }
     mbar_init(&sm.done_s, 1);
     mbar_init(&sm.done_o, 1);
     fence_mbar_init();
@@ -743,7 +744,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
-    const uint32_t stage = smem_u32(sm.ostage);
+    const uint32_t stage = smem_u32(sm.ostage[wg]);
     const long long per_head = T * topk;
     const bool issuer = r == 0;
     if (issuer) prefetch_tmap(&pmap);
@@ -760,12 +761,13 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
       tc::fence_after();
-      // the staging tile is free once the TMA stores of the previous tile (the
-      // other warpgroup's) have read it.  One barrier per tile parity: this
-      // group's warps can run a tile ahead of its own store thread, so a single
-      // barrier could be two phases behind and pass on a stale parity.
-      if (i > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[(i - 1) & 1], ((i - 1) >> 1) & 1, err, 725)))
-        break;
+      // the staging tile is free once the TMA stores of this group's previous
+      // tile have read it; the store thread signals that at the start of the tile
+      if (issuer) {
+        bulk_wait_read_all();
+        mbar_arrive(&sm.stage_free[wg]);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[wg], k & 1, err, 725))) break;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -786,17 +788,15 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.o_free[wg]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.stage_full);
+      if (lane == 0) mbar_arrive(&sm.stage_full[wg]);
       if (issuer) {
-        if (!mbar_wait(&sm.stage_full, i & 1, err, 726)) break;
+        if (!mbar_wait(&sm.stage_full[wg], k & 1, err, 726)) break;
         for (int e = 0; e < cnt; ++e) {
           const int row = static_cast<int>((static_cast<long long>(g) * per_head + ents[e]) * kGroup);
-          tma_store_2d(&pmap, sm.ostage + e * kBmQBox, 0, row);
-          tma_store_2d(&pmap, sm.ostage + kBmHalf + e * kBmQBox, 64, row);
+          tma_store_2d(&pmap, sm.ostage[wg] + e * kBmQBox, 0, row);
+          tma_store_2d(&pmap, sm.ostage[wg] + kBmHalf + e * kBmQBox, 64, row);
         }
         bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive(&sm.stage_free[i & 1]);
       }
     }
     if (issuer) bulk_wait_all();
