@@ -437,28 +437,47 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
+        // The contributors are the consecutive CTAs c_first .. c_last (at most
+        // topk: each holds at least one unit of the segment); every one but the
+        // first wrote this segment as its first partial.  All loads of a pass
+        // are issued before any is used.
         const long long c_first = cta_of(range0, N, G), c_last = cta_of(range0 + topk - 1, N, G);
-        float Mg = -INFINITY;
-        for (long long c = c_first; c <= c_last; ++c) {
-          const long long sl = 2 * c + (range0 <= seg_begin(c, N, G) ? 0 : 1);
-          Mg = fmaxf(Mg, __ldcg(partials + sl * kPartialFloats + row));
+        const int nc = static_cast<int>(c_last - c_first + 1);
+        const long long slot0 = 2 * c_first + (seg_begin(c_first, N, G) < range0 ? 1 : 0);
+        auto part_of = [&](int x) {
+          return partials + (x == 0 ? slot0 : 2 * (c_first + x)) * kPartialFloats;
+        };
+        float mc[kMaxTopk], lc[kMaxTopk];
+#pragma unroll
+        for (int x = 0; x < kMaxTopk; ++x) {
+          mc[x] = x < nc ? __ldcg(part_of(x) + row) : -INFINITY;
+          lc[x] = x < nc ? __ldcg(part_of(x) + 16 + row) : 0.f;
         }
+        float Mg = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < kMaxTopk; ++x) Mg = fmaxf(Mg, mc[x]);
         const float Mgu = Mg == -INFINITY ? 0.f : Mg;
         float Lg = 0.f, ag[64];
 #pragma unroll
         for (int d = 0; d < 64; ++d) ag[d] = 0.f;
-        for (long long c = c_first; c <= c_last; ++c) {
-          const long long sl = 2 * c + (range0 <= seg_begin(c, N, G) ? 0 : 1);
-          const float* pc = partials + sl * kPartialFloats;
-          const float f = exp2f(__ldcg(pc + row) - Mgu);
-          Lg += __ldcg(pc + 16 + row) * f;
 #pragma unroll
-          for (int d = 0; d < 64; d += 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(pc + 32 + row * kDim + d0 + d));
-            ag[d] += x.x * f;
-            ag[d + 1] += x.y * f;
-            ag[d + 2] += x.z * f;
-            ag[d + 3] += x.w * f;
+        for (int x = 0; x < kMaxTopk; ++x) {
+          mc[x] = exp2f(mc[x] - Mgu);  // the contributor's weight (0 past nc)
+          Lg += lc[x] * mc[x];
+        }
+#pragma unroll 2
+        for (int x = 0; x < nc; ++x) {
+          const float* pc = part_of(x) + 32 + row * kDim + d0;
+          float4 xs[16];
+#pragma unroll
+          for (int d = 0; d < 16; ++d) xs[d] = __ldcg(reinterpret_cast<const float4*>(pc) + d);
+          const float f = mc[x];
+#pragma unroll
+          for (int d = 0; d < 16; ++d) {
+            ag[4 * d] += xs[d].x * f;
+            ag[4 * d + 1] += xs[d].y * f;
+            ag[4 * d + 2] += xs[d].z * f;
+            ag[4 * d + 3] += xs[d].w * f;
           }
         }
         const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
@@ -511,8 +530,13 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows) ||
       !make_q_map(&qmap, q, geo.nq))
     return cudaErrorInvalidValue;
+  // At least 4 units per CTA: a segment is then shared by at most ~topk/4 + 1
+  // CTAs, which bounds the partials its last CTA has to merge.
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
-  const int grid = static_cast<int>(N < kNumSMs ? (N > 0 ? N : 1) : kNumSMs);
+  long long grid_l = (N + 3) / 4;
+  if (grid_l > kNumSMs) grid_l = kNumSMs;
+  if (grid_l < 1) grid_l = 1;
+  const int grid = static_cast<int>(grid_l);
   const size_t smem = sizeof(AttSmem) + 1024;
   cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const float scale_log2 = scale * 1.4426950408889634f;
