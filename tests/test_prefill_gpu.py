@@ -116,3 +116,36 @@ def test_prefill_workload_1doc_16k():
 def test_prefill_workload_packed_2x32k():
     p = msa_synth.workload("prefill_packed_2x32k", device="cuda")
     _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 1), init=1, local=1)
+
+
+def test_prefill_attend_empty_rows_and_bad_ids():
+    """A (query, KV head) row with no block outputs zeros; an id at or past the
+    query's block count is skipped and reported in the device error word
+    (MSA_DEVERR_BLOCK = 2, detail = the flat q2k index), the rest of the row is
+    attended as usual."""
+    from block_sparse_attention_08_gb300 import binding
+    p = msa_synth.prefill_inputs([300, 700], seed=6, device="cuda")
+    T = p.total_tokens
+    tok = np.arange(T, dtype=np.int64)
+    topk = 4
+    ref_q2k, _ = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=topk, init=1, local=1)
+    q2k = ref_q2k.copy()
+    q2k[1, 5, :] = -1                # token 5, KV head 1: nothing to attend
+    t_bad = 300 + 600                # document 1, position 600: blocks 0..4
+    j_bad = int(np.argmax(q2k[2, t_bad] >= 0))
+    q2k[2, t_bad, j_bad] = 5         # one past its last causal block
+    ws_q2k = torch.from_numpy(q2k).cuda()
+    msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=topk, init_blocks=1,
+                                  local_blocks=1)  # sizes the shared workspace
+    ws = binding._WS[("prefill", "cuda:0")]
+    ws.read_device_error()           # clear the error word
+    out = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, ws_q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE)
+    torch.cuda.synchronize()
+    code, detail = ws.read_device_error()
+    assert code == 2 and detail == (2 * T + t_bad) * topk + j_bad, (code, detail)
+    ref = q2k.copy()
+    ref[2, t_bad, j_bad] = -1        # the skipped id
+    ref_out = oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, ref, SCALE)
+    o = out.float().cpu().numpy()
+    assert not o[5, 16:32].any()
+    check_out(out, ref_out, "prefill out with empty and bad rows")
