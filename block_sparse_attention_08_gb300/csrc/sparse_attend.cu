@@ -22,7 +22,8 @@
 // (stage s always to warp s % 3), so every warp has one chunk landing while it
 // computes on the other, and none reads global memory on its critical path:
 // S = Q K^T (ldmatrix fragments), online softmax in base 2, O += P V
-// (ldmatrix.trans V fragments; P fed as bf16 hi + lo terms), mma.sync bf16 with
+// (ldmatrix.trans V fragments; P rounded to bf16, the row sum taken over the
+// rounded values), mma.sync bf16 with
 // fp32 accumulation.  At the end of a segment the three states are merged
 // through shared memory.  A segment cut by a CTA boundary is written as an fp32
 // partial (max, sum, unnormalised O); the CTA whose atomic ticket completes the
@@ -340,13 +341,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         const float al0 = exp2f(st.m0 - mu0), al1 = exp2f(st.m1 - mu1);
         st.m0 = mn0;
         st.m1 = mn1;
+        // p rounded to bf16 (the PV operand); the row sum adds the same rounded
+        // values, so the normalisation matches the weights the MMA applies
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-          sacc[p][0] = exp2f(sacc[p][0] - mu0);
-          sacc[p][1] = exp2f(sacc[p][1] - mu0);
-          sacc[p][2] = exp2f(sacc[p][2] - mu1);
-          sacc[p][3] = exp2f(sacc[p][3] - mu1);
+          sacc[p][0] = bf16_round(exp2f(sacc[p][0] - mu0));
+          sacc[p][1] = bf16_round(exp2f(sacc[p][1] - mu0));
+          sacc[p][2] = bf16_round(exp2f(sacc[p][2] - mu1));
+          sacc[p][3] = bf16_round(exp2f(sacc[p][3] - mu1));
           rs0 += sacc[p][0] + sacc[p][1];
           rs1 += sacc[p][2] + sacc[p][3];
         }
@@ -359,17 +362,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
           st.o[nd][2] *= al1;
           st.o[nd][3] *= al1;
         }
-        // ---- O += P V, one k-step per 16 keys; P = P_hi + P_lo in two bf16 terms
-        // (relative error ~2^-17) so the bf16 rounding of probabilities does not
-        // reach the output ----
+        // ---- O += P V, one k-step per 16 keys (P exact in bf16 after the rounding above) ----
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           if (16 * kp >= valid) break;
-          uint32_t pa[4], pl[4];
-          split_bf16(sacc[2 * kp][0], sacc[2 * kp][1], pa[0], pl[0]);
-          split_bf16(sacc[2 * kp][2], sacc[2 * kp][3], pa[1], pl[1]);
-          split_bf16(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1], pa[2], pl[2]);
-          split_bf16(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3], pa[3], pl[3]);
+          const uint32_t pa[4] = {pack_bf16(sacc[2 * kp][0], sacc[2 * kp][1]),
+                                  pack_bf16(sacc[2 * kp][2], sacc[2 * kp][3]),
+                                  pack_bf16(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1]),
+                                  pack_bf16(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3])};
           const int vrow = 16 * kp + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
           for (int nd = 0; nd < 16; nd += 2) {
@@ -378,8 +378,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             ldsm_x4_t(vb, stg + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7));
             mma_bf16(st.o[nd], pa, vb[0], vb[1]);
             mma_bf16(st.o[nd + 1], pa, vb[2], vb[3]);
-            mma_bf16(st.o[nd], pl, vb[0], vb[1]);
-            mma_bf16(st.o[nd + 1], pl, vb[2], vb[3]);
           }
         }
         __syncwarp();
