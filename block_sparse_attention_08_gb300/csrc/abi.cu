@@ -181,7 +181,7 @@ msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s) != cudaSuccess)
     return MSA_ERR_CUDA;
-  AttnGeom geo{0, batch, seq_lens, page_table, cu_seqlens_k, max_blocks, nullptr, 0, num_slots};
+  AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
   cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out,
                                        reinterpret_cast<float*>(ws + L.partials),
                                        reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);

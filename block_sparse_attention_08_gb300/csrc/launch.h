@@ -10,19 +10,14 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn get_encode_tiled();
 
-// Geometry of the queries of one attention call.
+// Geometry of the requests of one decode attention call.
 struct AttnGeom {
-  int prefill;  // 0 decode, 1 prefill
-  int nq;       // requests (decode) or compact tokens (prefill)
-  // decode
-  const int32_t* seq_lens;
-  const int32_t* page_table;
-  const int64_t* cu_k;
+  int nq;                     // requests
+  const int32_t* seq_lens;    // [nq]
+  const int32_t* page_table;  // [nq, max_blocks] or null (contiguous cache)
+  const int64_t* cu_k;        // [nq + 1] when contiguous
   int max_blocks;
-  // prefill
-  const int32_t* cu_seqlens;
-  int num_docs;
-  long long num_rows;  // rows of the K/V arrays (slots or tokens)
+  long long num_rows;         // slots of the K/V cache
 };
 
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,

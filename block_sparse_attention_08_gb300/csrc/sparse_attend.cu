@@ -1,6 +1,6 @@
-// sparse_attend.cu -- sparse GQA attention over the selected blocks, for a
-// decode step (one query per request over a paged or contiguous K/V cache) and
-// for packed-document prefill (every compact token).
+// sparse_attend.cu -- sparse GQA attention over the selected blocks for a
+// decode step: one query per request over a paged or contiguous K/V cache.
+// (Packed-document prefill has its own block-major kernel, prefill_attend.cu.)
 //
 // TensorRT-LLM "MiniMaxM3SparseAttentionConfig" (class description, second
 // step: a sparse GQA attention over only the selected blocks) and NeMo
@@ -50,32 +50,21 @@ static_assert(kAttStages % kConsumerWarps == 0, "stages must be a multiple of th
 struct QueryGeo {
   int pos;         // position of the query (keys 0..pos are causal)
   int nb;          // candidate blocks
-  long long base;  // prefill: first row of the document; decode contiguous: cu_k[r]
+  long long base;  // contiguous cache: first row of the request (cu_k[r])
 };
 
 __device__ __forceinline__ QueryGeo query_geo(const AttnGeom& geo, int qi) {
   QueryGeo q;
-  if (geo.prefill) {
-    int lo = 0, hi = geo.num_docs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (geo.cu_seqlens[mid] <= qi) lo = mid; else hi = mid - 1;
-    }
-    q.base = geo.cu_seqlens[lo];
-    q.pos = qi - static_cast<int>(q.base);
-    q.nb = q.pos / kBlock + 1;
-  } else {
-    const int L = geo.seq_lens[qi];
-    q.pos = L - 1;
-    q.nb = L < 1 ? 0 : min((L + kBlock - 1) / kBlock, geo.max_blocks);
-    q.base = geo.page_table ? 0 : geo.cu_k[qi];
-  }
+  const int L = geo.seq_lens[qi];
+  q.pos = L - 1;
+  q.nb = L < 1 ? 0 : min((L + kBlock - 1) / kBlock, geo.max_blocks);
+  q.base = geo.page_table ? 0 : geo.cu_k[qi];
   return q;
 }
 
 // First K/V row of block b of the query, or -1 when the page is outside the pool.
 __device__ __forceinline__ long long block_row0(const AttnGeom& geo, int qi, const QueryGeo& q, int b) {
-  if (!geo.prefill && geo.page_table) {
+  if (geo.page_table) {
     const int page = geo.page_table[static_cast<long long>(qi) * geo.max_blocks + b];
     const long long r0 = static_cast<long long>(page) * kBlock;
     return (page < 0 || r0 + kBlock > geo.num_rows) ? -1 : r0;
