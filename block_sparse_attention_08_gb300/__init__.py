@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     library_path,
     load,
     make_config,
+    msa_check_bounded_wait,
     msa_pack,
     msa_pack_metadata,
     msa_select_blocks_decode,

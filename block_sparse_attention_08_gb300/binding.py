@@ -55,6 +55,7 @@ _SIGS = {
                           ctypes.POINTER(I64), P, SZ, P],
     "msa_pack": [P, P, I64, I64, P, P],
     "msa_unpack": [P, P, I64, I64, I64, P, P],
+    "msa_check_bounded_wait": [P, P, ctypes.POINTER(I64)],
 }
 EXPORTS = tuple(_SIGS) + ("msa_status_string",)
 
@@ -325,3 +326,12 @@ def msa_unpack(packed, token_rows, batch, seq):
     _call("msa_unpack", _ptr(packed), _ptr(token_rows), packed.shape[0], batch * seq, row_bytes, _ptr(out),
           _stream(packed.device))
     return out
+
+
+def msa_check_bounded_wait(workspace=None, device=None):
+    """Run the bounded-wait diagnostic (C: msa_check_bounded_wait) on a
+    256-byte workspace; returns ((first_wait_ns, second_wait_ns), (code, detail))."""
+    ws = workspace if workspace is not None else Workspace(256, device)
+    waits = (I64 * 2)()
+    _call("msa_check_bounded_wait", _ptr(ws.buf), _stream(ws.buf.device), waits)
+    return (waits[0], waits[1]), ws.read_device_error()

@@ -118,6 +118,22 @@ msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64
   return MSA_OK;
 }
 
+msa_status msa_check_bounded_wait(void* workspace, void* stream, int64_t* waits_ns) {
+  if (!workspace || !waits_ns) return MSA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MSA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // the two durations go to the header, after the error word
+  long long* dev_waits = reinterpret_cast<long long*>(ws + 64);
+  long long h[2] = {0, 0};
+  if (launch_wait_check(reinterpret_cast<DevError*>(ws), dev_waits, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemcpyAsync(h, dev_waits, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  waits_ns[0] = h[0];
+  waits_ns[1] = h[1];
+  return MSA_OK;
+}
+
 const char* msa_status_string(msa_status s) {
   switch (s) {
     case MSA_OK: return "ok";

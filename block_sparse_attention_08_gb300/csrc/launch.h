@@ -42,6 +42,7 @@ size_t pack_workspace_bytes(int batch, int seq);
 msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
                              int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,
                              uint8_t* ws, cudaStream_t stream);
+cudaError_t launch_wait_check(DevError* err, long long* waits_ns, cudaStream_t stream);
 msa_status run_gather(const void* src, const int64_t* rows, long long n, long long row_bytes, void* dst,
                       cudaStream_t stream, bool scatter);
 

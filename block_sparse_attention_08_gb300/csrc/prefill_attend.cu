@@ -789,8 +789,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.stage_full[wg]);
+      bool staged = true;
+      if (issuer) staged = mbar_wait(&sm.stage_full[wg], k & 1, err, 726);
+      if (!__all_sync(0xffffffffu, staged)) break;  // the whole warp leaves together
       if (issuer) {
-        if (!mbar_wait(&sm.stage_full[wg], k & 1, err, 726)) break;
         for (int e = 0; e < cnt; ++e) {
           const int row = static_cast<int>((static_cast<long long>(g) * per_head + ents[e]) * kGroup);
           tma_store_2d(&pmap, sm.ostage[wg] + e * kBmQBox, 0, row);

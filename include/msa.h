@@ -123,6 +123,22 @@ msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64
 /* Human-readable name of a status. */
 const char* msa_status_string(msa_status status);
 
+/* Diagnostic of the library's bounded on-chip waits (every pipeline wait of
+ * every kernel above uses them).  Launches one CTA on `stream` whose first
+ * thread waits on a shared-memory mbarrier that nothing ever arrives on, then
+ * on a second such barrier, and returns.  Each wait gives up after the
+ * library's wait limit (200 ms of GPU global time); the first records
+ * MSA_DEVERR_TIMEOUT with detail 900 in the device error word of `workspace`
+ * (the second finds the word taken and leaves it).  `workspace` is any
+ * initialised workspace (only its first 256 bytes are used); `waits_ns`
+ * (host, 2 entries) receives the duration of each wait in nanoseconds, or -1
+ * for a wait that completed (which would be a library defect).  The device
+ * error word is left for msa_read_device_error.  Synchronises `stream`.
+ * Errors: MSA_ERR_NULL for a null workspace or waits_ns; MSA_ERR_WORKSPACE
+ * for a workspace not 256-byte aligned; MSA_ERR_CUDA for a failed launch or
+ * copy. */
+msa_status msa_check_bounded_wait(void* workspace, void* stream, int64_t* waits_ns);
+
 /* ---- step 1+2, decode: block scores + top-k ---------------------------------
  * One query per request at position seq_lens[r]-1 over keys 0..seq_lens[r]-1
  * (the query's own key is already in the cache).  Score of block b for index

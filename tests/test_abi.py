@@ -136,6 +136,13 @@ def test_pack_validation(lib):
     assert lib.msa_unpack(FAKE, FAKE, 10, 5, 32, FAKE, None) == SHAPE
 
 
+def test_bounded_wait_check_validation(lib):
+    waits = (ctypes.c_int64 * 2)()
+    assert lib.msa_check_bounded_wait(None, None, waits) == NULL
+    assert lib.msa_check_bounded_wait(FAKE, None, None) == NULL
+    assert lib.msa_check_bounded_wait(FAKE + 16, None, waits) == WORKSPACE
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert lib.msa_status_string(s)
