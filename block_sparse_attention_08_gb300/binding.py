@@ -241,10 +241,11 @@ def msa_select_blocks_prefill(index_q, index_k, cu_seqlens, max_seqlen, *, topk=
                               local_blocks=1, q2k=None, workspace=None):
     """q2k int32 [4, tokens, topk] for packed documents (C: msa_select_blocks_prefill)."""
     T = index_q.shape[0]
-    _need(index_q, "index_q", torch.bfloat16, (T, G, DI))
-    _need(index_k, "index_k", torch.bfloat16, (T, 1, DI))
+    idt = _index_dtype(index_q)
+    _need(index_q, "index_q", index_q.dtype, (T, G, DI))
+    _need(index_k, "index_k", index_q.dtype, (T, 1, DI))
     _need(cu_seqlens, "cu_seqlens", torch.int32, (None,))
-    cfg = make_config(topk, init_blocks, local_blocks, "bf16")
+    cfg = make_config(topk, init_blocks, local_blocks, idt)
     dev = index_q.device
     if q2k is None:
         q2k = torch.empty((G, T, topk), dtype=torch.int32, device=dev)

@@ -217,7 +217,6 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
                                      int32_t* q2k, void* workspace, size_t workspace_bytes, void* stream) {
   msa_status st = msa_config_check(cfg);
   if (st != MSA_OK) return st;
-  if (cfg->index_dtype != MSA_INDEX_BF16) return MSA_ERR_DTYPE;
   if (!index_q || !index_k || !q2k) return MSA_ERR_NULL;
   if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
   if (!aligned16(index_q) || !aligned16(index_k) || !aligned16(q2k)) return MSA_ERR_ALIGN;

@@ -2,18 +2,21 @@
 // fused into one tensor-core kernel.
 //
 // NeMo "...minimax_m3_vl.msa", MSAMicrobatch.select_blocks and
-// _SelectionPlan.select: bf16 index_q [tokens, 4, 128] against index_k
+// _SelectionPlan.select: bf16 or E4M3 index_q [tokens, 4, 128] against index_k
 // [tokens, 1, 128] -> int32 q2k [4, tokens, 16], a hard top-k over the
 // unnormalised QK maxima of each causal, document-local 128-key block, with the
 // candidate / forced [tokens, blocks] masks of the plan; TensorRT-LLM
 // "MiniMaxM3SparseAttentionConfig" fields sparse_score_type 'max',
-// sparse_init_blocks, sparse_local_blocks.
+// sparse_init_blocks, sparse_local_blocks, indexer_kv_dtype (bf16 or unscaled
+// E4M3).
 //
 // GB300 design.  One work unit is (document, 128-token query block, pair of
 // index heads).  A TMA producer warp loads the two 128x128 index-Q tiles once
 // and then streams the document's causal key blocks (128 keys x 128 dims of
 // index_k each) through a 3-deep shared-memory ring; an MMA warp issues
-// tcgen05.mma (M=128 tokens, N=128 keys, K=128, bf16 -> fp32) into a
+// tcgen05.mma (M=128 tokens, N=128 keys, K=128; bf16 with kind::f16, or E4M3
+// with kind::f8f6f4, where a 128-dim row is one 128-byte swizzle atom; fp32
+// accumulate) into a
 // double-buffered tensor-memory accumulator (2 heads x 2 buffers x 128
 // columns = all 512 columns); four epilogue warps read the scores back with
 // tcgen05.ld (one token row per thread), take the causal block max and insert
@@ -28,10 +31,22 @@
 namespace msa {
 
 constexpr int kPsStages = 3;
-constexpr int kPsTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-dim boxes)
+constexpr int kPsTile = 128 * 128 * 2;  // one 128x128 bf16 tile (two 64-dim boxes); E4M3 uses the first half
 constexpr int kPsBox = 128 * 128;       // 128 rows x 128 bytes
 constexpr int kPsThreads = 192;         // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr uint32_t kPsIdesc = tc::idesc_bf16_f32(128, 128);
+// kind::f8f6f4 instruction descriptor: E4M3 A and B (format 0), fp32 D, M = N = 128
+constexpr uint32_t kPsIdescE4m3 = (1u << 4) | (static_cast<uint32_t>(128 >> 3) << 17) |
+                                  (static_cast<uint32_t>(128 >> 4) << 24);
+
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 struct PsSmem {
   alignas(1024) uint8_t a[2][kPsTile];          // index-Q tiles of the head pair
@@ -200,6 +215,9 @@ __device__ __forceinline__ void write_row(int32_t* row, const TopList& L, int ne
   }
 }
 
+// kE4M3: the index tensors hold E4M3 bytes (one 128-byte box per tile row
+// block) instead of bf16 (two 64-dim boxes).
+template <int kE4M3>
 __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap, PsPlan plan,
     long long total_tokens, int32_t* __restrict__ q2k, int topk, int init, int local, DevError* err) {
@@ -243,18 +261,19 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
         const Unit x = unit_of(plan, u);
         if (x.qb + 1 <= topk) continue;
         mbar_wait(&sm.a_empty, (nunit & 1) ^ 1, err, 400);
-        mbar_expect_tx(&sm.a_full, 2 * kPsTile);
+        constexpr int kTileBytes = kE4M3 ? kPsBox : kPsTile;
+        mbar_expect_tx(&sm.a_full, 2 * kTileBytes);
         const int row = x.start + x.qb * kBlock;
         for (int hh = 0; hh < 2; ++hh) {
           tma_load_3d(sm.a[hh], &qmap, 0, 2 * x.hp + hh, row, &sm.a_full);
-          tma_load_3d(sm.a[hh] + kPsBox, &qmap, 64, 2 * x.hp + hh, row, &sm.a_full);
+          if (!kE4M3) tma_load_3d(sm.a[hh] + kPsBox, &qmap, 64, 2 * x.hp + hh, row, &sm.a_full);
         }
         for (int b = 0; b <= x.qb; ++b, ++bc) {
           const int s = bc % kPsStages;
           mbar_wait(&sm.b_empty[s], ((bc / kPsStages) & 1) ^ 1, err, 401);
-          mbar_expect_tx(&sm.b_full[s], kPsTile);
+          mbar_expect_tx(&sm.b_full[s], kTileBytes);
           tma_load_2d(sm.b[s], &kmap, 0, x.start + b * kBlock, &sm.b_full[s]);
-          tma_load_2d(sm.b[s] + kPsBox, &kmap, 64, x.start + b * kBlock, &sm.b_full[s]);
+          if (!kE4M3) tma_load_2d(sm.b[s] + kPsBox, &kmap, 64, x.start + b * kBlock, &sm.b_full[s]);
         }
         ++nunit;
       }
@@ -280,10 +299,18 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
           for (int hh = 0; hh < 2; ++hh) {
             const uint32_t asm_ = smem_u32(sm.a[hh]);
             const uint32_t d = tmem + static_cast<uint32_t>((buf * 2 + hh) * 128);
+            if (kE4M3) {
+              // K = 32 E4M3 values (32 bytes) per MMA: four steps through the 128-byte row
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kPsBox + (kk & 3) * 32;
-              tc::mma_bf16(d, tc::desc_k_sw128(asm_ + off), tc::desc_k_sw128(bsm + off), kPsIdesc, kk > 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_e4m3_ss(d, tc::desc_k_sw128(asm_ + kk * 32), tc::desc_k_sw128(bsm + kk * 32), kPsIdescE4m3,
+                            kk > 0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * kPsBox + (kk & 3) * 32;
+                tc::mma_bf16(d, tc::desc_k_sw128(asm_ + off), tc::desc_k_sw128(bsm + off), kPsIdesc, kk > 0);
+              }
             }
           }
           tc::commit(&sm.b_empty[s]);
@@ -388,25 +415,31 @@ cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, co
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
+  // bf16: 64-dim boxes (the 128-byte swizzle bounds a box row at 128 bytes);
+  // E4M3: the whole 128-byte row in one box
+  const bool e4m3 = cfg.index_dtype == MSA_INDEX_E4M3;
+  const CUtensorMapDataType dt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t esz = e4m3 ? 1 : 2;
+  const cuuint32_t bx = e4m3 ? 128 : 64;
   CUtensorMap qmap, kmap;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(kKvHeads),
                           static_cast<cuuint64_t>(total_tokens)};
-    cuuint64_t strides[2] = {kIdxDim * 2, kKvHeads * kIdxDim * 2};
-    cuuint32_t box[3] = {64, 1, 128};
+    cuuint64_t strides[2] = {kIdxDim * esz, kKvHeads * kIdxDim * esz};
+    cuuint32_t box[3] = {bx, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(index_q), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(&qmap, dt, 3, const_cast<void*>(index_q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kIdxDim), static_cast<cuuint64_t>(total_tokens)};
-    cuuint64_t strides[1] = {kIdxDim * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint64_t strides[1] = {kIdxDim * esz};
+    cuuint32_t box[2] = {bx, 128};
     cuuint32_t estr[2] = {1, 1};
-    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(index_k), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(&kmap, dt, 2, const_cast<void*>(index_k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -415,9 +448,17 @@ cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, co
   int grid = static_cast<int>(2 * tiles_upper < kNumSMs ? 2 * tiles_upper : kNumSMs);
   if (grid < 1) grid = 1;
   const size_t smem = sizeof(PsSmem) + 1024;
-  cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  prefill_select_kernel<<<grid, kPsThreads, smem, stream>>>(qmap, kmap, plan, total_tokens, q2k, cfg.topk,
-                                                            cfg.init_blocks, cfg.local_blocks, err);
+  if (e4m3) {
+    cudaFuncSetAttribute(prefill_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    prefill_select_kernel<1><<<grid, kPsThreads, smem, stream>>>(qmap, kmap, plan, total_tokens, q2k, cfg.topk,
+                                                                 cfg.init_blocks, cfg.local_blocks, err);
+  } else {
+    cudaFuncSetAttribute(prefill_select_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    prefill_select_kernel<0><<<grid, kPsThreads, smem, stream>>>(qmap, kmap, plan, total_tokens, q2k, cfg.topk,
+                                                                 cfg.init_blocks, cfg.local_blocks, err);
+  }
   return cudaGetLastError();
 }
 

@@ -208,12 +208,14 @@ msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const 
  * d spanning [cu_seqlens[d], cu_seqlens[d+1]); token t of document d has
  * position p = t - cu_seqlens[d] and candidate blocks 0..p/128 of its own
  * document; the diagonal block's score covers keys <= p only.
- *   index_q    dev [total_tokens, 4, 128] bf16 (post norm and RoPE)
- *   index_k    dev [total_tokens, 1, 128] bf16
+ *   index_q    dev [total_tokens, 4, 128] bf16, or E4M3 bytes when
+ *              cfg->index_dtype is MSA_INDEX_E4M3 (post norm and RoPE)
+ *   index_k    dev [total_tokens, 1, 128], same dtype as index_q
  *   cu_seqlens dev int32 [num_docs + 1], cu_seqlens[0] = 0, strictly increasing,
  *              cu_seqlens[num_docs] = total_tokens; max_seqlen = the longest document
  *   q2k        dev int32 [4, total_tokens, topk]
- * Only the bf16 index dtype is accepted here (MSA_ERR_DTYPE otherwise). */
+ * E4M3 scores are unscaled dot products of the decoded values, accumulated in
+ * fp32 (TRT indexer_kv_dtype). */
 msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
                                      const void* index_k, const int32_t* cu_seqlens, int num_docs,
                                      int64_t total_tokens, int max_seqlen, int32_t* q2k,

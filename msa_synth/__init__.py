@@ -200,7 +200,7 @@ def doc_lengths_from_map(ids: np.ndarray) -> list[int]:
     return out
 
 
-# ---- the five named workloads ------------------------------------------------
+# ---- the named workloads -------------------------------------------------------
 
 WORKLOADS = {
     "decode_b4_ctx8k_contig": "decode, 4 requests x 8192-token contexts, contiguous cache, bf16 index",
@@ -208,6 +208,7 @@ WORKLOADS = {
     "prefill_1doc_16k": "prefill, one 16384-token document, bf16 index",
     "prefill_packed_2x32k": "packed prefill, 2 rows x 32768 tokens, log-uniform documents, init=1",
     "decode_b16_ctx128k_paged_e4m3": "decode, 16 requests x 131072-token contexts, paged, E4M3 index",
+    "prefill_1doc_16k_e4m3": "prefill, one 16384-token document, E4M3 index",
 }
 
 
@@ -227,6 +228,8 @@ def workload(name: str, *, seed: int = 0, device="cpu", scale_down: int = 1, max
                              max_blocks=(65536 // scale_down + BLOCK - 1) // BLOCK)
     if name == "prefill_1doc_16k":
         return prefill_inputs([max(16384 // scale_down, 1)], seed=seed, device=device)
+    if name == "prefill_1doc_16k_e4m3":
+        return prefill_inputs([max(16384 // scale_down, 1)], seed=seed, device=device, index_dtype="e4m3")
     if name == "prefill_packed_2x32k":
         ids = packed_doc_map(2, 32768 // scale_down, max_len=max(16384 // scale_down, 64),
                              max_pad=1024 // scale_down, seed=seed)

@@ -110,8 +110,8 @@ def test_attend_and_prefill_validation(lib):
                                         32768, ctypes.c_float(0.1), FAKE, FAKE, 1 << 30, None) == NULL
     assert lib.msa_sparse_attend_decode(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, 64,
                                         32768, ctypes.c_float(0.1), FAKE + 4, FAKE, 1 << 30, None) == ALIGN
-    e4 = _cfg(index_dtype=1)
-    assert lib.msa_select_blocks_prefill(ctypes.byref(e4), FAKE, FAKE, FAKE, 1, 128, 128, FAKE, FAKE, 1 << 30,
+    bad = _cfg(index_dtype=5)  # neither bf16 nor E4M3
+    assert lib.msa_select_blocks_prefill(ctypes.byref(bad), FAKE, FAKE, FAKE, 1, 128, 128, FAKE, FAKE, 1 << 30,
                                          None) == DTYPE
     assert lib.msa_select_blocks_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 0, 128, 128, FAKE, FAKE, 1 << 30,
                                          None) == SHAPE

@@ -46,6 +46,21 @@ def test_prefill_small(topk, init, local):
     _check(p, topk=topk, init=init, local=local)
 
 
+@pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (16, 1, 1), (3, 0, 0)])
+def test_prefill_e4m3_small(topk, init, local):
+    # unscaled E4M3 index (the decoded values' dot products, fp32 accumulate)
+    p = msa_synth.prefill_inputs(DOCS, seed=21 + topk + init, device="cuda", index_dtype="e4m3")
+    assert p.index_q.dtype == torch.float8_e4m3fn
+    _check(p, topk=topk, init=init, local=local, attend=(topk == 16 and init == 0))
+
+
+def test_prefill_e4m3_repeated_calls_are_identical():
+    p = msa_synth.prefill_inputs([2500, 300], seed=6, device="cuda", index_dtype="e4m3")
+    a = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
+    for _ in range(2):
+        assert torch.equal(a, msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen))
+
+
 def test_prefill_single_short_document():
     p = msa_synth.prefill_inputs([37], seed=1, device="cuda")
     _check(p)
@@ -110,6 +125,12 @@ def _sample_tokens(cu, n, seed):
 def test_prefill_workload_1doc_16k():
     p = msa_synth.workload("prefill_1doc_16k", device="cuda")
     _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 0))
+
+
+@pytest.mark.slow
+def test_prefill_workload_1doc_16k_e4m3():
+    p = msa_synth.workload("prefill_1doc_16k_e4m3", device="cuda")
+    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 2), attend=False)
 
 
 @pytest.mark.slow
