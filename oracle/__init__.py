@@ -19,6 +19,10 @@ Which statement on the pages each function follows:
   * ``attend_prefill`` / ``attend_decode`` -- sparse GQA attention over the
     selected blocks: the TensorRT-LLM class description and NeMo
     ``sparse_attention`` / ``_SparseAttention.forward``.
+  * ``attend_prefill_backward`` -- gradients of the sparse attention (NeMo
+    ``_SparseAttention.backward``: grad_out -> dq, dk, dv), written out from
+    the forward; ``attend_loss_f64`` -- the forward on fp64 inputs reduced to
+    sum(out * dout), whose finite differences pin the backward.
   * ``pack_metadata`` / ``pack`` / ``unpack`` -- NeMo layout-from-doc_ids
     constructor, ``_contiguous_runs``, ``MSAMicrobatch.pack`` / ``unpack``.
 """
@@ -74,6 +78,9 @@ def _load():
             lib.oracle_select_decode.argtypes = [P, P, I, P, P, P, I, P, I64, I, I, I, P, P]
             lib.oracle_attend_decode.argtypes = [P, P, P, P, P, P, I, P, I64, P, I, Dbl, P]
             lib.oracle_pack_metadata.argtypes = [P, I64, I64, P, P, P, P, P, P]
+            lib.oracle_attend_prefill_backward.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl, P, P, P]
+            lib.oracle_attend_loss_f64.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl]
+            lib.oracle_attend_loss_f64.restype = Dbl
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = Dbl
             for f in (lib.oracle_select_prefill, lib.oracle_attend_prefill,
@@ -161,6 +168,33 @@ def attend_prefill(q, k, v, cu_seqlens, tokens, q2k, scale):
     lib.oracle_attend_prefill(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cu), cu.shape[0] - 1, _ptr(tok), n,
                               _ptr(q2k), topk, float(scale), _ptr(out))
     return out
+
+
+def attend_prefill_backward(q, k, v, dout, cu_seqlens, q2k, scale):
+    """fp64 (dq [T, H, D], dk [T, G, D], dv [T, G, D]) for every compact token,
+    given bf16 q, k, v, grad_out and the q2k rows of all tokens [G, T, topk]."""
+    lib = _load()
+    qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(dout)
+    cu = _i32(cu_seqlens)
+    q2k = _i32(q2k)
+    T, topk = q2k.shape[1], q2k.shape[2]
+    dq = np.zeros((T, H, D), dtype=np.float64)
+    dk = np.zeros((T, G, D), dtype=np.float64)
+    dv = np.zeros((T, G, D), dtype=np.float64)
+    lib.oracle_attend_prefill_backward(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(db), _ptr(cu), cu.shape[0] - 1, T,
+                                       _ptr(q2k), topk, float(scale), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
+
+
+def attend_loss_f64(q, k, v, dout, cu_seqlens, q2k, scale):
+    """sum(out * dout) of the forward on fp64 numpy inputs q [T, H, D],
+    k / v [T, G, D], dout [T, H, D] (no bf16 rounding anywhere)."""
+    lib = _load()
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    cu = _i32(cu_seqlens)
+    q2k = _i32(q2k)
+    return lib.oracle_attend_loss_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(cu), cu.shape[0] - 1,
+                                      q2k.shape[1], _ptr(q2k), q2k.shape[2], float(scale))
 
 
 def select_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None,

@@ -216,6 +216,74 @@ static void attend_query(const uint16_t* q_row /* [H][D] */,
   free(z);
 }
 
+/* ---- backward of step 3 --------------------------------------------------
+ * [NEMO] _SparseAttention.backward maps grad_out [tokens, 64, 128] to dq
+ * [tokens, 64, 128] and dk / dv [tokens, 4, 128].  Written out from the
+ * forward above: with z_p = scale <q_h, k_p> over the keys J of query head h,
+ * P = softmax(z), out_h = sum_p P_p v_p and dO_h = d loss / d out_h,
+ *   dv_p += P_p dO_h,   dP_p = <dO_h, v_p>,   D_h = sum_p P_p dP_p,
+ *   dz_p  = P_p (dP_p - D_h),
+ *   dq_h += scale sum_p dz_p k_p,   dk_p += scale dz_p q_h.
+ * One query token of one kv head; dk / dv of its keys accumulate into the
+ * caller's arrays (the caller gives each kv head to one thread). */
+static void attend_query_backward(const uint16_t* q_row /* [H][D] */, const uint16_t* dout_row /* [H][D] */,
+                                  const uint16_t* k, const uint16_t* v, int64_t start, int64_t pos,
+                                  const int32_t* q2k_row /* [topk] for kv head g */, int topk, int g,
+                                  double scale, double* dq_row /* [H][D] */,
+                                  double* dk /* [T][G][D] */, double* dv /* [T][G][D] */) {
+  int64_t nkeys_max = (int64_t)topk * OR_BLOCK;
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)nkeys_max);
+  double* z = (double*)malloc(sizeof(double) * (size_t)nkeys_max);
+  double* dp = (double*)malloc(sizeof(double) * (size_t)nkeys_max);
+  int64_t nk = 0;
+  for (int i = 0; i < topk; ++i) {
+    int32_t b = q2k_row[i];
+    if (b < 0) continue;
+    for (int64_t p = (int64_t)b * OR_BLOCK; p < (int64_t)(b + 1) * OR_BLOCK && p <= pos; ++p) keys[nk++] = start + p;
+  }
+  for (int hh = 0; hh < OR_HEADS / OR_KV; ++hh) {
+    int h = g * (OR_HEADS / OR_KV) + hh;
+    double* dqh = dq_row + (int64_t)h * OR_DIM;
+    for (int c = 0; c < OR_DIM; ++c) dqh[c] = 0.0;
+    if (nk == 0) continue;
+    double zmax = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < OR_DIM; ++c)
+        acc += bf16_value(q_row[h * OR_DIM + c]) * bf16_value(k[(keys[j] * OR_KV + g) * OR_DIM + c]);
+      z[j] = scale * acc;
+      if (z[j] > zmax) zmax = z[j];
+    }
+    double denom = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      z[j] = exp(z[j] - zmax);
+      denom += z[j];
+    }
+    double D = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      z[j] /= denom; /* P_p */
+      double acc = 0.0;
+      for (int c = 0; c < OR_DIM; ++c)
+        acc += bf16_value(dout_row[h * OR_DIM + c]) * bf16_value(v[(keys[j] * OR_KV + g) * OR_DIM + c]);
+      dp[j] = acc;
+      D += z[j] * acc;
+    }
+    for (int64_t j = 0; j < nk; ++j) {
+      double dz = z[j] * (dp[j] - D);
+      double* dkp = dk + (keys[j] * OR_KV + g) * OR_DIM;
+      double* dvp = dv + (keys[j] * OR_KV + g) * OR_DIM;
+      for (int c = 0; c < OR_DIM; ++c) {
+        dqh[c] += scale * dz * bf16_value(k[(keys[j] * OR_KV + g) * OR_DIM + c]);
+        dkp[c] += scale * dz * bf16_value(q_row[h * OR_DIM + c]);
+        dvp[c] += z[j] * bf16_value(dout_row[h * OR_DIM + c]);
+      }
+    }
+  }
+  free(keys);
+  free(z);
+  free(dp);
+}
+
 /* ---- geometry ------------------------------------------------------------ */
 
 /* Document of compact token t: the d with cu[d] <= t < cu[d+1]. */
@@ -301,6 +369,79 @@ int oracle_attend_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* 
     free(rows);
   }
   return 0;
+}
+
+/* Prefill attention backward over every compact token: q2k [G][T][topk],
+ * grads in fp64: dq [T][H][D], dk and dv [T][G][D] (zeroed here).  One kv head
+ * per thread, so the dk / dv sums of a head are formed in one fixed order. */
+int oracle_attend_prefill_backward(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const uint16_t* dout, const int32_t* cu_seqlens, int num_docs,
+                                   int64_t total_tokens, const int32_t* q2k, int topk, double scale,
+                                   double* dq, double* dk, double* dv) {
+  memset(dk, 0, sizeof(double) * (size_t)(total_tokens * OR_KV * OR_DIM));
+  memset(dv, 0, sizeof(double) * (size_t)(total_tokens * OR_KV * OR_DIM));
+#pragma omp parallel for schedule(static, 1)
+  for (int g = 0; g < OR_KV; ++g) {
+    for (int64_t t = 0; t < total_tokens; ++t) {
+      int d = doc_of(cu_seqlens, num_docs, t);
+      int64_t start = cu_seqlens[d];
+      attend_query_backward(q + t * OR_HEADS * OR_DIM, dout + t * OR_HEADS * OR_DIM, k, v, start, t - start,
+                            q2k + ((int64_t)g * total_tokens + t) * topk, topk, g, scale,
+                            dq + t * OR_HEADS * OR_DIM, dk, dv);
+    }
+  }
+  return 0;
+}
+
+/* The forward of step 3 on fp64 inputs (no bf16 rounding), reduced to the
+ * scalar loss sum_{t,h,c} out[t][h][c] * dout[t][h][c]: the function whose
+ * finite differences pin the backward above.  Arrays are fp64 [T][H][D] and
+ * [T][G][D]; q2k [G][T][topk]. */
+double oracle_attend_loss_f64(const double* q, const double* k, const double* v, const double* dout,
+                              const int32_t* cu_seqlens, int num_docs, int64_t total_tokens,
+                              const int32_t* q2k, int topk, double scale) {
+  double loss = 0.0;
+  int64_t nkeys_max = (int64_t)topk * OR_BLOCK;
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)nkeys_max);
+  double* z = (double*)malloc(sizeof(double) * (size_t)nkeys_max);
+  for (int64_t t = 0; t < total_tokens; ++t) {
+    int d = doc_of(cu_seqlens, num_docs, t);
+    int64_t start = cu_seqlens[d], pos = t - start;
+    for (int g = 0; g < OR_KV; ++g) {
+      int64_t nk = 0;
+      for (int i = 0; i < topk; ++i) {
+        int32_t b = q2k[((int64_t)g * total_tokens + t) * topk + i];
+        if (b < 0) continue;
+        for (int64_t p = (int64_t)b * OR_BLOCK; p < (int64_t)(b + 1) * OR_BLOCK && p <= pos; ++p)
+          keys[nk++] = start + p;
+      }
+      if (nk == 0) continue;
+      for (int hh = 0; hh < OR_HEADS / OR_KV; ++hh) {
+        int h = g * (OR_HEADS / OR_KV) + hh;
+        const double* qh = q + (t * OR_HEADS + h) * OR_DIM;
+        double zmax = -INFINITY, denom = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+          double acc = 0.0;
+          for (int c = 0; c < OR_DIM; ++c) acc += qh[c] * k[(keys[j] * OR_KV + g) * OR_DIM + c];
+          z[j] = scale * acc;
+          if (z[j] > zmax) zmax = z[j];
+        }
+        for (int64_t j = 0; j < nk; ++j) {
+          z[j] = exp(z[j] - zmax);
+          denom += z[j];
+        }
+        const double* doh = dout + (t * OR_HEADS + h) * OR_DIM;
+        for (int64_t j = 0; j < nk; ++j) {
+          double acc = 0.0;
+          for (int c = 0; c < OR_DIM; ++c) acc += doh[c] * v[(keys[j] * OR_KV + g) * OR_DIM + c];
+          loss += z[j] / denom * acc;
+        }
+      }
+    }
+  }
+  free(keys);
+  free(z);
+  return loss;
 }
 
 /* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n]. */
