@@ -180,6 +180,76 @@ def _staging(tensors, device):
     return host, dev, views
 
 
+def run_backward(args, device, config):
+    """One step = one msa_sparse_attend_prefill_backward call over the workload
+    (dq, dk, dv from q, k, v, q2k, the forward's out and log-sum-exp and a
+    seeded grad_out, all resident), replayed from a CUDA graph, L2 flushed
+    between steps.  Work: five 128-wide GEMM passes per attended key (S, dP,
+    dV, dK, dQ) against the forward's two, so 2.5 x the forward's FLOPs."""
+    import block_sparse_attention_08_gb300 as msa
+    torch.cuda.set_device(device)
+    p = msa_synth.workload(args.workload, seed=args.seed, device=device, scale_down=args.scale_down)
+    T = p.total_tokens
+    q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=p.topk,
+                                        init_blocks=p.init_blocks, local_blocks=p.local_blocks)
+    lse = torch.empty((T, 64), dtype=torch.float32, device=device)
+    out = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE, lse=lse)
+    gen = torch.Generator(device="cpu").manual_seed(args.seed + 1)
+    dout = torch.randn((T, 64, 128), generator=gen).to(torch.bfloat16).to(device)
+    dq = torch.empty_like(p.q)
+    dk = torch.empty_like(p.k)
+    dv = torch.empty_like(p.v)
+
+    def bwd():
+        msa.msa_sparse_attend_prefill_backward(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, out, lse, dout,
+                                               scale=SCALE, dq=dq, dk=dk, dv=dv)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        bwd()
+    torch.cuda.synchronize()
+    run = bwd
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                bwd()
+        stream.wait_stream(cap)
+        run = g.replay
+        run()
+        torch.cuda.synchronize()
+    hbm_peak, tf_peak, peak_src = _peaks()
+    ms_all = []
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 255)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            b.record(stream)
+            b.synchronize()
+            ms_all.append(a.elapsed_time(b))
+    ms = sum(ms_all) / len(ms_all)
+    _, f_att = prefill_work(p, q2k)
+    flop = 2.5 * f_att
+    tf = flop / (ms * 1e-3) / 1e12
+    config.update({"pass": "attention backward (dq, dk, dv)", "queries_per_step": T,
+                   "timing": "eager C-ABI call" if args.no_graph else "CUDA-graph replay of the C-ABI call",
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)"})
+    return {"metric": "prefill attention backward: query tokens/s; TFLOP/s", "value": round(T / (ms * 1e-3), 1),
+            "unit": "query tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": config,
+            "roofline": {"bound": "tensor", "kernel": "msa_sparse_attend_prefill_backward (bucketing, "
+                         "bw_rowdot_kernel, bw_attend_kernel, bw_to_bf16_kernel)", "achieved": round(tf, 2),
+                         "peak": tf_peak, "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4), "traffic": None,
+                         "flop": flop, "peak_source": peak_src + " bf16_tflops (burst)"},
+            "gpu_launches": 10 * args.steps, "clocks": clk.summary()}
+
+
 def run_gpu(args, rank, world, device):
     import block_sparse_attention_08_gb300 as msa
     torch.cuda.set_device(device)
@@ -416,6 +486,8 @@ def main():
                     help="divide the workload's lengths by this factor (small profiling cases)")
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of a decode workload (small profiling cases)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the attention backward of a prefill workload instead of the forward step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -431,6 +503,12 @@ def main():
         config["requests"] = args.requests
     if args.scale_down > 1:
         config["scale_down"] = args.scale_down
+
+    if args.backward:
+        if args.impl != "gb300" or not args.workload.startswith("prefill"):
+            raise SystemExit("--backward times the prefill attention backward of this library")
+        print(json.dumps(run_backward(args, torch.device("cuda", local), config)))
+        return
 
     if args.impl == "reference":
         if rank == 0:

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     msa_select_blocks_prefill,
     msa_sparse_attend_decode,
     msa_sparse_attend_prefill,
+    msa_sparse_attend_prefill_backward,
     msa_unpack,
     workspace_size,
 )

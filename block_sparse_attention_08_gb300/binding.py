@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 H, G, D, DI, BLOCK = 64, 4, 128, 128, 128
-MODE_DECODE, MODE_PREFILL, MODE_PACK = 0, 1, 2
+MODE_DECODE, MODE_PREFILL, MODE_PACK, MODE_PREFILL_BWD = 0, 1, 2, 3
 INDEX_DTYPES = {"bf16": 0, "e4m3": 1}
 DEVICE_ERRORS = {0: "none", 1: "page id outside the pool", 2: "block id outside the query's range",
                  3: "sequence length out of range", 4: "bounded on-chip wait gave up"}
@@ -51,6 +51,8 @@ _SIGS = {
     "msa_sparse_attend_decode": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, SZ, P],
     "msa_select_blocks_prefill": [CFG, P, P, P, I, I64, I, P, P, SZ, P],
     "msa_sparse_attend_prefill": [CFG, P, P, P, P, P, I, I64, I, F, P, P, SZ, P],
+    "msa_sparse_attend_prefill_lse": [CFG, P, P, P, P, P, I, I64, I, F, P, P, P, SZ, P],
+    "msa_sparse_attend_prefill_backward": [CFG, P, P, P, P, P, I, I64, I, F, P, P, P, P, P, P, P, SZ, P],
     "msa_pack_metadata": [P, I, I, P, P, ctypes.POINTER(I), ctypes.POINTER(I64), ctypes.POINTER(I),
                           ctypes.POINTER(I64), P, SZ, P],
     "msa_pack": [P, P, I64, I64, P, P],
@@ -257,8 +259,11 @@ def msa_select_blocks_prefill(index_q, index_k, cu_seqlens, max_seqlen, *, topk=
     return q2k
 
 
-def msa_sparse_attend_prefill(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=None, out=None, workspace=None):
-    """bf16 out [tokens, 64, 128] for packed documents (C: msa_sparse_attend_prefill)."""
+def msa_sparse_attend_prefill(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=None, out=None, lse=None,
+                              workspace=None):
+    """bf16 out [tokens, 64, 128] for packed documents (C: msa_sparse_attend_prefill).  With ``lse``
+    (fp32 [tokens, 64]) the call also writes the log-sum-exp the backward needs
+    (C: msa_sparse_attend_prefill_lse)."""
     T = q.shape[0]
     _need(q, "q", torch.bfloat16, (T, H, D))
     _need(k, "k", torch.bfloat16, (T, G, D))
@@ -273,9 +278,46 @@ def msa_sparse_attend_prefill(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=Non
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     mt = (int(max_seqlen) + BLOCK - 1) // BLOCK
     ws = _workspace("prefill", workspace_size(cfg, MODE_PREFILL, T, mt), dev, workspace)
-    _call("msa_sparse_attend_prefill", ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q2k), _ptr(cu_seqlens),
-          cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    if lse is None:
+        _call("msa_sparse_attend_prefill", ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q2k),
+              _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(ws.buf),
+              ws.nbytes, _stream(dev))
+    else:
+        _need(lse, "lse", torch.float32, (T, H))
+        _call("msa_sparse_attend_prefill_lse", ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q2k),
+              _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(lse),
+              _ptr(ws.buf), ws.nbytes, _stream(dev))
     return out
+
+
+def msa_sparse_attend_prefill_backward(q, k, v, q2k, cu_seqlens, max_seqlen, out, lse, grad_out, *, scale=None,
+                                       dq=None, dk=None, dv=None, workspace=None):
+    """(dq [tokens, 64, 128], dk [tokens, 4, 128], dv [tokens, 4, 128]) bf16 from the forward's
+    out and lse and grad_out (C: msa_sparse_attend_prefill_backward)."""
+    T = q.shape[0]
+    _need(q, "q", torch.bfloat16, (T, H, D))
+    _need(k, "k", torch.bfloat16, (T, G, D))
+    _need(v, "v", torch.bfloat16, (T, G, D))
+    _need(q2k, "q2k", torch.int32, (G, T, None))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (None,))
+    _need(out, "out", torch.bfloat16, (T, H, D))
+    _need(lse, "lse", torch.float32, (T, H))
+    _need(grad_out, "grad_out", torch.bfloat16, (T, H, D))
+    cfg = make_config(q2k.shape[2], 0, 0)
+    dev = q.device
+    dq = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev) if dq is None else dq
+    dk = torch.empty((T, G, D), dtype=torch.bfloat16, device=dev) if dk is None else dk
+    dv = torch.empty((T, G, D), dtype=torch.bfloat16, device=dev) if dv is None else dv
+    _need(dq, "dq", torch.bfloat16, (T, H, D))
+    _need(dk, "dk", torch.bfloat16, (T, G, D))
+    _need(dv, "dv", torch.bfloat16, (T, G, D))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    mt = (int(max_seqlen) + BLOCK - 1) // BLOCK
+    ws = _workspace("prefill_bwd", workspace_size(cfg, MODE_PREFILL_BWD, T, mt), dev, workspace)
+    _call("msa_sparse_attend_prefill_backward", ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(q2k),
+          _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(lse),
+          _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return dq, dk, dv
 
 
 # ---- packing ----------------------------------------------------------------------

@@ -46,6 +46,9 @@ static Layout layout(int mode, long long n, int max_blocks, int topk) {
     off += up256(prefill_plan_ints(static_cast<int>(n), max_blocks) * sizeof(int));
     L.bm = off;
     off += up256(prefill_attend_bytes(n, max_blocks * kBlock, topk));
+  } else if (mode == MSA_MODE_PREFILL_BWD) {
+    L.bm = off;
+    off += up256(prefill_backward_bytes(n, max_blocks * kBlock, topk));
   }
   L.total = off;
   return L;
@@ -94,8 +97,8 @@ msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int ma
     *bytes = kHeaderBytes + pack_workspace_bytes(max_blocks, static_cast<int>(n / max_blocks));
     return MSA_OK;
   }
-  if (mode != MSA_MODE_DECODE && mode != MSA_MODE_PREFILL) return MSA_ERR_SHAPE;
-  if (mode == MSA_MODE_PREFILL && !prefill_attend_fits(n, max_blocks * kBlock, cfg->topk)) return MSA_ERR_SHAPE;
+  if (mode != MSA_MODE_DECODE && mode != MSA_MODE_PREFILL && mode != MSA_MODE_PREFILL_BWD) return MSA_ERR_SHAPE;
+  if (mode != MSA_MODE_DECODE && !prefill_attend_fits(n, max_blocks * kBlock, cfg->topk)) return MSA_ERR_SHAPE;
   *bytes = layout(mode, n, max_blocks, cfg->topk).total;
   return MSA_OK;
 }
@@ -230,10 +233,10 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
-msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
-                                     const int32_t* q2k, const int32_t* cu_seqlens, int num_docs,
-                                     int64_t total_tokens, int max_seqlen, float scale, void* out, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+static msa_status attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
+                                 const int32_t* q2k, const int32_t* cu_seqlens, int num_docs, int64_t total_tokens,
+                                 int max_seqlen, float scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   msa_status st = msa_config_check(cfg);
   if (st != MSA_OK) return st;
   if (!q || !k || !v || !q2k || !out) return MSA_ERR_NULL;
@@ -245,8 +248,48 @@ msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const
   if (!prefill_attend_fits(total_tokens, max_seqlen, cfg->topk)) return MSA_ERR_SHAPE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = launch_prefill_attend(q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, cfg->topk,
-                                        scale, out, ws + L.bm, reinterpret_cast<DevError*>(ws),
+                                        scale, out, lse, ws + L.bm, reinterpret_cast<DevError*>(ws),
                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
+                                     const int32_t* q2k, const int32_t* cu_seqlens, int num_docs,
+                                     int64_t total_tokens, int max_seqlen, float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return attend_prefill(cfg, q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, scale, out, nullptr,
+                        workspace, workspace_bytes, stream);
+}
+
+msa_status msa_sparse_attend_prefill_lse(const msa_config* cfg, const void* q, const void* k, const void* v,
+                                         const int32_t* q2k, const int32_t* cu_seqlens, int num_docs,
+                                         int64_t total_tokens, int max_seqlen, float scale, void* out, float* lse,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!lse) return MSA_ERR_NULL;
+  return attend_prefill(cfg, q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, scale, out, lse,
+                        workspace, workspace_bytes, stream);
+}
+
+msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void* q, const void* k, const void* v,
+                                              const int32_t* q2k, const int32_t* cu_seqlens, int num_docs,
+                                              int64_t total_tokens, int max_seqlen, float scale, const void* out,
+                                              const float* lse, const void* grad_out, void* dq, void* dk, void* dv,
+                                              void* workspace, size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!q || !k || !v || !q2k || !out || !lse || !grad_out || !dq || !dk || !dv) return MSA_ERR_NULL;
+  if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(grad_out) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+    return MSA_ERR_ALIGN;
+  const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
+  const Layout L = layout(MSA_MODE_PREFILL_BWD, total_tokens, max_tiles, cfg->topk);
+  if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
+  if (!prefill_attend_fits(total_tokens, max_seqlen, cfg->topk)) return MSA_ERR_SHAPE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_prefill_backward(q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, cfg->topk,
+                                          scale, out, lse, grad_out, dq, dk, dv, ws + L.bm,
+                                          reinterpret_cast<DevError*>(ws), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -36,8 +36,14 @@ size_t prefill_attend_bytes(long long total_tokens, int max_seqlen, int topk);
 bool prefill_attend_fits(long long total_tokens, int max_seqlen, int topk);
 cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, const int32_t* q2k,
                                   const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
-                                  int topk, float scale, void* out, uint8_t* region, DevError* err,
+                                  int topk, float scale, void* out, float* lse, uint8_t* region, DevError* err,
                                   cudaStream_t stream);
+size_t prefill_backward_bytes(long long total_tokens, int max_seqlen, int topk);
+cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v, const int32_t* q2k,
+                                    const int32_t* cu_seqlens, int num_docs, long long total_tokens,
+                                    int max_seqlen, int topk, float scale, const void* out, const float* lse,
+                                    const void* grad_out, void* dq, void* dk, void* dv, uint8_t* region,
+                                    DevError* err, cudaStream_t stream);
 size_t pack_workspace_bytes(int batch, int seq);
 msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
                              int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,

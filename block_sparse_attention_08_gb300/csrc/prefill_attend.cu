@@ -813,10 +813,14 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
 
 // One 256-thread block per (token, KV head): combines the token's partials
 // out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, M = max_j m_j.
-// Thread (h, c) owns dims 8c..8c+7 of head h of the group.
+// Thread (h, c) owns dims 8c..8c+7 of head h of the group.  With `lse`, the
+// log2 of the softmax denominator in the scaled-score base-2 domain,
+// M + log2(sum_j 2^(m_j - M) l_j), goes to lse[t][g * 16 + h] (-inf for a row
+// with no key): what the backward needs to rebuild P.
 __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict__ q2k,
                                                        const int32_t* __restrict__ cu, int num_docs, long long T,
-                                                       int topk, BmPlan p, __nv_bfloat16* __restrict__ out) {
+                                                       int topk, BmPlan p, __nv_bfloat16* __restrict__ out,
+                                                       float* __restrict__ lse) {
   const long long t = blockIdx.x;
   const int g = blockIdx.y;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
@@ -862,6 +866,7 @@ __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict
   o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
   o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
   *reinterpret_cast<uint4*>(out + ((t * kHeads) + g * kGroup + h) * kDim + 8 * c) = o;
+  if (lse && c == 0) lse[t * kHeads + g * kGroup + h] = L > 0.f ? Mu + log2f(L) : -INFINITY;
 }
 
 
@@ -901,7 +906,7 @@ bool prefill_attend_fits(long long total_tokens, int max_seqlen, int topk) {
 
 cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, const int32_t* q2k,
                                   const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
-                                  int topk, float scale, void* out, uint8_t* region, DevError* err,
+                                  int topk, float scale, void* out, float* lse, uint8_t* region, DevError* err,
                                   cudaStream_t stream) {
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
@@ -930,7 +935,449 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, pmap, p, total_tokens, topk,
                                                        scale * 1.4426950408889634f, err);
   bm_merge_kernel<<<dim3(static_cast<unsigned>(total_tokens), kKvHeads), 256, 0, stream>>>(
-      q2k, cu_seqlens, num_docs, total_tokens, topk, p, static_cast<__nv_bfloat16*>(out));
+      q2k, cu_seqlens, num_docs, total_tokens, topk, p, static_cast<__nv_bfloat16*>(out), lse);
+  return cudaGetLastError();
+}
+
+
+// ==== backward =======================================================================
+//
+// NeMo _SparseAttention.backward: grad_out [tokens, 64, 128] -> dq [tokens, 64,
+// 128], dk / dv [tokens, 4, 128] (bf16), with the forward's log-sum-exp.  For
+// query head h and key p of its selected causal keys, z = scale <q, k_p>,
+// P = 2^(z log2 e - lse), dP = <dO, v_p>, D = <dO, out>, dS = P (dP - D):
+//   dv_p += P dO,   dk_p += scale dS q,   dq += scale sum_p dS k_p.
+//
+// Same bucketing and tiles as the forward: a tile is 8 (query, KV head) entries
+// x 16 heads against one key block.  Per tile, five 128 x 128 x 128 tcgen05
+// products, with S (then dQ), dP and the block's dV and dK accumulators in
+// the four 128-column quarters of tensor memory:
+//   S  = Q K^T          (A = Q, B = K: both K-major)
+//   dP = dO V^T         (A = dO, B = V: both K-major)
+//   dV += P^T dO        (A = P^T, B = dO: both read MN-major)
+//   dK += dS^T Q        (A = dS^T, B = Q: both read MN-major)
+//   dQ = dS K           (A = dS K-major, B = K read MN-major)
+// Four math warps (one tile row per thread) turn S and dP into P and dS in
+// shared memory and add each tile's dQ rows to an fp32 accumulator with vector
+// atomics; when the tiles of one key block end (a run), the same warps (one
+// key row per thread) add the block's dK and dV to fp32 accumulators.  A last
+// kernel converts the three accumulators to bf16.  Everything is single
+// buffered: this is the first, correct form of the backward.
+constexpr int kBwThreads = 192;  // warps 0-3 math, 4 TMA, 5 MMA
+constexpr int kBwInfo = 4;
+constexpr uint32_t kIdescKK = tc::idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescKM = tc::idesc_bf16_f32(128, 128) | (1u << 16);               // B MN-major
+constexpr uint32_t kIdescMM = tc::idesc_bf16_f32(128, 128) | (1u << 15) | (1u << 16);  // A and B MN-major
+
+struct BwInfo {
+  int row0, g, cnt, fresh, last;  // last: the run's final tile
+  int ent[kBmEntries];
+};
+
+struct BwSmem {
+  alignas(1024) uint8_t q[kBmTile];     // the tile's Q rows
+  alignas(1024) uint8_t dout[kBmTile];  // the tile's dO rows
+  alignas(1024) uint8_t k[kBmTile];     // the block's K
+  alignas(1024) uint8_t v[kBmTile];     // the block's V
+  alignas(1024) uint8_t p[kBmTile];     // P, bf16 [rows][keys]
+  alignas(1024) uint8_t ds[kBmTile];    // dS, bf16 [rows][keys]
+  uint64_t info_full[kBwInfo], info_empty[kBwInfo];
+  uint64_t kv_full, kv_empty, qd_full, qd_empty;
+  uint64_t s_full, p_full, dq_full, dq_free, acc_full, acc_free, done;
+  BwInfo info[kBwInfo];
+  uint32_t tmem_base;
+};
+static_assert(sizeof(BwSmem) + 1024 <= 227 * 1024, "shared memory of the backward kernel");
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// D[t][h] = <dO[t][h], out[t][h]> (fp32, bf16 inputs): one warp per (token, head).
+__global__ void __launch_bounds__(256) bw_rowdot_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                        const __nv_bfloat16* __restrict__ out, long long rows,
+                                                        float* __restrict__ D) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(dout + row * kDim) + 2 * lane;
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(out + row * kDim) + 2 * lane;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 x = __bfloat1622float2(a[i]), y = __bfloat1622float2(b[i]);
+    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) D[row] = acc;
+}
+
+// fp32 accumulator -> bf16, eight values per thread.
+__global__ void __launch_bounds__(256) bw_to_bf16_kernel(const float* __restrict__ src, long long n8,
+                                                         __nv_bfloat16* __restrict__ dst) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(src)[2 * i], b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+  uint4 o;
+  o.x = pack_bf16(a.x, a.y);
+  o.y = pack_bf16(a.z, a.w);
+  o.z = pack_bf16(b.x, b.y);
+  o.w = pack_bf16(b.z, b.w);
+  reinterpret_cast<uint4*>(dst)[i] = o;
+}
+
+__global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, BmPlan p, long long T,
+    int topk, float scale, float scale_log2, const float* __restrict__ lse, const float* __restrict__ Dsum,
+    float* __restrict__ dq_acc, float* __restrict__ dk_acc, float* __restrict__ dv_acc, DevError* err) {
+  extern __shared__ uint8_t smem_raw[];
+  BwSmem& sm = *reinterpret_cast<BwSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = local_tiles(p.meta[1]);
+
+  if (tid == 0) {
+    for (int i = 0; i < kBwInfo; ++i) {
+      mbar_init(&sm.info_full[i], 1);
+      mbar_init(&sm.info_empty[i], 5);  // four math warps and the MMA thread
+    }
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.qd_full, 1);
+    mbar_init(&sm.qd_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 4);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, 4);
+    mbar_init(&sm.done, 1);
+    fence_mbar_init();
+  }
+  // Rows of entries a tile does not fill keep earlier (finite) data; start
+  // from zeros so that no NaN pattern meets a zero weight in an MMA.
+  for (int i = tid; i < 6 * kBmTile / 16; i += kBwThreads)
+    sts128(smem_u32(sm.q) + 16 * i, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tc::alloc(&sm.tmem_base, 512);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4) {
+    // ---------------- scheduler + TMA ----------------
+    if (lane == 0) {
+      prefetch_tmap(&qmap);
+      prefetch_tmap(&omap);
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+    }
+    const BmTile none{-1, -1, 0, 0};
+    BmTile d_next = n > 0 ? p.tiles[tile_at(0)] : none;
+    int e_next = lane < d_next.cnt ? p.elist[d_next.off + lane] : 0;
+    BmTile d_after = n > 1 ? p.tiles[tile_at(1)] : none;
+    int prow = -1, pg = -1, nkv = 0, nqd = 0;
+    for (int i = 0; i < n; ++i) {
+      const BmTile d = d_next;
+      const int ent = e_next;
+      d_next = d_after;
+      e_next = (i + 1 < n && lane < d_next.cnt) ? p.elist[d_next.off + lane] : 0;
+      d_after = i + 2 < n ? p.tiles[tile_at(i + 2)] : none;
+      const bool fresh = d.row0 != prow || d.g != pg;
+      const bool last = i + 1 == n || d_next.row0 != d.row0 || d_next.g != d.g;
+      const int is = i % kBwInfo;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&sm.info_empty[is], ((i / kBwInfo) & 1) ^ 1, err, 800);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane < kBmEntries) sm.info[is].ent[lane] = ent;
+      if (lane == 0) {
+        sm.info[is].row0 = d.row0;
+        sm.info[is].g = d.g;
+        sm.info[is].cnt = d.cnt;
+        sm.info[is].fresh = fresh ? 1 : 0;
+        sm.info[is].last = last ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_full[is]);
+      if (lane == 0) {
+        if (fresh) {
+          ok = mbar_wait(&sm.kv_empty, (nkv & 1) ^ 1, err, 801);
+          if (ok) {
+            mbar_expect_tx(&sm.kv_full, 2 * kBmTile);
+            tma_load_3d(sm.k, &kmap, 0, d.g, d.row0, &sm.kv_full);
+            tma_load_3d(sm.k + kBmHalf, &kmap, 64, d.g, d.row0, &sm.kv_full);
+            tma_load_3d(sm.v, &vmap, 0, d.g, d.row0, &sm.kv_full);
+            tma_load_3d(sm.v + kBmHalf, &vmap, 64, d.g, d.row0, &sm.kv_full);
+            ++nkv;
+          }
+        }
+        ok = ok && mbar_wait(&sm.qd_empty, (nqd & 1) ^ 1, err, 802);
+        if (ok) mbar_expect_tx(&sm.qd_full, d.cnt * 4 * kBmQBox);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (fresh) {
+        prow = d.row0;
+        pg = d.g;
+      }
+      if (lane < d.cnt) {
+        const int t = ent / topk;
+        tma_load_3d(sm.q + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.q + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.dout + lane * kBmQBox, &omap, 0, d.g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.dout + kBmHalf + lane * kBmQBox, &omap, 64, d.g * kGroup, t, &sm.qd_full);
+      }
+      __syncwarp();
+      ++nqd;
+    }
+    // no copy may still be landing when the CTA exits
+    if (lane == 0) {
+      if (nkv > 0) mbar_wait(&sm.kv_full, (nkv - 1) & 1, err, 803);
+      if (nqd > 0) mbar_wait(&sm.qd_full, (nqd - 1) & 1, err, 804);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int nkv = 0;
+      for (int i = 0; i < n; ++i) {
+        const int is = i % kBwInfo;
+        if (!mbar_wait(&sm.info_full[is], (i / kBwInfo) & 1, err, 810)) break;
+        const bool fresh = sm.info[is].fresh != 0, last = sm.info[is].last != 0;
+        mbar_arrive(&sm.info_empty[is]);
+        const int run = nkv;  // the run this tile belongs to is run - 1 after a fresh tile
+        if (fresh) {
+          if (!mbar_wait(&sm.kv_full, nkv & 1, err, 811)) break;
+          ++nkv;
+        }
+        if (!mbar_wait(&sm.qd_full, i & 1, err, 812)) break;
+        if (i > 0 && !mbar_wait(&sm.dq_free, (i - 1) & 1, err, 813)) break;  // S reuses the dQ columns
+        tc::fence_after();
+        const uint32_t qa = smem_u32(sm.q), oa = smem_u32(sm.dout), ka = smem_u32(sm.k), va = smem_u32(sm.v);
+        const uint32_t pa = smem_u32(sm.p), dsa = smem_u32(sm.ds);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kIdescKK, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + 128, tc::desc_k_sw128(oa + off), tc::desc_k_sw128(va + off), kIdescKK, kk > 0);
+        }
+        tc::commit(&sm.s_full);
+        if (!mbar_wait(&sm.p_full, i & 1, err, 814)) break;
+        // the previous run's dK / dV must be read out before a fresh tile restarts them
+        if (fresh && run > 0 && !mbar_wait(&sm.acc_free, (run - 1) & 1, err, 815)) break;
+        tc::fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(tmem + 256, desc_v_mn_sw128(pa + kk * 2048), desc_v_mn_sw128(oa + kk * 2048), kIdescMM,
+                       kk > 0 || !fresh);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(tmem + 384, desc_v_mn_sw128(dsa + kk * 2048), desc_v_mn_sw128(qa + kk * 2048), kIdescMM,
+                       kk > 0 || !fresh);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem, tc::desc_k_sw128(dsa + off), desc_v_mn_sw128(ka + kk * 2048), kIdescKM, kk > 0);
+        }
+        tc::commit(&sm.dq_full);
+        tc::commit(&sm.qd_empty);
+        if (last) {
+          tc::commit(&sm.acc_full);
+          tc::commit(&sm.kv_empty);
+        }
+      }
+      // every MMA has finished before tensor memory is released
+      tc::commit(&sm.done);
+      mbar_wait(&sm.done, 0, err, 816);
+    }
+  } else {
+    // ---------------- math warps 0-3 ----------------
+    const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
+    const uint32_t lrow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t ps = smem_u32(sm.p), dss = smem_u32(sm.ds);
+    int nacc = 0;
+    for (int i = 0; i < n; ++i) {
+      const int is = i % kBwInfo;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBwInfo) & 1, err, 820))) break;
+      const int cnt = sm.info[is].cnt, row0 = sm.info[is].row0, g = sm.info[is].g;
+      const bool last = sm.info[is].last != 0;
+      const bool valid = e < cnt;
+      const int ent = valid ? sm.info[is].ent[e] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_empty[is]);
+      const long long t = ent / topk;
+      const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - row0 + 1)) : 0;
+      const long long hrow = t * kHeads + g * kGroup + h;  // (token, query head)
+      const float lse_r = valid ? lse[hrow] : 0.f, d_r = valid ? Dsum[hrow] : 0.f;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, i & 1, err, 821))) break;
+      tc::fence_after();
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], dp[32];
+        tc::ld_32x32b_x32(lrow + ch * 32, sv);
+        tc::ld_32x32b_x32(lrow + 128 + ch * 32, dp);
+        tc::wait_ld();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int kc = ch * 32 + 2 * q;
+          const float pa = kc < nkeys ? ex2(fmaf(__uint_as_float(sv[2 * q]), scale_log2, -lse_r)) : 0.f;
+          const float pb = kc + 1 < nkeys ? ex2(fmaf(__uint_as_float(sv[2 * q + 1]), scale_log2, -lse_r)) : 0.f;
+          pk[q] = pack_bf16(pa, pb);
+          dk[q] = pack_bf16(pa * (__uint_as_float(dp[2 * q]) - d_r), pb * (__uint_as_float(dp[2 * q + 1]) - d_r));
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte row
+          const uint32_t off = (c16 >> 3) * kBmHalf + sw128(r, c16 & 7);
+          sts128(ps + off, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          sts128(dss + off, dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        }
+      }
+      tc::fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, i & 1, err, 822))) break;
+      tc::fence_after();
+      float* dqr = dq_acc + hrow * kDim;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(lrow + ch * 32, v);
+        tc::wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            red_add_v4(dqr + ch * 32 + 4 * j, scale * __uint_as_float(v[4 * j]), scale * __uint_as_float(v[4 * j + 1]),
+                       scale * __uint_as_float(v[4 * j + 2]), scale * __uint_as_float(v[4 * j + 3]));
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.dq_free);
+      if (last) {
+        // the run's dK and dV: thread r holds key row0 + r of the block
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.acc_full, nacc & 1, err, 823))) break;
+        ++nacc;
+        tc::fence_after();
+        const long long krow = static_cast<long long>(row0) + r;
+        float* dvr = dv_acc + (krow * kKvHeads + g) * kDim;
+        float* dkr = dk_acc + (krow * kKvHeads + g) * kDim;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t a[32], b[32];
+          tc::ld_32x32b_x32(lrow + 256 + ch * 32, a);
+          tc::ld_32x32b_x32(lrow + 384 + ch * 32, b);
+          tc::wait_ld();
+          if (krow < T) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              red_add_v4(dvr + ch * 32 + 4 * j, __uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                         __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
+              red_add_v4(dkr + ch * 32 + 4 * j, scale * __uint_as_float(b[4 * j]),
+                         scale * __uint_as_float(b[4 * j + 1]), scale * __uint_as_float(b[4 * j + 2]),
+                         scale * __uint_as_float(b[4 * j + 3]));
+            }
+          }
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_free);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+// Backward workspace: the forward's bucketing region, then D [T][64] and the
+// fp32 accumulators dq [T][64][128], dk and dv [T][4][128].
+struct BwCarve {
+  float* D;
+  float* dq;
+  float* dk;
+  float* dv;
+  size_t bytes;
+};
+static BwCarve bw_carve(long long T, int max_seqlen, int topk, uint8_t* region) {
+  BwCarve c;
+  size_t off = prefill_attend_bytes(T, max_seqlen, topk);
+  auto take = [&](size_t bytes) {
+    uint8_t* ptr = region ? region + off : nullptr;
+    off += al256(bytes);
+    return reinterpret_cast<float*>(ptr);
+  };
+  c.D = take(static_cast<size_t>(T) * kHeads * sizeof(float));
+  c.dq = take(static_cast<size_t>(T) * kHeads * kDim * sizeof(float));
+  c.dk = take(static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float));
+  c.dv = take(static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float));
+  c.bytes = off;
+  return c;
+}
+
+size_t prefill_backward_bytes(long long total_tokens, int max_seqlen, int topk) {
+  return bw_carve(total_tokens, max_seqlen, topk, nullptr).bytes;
+}
+
+cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v, const int32_t* q2k,
+                                    const int32_t* cu_seqlens, int num_docs, long long total_tokens,
+                                    int max_seqlen, int topk, float scale, const void* out, const float* lse,
+                                    const void* grad_out, void* dq, void* dk, void* dv, uint8_t* region,
+                                    DevError* err, cudaStream_t stream) {
+  const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
+  BmPlan p;
+  bm_carve(dims, region, &p);
+  const BwCarve w = bw_carve(total_tokens, max_seqlen, topk, region);
+  CUtensorMap qmap, omap, kmap, vmap;
+  if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode3d(&omap, grad_out, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
+      !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
+    return cudaErrorInvalidValue;
+  const long long T = total_tokens;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(w.dq, 0, static_cast<size_t>(T) * kHeads * kDim * sizeof(float), stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(w.dk, 0, static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float), stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(w.dv, 0, static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float), stream)) != cudaSuccess)
+    return e;
+  // the forward's bucketing of the q2k entries
+  const long long keys = kKvHeads * dims.kg_max;
+  if ((e = cudaMemsetAsync(p.counts, 0, keys * sizeof(int), stream)) != cudaSuccess) return e;
+  bm_geom_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_docs, T, dims.W, dims.nw, dims.kg_max, p, err);
+  bm_count_kernel<<<static_cast<unsigned>((kKvHeads * T + 255) / 256), 256, 0, stream>>>(
+      q2k, cu_seqlens, num_docs, T, topk, dims.W, p, err);
+  bm_scan_kernel<<<1, 1024, 0, stream>>>(p);
+  bm_tiles_kernel<<<static_cast<unsigned>((keys + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs, dims.nw, p);
+  bm_scatter_kernel<<<static_cast<unsigned>((dims.entries + 255) / 256), 256, 0, stream>>>(dims.entries, T * topk,
+                                                                                           p);
+  bw_rowdot_kernel<<<static_cast<unsigned>((T * kHeads + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(grad_out), static_cast<const __nv_bfloat16*>(out), T * kHeads, w.D);
+  const size_t smem = sizeof(BwSmem) + 1024;
+  cudaFuncSetAttribute(bw_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
+  const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
+  bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, p, T, topk, scale,
+                                                       scale * 1.4426950408889634f, lse, w.D, w.dq, w.dk, w.dv, err);
+  const long long nq8 = T * kHeads * kDim / 8, nk8 = T * kKvHeads * kDim / 8;
+  bw_to_bf16_kernel<<<static_cast<unsigned>((nq8 + 255) / 256), 256, 0, stream>>>(w.dq, nq8,
+                                                                                 static_cast<__nv_bfloat16*>(dq));
+  bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dk, nk8,
+                                                                                 static_cast<__nv_bfloat16*>(dk));
+  bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dv, nk8,
+                                                                                 static_cast<__nv_bfloat16*>(dv));
   return cudaGetLastError();
 }
 

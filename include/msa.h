@@ -61,7 +61,7 @@ typedef enum {
 enum { MSA_INDEX_BF16 = 0, MSA_INDEX_E4M3 = 1 };
 
 /* Workspace modes for msa_workspace_size. */
-enum { MSA_MODE_DECODE = 0, MSA_MODE_PREFILL = 1, MSA_MODE_PACK = 2 };
+enum { MSA_MODE_DECODE = 0, MSA_MODE_PREFILL = 1, MSA_MODE_PACK = 2, MSA_MODE_PREFILL_BWD = 3 };
 
 /* Device error codes reported by msa_read_device_error. */
 enum {
@@ -103,6 +103,7 @@ msa_status msa_config_check(const msa_config* cfg);
  *                     page table (or ceil(max context / 128) when contiguous).
  *   MSA_MODE_PREFILL: n = total compact tokens, max_blocks = ceil(max_seqlen/128).
  *   MSA_MODE_PACK   : n = batch * seq of the document map, max_blocks = batch.
+ *   MSA_MODE_PREFILL_BWD: as MSA_MODE_PREFILL, for msa_sparse_attend_prefill_backward.
  * The workspace must be zero-filled once before its first use (see
  * msa_workspace_init), which clears the device error word in its first 256
  * bytes.  Each call clears its own completion counters (a cudaMemsetAsync on
@@ -231,6 +232,43 @@ msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const
                                      int num_docs, int64_t total_tokens, int max_seqlen,
                                      float scale, void* out, void* workspace,
                                      size_t workspace_bytes, void* stream);
+
+/* The same call, also writing the log-sum-exp the backward needs:
+ *   lse dev fp32 [total_tokens, 64]: log2 of the softmax denominator in the
+ *       base-2 domain of the scaled scores, log2(sum_p 2^(scale <q, k_p> log2 e)),
+ *       -inf for a (token, head) with no key (NeMo _SparseAttention saves the
+ *       forward's schedule for its backward; this is the row statistic of it).
+ * Errors as msa_sparse_attend_prefill; MSA_ERR_NULL for a null lse. */
+msa_status msa_sparse_attend_prefill_lse(const msa_config* cfg, const void* q, const void* k,
+                                         const void* v, const int32_t* q2k,
+                                         const int32_t* cu_seqlens, int num_docs,
+                                         int64_t total_tokens, int max_seqlen, float scale, void* out,
+                                         float* lse, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+/* ---- backward of step 3, prefill ------------------------------------------------
+ * NeMo _SparseAttention.backward: bf16 grad_out [tokens, 64, 128] -> bf16 dq
+ * [tokens, 64, 128], dk and dv [tokens, 4, 128], over the same keys as the
+ * forward (q2k, cu_seqlens, scale as given to it).  With z_p = scale <q, k_p>,
+ * P = softmax(z) (rebuilt from lse), dP_p = <grad_out, v_p> and D = <grad_out,
+ * out>: dv_p += P_p grad_out, dS_p = P_p (dP_p - D), dk_p += scale dS_p q,
+ * dq += scale sum_p dS_p k_p.
+ *   out, lse   the forward's bf16 output and fp32 log-sum-exp
+ *              (msa_sparse_attend_prefill_lse)
+ *   dq, dk, dv dev bf16, written whole (zero for tokens no query reaches)
+ *   workspace  >= msa_workspace_size(cfg, MSA_MODE_PREFILL_BWD, total_tokens,
+ *              ceil(max_seqlen / 128)); holds fp32 accumulators for dq, dk, dv
+ * Gradients are summed with fp32 atomics, so they are not bitwise
+ * reproducible from run to run (as the pages say of theirs).
+ * Errors: MSA_ERR_NULL, MSA_ERR_SHAPE, MSA_ERR_ALIGN (any tensor not 16-byte
+ * aligned), MSA_ERR_WORKSPACE, MSA_ERR_CUDA. */
+msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void* q, const void* k,
+                                              const void* v, const int32_t* q2k,
+                                              const int32_t* cu_seqlens, int num_docs,
+                                              int64_t total_tokens, int max_seqlen, float scale,
+                                              const void* out, const float* lse, const void* grad_out,
+                                              void* dq, void* dk, void* dv, void* workspace,
+                                              size_t workspace_bytes, void* stream);
 
 /* ---- packed layout of a document map ----------------------------------------
  * NeMo layout-from-doc_ids constructor and _contiguous_runs: doc_ids is an

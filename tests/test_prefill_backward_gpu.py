@@ -1,0 +1,80 @@
+"""Backward of the prefill sparse attention on the GPU (through the C ABI)
+against the fp64 oracle (NeMo _SparseAttention.backward: grad_out -> dq, dk, dv).
+
+Tolerance, from the arithmetic: the kernel rebuilds P from the forward's fp32
+log-sum-exp, rounds P and dS = P (dP - D) to bf16 for the tensor cores
+(relative 2^-9 each), takes D = <grad_out, out> from the bf16 output, sums
+in fp32 and rounds the gradients to bf16 (2^-9).  The bounds: one element's
+error within 1 % of the tensor's largest magnitude and the mean error within
+0.5 % of its mean magnitude (measured: at most 0.5 % and 0.25 %)."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_08_gb300 as msa
+import msa_synth
+import oracle
+from _parity import SCALE
+
+pytestmark = pytest.mark.gpu
+
+
+def _close(name, got, ref):
+    got = got.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    big, mean = np.abs(ref).max(), np.abs(ref).mean()
+    assert err.max() <= 1e-2 * big + 1e-6, (name, float(err.max()), float(big))
+    assert err.mean() <= 5e-3 * mean + 1e-7, (name, float(err.mean()), float(mean))
+
+
+def _run(docs, topk, init, local, seed):
+    p = msa_synth.prefill_inputs(docs, seed=seed, device="cuda", topk=topk, init_blocks=init,
+                                 local_blocks=local)
+    T = p.total_tokens
+    q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=topk,
+                                        init_blocks=init, local_blocks=local)
+    lse = torch.empty((T, 64), dtype=torch.float32, device="cuda")
+    out = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE, lse=lse)
+    gen = torch.Generator(device="cpu").manual_seed(seed + 100)
+    dout = torch.randn((T, 64, 128), generator=gen).to(torch.bfloat16).cuda()
+    dq, dk, dv = msa.msa_sparse_attend_prefill_backward(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, out, lse,
+                                                        dout, scale=SCALE)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attend_prefill_backward(p.q, p.k, p.v, dout, p.cu_seqlens, q2k, SCALE)
+    _close("dv", dv, rv)
+    _close("dk", dk, rk)
+    _close("dq", dq, rq)
+    return lse, q2k
+
+
+@pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (3, 1, 1), (1, 0, 1)])
+def test_prefill_backward_small(topk, init, local):
+    _run([1, 127, 128, 129, 300, 700], topk, init, local, seed=31 + topk)
+
+
+def test_prefill_backward_one_short_document():
+    _run([37], 16, 0, 1, seed=7)
+
+
+def test_prefill_lse_is_the_log_sum_exp():
+    # lse against the oracle's scores: log2 sum_p 2^(scale <q, k_p> log2 e) over the selected causal keys
+    p = msa_synth.prefill_inputs([300, 129], seed=3, device="cuda")
+    T = p.total_tokens
+    q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
+    lse = torch.empty((T, 64), dtype=torch.float32, device="cuda")
+    msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE, lse=lse)
+    torch.cuda.synchronize()
+    q = p.q.float().cpu().double().numpy()
+    k = p.k.float().cpu().double().numpy()
+    cu = p.cu_seqlens.cpu().numpy()
+    qk = q2k.cpu().numpy()
+    got = lse.cpu().numpy()
+    for t in (0, 5, 128, 200, 299, 300, 428):
+        d = int(np.searchsorted(cu, t, side="right") - 1)
+        pos = t - cu[d]
+        for h in (0, 17, 63):
+            g = h // 16
+            keys = [cu[d] + j for b in qk[g, t] if b >= 0 for j in range(b * 128, min(b * 128 + 128, pos + 1))]
+            z = SCALE * (k[keys, g] @ q[t, h])
+            ref = (np.log(np.sum(np.exp(z - z.max()))) + z.max()) / np.log(2.0)
+            assert abs(got[t, h] - ref) <= 1e-4 * (1 + abs(ref)), (t, h, got[t, h], ref)
