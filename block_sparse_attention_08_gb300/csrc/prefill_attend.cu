@@ -1303,8 +1303,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
   }
 }
 
-// Backward workspace: the forward's bucketing region, then D [T][64] and the
-// fp32 accumulators dq [T][64][128], dk and dv [T][4][128].
+// Backward workspace: the forward's bucketing arrays, then (in place of the
+// forward's partials, which the backward does not use) D [T][64] and the fp32
+// accumulators dq [T][64][128], dk and dv [T][4][128].
 struct BwCarve {
   float* D;
   float* dq;
@@ -1314,7 +1315,10 @@ struct BwCarve {
 };
 static BwCarve bw_carve(long long T, int max_seqlen, int topk, uint8_t* region) {
   BwCarve c;
-  size_t off = prefill_attend_bytes(T, max_seqlen, topk);
+  const BmDims d = bm_dims(T, max_seqlen, topk);
+  // po and pml are the last two arrays bm_carve takes
+  size_t off = bm_carve(d, nullptr, nullptr) - al256(d.entries * kGroup * kDim * sizeof(__half)) -
+               al256(d.entries * kGroup * sizeof(float2));
   auto take = [&](size_t bytes) {
     uint8_t* ptr = region ? region + off : nullptr;
     off += al256(bytes);
