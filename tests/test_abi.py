@@ -123,6 +123,28 @@ def test_attend_and_prefill_validation(lib):
                                          ctypes.c_float(0.1), FAKE, FAKE, 16, None) == WORKSPACE
 
 
+def test_backward_and_lse_validation(lib):
+    c = _cfg()
+    f = ctypes.c_float(0.1)
+    # lse variant: a null lse
+    assert lib.msa_sparse_attend_prefill_lse(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, f, FAKE,
+                                             None, FAKE, 1 << 30, None) == NULL
+    # backward: a null gradient, a misaligned output, a workspace too small
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 128, f, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]
+    bad = list(args)
+    bad[11] = None  # grad_out
+    assert lib.msa_sparse_attend_prefill_backward(ctypes.byref(c), *bad, FAKE, 1 << 30, None) == NULL
+    bad = list(args)
+    bad[12] = FAKE + 8  # dq
+    assert lib.msa_sparse_attend_prefill_backward(ctypes.byref(c), *bad, FAKE, 1 << 30, None) == ALIGN
+    assert lib.msa_sparse_attend_prefill_backward(ctypes.byref(c), *args, FAKE, 16, None) == WORKSPACE
+    # its workspace: a mode of its own, smaller than the forward's
+    fwd, bwd = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.msa_workspace_size(ctypes.byref(c), 1, 16384, 128, ctypes.byref(fwd)) == OK
+    assert lib.msa_workspace_size(ctypes.byref(c), 3, 16384, 128, ctypes.byref(bwd)) == OK
+    assert 0 < bwd.value < fwd.value
+
+
 def test_pack_validation(lib):
     n, t, m, bad = ctypes.c_int(), ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64()
     r = lib.msa_pack_metadata(FAKE, 0, 5, FAKE, FAKE, ctypes.byref(n), ctypes.byref(t), ctypes.byref(m),
