@@ -23,6 +23,9 @@ Which statement on the pages each function follows:
     ``_SparseAttention.backward``: grad_out -> dq, dk, dv), written out from
     the forward; ``attend_loss_f64`` -- the forward on fp64 inputs reduced to
     sum(out * dout), whose finite differences pin the backward.
+  * ``mxfp8_quantize`` -- the MXFP8 emission of the output (vLLM page,
+    forward_decode_mxfp8: E4M3 values, E8M0 scales per 32 elements), after the
+    OCP MX block rule, which the page names but does not print.
   * ``pack_metadata`` / ``pack`` / ``unpack`` -- NeMo layout-from-doc_ids
     constructor, ``_contiguous_runs``, ``MSAMicrobatch.pack`` / ``unpack``.
 """
@@ -81,6 +84,7 @@ def _load():
             lib.oracle_attend_prefill_backward.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl, P, P, P]
             lib.oracle_attend_loss_f64.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl]
             lib.oracle_attend_loss_f64.restype = Dbl
+            lib.oracle_mxfp8_quantize.argtypes = [P, I64, P, P]
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = Dbl
             for f in (lib.oracle_select_prefill, lib.oracle_attend_prefill,
@@ -195,6 +199,20 @@ def attend_loss_f64(q, k, v, dout, cu_seqlens, q2k, scale):
     q2k = _i32(q2k)
     return lib.oracle_attend_loss_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(cu), cu.shape[0] - 1,
                                       q2k.shape[1], _ptr(q2k), q2k.shape[2], float(scale))
+
+
+def mxfp8_quantize(x):
+    """(E4M3 bytes uint8 [..., n], E8M0 scale bytes uint8 [..., n / 32]) of a bf16 tensor whose
+    last dimension is a multiple of 32: the OCP MX block rule (see the C source)."""
+    lib = _load()
+    xb = np.ascontiguousarray(_bits(x))
+    shape = xb.shape
+    n = xb.size
+    q = np.zeros(n, dtype=np.uint8)
+    sc = np.zeros(n // 32, dtype=np.uint8)
+    if lib.oracle_mxfp8_quantize(_ptr(xb), n, _ptr(q), _ptr(sc)):
+        raise ValueError("the element count must be a multiple of 32")
+    return q.reshape(shape), sc.reshape(shape[:-1] + (shape[-1] // 32,))
 
 
 def select_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None,

@@ -444,6 +444,69 @@ double oracle_attend_loss_f64(const double* q, const double* k, const double* v,
   return loss;
 }
 
+/* ---- MXFP8 emission of the output ----------------------------------------
+ * The vLLM page's forward_decode_mxfp8 emits the bf16 output as MXFP8: E4M3
+ * values [tokens, H*D] and row-major E8M0 scales [tokens, H*D/32], equal to
+ * mxfp8_e4m3_quantize of the bf16 output.  The page does not print that
+ * function; this follows the OCP Microscaling (MX) v1.0 definition of an
+ * MXFP8 E4M3 block: 32 consecutive elements share the scale
+ * X = 2^(floor(log2(amax)) - 8) (8 = the largest E4M3 exponent), stored as the
+ * E8M0 byte floor(log2(amax)) - 8 + 127 (clamped to [0, 254]; amax = 0 gives
+ * byte 0); each element is v / X rounded to E4M3 (nearest, ties to even),
+ * saturated at +-448.  Arithmetic in double is exact here (bf16 inputs, power
+ * of two scales). */
+
+/* E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinity,
+ * 0x7F = NaN, largest finite 448) of y: nearest, ties to even mantissa,
+ * saturating. */
+static uint8_t e4m3_encode(double y) {
+  uint8_t sign = y < 0 ? 0x80 : 0x00;
+  double a = fabs(y);
+  if (a >= 448.0) return sign | 0x7E;
+  int e;
+  frexp(a, &e); /* a = m 2^e, m in [0.5, 1): floor(log2 a) = e - 1 */
+  int ex = (a == 0.0) ? -7 : e - 1;
+  if (ex < -6) ex = -6;                      /* subnormals share the quantum 2^-9 */
+  double quantum = ldexp(1.0, ex - 3);       /* 3 mantissa bits */
+  double qf = a / quantum;                   /* exact: a is a short binary fraction */
+  double fl = floor(qf);
+  double rem = qf - fl;
+  long long qi = (long long)fl;
+  if (rem > 0.5 || (rem == 0.5 && (qi & 1))) qi += 1;
+  /* qi in [0, 16]; 16 carries into the next binade */
+  if (qi == 0) return sign;
+  if (ex == -6 && qi < 8) return sign | (uint8_t)qi; /* subnormal */
+  if (qi == 16) {
+    qi = 8;
+    ex += 1;
+  }
+  double val = ldexp((double)qi, ex - 3);
+  if (val > 448.0) return sign | 0x7E;
+  return sign | (uint8_t)(((ex + 7) << 3) | (int)(qi - 8));
+}
+
+int oracle_mxfp8_quantize(const uint16_t* bf16, int64_t n, uint8_t* q, uint8_t* scales) {
+  if (n % 32) return 1;
+  for (int64_t b0 = 0; b0 < n; b0 += 32) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double v = fabs(bf16_value(bf16[b0 + i]));
+      if (v > amax) amax = v;
+    }
+    int sexp = -127;
+    if (amax > 0.0) {
+      int e;
+      frexp(amax, &e);
+      sexp = e - 1 - 8;
+      if (sexp < -127) sexp = -127;
+      if (sexp > 127) sexp = 127;
+    }
+    scales[b0 / 32] = (uint8_t)(sexp + 127);
+    for (int i = 0; i < 32; ++i) q[b0 + i] = e4m3_encode(ldexp(bf16_value(bf16[b0 + i]), -sexp));
+  }
+  return 0;
+}
+
 /* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n]. */
 int oracle_select_decode(const void* index_q, const void* index_k_cache, int dtype,
                          const int32_t* seq_lens, const int32_t* page_table,
