@@ -49,11 +49,12 @@ def _peaks():
 
 # ---- algorithmic work per step -------------------------------------------------------
 
-def decode_work(d, q2k):
+def decode_work(d, q2k, mxfp8=False):
     """(bytes_select, bytes_attend).  Select: the index-K of every scored context
     once (contexts with nb <= topk keep every block and read nothing) plus the
     index queries.  Attend: K and V of every attended key once per KV head, plus
-    q and out."""
+    q and out (bf16, or with ``mxfp8`` one E4M3 byte per element and one scale
+    byte per 32)."""
     lens = d.seq_lens.cpu().numpy().astype(np.int64)
     nb = (lens + 127) // 128
     scored = nb > d.topk
@@ -65,7 +66,8 @@ def decode_work(d, q2k):
         blk = q[g]
         k = np.minimum(128, lens[:, None] - 128 * blk)
         keys += int(np.where(blk >= 0, k, 0).sum())
-    b_att = keys * 2 * 128 * 2 + 2 * d.batch * 64 * 128 * 2
+    out_bytes = d.batch * 64 * 128 * (1 + 1 / 32 if mxfp8 else 2)
+    b_att = int(keys * 2 * 128 * 2 + d.batch * 64 * 128 * 2 + out_bytes)
     return b_sel, b_att
 
 
@@ -280,8 +282,19 @@ def run_gpu(args, rank, world, device):
             msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, topk=d.topk,
                                          init_blocks=d.init_blocks, local_blocks=d.local_blocks, q2k=q2k, **kw)
 
-        def att():
-            msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE, out=out, **kw)
+        if args.mxfp8:
+            out_q = torch.empty((d.batch, 64 * 128), dtype=torch.uint8, device=device)
+            out_sc = torch.empty((d.batch, 64 * 128 // 32), dtype=torch.uint8, device=device)
+
+            def att():
+                msa.msa_sparse_attend_decode_mxfp8(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE,
+                                                   out_q=out_q, out_scale=out_sc, **kw)
+            outs = [out_q, out_sc]
+        else:
+            def att():
+                msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE, out=out,
+                                             **kw)
+            outs = [out]
         n_queries = d.batch
     else:
         p = inp
@@ -294,6 +307,7 @@ def run_gpu(args, rank, world, device):
 
         def att():
             msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE, out=out)
+        outs = [out]
         n_queries = p.total_tokens
 
     for _ in range(args.warmup):
@@ -301,7 +315,7 @@ def run_gpu(args, rank, world, device):
         att()
         flush_l2(1)
     torch.cuda.synchronize()
-    work = decode_work(inp, q2k) if decode else prefill_work(inp, q2k)
+    work = decode_work(inp, q2k, args.mxfp8) if decode else prefill_work(inp, q2k)
     entries = 0 if decode else prefill_entries(q2k)
 
     # The timed steps replay CUDA graphs of the two C-ABI calls (captured once,
@@ -358,9 +372,9 @@ def run_gpu(args, rank, world, device):
         late = [p.q, p.k, p.v]
     h_early, d_early, dv_early = _staging(early, device)
     h_late, d_late, dv_late = _staging(late, device)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     h2d = sum(x.numel() * x.element_size() for x in early + late)
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = sum(h.numel() * h.element_size() for h in h_outs)
     side = torch.cuda.Stream(device)
 
     def e2e_step():
@@ -376,8 +390,12 @@ def run_gpu(args, rank, world, device):
             msa.msa_select_blocks_decode(diq, d.index_k_cache, dsl, topk=d.topk, init_blocks=d.init_blocks,
                                          local_blocks=d.local_blocks, q2k=q2k, max_blocks=d.max_blocks, **kw2)
             cur.wait_stream(side)
-            msa.msa_sparse_attend_decode(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out=out,
-                                         max_blocks=d.max_blocks, **kw2)
+            if args.mxfp8:
+                msa.msa_sparse_attend_decode_mxfp8(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out_q=outs[0],
+                                                   out_scale=outs[1], max_blocks=d.max_blocks, **kw2)
+            else:
+                msa.msa_sparse_attend_decode(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out=out,
+                                             max_blocks=d.max_blocks, **kw2)
         else:
             iq_, ik_, cu_ = dv_early
             q_, k_, v_ = dv_late
@@ -385,7 +403,8 @@ def run_gpu(args, rank, world, device):
                                           local_blocks=p.local_blocks, q2k=q2k)
             cur.wait_stream(side)
             msa.msa_sparse_attend_prefill(q_, k_, v_, q2k, cu_, p.max_seqlen, scale=SCALE, out=out)
-        h_out.copy_(out, non_blocking=True)
+        for h, o in zip(h_outs, outs):
+            h.copy_(o, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -486,6 +505,8 @@ def main():
                     help="divide the workload's lengths by this factor (small profiling cases)")
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of a decode workload (small profiling cases)")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="decode: emit the attention output as MXFP8 (E4M3 + E8M0 scales) instead of bf16")
     ap.add_argument("--backward", action="store_true",
                     help="time the attention backward of a prefill workload instead of the forward step")
     args = ap.parse_args()
@@ -501,6 +522,10 @@ def main():
     config = {"workload": args.workload, "desc": msa_synth.WORKLOADS[args.workload], "seed": args.seed}
     if args.requests:
         config["requests"] = args.requests
+    if args.mxfp8:
+        if not args.workload.startswith("decode"):
+            raise SystemExit("--mxfp8 applies to the decode attention")
+        config["output"] = "MXFP8: E4M3 values + one E8M0 scale per 32 elements"
     if args.scale_down > 1:
         config["scale_down"] = args.scale_down
 

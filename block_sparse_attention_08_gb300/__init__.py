@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     msa_select_blocks_decode,
     msa_select_blocks_prefill,
     msa_sparse_attend_decode,
+    msa_sparse_attend_decode_mxfp8,
     msa_sparse_attend_prefill,
     msa_sparse_attend_prefill_backward,
     msa_unpack,

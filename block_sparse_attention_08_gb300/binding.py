@@ -49,6 +49,7 @@ _SIGS = {
     "msa_read_device_error": [P, P, ctypes.POINTER(I), ctypes.POINTER(I64)],
     "msa_select_blocks_decode": [CFG, P, P, P, P, P, I, I, I64, P, P, SZ, P],
     "msa_sparse_attend_decode": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, SZ, P],
+    "msa_sparse_attend_decode_mxfp8": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, P, SZ, P],
     "msa_select_blocks_prefill": [CFG, P, P, P, I, I64, I, P, P, SZ, P],
     "msa_sparse_attend_prefill": [CFG, P, P, P, P, P, I, I64, I, F, P, P, SZ, P],
     "msa_sparse_attend_prefill_lse": [CFG, P, P, P, P, P, I, I64, I, F, P, P, P, SZ, P],
@@ -235,6 +236,38 @@ def msa_sparse_attend_decode(q, k_cache, v_cache, q2k, seq_lens, page_table=None
           _ptr(seq_lens), _ptr(page_table), _ptr(cu_seqlens_k if page_table is None else None), B, mb,
           k_cache.shape[0], scale, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(dev))
     return out
+
+
+def msa_sparse_attend_decode_mxfp8(q, k_cache, v_cache, q2k, seq_lens, page_table=None, cu_seqlens_k=None, *,
+                                   max_blocks=None, scale=None, out_q=None, out_scale=None, workspace=None):
+    """The decode attention with the output as MXFP8: (E4M3 bytes uint8 [batch, 64 * 128], E8M0 scale
+    bytes uint8 [batch, 256]) (C: msa_sparse_attend_decode_mxfp8)."""
+    B = q.shape[0]
+    _need(q, "q", torch.bfloat16, (B, H, D))
+    _need(k_cache, "k_cache", torch.bfloat16, (None, G, D))
+    _need(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape))
+    _need(q2k, "q2k", torch.int32, (G, B, None))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32, (B, None))
+        mb = page_table.shape[1]
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int64, (B + 1,))
+        mb = max_blocks
+    if mb is None:
+        raise ValueError("max_blocks is required with a contiguous cache")
+    cfg = make_config(q2k.shape[2], 0, 0)
+    dev = q.device
+    out_q = torch.empty((B, H * D), dtype=torch.uint8, device=dev) if out_q is None else out_q
+    out_scale = torch.empty((B, H * D // 32), dtype=torch.uint8, device=dev) if out_scale is None else out_scale
+    _need(out_q, "out_q", torch.uint8, (B, H * D))
+    _need(out_scale, "out_scale", torch.uint8, (B, H * D // 32))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws = _workspace("decode", workspace_size(cfg, MODE_DECODE, B, mb), dev, workspace)
+    _call("msa_sparse_attend_decode_mxfp8", ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(q2k),
+          _ptr(seq_lens), _ptr(page_table), _ptr(cu_seqlens_k if page_table is None else None), B, mb,
+          k_cache.shape[0], scale, _ptr(out_q), _ptr(out_scale), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return out_q, out_scale
 
 
 # ---- prefill ----------------------------------------------------------------------

@@ -185,15 +185,18 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
-msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
-                                    const int32_t* q2k, const int32_t* seq_lens, const int32_t* page_table,
-                                    const int64_t* cu_seqlens_k, int batch, int max_blocks, int64_t num_slots,
-                                    float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+static msa_status attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* q2k, const int32_t* seq_lens, const int32_t* page_table,
+                                const int64_t* cu_seqlens_k, int batch, int max_blocks, int64_t num_slots,
+                                float scale, void* out, uint8_t* out_q, uint8_t* out_scale, void* workspace,
+                                size_t workspace_bytes, void* stream) {
   msa_status st = msa_config_check(cfg);
   if (st != MSA_OK) return st;
-  if (!q || !k_cache || !v_cache || !q2k || !out) return MSA_ERR_NULL;
+  if (!q || !k_cache || !v_cache || !q2k || (!out && !(out_q && out_scale))) return MSA_ERR_NULL;
   if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return MSA_ERR_ALIGN;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || (out && !aligned16(out)) ||
+      (out_q && !aligned16(out_q)))
+    return MSA_ERR_ALIGN;
   const Layout L = layout(MSA_MODE_DECODE, batch, max_blocks, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -201,10 +204,30 @@ msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const 
   if (clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s) != cudaSuccess)
     return MSA_ERR_CUDA;
   AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
-  cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out,
+  cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out, out_q, out_scale,
                                        reinterpret_cast<float*>(ws + L.partials),
                                        reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* q2k, const int32_t* seq_lens, const int32_t* page_table,
+                                    const int64_t* cu_seqlens_k, int batch, int max_blocks, int64_t num_slots,
+                                    float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out) return MSA_ERR_NULL;
+  return attend_decode(cfg, q, k_cache, v_cache, q2k, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
+                       num_slots, scale, out, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+msa_status msa_sparse_attend_decode_mxfp8(const msa_config* cfg, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* q2k, const int32_t* seq_lens,
+                                          const int32_t* page_table, const int64_t* cu_seqlens_k, int batch,
+                                          int max_blocks, int64_t num_slots, float scale, void* out_q,
+                                          void* out_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!out_q || !out_scale) return MSA_ERR_NULL;
+  return attend_decode(cfg, q, k_cache, v_cache, q2k, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
+                       num_slots, scale, nullptr, static_cast<uint8_t*>(out_q), static_cast<uint8_t*>(out_scale),
+                       workspace, workspace_bytes, stream);
 }
 
 static msa_status check_prefill_geom(const int32_t* cu_seqlens, int num_docs, int64_t total_tokens, int max_seqlen) {

@@ -25,8 +25,9 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
                                  int* tickets, DevError* err, cudaStream_t stream);
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
-                                 const int32_t* q2k, int topk, float scale, void* out, float* partials,
-                                 int* tickets, DevError* err, cudaStream_t stream);
+                                 const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
+                                 uint8_t* out_scale, float* partials, int* tickets, DevError* err,
+                                 cudaStream_t stream);
 size_t attend_partials_bytes();
 size_t prefill_plan_ints(int num_docs, int max_tiles);
 cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, const void* index_k,

@@ -147,11 +147,50 @@ __device__ __forceinline__ void merge_from_smem(WarpState& st, const AttSmem& sm
   }
 }
 
+// Two E4M3 values, rounded to nearest (ties to even) and saturated at +-448;
+// `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// MXFP8 emission of one lane's 64 consecutive outputs v[i] * inv (vLLM
+// forward_decode_mxfp8: E4M3 values and one E8M0 scale per 32 elements, equal
+// to the MX quantisation of the bf16 output).  Per 32-element block: the bf16
+// output values b, amax = max |b|, scale exponent floor(log2 amax) - 8 (the
+// largest E4M3 exponent; clamped to [-127, 127], -127 for a zero block), each
+// b times 2^-exponent (exact) rounded to E4M3.
+__device__ __forceinline__ void store_mxfp8_64(const float* v, float inv, uint8_t* __restrict__ q,
+                                               uint8_t* __restrict__ sc) {
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    float b[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      b[i] = bf16_round(v[32 * blk + i] * inv);
+      amax = fmaxf(amax, fabsf(b[i]));
+    }
+    const int sexp = amax > 0.f ? max(-127, min(127, ilogbf(amax) - 8)) : -127;
+    sc[blk] = static_cast<uint8_t>(sexp + 127);
+    const float r = ldexpf(1.f, -sexp);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = e4m3x2(b[4 * i] * r, b[4 * i + 1] * r) | (e4m3x2(b[4 * i + 2] * r, b[4 * i + 3] * r) << 16);
+    reinterpret_cast<uint4*>(q + 32 * blk)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(q + 32 * blk)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// out_q / out_scale: when non-null, the output is emitted as MXFP8 there
+// instead of bf16 in `out`.
 __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
-    float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ partials,
-    int* __restrict__ tickets, DevError* err) {
+    float scale_log2, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q, uint8_t* __restrict__ out_scale,
+    float* __restrict__ partials, int* __restrict__ tickets, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   AttSmem& sm = *reinterpret_cast<AttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -394,14 +433,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const float M = sm.comb_m[0][row], Lsum = sm.comb_l[0][row];
     const float* src = &sm.comb[0][row][d0];
     const bool complete = (seg_lo == range0) && (seg_end == range0 + topk);
-    __nv_bfloat16* orow = out + (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+    const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+    __nv_bfloat16* orow = out_q ? nullptr : out + oelem;
     if (complete) {
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      if (out_q) {
+        store_mxfp8_64(src, inv, out_q + oelem, out_scale + oelem / 32);
+      } else {
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        reinterpret_cast<uint4*>(orow)[v] =
-            make_uint4(pack_bf16(src[8 * v] * inv, src[8 * v + 1] * inv), pack_bf16(src[8 * v + 2] * inv, src[8 * v + 3] * inv),
-                       pack_bf16(src[8 * v + 4] * inv, src[8 * v + 5] * inv), pack_bf16(src[8 * v + 6] * inv, src[8 * v + 7] * inv));
+        for (int v = 0; v < 8; ++v)
+          reinterpret_cast<uint4*>(orow)[v] = make_uint4(
+              pack_bf16(src[8 * v] * inv, src[8 * v + 1] * inv), pack_bf16(src[8 * v + 2] * inv, src[8 * v + 3] * inv),
+              pack_bf16(src[8 * v + 4] * inv, src[8 * v + 5] * inv), pack_bf16(src[8 * v + 6] * inv, src[8 * v + 7] * inv));
+      }
     } else {
       // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
       const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
@@ -468,11 +512,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
           }
         }
         const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
+        if (out_q) {
+          store_mxfp8_64(ag, inv, out_q + oelem, out_scale + oelem / 32);
+        } else {
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          reinterpret_cast<uint4*>(orow)[v] =
-              make_uint4(pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
-                         pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<uint4*>(orow)[v] = make_uint4(
+                pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
+                pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
+        }
         if (lane == 0) tickets[qi * kKvHeads + g] = 0;
       }
     }
@@ -511,8 +559,9 @@ static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
 size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
 
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
-                                 const int32_t* q2k, int topk, float scale, void* out, float* partials,
-                                 int* tickets, DevError* err, cudaStream_t stream) {
+                                 const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
+                                 uint8_t* out_scale, float* partials, int* tickets, DevError* err,
+                                 cudaStream_t stream) {
   CUtensorMap kmap, vmap, qmap;
   if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows) ||
       !make_q_map(&qmap, q, geo.nq))
@@ -528,8 +577,8 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const float scale_log2 = scale * 1.4426950408889634f;
   sparse_attend_kernel<<<grid, kAttThreads, smem, stream>>>(kmap, vmap, qmap, q2k, geo, topk, scale_log2,
-                                                            static_cast<__nv_bfloat16*>(out), partials, tickets,
-                                                            err);
+                                                            static_cast<__nv_bfloat16*>(out), out_q, out_scale,
+                                                            partials, tickets, err);
   return cudaGetLastError();
 }
 

@@ -204,6 +204,28 @@ msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const 
                                     int64_t num_slots, float scale, void* out, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/* The same decode attention with the output emitted as MXFP8 for the o_proj
+ * that follows (vLLM forward_decode_mxfp8: E4M3 values and row-major E8M0
+ * scales, equal to the MX quantisation of the bf16 output):
+ *   out_q     dev uint8 [batch, 64 * 128]: E4M3 bytes of each output element
+ *   out_scale dev uint8 [batch, 64 * 128 / 32]: the E8M0 scale byte of each
+ *             block of 32 consecutive elements of a row
+ * Per block: b = the bf16 output values, amax = max |b|, scale exponent
+ * e = floor(log2 amax) - 8 (8: the largest E4M3 exponent; clamped to
+ * [-127, 127]; -127 for an all-zero block), scale byte e + 127, and each value
+ * b * 2^-e rounded to E4M3 (nearest, ties to even, saturating at +-448).
+ * The page names this quantisation without printing it; the OCP
+ * Microscaling (MX) v1.0 block rule is the reading taken.
+ * Errors as msa_sparse_attend_decode; MSA_ERR_ALIGN if out_q is not 16-byte
+ * aligned. */
+msa_status msa_sparse_attend_decode_mxfp8(const msa_config* cfg, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* q2k,
+                                          const int32_t* seq_lens, const int32_t* page_table,
+                                          const int64_t* cu_seqlens_k, int batch, int max_blocks,
+                                          int64_t num_slots, float scale, void* out_q,
+                                          void* out_scale, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
 /* ---- step 1+2, prefill: block scores + top-k on packed documents ------------
  * NeMo MSAMicrobatch.select_blocks: compact tokens in document order, document
  * d spanning [cu_seqlens[d], cu_seqlens[d+1]); token t of document d has

@@ -103,3 +103,31 @@ def test_decode_workload_b64_paged():
 def test_decode_workload_b16_128k_e4m3():
     d = msa_synth.workload("decode_b16_ctx128k_paged_e4m3", device="cuda")
     _run(d, 16, 0, 1)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_mxfp8_output(paged):
+    # the MXFP8 emission equals the MX quantisation of the same call's bf16 output, bit for bit,
+    # and that bf16 output matches the oracle
+    d = msa_synth.decode_inputs(SMALL_LENS, paged=paged, seed=12, device="cuda")
+    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+    q2k, out = _run(d, 16, 0, 1)
+    ref_q2k = q2k  # the same q2k for both emissions
+    out = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, ref_q2k, d.seq_lens, scale=SCALE, **kw)
+    oq, osc = msa.msa_sparse_attend_decode_mxfp8(d.q, d.k_cache, d.v_cache, ref_q2k, d.seq_lens, scale=SCALE, **kw)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_quantize(out.reshape(out.shape[0], -1))
+    assert np.array_equal(oq.cpu().numpy(), rq)
+    assert np.array_equal(osc.cpu().numpy(), rs)
+
+
+def test_decode_mxfp8_workload_sample():
+    d = msa_synth.workload("decode_b64_ctx4k_64k_paged", device="cuda", max_requests=8)
+    q2k = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table)
+    out = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, page_table=d.page_table,
+                                       scale=SCALE)
+    oq, osc = msa.msa_sparse_attend_decode_mxfp8(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens,
+                                                 page_table=d.page_table, scale=SCALE)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_quantize(out.reshape(out.shape[0], -1))
+    assert np.array_equal(oq.cpu().numpy(), rq) and np.array_equal(osc.cpu().numpy(), rs)
