@@ -963,7 +963,8 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
 // key row per thread) add the block's dK and dV to fp32 accumulators.  A last
 // kernel converts the three accumulators to bf16.  Everything is single
 // buffered: this is the first, correct form of the backward.
-constexpr int kBwThreads = 192;  // warps 0-3 math, 4 TMA, 5 MMA
+constexpr int kBwThreads = 224;  // warps 0-3 math, 4 TMA (K, V, Q), 5 MMA, 6 TMA (dO)
+constexpr int kBwOWarp = 6;
 constexpr int kBwInfo = 4;
 constexpr uint32_t kIdescKK = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescKM = tc::idesc_bf16_f32(128, 128) | (1u << 16);               // B MN-major
@@ -1041,11 +1042,11 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
   if (tid == 0) {
     for (int i = 0; i < kBwInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
-      mbar_init(&sm.info_empty[i], 5);  // four math warps and the MMA thread
+      mbar_init(&sm.info_empty[i], 6);  // four math warps, the MMA thread, the dO warp
     }
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    mbar_init(&sm.qd_full, 1);
+    mbar_init(&sm.qd_full, 2);  // Q (warp 4) and dO (warp 6) each arm their bytes
     mbar_init(&sm.qd_empty, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.p_full, 4);
@@ -1074,7 +1075,6 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
     // ---------------- scheduler + TMA ----------------
     if (lane == 0) {
       prefetch_tmap(&qmap);
-      prefetch_tmap(&omap);
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
     }
@@ -1118,7 +1118,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
           }
         }
         ok = ok && mbar_wait(&sm.qd_empty, (nqd & 1) ^ 1, err, 802);
-        if (ok) mbar_expect_tx(&sm.qd_full, d.cnt * 4 * kBmQBox);
+        if (ok) mbar_expect_tx(&sm.qd_full, d.cnt * 2 * kBmQBox);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (fresh) {
@@ -1129,8 +1129,6 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
         const int t = ent / topk;
         tma_load_3d(sm.q + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.qd_full);
         tma_load_3d(sm.q + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.qd_full);
-        tma_load_3d(sm.dout + lane * kBmQBox, &omap, 0, d.g * kGroup, t, &sm.qd_full);
-        tma_load_3d(sm.dout + kBmHalf + lane * kBmQBox, &omap, 64, d.g * kGroup, t, &sm.qd_full);
       }
       __syncwarp();
       ++nqd;
@@ -1140,6 +1138,34 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       if (nkv > 0) mbar_wait(&sm.kv_full, (nkv - 1) & 1, err, 803);
       if (nqd > 0) mbar_wait(&sm.qd_full, (nqd - 1) & 1, err, 804);
     }
+  } else if (warp == kBwOWarp) {
+    // ---------------- dO rows of each tile (the tensor copies of Q and dO
+    // are issued from two warps: about 100 cycles of issue per 2 KB box) ----------------
+    if (lane == 0) prefetch_tmap(&omap);
+    int nqd = 0;
+    for (int i = 0; i < n; ++i) {
+      const int is = i % kBwInfo;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBwInfo) & 1, err, 805))) break;
+      const int cnt = sm.info[is].cnt, g = sm.info[is].g;
+      const int ent = lane < kBmEntries ? sm.info[is].ent[lane] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.info_empty[is]);
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.qd_empty, (nqd & 1) ^ 1, err, 806);
+        if (ok) mbar_expect_tx(&sm.qd_full, cnt * 2 * kBmQBox);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane < cnt) {
+        const int t = ent / topk;
+        tma_load_3d(sm.dout + lane * kBmQBox, &omap, 0, g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.dout + kBmHalf + lane * kBmQBox, &omap, 64, g * kGroup, t, &sm.qd_full);
+      }
+      __syncwarp();
+      ++nqd;
+    }
+    // no copy may still be landing when the CTA exits
+    if (lane == 0 && nqd > 0) mbar_wait(&sm.qd_full, (nqd - 1) & 1, err, 807);
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
@@ -1198,7 +1224,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       tc::commit(&sm.done);
       mbar_wait(&sm.done, 0, err, 816);
     }
-  } else {
+  } else if (warp < 4) {
     // ---------------- math warps 0-3 ----------------
     const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
     const uint32_t lrow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
