@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     msa_sparse_attend_prefill,
     msa_sparse_attend_prefill_backward,
     msa_unpack,
+    sparse_attention,
     workspace_size,
 )
 from ._build import build  # noqa: F401

@@ -18,6 +18,7 @@ import torch
 from . import _build
 
 H, G, D, DI, BLOCK = 64, 4, 128, 128, 128
+MSA_ERR_CUDA = 6  # msa_status for a failed CUDA call
 MODE_DECODE, MODE_PREFILL, MODE_PACK, MODE_PREFILL_BWD = 0, 1, 2, 3
 INDEX_DTYPES = {"bf16": 0, "e4m3": 1}
 DEVICE_ERRORS = {0: "none", 1: "page id outside the pool", 2: "block id outside the query's range",
@@ -60,7 +61,7 @@ _SIGS = {
     "msa_unpack": [P, P, I64, I64, I64, P, P],
     "msa_check_bounded_wait": [P, P, ctypes.POINTER(I64)],
 }
-EXPORTS = tuple(_SIGS) + ("msa_status_string",)
+EXPORTS = tuple(_SIGS) + ("msa_status_string", "msa_last_cuda_error", "msa_cuda_error_string")
 
 
 def library_path() -> str:
@@ -83,6 +84,10 @@ def load(build_if_missing: bool = True):
                 fn.restype = ctypes.c_int
             lib.msa_status_string.argtypes = [ctypes.c_int]
             lib.msa_status_string.restype = ctypes.c_char_p
+            lib.msa_last_cuda_error.argtypes = []
+            lib.msa_last_cuda_error.restype = ctypes.c_int
+            lib.msa_cuda_error_string.argtypes = [ctypes.c_int]
+            lib.msa_cuda_error_string.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 
@@ -91,7 +96,11 @@ def _call(name: str, *args):
     lib = load()
     st = getattr(lib, name)(*args)
     if st != 0:
-        raise MsaError(name, st, lib.msa_status_string(st).decode())
+        text = lib.msa_status_string(st).decode()
+        if st == MSA_ERR_CUDA:
+            code = lib.msa_last_cuda_error()
+            text += f": {lib.msa_cuda_error_string(code).decode()} (cudaError {code})"
+        raise MsaError(name, st, text)
     return st
 
 
@@ -351,6 +360,36 @@ def msa_sparse_attend_prefill_backward(q, k, v, q2k, cu_seqlens, max_seqlen, out
           _ptr(cu_seqlens), cu_seqlens.shape[0] - 1, T, int(max_seqlen), scale, _ptr(out), _ptr(lse),
           _ptr(grad_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws.buf), ws.nbytes, _stream(dev))
     return dq, dk, dv
+
+
+class _SparseAttention(torch.autograd.Function):
+    """NeMo ``_SparseAttention``: the prefill sparse attention as an autograd
+    function (forward: msa_sparse_attend_prefill_lse; backward:
+    msa_sparse_attend_prefill_backward).  q, k and v receive gradients; q2k and
+    the document layout do not."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, q2k, cu_seqlens, max_seqlen, scale):
+        T = q.shape[0]
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+        out = msa_sparse_attend_prefill(q, k, v, q2k, cu_seqlens, max_seqlen, scale=scale, lse=lse)
+        ctx.save_for_backward(q, k, v, q2k, cu_seqlens, out, lse)
+        ctx.max_seqlen, ctx.scale = max_seqlen, scale
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        q, k, v, q2k, cu_seqlens, out, lse = ctx.saved_tensors
+        dq, dk, dv = msa_sparse_attend_prefill_backward(q, k, v, q2k, cu_seqlens, ctx.max_seqlen, out, lse,
+                                                        grad_out.contiguous(), scale=ctx.scale)
+        return dq, dk, dv, None, None, None, None
+
+
+def sparse_attention(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=None):
+    """Differentiable prefill sparse attention (NeMo ``sparse_attention``): bf16 out
+    [tokens, 64, 128]; q, k and v receive gradients through the library's backward."""
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    return _SparseAttention.apply(q, k, v, q2k, cu_seqlens, int(max_seqlen), scale)
 
 
 # ---- packing ----------------------------------------------------------------------

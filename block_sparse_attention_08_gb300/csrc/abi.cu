@@ -62,6 +62,13 @@ static cudaError_t clear_counters(uint8_t* ws, size_t off, size_t bytes, cudaStr
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+thread_local int g_last_cuda_error = 0;
+
+msa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return MSA_ERR_CUDA;
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -105,17 +112,18 @@ msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int ma
 
 msa_status msa_workspace_init(void* workspace, size_t bytes, void* stream) {
   if (!workspace) return MSA_ERR_NULL;
-  return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK
-                                                                                                  : MSA_ERR_CUDA;
+  return cuda_result(cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64_t* detail) {
   if (!workspace || !code) return MSA_ERR_NULL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   DevError h{};
-  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MSA_ERR_CUDA;
-  if (cudaMemsetAsync(workspace, 0, sizeof(DevError), s) != cudaSuccess) return MSA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s); ce != cudaSuccess)
+    return cuda_fail(ce);
+  if (const cudaError_t ce = cudaMemsetAsync(workspace, 0, sizeof(DevError), s); ce != cudaSuccess)
+    return cuda_fail(ce);
+  if (const cudaError_t ce = cudaStreamSynchronize(s); ce != cudaSuccess) return cuda_fail(ce);
   *code = h.code;
   if (detail) *detail = h.detail;
   return MSA_OK;
@@ -129,13 +137,19 @@ msa_status msa_check_bounded_wait(void* workspace, void* stream, int64_t* waits_
   // the two durations go to the header, after the error word
   long long* dev_waits = reinterpret_cast<long long*>(ws + 64);
   long long h[2] = {0, 0};
-  if (launch_wait_check(reinterpret_cast<DevError*>(ws), dev_waits, s) != cudaSuccess) return MSA_ERR_CUDA;
-  if (cudaMemcpyAsync(h, dev_waits, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MSA_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = launch_wait_check(reinterpret_cast<DevError*>(ws), dev_waits, s); ce != cudaSuccess)
+    return cuda_fail(ce);
+  if (const cudaError_t ce = cudaMemcpyAsync(h, dev_waits, sizeof(h), cudaMemcpyDeviceToHost, s); ce != cudaSuccess)
+    return cuda_fail(ce);
+  if (const cudaError_t ce = cudaStreamSynchronize(s); ce != cudaSuccess) return cuda_fail(ce);
   waits_ns[0] = h[0];
   waits_ns[1] = h[1];
   return MSA_OK;
 }
+
+int msa_last_cuda_error(void) { return msa::g_last_cuda_error; }
+
+const char* msa_cuda_error_string(int code) { return cudaGetErrorString(static_cast<cudaError_t>(code)); }
 
 const char* msa_status_string(msa_status s) {
   switch (s) {
@@ -182,7 +196,7 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   cudaError_t e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch,
                                        max_blocks, num_slots, q2k, reinterpret_cast<float*>(ws + L.scores),
                                        reinterpret_cast<int*>(ws + L.sel_tickets), reinterpret_cast<DevError*>(ws), s);
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }
 
 static msa_status attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
@@ -201,13 +215,13 @@ static msa_status attend_decode(const msa_config* cfg, const void* q, const void
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s) != cudaSuccess)
-    return MSA_ERR_CUDA;
+  if (const cudaError_t ce = clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s); ce != cudaSuccess)
+    return cuda_fail(ce);
   AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
   cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out, out_q, out_scale,
                                        reinterpret_cast<float*>(ws + L.partials),
                                        reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }
 
 msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache, const void* v_cache,
@@ -253,7 +267,7 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
   cudaError_t e = launch_prefill_select(*cfg, index_q, index_k, cu_seqlens, num_docs, total_tokens, max_seqlen, q2k,
                                         reinterpret_cast<int*>(ws + L.plan), reinterpret_cast<DevError*>(ws),
                                         static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }
 
 static msa_status attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
@@ -273,7 +287,7 @@ static msa_status attend_prefill(const msa_config* cfg, const void* q, const voi
   cudaError_t e = launch_prefill_attend(q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, cfg->topk,
                                         scale, out, lse, ws + L.bm, reinterpret_cast<DevError*>(ws),
                                         static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }
 
 msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k, const void* v,
@@ -313,7 +327,7 @@ msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void*
   cudaError_t e = launch_prefill_backward(q, k, v, q2k, cu_seqlens, num_docs, total_tokens, max_seqlen, cfg->topk,
                                           scale, out, lse, grad_out, dq, dk, dv, ws + L.bm,
                                           reinterpret_cast<DevError*>(ws), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }
 
 msa_status msa_pack_metadata(const int64_t* doc_ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
@@ -343,7 +357,8 @@ msa_status msa_unpack(const void* packed, const int64_t* token_rows, int64_t tot
   if (total_tokens < 0 || batch_seq < total_tokens || row_bytes < 16 || row_bytes % 16) return MSA_ERR_SHAPE;
   if (!aligned16(external) || !aligned16(packed)) return MSA_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(external, 0, static_cast<size_t>(batch_seq) * row_bytes, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaMemsetAsync(external, 0, static_cast<size_t>(batch_seq) * row_bytes, s); ce != cudaSuccess)
+    return cuda_fail(ce);
   return run_gather(packed, token_rows, total_tokens, row_bytes, external, s, true);
 }
 

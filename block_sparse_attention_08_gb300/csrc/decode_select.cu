@@ -441,6 +441,7 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
                                  int* tickets, DevError* err, cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   DecodeGeom geo{seq_lens, page_table, cu_k, batch, max_blocks, num_slots};
   // one CTA per SM; never more CTAs than pages
   const long long blocks_upper = static_cast<long long>(batch) * max_blocks;
@@ -539,12 +540,12 @@ extern "C" msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, co
   if (need > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // sizes beyond the fixed scratch
   cudaError_t e;
   auto* base = static_cast<uint8_t*>(noalloc_scratch(&e));
-  if (!base) return MSA_ERR_CUDA;
+  if (!base) return cuda_fail(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the error word and the counters must start at zero; the scores are stored before they are read
-  if (cudaMemsetAsync(base, 0, off_scores, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaMemsetAsync(base, 0, off_scores, s); ce != cudaSuccess) return cuda_fail(ce);
   e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
                            num_slots, q2k, reinterpret_cast<float*>(base + off_scores),
                            reinterpret_cast<int*>(base + off_tickets), reinterpret_cast<DevError*>(base), s);
-  return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(e);
 }

@@ -26,6 +26,7 @@ __global__ void wait_check_kernel(DevError* err, long long* waits_ns) {
 }
 
 cudaError_t launch_wait_check(DevError* err, long long* waits_ns, cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   wait_check_kernel<<<1, 32, 0, stream>>>(err, waits_ns);
   return cudaGetLastError();
 }

@@ -46,6 +46,25 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
                                     const void* grad_out, void* dq, void* dk, void* dv, uint8_t* region,
                                     DevError* err, cudaStream_t stream);
 size_t pack_workspace_bytes(int batch, int seq);
+// First step of every launcher.  Clears the calling thread's last CUDA error
+// (the launches are checked with cudaGetLastError, which reports the calling
+// thread's error) and makes the current device's primary context current on
+// this thread: a thread that has made no runtime call yet (PyTorch's autograd
+// worker is one: PyTorch skips cudaSetDevice when the device is already the
+// current one) has no context, and the driver's tensor-map encoder then
+// rejects the device pointers as invalid.
+inline cudaError_t launch_prologue() {
+  (void)cudaGetLastError();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  return e == cudaSuccess ? cudaSetDevice(dev) : e;
+}
+
+// Records a failed CUDA call's code for msa_last_cuda_error (per calling
+// thread) and returns MSA_ERR_CUDA; cuda_result maps cudaSuccess to MSA_OK.
+msa_status cuda_fail(cudaError_t e);
+inline msa_status cuda_result(cudaError_t e) { return e == cudaSuccess ? MSA_OK : cuda_fail(e); }
+
 msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
                              int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,
                              uint8_t* ws, cudaStream_t stream);

@@ -229,6 +229,7 @@ size_t pack_workspace_bytes(int batch, int seq) {
 msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,
                              int* num_docs, int64_t* total_tokens, int* max_seqlen, int64_t* bad_index,
                              uint8_t* ws, cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return cuda_fail(e0);
   const int cap = pack_table_cap(seq);
   const size_t cap_b = static_cast<size_t>(cap);
   uint8_t* p = ws;
@@ -242,15 +243,17 @@ msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu
   auto* sum = reinterpret_cast<PackSummary*>(p);
 
   PackSummary init{0, 0, 0, 0x7fffffffffffffffLL, 0x7fffffffffffffffLL};
-  if (cudaMemcpyAsync(sum, &init, sizeof(init), cudaMemcpyHostToDevice, stream) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaMemcpyAsync(sum, &init, sizeof(init), cudaMemcpyHostToDevice, stream); ce != cudaSuccess)
+    return cuda_fail(ce);
   pack_rows_kernel<<<batch, kPackThreads, 0, stream>>>(ids, seq, cap, keys, minpos, row_real, row_runs, sum);
   pack_offsets_kernel<<<1, 32, 0, stream>>>(batch, row_real, row_runs, cu_seqlens, sum);
   pack_emit_kernel<<<batch, kPackThreads, 0, stream>>>(ids, seq, row_real, row_runs, cu_seqlens, token_rows);
   pack_finish_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, sum);
-  if (cudaGetLastError() != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaGetLastError(); ce != cudaSuccess) return cuda_fail(ce);
   PackSummary h;
-  if (cudaMemcpyAsync(&h, sum, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MSA_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_ERR_CUDA;
+  if (const cudaError_t ce = cudaMemcpyAsync(&h, sum, sizeof(h), cudaMemcpyDeviceToHost, stream); ce != cudaSuccess)
+    return cuda_fail(ce);
+  if (const cudaError_t ce = cudaStreamSynchronize(stream); ce != cudaSuccess) return cuda_fail(ce);
   if (bad_index) *bad_index = -1;
   if (h.first_negative != 0x7fffffffffffffffLL) {
     if (bad_index) *bad_index = h.first_negative;
@@ -269,6 +272,7 @@ msa_status run_pack_metadata(const int64_t* ids, int batch, int seq, int32_t* cu
 
 msa_status run_gather(const void* src, const int64_t* rows, long long n, long long row_bytes, void* dst,
                       cudaStream_t stream, bool scatter) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return cuda_fail(e0);
   const long long vpr = row_bytes / 16;
   const long long total = n * vpr;
   if (total == 0) return MSA_OK;
@@ -280,7 +284,7 @@ msa_status run_gather(const void* src, const int64_t* rows, long long n, long lo
   else
     gather_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), rows, n, vpr,
                                                  static_cast<uint4*>(dst));
-  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return cuda_result(cudaGetLastError());
 }
 
 }  // namespace msa

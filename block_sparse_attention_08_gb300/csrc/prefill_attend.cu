@@ -908,6 +908,7 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
                                   const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
                                   int topk, float scale, void* out, float* lse, uint8_t* region, DevError* err,
                                   cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
   bm_carve(dims, region, &p);
@@ -958,11 +959,12 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
 //   dK += dS^T Q        (A = dS^T, B = Q: both read MN-major)
 //   dQ = dS K           (A = dS K-major, B = K read MN-major)
 // Four math warps (one tile row per thread) turn S and dP into P and dS in
-// shared memory and add each tile's dQ rows to an fp32 accumulator with vector
-// atomics; when the tiles of one key block end (a run), the same warps (one
-// key row per thread) add the block's dK and dV to fp32 accumulators.  A last
-// kernel converts the three accumulators to bf16.  Everything is single
-// buffered: this is the first, correct form of the backward.
+// shared memory and add each tile's dQ rows to the bf16 dq output with packed
+// bf16 vector atomics (as the NeMo page says its backward does: half the
+// atomic traffic of fp32, which bounds the tile period); when the tiles of one
+// key block end (a run), the same warps (one key row per thread) add the
+// block's dK and dV to fp32 accumulators, which a last kernel converts to
+// bf16.  Everything is single buffered.
 constexpr int kBwThreads = 224;  // warps 0-3 math, 4 TMA (K, V, Q), 5 MMA, 6 TMA (dO)
 constexpr int kBwOWarp = 6;
 constexpr int kBwInfo = 4;
@@ -992,6 +994,11 @@ static_assert(sizeof(BwSmem) + 1024 <= 227 * 1024, "shared memory of the backwar
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+// Eight bf16 sums at once (four packed pairs, 16 bytes).
+__device__ __forceinline__ void red_add_bf16x8(__nv_bfloat16* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
 
@@ -1033,7 +1040,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, BmPlan p, long long T,
     int topk, float scale, float scale_log2, const float* __restrict__ lse, const float* __restrict__ Dsum,
-    float* __restrict__ dq_acc, float* __restrict__ dk_acc, float* __restrict__ dv_acc, DevError* err) {
+    __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc, float* __restrict__ dv_acc, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   BwSmem& sm = *reinterpret_cast<BwSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1274,7 +1281,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.p_full);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, i & 1, err, 822))) break;
       tc::fence_after();
-      float* dqr = dq_acc + hrow * kDim;
+      __nv_bfloat16* dqr = dq + hrow * kDim;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -1282,9 +1289,13 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
         tc::wait_ld();
         if (valid) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            red_add_v4(dqr + ch * 32 + 4 * j, scale * __uint_as_float(v[4 * j]), scale * __uint_as_float(v[4 * j + 1]),
-                       scale * __uint_as_float(v[4 * j + 2]), scale * __uint_as_float(v[4 * j + 3]));
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              w[x] = pack_bf16(scale * __uint_as_float(v[8 * j + 2 * x]), scale * __uint_as_float(v[8 * j + 2 * x + 1]));
+            red_add_bf16x8(dqr + ch * 32 + 8 * j, w[0], w[1], w[2], w[3]);
+          }
         }
       }
       tc::fence_before();
@@ -1331,10 +1342,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
 
 // Backward workspace: the forward's bucketing arrays, then (in place of the
 // forward's partials, which the backward does not use) D [T][64] and the fp32
-// accumulators dq [T][64][128], dk and dv [T][4][128].
+// accumulators dk and dv [T][4][128] (dq is summed in the bf16 output).
 struct BwCarve {
   float* D;
-  float* dq;
   float* dk;
   float* dv;
   size_t bytes;
@@ -1351,7 +1361,6 @@ static BwCarve bw_carve(long long T, int max_seqlen, int topk, uint8_t* region) 
     return reinterpret_cast<float*>(ptr);
   };
   c.D = take(static_cast<size_t>(T) * kHeads * sizeof(float));
-  c.dq = take(static_cast<size_t>(T) * kHeads * kDim * sizeof(float));
   c.dk = take(static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float));
   c.dv = take(static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float));
   c.bytes = off;
@@ -1367,6 +1376,7 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
                                     int max_seqlen, int topk, float scale, const void* out, const float* lse,
                                     const void* grad_out, void* dq, void* dk, void* dv, uint8_t* region,
                                     DevError* err, cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
   bm_carve(dims, region, &p);
@@ -1379,7 +1389,8 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
     return cudaErrorInvalidValue;
   const long long T = total_tokens;
   cudaError_t e;
-  if ((e = cudaMemsetAsync(w.dq, 0, static_cast<size_t>(T) * kHeads * kDim * sizeof(float), stream)) != cudaSuccess ||
+  if ((e = cudaMemsetAsync(dq, 0, static_cast<size_t>(T) * kHeads * kDim * sizeof(__nv_bfloat16), stream)) !=
+          cudaSuccess ||
       (e = cudaMemsetAsync(w.dk, 0, static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float), stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(w.dv, 0, static_cast<size_t>(T) * kKvHeads * kDim * sizeof(float), stream)) != cudaSuccess)
     return e;
@@ -1400,10 +1411,9 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
   const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
   bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, p, T, topk, scale,
-                                                       scale * 1.4426950408889634f, lse, w.D, w.dq, w.dk, w.dv, err);
-  const long long nq8 = T * kHeads * kDim / 8, nk8 = T * kKvHeads * kDim / 8;
-  bw_to_bf16_kernel<<<static_cast<unsigned>((nq8 + 255) / 256), 256, 0, stream>>>(w.dq, nq8,
-                                                                                 static_cast<__nv_bfloat16*>(dq));
+                                                       scale * 1.4426950408889634f, lse, w.D,
+                                                       static_cast<__nv_bfloat16*>(dq), w.dk, w.dv, err);
+  const long long nk8 = T * kKvHeads * kDim / 8;
   bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dk, nk8,
                                                                                  static_cast<__nv_bfloat16*>(dk));
   bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dv, nk8,

@@ -402,6 +402,7 @@ size_t prefill_plan_ints(int num_docs, int max_tiles) {
 cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, const void* index_k,
                                   const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,
                                   int32_t* q2k, int* plan_ints, DevError* err, cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return cudaErrorInvalidValue;
   const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;

@@ -562,6 +562,7 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,
                                  cudaStream_t stream) {
+  if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   CUtensorMap kmap, vmap, qmap;
   if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows) ||
       !make_q_map(&qmap, q, geo.nq))

@@ -18,6 +18,10 @@
  *     passed as void*; NULL = legacy default stream).
  *   - No entry point synchronises the stream except msa_pack_metadata and
  *     msa_read_device_error, which say so.
+ *   - Work runs on the calling thread's current device (cudaGetDevice), whose
+ *     primary context each call makes current on the calling thread, so any
+ *     thread may call (a fresh one, or PyTorch's autograd worker, included).
+ *     Device buffers and the stream must belong to that device.
  *   - Tensors are dense row-major with the shapes given; tensor base pointers
  *     must be 16-byte aligned.
  *   - Errors are returned synchronously as msa_status; nothing is thrown and
@@ -123,6 +127,14 @@ msa_status msa_read_device_error(void* workspace, void* stream, int* code, int64
 
 /* Human-readable name of a status. */
 const char* msa_status_string(msa_status status);
+
+/* The CUDA error code (a cudaError_t value) of the last call on the calling
+ * thread that returned MSA_ERR_CUDA; 0 if none has.  Calls that succeed leave
+ * it unchanged. */
+int msa_last_cuda_error(void);
+
+/* Text of a CUDA error code (cudaGetErrorString); the pointer is static. */
+const char* msa_cuda_error_string(int code);
 
 /* Diagnostic of the library's bounded on-chip waits (every pipeline wait of
  * every kernel above uses them).  Launches one CTA on `stream` whose first
@@ -279,9 +291,10 @@ msa_status msa_sparse_attend_prefill_lse(const msa_config* cfg, const void* q, c
  *              (msa_sparse_attend_prefill_lse)
  *   dq, dk, dv dev bf16, written whole (zero for tokens no query reaches)
  *   workspace  >= msa_workspace_size(cfg, MSA_MODE_PREFILL_BWD, total_tokens,
- *              ceil(max_seqlen / 128)); holds fp32 accumulators for dq, dk, dv
- * Gradients are summed with fp32 atomics, so they are not bitwise
- * reproducible from run to run (as the pages say of theirs).
+ *              ceil(max_seqlen / 128)); holds fp32 accumulators for dk, dv
+ * dk and dv are summed with fp32 atomics, dq with packed bf16 atomics into
+ * the output (as the NeMo page says of its backward), so the gradients are
+ * not bitwise reproducible from run to run.
  * Errors: MSA_ERR_NULL, MSA_ERR_SHAPE, MSA_ERR_ALIGN (any tensor not 16-byte
  * aligned), MSA_ERR_WORKSPACE, MSA_ERR_CUDA. */
 msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void* q, const void* k,

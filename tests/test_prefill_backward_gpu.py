@@ -78,3 +78,19 @@ def test_prefill_lse_is_the_log_sum_exp():
             z = SCALE * (k[keys, g] @ q[t, h])
             ref = (np.log(np.sum(np.exp(z - z.max()))) + z.max()) / np.log(2.0)
             assert abs(got[t, h] - ref) <= 1e-4 * (1 + abs(ref)), (t, h, got[t, h], ref)
+
+
+def test_sparse_attention_autograd():
+    # the autograd wrapper (NeMo sparse_attention: q, k and v receive gradients) against the oracle
+    p = msa_synth.prefill_inputs([200, 130], seed=9, device="cuda")
+    q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
+    q, k, v = (x.clone().requires_grad_(True) for x in (p.q, p.k, p.v))
+    out = msa.sparse_attention(q, k, v, q2k, p.cu_seqlens, p.max_seqlen, scale=SCALE)
+    gen = torch.Generator(device="cpu").manual_seed(10)
+    dout = torch.randn(out.shape, generator=gen).to(torch.bfloat16).cuda()
+    out.backward(dout)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attend_prefill_backward(p.q, p.k, p.v, dout, p.cu_seqlens, q2k, SCALE)
+    _close("dq", q.grad, rq)
+    _close("dk", k.grad, rk)
+    _close("dv", v.grad, rv)
