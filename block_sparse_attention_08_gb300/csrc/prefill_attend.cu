@@ -951,22 +951,31 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
 //
 // Same bucketing and tiles as the forward: a tile is 8 (query, KV head) entries
 // x 16 heads against one key block.  Per tile, five 128 x 128 x 128 tcgen05
-// products, with S (then dQ), dP and the block's dV and dK accumulators in
-// the four 128-column quarters of tensor memory:
+// products, in this order, with S, dP (then dQ) and the block's dV and dK
+// accumulators in the four 128-column quarters of tensor memory:
 //   S  = Q K^T          (A = Q, B = K: both K-major)
 //   dP = dO V^T         (A = dO, B = V: both K-major)
-//   dV += P^T dO        (A = P^T, B = dO: both read MN-major)
-//   dK += dS^T Q        (A = dS^T, B = Q: both read MN-major)
+//   dK += dS^T Q        (A = dS^T, B = Q: both read MN-major)   frees Q
+//   dV += P^T dO        (A = P^T, B = dO: both read MN-major)   frees dO
 //   dQ = dS K           (A = dS K-major, B = K read MN-major)
-// Four math warps (one tile row per thread) turn S and dP into P and dS in
-// shared memory and add each tile's dQ rows to the bf16 dq output with packed
-// bf16 vector atomics (as the NeMo page says its backward does: half the
-// atomic traffic of fp32, which bounds the tile period); when the tiles of one
-// key block end (a run), the same warps (one key row per thread) add the
-// block's dK and dV to fp32 accumulators, which a last kernel converts to
-// bf16.  Everything is single buffered.
-constexpr int kBwThreads = 224;  // warps 0-3 math, 4 TMA (K, V, Q), 5 MMA, 6 TMA (dO)
-constexpr int kBwOWarp = 6;
+// The tiles' Q and dO rows stream through a ring of three 32 KB slots, so the
+// next tile's Q is resident while a tile runs and its dO lands while dV and
+// dQ run; the next tile's S is issued right behind dQ (its columns are free
+// once P and dS are built), and only its dP waits for dQ to be read out.
+// Eight math warps (two per tensor-memory lane group, one half of the
+// columns each: P and dS are elementwise in S and dP given the forward's
+// lse, so the halves need no exchange) build P and dS in shared memory; each
+// then writes its quarter of the tile's dQ (bf16) into its own bytes of the
+// P buffer and has the tensor engine add those two 16 x 64 boxes into the
+// bf16 dq output (a bulk bf16 reduction, where the NeMo page sums dq with
+// bf16 atomics: per-thread atomics, 32 KB a tile, queued the memory
+// instructions of the whole SM).  When the tiles of one key block end (a
+// run), the same warps add the block's dK and dV to fp32 accumulators, which
+// a last kernel converts to bf16.
+constexpr int kBwThreads = 352;  // warps 0-7 math, 8 TMA (K, V, Q), 9 MMA, 10 TMA (dO)
+constexpr int kBwMath = 8;       // two per tensor-memory lane group, one half of the columns each
+constexpr int kBwTmaWarp = 8, kBwMmaWarp = 9, kBwOWarp = 10;
+constexpr int kBwSlots = 3;  // ring of Q / dO tiles: load 2i is tile i's Q, load 2i + 1 its dO
 constexpr int kBwInfo = 4;
 constexpr uint32_t kIdescKK = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescKM = tc::idesc_bf16_f32(128, 128) | (1u << 16);               // B MN-major
@@ -978,27 +987,22 @@ struct BwInfo {
 };
 
 struct BwSmem {
-  alignas(1024) uint8_t q[kBmTile];     // the tile's Q rows
-  alignas(1024) uint8_t dout[kBmTile];  // the tile's dO rows
-  alignas(1024) uint8_t k[kBmTile];     // the block's K
-  alignas(1024) uint8_t v[kBmTile];     // the block's V
-  alignas(1024) uint8_t p[kBmTile];     // P, bf16 [rows][keys]
-  alignas(1024) uint8_t ds[kBmTile];    // dS, bf16 [rows][keys]
+  alignas(1024) uint8_t qd[kBwSlots][kBmTile];  // Q and dO rows of the tiles, in load order
+  alignas(1024) uint8_t k[kBmTile];              // the block's K
+  alignas(1024) uint8_t v[kBmTile];              // the block's V
+  alignas(1024) uint8_t p[kBmTile];              // P, bf16 [rows][keys]
+  alignas(1024) uint8_t ds[kBmTile];             // dS, bf16 [rows][keys]
   uint64_t info_full[kBwInfo], info_empty[kBwInfo];
-  uint64_t kv_full, kv_empty, qd_full, qd_empty;
+  uint64_t kv_full, kv_empty, qd_full[kBwSlots], qd_empty[kBwSlots];
   uint64_t s_full, p_full, dq_full, dq_free, acc_full, acc_free, done;
   BwInfo info[kBwInfo];
+  int loads[2];  // Q and dO tiles issued, for the drain at exit
   uint32_t tmem_base;
 };
 static_assert(sizeof(BwSmem) + 1024 <= 227 * 1024, "shared memory of the backward kernel");
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-// Eight bf16 sums at once (four packed pairs, 16 bytes).
-__device__ __forceinline__ void red_add_bf16x8(__nv_bfloat16* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
 
@@ -1038,9 +1042,10 @@ __global__ void __launch_bounds__(256) bw_to_bf16_kernel(const float* __restrict
 
 __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, BmPlan p, long long T,
-    int topk, float scale, float scale_log2, const float* __restrict__ lse, const float* __restrict__ Dsum,
-    __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc, float* __restrict__ dv_acc, DevError* err) {
+    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+    const __grid_constant__ CUtensorMap dqmap, BmPlan p, long long T, int topk, float scale, float scale_log2,
+    const float* __restrict__ lse, const float* __restrict__ Dsum, float* __restrict__ dk_acc,
+    float* __restrict__ dv_acc, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   BwSmem& sm = *reinterpret_cast<BwSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1049,27 +1054,29 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
   if (tid == 0) {
     for (int i = 0; i < kBwInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
-      mbar_init(&sm.info_empty[i], 6);  // four math warps, the MMA thread, the dO warp
+      mbar_init(&sm.info_empty[i], kBwMath + 2);  // the math warps, the MMA thread, the dO warp
     }
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    mbar_init(&sm.qd_full, 2);  // Q (warp 4) and dO (warp 6) each arm their bytes
-    mbar_init(&sm.qd_empty, 1);
+    for (int i = 0; i < kBwSlots; ++i) {
+      mbar_init(&sm.qd_full[i], 1);
+      mbar_init(&sm.qd_empty[i], 1);
+    }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.p_full, kBwMath);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 4);
+    mbar_init(&sm.dq_free, kBwMath);
     mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_free, 4);
+    mbar_init(&sm.acc_free, kBwMath);
     mbar_init(&sm.done, 1);
     fence_mbar_init();
   }
   // Rows of entries a tile does not fill keep earlier (finite) data; start
   // from zeros so that no NaN pattern meets a zero weight in an MMA.
-  for (int i = tid; i < 6 * kBmTile / 16; i += kBwThreads)
-    sts128(smem_u32(sm.q) + 16 * i, 0u, 0u, 0u, 0u);
+  for (int i = tid; i < (kBwSlots + 4) * kBmTile / 16; i += kBwThreads)
+    sts128(smem_u32(sm.qd[0]) + 16 * i, 0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
-  if (warp == 5) {
+  if (warp == kBwMmaWarp) {
     tc::alloc(&sm.tmem_base, 512);
     tc::relinquish();
   }
@@ -1078,8 +1085,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
   tc::fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 4) {
-    // ---------------- scheduler + TMA ----------------
+  if (warp == kBwTmaWarp) {
+    // ---------------- scheduler + TMA (K, V and the tiles' Q) ----------------
     if (lane == 0) {
       prefetch_tmap(&qmap);
       prefetch_tmap(&kmap);
@@ -1089,7 +1096,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
     BmTile d_next = n > 0 ? p.tiles[tile_at(0)] : none;
     int e_next = lane < d_next.cnt ? p.elist[d_next.off + lane] : 0;
     BmTile d_after = n > 1 ? p.tiles[tile_at(1)] : none;
-    int prow = -1, pg = -1, nkv = 0, nqd = 0;
+    int prow = -1, pg = -1, nkv = 0, nq = 0;
     for (int i = 0; i < n; ++i) {
       const BmTile d = d_next;
       const int ent = e_next;
@@ -1112,6 +1119,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_full[is]);
+      const int ld = 2 * i, slot = ld % kBwSlots;
       if (lane == 0) {
         if (fresh) {
           ok = mbar_wait(&sm.kv_empty, (nkv & 1) ^ 1, err, 801);
@@ -1124,8 +1132,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
             ++nkv;
           }
         }
-        ok = ok && mbar_wait(&sm.qd_empty, (nqd & 1) ^ 1, err, 802);
-        if (ok) mbar_expect_tx(&sm.qd_full, d.cnt * 2 * kBmQBox);
+        ok = ok && mbar_wait(&sm.qd_empty[slot], ((ld / kBwSlots) & 1) ^ 1, err, 802);
+        if (ok) mbar_expect_tx(&sm.qd_full[slot], d.cnt * 2 * kBmQBox);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (fresh) {
@@ -1134,22 +1142,23 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       }
       if (lane < d.cnt) {
         const int t = ent / topk;
-        tma_load_3d(sm.q + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.qd_full);
-        tma_load_3d(sm.q + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.qd[slot] + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.qd_full[slot]);
+        tma_load_3d(sm.qd[slot] + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.qd_full[slot]);
       }
       __syncwarp();
-      ++nqd;
+      ++nq;
     }
-    // no copy may still be landing when the CTA exits
+    // no copy may still be landing when the CTA exits (the ring's slots are
+    // drained below, once both producers have stopped)
     if (lane == 0) {
       if (nkv > 0) mbar_wait(&sm.kv_full, (nkv - 1) & 1, err, 803);
-      if (nqd > 0) mbar_wait(&sm.qd_full, (nqd - 1) & 1, err, 804);
+      sm.loads[0] = nq;
     }
   } else if (warp == kBwOWarp) {
     // ---------------- dO rows of each tile (the tensor copies of Q and dO
     // are issued from two warps: about 100 cycles of issue per 2 KB box) ----------------
     if (lane == 0) prefetch_tmap(&omap);
-    int nqd = 0;
+    int no = 0;
     for (int i = 0; i < n; ++i) {
       const int is = i % kBwInfo;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBwInfo) & 1, err, 805))) break;
@@ -1157,26 +1166,27 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       const int ent = lane < kBmEntries ? sm.info[is].ent[lane] : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
+      const int ld = 2 * i + 1, slot = ld % kBwSlots;
       bool ok = true;
       if (lane == 0) {
-        ok = mbar_wait(&sm.qd_empty, (nqd & 1) ^ 1, err, 806);
-        if (ok) mbar_expect_tx(&sm.qd_full, cnt * 2 * kBmQBox);
+        ok = mbar_wait(&sm.qd_empty[slot], ((ld / kBwSlots) & 1) ^ 1, err, 806);
+        if (ok) mbar_expect_tx(&sm.qd_full[slot], cnt * 2 * kBmQBox);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (lane < cnt) {
         const int t = ent / topk;
-        tma_load_3d(sm.dout + lane * kBmQBox, &omap, 0, g * kGroup, t, &sm.qd_full);
-        tma_load_3d(sm.dout + kBmHalf + lane * kBmQBox, &omap, 64, g * kGroup, t, &sm.qd_full);
+        tma_load_3d(sm.qd[slot] + lane * kBmQBox, &omap, 0, g * kGroup, t, &sm.qd_full[slot]);
+        tma_load_3d(sm.qd[slot] + kBmHalf + lane * kBmQBox, &omap, 64, g * kGroup, t, &sm.qd_full[slot]);
       }
       __syncwarp();
-      ++nqd;
+      ++no;
     }
-    // no copy may still be landing when the CTA exits
-    if (lane == 0 && nqd > 0) mbar_wait(&sm.qd_full, (nqd - 1) & 1, err, 807);
-  } else if (warp == 5) {
+    if (lane == 0) sm.loads[1] = no;
+  } else if (warp == kBwMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       int nkv = 0;
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), pa = smem_u32(sm.p), dsa = smem_u32(sm.ds);
       for (int i = 0; i < n; ++i) {
         const int is = i % kBwInfo;
         if (!mbar_wait(&sm.info_full[is], (i / kBwInfo) & 1, err, 810)) break;
@@ -1187,41 +1197,47 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
           if (!mbar_wait(&sm.kv_full, nkv & 1, err, 811)) break;
           ++nkv;
         }
-        if (!mbar_wait(&sm.qd_full, i & 1, err, 812)) break;
-        if (i > 0 && !mbar_wait(&sm.dq_free, (i - 1) & 1, err, 813)) break;  // S reuses the dQ columns
+        const int lq = 2 * i, lo = 2 * i + 1, sq = lq % kBwSlots, so = lo % kBwSlots;
+        const uint32_t qa = smem_u32(sm.qd[sq]), oa = smem_u32(sm.qd[so]);
+        // S's columns were read out before the previous tile's P / dS were
+        // published, which this thread waited for
+        if (!mbar_wait(&sm.qd_full[sq], (lq / kBwSlots) & 1, err, 812)) break;
         tc::fence_after();
-        const uint32_t qa = smem_u32(sm.q), oa = smem_u32(sm.dout), ka = smem_u32(sm.k), va = smem_u32(sm.v);
-        const uint32_t pa = smem_u32(sm.p), dsa = smem_u32(sm.ds);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
           tc::mma_bf16(tmem, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kIdescKK, kk > 0);
         }
+        if (!mbar_wait(&sm.qd_full[so], (lo / kBwSlots) & 1, err, 813)) break;
+        // dP reuses the columns of the previous tile's dQ
+        if (i > 0 && !mbar_wait(&sm.dq_free, (i - 1) & 1, err, 814)) break;
+        tc::fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
           tc::mma_bf16(tmem + 128, tc::desc_k_sw128(oa + off), tc::desc_k_sw128(va + off), kIdescKK, kk > 0);
         }
         tc::commit(&sm.s_full);
-        if (!mbar_wait(&sm.p_full, i & 1, err, 814)) break;
+        if (!mbar_wait(&sm.p_full, i & 1, err, 815)) break;
         // the previous run's dK / dV must be read out before a fresh tile restarts them
-        if (fresh && run > 0 && !mbar_wait(&sm.acc_free, (run - 1) & 1, err, 815)) break;
+        if (fresh && run > 0 && !mbar_wait(&sm.acc_free, (run - 1) & 1, err, 816)) break;
         tc::fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc::mma_bf16(tmem + 256, desc_v_mn_sw128(pa + kk * 2048), desc_v_mn_sw128(oa + kk * 2048), kIdescMM,
-                       kk > 0 || !fresh);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc::mma_bf16(tmem + 384, desc_v_mn_sw128(dsa + kk * 2048), desc_v_mn_sw128(qa + kk * 2048), kIdescMM,
                        kk > 0 || !fresh);
+        tc::commit(&sm.qd_empty[sq]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc::mma_bf16(tmem + 256, desc_v_mn_sw128(pa + kk * 2048), desc_v_mn_sw128(oa + kk * 2048), kIdescMM,
+                       kk > 0 || !fresh);
+        tc::commit(&sm.qd_empty[so]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem, tc::desc_k_sw128(dsa + off), desc_v_mn_sw128(ka + kk * 2048), kIdescKM, kk > 0);
+          tc::mma_bf16(tmem + 128, tc::desc_k_sw128(dsa + off), desc_v_mn_sw128(ka + kk * 2048), kIdescKM, kk > 0);
         }
         tc::commit(&sm.dq_full);
-        tc::commit(&sm.qd_empty);
         if (last) {
           tc::commit(&sm.acc_full);
           tc::commit(&sm.kv_empty);
@@ -1229,13 +1245,15 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       }
       // every MMA has finished before tensor memory is released
       tc::commit(&sm.done);
-      mbar_wait(&sm.done, 0, err, 816);
+      mbar_wait(&sm.done, 0, err, 817);
     }
-  } else if (warp < 4) {
-    // ---------------- math warps 0-3 ----------------
-    const int r = warp * 32 + lane, e = r >> 4, h = r & 15;
-    const uint32_t lrow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  } else if (warp < kBwMath) {
+    // ---------------- math warps 0-7: warp w takes tile row (w % 4) * 32 + lane
+    // and columns (w / 4) * 64 ... + 63 of every 128-column quarter ----------------
+    const int r = (warp & 3) * 32 + lane, e = r >> 4, h = r & 15, c0 = (warp >> 2) * 2;
+    const uint32_t lrow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t ps = smem_u32(sm.p), dss = smem_u32(sm.ds);
+    if (tid == 0) prefetch_tmap(&dqmap);
     int nacc = 0;
     for (int i = 0; i < n; ++i) {
       const int is = i % kBwInfo;
@@ -1252,8 +1270,11 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       const float lse_r = valid ? lse[hrow] : 0.f, d_r = valid ? Dsum[hrow] : 0.f;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full, i & 1, err, 821))) break;
       tc::fence_after();
+      // the previous tile's dQ reductions read these bytes of the P buffer
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = c0; ch < c0 + 2; ++ch) {
         uint32_t sv[32], dp[32];
         tc::ld_32x32b_x32(lrow + ch * 32, sv);
         tc::ld_32x32b_x32(lrow + 128 + ch * 32, dp);
@@ -1281,26 +1302,37 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.p_full);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, i & 1, err, 822))) break;
       tc::fence_after();
-      __nv_bfloat16* dqr = dq + hrow * kDim;
+      // dQ (scaled, bf16) goes to this warp's own bytes of the P buffer (every
+      // product of the tile has finished), laid out as the Q tile's boxes: the
+      // warp's 32 rows are two entries, its 64 columns one d half, so it
+      // reduces exactly two boxes into dq with the tensor engine
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = c0; ch < c0 + 2; ++ch) {
         uint32_t v[32];
-        tc::ld_32x32b_x32(lrow + ch * 32, v);
+        tc::ld_32x32b_x32(lrow + 128 + ch * 32, v);
         tc::wait_ld();
-        if (valid) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
-              w[x] = pack_bf16(scale * __uint_as_float(v[8 * j + 2 * x]), scale * __uint_as_float(v[8 * j + 2 * x + 1]));
-            red_add_bf16x8(dqr + ch * 32 + 8 * j, w[0], w[1], w[2], w[3]);
-          }
+          for (int x = 0; x < 4; ++x)
+            w[x] = pack_bf16(scale * __uint_as_float(v[8 * c + 2 * x]), scale * __uint_as_float(v[8 * c + 2 * x + 1]));
+          const int c16 = ch * 4 + c;
+          sts128(ps + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), w[0], w[1], w[2], w[3]);
         }
       }
       tc::fence_before();
+      fence_proxy_async_smem();
+      const int t_hi = __shfl_sync(0xffffffffu, static_cast<int>(t), 16);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.dq_free);
+      if (lane == 0) {
+        mbar_arrive(&sm.dq_free);
+        const int e0 = 2 * (warp & 3), hf = warp >> 2;
+        if (e0 < cnt) tma_reduce_add_3d(&dqmap, sm.p + hf * kBmHalf + e0 * kBmQBox, hf * 64, g * kGroup, static_cast<int>(t));
+        if (e0 + 1 < cnt)
+          tma_reduce_add_3d(&dqmap, sm.p + hf * kBmHalf + (e0 + 1) * kBmQBox, hf * 64, g * kGroup, t_hi);
+        bulk_commit();
+      }
       if (last) {
         // the run's dK and dV: thread r holds key row0 + r of the block
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.acc_full, nacc & 1, err, 823))) break;
@@ -1310,7 +1342,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
         float* dvr = dv_acc + (krow * kKvHeads + g) * kDim;
         float* dkr = dk_acc + (krow * kKvHeads + g) * kDim;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = c0; ch < c0 + 2; ++ch) {
           uint32_t a[32], b[32];
           tc::ld_32x32b_x32(lrow + 256 + ch * 32, a);
           tc::ld_32x32b_x32(lrow + 384 + ch * 32, b);
@@ -1331,12 +1363,26 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
         if (lane == 0) mbar_arrive(&sm.acc_free);
       }
     }
+    if (lane == 0) bulk_wait_all();  // the dQ reductions have landed
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBwMmaWarp) {
     tc::fence_after();
     tc::dealloc(tmem, 512);
+  }
+  if (warp == kBwTmaWarp && lane == 0) {
+    // A slot is refilled only after its previous load was consumed (and so
+    // had landed): only the latest load into each slot can still be in
+    // flight (after an error stopped the MMA thread early).  Wait for those.
+    int latest[kBwSlots] = {-1, -1, -1};
+    for (int j = sm.loads[0] > 3 ? sm.loads[0] - 3 : 0; j < sm.loads[0]; ++j) latest[(2 * j) % kBwSlots] = 2 * j;
+    for (int j = sm.loads[1] > 3 ? sm.loads[1] - 3 : 0; j < sm.loads[1]; ++j) {
+      const int ld = 2 * j + 1;
+      if (ld > latest[ld % kBwSlots]) latest[ld % kBwSlots] = ld;
+    }
+    for (int s = 0; s < kBwSlots; ++s)
+      if (latest[s] >= 0) mbar_wait(&sm.qd_full[s], (latest[s] / kBwSlots) & 1, err, 804);
   }
 }
 
@@ -1381,9 +1427,10 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   BmPlan p;
   bm_carve(dims, region, &p);
   const BwCarve w = bw_carve(total_tokens, max_seqlen, topk, region);
-  CUtensorMap qmap, omap, kmap, vmap;
+  CUtensorMap qmap, omap, kmap, vmap, dqmap;
   if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&omap, grad_out, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode3d(&dqmap, dq, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
       !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
     return cudaErrorInvalidValue;
@@ -1410,9 +1457,8 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   cudaFuncSetAttribute(bw_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
   const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
-  bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, p, T, topk, scale,
-                                                       scale * 1.4426950408889634f, lse, w.D,
-                                                       static_cast<__nv_bfloat16*>(dq), w.dk, w.dv, err);
+  bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, dqmap, p, T, topk, scale,
+                                                       scale * 1.4426950408889634f, lse, w.D, w.dk, w.dv, err);
   const long long nk8 = T * kKvHeads * kDim / 8;
   bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dk, nk8,
                                                                                  static_cast<__nv_bfloat16*>(dk));
