@@ -885,6 +885,20 @@ static bool encode3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [d2][d1][d0] with a (b0, b1, b2) box, 128-byte swizzle (b0 = 32).
+static bool encode3d_f32(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+                         cuuint32_t b0, cuuint32_t b1, cuuint32_t b2) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over the fp16 partials viewed as [entries * 16 rows, 128]; box = 64 dims x 16 rows.
 static bool encode_partials(CUtensorMap* map, const void* base, long long rows) {
   EncodeTiledFn enc = get_encode_tiled();
@@ -1001,10 +1015,6 @@ struct BwSmem {
 };
 static_assert(sizeof(BwSmem) + 1024 <= 227 * 1024, "shared memory of the backward kernel");
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 // D[t][h] = <dO[t][h], out[t][h]> (fp32, bf16 inputs): one warp per (token, head).
 __global__ void __launch_bounds__(256) bw_rowdot_kernel(const __nv_bfloat16* __restrict__ dout,
@@ -1040,12 +1050,16 @@ __global__ void __launch_bounds__(256) bw_to_bf16_kernel(const float* __restrict
   reinterpret_cast<uint4*>(dst)[i] = o;
 }
 
-__global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
+// Registers: the busiest of the four sub-partitions holds ceil(11 / 4) = 3
+// warps, and a sub-partition has 16384 registers.
+constexpr int kBwMaxRegs = 168;
+static_assert((kBwThreads / 32 + 3) / 4 * 32 * kBwMaxRegs <= 16384, "registers of the backward kernel");
+__global__ void __maxnreg__(kBwMaxRegs) bw_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-    const __grid_constant__ CUtensorMap dqmap, BmPlan p, long long T, int topk, float scale, float scale_log2,
-    const float* __restrict__ lse, const float* __restrict__ Dsum, float* __restrict__ dk_acc,
-    float* __restrict__ dv_acc, DevError* err) {
+    const __grid_constant__ CUtensorMap dqmap, const __grid_constant__ CUtensorMap dkmap,
+    const __grid_constant__ CUtensorMap dvmap, BmPlan p, long long T, int topk, float scale, float scale_log2,
+    const float* __restrict__ lse, const float* __restrict__ Dsum, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   BwSmem& sm = *reinterpret_cast<BwSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1253,7 +1267,11 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
     const int r = (warp & 3) * 32 + lane, e = r >> 4, h = r & 15, c0 = (warp >> 2) * 2;
     const uint32_t lrow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t ps = smem_u32(sm.p), dss = smem_u32(sm.ds);
-    if (tid == 0) prefetch_tmap(&dqmap);
+    if (tid == 0) {
+      prefetch_tmap(&dqmap);
+      prefetch_tmap(&dkmap);
+      prefetch_tmap(&dvmap);
+    }
     int nacc = 0;
     for (int i = 0; i < n; ++i) {
       const int is = i % kBwInfo;
@@ -1273,24 +1291,41 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
       // the previous tile's dQ reductions read these bytes of the P buffer
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
-#pragma unroll 1
-      for (int ch = c0; ch < c0 + 2; ++ch) {
-        uint32_t sv[32], dp[32];
-        tc::ld_32x32b_x32(lrow + ch * 32, sv);
-        tc::ld_32x32b_x32(lrow + 128 + ch * 32, dp);
-        tc::wait_ld();
-        uint32_t pk[16], dk[16];
+      // 16-column pieces, the next piece's loads in flight while one is computed
+      uint32_t sv[2][16], dp[2][16];
+      tc::ld_32x32b_x16(lrow + c0 * 32, sv[0]);
+      tc::ld_32x32b_x16(lrow + 128 + c0 * 32, dp[0]);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int kc = ch * 32 + 2 * q;
-          const float pa = kc < nkeys ? ex2(fmaf(__uint_as_float(sv[2 * q]), scale_log2, -lse_r)) : 0.f;
-          const float pb = kc + 1 < nkeys ? ex2(fmaf(__uint_as_float(sv[2 * q + 1]), scale_log2, -lse_r)) : 0.f;
+      for (int pc = 0; pc < 4; ++pc) {
+        tc::wait_ld();
+        if (pc < 3) {
+          tc::ld_32x32b_x16(lrow + c0 * 32 + (pc + 1) * 16, sv[(pc + 1) & 1]);
+          tc::ld_32x32b_x16(lrow + 128 + c0 * 32 + (pc + 1) * 16, dp[(pc + 1) & 1]);
+        }
+        const uint32_t(&s_)[16] = sv[pc & 1];
+        const uint32_t(&d_)[16] = dp[pc & 1];
+        uint32_t pk[8], dk[8];
+        // keys at or past nkeys (the causal edge, the document's end) get P = 0;
+        // away from the diagonal block every key of the piece counts
+        const int kc0 = c0 * 32 + pc * 16;
+        const bool whole = kc0 + 16 <= nkeys;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float2 z = fma2(__uint_as_float(s_[2 * q]), __uint_as_float(s_[2 * q + 1]), scale_log2, scale_log2,
+                                -lse_r, -lse_r);
+          float pa = ex2(z.x), pb = ex2(z.y);
+          if (!whole) {
+            pa = kc0 + 2 * q < nkeys ? pa : 0.f;
+            pb = kc0 + 2 * q + 1 < nkeys ? pb : 0.f;
+          }
           pk[q] = pack_bf16(pa, pb);
-          dk[q] = pack_bf16(pa * (__uint_as_float(dp[2 * q]) - d_r), pb * (__uint_as_float(dp[2 * q + 1]) - d_r));
+          const float2 dd = sub2(__uint_as_float(d_[2 * q]), __uint_as_float(d_[2 * q + 1]), d_r, d_r);
+          const float2 ds = mul2(pa, pb, dd.x, dd.y);
+          dk[q] = pack_bf16(ds.x, ds.y);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte row
+        for (int c = 0; c < 2; ++c) {
+          const int c16 = c0 * 4 + pc * 2 + c;  // 16-byte chunk of the 256-byte row
           const uint32_t off = (c16 >> 3) * kBmHalf + sw128(r, c16 & 7);
           sts128(ps + off, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           sts128(dss + off, dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
@@ -1316,7 +1351,10 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
           uint32_t w[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x)
-            w[x] = pack_bf16(scale * __uint_as_float(v[8 * c + 2 * x]), scale * __uint_as_float(v[8 * c + 2 * x + 1]));
+          {
+            const float2 y = mul2(__uint_as_float(v[8 * c + 2 * x]), __uint_as_float(v[8 * c + 2 * x + 1]), scale, scale);
+            w[x] = pack_bf16(y.x, y.y);
+          }
           const int c16 = ch * 4 + c;
           sts128(ps + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), w[0], w[1], w[2], w[3]);
         }
@@ -1334,28 +1372,44 @@ __global__ void __launch_bounds__(kBwThreads, 1) bw_attend_kernel(
         bulk_commit();
       }
       if (last) {
-        // the run's dK and dV: thread r holds key row0 + r of the block
+        // The run's dV, then its dK, through this warp's own 8 KB of the P
+        // and dS buffers (every product of the run has finished): its 32 key
+        // rows x 64 columns in fp32 are two 32 x 32 boxes with the 128-byte
+        // swizzle, which the tensor engine adds into the fp32 accumulators.
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.acc_full, nacc & 1, err, 823))) break;
         ++nacc;
         tc::fence_after();
-        const long long krow = static_cast<long long>(row0) + r;
-        float* dvr = dv_acc + (krow * kKvHeads + g) * kDim;
-        float* dkr = dk_acc + (krow * kKvHeads + g) * kDim;
+        const int krow0 = row0 + (warp & 3) * 32;
+        const uint32_t own[2] = {ps + (warp >> 2) * kBmHalf + (warp & 3) * 4096,
+                                 dss + (warp >> 2) * kBmHalf + (warp & 3) * 4096};
 #pragma unroll 1
-        for (int ch = c0; ch < c0 + 2; ++ch) {
-          uint32_t a[32], b[32];
-          tc::ld_32x32b_x32(lrow + 256 + ch * 32, a);
-          tc::ld_32x32b_x32(lrow + 384 + ch * 32, b);
-          tc::wait_ld();
-          if (krow < T) {
+        for (int acc = 0; acc < 2; ++acc) {
+          // the earlier reductions of this warp have read these bytes
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          const float f = acc == 0 ? 1.f : scale;
+#pragma unroll 1
+          for (int jj = 0; jj < 2; ++jj) {
+            uint32_t a[32];
+            tc::ld_32x32b_x32(lrow + (acc == 0 ? 256 : 384) + (c0 + jj) * 32, a);
+            tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              red_add_v4(dvr + ch * 32 + 4 * j, __uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                         __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3]));
-              red_add_v4(dkr + ch * 32 + 4 * j, scale * __uint_as_float(b[4 * j]),
-                         scale * __uint_as_float(b[4 * j + 1]), scale * __uint_as_float(b[4 * j + 2]),
-                         scale * __uint_as_float(b[4 * j + 3]));
+            for (int j = 0; j < 8; ++j)
+              sts128(own[jj] + sw128(lane, j), __float_as_uint(f * __uint_as_float(a[4 * j])),
+                     __float_as_uint(f * __uint_as_float(a[4 * j + 1])),
+                     __float_as_uint(f * __uint_as_float(a[4 * j + 2])),
+                     __float_as_uint(f * __uint_as_float(a[4 * j + 3])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (krow0 < T) {
+              const CUtensorMap* m = acc == 0 ? &dvmap : &dkmap;
+              for (int jj = 0; jj < 2; ++jj)
+                tma_reduce_add_3d(m, (jj == 0 ? sm.p : sm.ds) + (warp >> 2) * kBmHalf + (warp & 3) * 4096,
+                                  (c0 + jj) * 32, g, krow0);
             }
+            bulk_commit();
           }
         }
         tc::fence_before();
@@ -1427,10 +1481,12 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   BmPlan p;
   bm_carve(dims, region, &p);
   const BwCarve w = bw_carve(total_tokens, max_seqlen, topk, region);
-  CUtensorMap qmap, omap, kmap, vmap, dqmap;
+  CUtensorMap qmap, omap, kmap, vmap, dqmap, dkmap, dvmap;
   if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&omap, grad_out, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&dqmap, dq, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode3d_f32(&dkmap, w.dk, kDim, kKvHeads, total_tokens, 32, 1, 32) ||
+      !encode3d_f32(&dvmap, w.dv, kDim, kKvHeads, total_tokens, 32, 1, 32) ||
       !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
       !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
     return cudaErrorInvalidValue;
@@ -1457,8 +1513,8 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   cudaFuncSetAttribute(bw_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
   const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
-  bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, dqmap, p, T, topk, scale,
-                                                       scale * 1.4426950408889634f, lse, w.D, w.dk, w.dv, err);
+  bw_attend_kernel<<<grid, kBwThreads, smem, stream>>>(qmap, omap, kmap, vmap, dqmap, dkmap, dvmap, p, T, topk,
+                                                       scale, scale * 1.4426950408889634f, lse, w.D, err);
   const long long nk8 = T * kKvHeads * kDim / 8;
   bw_to_bf16_kernel<<<static_cast<unsigned>((nk8 + 255) / 256), 256, 0, stream>>>(w.dk, nk8,
                                                                                  static_cast<__nv_bfloat16*>(dk));
