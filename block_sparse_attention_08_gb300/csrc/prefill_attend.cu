@@ -687,9 +687,13 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           tc::ld_32x32b_x32(srow + ch * 32, v);
           tc::wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const float x = __uint_as_float(v[q]);
-            m8[q & 7] = fmaxf(m8[q & 7], (!kMask || ch * 32 + q < nkeys) ? x : -INFINITY);
+          for (int q = 0; q < 16; ++q) {
+            float xa = __uint_as_float(v[2 * q]), xb = __uint_as_float(v[2 * q + 1]);
+            if (kMask) {
+              xa = ch * 32 + 2 * q < nkeys ? xa : -INFINITY;
+              xb = ch * 32 + 2 * q + 1 < nkeys ? xb : -INFINITY;
+            }
+            m8[q & 7] = fmax3(m8[q & 7], xa, xb);
           }
         }
         mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
@@ -699,9 +703,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         const float shift = mu + 7.f;  // p / 128 = 2^(s * scale * log2 e - mu - 7)
         // pass 2: bf16 p / 128 written over the S columns already read (P chunk
         // ch, 16 columns, lands in S chunk ch / 2), fp32 row sum
-        float l8[8];
+        float2 l4[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) l8[q] = 0.f;
+        for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t v[32];
@@ -711,19 +715,19 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int kc = ch * 32 + 2 * q;
-            float xa = fmaf(__uint_as_float(v[2 * q]), scale_log2, -shift);
-            float xb = fmaf(__uint_as_float(v[2 * q + 1]), scale_log2, -shift);
+            float2 x = fma2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), scale_log2, scale_log2, -shift,
+                            -shift);
             if (kMask) {
-              xa = kc < nkeys ? xa : -INFINITY;
-              xb = kc + 1 < nkeys ? xb : -INFINITY;
+              x.x = kc < nkeys ? x.x : -INFINITY;
+              x.y = kc + 1 < nkeys ? x.y : -INFINITY;
             }
-            const float pa = ex2(xa), pb = ex2(xb);
-            l8[q & 7] += pa + pb;
+            const float pa = ex2(x.x), pb = ex2(x.y);
+            l4[q & 3] = add2(l4[q & 3].x, l4[q & 3].y, pa, pb);
             pk[q] = pack_bf16(pa, pb);
           }
           tc::st_32x32b_x16(srow + ch * 16, pk);
         }
-        l = 128.f * (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        l = 128.f * (((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y)));
         mx = mu;
         return true;
       };
