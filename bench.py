@@ -78,9 +78,13 @@ TRAFFIC = {
     # decode_select_kernel<bf16> + scores, first 16 requests: 147.1 MB DRAM / 143.7 MB algorithmic
     "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0237,
                                    "capture": "profiles/decode_b64_ctx4k_64k_paged.md"},
-    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.128 GB DRAM / 462848 entries
-    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8919.0,
+    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.132 GB DRAM / 462848 entries
+    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8927.0,
                          "capture": "profiles/bm_attend_merge_prefill_1doc_8k.md"},
+}
+# bw_attend_kernel, 8192-token document: 0.604 GB DRAM / 462848 entries (scaled by entries)
+TRAFFIC_BACKWARD = {
+    "prefill_1doc_16k": {"per": "entry", "value": 1306.0, "capture": "profiles/bw_attend_prefill_1doc_16k.md"},
 }
 
 
@@ -238,6 +242,8 @@ def run_backward(args, device, config):
     _, f_att = prefill_work(p, q2k)
     flop = 2.5 * f_att
     tf = flop / (ms * 1e-3) / 1e12
+    tr = TRAFFIC_BACKWARD.get(args.workload) if args.scale_down == 1 else None
+    traffic = round(tr["value"] * prefill_entries(q2k)) if tr else None
     config.update({"pass": "attention backward (dq, dk, dv)", "queries_per_step": T,
                    "timing": "eager C-ABI call" if args.no_graph else "CUDA-graph replay of the C-ABI call",
                    "l2": "flushed between steps (256 MiB write, outside the timed events)"})
@@ -247,7 +253,8 @@ def run_backward(args, device, config):
             "config": config,
             "roofline": {"bound": "tensor", "kernel": "msa_sparse_attend_prefill_backward (bucketing, "
                          "bw_rowdot_kernel, bw_attend_kernel, bw_to_bf16_kernel)", "achieved": round(tf, 2),
-                         "peak": tf_peak, "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4), "traffic": None,
+                         "peak": tf_peak, "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4), "traffic": traffic,
+                         "traffic_source": tr["capture"] + " (scaled by entries)" if tr else None,
                          "flop": flop, "peak_source": peak_src + " bf16_tflops (burst)"},
             "gpu_launches": 9 * args.steps, "clocks": clk.summary()}
 

@@ -16,8 +16,8 @@
 // tensor cores see full 128 x 128 x 128 products:
 //
 //   S = Q K^T   (A = gathered Q rows, B = K block; both K-major, 128-byte swizzle)
-//   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 to shared memory)
-//   O = P V     (A = P, B = V read MN-major straight from the TMA tile)
+//   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 back into S's columns)
+//   O = P V     (A = P read from tensor memory, B = V read MN-major from the TMA tile)
 //
 // with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 16
 // schedules the tiles (descriptors and entries read ahead from global memory,
