@@ -56,10 +56,6 @@ static Layout layout(int mode, long long n, int max_blocks, int topk) {
 
 // The completion counters of a call start at zero whatever an earlier call
 // with other sizes left in the same workspace.
-static cudaError_t clear_counters(uint8_t* ws, size_t off, size_t bytes, cudaStream_t s) {
-  return cudaMemsetAsync(ws + off, 0, bytes, s);
-}
-
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 thread_local int g_last_cuda_error = 0;
@@ -215,8 +211,8 @@ static msa_status attend_decode(const msa_config* cfg, const void* q, const void
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (const cudaError_t ce = clear_counters(ws, L.att_tickets, static_cast<size_t>(batch) * kKvHeads * sizeof(int), s); ce != cudaSuccess)
-    return cuda_fail(ce);
+  // the merge tickets start at zero: the workspace was zero-filled once and
+  // every call leaves them at zero (the CTA that completes a segment resets it)
   AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
   cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out, out_q, out_scale,
                                        reinterpret_cast<float*>(ws + L.partials),

@@ -110,11 +110,14 @@ msa_status msa_config_check(const msa_config* cfg);
  *   MSA_MODE_PREFILL_BWD: as MSA_MODE_PREFILL, for msa_sparse_attend_prefill_backward.
  * The workspace must be zero-filled once before its first use (see
  * msa_workspace_init), which clears the device error word in its first 256
- * bytes.  Each call clears its own completion counters (a cudaMemsetAsync on
- * `stream`) and the scorer stores rather than accumulates (NeMo
- * _score_scratch), so one workspace can serve later calls of any size up to
- * the one it was sized for.  Calls that share a workspace must not run
- * concurrently. */
+ * bytes and the completion counters.  Every call that completes leaves its
+ * counters at zero again (the decode calls enqueue no memset; the prefill
+ * calls clear theirs with a cudaMemsetAsync on `stream`), and the scorer
+ * stores rather than accumulates (NeMo _score_scratch), so one workspace can
+ * serve later calls of any size up to the one it was sized for.  After a call
+ * whose device error word reads MSA_DEVERR_TIMEOUT (a pipeline that gave up
+ * part-way), zero-fill the workspace again before reusing it.  Calls that
+ * share a workspace must not run concurrently. */
 msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int max_blocks,
                               size_t* bytes);
 
