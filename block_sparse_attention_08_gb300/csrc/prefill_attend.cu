@@ -828,21 +828,32 @@ __global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict
   const long long t = blockIdx.x;
   const int g = blockIdx.y;
   const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
-  const int d = doc_of(cu, num_docs, t);
-  const int nb = static_cast<int>(t - cu[d]) / kBlock + 1;
   const long long e0 = (static_cast<long long>(g) * T + t) * topk;
-  // all of the token's partials are requested before any is used
+  // All of the token's partials are requested before any is used, and before
+  // the document lookup: every entry owns a partial slot, so a load needs
+  // only its q2k entry; an entry past the token's causal blocks (bad q2k data,
+  // which the attention skipped, leaving its slot unwritten) is dropped after.
   float2 ml[kMaxTopk];
   uint4 u[kMaxTopk];
+  int bj[kMaxTopk];
 #pragma unroll
   for (int j = 0; j < kMaxTopk; ++j) {
-    const int b = j < topk ? q2k[e0 + j] : -1;
+    bj[j] = j < topk ? q2k[e0 + j] : -1;
     ml[j] = make_float2(-INFINITY, 0.f);
     u[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (b >= 0 && b < nb) {
+    if (bj[j] >= 0) {
       const long long slot = e0 + j;
       ml[j] = p.pml[slot * kGroup + h];
       u[j] = __ldcs(reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c));
+    }
+  }
+  const int d = doc_of(cu, num_docs, t);
+  const int nb = static_cast<int>(t - cu[d]) / kBlock + 1;
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    if (bj[j] >= nb) {
+      ml[j] = make_float2(-INFINITY, 0.f);
+      u[j] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   float M = -INFINITY;
