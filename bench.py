@@ -78,8 +78,8 @@ TRAFFIC = {
     # decode_select_kernel<bf16> + scores, first 16 requests: 147.1 MB DRAM / 143.7 MB algorithmic
     "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0237,
                                    "capture": "profiles/decode_b64_ctx4k_64k_paged.md"},
-    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.132 GB DRAM / 462848 entries
-    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8927.0,
+    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.134 GB DRAM / 462848 entries
+    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8931.0,
                          "capture": "profiles/bm_attend_merge_prefill_1doc_8k.md"},
 }
 # bw_attend_kernel, 8192-token document: 0.604 GB DRAM / 462848 entries (scaled by entries)
