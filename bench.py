@@ -7,8 +7,9 @@ msa_select_blocks_decode + msa_sparse_attend_decode over the whole batch.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints one JSON line (rank 0).  The device-timed value uses CUDA events on the
-launching stream around each step; L2 is flushed (a 256 MiB write) between
-steps, outside the timed events.  Under torchrun each rank runs its own
+launching stream around each step, replayed as one CUDA graph of the two calls;
+L2 is flushed (256 MiB written, then 256 MiB read) between steps, outside the
+timed events.  Under torchrun each rank runs its own
 independent batch (weak scaling, no collective on the data path); the time is
 the max over ranks.  ``--impl reference`` times the CPU oracle on this host's
 cores on a bounded sample of the same workload.
@@ -325,11 +326,17 @@ def run_gpu(args, rank, world, device):
     work = decode_work(inp, q2k, args.mxfp8) if decode else prefill_work(inp, q2k)
     entries = 0 if decode else prefill_entries(q2k)
 
-    # The timed steps replay CUDA graphs of the two C-ABI calls (captured once,
-    # same buffers), so host submission cost does not leak into device time.
+    # The timed steps replay a CUDA graph of the step, the two C-ABI calls
+    # (captured once, same buffers, as a serving engine replays its decode or
+    # prefill step), so host submission cost does not leak into device time.
+    # A second pass replays one graph per call, timed call by call, for the
+    # per-kernel figures.
+    def run_step():
+        sel()
+        att()
     run_sel, run_att = sel, att
     if not args.no_graph:
-        g_sel, g_att = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_sel, g_att, g_step = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(device)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
@@ -337,18 +344,28 @@ def run_gpu(args, rank, world, device):
                 sel()
             with torch.cuda.graph(g_att, stream=cap):
                 att()
+            with torch.cuda.graph(g_step, stream=cap):
+                sel()
+                att()
         stream.wait_stream(cap)
-        run_sel, run_att = g_sel.replay, g_att.replay
+        run_sel, run_att, run_step = g_sel.replay, g_att.replay, g_step.replay
         for _ in range(2):
             run_sel()
             run_att()
+            run_step()
         torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(device.index if device.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush_l2(i)
+            evs[i][0].record(stream)
+            run_step()
+            evs[i][1].record(stream)
         for i in range(args.steps):
             flush_l2(i)
             ev[i][0].record(stream)
@@ -361,7 +378,7 @@ def run_gpu(args, rank, world, device):
         torch.distributed.barrier()
     t_sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     t_att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    ms = sum(a + b for a, b in zip(t_sel, t_att)) / args.steps
+    ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)) / args.steps
 
     # end to end through the public API with host buffers (pinned), per step:
     # H2D of the step's inputs, D2H of the output.  Decode: the new queries,
@@ -616,7 +633,9 @@ def main():
                                "step_TFLOP/s": round((f_sel + f_att) / (ms * 1e-3) / 1e12, 2)}}
         dtype = "e4m3-index/bf16" if fp8_index else "bf16"
     config.update({"queries_per_step": res["n_queries"],
-                   "timing": "eager C-ABI calls" if args.no_graph else "CUDA-graph replay of the two C-ABI calls",
+                   "timing": ("eager C-ABI calls" if args.no_graph else
+                              "CUDA-graph replay of the step (the two C-ABI calls in one graph); per-kernel "
+                              "figures from a second pass with one graph per call, timed call by call"),
                    "l2": "flushed between steps (256 MiB write + 256 MiB read, outside the timed events)",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"})
     line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,

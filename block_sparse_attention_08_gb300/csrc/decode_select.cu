@@ -428,6 +428,10 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
                                                           DevError* err) {
   __shared__ unsigned long long cand[kKvHeads][kCandCap];
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the scores are complete: a programmatic dependent (the decode attention)
+  // may now be scheduled and run its prologue; it waits for this grid to end
+  // before it reads q2k
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x, h = threadIdx.x >> 5;
   const int L = geo.seq_lens[r];
   if (threadIdx.x == 0 && (L < 1 || L > geo.max_blocks * kBlock)) record_error(err, MSA_DEVERR_LENGTH, r);

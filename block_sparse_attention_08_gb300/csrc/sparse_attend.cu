@@ -209,16 +209,30 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     }
     fence_mbar_init();
   }
-  __syncthreads();
-  if (lo >= hi) return;
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer warp ----------------
+  if (warp == kConsumerWarps && lo < hi) {
     if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
       prefetch_tmap(&qmap);
     }
+    // the page-table rows of this CTA's requests into L2 (a hint: the rows are
+    // read only after the wait below)
+    if (geo.page_table) {
+      const int q0 = static_cast<int>(lo / (kKvHeads * topk)), q1 = static_cast<int>((hi - 1) / (kKvHeads * topk));
+      for (int qi = q0; qi <= q1; ++qi)
+        for (int o = lane * 32; o < geo.max_blocks; o += 32 * 32)
+          prefetch_l2(geo.page_table + static_cast<long long>(qi) * geo.max_blocks + o);
+    }
+  }
+  // Launched as a programmatic dependent of the previous kernel (the decode
+  // top-k): everything above overlaps it; no input is read and no output
+  // written before that grid has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  if (lo >= hi) return;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp ----------------
     long long sc = 0;
     int nseg = 0;
     long long it = lo;
@@ -577,10 +591,21 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   const size_t smem = sizeof(AttSmem) + 1024;
   cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const float scale_log2 = scale * 1.4426950408889634f;
-  sparse_attend_kernel<<<grid, kAttThreads, smem, stream>>>(kmap, vmap, qmap, q2k, geo, topk, scale_log2,
-                                                            static_cast<__nv_bfloat16*>(out), out_q, out_scale,
-                                                            partials, tickets, err);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel in the stream (the kernel
+  // waits for that grid before touching memory), so its launch and prologue
+  // overlap the decode top-k
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(kAttThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, sparse_attend_kernel, kmap, vmap, qmap, q2k, geo, topk, scale_log2,
+                            static_cast<__nv_bfloat16*>(out), out_q, out_scale, partials, tickets, err);
 }
 
 }  // namespace msa
