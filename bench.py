@@ -76,8 +76,8 @@ def decode_work(d, q2k, mxfp8=False):
 # smaller case of the same workload (profiles/), scaled by the units of a full launch.
 # Set to None when the kernels change after the capture.
 TRAFFIC = {
-    # decode_select_kernel<bf16> + scores, first 16 requests: 147.1 MB DRAM / 143.7 MB algorithmic
-    "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0237,
+    # decode_select_kernel<bf16> + scores, first 16 requests: 147.0 MB DRAM / 143.7 MB algorithmic
+    "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0227,
                                    "capture": "profiles/decode_b64_ctx4k_64k_paged.md"},
     # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.134 GB DRAM / 462848 entries
     "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8931.0,
