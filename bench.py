@@ -569,8 +569,14 @@ def main():
                 vals.append(info["value"])
             v = sum(vals) / len(vals)
             info["value"] = v
+            inp = _CPU_INPUTS[(args.workload, args.seed)]
+            per_step = inp.batch if args.workload.startswith("decode") else inp.total_tokens
+            config["queries_per_step"] = per_step
             line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
-                    "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                    "steps": args.steps, "warmup": args.warmup,
+                    # a whole step of the workload at the sample's rate
+                    "ms_per_step": round(per_step / v * 1e3, 4) if v > 0 else None,
+                    "higher_is_better": True, "scaling": "weak",
                     "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
                     "cpu_baseline": info,
                     "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
