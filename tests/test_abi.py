@@ -169,3 +169,22 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.msa_status_string(s)
     assert lib.msa_status_string(99) == b"unknown status"
+
+
+def test_cuda_error_reporting(lib):
+    # no call of this thread has failed in CUDA; the text is the runtime's
+    # own for a code (a table lookup: no device is touched)
+    assert lib.msa_last_cuda_error() == 0
+    assert lib.msa_cuda_error_string(0) == b"no error"
+    assert lib.msa_cuda_error_string(1) == b"invalid argument"
+    # argument errors are caught before any CUDA call and leave it unchanged
+    assert lib.msa_check_bounded_wait(None, None, None) == NULL
+    assert lib.msa_last_cuda_error() == 0
+
+
+def test_cuda_error_text_in_binding_errors():
+    # the binding appends the CUDA error text to MSA_ERR_CUDA failures
+    from block_sparse_attention_08_gb300 import binding
+    assert binding.MSA_ERR_CUDA == 6
+    e = binding.MsaError("msa_x", 6, "CUDA error: invalid argument (cudaError 1)")
+    assert "invalid argument" in str(e) and e.status == 6
