@@ -295,9 +295,10 @@ msa_status msa_sparse_attend_prefill_lse(const msa_config* cfg, const void* q, c
  *   dq, dk, dv dev bf16, written whole (zero for tokens no query reaches)
  *   workspace  >= msa_workspace_size(cfg, MSA_MODE_PREFILL_BWD, total_tokens,
  *              ceil(max_seqlen / 128)); holds fp32 accumulators for dk, dv
- * dk and dv are summed with fp32 atomics, dq with packed bf16 atomics into
- * the output (as the NeMo page says of its backward), so the gradients are
- * not bitwise reproducible from run to run.
+ * dk and dv are summed in fp32 and dq in bf16 straight into the output (as
+ * the NeMo page says of its backward), by the tensor engine's bulk adds in an
+ * order that varies, so the gradients are not bitwise reproducible from run
+ * to run.
  * Errors: MSA_ERR_NULL, MSA_ERR_SHAPE, MSA_ERR_ALIGN (any tensor not 16-byte
  * aligned), MSA_ERR_WORKSPACE, MSA_ERR_CUDA. */
 msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void* q, const void* k,
