@@ -29,13 +29,15 @@
  * on the fp32 rounding of that sum, because the pages fix FP32 as the score
  * precision ([TRT] indexer_kv_dtype).  Attention is computed in fp64.
  *
- * Readings where the pages are silent (each one is listed in the design notes):
- * forced blocks occupy top-k slots; q2k rows list block ids ascending then -1;
- * equal scores prefer the lower block id; no scale on index scores; the
- * diagonal block takes its max over causal keys only; blocks restart at each
- * document (request) start; query head h uses kv/index head h / (H / G);
- * softmax scale is a caller argument (1/sqrt(128) in the workloads); a decode
- * query sits at position len-1 and sees its own key.
+ * Readings where the pages are silent: forced blocks occupy top-k slots; q2k
+ * rows list block ids ascending then -1; equal scores prefer the lower block
+ * id; no scale on index scores; the diagonal block takes its max over causal
+ * keys only; blocks restart at each document (request) start; a decode query
+ * sits at position len-1 and sees its own key.  Two readings no page fixes,
+ * so parity on them is unpinned beyond the reading itself (parity unpinned):
+ * query head h uses kv/index head h / (H / G) (contiguous GQA groups), and the
+ * softmax scale is a caller argument (1/sqrt(128) in the workloads; no
+ * softcap, no sinks).
  */
 #include <math.h>
 #include <stdint.h>
