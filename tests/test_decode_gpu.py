@@ -39,6 +39,14 @@ def test_decode_small(paged, topk, init, local):
     _run(d, topk, init, local)
 
 
+def test_decode_many_requests():
+    # more (request, KV head) segments than SMs several times over: every CTA
+    # walks many segments and the stream-K cuts land inside short ones
+    lens = np.random.default_rng(71).integers(1, 3000, size=200).tolist()
+    d = msa_synth.decode_inputs(lens, paged=True, seed=71, device="cuda")
+    _run(d, 16, 1, 1)
+
+
 def test_decode_e4m3_small():
     d = msa_synth.decode_inputs(SMALL_LENS, paged=True, index_dtype="e4m3", seed=3, device="cuda")
     _run(d, 16, 0, 1)

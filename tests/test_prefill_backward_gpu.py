@@ -4,9 +4,10 @@ against the fp64 oracle (NeMo _SparseAttention.backward: grad_out -> dq, dk, dv)
 Tolerance, from the arithmetic: the kernel rebuilds P from the forward's fp32
 log-sum-exp, rounds P and dS = P (dP - D) to bf16 for the tensor cores
 (relative 2^-9 each), takes D = <grad_out, out> from the bf16 output, sums
-in fp32 and rounds the gradients to bf16 (2^-9).  The bounds: one element's
-error within 1 % of the tensor's largest magnitude and the mean error within
-0.5 % of its mean magnitude (measured: at most 0.5 % and 0.25 %)."""
+dk and dv in fp32 and dq in bf16 (as the NeMo page does), and rounds the
+gradients to bf16 (2^-9).  The bounds: one element's error within 1 % of the
+tensor's largest magnitude and the mean error within 0.5 % of its mean
+magnitude (measured: at most 0.43 % and 0.26 %)."""
 import numpy as np
 import pytest
 import torch
@@ -50,6 +51,13 @@ def _run(docs, topk, init, local, seed):
 @pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (3, 1, 1), (1, 0, 1)])
 def test_prefill_backward_small(topk, init, local):
     _run([1, 127, 128, 129, 300, 700], topk, init, local, seed=31 + topk)
+
+
+def test_prefill_backward_long_runs():
+    # documents spanning several 256-token windows: a key block is reached by
+    # several runs of about 32 tiles each, so the Q / dO ring cycles many
+    # times and dK / dV of one block are summed across runs
+    _run([1536, 700], 16, 1, 1, 61)
 
 
 def test_prefill_backward_one_short_document():
