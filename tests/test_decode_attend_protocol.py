@@ -1,0 +1,177 @@
+"""Host model of the decode attention's synchronisation (sparse_attend_kernel).
+
+The producer warp and the consumer warps are generators that wait on and
+arrive at mbarriers with the kernel's counts and wait parities: a 2-slot
+segment ring (key counts and the Q tile of a (request, KV head) segment) and a
+6-stage ring of 64-key chunks, stage s always taken by consumer warp s mod 3;
+the consumers meet at the end of every segment (the kernel's named barrier)
+to merge their states.  TMA copies land in any order at random moments.
+Random segment lists (blocks of 1..128 keys, empty entries) are run under
+random schedules, and every run must finish, never poll a barrier two phases
+away from the phase it waits for, never copy into a slot or stage that is
+still being read, and read in every use the segment or chunk it expects.
+
+A warp that took chunks round-robin (chunk c to warp c mod C) with a stage
+count that is not a multiple of C could wait on a stage two phases ahead and
+read a stale chunk; the last test plants that assignment and checks that the
+model reports it.  No GPU is involved.
+"""
+import random
+
+import pytest
+
+SEG_SLOTS, CHUNK_KEYS = 2, 64
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.done = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, self.name
+        if self.pending == 0:
+            self.done += 1
+            self.pending = self.count
+
+
+class Sim:
+    def __init__(self, segments, rng, stages=6, consumers=3, by_chunk=False):
+        # segments: list of lists of key counts (0 = an empty / padded entry)
+        self.segs, self.rng = segments, rng
+        self.S, self.C, self.by_chunk = stages, consumers, by_chunk
+        self.bars = {}
+        for i in range(SEG_SLOTS):
+            self.bars[f"seg_full{i}"] = Bar(f"seg_full{i}", 1)
+            self.bars[f"seg_empty{i}"] = Bar(f"seg_empty{i}", consumers)
+        for s in range(stages):
+            self.bars[f"full{s}"] = Bar(f"full{s}", 1)
+            self.bars[f"empty{s}"] = Bar(f"empty{s}", 1)
+        self.tag, self.reading, self.landing = {}, {}, set()
+        self.loads = []
+        self.meet = [0, 0]  # segment-end rendezvous: arrivals, generation
+
+    def wait(self, name, parity, need):
+        bar = self.bars[name]
+
+        def ok():
+            c = bar.done
+            assert need - 1 <= c <= need, f"{name}: {c} phases done, waiting for phase {need - 1}"
+            return (c & 1) != parity
+        return ok
+
+    def load(self, buf, tag, name):
+        assert not self.reading.get(buf), f"copy into {buf} while it is read"
+        assert buf not in self.landing, f"two copies into {buf}"
+        self.landing.add(buf)
+        self.loads.append((buf, tag, name))
+
+    def read(self, buf, tag):
+        assert buf not in self.landing, f"read of {buf} while a copy lands"
+        assert self.tag.get(buf) == tag, f"{buf} holds {self.tag.get(buf)}, expected {tag}"
+
+    def owner(self, sc):
+        return (sc % self.C) if self.by_chunk else (sc % self.S) % self.C
+
+    def chunks(self, keys):
+        return [(k + CHUNK_KEYS - 1) // CHUNK_KEYS for k in keys]
+
+    def producer(self):
+        sc = 0
+        for nseg, keys in enumerate(self.segs):
+            ss = nseg % SEG_SLOTS
+            yield self.wait(f"seg_empty{ss}", ((nseg // SEG_SLOTS) & 1) ^ 1, nseg // SEG_SLOTS)
+            self.load(f"seg{ss}", ("seg", nseg), f"seg_full{ss}")
+            for nch in self.chunks(keys):
+                for _ in range(nch):
+                    s = sc % self.S
+                    yield self.wait(f"empty{s}", ((sc // self.S) & 1) ^ 1, sc // self.S)
+                    self.load(f"stage{s}", ("chunk", sc), f"full{s}")
+                    sc += 1
+
+    def consumer(self, w):
+        sc = 0
+        for nseg, keys in enumerate(self.segs):
+            ss = nseg % SEG_SLOTS
+            yield self.wait(f"seg_full{ss}", (nseg // SEG_SLOTS) & 1, nseg // SEG_SLOTS + 1)
+            self.read(f"seg{ss}", ("seg", nseg))
+            self.reading[f"seg{ss}"] = self.reading.get(f"seg{ss}", 0) + 1
+            yield None  # the Q fragments are loaded
+            self.reading[f"seg{ss}"] -= 1
+            self.bars[f"seg_empty{ss}"].arrive()
+            for nch in self.chunks(keys):
+                for _ in range(nch):
+                    if self.owner(sc) == w:
+                        s = sc % self.S
+                        yield self.wait(f"full{s}", (sc // self.S) & 1, sc // self.S + 1)
+                        self.read(f"stage{s}", ("chunk", sc))
+                        self.reading[f"stage{s}"] = self.reading.get(f"stage{s}", 0) + 1
+                        yield None  # S, softmax, O on the chunk
+                        self.reading[f"stage{s}"] -= 1
+                        self.bars[f"empty{s}"].arrive()
+                    sc += 1
+            # the consumers meet twice at the end of the segment (merge through
+            # shared memory); warp 0 then writes while the others go on
+            for _ in range(2):
+                gen = self.meet[1]
+                self.meet[0] += 1
+                if self.meet[0] == self.C:
+                    self.meet = [0, gen + 1]
+                yield lambda gen=gen: self.meet[1] != gen
+
+    def run(self):
+        roles = [self.producer()] + [self.consumer(w) for w in range(self.C)]
+        blocked = [None] * len(roles)
+        live = set(range(len(roles)))
+        steps = 0
+        while live or self.loads:
+            steps += 1
+            assert steps < 500000, "no progress"
+            ready = [r for r in live if blocked[r] is None or blocked[r]()]
+            moves = [("role", r) for r in ready] + [("land", k) for k in range(len(self.loads))]
+            assert moves, "deadlock"
+            kind, x = self.rng.choice(moves)
+            if kind == "land":
+                buf, tag, name = self.loads.pop(x)
+                self.landing.discard(buf)
+                self.tag[buf] = tag
+                self.bars[name].arrive()
+                continue
+            try:
+                blocked[x] = next(roles[x])
+            except StopIteration:
+                live.discard(x)
+                blocked[x] = None
+
+
+def segment_list(rng, n):
+    segs = []
+    for _ in range(n):
+        segs.append([rng.choice([0, 1, 37, 64, 65, 100, 128, 128, 128]) for _ in range(rng.randint(1, 16))])
+    return segs
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_decode_attend_protocol_random_schedules(seed):
+    rng = random.Random(seed)
+    Sim(segment_list(rng, rng.randint(1, 6)), rng).run()
+
+
+def test_decode_attend_protocol_twelve_stages():
+    # the stage count only has to be a multiple of the consumer warps
+    for seed in range(5):
+        rng = random.Random(100 + seed)
+        Sim(segment_list(rng, 4), rng, stages=12).run()
+
+
+def test_model_catches_round_robin_chunks():
+    # chunks handed out round-robin over 4 warps through 6 stages: a warp can
+    # wait on a stage two phases ahead; the model must report it
+    failed = 0
+    for seed in range(30):
+        rng = random.Random(seed)
+        try:
+            Sim(segment_list(rng, 4), rng, stages=6, consumers=4, by_chunk=True).run()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
