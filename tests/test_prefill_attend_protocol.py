@@ -1,0 +1,303 @@
+"""Host model of the prefill attention's synchronisation (bm_attend_kernel).
+
+Roles as in the kernel: the scheduler / TMA warp (K of a new block, the
+tile's Q rows, V of a new block), the S-MMA thread, the O-MMA thread, two
+softmax warpgroups and two epilogue warpgroups taking the even and the odd
+tiles (four warps each; the epilogue's first thread also issues the tile's
+TMA stores).  Tensor memory holds S (then P over it) and O twice; shared
+memory holds Q twice, K twice, V once and one fp16 staging tile per epilogue
+warpgroup.  The TMA copies land in any order, each MMA thread's groups and
+commits execute in that thread's issue order (no order is assumed between
+the two threads: what one reads the other writes only behind a barrier), and the
+stores read their staging at random moments.  Random tile sequences (runs of
+tiles over one key block) under random schedules must finish, never poll a
+barrier two phases away from the phase they wait for, never write anything
+under a pending access, and read in every use the content it expects.  A
+planted mistake (the O MMA not waiting for the epilogue to free its O
+buffer) must be reported.  No GPU is involved.
+"""
+import random
+
+import pytest
+
+INFO, QST, KST, VST = 8, 2, 2, 1
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.done = name, count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, self.name
+        if self.pending == 0:
+            self.done += 1
+            self.pending = self.count
+
+
+class Sim:
+    def __init__(self, tiles, rng, skip_o_free=False):
+        self.tiles, self.rng, self.skip_o_free = tiles, rng, skip_o_free  # tiles: list of block ids
+        self.bars = {}
+
+        def bar(name, count=1):
+            self.bars[name] = Bar(name, count)
+        for i in range(QST):
+            bar(f"q_full{i}")
+            bar(f"q_empty{i}")
+        for i in range(KST):
+            bar(f"k_full{i}")
+            bar(f"k_empty{i}")
+        for i in range(VST):
+            bar(f"v_full{i}")
+            bar(f"v_empty{i}")
+        for b in range(2):
+            bar(f"s_full{b}")
+            bar(f"s_free{b}")
+            bar(f"o_full{b}")
+            bar(f"o_free{b}", 4)
+            bar(f"p_full{b}", 4)
+            bar(f"stage_free{b}")
+            bar(f"stage_full{b}", 4)
+        for i in range(INFO):
+            bar(f"info_full{i}")
+            bar(f"info_empty{i}", 10)
+        self.tag, self.pend_r, self.pend_w, self.warp_r = {}, {}, {}, {}
+        self.pipe = {"S": [], "O": []}  # per MMA thread, in issue order
+        self.loads = []
+        self.stores = {0: [], 1: []}  # per epilogue warpgroup: staging reads of its stores
+
+    def wait(self, name, parity, need):
+        bar = self.bars[name]
+
+        def ok():
+            c = bar.done
+            assert need - 1 <= c <= need, f"{name}: {c} phases done, waiting for phase {need - 1}"
+            return (c & 1) != parity
+        return ok
+
+    def _add(self, d, k, v):
+        d[k] = d.get(k, 0) + v
+        assert d[k] >= 0
+
+    # accesses -------------------------------------------------------------
+    def warp_read(self, buf, tag):
+        assert not self.pend_w.get(buf), f"read of {buf} under a pending write"
+        assert self.tag.get(buf) == tag, f"{buf} holds {self.tag.get(buf)}, expected {tag}"
+        self._add(self.warp_r, buf, 1)
+
+    def warp_read_end(self, buf):
+        self._add(self.warp_r, buf, -1)
+
+    def warp_write(self, buf, tag):
+        assert not self.pend_r.get(buf) and not self.pend_w.get(buf), f"write of {buf} under a pending access"
+        self.tag[buf] = tag
+
+    def mma(self, pipe, reads, writes):
+        for w, _ in writes:
+            assert not self.warp_r.get(w), f"MMA writes {w} while a warp reads it"
+            assert not self.pend_r.get(w), f"MMA writes {w} while an earlier MMA may still read it"
+        for r, tag in reads:
+            assert not self.pend_w.get(r), f"MMA reads {r} while it is being written"
+            assert self.tag.get(r) == tag, f"MMA reads {r} holding {self.tag.get(r)}, expected {tag}"
+            self._add(self.pend_r, r, 1)
+        for w, _ in writes:
+            self._add(self.pend_w, w, 1)
+        self.pipe[pipe].append(("mma", [r for r, _ in reads], writes))
+
+    def commit(self, pipe, name):
+        self.pipe[pipe].append(("commit", name))
+
+    def load(self, buf, tag, name):
+        assert not self.pend_r.get(buf) and not self.pend_w.get(buf), f"copy into {buf} under a pending access"
+        self._add(self.pend_w, buf, 1)
+        self.loads.append((buf, tag, name))
+
+    # roles ------------------------------------------------------------------
+    def fresh(self, i):
+        return i == 0 or self.tiles[i] != self.tiles[i - 1]
+
+    def producer(self):
+        nkf = nvf = 0
+        for i, blk in enumerate(self.tiles):
+            s, u = i % INFO, i // INFO
+            yield self.wait(f"info_empty{s}", (u & 1) ^ 1, u)
+            self.bars[f"info_full{s}"].arrive()
+            if self.fresh(i):
+                ks = nkf % KST
+                yield self.wait(f"k_empty{ks}", ((nkf // KST) & 1) ^ 1, nkf // KST)
+                self.load(f"K{ks}", ("K", i), f"k_full{ks}")
+                nkf += 1
+            qs = i % QST
+            yield self.wait(f"q_empty{qs}", ((i // QST) & 1) ^ 1, i // QST)
+            self.load(f"Q{qs}", ("Q", i), f"q_full{qs}")
+            if self.fresh(i):
+                vs = nvf % VST
+                yield self.wait(f"v_empty{vs}", ((nvf // VST) & 1) ^ 1, nvf // VST)
+                self.load(f"V{vs}", ("V", i), f"v_full{vs}")
+                nvf += 1
+
+    def s_mma(self):
+        nk = ks = 0
+        first = 0  # first tile of the current block (its K / V carry that tile's tag)
+        for i in range(len(self.tiles)):
+            s, u = i % INFO, i // INFO
+            yield self.wait(f"info_full{s}", u & 1, u + 1)
+            self.bars[f"info_empty{s}"].arrive()
+            if self.fresh(i):
+                if nk > 0:
+                    self.commit("S", f"k_empty{ks}")
+                ks = nk % KST
+                yield self.wait(f"k_full{ks}", (nk // KST) & 1, nk // KST + 1)
+                nk += 1
+                first = i
+            b, qs = i & 1, i % QST
+            yield self.wait(f"q_full{qs}", (i // QST) & 1, i // QST + 1)
+            yield self.wait(f"s_free{b}", ((i >> 1) & 1) ^ 1, i >> 1)
+            self.mma("S", [(f"Q{qs}", ("Q", i)), (f"K{ks}", ("K", first))],
+                     [(f"S{b}_{q}", ("S", i)) for q in range(4)])
+            self.commit("S", f"s_full{b}")
+            self.commit("S", f"q_empty{qs}")
+
+    def o_mma(self):
+        nv = vs = 0
+        first = 0
+        for i in range(len(self.tiles)):
+            s, u = i % INFO, i // INFO
+            yield self.wait(f"info_full{s}", u & 1, u + 1)
+            self.bars[f"info_empty{s}"].arrive()
+            if self.fresh(i):
+                if nv > 0:
+                    self.commit("O", f"v_empty{vs}")
+                vs = nv % VST
+                yield self.wait(f"v_full{vs}", (nv // VST) & 1, nv // VST + 1)
+                nv += 1
+                first = i
+            b = i & 1
+            yield self.wait(f"p_full{b}", (i >> 1) & 1, (i >> 1) + 1)
+            if not self.skip_o_free:
+                yield self.wait(f"o_free{b}", ((i >> 1) & 1) ^ 1, i >> 1)
+            self.mma("O", [(f"S{b}_{q}", ("P", i)) for q in range(4)] + [(f"V{vs}", ("V", first))],
+                     [(f"O{b}_{q}", ("O", i)) for q in range(4)])
+            self.commit("O", f"o_full{b}")
+            self.commit("O", f"s_free{b}")
+
+    def softmax(self, wg, q):
+        for i in range(wg, len(self.tiles), 2):
+            s, u, k = i % INFO, i // INFO, i >> 1
+            yield self.wait(f"info_full{s}", u & 1, u + 1)
+            self.bars[f"info_empty{s}"].arrive()
+            yield self.wait(f"s_full{wg}", k & 1, k + 1)
+            buf = f"S{wg}_{q}"
+            self.warp_read(buf, ("S", i))
+            yield None  # two passes over the row
+            self.warp_read_end(buf)
+            self.warp_write(buf, ("P", i))  # P over the S columns this warp read
+            self.bars[f"p_full{wg}"].arrive()
+
+    def epilogue(self, wg, q):
+        issuer = q == 0
+        for i in range(wg, len(self.tiles), 2):
+            s, u, k = i % INFO, i // INFO, i >> 1
+            yield self.wait(f"info_full{s}", u & 1, u + 1)
+            self.bars[f"info_empty{s}"].arrive()
+            yield self.wait(f"o_full{wg}", k & 1, k + 1)
+            if issuer:
+                yield lambda: not self.stores[wg]  # the previous tile's stores have read the staging
+                self.bars[f"stage_free{wg}"].arrive()
+            yield self.wait(f"stage_free{wg}", k & 1, k + 1)
+            self.warp_read(f"O{wg}_{q}", ("O", i))
+            yield None
+            self.warp_write(f"stage{wg}_{q}", ("stage", i))
+            self.warp_read_end(f"O{wg}_{q}")
+            self.bars[f"o_free{wg}"].arrive()
+            self.bars[f"stage_full{wg}"].arrive()
+            if issuer:
+                yield self.wait(f"stage_full{wg}", k & 1, k + 1)
+                bufs = [f"stage{wg}_{x}" for x in range(4)]
+                for b in bufs:
+                    assert self.tag.get(b) == ("stage", i), f"store of {b} holding {self.tag.get(b)}"
+                    self._add(self.pend_r, b, 1)
+                self.stores[wg].append(bufs)
+
+    # engines ----------------------------------------------------------------
+    def engines(self):
+        out = [lambda p=p: self.step_pipe(p) for p in ("S", "O") if self.pipe[p]]
+        out += [lambda k=k: self.land(k) for k in range(len(self.loads))]
+        out += [lambda w=w: self.store_read(w) for w in (0, 1) if self.stores[w]]
+        return out
+
+    def step_pipe(self, pipe):
+        op = self.pipe[pipe].pop(0)
+        if op[0] == "mma":
+            for r in op[1]:
+                self._add(self.pend_r, r, -1)
+            for w, tag in op[2]:
+                self._add(self.pend_w, w, -1)
+                self.tag[w] = tag
+        else:
+            self.bars[op[1]].arrive()
+
+    def land(self, k):
+        buf, tag, name = self.loads.pop(k)
+        self._add(self.pend_w, buf, -1)
+        self.tag[buf] = tag
+        self.bars[name].arrive()
+
+    def store_read(self, wg):
+        for b in self.stores[wg].pop(0):
+            self._add(self.pend_r, b, -1)
+
+    def run(self):
+        roles = [self.producer(), self.s_mma(), self.o_mma()]
+        roles += [self.softmax(wg, q) for wg in (0, 1) for q in range(4)]
+        roles += [self.epilogue(wg, q) for wg in (0, 1) for q in range(4)]
+        blocked = [None] * len(roles)
+        live = set(range(len(roles)))
+        steps = 0
+        while live or any(self.pipe.values()) or self.loads or any(self.stores.values()):
+            steps += 1
+            assert steps < 500000, "no progress"
+            ready = [r for r in live if blocked[r] is None or blocked[r]()]
+            moves = [("role", r) for r in ready] + [("engine", e) for e in self.engines()]
+            assert moves, "deadlock"
+            kind, x = self.rng.choice(moves)
+            if kind == "engine":
+                x()
+                continue
+            try:
+                blocked[x] = next(roles[x])
+            except StopIteration:
+                live.discard(x)
+                blocked[x] = None
+
+
+def tile_sequence(rng, n_blocks):
+    tiles = []
+    for blk in range(n_blocks):
+        tiles += [blk] * rng.randint(1, 5)
+    return tiles
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_prefill_attend_protocol_random_schedules(seed):
+    rng = random.Random(seed)
+    Sim(tile_sequence(rng, rng.randint(1, 8)), rng).run()
+
+
+def test_prefill_attend_protocol_single_tiles():
+    # every tile a new block: K, V and the info ring turn over on every tile
+    for seed in range(5):
+        rng = random.Random(50 + seed)
+        Sim(list(range(20)), rng).run()
+
+
+def test_model_catches_a_missing_o_free_wait():
+    failed = 0
+    for seed in range(30):
+        rng = random.Random(seed)
+        try:
+            Sim(tile_sequence(rng, 5), rng, skip_o_free=True).run()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
