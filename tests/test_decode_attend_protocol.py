@@ -13,8 +13,11 @@ still being read, and read in every use the segment or chunk it expects.
 
 A warp that took chunks round-robin (chunk c to warp c mod C) with a stage
 count that is not a multiple of C could wait on a stage two phases ahead and
-read a stale chunk; the last test plants that assignment and checks that the
-model reports it.  No GPU is involved.
+read a stale chunk; a test plants that assignment and checks that the model
+reports it.  Without the segment ring the same model is the decode scorer's
+page ring (decode_select_kernel: page i to warp i mod 6 through 6 or 12
+stages), checked as it is and in the eight-warp form that once faulted.  No
+GPU is involved.
 """
 import random
 
@@ -36,10 +39,12 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, segments, rng, stages=6, consumers=3, by_chunk=False):
-        # segments: list of lists of key counts (0 = an empty / padded entry)
+    def __init__(self, segments, rng, stages=6, consumers=3, by_chunk=False, segment_ring=True):
+        # segments: list of lists of key counts (0 = an empty / padded entry).
+        # Without the segment ring (and its end-of-segment meetings) this is the
+        # decode scorer's page ring: one stage per item, item i to a warp.
         self.segs, self.rng = segments, rng
-        self.S, self.C, self.by_chunk = stages, consumers, by_chunk
+        self.S, self.C, self.by_chunk, self.seg_ring = stages, consumers, by_chunk, segment_ring
         self.bars = {}
         for i in range(SEG_SLOTS):
             self.bars[f"seg_full{i}"] = Bar(f"seg_full{i}", 1)
@@ -80,8 +85,9 @@ class Sim:
         sc = 0
         for nseg, keys in enumerate(self.segs):
             ss = nseg % SEG_SLOTS
-            yield self.wait(f"seg_empty{ss}", ((nseg // SEG_SLOTS) & 1) ^ 1, nseg // SEG_SLOTS)
-            self.load(f"seg{ss}", ("seg", nseg), f"seg_full{ss}")
+            if self.seg_ring:
+                yield self.wait(f"seg_empty{ss}", ((nseg // SEG_SLOTS) & 1) ^ 1, nseg // SEG_SLOTS)
+                self.load(f"seg{ss}", ("seg", nseg), f"seg_full{ss}")
             for nch in self.chunks(keys):
                 for _ in range(nch):
                     s = sc % self.S
@@ -93,12 +99,13 @@ class Sim:
         sc = 0
         for nseg, keys in enumerate(self.segs):
             ss = nseg % SEG_SLOTS
-            yield self.wait(f"seg_full{ss}", (nseg // SEG_SLOTS) & 1, nseg // SEG_SLOTS + 1)
-            self.read(f"seg{ss}", ("seg", nseg))
-            self.reading[f"seg{ss}"] = self.reading.get(f"seg{ss}", 0) + 1
-            yield None  # the Q fragments are loaded
-            self.reading[f"seg{ss}"] -= 1
-            self.bars[f"seg_empty{ss}"].arrive()
+            if self.seg_ring:
+                yield self.wait(f"seg_full{ss}", (nseg // SEG_SLOTS) & 1, nseg // SEG_SLOTS + 1)
+                self.read(f"seg{ss}", ("seg", nseg))
+                self.reading[f"seg{ss}"] = self.reading.get(f"seg{ss}", 0) + 1
+                yield None  # the Q fragments are loaded
+                self.reading[f"seg{ss}"] -= 1
+                self.bars[f"seg_empty{ss}"].arrive()
             for nch in self.chunks(keys):
                 for _ in range(nch):
                     if self.owner(sc) == w:
@@ -112,7 +119,7 @@ class Sim:
                     sc += 1
             # the consumers meet twice at the end of the segment (merge through
             # shared memory); warp 0 then writes while the others go on
-            for _ in range(2):
+            for _ in range(2 if self.seg_ring else 0):
                 gen = self.meet[1]
                 self.meet[0] += 1
                 if self.meet[0] == self.C:
@@ -172,6 +179,29 @@ def test_model_catches_round_robin_chunks():
         rng = random.Random(seed)
         try:
             Sim(segment_list(rng, 4), rng, stages=6, consumers=4, by_chunk=True).run()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
+
+
+@pytest.mark.parametrize("stages", [6, 12])
+def test_decode_scorer_page_ring(stages):
+    # the decode scorer: item (page) i to warp i mod 6 through 6 (bf16) or 12
+    # (E4M3) stages -- round-robin, safe because the stage count is a multiple
+    # of the warps
+    for seed in range(10):
+        rng = random.Random(200 + seed)
+        Sim(segment_list(rng, 4), rng, stages=stages, consumers=6, by_chunk=True, segment_ring=False).run()
+
+
+def test_model_reports_the_eight_warp_scorer_ring():
+    # the scorer's first form: eight warps round-robin over six stages (the
+    # Xid 31 recorded for it); the model must report a parity aliasing
+    failed = 0
+    for seed in range(30):
+        rng = random.Random(seed)
+        try:
+            Sim(segment_list(rng, 4), rng, stages=6, consumers=8, by_chunk=True, segment_ring=False).run()
         except AssertionError:
             failed += 1
     assert failed > 0
