@@ -27,14 +27,12 @@ static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 // Workspace layout, shared by msa_workspace_size and the calls.  Completion
 // counters come first, right after the error-word header.
 struct Layout {
-  size_t scores = 0, sel_tickets = 0, att_tickets = 0, partials = 0, plan = 0, bm = 0, total = 0;
+  size_t scores = 0, att_tickets = 0, partials = 0, plan = 0, bm = 0, total = 0;
 };
 static Layout layout(int mode, long long n, int max_blocks, int topk) {
   Layout L;
   size_t off = kHeaderBytes;
   if (mode == MSA_MODE_DECODE) {
-    L.sel_tickets = off;
-    off += up256(static_cast<size_t>(n) * sizeof(int));
     L.att_tickets = off;
     off += up256(static_cast<size_t>(n) * kKvHeads * sizeof(int));
     L.scores = off;
@@ -54,8 +52,6 @@ static Layout layout(int mode, long long n, int max_blocks, int topk) {
   return L;
 }
 
-// The completion counters of a call start at zero whatever an earlier call
-// with other sizes left in the same workspace.
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 thread_local int g_last_cuda_error = 0;
@@ -191,7 +187,7 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch,
                                        max_blocks, num_slots, q2k, reinterpret_cast<float*>(ws + L.scores),
-                                       reinterpret_cast<int*>(ws + L.sel_tickets), reinterpret_cast<DevError*>(ws), s);
+                                       reinterpret_cast<DevError*>(ws), s);
   return cuda_result(e);
 }
 

@@ -198,8 +198,7 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
 template <int kE4M3>
 __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     const uint8_t* __restrict__ index_q, const uint8_t* __restrict__ index_k, DecodeGeom geo,
-    float* __restrict__ scores, int* __restrict__ tickets, int32_t* __restrict__ q2k, int topk,
-    int init, int local, DevError* err) {
+    float* __restrict__ scores, int topk, DevError* err) {
   constexpr int kRowBytes = kE4M3 ? kIdxDim : kIdxDim * 2;
   constexpr int kPageBytes = kBlock * kRowBytes;
   constexpr int kStages = kSelRingBytes / kPageBytes;
@@ -444,7 +443,7 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
-                                 int* tickets, DevError* err, cudaStream_t stream) {
+                                 DevError* err, cudaStream_t stream) {
   if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   DecodeGeom geo{seq_lens, page_table, cu_k, batch, max_blocks, num_slots};
   // one CTA per SM; never more CTAs than pages
@@ -457,14 +456,12 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
     auto k = decode_select_kernel<1>;
     const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, tickets, q2k, cfg.topk, cfg.init_blocks,
-                                           cfg.local_blocks, err);
+    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, err);
   } else {
     auto k = decode_select_kernel<0>;
     const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim * 2)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, tickets, q2k, cfg.topk, cfg.init_blocks,
-                                           cfg.local_blocks, err);
+    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, err);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -521,7 +518,6 @@ static void* noalloc_scratch(cudaError_t* err) {
   return g_noalloc_ptr[dev];
 }
 
-static size_t noalloc_up256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace msa
 
@@ -538,18 +534,17 @@ extern "C" msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, co
   if (page_table && num_slots % kBlock) return MSA_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(index_q) & 15) || (reinterpret_cast<uintptr_t>(index_k_cache) & 15))
     return MSA_ERR_ALIGN;
-  const size_t off_tickets = kHeaderBytes;
-  const size_t off_scores = off_tickets + noalloc_up256(static_cast<size_t>(batch) * sizeof(int));
+  const size_t off_scores = kHeaderBytes;
   const size_t need = off_scores + static_cast<size_t>(batch) * kKvHeads * max_blocks * sizeof(float);
   if (need > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // sizes beyond the fixed scratch
   cudaError_t e;
   auto* base = static_cast<uint8_t*>(noalloc_scratch(&e));
   if (!base) return cuda_fail(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the error word and the counters must start at zero; the scores are stored before they are read
+  // the error word must start at zero; the scores are stored before they are read
   if (const cudaError_t ce = cudaMemsetAsync(base, 0, off_scores, s); ce != cudaSuccess) return cuda_fail(ce);
   e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
                            num_slots, q2k, reinterpret_cast<float*>(base + off_scores),
-                           reinterpret_cast<int*>(base + off_tickets), reinterpret_cast<DevError*>(base), s);
+                           reinterpret_cast<DevError*>(base), s);
   return cuda_result(e);
 }

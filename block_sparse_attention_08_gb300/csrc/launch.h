@@ -23,7 +23,7 @@ struct AttnGeom {
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
-                                 int* tickets, DevError* err, cudaStream_t stream);
+                                 DevError* err, cudaStream_t stream);
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,

@@ -187,7 +187,7 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q,
  * deployment convenience of this library.
  *   - Scratch is one fixed 4 MiB array in the library's device memory, held by
  *     every GPU that loads the library until the process exits.  It must hold
- *     256 + round_up(4*batch, 256) + 16*batch*max_blocks bytes; larger sizes
+ *     256 + 16*batch*max_blocks bytes; larger sizes
  *     are rejected with MSA_ERR_WORKSPACE before any work is enqueued.
  *   - The first call on each device looks up the array's device address on
  *     the current device; make that first call before any stream capture.
