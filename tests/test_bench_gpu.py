@@ -1,0 +1,41 @@
+"""The bench line's contract on the GPU: one short run of the small decode
+workload through bench.py, its JSON line checked key by key."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def check_line(line, steps):
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["steps"] == steps and line["warmup"] >= 3 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["ms_per_step"] > 0 and line["higher_is_better"] is True
+    assert "workload" in line["config"]
+    roof = line["roofline"]
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in roof, key
+    assert roof["bound"] in ("hbm", "tensor") and 0 < roof["frac"] < 1.5
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert e2e["value"] <= line["value"] * 1.05  # the copies only add time
+    assert line["gpu_launches"] > 0
+    assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+
+
+def test_bench_line_contract():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "decode_b4_ctx8k_contig", "--steps", "3",
+           "--warmup", "3", "--no-cpu-baseline"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    check_line(json.loads(lines[0]), 3)
