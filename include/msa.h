@@ -211,6 +211,10 @@ msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, const void* i
  *   k_cache  dev [num_slots, 4, 128] bf16;  v_cache: same
  *   q2k      dev int32 [4, batch, topk]
  *   out      dev [batch, 64, 128] bf16
+ * The kernel is launched as a programmatic dependent of the kernel before it
+ * on `stream` (after msa_select_blocks_decode, its launch overlaps the
+ * top-k); it touches no memory before that kernel has completed, so stream
+ * order is kept whatever precedes it.
  */
 msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* q2k,
