@@ -73,20 +73,27 @@ def decode_work(d, q2k, mxfp8=False):
 
 
 # DRAM traffic of the dominant kernel(s) per unit of work, from one ncu capture of a
-# smaller case of the same workload (profiles/), scaled by the units of a full launch.
-# Set to None when the kernels change after the capture.
+# smaller case of the same workload, scaled by the units of a full launch.  Set to
+# None when the kernels change after the capture.
 TRAFFIC = {
     # decode_select_kernel<bf16> + scores, first 16 requests: 147.0 MB DRAM / 143.7 MB algorithmic
     "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0227,
-                                   "capture": "profiles/decode_b64_ctx4k_64k_paged.md"},
+                                   "capture": "ncu: decode_select_kernel<0>, first 16 requests of "
+                                              "decode_b64_ctx4k_64k_paged"},
     # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.134 GB DRAM / 462848 entries
     "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8931.0,
-                         "capture": "profiles/bm_attend_merge_prefill_1doc_8k.md"},
+                         "capture": "ncu: bm_attend_kernel + bm_merge_kernel, prefill_1doc_16k at half size"},
 }
 # bw_attend_kernel, 8192-token document: 0.604 GB DRAM / 462848 entries (scaled by entries)
 TRAFFIC_BACKWARD = {
-    "prefill_1doc_16k": {"per": "entry", "value": 1306.0, "capture": "profiles/bw_attend_prefill_1doc_16k.md"},
+    "prefill_1doc_16k": {"per": "entry", "value": 1306.0,
+                         "capture": "ncu: bw_attend_kernel, prefill_1doc_16k at half size"},
 }
+
+# The other headline workloads, measured in the same run after the bench workload
+# and reported in the line's "workloads" object (one GPU only).
+EXTRA_WORKLOADS = ["decode_b4_ctx8k_contig", "prefill_1doc_16k", "prefill_packed_2x32k",
+                   "decode_b16_ctx128k_paged_e4m3"]
 
 
 def prefill_entries(q2k):
@@ -260,10 +267,11 @@ def run_backward(args, device, config):
             "gpu_launches": 9 * args.steps, "clocks": clk.summary()}
 
 
-def run_gpu(args, rank, world, device):
+def run_gpu(args, rank, world, device, name=None, steps=None):
     import block_sparse_attention_08_gb300 as msa
     torch.cuda.set_device(device)
-    name = args.workload
+    name = name or args.workload
+    steps = steps or args.steps
     inp = msa_synth.workload(name, seed=args.seed + rank, device=device, max_requests=args.requests,
                             scale_down=args.scale_down)
     decode = name.startswith("decode")
@@ -355,18 +363,18 @@ def run_gpu(args, rank, world, device):
             run_step()
         torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(device.index if device.index is not None else 0) as clk:
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2(i)
             evs[i][0].record(stream)
             run_step()
             evs[i][1].record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2(i)
             ev[i][0].record(stream)
             run_sel()
@@ -376,9 +384,9 @@ def run_gpu(args, rank, world, device):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    t_sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in range(args.steps)) / args.steps
+    t_sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
+    t_att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in range(steps)) / steps
 
     # end to end through the public API with host buffers (pinned), per step:
     # H2D of the step's inputs, D2H of the output.  Decode: the new queries,
@@ -445,7 +453,7 @@ def run_gpu(args, rank, world, device):
         run_e2e()
         torch.cuda.synchronize()
     e_ms = []
-    for i in range(args.steps):
+    for i in range(steps):
         flush_l2(i)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
@@ -456,36 +464,56 @@ def run_gpu(args, rank, world, device):
         e_ms.append(a.elapsed_time(b))
     return dict(ms=ms, sel_ms=sum(t_sel) / len(t_sel), att_ms=sum(t_att) / len(t_att),
                 e2e_ms=sum(e_ms) / len(e_ms), n_queries=n_queries, work=work, entries=entries, h2d=h2d, d2h=d2h,
-                clocks=clk.summary(), decode=decode, hbm_peak=hbm_peak, tf_peak=tf_peak, peak_src=peak_src)
+                clocks=clk.summary(), decode=decode, hbm_peak=hbm_peak, tf_peak=tf_peak, peak_src=peak_src,
+                inputs=inp, q2k=q2k, steps=steps, name=name)
 
 
 _CPU_INPUTS: dict = {}
 
 
-def cpu_baseline(name, seed, budget_s=15.0):
+def _host_copy(inp):
+    """The same workload object with every tensor moved to host memory."""
+    import dataclasses
+    return dataclasses.replace(inp, **{f.name: getattr(inp, f.name).cpu() for f in dataclasses.fields(inp)
+                                       if isinstance(getattr(inp, f.name), torch.Tensor)})
+
+
+def cpu_baseline(name, seed, budget_s=15.0, inputs=None, gpu_q2k=None):
     """The oracle, as it stands, on this host's cores over a bounded sample:
     whole requests (decode) or random query tokens (prefill), until the
-    budget is spent."""
+    budget is spent.  With ``inputs`` (the GPU run's own inputs, on the host)
+    and ``gpu_q2k`` (the GPU run's q2k), the oracle's selection of the sampled
+    rows is also compared with the GPU's: rows checked, rows that differ, and
+    the rows the oracle finds to be near ties (exempt), reported, not hidden."""
     import oracle
     oracle.build()
-    key = (name, seed)
-    if key not in _CPU_INPUTS:
-        _CPU_INPUTS[key] = msa_synth.workload(name, seed=seed, device="cpu")
-    inp = _CPU_INPUTS[key]
+    if inputs is None:
+        key = (name, seed)
+        if key not in _CPU_INPUTS:
+            _CPU_INPUTS[key] = msa_synth.workload(name, seed=seed, device="cpu")
+        inp = _CPU_INPUTS[key]
+    else:
+        inp = inputs
     cores = os.cpu_count()
     t0 = time.time()
     done = 0
+    checked = differ = exempt = 0
+    gq = None if gpu_q2k is None else gpu_q2k.cpu().numpy()
     if name.startswith("decode"):
         d = inp
         B = d.batch
         chunk = max(1, min(B, cores))
         while done < B and time.time() - t0 < budget_s:
             req = np.arange(done, min(B, done + chunk), dtype=np.int64)
-            q2k, _ = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
-                                          cu_seqlens_k=d.cu_seqlens_k, requests=req, topk=d.topk,
-                                          init=d.init_blocks, local=d.local_blocks)
+            q2k, gap = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
+                                            cu_seqlens_k=d.cu_seqlens_k, requests=req, topk=d.topk,
+                                            init=d.init_blocks, local=d.local_blocks)
             oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, q2k, SCALE, page_table=d.page_table,
                                  cu_seqlens_k=d.cu_seqlens_k, requests=req)
+            if gq is not None:
+                checked += q2k.shape[0] * q2k.shape[1]
+                differ += int((gq[:, req] != q2k).any(axis=2).sum())
+                exempt += int(oracle.exempt_rows(gap).sum())
             done += len(req)
         sample = f"{done} of {B} requests of {name}, whole select+attend per request"
     else:
@@ -495,14 +523,24 @@ def cpu_baseline(name, seed, budget_s=15.0):
         chunk = max(1, cores)
         while done < T and time.time() - t0 < budget_s:
             tok = np.sort(perm[done: done + chunk]).astype(np.int64)
-            q2k, _ = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=p.topk,
-                                           init=p.init_blocks, local=p.local_blocks)
+            q2k, gap = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=p.topk,
+                                             init=p.init_blocks, local=p.local_blocks)
             oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, q2k, SCALE)
+            if gq is not None:
+                checked += q2k.shape[0] * q2k.shape[1]
+                differ += int((gq[:, tok] != q2k).any(axis=2).sum())
+                exempt += int(oracle.exempt_rows(gap).sum())
             done += len(tok)
         sample = f"{done} random query tokens of {T} of {name}"
     dt = time.time() - t0
-    return {"value": round(done / dt, 3), "unit": "query tokens/s", "cores": cores, "kind": "oracle",
-            "sample": sample, "seconds": round(dt, 2)}
+    out = {"value": round(done / dt, 3), "unit": "query tokens/s", "cores": cores, "kind": "oracle",
+           "sample": sample, "seconds": round(dt, 2)}
+    if gq is not None:
+        out.update({"q2k_rows_checked": checked, "q2k_rows_differing": differ, "q2k_exempt_rows": exempt,
+                    "q2k_note": "(query, KV head) rows of the sample, GPU q2k against the oracle on the GPU "
+                                "run's own inputs; exempt = the oracle's k-th and (k+1)-th scores within "
+                                "1e-5 relative"})
+    return out
 
 
 def max_over_ranks(values, world):
@@ -531,6 +569,8 @@ def main():
                     help="keep only the first N requests of a decode workload (small profiling cases)")
     ap.add_argument("--mxfp8", action="store_true",
                     help="decode: emit the attention output as MXFP8 (E4M3 + E8M0 scales) instead of bf16")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other headline workloads (measured after the bench workload at one GPU)")
     ap.add_argument("--backward", action="store_true",
                     help="time the attention backward of a prefill workload instead of the forward step")
     args = ap.parse_args()
@@ -590,15 +630,65 @@ def main():
     ms, e2e_ms = max_over_ranks([res["ms"], res["e2e_ms"]], world)
     if rank != 0:
         return
+    summ = summarize(res, args, ms, e2e_ms, world)
+    config.update({"queries_per_step": res["n_queries"],
+                   "timing": ("eager C-ABI calls" if args.no_graph else
+                              "CUDA-graph replay of the step (the two C-ABI calls in one graph); per-kernel "
+                              "figures from a second pass with one graph per call, timed call by call"),
+                   "l2": "flushed between steps (256 MiB write + 256 MiB read, outside the timed events)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"})
+    line = {"metric": METRIC, "value": summ["value"], "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": summ["dtype"], "data": "synthetic", "config": config,
+            "roofline": summ["roofline"], "e2e": summ["e2e"],
+            # decode: scorer + top-k + attention; prefill: plan + scorer, then geometry, count, scan,
+            # tiles, scatter, tensor-core attention and merge
+            "gpu_launches": launches_per_step(res["decode"]) * args.steps, "clocks": res["clocks"]}
+    if not args.no_cpu_baseline and world == 1:
+        inputs, gpu_q2k = _host_copy(res["inputs"]), res["q2k"]
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed, inputs=inputs, gpu_q2k=gpu_q2k)
+        del inputs
+    # The other headline workloads, one GPU: each measured the same way (fewer steps), reported with its
+    # step time, roofline fraction and end-to-end figure.
+    if world == 1 and not (args.no_workloads or args.mxfp8) and args.requests is None and args.scale_down == 1:
+        extra = {}
+        del res
+        for name in EXTRA_WORKLOADS:
+            if name == args.workload:
+                continue
+            torch.cuda.empty_cache()
+            r = run_gpu(args, 0, 1, device, name=name, steps=min(args.steps, 10))
+            sm = summarize(r, args, r["ms"], r["e2e_ms"], 1)
+            extra[name] = {"desc": msa_synth.WORKLOADS[name], "steps": r["steps"], "warmup": args.warmup,
+                           "ms_per_step": round(r["ms"], 4), "value": sm["value"], "unit": unit,
+                           "dtype": sm["dtype"], "roofline": sm["roofline"], "e2e": sm["e2e"],
+                           "gpu_launches": launches_per_step(r["decode"]) * r["steps"], "clocks": r["clocks"]}
+            del r
+        line["workloads"] = extra
+    print(json.dumps(line))
+
+
+def launches_per_step(decode):
+    """The library's kernels in one step: decode scorer, top-k and attention;
+    prefill plan and scorer, then geometry, count, scan, tiles, scatter,
+    tensor-core attention and merge."""
+    return 3 if decode else 9
+
+
+def summarize(res, args, ms, e2e_ms, world):
+    """value, dtype, roofline (the dominant call) and e2e of one measured workload."""
+    unit = "query tokens/s"
+    name = res["name"]
     value = res["n_queries"] * world / (ms * 1e-3)
     e2e = res["n_queries"] * world / (e2e_ms * 1e-3)
     dom = "select" if res["sel_ms"] >= res["att_ms"] else "attend"
+    full = args.requests is None and args.scale_down == 1
     if res["decode"]:
         b_sel, b_att = res["work"]
         sel_r = b_sel / (res["sel_ms"] * 1e-3) / 1e9
         att_r = b_att / (res["att_ms"] * 1e-3) / 1e9
         ach = sel_r if dom == "select" else att_r
-        tr = TRAFFIC.get(args.workload) if args.requests is None and args.scale_down == 1 else None
+        tr = TRAFFIC.get(name) if full else None
         traffic = None
         if tr and tr["kernel"] == dom:
             traffic = round(tr["value"] * (b_sel if dom == "select" else b_att))
@@ -611,15 +701,16 @@ def main():
                 "peak_source": res["peak_src"] + " hbm_gbs (copy, burst)",
                 "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "bytes": b_sel, "GB/s": round(sel_r, 1)},
                                "attend": {"ms": round(res["att_ms"], 4), "bytes": b_att, "GB/s": round(att_r, 1)},
-                               "step_GB/s": round((b_sel + b_att) / (ms * 1e-3) / 1e9, 1)}}
-        dtype = "bf16" if "e4m3" not in args.workload else "e4m3-index/bf16"
+                               "step_GB/s": round((b_sel + b_att) / (ms * 1e-3) / 1e9, 1),
+                               "step_frac": round((b_sel + b_att) / (ms * 1e-3) / 1e9 / res["hbm_peak"], 4)}}
+        dtype = "bf16" if "e4m3" not in name else "e4m3-index/bf16"
     else:
-        fp8_index = "e4m3" in args.workload
+        fp8_index = "e4m3" in name
         f_sel, f_att = res["work"]
         sel_r = f_sel / (res["sel_ms"] * 1e-3) / 1e12
         att_r = f_att / (res["att_ms"] * 1e-3) / 1e12
         ach = sel_r if dom == "select" else att_r
-        tr = TRAFFIC.get(args.workload) if args.scale_down == 1 else None
+        tr = TRAFFIC.get(name) if full else None
         traffic = None
         if tr and tr["kernel"] == dom:
             traffic = round(tr["value"] * res["entries"])
@@ -636,28 +727,15 @@ def main():
                                           "peak_TFLOP/s": round(res["tf_peak"] * (2.0 if fp8_index else 1.0), 1),
                                           "frac": round(sel_r / (res["tf_peak"] * (2.0 if fp8_index else 1.0)), 4)},
                                "attend": {"ms": round(res["att_ms"], 4), "flop": f_att, "TFLOP/s": round(att_r, 2)},
-                               "step_TFLOP/s": round((f_sel + f_att) / (ms * 1e-3) / 1e12, 2)}}
+                               "step_TFLOP/s": round((f_sel + f_att) / (ms * 1e-3) / 1e12, 2),
+                               "step_frac": round((f_sel + f_att) / (ms * 1e-3) / 1e12 / res["tf_peak"], 4)}}
         dtype = "e4m3-index/bf16" if fp8_index else "bf16"
-    config.update({"queries_per_step": res["n_queries"],
-                   "timing": ("eager C-ABI calls" if args.no_graph else
-                              "CUDA-graph replay of the step (the two C-ABI calls in one graph); per-kernel "
-                              "figures from a second pass with one graph per call, timed call by call"),
-                   "l2": "flushed between steps (256 MiB write + 256 MiB read, outside the timed events)",
-                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"})
-    line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config, "roofline": roof,
-            "e2e": {"value": round(e2e, 1), "unit": unit, "h2d_bytes_per_step": res["h2d"],
-                    "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 4),
-                    "method": ("pinned staging buffers, one H2D copy for the select inputs and one (side stream, "
-                               "overlapping the select call) for the attention inputs, the two C-ABI calls, "
-                               "D2H of the output; " + ("eager" if args.no_graph else "replayed as one CUDA graph"))},
-            # decode: scorer + top-k + attention; prefill: plan + scorer, then geometry, count, scan,
-            # tiles, scatter, tensor-core attention and merge
-            "gpu_launches": (3 if res["decode"] else 9) * args.steps, "clocks": res["clocks"]}
-    if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
-    print(json.dumps(line))
+    e2e_d = {"value": round(e2e, 1), "unit": unit, "h2d_bytes_per_step": res["h2d"],
+             "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(e2e_ms, 4),
+             "method": ("pinned staging buffers, one H2D copy for the select inputs and one (side stream, "
+                        "overlapping the select call) for the attention inputs, the two C-ABI calls, "
+                        "D2H of the output; " + ("eager" if args.no_graph else "replayed as one CUDA graph"))}
+    return {"value": round(value, 1), "dtype": dtype, "roofline": roof, "e2e": e2e_d}
 
 
 if __name__ == "__main__":

@@ -24,8 +24,11 @@ EncodeTiledFn get_encode_tiled() {
 
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace layout, shared by msa_workspace_size and the calls.  Completion
-// counters come first, right after the error-word header.
+// Workspace layout, shared by msa_workspace_size and the calls.  Decode: the
+// regions whose size does not depend on the call come first, at fixed offsets
+// (the attention's merge counters, one per CTA, and its partials), then the
+// block scores, whose size grows with batch and max_blocks.  So a call of any
+// size never writes over the counters, which must stay at zero between calls.
 struct Layout {
   size_t scores = 0, att_tickets = 0, partials = 0, plan = 0, bm = 0, total = 0;
 };
@@ -34,11 +37,11 @@ static Layout layout(int mode, long long n, int max_blocks, int topk) {
   size_t off = kHeaderBytes;
   if (mode == MSA_MODE_DECODE) {
     L.att_tickets = off;
-    off += up256(static_cast<size_t>(n) * kKvHeads * sizeof(int));
-    L.scores = off;
-    off += up256(static_cast<size_t>(n) * kKvHeads * max_blocks * sizeof(float));
+    off += up256(attend_tickets_bytes());
     L.partials = off;
     off += up256(attend_partials_bytes());
+    L.scores = off;
+    off += up256(static_cast<size_t>(n) * kKvHeads * max_blocks * sizeof(float));
   } else if (mode == MSA_MODE_PREFILL) {
     L.plan = off;
     off += up256(prefill_plan_ints(static_cast<int>(n), max_blocks) * sizeof(int));
@@ -208,7 +211,8 @@ static msa_status attend_decode(const msa_config* cfg, const void* q, const void
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the merge tickets start at zero: the workspace was zero-filled once and
-  // every call leaves them at zero (the CTA that completes a segment resets it)
+  // every call leaves them at zero (the CTA that completes a segment resets
+  // it); no other region of any decode call overlaps them
   AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
   cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out, out_q, out_scale,
                                        reinterpret_cast<float*>(ws + L.partials),

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     }
     fence_mbar_init();
   }
-  // total scored pages; rows of requests that need no scoring are written here
+  // total scored pages (rows of requests that need no scoring are written by the top-k kernel)
   int total = 0;
   for (int r0 = 0; r0 < B; r0 += kSelThreads) {
     const int r = r0 + tid;
@@ -318,6 +318,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
         } while (scored_blocks(geo, r, topk, nullptr) == 0);
       }
     }
+    // No copy may still be landing when the CTA exits, also after a wait gave
+    // up: wait (bounded) for the last fill of every stage.  Only this thread
+    // arms the full barriers, so that phase cannot have been passed.
+    if (lane == 0)
+      for (int s = 0; s < kStages; ++s) {
+        const int f = (i - s + kStages - 1) / kStages;  // fills of stage s
+        if (f > 0) mbar_wait(&sm.full[s], (f - 1) & 1, err, 102);
+      }
     return;
   }
 

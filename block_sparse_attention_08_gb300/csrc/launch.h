@@ -29,6 +29,7 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,
                                  cudaStream_t stream);
 size_t attend_partials_bytes();
+size_t attend_tickets_bytes();
 size_t prefill_plan_ints(int num_docs, int max_tiles);
 cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, const void* index_k,
                                   const int32_t* cu_seqlens, int num_docs, long long total_tokens, int max_seqlen,

@@ -54,6 +54,7 @@ struct PsSmem {
   uint64_t a_full, a_empty;
   uint64_t b_full[kPsStages], b_empty[kPsStages];
   uint64_t t_full[2], t_empty[2];
+  uint64_t mma_done;  // the MMA thread's last commit, waited on before tensor memory is released
   uint32_t tmem_base;
 };
 
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
       mbar_init(&sm.t_full[i], 1);
       mbar_init(&sm.t_empty[i], 4);
     }
+    mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -276,6 +278,14 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
           if (!kE4M3) tma_load_2d(sm.b[s] + kPsBox, &kmap, 64, x.start + b * kBlock, &sm.b_full[s]);
         }
         ++nunit;
+      }
+      // No copy may still be landing when the CTA exits, also after a wait
+      // gave up: wait (bounded) for the last fill of the A tile and of every
+      // key stage.  Only this thread arms those barriers.
+      if (nunit > 0) mbar_wait(&sm.a_full, (nunit - 1) & 1, err, 402);
+      for (int s = 0; s < kPsStages; ++s) {
+        const uint32_t f = (bc + kPsStages - 1 - s) / kPsStages;  // fills of stage s
+        if (f > 0) mbar_wait(&sm.b_full[s], (f - 1) & 1, err, 403);
       }
     }
   } else if (warp == 5) {
@@ -319,6 +329,10 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
         tc::commit(&sm.a_empty);
         ++nunit;
       }
+      // every MMA of this thread has finished before tensor memory is released
+      // (the epilogue's waits cover this unless one of them gave up)
+      tc::commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0, err, 503);
     }
   } else {
     // ---------------- epilogue warps 0-3: one token row per thread ----------------

@@ -294,6 +294,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       }
       it = seg_end;
     }
+    // No copy may still be landing when the CTA exits, also after a wait gave
+    // up: wait (bounded) for the last fill of every chunk stage and segment
+    // slot.  Only this thread arms those barriers, so that phase cannot have
+    // been passed.
+    if (lane == 0) {
+      for (int s = 0; s < kAttStages; ++s) {
+        const long long f = (sc - s + kAttStages - 1) / kAttStages;  // fills of stage s
+        if (f > 0) mbar_wait(&sm.full[s], static_cast<uint32_t>((f - 1) & 1), err, 220);
+      }
+      for (int s = 0; s < kSegSlots; ++s) {
+        const int f = (nseg - s + kSegSlots - 1) / kSegSlots;
+        if (f > 0) mbar_wait(&sm.seg_full[s], (f - 1) & 1, err, 221);
+      }
+    }
     return;
   }
 
@@ -474,19 +488,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             make_float4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
       __threadfence();
       __syncwarp();
+      // The contributors are the consecutive CTAs c_first .. c_last (at most
+      // topk: each holds at least one unit of the segment).  The segment's
+      // counter is the one of c_first: a CTA is the first contributor of a cut
+      // segment only for its last segment, so each counter serves one segment.
+      const long long c_first = cta_of(range0, N, G);
       int last = 0;
       if (lane == 0) {
         const int cnt = static_cast<int>(seg_end - seg_lo);
-        last = (atomicAdd(&tickets[qi * kKvHeads + g], cnt) + cnt == topk) ? 1 : 0;
+        last = (atomicAdd(&tickets[c_first], cnt) + cnt == topk) ? 1 : 0;
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
-        // The contributors are the consecutive CTAs c_first .. c_last (at most
-        // topk: each holds at least one unit of the segment); every one but the
-        // first wrote this segment as its first partial.  All loads of a pass
-        // are issued before any is used.
-        const long long c_first = cta_of(range0, N, G), c_last = cta_of(range0 + topk - 1, N, G);
+        // Every contributor but the first wrote this segment as its first
+        // partial.  All loads of a pass are issued before any is used.
+        const long long c_last = cta_of(range0 + topk - 1, N, G);
         const int nc = static_cast<int>(c_last - c_first + 1);
         const long long slot0 = 2 * c_first + (seg_begin(c_first, N, G) < range0 ? 1 : 0);
         auto part_of = [&](int x) {
@@ -535,7 +552,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
                 pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
                 pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
         }
-        if (lane == 0) tickets[qi * kKvHeads + g] = 0;
+        if (lane == 0) tickets[c_first] = 0;
       }
     }
   }
@@ -571,6 +588,8 @@ static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
 }
 
 size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
+// one merge counter per CTA of the persistent grid (at most kNumSMs CTAs)
+size_t attend_tickets_bytes() { return static_cast<size_t>(kNumSMs) * sizeof(int); }
 
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,

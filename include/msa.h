@@ -113,11 +113,16 @@ msa_status msa_config_check(const msa_config* cfg);
  * bytes and the completion counters.  Every call that completes leaves its
  * counters at zero again (the decode calls enqueue no memset; the prefill
  * calls clear theirs with a cudaMemsetAsync on `stream`), and the scorer
- * stores rather than accumulates (NeMo _score_scratch), so one workspace can
- * serve later calls of any size up to the one it was sized for.  After a call
- * whose device error word reads MSA_DEVERR_TIMEOUT (a pipeline that gave up
- * part-way), zero-fill the workspace again before reusing it.  Calls that
- * share a workspace must not run concurrently. */
+ * stores rather than accumulates (NeMo _score_scratch).  In the decode layout
+ * the decode attention's counters (one per CTA) sit at a fixed offset that no
+ * decode call of any batch or max_blocks writes over, so one workspace serves
+ * decode calls of any size whose msa_workspace_size fits in it, in any order.
+ * The prefill layouts do not keep that region: a workspace that served a
+ * prefill or backward call must be zero-filled again before it serves a
+ * decode attention call.  After a call whose device error word reads
+ * MSA_DEVERR_TIMEOUT (a pipeline that gave up part-way), zero-fill the
+ * workspace again before reusing it.  Calls that share a workspace must not
+ * run concurrently. */
 msa_status msa_workspace_size(const msa_config* cfg, int mode, int64_t n, int max_blocks,
                               size_t* bytes);
 
@@ -213,8 +218,9 @@ msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, const void* i
  *   out      dev [batch, 64, 128] bf16
  * The kernel is launched as a programmatic dependent of the kernel before it
  * on `stream` (after msa_select_blocks_decode, its launch overlaps the
- * top-k); it touches no memory before that kernel has completed, so stream
- * order is kept whatever precedes it.
+ * top-k).  Before that kernel has completed it reads no input and writes no
+ * output; it only issues L2 prefetch hints for its requests' page-table rows,
+ * which change no memory, so stream order is kept whatever precedes it.
  */
 msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* q2k,

@@ -78,7 +78,7 @@ def _load():
             Dbl = ctypes.c_double
             lib.oracle_select_prefill.argtypes = [P, P, I, P, I, P, I64, I, I, I, P, P, P, I]
             lib.oracle_attend_prefill.argtypes = [P, P, P, P, I, P, I64, P, I, Dbl, P]
-            lib.oracle_select_decode.argtypes = [P, P, I, P, P, P, I, P, I64, I, I, I, P, P]
+            lib.oracle_select_decode.argtypes = [P, P, I, P, P, P, I, P, I64, I, I, I, P, P, P, I]
             lib.oracle_attend_decode.argtypes = [P, P, P, P, P, P, I, P, I64, P, I, Dbl, P]
             lib.oracle_pack_metadata.argtypes = [P, I64, I64, P, P, P, P, P, P]
             lib.oracle_attend_prefill_backward.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl, P, P, P]
@@ -216,8 +216,10 @@ def mxfp8_quantize(x):
 
 
 def select_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None,
-                  requests=None, topk=16, init=0, local=1):
-    """q2k int32 [G, n, topk] and gap [G, n] for the listed requests."""
+                  requests=None, topk=16, init=0, local=1, return_scores=False):
+    """q2k int32 [G, n, topk] and gap [G, n] for the listed requests (and, with
+    ``return_scores``, the fp64 block scores [n, G, max_nb], NaN past a request's
+    blocks)."""
     lib = _load()
     iq, ik = _bits(index_q), _bits(index_k_cache)
     code = _dtype_code(iq)
@@ -231,11 +233,15 @@ def select_decode(index_q, index_k_cache, seq_lens, page_table=None, cu_seqlens_
     max_pages = 0 if pt is None else pt.shape[1]
     q2k = np.full((G, n, topk), -7, dtype=np.int32)
     gap = np.zeros((G, n), dtype=np.float64)
+    scores, max_nb = None, 0
+    if return_scores:
+        max_nb = int((sl[req].max() + BLOCK - 1) // BLOCK) if n else 0
+        scores = np.full((n, G, max(max_nb, 1)), np.nan)
     rc = lib.oracle_select_decode(_ptr(iq), _ptr(ik), code, _ptr(sl), _ptr(pt), _ptr(cuk), max_pages,
-                                  _ptr(req), n, topk, init, local, _ptr(q2k), _ptr(gap))
+                                  _ptr(req), n, topk, init, local, _ptr(q2k), _ptr(gap), _ptr(scores), max_nb)
     if rc:
         raise ValueError("oracle_select_decode failed")
-    return q2k, gap
+    return (q2k, gap, scores) if return_scores else (q2k, gap)
 
 
 def attend_decode(q, k_cache, v_cache, seq_lens, q2k, scale, page_table=None, cu_seqlens_k=None,

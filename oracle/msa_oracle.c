@@ -509,12 +509,14 @@ int oracle_mxfp8_quantize(const uint16_t* bf16, int64_t n, uint8_t* q, uint8_t* 
   return 0;
 }
 
-/* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n]. */
+/* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n];
+ * s64_out (optional): [n][G][max_nb]. */
 int oracle_select_decode(const void* index_q, const void* index_k_cache, int dtype,
                          const int32_t* seq_lens, const int32_t* page_table,
                          const int64_t* cu_seqlens_k, int max_pages,
                          const int64_t* requests, int64_t n, int topk, int init,
-                         int local, int32_t* q2k, double* gap) {
+                         int local, int32_t* q2k, double* gap, double* s64_out,
+                         int max_nb) {
   if (topk < 1 || topk > OR_MAXTOPK) return 1;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t i = 0; i < n; ++i) {
@@ -532,6 +534,8 @@ int oracle_select_decode(const void* index_q, const void* index_k_cache, int dty
     for (int g = 0; g < OR_KV; ++g) {
       for (int b = 0; b < nb; ++b) s32[b] = (float)s64[g * nb + b];
       gap[g * n + i] = select_row(s32, nb, topk, init, local, q2k + ((int64_t)g * n + i) * topk);
+      if (s64_out && nb <= max_nb)
+        for (int b = 0; b < nb; ++b) s64_out[(i * OR_KV + g) * max_nb + b] = s64[g * nb + b];
     }
     free(rows);
     free(s64);

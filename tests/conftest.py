@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Every parity comparison of the run, with its differing and exempt q2k rows
+    and its output error, so the near-tie exemptions are reported, not hidden."""
+    try:
+        from _parity import REPORT
+    except ImportError:  # pragma: no cover
+        return
+    if REPORT:
+        terminalreporter.section("parity report")
+        for line in REPORT:
+            terminalreporter.write_line(line)

@@ -33,7 +33,7 @@ def check_line(line, steps):
 
 def test_bench_line_contract():
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "decode_b4_ctx8k_contig", "--steps", "3",
-           "--warmup", "3", "--no-cpu-baseline"]
+           "--warmup", "3", "--no-cpu-baseline", "--no-workloads"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]

@@ -13,22 +13,24 @@ pytestmark = pytest.mark.gpu
 SMALL_LENS = [1, 2, 127, 128, 129, 300, 1000, 2048, 2049, 2050, 4095, 5000, 8191]
 
 
-def _run(d, topk, init, local):
-    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+def _run(d, topk, init, local, label="decode", workspace=None):
+    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks, workspace=workspace)
     q2k = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, topk=topk, init_blocks=init,
                                        local_blocks=local, **kw)
     torch.cuda.synchronize()
-    ref_q2k, gap = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
-                                        cu_seqlens_k=d.cu_seqlens_k, topk=topk, init=init, local=local)
+    ref_q2k, gap, scores = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
+                                                cu_seqlens_k=d.cu_seqlens_k, topk=topk, init=init, local=local,
+                                                return_scores=True)
     nb = decode_nb(d.seq_lens, d.max_blocks)
-    check_q2k(q2k.cpu().numpy(), ref_q2k, gap, nb, topk, init, local, "decode q2k")
+    check_q2k(q2k.cpu().numpy(), ref_q2k, gap, nb, topk, init, local, f"{label} (topk {topk}, init {init}, "
+              f"local {local})", scores=scores)
     # attention on the oracle's selection (identical q2k on both sides)
     out = msa.msa_sparse_attend_decode(d.q, d.k_cache, d.v_cache, torch.from_numpy(ref_q2k).cuda(), d.seq_lens,
                                        scale=SCALE, **kw)
     torch.cuda.synchronize()
     ref_out = oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, ref_q2k, SCALE,
                                    page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k)
-    check_out(out, ref_out, "decode out")
+    check_out(out, ref_out, f"{label} out")
     return q2k, out
 
 
@@ -85,6 +87,27 @@ def test_decode_repeated_calls_reuse_workspace():
         assert torch.equal(first, again) and torch.equal(o1, o2)
 
 
+def test_decode_workspace_shared_across_batch_sizes():
+    """One workspace serves decode calls of different sizes in any order: a
+    64-request call, a 4-request call over long contexts (its block scores
+    reach far into the workspace), then the 64-request call again.  The
+    attention's merge counters sit at a fixed place that no call's scores or
+    partials cover, so every call matches the oracle and the repeated call its
+    first result bit for bit."""
+    big = msa_synth.decode_inputs(np.random.default_rng(81).integers(1, 6000, size=64).tolist(), paged=True,
+                                  seed=81, device="cuda")
+    small = msa_synth.decode_inputs([60000, 40000, 30000, 20000], paged=True, seed=82, device="cuda")
+    cfg = msa.make_config()
+    need = max(msa.workspace_size(cfg, 0, big.batch, big.max_blocks),
+               msa.workspace_size(cfg, 0, small.batch, small.max_blocks))
+    ws = msa.Workspace(need)
+    q2k_a, out_a = _run(big, 16, 0, 1, "decode 64 requests, first call", workspace=ws)
+    _run(small, 16, 0, 1, "decode 4 long requests, same workspace", workspace=ws)
+    q2k_b, out_b = _run(big, 16, 0, 1, "decode 64 requests, after the 4-request call", workspace=ws)
+    assert torch.equal(q2k_a, q2k_b) and torch.equal(out_a, out_b)
+    assert ws.read_device_error() == (0, 0)
+
+
 def test_decode_bad_page_is_reported_not_faulted():
     d = msa_synth.decode_inputs([3000, 4000], paged=True, seed=2, device="cuda")
     pt = d.page_table.clone()
@@ -98,19 +121,19 @@ def test_decode_bad_page_is_reported_not_faulted():
 
 def test_decode_workload_b4_ctx8k_contig():
     d = msa_synth.workload("decode_b4_ctx8k_contig", device="cuda")
-    _run(d, 16, 0, 1)
+    _run(d, 16, 0, 1, "decode_b4_ctx8k_contig")
 
 
 @pytest.mark.slow
 def test_decode_workload_b64_paged():
     d = msa_synth.workload("decode_b64_ctx4k_64k_paged", device="cuda")
-    _run(d, 16, 0, 1)
+    _run(d, 16, 0, 1, "decode_b64_ctx4k_64k_paged")
 
 
 @pytest.mark.slow
 def test_decode_workload_b16_128k_e4m3():
     d = msa_synth.workload("decode_b16_ctx128k_paged_e4m3", device="cuda")
-    _run(d, 16, 0, 1)
+    _run(d, 16, 0, 1, "decode_b16_ctx128k_paged_e4m3")
 
 
 @pytest.mark.parametrize("paged", [False, True])

@@ -176,3 +176,82 @@ def test_exempt_rows_are_rare_and_reported():
     _, _, _, gap, _ = _random_prefill(1500, seed=2)
     ex = oracle.exempt_rows(gap)
     assert ex.sum() < 0.02 * ex.size
+
+
+# ---- the near-tie gap (the exemption's only input) ---------------------------
+#
+# One 640-token document; the query at position 639 has nb = 5 candidate blocks,
+# block 4 is forced (local 1) and topk 3 leaves need = 2 of blocks 0..3 to the
+# scores.  Every key of block b holds the same index key (a_b, c_b, 0, ...) and
+# every index query is (1, 1, 0, ...), so block b scores exactly a_b + c_b (both
+# bf16, the sum exact in fp32).  The gap is |s_k - s_k+1| / max(|s_k|, |s_k+1|)
+# between the k-th kept and the first rejected non-forced score, in the
+# (score desc, id asc) order.
+
+def _gap_case(block_scores):
+    T = 640
+    iq = np.zeros((T, 4, 128), np.float32)
+    iq[:, :, 0] = 1.0
+    iq[:, :, 1] = 1.0
+    ik = np.zeros((T, 1, 128), np.float32)
+    for b, (a, c) in enumerate(block_scores):
+        ik[128 * b: 128 * (b + 1), 0, 0] = a
+        ik[128 * b: 128 * (b + 1), 0, 1] = c
+    cu = np.array([0, T], np.int32)
+    toks = np.array([639, 200], np.int64)
+    q2k, gap, scores = oracle.select_prefill(_bf16(iq), _bf16(ik), cu, toks, topk=3, init=0, local=1,
+                                             return_scores=True)
+    return q2k, gap, scores
+
+
+E18, E16 = 2.0 ** -18, 2.0 ** -16
+
+
+@pytest.mark.parametrize("name,blocks,keep,gap,exempt", [
+    # k-th 1, next 1 - 2^-18: a near tie (3.8e-6 < 1e-5)
+    ("near_tie", [(2.0, 0.0), (1.0, 0.0), (1.0, -E18), (0.25, 0.0), (0.0, 0.0)], [0, 1, 4], E18, True),
+    # k-th 1, next 1 - 2^-16: 1.5e-5, decided by score
+    ("decided", [(2.0, 0.0), (1.0, 0.0), (1.0, -E16), (0.25, 0.0), (0.0, 0.0)], [0, 1, 4], E16, False),
+    # the near tie sits above the boundary (1st and 2nd); the boundary (2nd 1 - 2^-18,
+    # 3rd 0.5) is decided: a gap taken between the wrong pair would call it exempt
+    ("tie_above_boundary", [(1.0, 0.0), (1.0, -E18), (0.5, 0.0), (0.25, 0.0), (0.0, 0.0)], [0, 1, 4],
+     (0.5 - E18) / (1.0 - E18), False),
+    # the near tie sits below the boundary (3rd and 4th), the boundary gap is 0.5
+    ("tie_below_boundary", [(2.0, 0.0), (1.0, 0.0), (0.5, 0.0), (0.5, -E18), (0.0, 0.0)], [0, 1, 4], 0.5, False),
+    # negative scores: k-th -0.5, next -(0.5 + 2^-18); relative to the larger magnitude
+    ("negative", [(1.0, 0.0), (-0.5, 0.0), (-0.5, -E18), (-1.0, 0.0), (0.0, 0.0)], [0, 1, 4],
+     E18 / (0.5 + E18), True),
+    # an exact tie at the boundary: the lower id is kept, the gap is 0 (exempt)
+    ("exact_tie", [(2.0, 0.0), (1.0, 0.0), (1.0, 0.0), (0.25, 0.0), (0.0, 0.0)], [0, 1, 4], 0.0, True),
+    # the forced block's score plays no part, however close it is to the boundary
+    ("forced_not_counted", [(2.0, 0.0), (1.0, 0.0), (0.5, 0.0), (0.25, 0.0), (1.0, -E18)], [0, 1, 4], 0.5,
+     False),
+])
+def test_near_tie_gap(name, blocks, keep, gap, exempt):
+    q2k, g, scores = _gap_case(blocks)
+    for h in range(4):
+        assert list(q2k[h, 0]) == keep, name
+        np.testing.assert_array_equal(scores[0, h, :5], [a + c for a, c in blocks])
+        assert g[h, 0] == gap, (name, g[h, 0], gap)
+        assert bool(oracle.exempt_rows(g)[h, 0]) == exempt, name
+        # position 200: nb = 2 <= topk, nothing is decided by score
+        assert g[h, 1] == np.inf and not oracle.exempt_rows(g)[h, 1]
+        assert list(q2k[h, 1]) == [0, 1, -1]
+
+
+def test_near_tie_gap_decode_matches_prefill():
+    # the decode select reports the same gap for the same context (query at position 639)
+    q2k_p, g_p, _ = _gap_case([(2.0, 0.0), (1.0, 0.0), (1.0, -E18), (0.25, 0.0), (0.0, 0.0)])
+    T = 640
+    iq = np.zeros((1, 4, 128), np.float32)
+    iq[:, :, :2] = 1.0
+    ik = np.zeros((T, 1, 128), np.float32)
+    for b, (a, c) in enumerate([(2.0, 0.0), (1.0, 0.0), (1.0, -E18), (0.25, 0.0), (0.0, 0.0)]):
+        ik[128 * b: 128 * (b + 1), 0, 0] = a
+        ik[128 * b: 128 * (b + 1), 0, 1] = c
+    q2k_d, g_d, s_d = oracle.select_decode(_bf16(iq), _bf16(ik), np.array([T], np.int32),
+                                           cu_seqlens_k=np.array([0, T], np.int64), topk=3, init=0, local=1,
+                                           return_scores=True)
+    np.testing.assert_array_equal(q2k_d[:, 0], q2k_p[:, 0])
+    np.testing.assert_array_equal(g_d[:, 0], g_p[:, 0])
+    np.testing.assert_array_equal(s_d[0, :, :5], np.tile([2.0, 1.0, 1.0 - E18, 0.25, 0.0], (4, 1)))

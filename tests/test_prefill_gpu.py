@@ -15,26 +15,27 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def _check(p, tokens=None, topk=16, init=0, local=1, attend=True):
+def _check(p, tokens=None, topk=16, init=0, local=1, attend=True, label="prefill"):
+    """q2k of every token against the oracle (bit-exact but for reported near
+    ties); the attention, on the oracle's selection, on `tokens` (all when None)."""
     q2k = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen, topk=topk,
                                         init_blocks=init, local_blocks=local)
     torch.cuda.synchronize()
     T = p.total_tokens
-    tok = np.arange(T, dtype=np.int64) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    ref_q2k, gap = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=topk, init=init,
-                                         local=local)
-    gq = q2k.cpu().numpy()[:, tok]
-    check_q2k(gq, ref_q2k, gap, prefill_nb(p.cu_seqlens, tok), topk, init, local, "prefill q2k")
+    every = np.arange(T, dtype=np.int64)
+    ref_q2k, gap, scores = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, every, topk=topk, init=init,
+                                                 local=local, return_scores=True)
+    check_q2k(q2k.cpu().numpy(), ref_q2k, gap, prefill_nb(p.cu_seqlens, every), topk, init, local,
+              f"{label} (topk {topk}, init {init}, local {local})", scores=scores)
     if not attend:
         return
-    # attention on the oracle's selection for the checked rows
-    full = q2k.clone()
-    idx = torch.from_numpy(tok).cuda()
-    full[:, idx] = torch.from_numpy(ref_q2k).cuda()
+    # attention on the oracle's selection
+    tok = every if tokens is None else np.asarray(tokens, dtype=np.int64)
+    full = torch.from_numpy(ref_q2k).cuda()
     out = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, full, p.cu_seqlens, p.max_seqlen, scale=SCALE)
     torch.cuda.synchronize()
-    ref_out = oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, ref_q2k, SCALE)
-    check_out(out[idx], ref_out, "prefill out")
+    ref_out = oracle.attend_prefill(p.q, p.k, p.v, p.cu_seqlens, tok, ref_q2k[:, tok], SCALE)
+    check_out(out[torch.from_numpy(tok).cuda()], ref_out, f"{label} out ({len(tok)} of {T} tokens)")
 
 
 DOCS = [1, 127, 128, 129, 700, 2047, 2048, 2049, 3000, 5000]
@@ -43,7 +44,7 @@ DOCS = [1, 127, 128, 129, 700, 2047, 2048, 2049, 3000, 5000]
 @pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (16, 1, 1), (4, 1, 1), (3, 0, 0), (2, 0, 2), (1, 1, 0)])
 def test_prefill_small(topk, init, local):
     p = msa_synth.prefill_inputs(DOCS, seed=11 + topk + init, device="cuda")
-    _check(p, topk=topk, init=init, local=local)
+    _check(p, topk=topk, init=init, local=local, label="prefill small documents")
 
 
 @pytest.mark.parametrize("topk,init,local", [(16, 0, 1), (16, 1, 1), (3, 0, 0)])
@@ -51,7 +52,8 @@ def test_prefill_e4m3_small(topk, init, local):
     # unscaled E4M3 index (the decoded values' dot products, fp32 accumulate)
     p = msa_synth.prefill_inputs(DOCS, seed=21 + topk + init, device="cuda", index_dtype="e4m3")
     assert p.index_q.dtype == torch.float8_e4m3fn
-    _check(p, topk=topk, init=init, local=local, attend=(topk == 16 and init == 0))
+    _check(p, topk=topk, init=init, local=local, attend=(topk == 16 and init == 0),
+           label="prefill small documents, E4M3 index")
 
 
 def test_prefill_e4m3_repeated_calls_are_identical():
@@ -121,22 +123,25 @@ def _sample_tokens(cu, n, seed):
     return np.array(sorted(pick), dtype=np.int64)
 
 
+# The full-size workloads: q2k of every token against the oracle; the attention
+# on a sample of tokens (random ones plus document and block edges).
+
 @pytest.mark.slow
 def test_prefill_workload_1doc_16k():
     p = msa_synth.workload("prefill_1doc_16k", device="cuda")
-    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 0))
+    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 0), label="prefill_1doc_16k")
 
 
 @pytest.mark.slow
 def test_prefill_workload_1doc_16k_e4m3():
     p = msa_synth.workload("prefill_1doc_16k_e4m3", device="cuda")
-    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 2), attend=False)
+    _check(p, attend=False, label="prefill_1doc_16k_e4m3")
 
 
 @pytest.mark.slow
 def test_prefill_workload_packed_2x32k():
     p = msa_synth.workload("prefill_packed_2x32k", device="cuda")
-    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 1), init=1, local=1)
+    _check(p, tokens=_sample_tokens(p.cu_seqlens, 384, 1), init=1, local=1, label="prefill_packed_2x32k")
 
 
 def test_prefill_attend_empty_rows_and_bad_ids():
