@@ -28,6 +28,11 @@ Which statement on the pages each function follows:
     OCP MX block rule, which the page names but does not print.
   * ``pack_metadata`` / ``pack`` / ``unpack`` -- NeMo layout-from-doc_ids
     constructor, ``_contiguous_runs``, ``MSAMicrobatch.pack`` / ``unpack``.
+  * ``index_normalize`` / ``index_produce_prefill`` / ``index_produce_decode``
+    -- the index producer: L2 norm, storage cast (bf16 or unscaled E4M3) and
+    insertion of index-K into the paged side cache (TensorRT-LLM fields
+    fuse_qkv_index_projection and indexer_kv_dtype, the class description's
+    paged index-K cache; NeMo select_blocks takes index tensors "post norm").
 """
 from __future__ import annotations
 
@@ -56,12 +61,12 @@ PACK_ERRORS = {
 
 
 def build(force: bool = False) -> str:
-    """Compile liboracle.so with gcc (-O2, OpenMP, no fast-math)."""
+    """Compile liboracle.so with gcc (-O2, OpenMP, no fast-math, no FMA contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+            ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11",
              "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -85,6 +90,7 @@ def _load():
             lib.oracle_attend_loss_f64.argtypes = [P, P, P, P, P, I, I64, P, I, Dbl]
             lib.oracle_attend_loss_f64.restype = Dbl
             lib.oracle_mxfp8_quantize.argtypes = [P, I64, P, P]
+            lib.oracle_index_normalize.argtypes = [P, I64, I, P]
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = Dbl
             for f in (lib.oracle_select_prefill, lib.oracle_attend_prefill,
@@ -302,3 +308,66 @@ def unpack(packed, token_rows, batch, seq):
 def exempt_rows(gap, rel=1e-5):
     """Boolean [G, n]: rows whose k-th / (k+1)-th non-forced scores are a near tie."""
     return np.asarray(gap) < rel
+
+
+# ---- index producer ------------------------------------------------------------
+
+def index_normalize(x, dtype="bf16"):
+    """L2-normalised 128-vectors of a bf16 tensor [..., 128], stored as bf16 bits
+    (uint16) or E4M3 bytes (uint8) of the same shape (see the C source for the
+    reading of the norm's precision)."""
+    lib = _load()
+    xb = np.ascontiguousarray(_bits(x))
+    if xb.dtype != np.uint16 or xb.shape[-1] != DI:
+        raise TypeError("index_normalize takes bf16 [..., 128]")
+    n = xb.size // DI
+    out = np.zeros(xb.shape, dtype=np.uint16 if dtype == "bf16" else np.uint8)
+    lib.oracle_index_normalize(_ptr(xb), n, 0 if dtype == "bf16" else 1, _ptr(out))
+    return out
+
+
+def index_slots_decode(seq_lens, page_table=None, cu_seqlens_k=None):
+    """Slot of each request's newest key (position seq_lens[r] - 1): page_table[r][p // 128] * 128 + p % 128
+    (paged, the TensorRT-LLM page's index-K cache parallel to the K/V cache) or cu_seqlens_k[r] + p."""
+    L = _i64(seq_lens)
+    p = L - 1
+    if page_table is not None:
+        pt = _i64(page_table)
+        return pt[np.arange(L.shape[0]), p // BLOCK] * BLOCK + p % BLOCK
+    return _i64(cu_seqlens_k)[:-1] + p
+
+
+def index_slots_prefill(cu_seqlens, page_table):
+    """Slot of every compact token: document d, position p = t - cu_seqlens[d], slot
+    page_table[d][p // 128] * 128 + p % 128."""
+    cu = _i64(cu_seqlens)
+    pt = _i64(page_table)
+    T = int(cu[-1])
+    t = np.arange(T, dtype=np.int64)
+    d = np.searchsorted(cu, t, side="right") - 1
+    p = t - cu[d]
+    return pt[d, p // BLOCK] * BLOCK + p % BLOCK
+
+
+def index_produce_decode(index_q, index_k, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None,
+                         dtype="bf16"):
+    """(index_q_out [B, 4, 128], the index-K cache [slots, 1, 128] with each request's new
+    normalised row written at its slot) as raw bits / bytes; the cache passed in is copied."""
+    q_out = index_normalize(index_q, dtype)
+    k_rows = index_normalize(index_k, dtype)
+    cache = np.array(_bits(index_k_cache), copy=True)
+    slots = index_slots_decode(seq_lens, page_table, cu_seqlens_k)
+    cache[slots] = k_rows
+    return q_out, cache
+
+
+def index_produce_prefill(index_q, index_k, cu_seqlens, dtype="bf16", index_k_cache=None, page_table=None):
+    """(index_q_out [T, 4, 128], index_k_out [T, 1, 128], the cache with every token's row at its
+    slot, or None) as raw bits / bytes."""
+    q_out = index_normalize(index_q, dtype)
+    k_out = index_normalize(index_k, dtype)
+    cache = None
+    if index_k_cache is not None:
+        cache = np.array(_bits(index_k_cache), copy=True)
+        cache[index_slots_prefill(cu_seqlens, page_table)] = k_out
+    return q_out, k_out, cache

@@ -509,6 +509,63 @@ int oracle_mxfp8_quantize(const uint16_t* bf16, int64_t n, uint8_t* q, uint8_t* 
   return 0;
 }
 
+/* ---- index producer: L2 norm and storage cast ------------------------------
+ * [TRT] fuse_qkv_index_projection: MSA batches use a norm / RoPE /
+ * cache-insertion producer; [TRT] indexer_kv_dtype: index Q/K are stored
+ * "normalized", as bf16 or unscaled E4M3; [NEMO] select_blocks takes index
+ * tensors "post norm and RoPE".  The pages fix neither the norm's precision
+ * nor its summation order; the reading taken (the workloads' "L2-normalised per
+ * vector"): in IEEE binary32, s = sum over c = 0..127 in that order of x_c^2
+ * (each square exact in binary32: bf16 has 8 significant bits), r = sqrt(s),
+ * y_c = x_c / r (each correctly rounded), then one rounding of y_c to the
+ * storage type (bf16 or E4M3, nearest, ties to even).  A vector whose s is 0
+ * (all zero, or all squares below binary32's range) is stored as zeros.  RoPE
+ * is a rotation, so it leaves the L2 norm unchanged; the pages fix no RoPE
+ * variant and none is applied here. */
+
+/* bf16 nearest to the binary32 value f (ties to even): the two bf16 values
+ * around f (f with its low 16 bits cleared, and the next one away from zero)
+ * and their midpoint, compared in double (all exact). */
+static uint16_t bf16_round_from_f32(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u) /* inf or NaN: keep the class */
+    return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+  uint32_t lo_bits = u & 0xffff0000u, hi_bits = lo_bits + 0x10000u;
+  float lo, hi;
+  memcpy(&lo, &lo_bits, sizeof lo);
+  memcpy(&hi, &hi_bits, sizeof hi);
+  double a = fabs((double)f), mid = 0.5 * (fabs((double)lo) + fabs((double)hi));
+  if (a < mid) return (uint16_t)(lo_bits >> 16);
+  if (a > mid) return (uint16_t)(hi_bits >> 16);
+  return (uint16_t)((((lo_bits >> 16) & 1u) ? hi_bits : lo_bits) >> 16); /* tie: even */
+}
+
+/* Normalises n vectors of 128 bf16 values (raw bits) and stores them as bf16
+ * bits (dtype 0, out is uint16_t[n][128]) or E4M3 bytes (dtype 1, out is
+ * uint8_t[n][128]). */
+int oracle_index_normalize(const uint16_t* x, int64_t n, int dtype, void* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    const uint16_t* xv = x + i * OR_IDIM;
+    float s = 0.0f;
+    for (int c = 0; c < OR_IDIM; ++c) {
+      float v = (float)bf16_value(xv[c]);
+      float sq = v * v; /* exact */
+      s = s + sq;
+    }
+    float r = sqrtf(s);
+    for (int c = 0; c < OR_IDIM; ++c) {
+      float y = (s == 0.0f) ? 0.0f : (float)bf16_value(xv[c]) / r;
+      if (dtype == 0)
+        ((uint16_t*)out)[i * OR_IDIM + c] = bf16_round_from_f32(y);
+      else
+        ((uint8_t*)out)[i * OR_IDIM + c] = e4m3_encode((double)y);
+    }
+  }
+  return 0;
+}
+
 /* Decode selection for a list of requests.  q2k: [G][n][topk]; gap: [G][n];
  * s64_out (optional): [n][G][max_nb]. */
 int oracle_select_decode(const void* index_q, const void* index_k_cache, int dtype,
