@@ -462,7 +462,7 @@ double oracle_attend_loss_f64(const double* q, const double* k, const double* v,
  * 0x7F = NaN, largest finite 448) of y: nearest, ties to even mantissa,
  * saturating. */
 static uint8_t e4m3_encode(double y) {
-  uint8_t sign = y < 0 ? 0x80 : 0x00;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00; /* OCP E4M3 keeps the sign of zero */
   double a = fabs(y);
   if (a >= 448.0) return sign | 0x7E;
   int e;

@@ -116,3 +116,10 @@ def test_prefill_insertion_slots():
     pt = np.array([[2, -1], [0, 1]], np.int32)
     want = [256, 257, 258] + list(range(130))
     np.testing.assert_array_equal(oracle.index_slots_prefill(cu, pt), want)
+
+
+def test_negative_zero_elements_keep_their_sign():
+    # y = -0.0 / 5 = -0.0: bf16 0x8000, E4M3 0x80 (signed zeros of both formats)
+    x = _vec([3.0, 4.0, -0.0])
+    assert oracle.index_normalize(x)[2] == 0x8000 and oracle.index_normalize(x)[3] == 0
+    assert oracle.index_normalize(x, "e4m3")[2] == 0x80 and oracle.index_normalize(x, "e4m3")[3] == 0

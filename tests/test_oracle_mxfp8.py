@@ -67,3 +67,10 @@ def test_scale_rule_and_round_trip():
         ok = ~sat
         tol = np.maximum(np.abs(b[ok]) * 2.0 ** -4, 2.0 ** -10 * X) + 1e-300
         assert np.all(np.abs(deq[ok] - b[ok]) <= tol)
+
+
+def test_negative_zero_keeps_its_sign():
+    # OCP E4M3 has a signed zero: -0.0 encodes as S=1, E=0, M=0 (0x80), as PyTorch's cast does
+    q, s = _q([-0.0] * 32)
+    assert s.tolist() == [0] and q.tolist() == [0x80] * 32
+    assert torch.tensor([-0.0]).to(torch.float8_e4m3fn).view(torch.uint8).item() == 0x80
