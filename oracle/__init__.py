@@ -19,6 +19,10 @@ Which statement on the pages each function follows:
   * ``attend_prefill`` / ``attend_decode`` -- sparse GQA attention over the
     selected blocks: the TensorRT-LLM class description and NeMo
     ``sparse_attention`` / ``_SparseAttention.forward``.
+  * ``attend_decode_fp8`` -- the decode attention over an FP8 (E4M3) main K/V
+    cache with one dequantisation scale per cache (TensorRT-LLM field
+    fuse_qkv_index_projection: "an FP8 main KV cache"; the scale rule is a
+    reading, see the C source).
   * ``attend_prefill_backward`` -- gradients of the sparse attention (NeMo
     ``_SparseAttention.backward``: grad_out -> dq, dk, dv), written out from
     the forward; ``attend_loss_f64`` -- the forward on fp64 inputs reduced to
@@ -91,6 +95,7 @@ def _load():
             lib.oracle_attend_loss_f64.restype = Dbl
             lib.oracle_mxfp8_quantize.argtypes = [P, I64, P, P]
             lib.oracle_index_normalize.argtypes = [P, I64, I, P]
+            lib.oracle_attend_decode_fp8.argtypes = [P, P, P, Dbl, Dbl, P, P, P, I, P, I64, P, I, Dbl, P]
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = Dbl
             for f in (lib.oracle_select_prefill, lib.oracle_attend_prefill,
@@ -266,6 +271,27 @@ def attend_decode(q, k_cache, v_cache, seq_lens, q2k, scale, page_table=None, cu
     out = np.zeros((n, H, D), dtype=np.float64)
     lib.oracle_attend_decode(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(sl), _ptr(pt), _ptr(cuk), max_pages,
                              _ptr(req), n, _ptr(q2k), topk, float(scale), _ptr(out))
+    return out
+
+
+def attend_decode_fp8(q, k_cache, v_cache, seq_lens, q2k, scale, k_scale=1.0, v_scale=1.0, page_table=None,
+                      cu_seqlens_k=None, requests=None):
+    """fp64 out [n, H, D] over E4M3 K/V caches (raw bytes or float8_e4m3fn tensors) standing for
+    k_scale * k and v_scale * v, for the listed requests given their q2k rows [G, n, topk]."""
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    if kb.dtype != np.uint8 or vb.dtype != np.uint8:
+        raise TypeError("the K/V caches must be E4M3 bytes")
+    sl = _i32(seq_lens)
+    pt = None if page_table is None else _i32(page_table)
+    cuk = None if cu_seqlens_k is None else _i64(cu_seqlens_k)
+    req = _i64(np.arange(sl.shape[0]) if requests is None else requests)
+    n = req.shape[0]
+    q2k = _i32(q2k)
+    out = np.zeros((n, H, D), dtype=np.float64)
+    lib.oracle_attend_decode_fp8(_ptr(qb), _ptr(kb), _ptr(vb), float(k_scale), float(v_scale), _ptr(sl), _ptr(pt),
+                                 _ptr(cuk), 0 if pt is None else pt.shape[1], _ptr(req), n, _ptr(q2k), q2k.shape[2],
+                                 float(scale), _ptr(out))
     return out
 
 

@@ -621,6 +621,73 @@ int oracle_attend_decode(const uint16_t* q, const uint16_t* k_cache,
   return 0;
 }
 
+/* Decode attention over an FP8 main K/V cache ([TRT] fuse_qkv_index_projection:
+ * the MiniMax-M3 path uses "an FP8 main KV cache").  The pages give no scale
+ * rule; the reading taken: K and V are stored as E4M3 bytes and stand for
+ * k_scale * e4m3(k) and v_scale * e4m3(v), one fp32 scale per cache (1.0 =
+ * unscaled).  Everything else is step 3 above, in fp64. */
+static void attend_query_fp8(const uint16_t* q_row, const uint8_t* k, const uint8_t* v, double k_scale,
+                             double v_scale, const int64_t* key_row, int64_t pos, const int32_t* q2k_g,
+                             int64_t q2k_stride, int topk, double scale, double* out) {
+  int64_t nkeys_max = (int64_t)topk * OR_BLOCK;
+  int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)nkeys_max);
+  double* z = (double*)malloc(sizeof(double) * (size_t)nkeys_max);
+  for (int g = 0; g < OR_KV; ++g) {
+    int64_t nk = 0;
+    for (int i = 0; i < topk; ++i) {
+      int32_t b = q2k_g[g * q2k_stride + i];
+      if (b < 0) continue;
+      for (int64_t p = (int64_t)b * OR_BLOCK; p < (int64_t)(b + 1) * OR_BLOCK && p <= pos; ++p) keys[nk++] = p;
+    }
+    for (int hh = 0; hh < OR_HEADS / OR_KV; ++hh) {
+      int h = g * (OR_HEADS / OR_KV) + hh;
+      double* o = out + (int64_t)h * OR_DIM;
+      for (int c = 0; c < OR_DIM; ++c) o[c] = 0.0;
+      if (nk == 0) continue;
+      double zmax = -INFINITY;
+      for (int64_t j = 0; j < nk; ++j) {
+        int64_t row = key_row[keys[j]];
+        double acc = 0.0;
+        for (int c = 0; c < OR_DIM; ++c)
+          acc += bf16_value(q_row[h * OR_DIM + c]) * k_scale * oracle_e4m3_value(k[(row * OR_KV + g) * OR_DIM + c]);
+        z[j] = scale * acc;
+        if (z[j] > zmax) zmax = z[j];
+      }
+      double denom = 0.0;
+      for (int64_t j = 0; j < nk; ++j) {
+        z[j] = exp(z[j] - zmax);
+        denom += z[j];
+      }
+      for (int64_t j = 0; j < nk; ++j) {
+        int64_t row = key_row[keys[j]];
+        double w = z[j] / denom;
+        for (int c = 0; c < OR_DIM; ++c) o[c] += w * v_scale * oracle_e4m3_value(v[(row * OR_KV + g) * OR_DIM + c]);
+      }
+    }
+  }
+  free(keys);
+  free(z);
+}
+
+/* Decode attention over E4M3 K/V caches for a list of requests given q2k rows
+ * ([G][n][topk]).  out: [n][H][D] fp64. */
+int oracle_attend_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache, double k_scale,
+                             double v_scale, const int32_t* seq_lens, const int32_t* page_table,
+                             const int64_t* cu_seqlens_k, int max_pages, const int64_t* requests, int64_t n,
+                             const int32_t* q2k, int topk, double scale, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < n; ++i) {
+    int r = (int)requests[i];
+    int64_t len = seq_lens[r];
+    int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)len);
+    decode_rows(page_table, cu_seqlens_k, max_pages, r, len, rows);
+    attend_query_fp8(q + (int64_t)r * OR_HEADS * OR_DIM, k_cache, v_cache, k_scale, v_scale, rows, len - 1,
+                     q2k + i * topk, n * topk, topk, scale, out + i * OR_HEADS * OR_DIM);
+    free(rows);
+  }
+  return 0;
+}
+
 /* Packed layout of a document map ([NEMO] layout-from-doc_ids constructor and
  * _contiguous_runs): ids [batch][seq], 0 = padding, each positive id one
  * contiguous run within its row.  Documents are the runs in row-major order;

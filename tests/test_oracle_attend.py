@@ -190,3 +190,50 @@ def test_packed_doc_map_recipe():
     assert lens.min() >= 1 and mx <= 16384
     assert 32768 * 2 - 2048 <= cu[-1] <= 32768 * 2
     assert list(lens) == msa_synth.doc_lengths_from_map(ids)
+
+
+# ---- decode attention over an FP8 (E4M3) main K/V cache ----------------------
+
+def _fp8_case(seed=4, lens=(300, 1000, 129)):
+    d = msa_synth.decode_inputs(list(lens), paged=True, seed=seed)
+    k8 = (d.k_cache.float() * 0.5).to(torch.float8_e4m3fn)
+    v8 = (d.v_cache.float() * 0.5).to(torch.float8_e4m3fn)
+    q2k, _ = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table, topk=4)
+    return d, k8, v8, q2k
+
+
+def test_fp8_cache_equals_bf16_cache_of_the_same_values():
+    # every E4M3 value is exact in bf16: the FP8 attention with unit scales is the pinned bf16
+    # attention on the decoded values, to the last bit
+    d, k8, v8, q2k = _fp8_case()
+    a = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, q2k, SCALE, page_table=d.page_table)
+    b = oracle.attend_decode(d.q, k8.to(torch.bfloat16), v8.to(torch.bfloat16), d.seq_lens, q2k, SCALE,
+                             page_table=d.page_table)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_fp8_scales_are_exact_powers_of_two():
+    # scales 2 and 0.25 equal bf16 caches holding 2x and 0.25x the values (exact in bf16)
+    d, k8, v8, q2k = _fp8_case(seed=5)
+    a = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, q2k, SCALE, k_scale=2.0, v_scale=0.25,
+                                 page_table=d.page_table)
+    b = oracle.attend_decode(d.q, (k8.float() * 2).to(torch.bfloat16), (v8.float() * 0.25).to(torch.bfloat16),
+                             d.seq_lens, q2k, SCALE, page_table=d.page_table)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_fp8_zero_query_gives_the_scaled_mean_of_v():
+    # q = 0: equal weights, out = v_scale * the mean of the attended values
+    d, k8, v8, q2k = _fp8_case(seed=6, lens=(200,))
+    q = torch.zeros_like(d.q)
+    out = oracle.attend_decode_fp8(q, k8, v8, d.seq_lens, q2k, SCALE, k_scale=3.0, v_scale=1.5,
+                                   page_table=d.page_table)
+    v = v8.float().double().numpy()
+    pt = d.page_table.numpy()
+    L = int(d.seq_lens[0])
+    for g in range(4):
+        keys = [p for b in q2k[g, 0] if b >= 0 for p in range(128 * b, min(128 * b + 128, L))]
+        rows = [pt[0, p // 128] * 128 + p % 128 for p in keys]
+        want = 1.5 * v[rows, g, :].mean(axis=0)
+        for hh in range(16):
+            np.testing.assert_allclose(out[0, 16 * g + hh], want, rtol=1e-12, atol=1e-12)
