@@ -50,12 +50,12 @@ def _peaks():
 
 # ---- algorithmic work per step -------------------------------------------------------
 
-def decode_work(d, q2k, mxfp8=False):
+def decode_work(d, q2k, mxfp8=False, fp8_kv=False):
     """(bytes_select, bytes_attend).  Select: the index-K of every scored context
     once (contexts with nb <= topk keep every block and read nothing) plus the
-    index queries.  Attend: K and V of every attended key once per KV head, plus
-    q and out (bf16, or with ``mxfp8`` one E4M3 byte per element and one scale
-    byte per 32)."""
+    index queries.  Attend: K and V of every attended key once per KV head (2
+    bytes per element, or 1 with ``fp8_kv``), plus q and out (bf16, or with
+    ``mxfp8`` one E4M3 byte per element and one scale byte per 32)."""
     lens = d.seq_lens.cpu().numpy().astype(np.int64)
     nb = (lens + 127) // 128
     scored = nb > d.topk
@@ -68,7 +68,7 @@ def decode_work(d, q2k, mxfp8=False):
         k = np.minimum(128, lens[:, None] - 128 * blk)
         keys += int(np.where(blk >= 0, k, 0).sum())
     out_bytes = d.batch * 64 * 128 * (1 + 1 / 32 if mxfp8 else 2)
-    b_att = int(keys * 2 * 128 * 2 + d.batch * 64 * 128 * 2 + out_bytes)
+    b_att = int(keys * 2 * 128 * (1 if fp8_kv else 2) + d.batch * 64 * 128 * 2 + out_bytes)
     return b_sel, b_att
 
 
@@ -80,9 +80,6 @@ TRAFFIC = {
     "decode_b64_ctx4k_64k_paged": {"kernel": "select", "per": "algorithmic byte", "value": 1.0227,
                                    "capture": "ncu: decode_select_kernel<0>, first 16 requests of "
                                               "decode_b64_ctx4k_64k_paged"},
-    # bm_attend_kernel + bm_merge_kernel, 8192-token document: 4.134 GB DRAM / 462848 entries
-    "prefill_1doc_16k": {"kernel": "attend", "per": "entry", "value": 8931.0,
-                         "capture": "ncu: bm_attend_kernel + bm_merge_kernel, prefill_1doc_16k at half size"},
 }
 # bw_attend_kernel, 8192-token document: 0.604 GB DRAM / 462848 entries (scaled by entries)
 TRAFFIC_BACKWARD = {
@@ -298,7 +295,16 @@ def run_gpu(args, rank, world, device, name=None, steps=None):
             msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, topk=d.topk,
                                          init_blocks=d.init_blocks, local_blocks=d.local_blocks, q2k=q2k, **kw)
 
-        if args.mxfp8:
+        if args.fp8_kv:
+            # the main K / V caches as E4M3 (unit scales): the attention streams half the bytes
+            d.k_cache = d.k_cache.to(torch.float8_e4m3fn)
+            d.v_cache = d.v_cache.to(torch.float8_e4m3fn)
+
+            def att():
+                msa.msa_sparse_attend_decode_fp8kv(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE, out=out,
+                                                   **kw)
+            outs = [out]
+        elif args.mxfp8:
             out_q = torch.empty((d.batch, 64 * 128), dtype=torch.uint8, device=device)
             out_sc = torch.empty((d.batch, 64 * 128 // 32), dtype=torch.uint8, device=device)
 
@@ -331,7 +337,7 @@ def run_gpu(args, rank, world, device, name=None, steps=None):
         att()
         flush_l2(1)
     torch.cuda.synchronize()
-    work = decode_work(inp, q2k, args.mxfp8) if decode else prefill_work(inp, q2k)
+    work = decode_work(inp, q2k, args.mxfp8, args.fp8_kv) if decode else prefill_work(inp, q2k)
     entries = 0 if decode else prefill_entries(q2k)
 
     # The timed steps replay a CUDA graph of the step, the two C-ABI calls
@@ -422,7 +428,10 @@ def run_gpu(args, rank, world, device, name=None, steps=None):
             msa.msa_select_blocks_decode(diq, d.index_k_cache, dsl, topk=d.topk, init_blocks=d.init_blocks,
                                          local_blocks=d.local_blocks, q2k=q2k, max_blocks=d.max_blocks, **kw2)
             cur.wait_stream(side)
-            if args.mxfp8:
+            if args.fp8_kv:
+                msa.msa_sparse_attend_decode_fp8kv(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out=out,
+                                                   max_blocks=d.max_blocks, **kw2)
+            elif args.mxfp8:
                 msa.msa_sparse_attend_decode_mxfp8(dq, d.k_cache, d.v_cache, q2k, dsl, scale=SCALE, out_q=outs[0],
                                                    out_scale=outs[1], max_blocks=d.max_blocks, **kw2)
             else:
@@ -508,8 +517,12 @@ def cpu_baseline(name, seed, budget_s=15.0, inputs=None, gpu_q2k=None):
             q2k, gap = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table,
                                             cu_seqlens_k=d.cu_seqlens_k, requests=req, topk=d.topk,
                                             init=d.init_blocks, local=d.local_blocks)
-            oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, q2k, SCALE, page_table=d.page_table,
-                                 cu_seqlens_k=d.cu_seqlens_k, requests=req)
+            if d.k_cache.dtype == torch.float8_e4m3fn:
+                oracle.attend_decode_fp8(d.q, d.k_cache, d.v_cache, d.seq_lens, q2k, SCALE, page_table=d.page_table,
+                                         cu_seqlens_k=d.cu_seqlens_k, requests=req)
+            else:
+                oracle.attend_decode(d.q, d.k_cache, d.v_cache, d.seq_lens, q2k, SCALE, page_table=d.page_table,
+                                     cu_seqlens_k=d.cu_seqlens_k, requests=req)
             if gq is not None:
                 checked += q2k.shape[0] * q2k.shape[1]
                 differ += int((gq[:, req] != q2k).any(axis=2).sum())
@@ -569,6 +582,8 @@ def main():
                     help="keep only the first N requests of a decode workload (small profiling cases)")
     ap.add_argument("--mxfp8", action="store_true",
                     help="decode: emit the attention output as MXFP8 (E4M3 + E8M0 scales) instead of bf16")
+    ap.add_argument("--fp8-kv", action="store_true",
+                    help="decode: main K / V caches as E4M3 (msa_sparse_attend_decode_fp8kv, unit scales)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other headline workloads (measured after the bench workload at one GPU)")
     ap.add_argument("--backward", action="store_true",
@@ -586,10 +601,13 @@ def main():
     config = {"workload": args.workload, "desc": msa_synth.WORKLOADS[args.workload], "seed": args.seed}
     if args.requests:
         config["requests"] = args.requests
-    if args.mxfp8:
-        if not args.workload.startswith("decode"):
-            raise SystemExit("--mxfp8 applies to the decode attention")
-        config["output"] = "MXFP8: E4M3 values + one E8M0 scale per 32 elements"
+    if args.mxfp8 or args.fp8_kv:
+        if not args.workload.startswith("decode") or (args.mxfp8 and args.fp8_kv):
+            raise SystemExit("--mxfp8 and --fp8-kv apply (one at a time) to the decode attention")
+        if args.mxfp8:
+            config["output"] = "MXFP8: E4M3 values + one E8M0 scale per 32 elements"
+        else:
+            config["kv_cache"] = "E4M3 main K / V caches (unit scales)"
     if args.scale_down > 1:
         config["scale_down"] = args.scale_down
 
@@ -641,8 +659,6 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": summ["dtype"], "data": "synthetic", "config": config,
             "roofline": summ["roofline"], "e2e": summ["e2e"],
-            # decode: scorer + top-k + attention; prefill: plan + scorer, then geometry, count, scan,
-            # tiles, scatter, tensor-core attention and merge
             "gpu_launches": launches_per_step(res["decode"]) * args.steps, "clocks": res["clocks"]}
     if not args.no_cpu_baseline and world == 1:
         inputs, gpu_q2k = _host_copy(res["inputs"]), res["q2k"]
@@ -650,7 +666,8 @@ def main():
         del inputs
     # The other headline workloads, one GPU: each measured the same way (fewer steps), reported with its
     # step time, roofline fraction and end-to-end figure.
-    if world == 1 and not (args.no_workloads or args.mxfp8) and args.requests is None and args.scale_down == 1:
+    if world == 1 and not (args.no_workloads or args.mxfp8 or args.fp8_kv) and args.requests is None and \
+            args.scale_down == 1:
         extra = {}
         del res
         for name in EXTRA_WORKLOADS:
@@ -670,9 +687,9 @@ def main():
 
 def launches_per_step(decode):
     """The library's kernels in one step: decode scorer, top-k and attention;
-    prefill plan and scorer, then geometry, count, scan, tiles, scatter,
-    tensor-core attention and merge."""
-    return 3 if decode else 9
+    prefill plan and scorer, then geometry, count, scan, tiles, scatter, the
+    tensor-core attention's two phases and the normalisation."""
+    return 3 if decode else 10
 
 
 def summarize(res, args, ms, e2e_ms, world):
@@ -694,7 +711,8 @@ def summarize(res, args, ms, e2e_ms, world):
             traffic = round(tr["value"] * (b_sel if dom == "select" else b_att))
         roof = {"bound": "hbm",
                 "kernel": ("msa_select_blocks_decode (decode_select_kernel + decode_topk_kernel)" if dom == "select"
-                           else "msa_sparse_attend_decode (sparse_attend_kernel)"),
+                           else "msa_sparse_attend_decode (sparse_attend_kernel)" if not args.fp8_kv
+                           else "msa_sparse_attend_decode_fp8kv (sparse_attend_kernel<1>)"),
                 "achieved": round(ach, 1), "peak": res["hbm_peak"], "unit": "GB/s",
                 "frac": round(ach / res["hbm_peak"], 4), "traffic": traffic,
                 "traffic_source": tr["capture"] + " (scaled by algorithmic bytes)" if traffic else None,
@@ -703,7 +721,8 @@ def summarize(res, args, ms, e2e_ms, world):
                                "attend": {"ms": round(res["att_ms"], 4), "bytes": b_att, "GB/s": round(att_r, 1)},
                                "step_GB/s": round((b_sel + b_att) / (ms * 1e-3) / 1e9, 1),
                                "step_frac": round((b_sel + b_att) / (ms * 1e-3) / 1e9 / res["hbm_peak"], 4)}}
-        dtype = "bf16" if "e4m3" not in name else "e4m3-index/bf16"
+        dtype = ("bf16" if "e4m3" not in name else "e4m3-index/bf16") if not args.fp8_kv else \
+            ("bf16-index/e4m3-kv" if "e4m3" not in name else "e4m3-index/e4m3-kv")
     else:
         fp8_index = "e4m3" in name
         f_sel, f_att = res["work"]
@@ -716,7 +735,8 @@ def summarize(res, args, ms, e2e_ms, world):
             traffic = round(tr["value"] * res["entries"])
         roof = {"bound": "tensor",
                 "kernel": ("msa_select_blocks_prefill (prefill_plan_kernel + prefill_select_kernel)" if dom == "select"
-                           else "msa_sparse_attend_prefill (bucketing, bm_attend_kernel, bm_merge_kernel)"),
+                           else "msa_sparse_attend_prefill (bucketing, bm_attend_kernel reference and "
+                                "accumulate phases, bm_norm_kernel)"),
                 "achieved": round(ach, 2), "peak": res["tf_peak"], "unit": "TFLOP/s",
                 "frac": round(ach / res["tf_peak"], 4), "traffic": traffic,
                 "traffic_source": tr["capture"] + " (scaled by entries)" if traffic else None,

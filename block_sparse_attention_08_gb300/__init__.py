@@ -13,11 +13,14 @@ from .binding import (  # noqa: F401
     load,
     make_config,
     msa_check_bounded_wait,
+    msa_index_produce_decode,
+    msa_index_produce_prefill,
     msa_pack,
     msa_pack_metadata,
     msa_select_blocks_decode,
     msa_select_blocks_prefill,
     msa_sparse_attend_decode,
+    msa_sparse_attend_decode_fp8kv,
     msa_sparse_attend_decode_mxfp8,
     msa_sparse_attend_prefill,
     msa_sparse_attend_prefill_backward,

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmsa.so")
 SOURCES = ["abi.cu", "decode_select.cu", "sparse_attend.cu", "prefill_select.cu", "prefill_attend.cu", "pack.cu",
-           "diag.cu"]
+           "diag.cu", "index_produce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

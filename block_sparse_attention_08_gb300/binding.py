@@ -22,7 +22,8 @@ MSA_ERR_CUDA = 6  # msa_status for a failed CUDA call
 MODE_DECODE, MODE_PREFILL, MODE_PACK, MODE_PREFILL_BWD = 0, 1, 2, 3
 INDEX_DTYPES = {"bf16": 0, "e4m3": 1}
 DEVICE_ERRORS = {0: "none", 1: "page id outside the pool", 2: "block id outside the query's range",
-                 3: "sequence length out of range", 4: "bounded on-chip wait gave up"}
+                 3: "sequence length out of range", 4: "bounded on-chip wait gave up",
+                 5: "prefill attention score outside the fixed-reference range"}
 
 
 class MsaError(RuntimeError):
@@ -51,6 +52,7 @@ _SIGS = {
     "msa_select_blocks_decode": [CFG, P, P, P, P, P, I, I, I64, P, P, SZ, P],
     "msa_sparse_attend_decode": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, SZ, P],
     "msa_sparse_attend_decode_mxfp8": [CFG, P, P, P, P, P, P, P, I, I, I64, F, P, P, P, SZ, P],
+    "msa_sparse_attend_decode_fp8kv": [CFG, P, P, P, F, F, P, P, P, P, I, I, I64, F, P, P, SZ, P],
     "msa_select_blocks_prefill": [CFG, P, P, P, I, I64, I, P, P, SZ, P],
     "msa_sparse_attend_prefill": [CFG, P, P, P, P, P, I, I64, I, F, P, P, SZ, P],
     "msa_sparse_attend_prefill_lse": [CFG, P, P, P, P, P, I, I64, I, F, P, P, P, SZ, P],
@@ -60,6 +62,8 @@ _SIGS = {
     "msa_pack": [P, P, I64, I64, P, P],
     "msa_unpack": [P, P, I64, I64, I64, P, P],
     "msa_check_bounded_wait": [P, P, ctypes.POINTER(I64)],
+    "msa_index_produce_prefill": [CFG, P, P, P, I, I64, P, P, P, P, I, I64, P, SZ, P],
+    "msa_index_produce_decode": [CFG, P, P, P, P, P, I, I, I64, P, P, P, SZ, P],
 }
 EXPORTS = tuple(_SIGS) + ("msa_status_string", "msa_last_cuda_error", "msa_cuda_error_string")
 
@@ -279,6 +283,39 @@ def msa_sparse_attend_decode_mxfp8(q, k_cache, v_cache, q2k, seq_lens, page_tabl
     return out_q, out_scale
 
 
+def msa_sparse_attend_decode_fp8kv(q, k_cache, v_cache, q2k, seq_lens, page_table=None, cu_seqlens_k=None, *,
+                                   k_scale=1.0, v_scale=1.0, max_blocks=None, scale=None, out=None,
+                                   workspace=None):
+    """bf16 out [batch, 64, 128] over FP8 (E4M3) K/V caches standing for k_scale * k and
+    v_scale * v (C: msa_sparse_attend_decode_fp8kv)."""
+    B = q.shape[0]
+    _need(q, "q", torch.bfloat16, (B, H, D))
+    _need(k_cache, "k_cache", (torch.float8_e4m3fn, torch.uint8), (None, G, D))
+    _need(v_cache, "v_cache", k_cache.dtype, tuple(k_cache.shape))
+    _need(q2k, "q2k", torch.int32, (G, B, None))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32, (B, None))
+        mb = page_table.shape[1]
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int64, (B + 1,))
+        mb = max_blocks
+    if mb is None:
+        raise ValueError("max_blocks is required with a contiguous cache")
+    cfg = make_config(q2k.shape[2], 0, 0)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B, H, D))
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    ws = _workspace("decode", workspace_size(cfg, MODE_DECODE, B, mb), dev, workspace)
+    _call("msa_sparse_attend_decode_fp8kv", ctypes.byref(cfg), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          float(k_scale), float(v_scale), _ptr(q2k), _ptr(seq_lens), _ptr(page_table),
+          _ptr(cu_seqlens_k if page_table is None else None), B, mb, k_cache.shape[0], scale, _ptr(out),
+          _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return out
+
+
 # ---- prefill ----------------------------------------------------------------------
 
 def msa_select_blocks_prefill(index_q, index_k, cu_seqlens, max_seqlen, *, topk=16, init_blocks=0,
@@ -390,6 +427,75 @@ def sparse_attention(q, k, v, q2k, cu_seqlens, max_seqlen, *, scale=None):
     [tokens, 64, 128]; q, k and v receive gradients through the library's backward."""
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     return _SparseAttention.apply(q, k, v, q2k, cu_seqlens, int(max_seqlen), scale)
+
+
+# ---- index producer -----------------------------------------------------------------
+
+_INDEX_TORCH = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+
+
+def _produce_ws(device, workspace):
+    return _workspace("produce", 256, device, workspace)
+
+
+def msa_index_produce_prefill(index_q, index_k, cu_seqlens, *, index_dtype="bf16", index_k_cache=None,
+                              page_table=None, q_out=None, k_out=None, write_k_out=True, workspace=None):
+    """Normalised index tensors for a packed prefill (C: msa_index_produce_prefill): returns
+    (index_q_out [T, 4, 128], index_k_out [T, 1, 128] or None) in ``index_dtype``; with
+    ``index_k_cache`` and ``page_table`` ([docs, max_blocks]) every token's key is also
+    written into the paged cache."""
+    T = index_q.shape[0]
+    _need(index_q, "index_q", torch.bfloat16, (T, G, DI))
+    _need(index_k, "index_k", torch.bfloat16, (T, 1, DI))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (None,))
+    dt = _INDEX_TORCH[index_dtype]
+    cfg = make_config(index_dtype=index_dtype)
+    dev = index_q.device
+    q_out = torch.empty((T, G, DI), dtype=dt, device=dev) if q_out is None else q_out
+    _need(q_out, "q_out", dt, (T, G, DI))
+    if write_k_out:
+        k_out = torch.empty((T, 1, DI), dtype=dt, device=dev) if k_out is None else k_out
+        _need(k_out, "k_out", dt, (T, 1, DI))
+    else:
+        k_out = None
+    mb, ns = 0, 0
+    if index_k_cache is not None:
+        _need(index_k_cache, "index_k_cache", dt, (None, 1, DI))
+        _need(page_table, "page_table", torch.int32, (cu_seqlens.shape[0] - 1, None))
+        mb, ns = page_table.shape[1], index_k_cache.shape[0]
+    ws = _produce_ws(dev, workspace)
+    _call("msa_index_produce_prefill", ctypes.byref(cfg), _ptr(index_q), _ptr(index_k), _ptr(cu_seqlens),
+          cu_seqlens.shape[0] - 1, T, _ptr(q_out), _ptr(k_out), _ptr(index_k_cache), _ptr(page_table), mb, ns,
+          _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return q_out, k_out
+
+
+def msa_index_produce_decode(index_q, index_k, index_k_cache, seq_lens, page_table=None, cu_seqlens_k=None, *,
+                             max_blocks=None, q_out=None, workspace=None):
+    """Normalised index queries [batch, 4, 128] in the cache's dtype, with each request's new
+    normalised key written into ``index_k_cache`` at the slot of position seq_lens[r] - 1
+    (C: msa_index_produce_decode)."""
+    B = index_q.shape[0]
+    _need(index_q, "index_q", torch.bfloat16, (B, G, DI))
+    _need(index_k, "index_k", torch.bfloat16, (B, 1, DI))
+    dtn = _index_dtype(index_k_cache)
+    _need(index_k_cache, "index_k_cache", index_k_cache.dtype, (None, 1, DI))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32, (B, None))
+        mb = page_table.shape[1]
+    else:
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int64, (B + 1,))
+        mb = max_blocks if max_blocks is not None else 1
+    cfg = make_config(index_dtype=dtn)
+    dev = index_q.device
+    q_out = torch.empty((B, G, DI), dtype=index_k_cache.dtype, device=dev) if q_out is None else q_out
+    _need(q_out, "q_out", index_k_cache.dtype, (B, G, DI))
+    ws = _produce_ws(dev, workspace)
+    _call("msa_index_produce_decode", ctypes.byref(cfg), _ptr(index_q), _ptr(index_k), _ptr(seq_lens),
+          _ptr(page_table), _ptr(cu_seqlens_k if page_table is None else None), B, mb, index_k_cache.shape[0],
+          _ptr(q_out), _ptr(index_k_cache), _ptr(ws.buf), ws.nbytes, _stream(dev))
+    return q_out
 
 
 # ---- packing ----------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points of libmsa: argument validation,
 // workspace layout and kernel launches.  Declarations and contracts are in
 // include/msa.h.
+#include <cmath>
 #include <mutex>
 
 #include "launch.h"
@@ -198,7 +199,8 @@ static msa_status attend_decode(const msa_config* cfg, const void* q, const void
                                 const int32_t* q2k, const int32_t* seq_lens, const int32_t* page_table,
                                 const int64_t* cu_seqlens_k, int batch, int max_blocks, int64_t num_slots,
                                 float scale, void* out, uint8_t* out_q, uint8_t* out_scale, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+                                size_t workspace_bytes, void* stream, int kv_fp8 = 0, float k_scale = 1.f,
+                                float v_scale = 1.f) {
   msa_status st = msa_config_check(cfg);
   if (st != MSA_OK) return st;
   if (!q || !k_cache || !v_cache || !q2k || (!out && !(out_q && out_scale))) return MSA_ERR_NULL;
@@ -216,7 +218,8 @@ static msa_status attend_decode(const msa_config* cfg, const void* q, const void
   AttnGeom geo{batch, seq_lens, page_table, cu_seqlens_k, max_blocks, num_slots};
   cudaError_t e = launch_sparse_attend(geo, q, k_cache, v_cache, q2k, cfg->topk, scale, out, out_q, out_scale,
                                        reinterpret_cast<float*>(ws + L.partials),
-                                       reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s);
+                                       reinterpret_cast<int*>(ws + L.att_tickets), reinterpret_cast<DevError*>(ws), s,
+                                       kv_fp8, k_scale, v_scale);
   return cuda_result(e);
 }
 
@@ -238,6 +241,20 @@ msa_status msa_sparse_attend_decode_mxfp8(const msa_config* cfg, const void* q, 
   return attend_decode(cfg, q, k_cache, v_cache, q2k, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
                        num_slots, scale, nullptr, static_cast<uint8_t*>(out_q), static_cast<uint8_t*>(out_scale),
                        workspace, workspace_bytes, stream);
+}
+
+msa_status msa_sparse_attend_decode_fp8kv(const msa_config* cfg, const void* q, const void* k_cache,
+                                          const void* v_cache, float k_scale, float v_scale, const int32_t* q2k,
+                                          const int32_t* seq_lens, const int32_t* page_table,
+                                          const int64_t* cu_seqlens_k, int batch, int max_blocks,
+                                          int64_t num_slots, float scale, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  if (!out) return MSA_ERR_NULL;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return MSA_ERR_SHAPE;
+  return attend_decode(cfg, q, k_cache, v_cache, q2k, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
+                       num_slots, scale, out, nullptr, nullptr, workspace, workspace_bytes, stream, 1, k_scale,
+                       v_scale);
 }
 
 static msa_status check_prefill_geom(const int32_t* cu_seqlens, int num_docs, int64_t total_tokens, int max_seqlen) {
@@ -324,6 +341,69 @@ msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void*
                                           scale, out, lse, grad_out, dq, dk, dv, ws + L.bm,
                                           reinterpret_cast<DevError*>(ws), static_cast<cudaStream_t>(stream));
   return cuda_result(e);
+}
+
+msa_status msa_index_produce_prefill(const msa_config* cfg, const void* index_q_in, const void* index_k_in,
+                                     const int32_t* cu_seqlens, int num_docs, int64_t total_tokens, void* index_q_out,
+                                     void* index_k_out, void* index_k_cache, const int32_t* page_table, int max_blocks,
+                                     int64_t num_slots, void* workspace, size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!index_q_in || !index_k_in || !cu_seqlens || !index_q_out || (!index_k_out && !index_k_cache))
+    return MSA_ERR_NULL;
+  if (index_k_cache && !page_table) return MSA_ERR_NULL;
+  if (num_docs < 1 || total_tokens < 1 || total_tokens >= (1LL << 31) || num_docs > total_tokens)
+    return MSA_ERR_SHAPE;
+  if (index_k_cache && (max_blocks < 1 || num_slots < 1 || num_slots >= (1LL << 31) || num_slots % kBlock))
+    return MSA_ERR_SHAPE;
+  if (!aligned16(index_q_in) || !aligned16(index_k_in) || !aligned16(index_q_out) ||
+      (index_k_out && !aligned16(index_k_out)) || (index_k_cache && !aligned16(index_k_cache)))
+    return MSA_ERR_ALIGN;
+  if ((st = check_ws(workspace, workspace_bytes, kHeaderBytes)) != MSA_OK) return st;
+  IpLaunch L{};
+  L.q_in = index_q_in;
+  L.k_in = index_k_in;
+  L.n = total_tokens;
+  L.q_out = index_q_out;
+  L.k_out = index_k_out;
+  L.cache = index_k_cache;
+  L.num_slots = num_slots;
+  L.e4m3 = cfg->index_dtype == MSA_INDEX_E4M3;
+  L.decode = 0;
+  L.cu = cu_seqlens;
+  L.num_docs = num_docs;
+  L.page_table = page_table;
+  L.max_blocks = max_blocks;
+  L.err = static_cast<DevError*>(workspace);
+  return cuda_result(launch_index_produce(L, static_cast<cudaStream_t>(stream)));
+}
+
+msa_status msa_index_produce_decode(const msa_config* cfg, const void* index_q_in, const void* index_k_in,
+                                    const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                    int batch, int max_blocks, int64_t num_slots, void* index_q_out,
+                                    void* index_k_cache, void* workspace, size_t workspace_bytes, void* stream) {
+  msa_status st = msa_config_check(cfg);
+  if (st != MSA_OK) return st;
+  if (!index_q_in || !index_k_in || !index_q_out || !index_k_cache) return MSA_ERR_NULL;
+  if ((st = check_decode_geom(seq_lens, page_table, cu_seqlens_k, batch, max_blocks, num_slots)) != MSA_OK) return st;
+  if (!aligned16(index_q_in) || !aligned16(index_k_in) || !aligned16(index_q_out) || !aligned16(index_k_cache))
+    return MSA_ERR_ALIGN;
+  if ((st = check_ws(workspace, workspace_bytes, kHeaderBytes)) != MSA_OK) return st;
+  IpLaunch L{};
+  L.q_in = index_q_in;
+  L.k_in = index_k_in;
+  L.n = batch;
+  L.q_out = index_q_out;
+  L.cache = index_k_cache;
+  L.num_slots = num_slots;
+  L.e4m3 = cfg->index_dtype == MSA_INDEX_E4M3;
+  L.decode = 1;
+  L.seq_lens = seq_lens;
+  L.page_table = page_table;
+  L.cu_k = cu_seqlens_k;
+  L.max_blocks = max_blocks;
+  L.err = static_cast<DevError*>(workspace);
+  return cuda_result(launch_index_produce(L, static_cast<cudaStream_t>(stream)));
 }
 
 msa_status msa_pack_metadata(const int64_t* doc_ids, int batch, int seq, int32_t* cu_seqlens, int64_t* token_rows,

@@ -24,10 +24,11 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
                                  DevError* err, cudaStream_t stream);
+// kv_fp8: the K / V caches hold E4M3 bytes standing for k_scale * k and v_scale * v.
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.f, float v_scale = 1.f);
 size_t attend_partials_bytes();
 size_t attend_tickets_bytes();
 size_t prefill_plan_ints(int num_docs, int max_tiles);
@@ -47,6 +48,26 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
                                     const void* grad_out, void* dq, void* dk, void* dv, uint8_t* region,
                                     DevError* err, cudaStream_t stream);
 size_t pack_workspace_bytes(int batch, int seq);
+// One index-producer call: n tokens (prefill) or requests (decode).
+struct IpLaunch {
+  const void* q_in;           // bf16 [n, 4, 128]
+  const void* k_in;           // bf16 [n, 1, 128]
+  long long n;
+  void* q_out;                // [n, 4, 128] in the index dtype
+  void* k_out;                // packed [n, 1, 128] in the index dtype, or null
+  void* cache;                // paged / contiguous index-K cache [num_slots, 1, 128], or null
+  long long num_slots;
+  int e4m3;
+  int decode;                 // 1: request r's new key sits at position seq_lens[r] - 1
+  const int32_t* cu;          // prefill: [num_docs + 1]
+  int num_docs;
+  const int32_t* seq_lens;    // decode: [n]
+  const int32_t* page_table;  // [n or num_docs, max_blocks], or null
+  const int64_t* cu_k;        // decode, contiguous cache: [n + 1]
+  int max_blocks;
+  DevError* err;
+};
+cudaError_t launch_index_produce(const IpLaunch& L, cudaStream_t stream);
 // First step of every launcher.  Clears the calling thread's last CUDA error
 // (the launches are checked with cudaGetLastError, which reports the calling
 // thread's error) and makes the current device's primary context current on

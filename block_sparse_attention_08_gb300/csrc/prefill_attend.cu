@@ -80,12 +80,11 @@ struct BmSmem {
   alignas(1024) uint8_t q[kBmQStages][kBmTile];
   alignas(1024) uint8_t k[kBmKStages][kBmTile];
   alignas(1024) uint8_t v[kBmVStages][kBmTile];
-  alignas(1024) uint8_t ostage[2][kBmTile];  // per epilogue warpgroup: 128 rows x 128 fp16, two 64-dim halves
+  alignas(1024) uint8_t ostage[2][kBmTile];  // 8 KB of fp32 staging per epilogue warp (two 4 KB halves)
   uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full[kBmKStages], k_empty[kBmKStages];
   uint64_t v_full[kBmVStages], v_empty[kBmVStages];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
   uint64_t p_full[2], done_s, done_o;
-  uint64_t stage_free[2], stage_full[2];  // per epilogue warpgroup: staging tile free / written
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -119,17 +118,21 @@ static BmDims bm_dims(long long T, int max_seqlen, int topk) {
   // smaller one.
   d.kg_max = (T + 255) / 256 * mb + T + 1;
   d.entries = static_cast<long long>(kKvHeads) * T * topk;
-  const long long keys = kKvHeads * d.kg_max;
+  // two phases of keys (the forward's reference entries, then the rest; the
+  // backward uses the first only), each key's last tile possibly partial
+  const long long keys = 2 * kKvHeads * d.kg_max;
   d.tiles_max = d.entries / kBmEntries + (keys < d.entries ? keys : d.entries) + 1;
   return d;
 }
 
-// Carving of the prefill-attention part of the workspace.
+// Carving of the prefill-attention part of the workspace.  Keys: (phase, KV
+// head, window, global block); phase 0 holds each (query, KV head) row's
+// reference entry (the forward only), phase 1 the others.
 struct BmPlan {
-  int* meta;       // [0] keys per KV head (Kg), [1] tiles
-  int* counts;     // [4 * kg_max] entries per key
-  int* offs;       // [4 * kg_max + 1] first entry of each key
-  int* toff;       // [4 * kg_max + 1] first tile of each key
+  int* meta;       // [0] keys per KV head (Kg), [1] tiles, [2] first tile of phase 1
+  int* counts;     // [2 * 4 * kg_max] entries per key
+  int* offs;       // [2 * 4 * kg_max + 1] first entry of each key
+  int* toff;       // [2 * 4 * kg_max + 1] first tile of each key
   int* blk_base;   // [T + 1] first global block of each document
   int* wlo;        // [nw] first global block a window can reach
   int* wbase;      // [nw + 1] first key of each window (per KV head)
@@ -137,21 +140,27 @@ struct BmPlan {
   int* erank;      // [entries] rank of the entry inside its key
   int* elist;      // [entries] bucketed entries: t * topk + j
   BmTile* tiles;   // [tiles_max]
-  __half* po;      // [entries][16][128] partial O / 128 (O = sum_k p_k v_k, unnormalised)
-  float2* pml;     // [entries][16] partial (row max in log2 units, row sum of p)
+  int phases;      // 2: the forward's reference split; 1: one phase (the backward)
+  // the forward's accumulators, per (token, query head):
+  float* acc;      // [T][64][128] unnormalised O = sum_p 2^(s_p - mref) v_p
+  float* mref;     // [T][64] the reference exponent: the row max over its reference block
+  float* lacc;     // [T][64] sum_p 2^(s_p - mref); 0 for a row with no key
 };
 
 static size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
-static size_t bm_carve(const BmDims& d, uint8_t* base, BmPlan* p) {
+// The bucketing arrays (shared by the forward and the backward), then, with
+// `outputs`, the forward's accumulators.
+static size_t bm_carve(const BmDims& d, uint8_t* base, BmPlan* p, bool outputs = true) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     uint8_t* ptr = base ? base + off : nullptr;
     off += al256(bytes);
     return ptr;
   };
-  const size_t keys = static_cast<size_t>(kKvHeads) * d.kg_max;
-  BmPlan q;
+  const size_t keys = 2 * static_cast<size_t>(kKvHeads) * d.kg_max;
+  BmPlan q{};
+  q.phases = 2;
   q.meta = reinterpret_cast<int*>(take(4 * sizeof(int)));
   q.counts = reinterpret_cast<int*>(take(keys * sizeof(int)));
   q.offs = reinterpret_cast<int*>(take((keys + 1) * sizeof(int)));
@@ -163,8 +172,11 @@ static size_t bm_carve(const BmDims& d, uint8_t* base, BmPlan* p) {
   q.erank = reinterpret_cast<int*>(take(d.entries * sizeof(int)));
   q.elist = reinterpret_cast<int*>(take(d.entries * sizeof(int)));
   q.tiles = reinterpret_cast<BmTile*>(take(d.tiles_max * sizeof(BmTile)));
-  q.po = reinterpret_cast<__half*>(take(d.entries * kGroup * kDim * sizeof(__half)));
-  q.pml = reinterpret_cast<float2*>(take(d.entries * kGroup * sizeof(float2)));
+  if (outputs) {
+    q.acc = reinterpret_cast<float*>(take(static_cast<size_t>(d.T) * kHeads * kDim * sizeof(float)));
+    q.mref = reinterpret_cast<float*>(take(static_cast<size_t>(d.T) * kHeads * sizeof(float)));
+    q.lacc = reinterpret_cast<float*>(take(static_cast<size_t>(d.T) * kHeads * sizeof(float)));
+  }
   if (p) *p = q;
   return off;
 }
@@ -304,12 +316,26 @@ __global__ void __launch_bounds__(256) bm_count_kernel(const int32_t* __restrict
   }
   const long long e0 = idx * topk;  // == (g * T + t) * topk
   const unsigned lt = (1u << lane) - 1u;
+  // With two phases, the row's reference entry -- its highest valid block,
+  // first occurrence -- goes to phase 0 and the other entries to phase 1.
+  int ref_j = -1;
+  if (live && p.phases == 2) {
+    int best = -1;
+    for (int j = 0; j < topk; ++j) {
+      const int b = q2k[e0 + j];
+      if (b >= 0 && b < nb && b > best) {
+        best = b;
+        ref_j = j;
+      }
+    }
+  }
+  const int phase1 = kKvHeads * Kg;  // first key of phase 1
   for (int j = 0; j < topk; ++j) {
     int key = -1;
     if (live) {
       const int b = q2k[e0 + j];
       if (b >= nb) record_error(err, MSA_DEVERR_BLOCK, e0 + j);
-      else if (b >= 0) key = kbase + gb0 + b;
+      else if (b >= 0) key = kbase + gb0 + b + (p.phases == 2 && j != ref_j ? phase1 : 0);
     }
     const unsigned grp = __match_any_sync(0xffffffffu, key);
     const int leader = __ffs(grp) - 1;
@@ -328,7 +354,7 @@ __global__ void __launch_bounds__(256) bm_count_kernel(const int32_t* __restrict
 __global__ void __launch_bounds__(1024) bm_scan_kernel(BmPlan p) {
   __shared__ long long sh[32];
   const int tid = threadIdx.x;
-  const long long K = static_cast<long long>(kKvHeads) * p.meta[0];
+  const long long K = static_cast<long long>(p.phases) * kKvHeads * p.meta[0];
   const long long per = (K + 1023) / 1024;
   const long long k0 = min(K, tid * per), k1 = min(K, k0 + per);
   long long se = 0, st = 0;
@@ -347,10 +373,12 @@ __global__ void __launch_bounds__(1024) bm_scan_kernel(BmPlan p) {
     re += c;
     rt += (c + kBmEntries - 1) / kBmEntries;
   }
+  __syncthreads();
   if (tid == 0) {
     p.offs[K] = static_cast<int>(te);
     p.toff[K] = static_cast<int>(tt);
     p.meta[1] = static_cast<int>(tt);
+    p.meta[2] = p.phases == 2 ? p.toff[K / 2] : static_cast<int>(tt);
   }
 }
 
@@ -360,10 +388,11 @@ __global__ void __launch_bounds__(256) bm_tiles_kernel(const int32_t* __restrict
                                                        BmPlan p) {
   const long long key = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int Kg = p.meta[0];
-  if (key >= static_cast<long long>(kKvHeads) * Kg) return;
+  if (key >= static_cast<long long>(p.phases) * kKvHeads * Kg) return;
   const int c = p.counts[key];
   if (c == 0) return;
-  const int g = static_cast<int>(key / Kg), kk = static_cast<int>(key - static_cast<long long>(g) * Kg);
+  const long long kh = key % (static_cast<long long>(kKvHeads) * Kg);  // the key within its phase
+  const int g = static_cast<int>(kh / Kg), kk = static_cast<int>(kh - static_cast<long long>(g) * Kg);
   const int w = last_le(p.wbase, nw, kk);
   const int gb = p.wlo[w] + kk - p.wbase[w];
   const int d = last_le(p.blk_base, num_docs, gb);
@@ -435,12 +464,13 @@ __device__ __forceinline__ void stg128(void* p, uint32_t a, uint32_t b, uint32_t
 
 __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap pmap, BmPlan p, long long T,
-    int topk, float scale_log2, DevError* err) {
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap amap, BmPlan p, long long T,
+    int topk, float scale_log2, int phase, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   BmSmem& sm = *reinterpret_cast<BmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = local_tiles(p.meta[1]);  // tiles of this CTA
+  const int t_lo = phase ? p.meta[2] : 0, t_hi = phase ? p.meta[1] : p.meta[2];  // this phase's tiles
+  const int n = local_tiles(t_hi - t_lo);  // tiles of this CTA
 
   if (tid == 0) {
     for (int i = 0; i < kBmQStages; ++i) {
@@ -465,10 +495,6 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
       mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.stage_free[i], 1);
-      mbar_init(&sm.stage_full[i], 4);
     }
     mbar_init(&sm.done_s, 1);
     mbar_init(&sm.done_o, 1);
@@ -499,9 +525,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       prefetch_tmap(&vmap);
     }
     const BmTile none{-1, -1, 0, 0};
-    BmTile d_next = n > 0 ? p.tiles[tile_at(0)] : none;
+    BmTile d_next = n > 0 ? p.tiles[t_lo + tile_at(0)] : none;
     int e_next = lane < d_next.cnt ? p.elist[d_next.off + lane] : 0;
-    BmTile d_after = n > 1 ? p.tiles[tile_at(1)] : none;
+    BmTile d_after = n > 1 ? p.tiles[t_lo + tile_at(1)] : none;
     int prow = -1, pg = -1;
     int nkf = 0, nvf = 0;  // K and V fills issued (lane 0)
     int i = 0;
@@ -510,7 +536,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const int ent = e_next;
       d_next = d_after;
       e_next = (i + 1 < n && lane < d_next.cnt) ? p.elist[d_next.off + lane] : 0;
-      d_after = i + 2 < n ? p.tiles[tile_at(i + 2)] : none;
+      d_after = i + 2 < n ? p.tiles[t_lo + tile_at(i + 2)] : none;
       const bool fresh = d.row0 != prow || d.g != pg;
       // publish the tile
       const int is = i % kBmInfo;
@@ -657,7 +683,6 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const int wg = warp >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
     const uint32_t srow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 128;
-    const long long per_head = T * topk;
     for (int i = wg; i < n; i += 2) {
       const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 723))) break;
@@ -667,42 +692,47 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       const long long t = ent / topk;
+      const long long row = t * kHeads + g * kGroup + h;  // (token, query head) accumulator row
       const int nkeys = valid ? static_cast<int>(min(static_cast<long long>(kBlock), t - row0 + 1)) : 0;
+      // phase 1: the row's exponent reference, requested before the wait for S
+      const float mr = phase && valid ? __ldcg(p.mref + row) : 0.f;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, 720))) break;
       tc::fence_after();
       // Rows whose keys are all causal (every block but the diagonal one) skip
-      // the per-key mask.  P is produced as p / 128 (the exponent is lowered by
-      // 7), so the O MMA writes O / 128 and the epilogue only converts.
+      // the per-key mask.
       const bool masked = !__all_sync(0xffffffffu, nkeys >= kBlock);
-      float mx = -INFINITY, l = 0.f;
-      auto softmax_rows = [&](auto mask_tag) -> bool {
+      float mu = 0.f, l = 0.f;
+      auto softmax_rows = [&](auto mask_tag) {
         constexpr bool kMask = decltype(mask_tag)::value;
-        // pass 1: row max (eight independent chains)
-        float m8[8];
+        if (phase == 0) {
+          // pass 1: row max (eight independent chains)
+          float m8[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
+          for (int q = 0; q < 8; ++q) m8[q] = -INFINITY;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t v[32];
-          tc::ld_32x32b_x32(srow + ch * 32, v);
-          tc::wait_ld();
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t v[32];
+            tc::ld_32x32b_x32(srow + ch * 32, v);
+            tc::wait_ld();
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float xa = __uint_as_float(v[2 * q]), xb = __uint_as_float(v[2 * q + 1]);
-            if (kMask) {
-              xa = ch * 32 + 2 * q < nkeys ? xa : -INFINITY;
-              xb = ch * 32 + 2 * q + 1 < nkeys ? xb : -INFINITY;
+            for (int q = 0; q < 16; ++q) {
+              float xa = __uint_as_float(v[2 * q]), xb = __uint_as_float(v[2 * q + 1]);
+              if (kMask) {
+                xa = ch * 32 + 2 * q < nkeys ? xa : -INFINITY;
+                xb = ch * 32 + 2 * q + 1 < nkeys ? xb : -INFINITY;
+              }
+              m8[q & 7] = fmax3(m8[q & 7], xa, xb);
             }
-            m8[q & 7] = fmax3(m8[q & 7], xa, xb);
           }
+          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          // scale > 0, so the max of the scaled scores is the scaled max
+          mu = mx == -INFINITY ? 0.f : mx * scale_log2;
+        } else {
+          mu = mr;
         }
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        // scale > 0, so the max of the scaled scores is the scaled max
-        const float mu = mx == -INFINITY ? 0.f : mx * scale_log2;
-        const float shift = mu + 7.f;  // p / 128 = 2^(s * scale * log2 e - mu - 7)
-        // pass 2: bf16 p / 128 written over the S columns already read (P chunk
-        // ch, 16 columns, lands in S chunk ch / 2), fp32 row sum
+        // p = 2^(s * scale * log2 e - mu) in bf16 over the S columns already
+        // read (P chunk ch, 16 columns, lands in S chunk ch / 2), fp32 row sum
         float2 l4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
@@ -715,8 +745,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int kc = ch * 32 + 2 * q;
-            float2 x = fma2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), scale_log2, scale_log2, -shift,
-                            -shift);
+            float2 x = fma2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]), scale_log2, scale_log2, -mu,
+                            -mu);
             if (kMask) {
               x.x = kc < nkeys ? x.x : -INFINITY;
               x.y = kc + 1 < nkeys ? x.y : -INFINITY;
@@ -727,85 +757,81 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           }
           tc::st_32x32b_x16(srow + ch * 16, pk);
         }
-        l = 128.f * (((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y)));
-        mx = mu;
-        return true;
+        l = ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
       };
-      const bool ok = masked ? softmax_rows(std::true_type{}) : softmax_rows(std::false_type{});
-      if (!ok) break;
-      const float mu = mx;
+      if (masked) softmax_rows(std::true_type{});
+      else softmax_rows(std::false_type{});
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[wg]);
-      if (valid) p.pml[(static_cast<long long>(g) * per_head + ent) * kGroup + h] = make_float2(mu, l);
+      if (valid) {
+        if (phase == 0) {
+          p.mref[row] = mu;
+          p.lacc[row] = l;
+        } else {
+          atomicAdd(p.lacc + row, l);
+          // a key above the reference by 2^64 or more (or a non-finite score)
+          // leaves the range of the fixed reference: reported, not hidden
+          if (!(l < 0x1p64f)) record_error(err, MSA_DEVERR_RANGE, static_cast<long long>(g) * T * topk + ent);
+        }
+      }
     }
   } else {
-    // ---------------- warps 8-15: epilogue, O / 128 (as the MMA wrote it) to fp16 partials ----------------
-    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Each
-    // thread converts its row to fp16 in a 128-byte-swizzled staging tile;
-    // one thread then writes each entry's 16 rows with two tiled TMA stores.
+    // ---------------- warps 8-15: epilogue, fp32 O into the row accumulators ----------------
+    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Warp w
+    // owns 32 rows of the tile (entries 2 (w % 4) and 2 (w % 4) + 1): per
+    // 32-column quarter it copies its rows from tensor memory into one 4 KB
+    // half of its own 8 KB of staging (128-byte swizzle), and its lane 0 has
+    // the tensor engine store (phase 0) or add (phase 1) the two 16-row boxes
+    // into the fp32 accumulators [T][64][128].
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
-    const int r = quarter * 32 + lane;
     const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
-    const uint32_t stage = smem_u32(sm.ostage[wg]);
-    const long long per_head = T * topk;
-    const bool issuer = r == 0;
-    if (issuer) prefetch_tmap(&pmap);
+    uint8_t* own = &sm.ostage[0][0] + (warp - 8) * 8192;
+    if (lane == 0) prefetch_tmap(&amap);
     for (int i = wg; i < n; i += 2) {
       const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 724))) break;
       const int cnt = sm.info[is].cnt, g = sm.info[is].g;
-      int ents[kBmEntries];
-      if (issuer) {
-#pragma unroll
-        for (int e = 0; e < kBmEntries; ++e) ents[e] = sm.info[is].ent[e];
-      }
+      const int ea = 2 * quarter;
+      const int ta = ea < cnt ? static_cast<int>(sm.info[is].ent[ea] / topk) : -1;
+      const int tb = ea + 1 < cnt ? static_cast<int>(sm.info[is].ent[ea + 1] / topk) : -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
       tc::fence_after();
-      // the staging tile is free once the TMA stores of this group's previous
-      // tile have read it; the store thread signals that at the start of the tile
-      if (issuer) {
-        bulk_wait_read_all();
-        mbar_arrive(&sm.stage_free[wg]);
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.stage_free[wg], k & 1, err, 725))) break;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int qq = 0; qq < 4; ++qq) {
         uint32_t v[32];
-        tc::ld_32x32b_x32(orow + ch * 32, v);
+        tc::ld_32x32b_x32(orow + qq * 32, v);
         tc::wait_ld();
-        uint32_t u[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) u[q] = pack_half2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int c16 = ch * 4 + c;  // 16-byte chunk of the 256-byte row
-          sts128(stage + (c16 >> 3) * kBmHalf + sw128(r, c16 & 7), u[4 * c], u[4 * c + 1], u[4 * c + 2],
-                 u[4 * c + 3]);
+        if (qq == 3) {  // every column of the O buffer has been read
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.o_free[wg]);
         }
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[wg]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.stage_full[wg]);
-      bool staged = true;
-      if (issuer) staged = mbar_wait(&sm.stage_full[wg], k & 1, err, 726);
-      if (!__all_sync(0xffffffffu, staged)) break;  // the whole warp leaves together
-      if (issuer) {
-        for (int e = 0; e < cnt; ++e) {
-          const int row = static_cast<int>((static_cast<long long>(g) * per_head + ents[e]) * kGroup);
-          tma_store_2d(&pmap, sm.ostage[wg] + e * kBmQBox, 0, row);
-          tma_store_2d(&pmap, sm.ostage[wg] + kBmHalf + e * kBmQBox, 64, row);
+        // this half was last read by the bulk group of two quarters ago
+        if (lane == 0) bulk_wait_read_1();
+        __syncwarp();
+        uint8_t* half = own + (qq & 1) * 4096;
+        const uint32_t hs = smem_u32(half);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sts128(hs + sw128(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (phase == 0) {
+            if (ta >= 0) tma_store_3d(&amap, half, qq * 32, g * kGroup, ta);
+            if (tb >= 0) tma_store_3d(&amap, half + 2048, qq * 32, g * kGroup, tb);
+          } else {
+            if (ta >= 0) tma_reduce_add_3d(&amap, half, qq * 32, g * kGroup, ta);
+            if (tb >= 0) tma_reduce_add_3d(&amap, half + 2048, qq * 32, g * kGroup, tb);
+          }
+          bulk_commit();
         }
-        bulk_commit();
       }
     }
-    if (issuer) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();  // the stores and adds have landed before the CTA exits
   }
   tc::fence_before();
   __syncthreads();
@@ -815,73 +841,26 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
   }
 }
 
-// One 256-thread block per (token, KV head): combines the token's partials
-// out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j, M = max_j m_j.
-// Thread (h, c) owns dims 8c..8c+7 of head h of the group.  With `lse`, the
-// log2 of the softmax denominator in the scaled-score base-2 domain,
-// M + log2(sum_j 2^(m_j - M) l_j), goes to lse[t][g * 16 + h] (-inf for a row
-// with no key): what the backward needs to rebuild P.
-__global__ void __launch_bounds__(256) bm_merge_kernel(const int32_t* __restrict__ q2k,
-                                                       const int32_t* __restrict__ cu, int num_docs, long long T,
-                                                       int topk, BmPlan p, __nv_bfloat16* __restrict__ out,
-                                                       float* __restrict__ lse) {
-  const long long t = blockIdx.x;
-  const int g = blockIdx.y;
-  const int h = threadIdx.x >> 4, c = threadIdx.x & 15;
-  const long long e0 = (static_cast<long long>(g) * T + t) * topk;
-  // All of the token's partials are requested before any is used, and before
-  // the document lookup: every entry owns a partial slot, so a load needs
-  // only its q2k entry; an entry past the token's causal blocks (bad q2k data,
-  // which the attention skipped, leaving its slot unwritten) is dropped after.
-  float2 ml[kMaxTopk];
-  uint4 u[kMaxTopk];
-  int bj[kMaxTopk];
-#pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) {
-    bj[j] = j < topk ? q2k[e0 + j] : -1;
-    ml[j] = make_float2(-INFINITY, 0.f);
-    u[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (bj[j] >= 0) {
-      const long long slot = e0 + j;
-      ml[j] = p.pml[slot * kGroup + h];
-      u[j] = __ldcs(reinterpret_cast<const uint4*>(p.po + (slot * kGroup + h) * kDim + 8 * c));
-    }
+// The output of every (token, query head) row: out = acc / lacc in bf16, zeros
+// for a row with no key; with `lse`, the log2 of the softmax denominator in the
+// scaled-score base-2 domain, mref + log2(lacc) (-inf for a row with no key):
+// what the backward needs to rebuild P.  16 threads per row, 8 dims each.
+__global__ void __launch_bounds__(256) bm_norm_kernel(BmPlan p, long long rows, __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  const long long row = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int c = threadIdx.x & 15;
+  if (row >= rows) return;
+  const float l = __ldcs(p.lacc + row);
+  const float4* a = reinterpret_cast<const float4*>(p.acc + row * kDim + 8 * c);
+  uint4 o = make_uint4(0u, 0u, 0u, 0u);
+  if (l > 0.f) {  // a row with no key was never written: its accumulator is not read
+    const float4 x = __ldcs(a), y = __ldcs(a + 1);
+    const float inv = 1.f / l;
+    o = make_uint4(pack_bf16(x.x * inv, x.y * inv), pack_bf16(x.z * inv, x.w * inv), pack_bf16(y.x * inv, y.y * inv),
+                   pack_bf16(y.z * inv, y.w * inv));
   }
-  const int d = doc_of(cu, num_docs, t);
-  const int nb = static_cast<int>(t - cu[d]) / kBlock + 1;
-#pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) {
-    if (bj[j] >= nb) {
-      ml[j] = make_float2(-INFINITY, 0.f);
-      u[j] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) M = fmaxf(M, ml[j].x);
-  const float Mu = M == -INFINITY ? 0.f : M;
-  float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < kMaxTopk; ++j) {
-    const float f = exp2f(ml[j].x - Mu);  // 0 for a skipped entry
-    L += ml[j].y * f;
-    const float w = 128.f * f;  // the partial holds O / 128, O unnormalised
-    const __half2* hv = reinterpret_cast<const __half2*>(&u[j]);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 x = __half22float2(hv[q]);
-      acc[2 * q] += w * x.x;
-      acc[2 * q + 1] += w * x.y;
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint4 o;
-  o.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-  o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-  o.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-  o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(out + ((t * kHeads) + g * kGroup + h) * kDim + 8 * c) = o;
-  if (lse && c == 0) lse[t * kHeads + g * kGroup + h] = L > 0.f ? Mu + log2f(L) : -INFINITY;
+  *reinterpret_cast<uint4*>(out + row * kDim + 8 * c) = o;
+  if (lse && c == 0) lse[row] = l > 0.f ? p.mref[row] + log2f(l) : -INFINITY;
 }
 
 
@@ -914,23 +893,10 @@ static bool encode3d_f32(CUtensorMap* map, const void* base, cuuint64_t d0, cuui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map over the fp16 partials viewed as [entries * 16 rows, 128]; box = 64 dims x 16 rows.
-static bool encode_partials(CUtensorMap* map, const void* base, long long rows) {
-  EncodeTiledFn enc = get_encode_tiled();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {kDim * 2};
-  cuuint32_t box[2] = {64, kGroup};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool prefill_attend_fits(long long total_tokens, int max_seqlen, int topk) {
   const BmDims d = bm_dims(total_tokens, max_seqlen, topk);
-  // partial rows are addressed by 32-bit TMA coordinates
-  return d.entries * kGroup < (1LL << 31) && kKvHeads * d.kg_max < (1LL << 31) && d.tiles_max < (1LL << 31);
+  // entries, keys and tiles are int32 on the device
+  return d.entries < (1LL << 31) && 2 * kKvHeads * d.kg_max < (1LL << 31) && d.tiles_max < (1LL << 31);
 }
 
 cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, const int32_t* q2k,
@@ -941,14 +907,17 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
   bm_carve(dims, region, &p);
-  CUtensorMap qmap, kmap, vmap, pmap;
-  if (!encode_partials(&pmap, p.po, dims.entries * kGroup) ||
+  CUtensorMap qmap, kmap, vmap, amap;
+  if (!encode3d_f32(&amap, p.acc, kDim, kHeads, total_tokens, 32, kGroup, 1) ||
       !encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
       !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
       !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
     return cudaErrorInvalidValue;
-  const long long keys = kKvHeads * dims.kg_max;
+  const long long keys = 2 * kKvHeads * dims.kg_max;
   cudaError_t e = cudaMemsetAsync(p.counts, 0, keys * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  // rows that no entry reaches keep lacc = 0 (the reference phase stores the others)
+  e = cudaMemsetAsync(p.lacc, 0, static_cast<size_t>(total_tokens) * kHeads * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   bm_geom_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_docs, total_tokens, dims.W, dims.nw, dims.kg_max, p, err);
   const long long pairs = kKvHeads * total_tokens;
@@ -962,10 +931,14 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   cudaFuncSetAttribute(bm_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const long long chunks = (dims.tiles_max + kBmChunk - 1) / kBmChunk;
   const int grid = static_cast<int>(chunks < kNumSMs ? chunks : kNumSMs);
-  bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, pmap, p, total_tokens, topk,
-                                                       scale * 1.4426950408889634f, err);
-  bm_merge_kernel<<<dim3(static_cast<unsigned>(total_tokens), kKvHeads), 256, 0, stream>>>(
-      q2k, cu_seqlens, num_docs, total_tokens, topk, p, static_cast<__nv_bfloat16*>(out), lse);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  // the reference tiles, then (once their mref, lacc and acc are written) the others
+  for (int phase = 0; phase < 2; ++phase)
+    bm_attend_kernel<<<grid, kBmThreads, smem, stream>>>(qmap, kmap, vmap, amap, p, total_tokens, topk, scale_log2,
+                                                         phase, err);
+  const long long rows = total_tokens * kHeads;
+  bm_norm_kernel<<<static_cast<unsigned>((rows + 15) / 16), 256, 0, stream>>>(p, rows,
+                                                                            static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }
 
@@ -1456,8 +1429,8 @@ __global__ void __maxnreg__(kBwMaxRegs) bw_attend_kernel(
 }
 
 // Backward workspace: the forward's bucketing arrays, then (in place of the
-// forward's partials, which the backward does not use) D [T][64] and the fp32
-// accumulators dk and dv [T][4][128] (dq is summed in the bf16 output).
+// forward's accumulators, which the backward does not use) D [T][64] and the
+// fp32 accumulators dk and dv [T][4][128] (dq is summed in the bf16 output).
 struct BwCarve {
   float* D;
   float* dk;
@@ -1467,9 +1440,7 @@ struct BwCarve {
 static BwCarve bw_carve(long long T, int max_seqlen, int topk, uint8_t* region) {
   BwCarve c;
   const BmDims d = bm_dims(T, max_seqlen, topk);
-  // po and pml are the last two arrays bm_carve takes
-  size_t off = bm_carve(d, nullptr, nullptr) - al256(d.entries * kGroup * kDim * sizeof(__half)) -
-               al256(d.entries * kGroup * sizeof(float2));
+  size_t off = bm_carve(d, nullptr, nullptr, false);  // the bucketing arrays
   auto take = [&](size_t bytes) {
     uint8_t* ptr = region ? region + off : nullptr;
     off += al256(bytes);
@@ -1494,7 +1465,8 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   const BmDims dims = bm_dims(total_tokens, max_seqlen, topk);
   BmPlan p;
-  bm_carve(dims, region, &p);
+  bm_carve(dims, region, &p, false);
+  p.phases = 1;  // no reference split: one phase of keys
   const BwCarve w = bw_carve(total_tokens, max_seqlen, topk, region);
   CUtensorMap qmap, omap, kmap, vmap, dqmap, dkmap, dvmap;
   if (!encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||

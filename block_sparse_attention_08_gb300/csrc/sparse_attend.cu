@@ -28,14 +28,26 @@
 // through shared memory.  A segment cut by a CTA boundary is written as an fp32
 // partial (max, sum, unnormalised O); the CTA whose atomic ticket completes the
 // segment (no waiting) merges the partials and writes bf16.
+//
+// FP8 main K/V cache (TensorRT-LLM field fuse_qkv_index_projection: the M3 path
+// uses "an FP8 main KV cache"): the caches hold E4M3 bytes standing for
+// k_scale * k and v_scale * v.  A chunk is then 64 keys x 128 bytes of K and of
+// V (one 128-byte-swizzled box each, 16 KB a stage); the consumer warp that owns
+// the stage converts it into its own fp16 tile with the bf16 stage's layout
+// (every E4M3 value is exact in fp16), releases the stage at once, and runs the
+// same MMA code in fp16 (q rounded to fp16 once per segment, P rounded to fp16).
+// k_scale is folded into the softmax scale and v_scale into the normalisation.
+#include <cuda_fp8.h>
+
 #include "launch.h"
 
 namespace msa {
 
 constexpr int kAttStages = 6;
 constexpr int kChunkKeys = 64;
-constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 dims)
+constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 bf16 dims, or 128 E4M3 dims)
 constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
+constexpr int kAttStage8Bytes = 2 * kBoxBytes;     // FP8 K/V: K + V, one box each
 constexpr int kConsumerWarps = 3;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kAttThreads = kConsumerThreads + 32;
@@ -82,8 +94,20 @@ struct SegInfo {
   int nk[kMaxTopk];  // causal keys of each of the segment's units (0 = nothing to do)
 };
 
-struct AttSmem {
+// The chunk ring; with an FP8 cache also one fp16 tile per consumer warp.
+template <int kFp8>
+struct AttTiles {
   alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
+};
+template <>
+struct AttTiles<1> {
+  alignas(1024) uint8_t stage[kAttStages][kAttStage8Bytes];
+  alignas(1024) uint8_t wtile[kConsumerWarps][kAttStageBytes];
+};
+
+template <int kFp8>
+struct AttSmem {
+  AttTiles<kFp8> t;
   alignas(1024) uint8_t qtile[kSegSlots][2 * kQBoxBytes];
   float comb[kConsumerWarps - 1][kGroup][kCombStride];
   float comb_m[kConsumerWarps - 1][kGroup];
@@ -112,7 +136,8 @@ struct WarpState {
   float o[16][4];
 };
 
-__device__ __forceinline__ void state_to_smem(const WarpState& st, AttSmem& sm, int slot, int g8, int t4) {
+template <class Smem>
+__device__ __forceinline__ void state_to_smem(const WarpState& st, Smem& sm, int slot, int g8, int t4) {
   if (t4 == 0) {
     sm.comb_m[slot][g8] = st.m0;
     sm.comb_m[slot][g8 + 8] = st.m1;
@@ -126,7 +151,8 @@ __device__ __forceinline__ void state_to_smem(const WarpState& st, AttSmem& sm, 
   }
 }
 
-__device__ __forceinline__ void merge_from_smem(WarpState& st, const AttSmem& sm, int slot, int g8, int t4) {
+template <class Smem>
+__device__ __forceinline__ void merge_from_smem(WarpState& st, const Smem& sm, int slot, int g8, int t4) {
   const float mb0 = sm.comb_m[slot][g8], mb1 = sm.comb_m[slot][g8 + 8];
   const float M0 = fmaxf(st.m0, mb0), M1 = fmaxf(st.m1, mb1);
   const float u0 = M0 == -INFINITY ? 0.f : M0, u1 = M1 == -INFINITY ? 0.f : M1;
@@ -184,15 +210,68 @@ __device__ __forceinline__ void store_mxfp8_64(const float* v, float inv, uint8_
   }
 }
 
+// The 16-bit MMA type of the attention: bf16 (a bf16 K/V cache) or fp16 (an
+// FP8 K/V cache, converted to fp16 on chip).
+template <int kFp8>
+__device__ __forceinline__ void mma16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if (kFp8) mma_f16(c, a, b0, b1);
+  else mma_bf16(c, a, b0, b1);
+}
+template <int kFp8>
+__device__ __forceinline__ float round16(float x) {
+  return kFp8 ? __half2float(__float2half_rn(x)) : bf16_round(x);
+}
+template <int kFp8>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if (kFp8) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  return pack_bf16(lo, hi);
+}
+// bf16x2 -> fp16x2 (q of an FP8-cache call; exact for |q| in fp16's normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two E4M3 bytes (low byte first) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// One FP8 stage (K and V: 64 rows x 128 E4M3 bytes each, 128-byte swizzle) into
+// an fp16 tile laid out like a bf16 stage (K lo, K hi, V lo, V hi: 64 rows x 64
+// dims each, 128-byte swizzle).  Lane work: 16 E4M3 bytes -> two 16-byte fp16 chunks.
+__device__ __forceinline__ void fp8_stage_to_f16(const uint8_t* src, uint8_t* dst, int lane) {
+#pragma unroll 4
+  for (int i = 0; i < 2 * kChunkKeys * 8 / 32; ++i) {
+    const int idx = i * 32 + lane;
+    const int which = idx >> 9, rr = (idx >> 3) & (kChunkKeys - 1), c = idx & 7;  // K / V, row, 16-dim chunk
+    const uint4 x = *reinterpret_cast<const uint4*>(src + which * kBoxBytes + sw128(rr, c));
+    const uint4 lo = make_uint4(e4m3x2_to_f16x2(x.x & 0xffffu), e4m3x2_to_f16x2(x.x >> 16),
+                                e4m3x2_to_f16x2(x.y & 0xffffu), e4m3x2_to_f16x2(x.y >> 16));
+    const uint4 hi = make_uint4(e4m3x2_to_f16x2(x.z & 0xffffu), e4m3x2_to_f16x2(x.z >> 16),
+                                e4m3x2_to_f16x2(x.w & 0xffffu), e4m3x2_to_f16x2(x.w >> 16));
+    const int cc = 2 * c;  // first fp16 chunk of the 256-byte row; chunks 8.. are the hi half
+    uint8_t* base = dst + (2 * which + (cc >> 3)) * kBoxBytes;
+    *reinterpret_cast<uint4*>(base + sw128(rr, cc & 7)) = lo;
+    *reinterpret_cast<uint4*>(base + sw128(rr, (cc + 1) & 7)) = hi;
+  }
+}
+
 // out_q / out_scale: when non-null, the output is emitted as MXFP8 there
-// instead of bf16 in `out`.
+// instead of bf16 in `out`.  kFp8: the K / V caches hold E4M3 bytes;
+// scale_log2 then includes k_scale, and v_scale multiplies the output.
+template <int kFp8>
 __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
-    float scale_log2, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q, uint8_t* __restrict__ out_scale,
-    float* __restrict__ partials, int* __restrict__ tickets, DevError* err) {
+    float scale_log2, float v_scale, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
+    uint8_t* __restrict__ out_scale, float* __restrict__ partials, int* __restrict__ tickets, DevError* err) {
   extern __shared__ uint8_t smem_raw[];
-  AttSmem& sm = *reinterpret_cast<AttSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  AttSmem<kFp8>& sm =
+      *reinterpret_cast<AttSmem<kFp8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
@@ -281,13 +360,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
           if (lane == 0) {
             const int s = static_cast<int>(sc % kAttStages);
             mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kAttStages) & 1) ^ 1), err, 200);
-            mbar_expect_tx(&sm.full[s], kAttStageBytes);
             const int row = static_cast<int>(r0 + ch * kChunkKeys);
-            uint8_t* st = sm.stage[s];
-            tma_load_3d(st + 0 * kBoxBytes, &kmap, 0, g, row, &sm.full[s]);
-            tma_load_3d(st + 1 * kBoxBytes, &kmap, 64, g, row, &sm.full[s]);
-            tma_load_3d(st + 2 * kBoxBytes, &vmap, 0, g, row, &sm.full[s]);
-            tma_load_3d(st + 3 * kBoxBytes, &vmap, 64, g, row, &sm.full[s]);
+            uint8_t* st = sm.t.stage[s];
+            if (kFp8) {
+              mbar_expect_tx(&sm.full[s], kAttStage8Bytes);
+              tma_load_3d(st, &kmap, 0, g, row, &sm.full[s]);
+              tma_load_3d(st + kBoxBytes, &vmap, 0, g, row, &sm.full[s]);
+            } else {
+              mbar_expect_tx(&sm.full[s], kAttStageBytes);
+              tma_load_3d(st + 0 * kBoxBytes, &kmap, 0, g, row, &sm.full[s]);
+              tma_load_3d(st + 1 * kBoxBytes, &kmap, 64, g, row, &sm.full[s]);
+              tma_load_3d(st + 2 * kBoxBytes, &vmap, 0, g, row, &sm.full[s]);
+              tma_load_3d(st + 3 * kBoxBytes, &vmap, 64, g, row, &sm.full[s]);
+            }
           }
           __syncwarp();
         }
@@ -335,6 +420,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       for (int kk = 0; kk < 8; ++kk) {
         const int chunk = 2 * kk + (lane >> 4);
         ldsm_x4(qa[kk], qt + (chunk >> 3) * kQBoxBytes + sw128(qrow, chunk & 7));
+        if (kFp8)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) qa[kk][j] = bf16x2_to_f16x2(qa[kk][j]);
       }
     }
     __syncwarp();
@@ -356,7 +444,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         if (s % kConsumerWarps != warp) continue;
         const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
         mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kAttStages) & 1), err, 300);
-        const uint32_t stg = smem_u32(sm.stage[s]);
+        uint32_t stg;
+        if constexpr (kFp8 != 0) {
+          // to this warp's fp16 tile; the stage is free again at once
+          fp8_stage_to_f16(sm.t.stage[s], sm.t.wtile[warp], lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[s]);
+          stg = smem_u32(sm.t.wtile[warp]);
+        } else {
+          stg = smem_u32(sm.t.stage[s]);
+        }
         const int mi = lane >> 3;
         // ---- S = Q K^T over the chunk's keys (n-tiles of 8 keys, in pairs) ----
         float sacc[8][4];
@@ -371,8 +468,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
             uint32_t kb[4];
             ldsm_x4(kb, stg + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7));
-            mma_bf16(sacc[2 * kp], qa[kk], kb[0], kb[1]);
-            mma_bf16(sacc[2 * kp + 1], qa[kk], kb[2], kb[3]);
+            mma16<kFp8>(sacc[2 * kp], qa[kk], kb[0], kb[1]);
+            mma16<kFp8>(sacc[2 * kp + 1], qa[kk], kb[2], kb[3]);
           }
         }
         // ---- mask, online softmax (base 2, scale folded in) ----
@@ -397,15 +494,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         const float al0 = exp2f(st.m0 - mu0), al1 = exp2f(st.m1 - mu1);
         st.m0 = mn0;
         st.m1 = mn1;
-        // p rounded to bf16 (the PV operand); the row sum adds the same rounded
-        // values, so the normalisation matches the weights the MMA applies
+        // p rounded to the 16-bit MMA type (the PV operand); the row sum adds the
+        // same rounded values, so the normalisation matches the weights the MMA applies
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-          sacc[p][0] = bf16_round(exp2f(sacc[p][0] - mu0));
-          sacc[p][1] = bf16_round(exp2f(sacc[p][1] - mu0));
-          sacc[p][2] = bf16_round(exp2f(sacc[p][2] - mu1));
-          sacc[p][3] = bf16_round(exp2f(sacc[p][3] - mu1));
+          sacc[p][0] = round16<kFp8>(exp2f(sacc[p][0] - mu0));
+          sacc[p][1] = round16<kFp8>(exp2f(sacc[p][1] - mu0));
+          sacc[p][2] = round16<kFp8>(exp2f(sacc[p][2] - mu1));
+          sacc[p][3] = round16<kFp8>(exp2f(sacc[p][3] - mu1));
           rs0 += sacc[p][0] + sacc[p][1];
           rs1 += sacc[p][2] + sacc[p][3];
         }
@@ -422,22 +519,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           if (16 * kp >= valid) break;
-          const uint32_t pa[4] = {pack_bf16(sacc[2 * kp][0], sacc[2 * kp][1]),
-                                  pack_bf16(sacc[2 * kp][2], sacc[2 * kp][3]),
-                                  pack_bf16(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1]),
-                                  pack_bf16(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3])};
+          const uint32_t pa[4] = {pack16<kFp8>(sacc[2 * kp][0], sacc[2 * kp][1]),
+                                  pack16<kFp8>(sacc[2 * kp][2], sacc[2 * kp][3]),
+                                  pack16<kFp8>(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1]),
+                                  pack16<kFp8>(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3])};
           const int vrow = 16 * kp + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
           for (int nd = 0; nd < 16; nd += 2) {
             const int chunk = nd + (mi >> 1);
             uint32_t vb[4];
             ldsm_x4_t(vb, stg + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7));
-            mma_bf16(st.o[nd], pa, vb[0], vb[1]);
-            mma_bf16(st.o[nd + 1], pa, vb[2], vb[3]);
+            mma16<kFp8>(st.o[nd], pa, vb[0], vb[1]);
+            mma16<kFp8>(st.o[nd + 1], pa, vb[2], vb[3]);
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        if (!kFp8 && lane == 0) mbar_arrive(&sm.empty[s]);
       }
     }
     it = seg_end;
@@ -464,7 +561,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
     __nv_bfloat16* orow = out_q ? nullptr : out + oelem;
     if (complete) {
-      const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+      const float inv = Lsum > 0.f ? (kFp8 ? v_scale : 1.f) / Lsum : 0.f;
       if (out_q) {
         store_mxfp8_64(src, inv, out_q + oelem, out_scale + oelem / 32);
       } else {
@@ -542,7 +639,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             ag[4 * d + 3] += xs[d].w * f;
           }
         }
-        const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
+        const float inv = Lg > 0.f ? (kFp8 ? v_scale : 1.f) / Lg : 0.f;
         if (out_q) {
           store_mxfp8_64(ag, inv, out_q + oelem, out_scale + oelem / 32);
         } else {
@@ -574,6 +671,20 @@ static bool make_kv_map(CUtensorMap* map, const void* base, long long rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a [rows, 4, 128] E4M3 array; box = 128 dims (128 bytes) x 1 head x 64 rows, 128-byte swizzle.
+static bool make_kv_map8(CUtensorMap* map, const void* base, long long rows) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kKvHeads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {kDim, kKvHeads * kDim};
+  cuuint32_t box[3] = {128, 1, kChunkKeys};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over q viewed as [queries * 64, 128] bf16; box = 64 dims x 16 heads, 128-byte swizzle.
 static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
   EncodeTiledFn enc = get_encode_tiled();
@@ -587,6 +698,9 @@ static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static_assert(sizeof(AttSmem<0>) + 1024 <= 227 * 1024, "shared memory of the decode attention");
+static_assert(sizeof(AttSmem<1>) + 1024 <= 227 * 1024, "shared memory of the decode attention, FP8 K/V");
+
 size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
 // one merge counter per CTA of the persistent grid (at most kNumSMs CTAs)
 size_t attend_tickets_bytes() { return static_cast<size_t>(kNumSMs) * sizeof(int); }
@@ -594,12 +708,12 @@ size_t attend_tickets_bytes() { return static_cast<size_t>(kNumSMs) * sizeof(int
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int kv_fp8, float k_scale, float v_scale) {
   if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   CUtensorMap kmap, vmap, qmap;
-  if (!make_kv_map(&kmap, k, geo.num_rows) || !make_kv_map(&vmap, v, geo.num_rows) ||
-      !make_q_map(&qmap, q, geo.nq))
-    return cudaErrorInvalidValue;
+  const bool maps = kv_fp8 ? make_kv_map8(&kmap, k, geo.num_rows) && make_kv_map8(&vmap, v, geo.num_rows)
+                           : make_kv_map(&kmap, k, geo.num_rows) && make_kv_map(&vmap, v, geo.num_rows);
+  if (!maps || !make_q_map(&qmap, q, geo.nq)) return cudaErrorInvalidValue;
   // At least 4 units per CTA: a segment is then shared by at most ~topk/4 + 1
   // CTAs, which bounds the partials its last CTA has to merge.
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
@@ -607,9 +721,11 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   if (grid_l > kNumSMs) grid_l = kNumSMs;
   if (grid_l < 1) grid_l = 1;
   const int grid = static_cast<int>(grid_l);
-  const size_t smem = sizeof(AttSmem) + 1024;
-  cudaFuncSetAttribute(sparse_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  const float scale_log2 = scale * 1.4426950408889634f;
+  auto kern = kv_fp8 ? sparse_attend_kernel<1> : sparse_attend_kernel<0>;
+  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  // an FP8 cache holds k / k_scale: the scores are scaled by k_scale as well
+  const float scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
   // a programmatic dependent of the previous kernel in the stream (the kernel
   // waits for that grid before touching memory), so its launch and prologue
   // overlap the decode top-k
@@ -623,7 +739,7 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, sparse_attend_kernel, kmap, vmap, qmap, q2k, geo, topk, scale_log2,
+  return cudaLaunchKernelEx(&lc, kern, kmap, vmap, qmap, q2k, geo, topk, scale_log2, kv_fp8 ? v_scale : 1.f,
                             static_cast<__nv_bfloat16*>(out), out_q, out_scale, partials, tickets, err);
 }
 

@@ -73,7 +73,9 @@ enum {
   MSA_DEVERR_PAGE = 1,     /* page id outside [0, num_slots/128) */
   MSA_DEVERR_BLOCK = 2,    /* q2k id outside [0, blocks of the query) */
   MSA_DEVERR_LENGTH = 3,   /* seq_len < 1, or above max_blocks * 128 */
-  MSA_DEVERR_TIMEOUT = 4   /* a bounded on-chip wait gave up */
+  MSA_DEVERR_TIMEOUT = 4,  /* a bounded on-chip wait gave up */
+  MSA_DEVERR_RANGE = 5     /* prefill attention: a score outside the fixed-reference range (see
+                              msa_sparse_attend_prefill); detail = the flat q2k index */
 };
 
 /* Layer configuration (TensorRT-LLM MiniMaxM3SparseAttentionConfig fields:
@@ -251,6 +253,26 @@ msa_status msa_sparse_attend_decode_mxfp8(const msa_config* cfg, const void* q, 
                                           void* out_scale, void* workspace, size_t workspace_bytes,
                                           void* stream);
 
+/* The same decode attention over an FP8 main K/V cache (TensorRT-LLM field
+ * fuse_qkv_index_projection: the MiniMax-M3 path uses "an FP8 main KV cache").
+ * The pages give no scale rule; the reading taken: the caches hold E4M3 bytes
+ * (OCP E4M3, "fn") standing for k_scale * k and v_scale * v, one fp32 scale per
+ * cache (1.0 for an unscaled cache).
+ *   k_cache, v_cache dev uint8 [num_slots, 4, 128] E4M3
+ *   k_scale, v_scale finite and > 0
+ * Inside, the E4M3 values enter fp16 MMAs exactly, q is rounded to fp16 once
+ * (exact for |q| in fp16's normal range, 2^-14 .. 65504), P is rounded to fp16
+ * with the row sum taken over the rounded values, accumulation is fp32.  Other
+ * arguments, the output and the errors as msa_sparse_attend_decode;
+ * MSA_ERR_SHAPE for a scale that is not finite and positive. */
+msa_status msa_sparse_attend_decode_fp8kv(const msa_config* cfg, const void* q, const void* k_cache,
+                                          const void* v_cache, float k_scale, float v_scale,
+                                          const int32_t* q2k, const int32_t* seq_lens,
+                                          const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                          int batch, int max_blocks, int64_t num_slots, float scale,
+                                          void* out, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+
 /* ---- step 1+2, prefill: block scores + top-k on packed documents ------------
  * NeMo MSAMicrobatch.select_blocks: compact tokens in document order, document
  * d spanning [cu_seqlens[d], cu_seqlens[d+1]); token t of document d has
@@ -273,7 +295,15 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
  * NeMo sparse_attention / _SparseAttention.forward: bf16 q [tokens, 64, 128],
  * k / v [tokens, 4, 128], int32 q2k [4, tokens, topk] -> bf16 out
  * [tokens, 64, 128]; keys are the causal keys (position <= the query's) of the
- * query's document inside the listed blocks. */
+ * query's document inside the listed blocks.
+ * Each (query, KV head) row's softmax takes its exponent reference from the
+ * row's highest listed block (the local block when local_blocks >= 1): the
+ * row max over that block's causal keys.  The other blocks are summed against
+ * that fixed reference in fp32.  A key of another listed block whose scaled
+ * score (in log2 units) exceeds the reference by 64 or more (a logit gap above
+ * about 44) is outside this scheme's range: the call records MSA_DEVERR_RANGE
+ * (detail: the flat q2k index of the entry) and that row's output is not
+ * valid.  Nothing else is affected. */
 msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k,
                                      const void* v, const int32_t* q2k, const int32_t* cu_seqlens,
                                      int num_docs, int64_t total_tokens, int max_seqlen,
@@ -318,6 +348,65 @@ msa_status msa_sparse_attend_prefill_backward(const msa_config* cfg, const void*
                                               const void* out, const float* lse, const void* grad_out,
                                               void* dq, void* dk, void* dv, void* workspace,
                                               size_t workspace_bytes, void* stream);
+
+/* ---- the index producer: L2 norm, storage cast, index-K cache insertion ------
+ * TensorRT-LLM "MiniMaxM3SparseAttentionConfig", field fuse_qkv_index_projection
+ * (MSA batches use a horizontal norm / RoPE / cache-insertion producer for
+ * prefill, mixed and CUDA-graph decode), field indexer_kv_dtype (index Q/K are
+ * stored normalized, as bf16 or unscaled E4M3) and the class description (the
+ * paged index-K cache [num_slots, 1, 128] parallel to the main K/V cache); NeMo
+ * select_blocks takes index tensors "post norm".  Each 128-vector x of the
+ * projection's output is stored as y = x / ||x||_2 in cfg->index_dtype:
+ * computed in IEEE binary32 with the squares summed in index order c = 0..127,
+ * sqrt and division correctly rounded, then one rounding to bf16 or E4M3
+ * (nearest, ties to even).  A vector whose sum of squares is 0 in binary32 is
+ * stored as zeros.  The pages fix neither the precision nor the order; this is
+ * the reading the library takes, and it makes the result bit-reproducible.
+ * RoPE, which the pages name without giving its variant, is not applied: it is
+ * a rotation and leaves the L2 norm unchanged, so a caller may apply it to the
+ * input.  Inputs are the projection's bf16 output.
+ *   workspace  >= 256 bytes, 256-byte aligned (only its device error word is
+ *              used: a page id or position out of range is skipped and
+ *              recorded there, MSA_DEVERR_PAGE / MSA_DEVERR_LENGTH, detail =
+ *              the token or request)
+ * Errors: MSA_ERR_NULL, MSA_ERR_SHAPE, MSA_ERR_DTYPE, MSA_ERR_ALIGN (a tensor
+ * not 16-byte aligned), MSA_ERR_WORKSPACE, MSA_ERR_CUDA. */
+
+/* Prefill / packed documents (the input of msa_select_blocks_prefill):
+ *   index_q_in  dev bf16 [total_tokens, 4, 128]; index_k_in dev bf16 [total_tokens, 1, 128]
+ *   cu_seqlens  dev int32 [num_docs + 1], as for msa_select_blocks_prefill
+ *   index_q_out dev [total_tokens, 4, 128] in cfg->index_dtype (written whole)
+ *   index_k_out dev [total_tokens, 1, 128] in cfg->index_dtype, or NULL
+ *   index_k_cache dev [num_slots, 1, 128] in cfg->index_dtype, or NULL: when
+ *              given, the key of the token at position p of document d is also
+ *              written at slot page_table[d * max_blocks + p / 128] * 128 + p % 128
+ *              (page_table dev int32 [num_docs, max_blocks]; num_slots a
+ *              multiple of 128); no other slot is touched
+ * At least one of index_k_out and index_k_cache must be given. */
+msa_status msa_index_produce_prefill(const msa_config* cfg, const void* index_q_in,
+                                     const void* index_k_in, const int32_t* cu_seqlens,
+                                     int num_docs, int64_t total_tokens, void* index_q_out,
+                                     void* index_k_out, void* index_k_cache,
+                                     const int32_t* page_table, int max_blocks, int64_t num_slots,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Decode (one new token per request, the input of msa_select_blocks_decode):
+ * the new token of request r sits at position p = seq_lens[r] - 1 (the
+ * length includes it); its normalised key is written at the slot
+ *   page_table[r * max_blocks + p / 128] * 128 + p % 128   (paged), or
+ *   cu_seqlens_k[r] + p                                   (page_table == NULL)
+ * of index_k_cache, and no other slot is touched.
+ *   index_q_in  dev bf16 [batch, 4, 128]; index_k_in dev bf16 [batch, 1, 128]
+ *   seq_lens / page_table / cu_seqlens_k / max_blocks / num_slots: as for
+ *              msa_select_blocks_decode
+ *   index_q_out dev [batch, 4, 128] in cfg->index_dtype
+ *   index_k_cache dev [num_slots, 1, 128] in cfg->index_dtype, updated in place */
+msa_status msa_index_produce_decode(const msa_config* cfg, const void* index_q_in,
+                                    const void* index_k_in, const int32_t* seq_lens,
+                                    const int32_t* page_table, const int64_t* cu_seqlens_k,
+                                    int batch, int max_blocks, int64_t num_slots, void* index_q_out,
+                                    void* index_k_cache, void* workspace, size_t workspace_bytes,
+                                    void* stream);
 
 /* ---- packed layout of a document map ----------------------------------------
  * NeMo layout-from-doc_ids constructor and _contiguous_runs: doc_ids is an

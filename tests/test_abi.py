@@ -165,6 +165,32 @@ def test_bounded_wait_check_validation(lib):
     assert lib.msa_check_bounded_wait(FAKE + 16, None, waits) == WORKSPACE
 
 
+def test_index_produce_validation(lib):
+    c = _cfg()
+    # prefill: neither a packed key output nor a cache; a cache without a page table
+    assert lib.msa_index_produce_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 1, 128, FAKE, None, None, None, 0, 0,
+                                         FAKE, 256, None) == NULL
+    assert lib.msa_index_produce_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 1, 128, FAKE, None, FAKE, None, 1,
+                                         128, FAKE, 256, None) == NULL
+    # a cache whose slot count is not a whole number of pages; a misaligned output; a small workspace
+    assert lib.msa_index_produce_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 1, 128, FAKE, None, FAKE, FAKE, 1,
+                                         100, FAKE, 256, None) == SHAPE
+    assert lib.msa_index_produce_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 1, 128, FAKE + 8, FAKE, None, None,
+                                         0, 0, FAKE, 256, None) == ALIGN
+    assert lib.msa_index_produce_prefill(ctypes.byref(c), FAKE, FAKE, FAKE, 1, 128, FAKE, FAKE, None, None, 0, 0,
+                                         FAKE, 128, None) == WORKSPACE
+    bad = _cfg(index_dtype=7)
+    assert lib.msa_index_produce_prefill(ctypes.byref(bad), FAKE, FAKE, FAKE, 1, 128, FAKE, FAKE, None, None, 0,
+                                         0, FAKE, 256, None) == DTYPE
+    # decode: no cache; no geometry; a bad batch
+    assert lib.msa_index_produce_decode(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, None, 4, 8, 1024, FAKE, None,
+                                        FAKE, 256, None) == NULL
+    assert lib.msa_index_produce_decode(ctypes.byref(c), FAKE, FAKE, FAKE, None, None, 4, 8, 1024, FAKE, FAKE,
+                                        FAKE, 256, None) == NULL
+    assert lib.msa_index_produce_decode(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, None, 0, 8, 1024, FAKE, FAKE,
+                                        FAKE, 256, None) == SHAPE
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert lib.msa_status_string(s)

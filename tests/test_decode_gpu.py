@@ -162,3 +162,52 @@ def test_decode_mxfp8_workload_sample():
     torch.cuda.synchronize()
     rq, rs = oracle.mxfp8_quantize(out.reshape(out.shape[0], -1))
     assert np.array_equal(oq.cpu().numpy(), rq) and np.array_equal(osc.cpu().numpy(), rs)
+
+
+def _fp8_caches(d, k_scale, v_scale):
+    k8 = (d.k_cache.float() / k_scale).to(torch.float8_e4m3fn)
+    v8 = (d.v_cache.float() / v_scale).to(torch.float8_e4m3fn)
+    return k8, v8
+
+
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("k_scale,v_scale", [(1.0, 1.0), (0.0625, 0.5), (3.0, 0.2)])
+def test_decode_fp8_kv_cache(paged, k_scale, v_scale):
+    """The decode attention over an FP8 (E4M3) main K/V cache against the fp64 oracle on the
+    same bytes and scales, on the oracle's selection."""
+    d = msa_synth.decode_inputs(SMALL_LENS, paged=paged, seed=41, device="cuda")
+    k8, v8 = _fp8_caches(d, k_scale, v_scale)
+    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k)
+    ref_q2k, _ = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, **kw)
+    q2k = torch.from_numpy(ref_q2k).cuda()
+    out = msa.msa_sparse_attend_decode_fp8kv(d.q, k8, v8, q2k, d.seq_lens, k_scale=k_scale, v_scale=v_scale,
+                                             max_blocks=d.max_blocks, scale=SCALE, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, ref_q2k, SCALE, k_scale=k_scale, v_scale=v_scale, **kw)
+    check_out(out, ref, f"decode attention, FP8 K/V ({'paged' if paged else 'contiguous'}, "
+                        f"k_scale {k_scale}, v_scale {v_scale})")
+
+
+def test_decode_fp8_kv_cache_many_requests():
+    # many segments per CTA and stream-K cuts inside them, as for the bf16 cache
+    lens = np.random.default_rng(72).integers(1, 3000, size=200).tolist()
+    d = msa_synth.decode_inputs(lens, paged=True, seed=72, device="cuda")
+    k8, v8 = _fp8_caches(d, 1.0, 1.0)
+    ref_q2k, _ = oracle.select_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table, topk=16,
+                                      init=1, local=1)
+    q2k = torch.from_numpy(ref_q2k).cuda()
+    out = msa.msa_sparse_attend_decode_fp8kv(d.q, k8, v8, q2k, d.seq_lens, page_table=d.page_table, scale=SCALE)
+    torch.cuda.synchronize()
+    ref = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, ref_q2k, SCALE, page_table=d.page_table)
+    check_out(out, ref, "decode attention, FP8 K/V, 200 requests")
+
+
+@pytest.mark.slow
+def test_decode_fp8_kv_workload_b64_paged():
+    d = msa_synth.workload("decode_b64_ctx4k_64k_paged", device="cuda")
+    k8, v8 = _fp8_caches(d, 1.0, 1.0)
+    q2k = msa.msa_select_blocks_decode(d.index_q, d.index_k_cache, d.seq_lens, page_table=d.page_table)
+    out = msa.msa_sparse_attend_decode_fp8kv(d.q, k8, v8, q2k, d.seq_lens, page_table=d.page_table, scale=SCALE)
+    torch.cuda.synchronize()
+    ref = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, q2k, SCALE, page_table=d.page_table)
+    check_out(out, ref, "decode_b64_ctx4k_64k_paged attention, FP8 K/V")

@@ -3,18 +3,22 @@
 Roles as in the kernel: the scheduler / TMA warp (K of a new block, the
 tile's Q rows, V of a new block), the S-MMA thread, the O-MMA thread, two
 softmax warpgroups and two epilogue warpgroups taking the even and the odd
-tiles (four warps each; the epilogue's first thread also issues the tile's
-TMA stores).  Tensor memory holds S (then P over it) and O twice; shared
-memory holds Q twice, K twice, V once and one fp16 staging tile per epilogue
-warpgroup.  The TMA copies land in any order, each MMA thread's groups and
-commits execute in that thread's issue order (no order is assumed between
-the two threads: what one reads the other writes only behind a barrier), and the
-stores read their staging at random moments.  Random tile sequences (runs of
-tiles over one key block) under random schedules must finish, never poll a
-barrier two phases away from the phase they wait for, never write anything
-under a pending access, and read in every use the content it expects.  A
-planted mistake (the O MMA not waiting for the epilogue to free its O
-buffer) must be reported.  No GPU is involved.
+tiles (four warps each).  Tensor memory holds S (then P over it) and O twice;
+shared memory holds Q twice, K twice, V once, and per epilogue warp two 4 KB
+staging halves: per 32-column quarter of its rows the warp waits until the
+bulk group of two quarters ago has read the half it is about to fill
+(cp.async.bulk.wait_group.read 1), writes it, and issues that quarter's
+tensor-engine store / add as a new bulk group.  The TMA copies land in any
+order, each MMA thread's groups and commits execute in that thread's issue
+order (no order is assumed between the two threads: what one reads the other
+writes only behind a barrier), and the bulk groups read their staging at
+random moments, in any order.  Random tile sequences (runs of tiles over one
+key block) under random schedules must finish, never poll a barrier two
+phases away from the phase they wait for, never write anything under a
+pending access, and read in every use the content it expects.  Planted
+mistakes (the O MMA not waiting for the epilogue to free its O buffer; the
+epilogue refilling a staging half without the bulk read wait) must be
+reported.  No GPU is involved.
 """
 import random
 
@@ -36,8 +40,9 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, tiles, rng, skip_o_free=False):
+    def __init__(self, tiles, rng, skip_o_free=False, skip_bulk_wait=False):
         self.tiles, self.rng, self.skip_o_free = tiles, rng, skip_o_free  # tiles: list of block ids
+        self.skip_bulk_wait = skip_bulk_wait
         self.bars = {}
 
         def bar(name, count=1):
@@ -57,15 +62,15 @@ class Sim:
             bar(f"o_full{b}")
             bar(f"o_free{b}", 4)
             bar(f"p_full{b}", 4)
-            bar(f"stage_free{b}")
-            bar(f"stage_full{b}", 4)
         for i in range(INFO):
             bar(f"info_full{i}")
             bar(f"info_empty{i}", 10)
         self.tag, self.pend_r, self.pend_w, self.warp_r = {}, {}, {}, {}
         self.pipe = {"S": [], "O": []}  # per MMA thread, in issue order
         self.loads = []
-        self.stores = {0: [], 1: []}  # per epilogue warpgroup: staging reads of its stores
+        # per epilogue warp: its bulk groups not yet done reading their staging half, (group id, half)
+        self.groups = {(wg, q): [] for wg in (0, 1) for q in range(4)}
+        self.issued = {(wg, q): 0 for wg in (0, 1) for q in range(4)}
 
     def wait(self, name, parity, need):
         bar = self.bars[name]
@@ -196,35 +201,36 @@ class Sim:
             self.bars[f"p_full{wg}"].arrive()
 
     def epilogue(self, wg, q):
-        issuer = q == 0
+        w = (wg, q)
         for i in range(wg, len(self.tiles), 2):
             s, u, k = i % INFO, i // INFO, i >> 1
             yield self.wait(f"info_full{s}", u & 1, u + 1)
             self.bars[f"info_empty{s}"].arrive()
             yield self.wait(f"o_full{wg}", k & 1, k + 1)
-            if issuer:
-                yield lambda: not self.stores[wg]  # the previous tile's stores have read the staging
-                self.bars[f"stage_free{wg}"].arrive()
-            yield self.wait(f"stage_free{wg}", k & 1, k + 1)
-            self.warp_read(f"O{wg}_{q}", ("O", i))
-            yield None
-            self.warp_write(f"stage{wg}_{q}", ("stage", i))
-            self.warp_read_end(f"O{wg}_{q}")
-            self.bars[f"o_free{wg}"].arrive()
-            self.bars[f"stage_full{wg}"].arrive()
-            if issuer:
-                yield self.wait(f"stage_full{wg}", k & 1, k + 1)
-                bufs = [f"stage{wg}_{x}" for x in range(4)]
-                for b in bufs:
-                    assert self.tag.get(b) == ("stage", i), f"store of {b} holding {self.tag.get(b)}"
-                    self._add(self.pend_r, b, 1)
-                self.stores[wg].append(bufs)
+            self.warp_read(f"O{wg}_{q}", ("O", i))  # the warp's rows, one 32-column quarter at a time
+            for qq in range(4):
+                yield None
+                assert self.tag.get(f"O{wg}_{q}") == ("O", i), f"O{wg}_{q} changed under the epilogue's reads"
+                if qq == 3:
+                    self.warp_read_end(f"O{wg}_{q}")
+                    self.bars[f"o_free{wg}"].arrive()
+                if not self.skip_bulk_wait:
+                    # cp.async.bulk.wait_group.read 1: every group but the newest has read its half
+                    newest = self.issued[w] - 1
+                    yield lambda: all(g == newest for g, _ in self.groups[w])
+                half = f"stage{wg}_{q}_{qq & 1}"
+                self.warp_write(half, ("stage", i, qq))
+                yield None
+                assert self.tag.get(half) == ("stage", i, qq)
+                self._add(self.pend_r, half, 1)
+                self.groups[w].append((self.issued[w], half))
+                self.issued[w] += 1
 
     # engines ----------------------------------------------------------------
     def engines(self):
         out = [lambda p=p: self.step_pipe(p) for p in ("S", "O") if self.pipe[p]]
         out += [lambda k=k: self.land(k) for k in range(len(self.loads))]
-        out += [lambda w=w: self.store_read(w) for w in (0, 1) if self.stores[w]]
+        out += [lambda w=w, j=j: self.group_read(w, j) for w, gs in self.groups.items() for j in range(len(gs))]
         return out
 
     def step_pipe(self, pipe):
@@ -244,9 +250,9 @@ class Sim:
         self.tag[buf] = tag
         self.bars[name].arrive()
 
-    def store_read(self, wg):
-        for b in self.stores[wg].pop(0):
-            self._add(self.pend_r, b, -1)
+    def group_read(self, w, j):
+        _, half = self.groups[w].pop(j)
+        self._add(self.pend_r, half, -1)
 
     def run(self):
         roles = [self.producer(), self.s_mma(), self.o_mma()]
@@ -255,7 +261,7 @@ class Sim:
         blocked = [None] * len(roles)
         live = set(range(len(roles)))
         steps = 0
-        while live or any(self.pipe.values()) or self.loads or any(self.stores.values()):
+        while live or any(self.pipe.values()) or self.loads or any(self.groups.values()):
             steps += 1
             assert steps < 500000, "no progress"
             ready = [r for r in live if blocked[r] is None or blocked[r]()]
@@ -298,6 +304,17 @@ def test_model_catches_a_missing_o_free_wait():
         rng = random.Random(seed)
         try:
             Sim(tile_sequence(rng, 5), rng, skip_o_free=True).run()
+        except AssertionError:
+            failed += 1
+    assert failed > 0
+
+
+def test_model_catches_a_missing_bulk_read_wait():
+    failed = 0
+    for seed in range(30):
+        rng = random.Random(seed)
+        try:
+            Sim(tile_sequence(rng, 5), rng, skip_bulk_wait=True).run()
         except AssertionError:
             failed += 1
     assert failed > 0

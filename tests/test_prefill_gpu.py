@@ -175,3 +175,48 @@ def test_prefill_attend_empty_rows_and_bad_ids():
     o = out.float().cpu().numpy()
     assert not o[5, 16:32].any()
     check_out(out, ref_out, "prefill out with empty and bad rows")
+
+
+def test_prefill_far_block_within_the_reference_range():
+    """Keys of block 0 scored far above the local block (exponents up to about 2^40
+    over each row's reference) are summed exactly against the fixed reference."""
+    p = msa_synth.prefill_inputs([900, 400], seed=13, device="cuda")
+    k = p.k.clone()
+    k[:128] = (k[:128].float() * 8).to(torch.bfloat16)      # document 0, block 0
+    k[900:1028] = (k[900:1028].float() * 8).to(torch.bfloat16)  # document 1, block 0
+    T = p.total_tokens
+    tok = np.arange(T, dtype=np.int64)
+    ref_q2k, _ = oracle.select_prefill(p.index_q, p.index_k, p.cu_seqlens, tok, topk=4, init=1, local=1)
+    ws = msa.Workspace(msa.workspace_size(msa.make_config(4, 1, 1), 1, T, (p.max_seqlen + 127) // 128))
+    out = msa.msa_sparse_attend_prefill(p.q, k, p.v, torch.from_numpy(ref_q2k).cuda(), p.cu_seqlens, p.max_seqlen,
+                                        scale=SCALE, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.read_device_error() == (0, 0)
+    ref = oracle.attend_prefill(p.q, k, p.v, p.cu_seqlens, tok, ref_q2k, SCALE)
+    check_out(out, ref, "prefill, block 0 scored up to 2^40 above the reference")
+
+
+def test_prefill_score_past_the_reference_range_is_reported():
+    """One key of block 0 scores 2^115 above the local block's max for KV head 1:
+    MSA_DEVERR_RANGE is recorded; the other KV heads' rows are exact."""
+    T = 300
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    q = torch.zeros(T, 64, 128)
+    q[:, :, 0] = 30.0
+    k = torch.zeros(T, 4, 128)
+    k[10, 1, 0] = 30.0          # s = 900 for head group 1 against key 10; every other score is 0
+    v = torch.randn(T, 4, 128, generator=torch.Generator().manual_seed(3))
+    q, k, v = (x.to(torch.bfloat16).cuda() for x in (q, k, v))
+    q2k = torch.full((4, T, 2), -1, dtype=torch.int32)
+    pos = torch.arange(T)
+    q2k[:, :, 0] = 0
+    q2k[:, :, 1] = torch.where(pos >= 128, pos // 128, torch.tensor(-1))
+    q2k = q2k.cuda()
+    ws = msa.Workspace(msa.workspace_size(msa.make_config(2, 0, 1), 1, T, 3))
+    out = msa.msa_sparse_attend_prefill(q, k, v, q2k, cu, T, scale=SCALE, workspace=ws)
+    torch.cuda.synchronize()
+    code, detail = ws.read_device_error()
+    assert code == 5 and (detail // 2) // T == 1, (code, detail)   # an entry of KV head 1
+    ref = oracle.attend_prefill(q, k, v, cu, np.arange(T, dtype=np.int64), q2k.cpu().numpy(), SCALE)
+    for g in (0, 2, 3):
+        check_out(out[:, 16 * g:16 * g + 16], ref[:, 16 * g:16 * g + 16], f"prefill out of range: KV head {g}")
