@@ -264,6 +264,102 @@ def run_backward(args, device, config):
             "gpu_launches": 9 * args.steps, "clocks": clk.summary()}
 
 
+def run_produce(args, device, config):
+    """One step = one index-producer call over the workload (C ABI
+    msa_index_produce_prefill for a prefill workload: index Q and K of every
+    token normalised and stored in the index dtype, the keys also inserted
+    into a paged cache; msa_index_produce_decode for a decode workload: each
+    request's new index Q and key), replayed from a CUDA graph, L2 flushed
+    between steps.  Bytes: the bf16 inputs read once and the outputs written
+    once (the HBM roofline of a streaming kernel)."""
+    import block_sparse_attention_08_gb300 as msa
+    torch.cuda.set_device(device)
+    inp = msa_synth.workload(args.workload, seed=args.seed, device=device, scale_down=args.scale_down)
+    gen = torch.Generator(device=device).manual_seed(args.seed + 7)
+    e4m3 = "e4m3" in args.workload
+    esz = 1 if e4m3 else 2
+    if args.workload.startswith("prefill"):
+        T = inp.total_tokens
+        iq = torch.randn((T, 4, 128), generator=gen, device=device).to(torch.bfloat16)
+        ik = torch.randn((T, 1, 128), generator=gen, device=device).to(torch.bfloat16)
+        dt = torch.float8_e4m3fn if e4m3 else torch.bfloat16
+        qo = torch.empty((T, 4, 128), dtype=dt, device=device)
+        ko = torch.empty((T, 1, 128), dtype=dt, device=device)
+        cu = inp.cu_seqlens
+        docs = cu.shape[0] - 1
+        nbs = ((cu[1:] - cu[:-1] + 127) // 128).cpu()
+        mb = int(nbs.max())
+        pages = int(nbs.sum())
+        perm = torch.randperm(pages, generator=torch.Generator().manual_seed(args.seed)).to(torch.int32)
+        pt = torch.full((docs, mb), -1, dtype=torch.int32)
+        o = 0
+        for d in range(docs):
+            pt[d, : nbs[d]] = perm[o: o + nbs[d]]
+            o += int(nbs[d])
+        pt = pt.to(device)
+        cache = torch.empty((pages * 128, 1, 128), dtype=dt, device=device)
+
+        def call():
+            msa.msa_index_produce_prefill(iq, ik, cu, index_dtype="e4m3" if e4m3 else "bf16", index_k_cache=cache,
+                                          page_table=pt, q_out=qo, k_out=ko)
+        n_q = T
+        nbytes = T * 5 * 128 * 2 + T * 5 * 128 * esz + T * 128 * esz
+    else:
+        d = inp
+        B = d.batch
+        iq = torch.randn((B, 4, 128), generator=gen, device=device).to(torch.bfloat16)
+        ik = torch.randn((B, 1, 128), generator=gen, device=device).to(torch.bfloat16)
+        qo = torch.empty((B, 4, 128), dtype=d.index_k_cache.dtype, device=device)
+
+        def call():
+            msa.msa_index_produce_decode(iq, ik, d.index_k_cache, d.seq_lens, page_table=d.page_table,
+                                         cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks, q_out=qo)
+        n_q = B
+        nbytes = B * 5 * 128 * 2 + B * 5 * 128 * esz
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    run = call
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                call()
+        stream.wait_stream(cap)
+        run = g.replay
+        run()
+        torch.cuda.synchronize()
+    hbm_peak, _, peak_src = _peaks()
+    ms_all = []
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 255)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            b.record(stream)
+            b.synchronize()
+            ms_all.append(a.elapsed_time(b))
+    ms = sum(ms_all) / len(ms_all)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    config.update({"pass": "index producer (L2 norm, storage cast, index-K cache insertion)",
+                   "queries_per_step": n_q, "timing": "CUDA-graph replay of the C-ABI call",
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)"})
+    return {"metric": "index producer: query tokens/s; HBM GB/s", "value": round(n_q / (ms * 1e-3), 1),
+            "unit": "query tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "e4m3" if e4m3 else "bf16",
+            "data": "synthetic", "config": config,
+            "roofline": {"bound": "hbm", "kernel": "index_produce_kernel", "achieved": round(gbs, 1),
+                         "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "bytes": nbytes, "peak_source": peak_src + " hbm_gbs (copy, burst)"},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+
+
 def run_gpu(args, rank, world, device, name=None, steps=None):
     import block_sparse_attention_08_gb300 as msa
     torch.cuda.set_device(device)
@@ -586,6 +682,8 @@ def main():
                     help="decode: main K / V caches as E4M3 (msa_sparse_attend_decode_fp8kv, unit scales)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other headline workloads (measured after the bench workload at one GPU)")
+    ap.add_argument("--produce", action="store_true",
+                    help="time the index producer (norm, storage cast, cache insertion) on the workload's shapes")
     ap.add_argument("--backward", action="store_true",
                     help="time the attention backward of a prefill workload instead of the forward step")
     args = ap.parse_args()
@@ -610,6 +708,12 @@ def main():
             config["kv_cache"] = "E4M3 main K / V caches (unit scales)"
     if args.scale_down > 1:
         config["scale_down"] = args.scale_down
+
+    if args.produce:
+        if args.impl != "gb300":
+            raise SystemExit("--produce times the index producer of this library")
+        print(json.dumps(run_produce(args, torch.device("cuda", local), config)))
+        return
 
     if args.backward:
         if args.impl != "gb300" or not args.workload.startswith("prefill"):

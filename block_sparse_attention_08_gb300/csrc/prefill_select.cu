@@ -365,21 +365,33 @@ __global__ void __launch_bounds__(kPsThreads, 1) prefill_select_kernel(
         float mx[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          float m = -INFINITY;
-          const uint32_t col0 = static_cast<uint32_t>((buf * 2 + hh) * 128);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t v[32];
-            tc::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + col0 + ch * 32, v);
-            tc::wait_ld();
+          // the head's 128 scores of this row: four loads in flight, one wait
+          const uint32_t a0 = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>((buf * 2 + hh) * 128);
+          uint32_t v0[32], v1[32], v2[32], v3[32];
+          tc::ld_32x32b_x32(a0, v0);
+          tc::ld_32x32b_x32(a0 + 32, v1);
+          tc::ld_32x32b_x32(a0 + 64, v2);
+          tc::ld_32x32b_x32(a0 + 96, v3);
+          tc::wait_ld();
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (diag) {  // causal keys only: key column j <= this row's position r
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const float f = __uint_as_float(v[j]);
-              const bool ok = !diag || (ch * 32 + j <= r);
-              m = ok ? fmaxf(m, f) : m;
+              m4[0] = j <= r ? fmaxf(m4[0], __uint_as_float(v0[j])) : m4[0];
+              m4[1] = 32 + j <= r ? fmaxf(m4[1], __uint_as_float(v1[j])) : m4[1];
+              m4[2] = 64 + j <= r ? fmaxf(m4[2], __uint_as_float(v2[j])) : m4[2];
+              m4[3] = 96 + j <= r ? fmaxf(m4[3], __uint_as_float(v3[j])) : m4[3];
+            }
+          } else {  // every key is causal: four independent chains of three-input max
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              m4[0] = fmax3(m4[0], __uint_as_float(v0[j]), __uint_as_float(v0[j + 1]));
+              m4[1] = fmax3(m4[1], __uint_as_float(v1[j]), __uint_as_float(v1[j + 1]));
+              m4[2] = fmax3(m4[2], __uint_as_float(v2[j]), __uint_as_float(v2[j + 1]));
+              m4[3] = fmax3(m4[3], __uint_as_float(v3[j]), __uint_as_float(v3[j + 1]));
             }
           }
-          mx[hh] = m;
+          mx[hh] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         tc::fence_before();
         __syncwarp();

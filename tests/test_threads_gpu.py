@@ -43,13 +43,14 @@ def test_prefill_path_on_a_fresh_thread():
     grads = msa.msa_sparse_attend_prefill_backward(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, out, lse, dout,
                                                    scale=SCALE)
     torch.cuda.synchronize()
-    # the same calls on a fresh thread give the same integers and the same forward bits
+    # the same calls on a fresh thread give the same integers, and the forward within one bf16
+    # rounding (its fp32 row sums are added in an order that varies)
     q2k_t = _on_fresh_thread(lambda: msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens,
                                                                    p.max_seqlen))
     assert torch.equal(q2k_t, q2k)
     out_t = _on_fresh_thread(lambda: msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen,
                                                                    scale=SCALE))
-    assert torch.equal(out_t, out)
+    assert ((out_t.float() - out.float()).abs() <= 2.0 ** -8 * out.float().abs() + 1e-6).all()
     g_t = _on_fresh_thread(lambda: msa.msa_sparse_attend_prefill_backward(
         p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, out, lse, dout, scale=SCALE))
     # the gradients are summed with atomics (order varies): compare within bf16 rounding
