@@ -306,7 +306,7 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
  * valid.  Nothing else is affected.  The fp32 sums are added by the tensor
  * engine in an order that varies from run to run, so the bf16 output is not
  * bitwise reproducible (the pages give no deterministic-mode guarantee); two
- * runs differ by at most the last bf16 rounding. */
+ * runs differ by at most one bf16 ulp. */
 msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const void* k,
                                      const void* v, const int32_t* q2k, const int32_t* cu_seqlens,
                                      int num_docs, int64_t total_tokens, int max_seqlen,

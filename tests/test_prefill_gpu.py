@@ -101,7 +101,7 @@ def test_hand_worked_three_blocks_on_gpu():
 def test_prefill_repeated_calls_agree():
     """One workspace serves calls of different sizes: the selection repeats bit
     for bit; the attention's fp32 row sums are added by the tensor engine in an
-    order that varies, so its bf16 output repeats to within one bf16 rounding."""
+    order that varies, so its bf16 output repeats to within one bf16 ulp."""
     p = msa_synth.prefill_inputs([3000, 400, 2500], seed=4, device="cuda")
     o = msa_synth.prefill_inputs([9000], seed=5, device="cuda")
     a = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
@@ -113,7 +113,7 @@ def test_prefill_repeated_calls_agree():
         ob = msa.msa_sparse_attend_prefill(p.q, p.k, p.v, b, p.cu_seqlens, p.max_seqlen)
         assert torch.equal(a, b)
         d = (oa.float() - ob.float()).abs()
-        assert (d <= 2.0 ** -8 * oa.float().abs() + 1e-6).all(), float(d.max())
+        assert (d <= 2.0 ** -7 * oa.float().abs() + 1e-6).all(), float(d.max())  # one bf16 ulp
 
 
 def _sample_tokens(cu, n, seed):

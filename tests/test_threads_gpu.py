@@ -50,7 +50,7 @@ def test_prefill_path_on_a_fresh_thread():
     assert torch.equal(q2k_t, q2k)
     out_t = _on_fresh_thread(lambda: msa.msa_sparse_attend_prefill(p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen,
                                                                    scale=SCALE))
-    assert ((out_t.float() - out.float()).abs() <= 2.0 ** -8 * out.float().abs() + 1e-6).all()
+    assert ((out_t.float() - out.float()).abs() <= 2.0 ** -7 * out.float().abs() + 1e-6).all()  # one bf16 ulp
     g_t = _on_fresh_thread(lambda: msa.msa_sparse_attend_prefill_backward(
         p.q, p.k, p.v, q2k, p.cu_seqlens, p.max_seqlen, out, lse, dout, scale=SCALE))
     # the gradients are summed with atomics (order varies): compare within bf16 rounding
