@@ -732,7 +732,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           mu = mr;
         }
         // p = 2^(s * scale * log2 e - mu) in bf16 over the S columns already
-        // read (P chunk ch, 16 columns, lands in S chunk ch / 2), fp32 row sum
+        // read (P chunk ch, 16 columns, lands in S chunk ch / 2); the fp32 row
+        // sum adds the same bf16-rounded values, so the normalisation matches
+        // the weights the PV product applies (which matters when one key
+        // dominates a row and its p is not a power of two)
         float2 l4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
@@ -751,9 +754,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
               x.x = kc < nkeys ? x.x : -INFINITY;
               x.y = kc + 1 < nkeys ? x.y : -INFINITY;
             }
-            const float pa = ex2(x.x), pb = ex2(x.y);
-            l4[q & 3] = add2(l4[q & 3].x, l4[q & 3].y, pa, pb);
-            pk[q] = pack_bf16(pa, pb);
+            const uint32_t pp = pack_bf16(ex2(x.x), ex2(x.y));
+            pk[q] = pp;
+            l4[q & 3] = add2(l4[q & 3].x, l4[q & 3].y, __uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
           }
           tc::st_32x32b_x16(srow + ch * 16, pk);
         }
