@@ -274,6 +274,8 @@ msa_status msa_select_blocks_prefill(const msa_config* cfg, const void* index_q,
   if ((st = check_prefill_geom(cu_seqlens, num_docs, total_tokens, max_seqlen)) != MSA_OK) return st;
   if (!aligned16(index_q) || !aligned16(index_k) || !aligned16(q2k)) return MSA_ERR_ALIGN;
   const int max_tiles = (max_seqlen + kBlock - 1) / kBlock;
+  // the scorer's plan keeps three ints per 128-token block of the longest document on chip
+  if ((3LL * max_tiles + 2) * 4 > 200 * 1024) return MSA_ERR_SHAPE;
   const Layout L = layout(MSA_MODE_PREFILL, total_tokens, max_tiles, cfg->topk);
   if ((st = check_ws(workspace, workspace_bytes, L.total)) != MSA_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

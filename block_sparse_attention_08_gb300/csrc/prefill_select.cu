@@ -94,10 +94,17 @@ __device__ __forceinline__ Unit unit_of(const PsPlan& p, int u) {
 __device__ __forceinline__ int snake(int k, int c, int G) { return (k & 1) ? (k + 1) * G - 1 - c : k * G + c; }
 
 // One-CTA plan: documents sorted by tile count (descending), level bases.
+// One block: documents counting-sorted by tile count (descending), the per-level
+// tile counts and bases.  The histogram and its scans live in shared memory
+// (`sh`: max_tiles + 2 ints); thread 0's two scans are sequential over the
+// levels, so they must not go through global memory.
 __global__ void prefill_plan_kernel(const int32_t* __restrict__ cu, int num_docs, int max_tiles,
-                                    int* __restrict__ hist /*[max_tiles+2]*/, int* __restrict__ sorted_docs,
-                                    int* __restrict__ level_base, int* __restrict__ level_cnt,
-                                    int* __restrict__ n_tiles, DevError* err) {
+                                    int* __restrict__ sorted_docs, int* __restrict__ level_base,
+                                    int* __restrict__ level_cnt, int* __restrict__ n_tiles, DevError* err) {
+  extern __shared__ int sh[];
+  int* hist = sh;                        // [max_tiles + 2]: docs per tile count, then scatter cursors
+  int* lcnt = sh + (max_tiles + 2);      // [max_tiles]
+  int* lbase = lcnt + max_tiles;         // [max_tiles]
   const int tid = threadIdx.x;
   for (int i = tid; i < max_tiles + 2; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -112,16 +119,16 @@ __global__ void prefill_plan_kernel(const int32_t* __restrict__ cu, int num_docs
   }
   __syncthreads();
   if (tid == 0) {
-    // level_cnt[qb] = #docs with tile count > qb ; level_base: levels in decreasing qb
+    // lcnt[qb] = #docs with tile count > qb ; lbase: levels in decreasing qb
     int above = 0;
     for (int n = max_tiles; n >= 1; --n) {
       above += hist[n];
-      level_cnt[n - 1] = above;
+      lcnt[n - 1] = above;
     }
     int base = 0;
     for (int qb = max_tiles - 1; qb >= 0; --qb) {
-      level_base[qb] = base;
-      base += level_cnt[qb];
+      lbase[qb] = base;
+      base += lcnt[qb];
     }
     *n_tiles = base;
     // scatter cursors: docs with tile count n start after all docs with more tiles
@@ -133,6 +140,10 @@ __global__ void prefill_plan_kernel(const int32_t* __restrict__ cu, int num_docs
     }
   }
   __syncthreads();
+  for (int qb = tid; qb < max_tiles; qb += blockDim.x) {
+    level_cnt[qb] = lcnt[qb];
+    level_base[qb] = lbase[qb];
+  }
   for (int d = tid; d < num_docs; d += blockDim.x) {
     const int len = cu[d + 1] - cu[d];
     const int nt = len < 1 ? 0 : min((len + kBlock - 1) / kBlock, max_tiles);
@@ -437,8 +448,11 @@ cudaError_t launch_prefill_select(const msa_config& cfg, const void* index_q, co
   int* level_base = sorted_docs + num_docs;
   int* level_cnt = level_base + max_tiles;
   int* n_tiles = level_cnt + max_tiles;
-  prefill_plan_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_docs, max_tiles, hist, sorted_docs, level_base,
-                                               level_cnt, n_tiles, err);
+  const size_t plan_smem = (3 * static_cast<size_t>(max_tiles) + 2) * sizeof(int);
+  if (plan_smem > 200 * 1024) return cudaErrorInvalidValue;  // the ABI rejects longer documents first
+  cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(plan_smem));
+  prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(cu_seqlens, num_docs, max_tiles, sorted_docs, level_base,
+                                                      level_cnt, n_tiles, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

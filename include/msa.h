@@ -283,6 +283,7 @@ msa_status msa_sparse_attend_decode_fp8kv(const msa_config* cfg, const void* q, 
  *   index_k    dev [total_tokens, 1, 128], same dtype as index_q
  *   cu_seqlens dev int32 [num_docs + 1], cu_seqlens[0] = 0, strictly increasing,
  *              cu_seqlens[num_docs] = total_tokens; max_seqlen = the longest document
+ *              (at most 17066 blocks of 128 tokens, about 2.18M tokens; longer: MSA_ERR_SHAPE)
  *   q2k        dev int32 [4, total_tokens, topk]
  * E4M3 scores are unscaled dot products of the decoded values, accumulated in
  * fp32 (TRT indexer_kv_dtype). */
@@ -316,7 +317,9 @@ msa_status msa_sparse_attend_prefill(const msa_config* cfg, const void* q, const
 /* The same call, also writing the log-sum-exp the backward needs:
  *   lse dev fp32 [total_tokens, 64]: log2 of the softmax denominator in the
  *       base-2 domain of the scaled scores, log2(sum_p 2^(scale <q, k_p> log2 e)),
- *       -inf for a (token, head) with no key (NeMo _SparseAttention saves the
+ *       -inf for a (token, head) with no key.  The sum is taken over the
+ *       bf16-rounded weights the output applies, so it is within
+ *       log2(1 + 2^-9) of the exact value (NeMo _SparseAttention saves the
  *       forward's schedule for its backward; this is the row statistic of it).
  * Errors as msa_sparse_attend_prefill; MSA_ERR_NULL for a null lse. */
 msa_status msa_sparse_attend_prefill_lse(const msa_config* cfg, const void* q, const void* k,

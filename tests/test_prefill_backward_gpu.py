@@ -85,7 +85,9 @@ def test_prefill_lse_is_the_log_sum_exp():
             keys = [cu[d] + j for b in qk[g, t] if b >= 0 for j in range(b * 128, min(b * 128 + 128, pos + 1))]
             z = SCALE * (k[keys, g] @ q[t, h])
             ref = (np.log(np.sum(np.exp(z - z.max()))) + z.max()) / np.log(2.0)
-            assert abs(got[t, h] - ref) <= 1e-4 * (1 + abs(ref)), (t, h, got[t, h], ref)
+            # the forward's row sum adds the bf16-rounded weights its PV product applies, each
+            # within 2^-9 of the exact one: its log2 is within log2(1 + 2^-9) of the exact lse
+            assert abs(got[t, h] - ref) <= np.log2(1 + 2.0 ** -9) + 1e-4 * (1 + abs(ref)), (t, h, got[t, h], ref)
 
 
 def test_sparse_attention_autograd():
