@@ -191,7 +191,7 @@ msa_status msa_select_blocks_decode(const msa_config* cfg, const void* index_q, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch,
                                        max_blocks, num_slots, q2k, reinterpret_cast<float*>(ws + L.scores),
-                                       reinterpret_cast<DevError*>(ws), s);
+                                       reinterpret_cast<int*>(ws + kSelSchedOffset), reinterpret_cast<DevError*>(ws), s);
   return cuda_result(e);
 }
 

@@ -10,9 +10,12 @@
 //
 // GB300 design: the paged index-K cache is streamed from HBM once.  Each
 // 128-key page (32 KB bf16 / 16 KB E4M3, contiguous) is one work item.  The
-// (request, page) items of all requests are split evenly across a persistent
-// grid of one CTA per SM (stream-K), so every SM streams the same number of
-// bytes.  Inside a CTA a producer warp resolves 32 page ids at a time with
+// (request, page) items of all requests, in order, are cut into chunks of a
+// few pages; a persistent grid of one CTA per SM takes the first wave of
+// chunks by CTA index and then claims chunks from a counter, so an SM that
+// streams faster takes more of them and all SMs finish together (a fixed even
+// split left the slowest SM 20-40 % behind the median on the long-context
+// batches).  Inside a CTA a producer warp resolves 32 page ids at a time with
 // one coalesced load and issues one 1-D bulk TMA copy per page into a ring of
 // 192 KB of shared memory (6 bf16 / 12 E4M3 pages in flight); six consumer
 // warps each take whole pages round-robin (stage s always to warp s % 6) and
@@ -49,12 +52,12 @@ struct SelMeta {
 template <int kStages>
 struct SelSmem {
   alignas(1024) uint8_t ring[kSelRingBytes];
+  // the page's request's index query (4 heads), landed with the page
+  alignas(16) uint8_t qs[kStages][kSelRingBytes / kStages / kBlock * kKvHeads];
   uint64_t full[kStages];
   uint64_t empty[kStages];
   SelMeta meta[kStages];
-  unsigned long long cand[kSelConsumers][kCandCap];
   int scan[kSelThreads / 32];
-  int bcast[4];
 };
 
 // Blocks of request r that are scored (0 when every candidate is kept anyway).
@@ -80,26 +83,34 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 // Exact top-`need` by (score desc, id asc) over the non-forced blocks of one
 // (request, head) row, then the ascending q2k row.  One warp.  Rows of up to
 // 32 x 32 candidates are read once into registers with independent loads.
+// The need-th largest of the 32 lane maxima is a threshold that at least
+// `need` candidates reach, so it keeps every one of the top `need`; those
+// candidates (a few more than `need` as a rule) go to shared memory, where
+// each lane ranks its own against all of them.  Ranks, not rounds of a
+// warp-wide argmax: no step waits on a chain of dependent shuffles.
 constexpr int kTopkRegs = 32;
 
 __device__ __forceinline__ unsigned long long score_key(float v, int b) {
   return (static_cast<unsigned long long>(float_key(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(b));
 }
+__device__ __forceinline__ int key_block(unsigned long long key) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
+}
 
+// cand: kCandCap keys of shared memory; ids: kMaxTopk ints of shared memory.
 __device__ void topk_row(const float* s, int nb, int topk, int init, int local, int32_t* out,
-                         unsigned long long* cand) {
+                         unsigned long long* cand, int* ids) {
   const int lane = threadIdx.x & 31;
   if (nb <= topk) {
     for (int i = lane; i < topk; i += 32) out[i] = i < nb ? i : -1;
     return;
   }
   const int need = topk - init - local;
-  const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi)
-  int picked = -1;
+  const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi), more than `need` of them
   if (need > 0) {
     const bool in_regs = c_hi - c_lo <= 32 * kTopkRegs;
     float v[kTopkRegs];
-    unsigned long long best = 0;
+    unsigned long long best = 0;  // real keys are nonzero; a lane without candidates keeps 0
     if (in_regs) {
 #pragma unroll
       for (int k = 0; k < kTopkRegs; ++k) {
@@ -118,16 +129,13 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
         best = key > best ? key : best;
       }
     }
-    // need-th largest lane maximum (bitonic sort of 32 keys, ascending): at
-    // least `need` candidates are >= theta, so the top `need` all are
-    unsigned long long t = best;
-    for (int k = 2; k <= 32; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, t, j);
-        const bool lower = (lane & j) == 0, asc = (lane & k) == 0;
-        t = (lower == asc) ? (t < o ? t : o) : (t > o ? t : o);
-      }
-    const unsigned long long theta = __shfl_sync(0xffffffffu, t, 32 - need);
+    // rank of this lane's maximum among the 32 (real keys are distinct and
+    // at least need + 1 lanes hold one, so exactly one lane has rank need - 1)
+    int rk = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) rk += __shfl_sync(0xffffffffu, best, j) > best ? 1 : 0;
+    const unsigned who = __ballot_sync(0xffffffffu, rk == need - 1);
+    const unsigned long long theta = __shfl_sync(0xffffffffu, best, who ? __ffs(who) - 1 : 0);
     int count = 0;
     auto consider = [&](unsigned long long key) {
       const bool c = key >= theta && key != 0ull;
@@ -152,18 +160,17 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
     }
     __syncwarp();
     if (count <= kCandCap) {
-      unsigned long long e0 = lane < count ? cand[lane] : 0ull;
-      unsigned long long e1 = lane + 32 < count ? cand[lane + 32] : 0ull;
-      for (int i = 0; i < need; ++i) {
-        unsigned long long m = e0 > e1 ? e0 : e1;
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
-          m = x > m ? x : m;
-        }
-        if (e0 == m) e0 = 0;
-        if (e1 == m) e1 = 0;
-        if (lane == i) picked = static_cast<int>(0xffffffffu - static_cast<uint32_t>(m));
+      // candidate j's rank = how many candidates are larger; ranks 0 .. need-1 are picked
+      const unsigned long long e0 = lane < count ? cand[lane] : 0ull;
+      const unsigned long long e1 = lane + 32 < count ? cand[lane + 32] : 0ull;
+      int r0 = 0, r1 = 0;
+      for (int j = 0; j < count; ++j) {
+        const unsigned long long c = cand[j];
+        r0 += c > e0 ? 1 : 0;
+        r1 += c > e1 ? 1 : 0;
       }
+      if (lane < count && r0 < need) ids[r0] = key_block(e0);
+      if (lane + 32 < count && r1 < need) ids[r1] = key_block(e1);
     } else {
       // rare: too many candidates at or above the threshold -- exact rounds
       unsigned long long prev = ~0ull;
@@ -178,27 +185,85 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
           m = x > m ? x : m;
         }
         prev = m;
-        if (lane == i) picked = static_cast<int>(0xffffffffu - static_cast<uint32_t>(m));
+        if (lane == 0) ids[i] = key_block(m);
       }
     }
-    __syncwarp();
   }
-  // forced ids occupy the remaining lanes; then rank-sort ascending
-  int id = picked;
-  if (lane >= need && lane < need + init) id = lane - need;
-  if (lane >= need + init && lane < topk) id = nb - local + (lane - need - init);
-  int rank = 0;
-  for (int i = 0; i < topk; ++i) {
-    const int o = __shfl_sync(0xffffffffu, id, i);
-    rank += (o < id) ? 1 : 0;
+  // forced ids after the picks; then each id's place in the ascending row
+  if (lane < init) ids[need + lane] = lane;
+  if (lane < local) ids[need + init + lane] = nb - local + lane;
+  __syncwarp();
+  if (lane < topk) {
+    const int id = ids[lane];
+    int pos = 0;
+    for (int j = 0; j < topk; ++j) pos += ids[j] < id ? 1 : 0;
+    out[pos] = id;
   }
-  if (lane < topk) out[rank] = id;
 }
 
+// How the page items [0, total) are shared out.  Each CTA first streams a
+// fixed range of p0 items (CTA b: [b p0, (b + 1) p0), about three quarters of
+// its fair share); the rest, [f, total), is cut into chunks of p1 items that
+// the CTAs claim from a counter, so an SM that streams faster takes more of
+// them and the SMs finish close together.  A small total is all fixed ranges.
+struct SelSplit {
+  int p0, p1, n_dyn;
+  long long f;
+};
+__device__ __forceinline__ SelSplit sel_split(int total, int grid) {
+  SelSplit t;
+  if (total < 8 * grid) {
+    t.p0 = (total + grid - 1) / grid;
+    t.f = total;
+    t.p1 = 1;
+    t.n_dyn = 0;
+  } else {
+    t.p0 = static_cast<int>(3LL * total / (4LL * grid));
+    t.f = static_cast<long long>(t.p0) * grid;
+    const long long p1 = (total - t.f) / (4LL * grid);
+    t.p1 = static_cast<int>(p1 < 1 ? 1 : (p1 > 8 ? 8 : p1));
+    t.n_dyn = static_cast<int>((total - t.f + t.p1 - 1) / t.p1);
+  }
+  return t;
+}
+
+// Moves (r, r_start) forward to the scored request holding page item `item`
+// (r_start = item index of its first page).  Items only grow along one CTA's
+// claims, so the walk never goes back; 32 requests per step, their lengths
+// read with one coalesced load (L1-resident after the first pass).  Returns
+// false when `item` lies past the last request (never expected).
+__device__ __forceinline__ bool walk_to(const DecodeGeom& geo, int topk, long long item, int& r, long long& r_start) {
+  const int lane = threadIdx.x & 31;
+  while (r < geo.batch) {
+    const int rl = r + lane;
+    const int v = rl < geo.batch ? scored_blocks(geo, rl, topk, nullptr) : 0;
+    int x = v;  // inclusive scan over the lanes
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, rl < geo.batch && r_start + x > item);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      r_start += __shfl_sync(0xffffffffu, x - v, l);
+      r += l;
+      return true;
+    }
+    r_start += __shfl_sync(0xffffffffu, x, 31);
+    r += 32;
+  }
+  return false;
+}
+
+constexpr int kSelEnd = -2;  // meta.r of the stage that ends a consumer warp's loop
+
+// sched: two ints in the workspace header, zero between calls -- [0] claims
+// past the first wave, [1] CTAs that have finished claiming (the last one
+// puts both back to zero).
 template <int kE4M3>
 __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     const uint8_t* __restrict__ index_q, const uint8_t* __restrict__ index_k, DecodeGeom geo,
-    float* __restrict__ scores, int topk, DevError* err) {
+    float* __restrict__ scores, int topk, int* __restrict__ sched, DevError* err) {
   constexpr int kRowBytes = kE4M3 ? kIdxDim : kIdxDim * 2;
   constexpr int kPageBytes = kBlock * kRowBytes;
   constexpr int kStages = kSelRingBytes / kPageBytes;
@@ -222,139 +287,200 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
   int total = 0;
   for (int r0 = 0; r0 < B; r0 += kSelThreads) {
     const int r = r0 + tid;
-    int v = 0;
-    if (r < B) {
-      int nb;
-      v = scored_blocks(geo, r, topk, &nb);
-    }
+    const int v = r < B ? scored_blocks(geo, r, topk, nullptr) : 0;
     total += block_sum(v, sm.scan);
   }
-  const long long lo = static_cast<long long>(total) * blockIdx.x / gridDim.x;
-  const long long hi = static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x;
-  if (lo >= hi) return;
-  // locate the request holding item `lo`
-  int r_lo = 0, off_lo = 0;
-  {
-    int run = 0;
-    bool found = false;
-    for (int r0 = 0; r0 < B && !found; r0 += kSelThreads) {
-      const int r = r0 + tid;
-      const int v = r < B ? scored_blocks(geo, r, topk, nullptr) : 0;
-      int x = v;  // inclusive scan within the warp
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      __syncthreads();
-      if (lane == 31) sm.scan[warp] = x;
-      __syncthreads();
-      int before = run;
-      for (int w = 0; w < warp; ++w) before += sm.scan[w];
-      const int incl = before + x, excl = incl - v;
-      if (r < B && v > 0 && excl <= lo && lo < incl) {
-        sm.bcast[0] = r;
-        sm.bcast[1] = excl;
-      }
-      int chunk_total = 0;
-      for (int w = 0; w < kSelThreads / 32; ++w) chunk_total += sm.scan[w];
-      __syncthreads();
-      if (run <= lo && lo < run + chunk_total) found = true;
-      run += chunk_total;
-    }
-    __syncthreads();
-    r_lo = sm.bcast[0];
-    off_lo = sm.bcast[1];
-  }
-  const int n_items = static_cast<int>(hi - lo);
+  __syncthreads();  // the barriers are initialised
+  const SelSplit split = sel_split(total, gridDim.x);
 
   if (warp == kSelConsumers) {
     // ---------------- producer warp ----------------
-    int r = r_lo, b = static_cast<int>(lo - off_lo);
-    int i = 0;
-    while (i < n_items) {
-      const int nbr = scored_blocks(geo, r, topk, nullptr);
-      const int L = geo.seq_lens[r];
-      const int cnt = min(min(nbr - b, n_items - i), 32);
-      // one coalesced load resolves the next (up to) 32 pages of this request
-      long long row0 = 0;
-      int ok = 0;
-      if (lane < cnt) {
-        const int bb = b + lane;
-        const int rows = min(kBlock, L - bb * kBlock);
-        if (geo.page_table) {
-          const int page = geo.page_table[static_cast<long long>(r) * mb + bb];
-          row0 = static_cast<long long>(page) * kBlock;
-          ok = page >= 0 && row0 + kBlock <= geo.num_slots;
-          if (!ok) record_error(err, MSA_DEVERR_PAGE, static_cast<long long>(r) * mb + bb);
-        } else {
-          row0 = geo.cu_k[r] + static_cast<long long>(bb) * kBlock;
-          ok = row0 >= 0 && row0 + rows <= geo.num_slots;
-          if (!ok) record_error(err, MSA_DEVERR_PAGE, r);
-        }
-        ok = ok && rows > 0 ? rows : 0;
+    // Pages go out in groups of up to 32 consecutive items.  While one group's
+    // copies are issued, the next group is already located (its requests from
+    // a forward walk over the lengths, its page ids loading), and the next
+    // claim is in flight, so no lookup waits on the copies' critical path.
+    int i = 0;                  // stages used
+    int alive = 1;              // 0 after a wait gave up: locate and issue nothing more
+    int wr = 0;                 // walk: scored request ...
+    long long wstart = 0;       // ... and its first item
+    long long s_lo = min(static_cast<long long>(blockIdx.x) * split.p0, split.f);
+    const long long s_hi = min(s_lo + split.p0, split.f);
+    long long d_lo = 0, d_hi = 0;  // the claimed chunk's items not yet grouped
+    int claim = 0;                 // lane 0: answer of the pending claim
+    if (lane == 0 && split.n_dyn > 0) claim = atomicAdd(&sched[0], 1);
+    auto next_group = [&](long long& a, int& n) {
+      n = 0;
+      if (s_lo < s_hi) {
+        a = s_lo;
+        n = static_cast<int>(min(32LL, s_hi - s_lo));
+        s_lo += n;
+        return;
       }
-      for (int k = 0; k < cnt; ++k, ++i) {
+      if (d_lo >= d_hi) {
+        if (split.n_dyn == 0 || !alive) return;
+        const int c = __shfl_sync(0xffffffffu, claim, 0);
+        if (c >= split.n_dyn) return;
+        d_lo = split.f + static_cast<long long>(c) * split.p1;
+        d_hi = min(static_cast<long long>(total), d_lo + split.p1);
+        if (lane == 0) claim = atomicAdd(&sched[0], 1);  // answered while this chunk is issued
+      }
+      a = d_lo;
+      n = static_cast<int>(min(32LL, d_hi - d_lo));
+      d_lo += n;
+    };
+    // Lane l < n: request and block of item a + l, and the raw page id (or
+    // the request's first row) whose load stays in flight until finish().
+    struct Group {
+      int n, r, b, L;
+      long long raw;
+    };
+    auto locate = [&](long long a, int n, Group& g) {
+      g.n = n;
+      g.r = -1;
+      g.b = 0;
+      g.L = 0;
+      g.raw = 0;
+      if (n == 0) return;
+      if (!walk_to(geo, topk, a, wr, wstart)) {  // never expected: the items outnumber the pages
+        record_error(err, MSA_DEVERR_TIMEOUT, 1100000);
+        g.n = 0;
+        return;
+      }
+      if (lane < n) {
+        const long long item = a + lane;
+        int rl = wr;
+        long long rs = wstart;
+        int nbl = scored_blocks(geo, rl, topk, nullptr);
+        while (item >= rs + nbl) {
+          rs += nbl;
+          if (++rl >= B) break;
+          nbl = scored_blocks(geo, rl, topk, nullptr);
+        }
+        if (rl < B) {
+          g.r = rl;
+          g.b = static_cast<int>(item - rs);
+          g.L = geo.seq_lens[rl];
+          g.raw = geo.page_table ? static_cast<long long>(geo.page_table[static_cast<long long>(rl) * mb + g.b])
+                                 : geo.cu_k[rl];
+        }
+      }
+    };
+    // first row and key count of the lane's page (0 keys: nothing to copy)
+    auto finish = [&](const Group& g, long long& row0, int& rows) {
+      row0 = 0;
+      rows = 0;
+      if (lane >= g.n || g.r < 0) return;
+      const int want = min(kBlock, g.L - g.b * kBlock);
+      bool ok;
+      if (geo.page_table) {
+        row0 = g.raw * kBlock;
+        ok = g.raw >= 0 && row0 + kBlock <= geo.num_slots;
+        if (!ok) record_error(err, MSA_DEVERR_PAGE, static_cast<long long>(g.r) * mb + g.b);
+      } else {
+        row0 = g.raw + static_cast<long long>(g.b) * kBlock;
+        ok = row0 >= 0 && row0 + want <= geo.num_slots;
+        if (!ok) record_error(err, MSA_DEVERR_PAGE, g.r);
+      }
+      rows = ok && want > 0 ? want : 0;
+    };
+    Group cur, nxt;
+    {
+      long long a = 0;
+      int n;
+      next_group(a, n);
+      locate(a, n, cur);
+    }
+    while (cur.n > 0) {
+      long long row0;
+      int rows_l;
+      finish(cur, row0, rows_l);
+      {
+        long long a = 0;
+        int n;
+        next_group(a, n);
+        locate(a, n, nxt);
+      }
+      for (int k = 0; k < cur.n; ++k, ++i) {
         const long long pr0 = __shfl_sync(0xffffffffu, row0, k);
-        const int rows = __shfl_sync(0xffffffffu, ok, k);
+        const int rows = __shfl_sync(0xffffffffu, rows_l, k);
+        const int rk = __shfl_sync(0xffffffffu, cur.r, k);
+        const int bk = __shfl_sync(0xffffffffu, cur.b, k);
         if (lane == 0) {
           const int s = i % kStages;
-          mbar_wait(&sm.empty[s], ((i / kStages) & 1) ^ 1, err, 101);
-          sm.meta[s] = SelMeta{r, b + k, rows, 0};
+          if (!mbar_wait(&sm.empty[s], ((i / kStages) & 1) ^ 1, err, 101)) alive = 0;
+          sm.meta[s] = SelMeta{rk, bk, rows, 0};
           if (rows > 0) {
-            mbar_expect_tx(&sm.full[s], static_cast<uint32_t>(rows * kRowBytes));
+            mbar_expect_tx(&sm.full[s], static_cast<uint32_t>((rows + kKvHeads) * kRowBytes));
             tma_bulk_g2s(sm.ring + s * kPageBytes, index_k + pr0 * kRowBytes, static_cast<uint32_t>(rows * kRowBytes),
                          &sm.full[s]);
+            tma_bulk_g2s(sm.qs[s], index_q + static_cast<long long>(rk) * kKvHeads * kRowBytes,
+                         static_cast<uint32_t>(kKvHeads * kRowBytes), &sm.full[s]);
           } else {
             mbar_arrive(&sm.full[s]);
           }
         }
         __syncwarp();
       }
-      b += cnt;
-      if (b == nbr && i < n_items) {
-        b = 0;
-        do {
-          ++r;
-        } while (scored_blocks(geo, r, topk, nullptr) == 0);
+      alive = __shfl_sync(0xffffffffu, alive, 0);
+      if (!alive) break;
+      cur = nxt;
+    }
+    // one end marker per consumer warp: consecutive stages go to distinct warps
+    for (int k = 0; k < kSelConsumers; ++k, ++i) {
+      if (lane == 0) {
+        const int s = i % kStages;
+        mbar_wait(&sm.empty[s], ((i / kStages) & 1) ^ 1, err, 101);
+        sm.meta[s] = SelMeta{kSelEnd, 0, 0, 0};
+        mbar_arrive(&sm.full[s]);
       }
+      __syncwarp();
     }
     // No copy may still be landing when the CTA exits, also after a wait gave
     // up: wait (bounded) for the last fill of every stage.  Only this thread
     // arms the full barriers, so that phase cannot have been passed.
-    if (lane == 0)
+    if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
         const int f = (i - s + kStages - 1) / kStages;  // fills of stage s
         if (f > 0) mbar_wait(&sm.full[s], (f - 1) & 1, err, 102);
       }
+      // This CTA claims nothing more (its claims are ordered before the count
+      // by the fence): the last CTA to be counted puts both counters back to 0.
+      __threadfence();
+      if (atomicAdd(&sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+        atomicExch(&sched[0], 0);
+        atomicExch(&sched[1], 0);
+      }
+    }
     return;
   }
 
   // ---------------- consumer warps: whole pages, round-robin ----------------
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int g8 = lane >> 2, t4 = lane & 3;
-  int cur_r = -1;
   uint32_t qf[4][4];
-  for (int i = warp; i < n_items; i += kSelConsumers) {
+  for (int i = warp;; i += kSelConsumers) {
     const int s = i % kStages;
-    mbar_wait(&sm.full[s], (i / kStages) & 1, err, 100);
+    if (!mbar_wait(&sm.full[s], (i / kStages) & 1, err, 100)) break;  // gave up: stop consuming
     const SelMeta meta = sm.meta[s];
+    if (meta.r == kSelEnd) break;
     if (meta.r < 0 || meta.r >= B || meta.b < 0 || meta.b >= mb) {  // never expected: guard the stores
       record_error(err, MSA_DEVERR_TIMEOUT, 1000000 + i);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[s]);
       continue;
     }
-    if (meta.r != cur_r) {
-      cur_r = meta.r;
+    const int cur_r = meta.r;
+    {
+      // the request's index query, landed with the page
       constexpr int kQChunks = kE4M3 ? 2 : 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) qf[j][0] = qf[j][1] = qf[j][2] = qf[j][3] = 0u;
-      if (g8 < kKvHeads) {
+      if (g8 < kKvHeads && meta.rows > 0) {
+        const uint32_t qbase = smem_u32(sm.qs[s]) + g8 * kRowBytes + 16 * t4;
 #pragma unroll
         for (int j = 0; j < kQChunks; ++j) {
           // bf16: dims 32j + 8t .. +8 ; e4m3: dims 64j + 16t .. +16 -- both at byte 64j + 16t
-          const uint4 v = *reinterpret_cast<const uint4*>(
-              index_q + (static_cast<long long>(cur_r) * kKvHeads + g8) * kRowBytes + 64 * j + 16 * t4);
+          const uint4 v = lds128(qbase + 64 * j);
           qf[j][0] = v.x;
           qf[j][1] = v.y;
           qf[j][2] = v.z;
@@ -434,6 +560,7 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
                                                           int32_t* __restrict__ q2k, int topk, int init, int local,
                                                           DevError* err) {
   __shared__ unsigned long long cand[kKvHeads][kCandCap];
+  __shared__ int ids[kKvHeads][kMaxTopk];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the scores are complete: a programmatic dependent (the decode attention)
   // may now be scheduled and run its prologue; it waits for this grid to end
@@ -445,13 +572,13 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
   int nb;
   scored_blocks(geo, r, topk, &nb);
   topk_row(scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks, nb, topk, init, local,
-           q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h]);
+           q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h], ids[h]);
 }
 
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
-                                 DevError* err, cudaStream_t stream) {
+                                 int* sched, DevError* err, cudaStream_t stream) {
   if (const cudaError_t e0 = launch_prologue(); e0 != cudaSuccess) return e0;
   DecodeGeom geo{seq_lens, page_table, cu_k, batch, max_blocks, num_slots};
   // one CTA per SM; never more CTAs than pages
@@ -464,12 +591,12 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
     auto k = decode_select_kernel<1>;
     const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, err);
+    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, sched, err);
   } else {
     auto k = decode_select_kernel<0>;
     const size_t smem = sizeof(SelSmem<kSelRingBytes / (kBlock * kIdxDim * 2)>) + 1024;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, err);
+    k<<<grid, kSelThreads, smem, stream>>>(iq, ik, geo, scores, cfg.topk, sched, err);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -549,10 +676,11 @@ extern "C" msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, co
   auto* base = static_cast<uint8_t*>(noalloc_scratch(&e));
   if (!base) return cuda_fail(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the error word must start at zero; the scores are stored before they are read
+  // the error word and the scorer's claim counters (both in the header) must
+  // start at zero; the scores are stored before they are read
   if (const cudaError_t ce = cudaMemsetAsync(base, 0, off_scores, s); ce != cudaSuccess) return cuda_fail(ce);
   e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,
                            num_slots, q2k, reinterpret_cast<float*>(base + off_scores),
-                           reinterpret_cast<DevError*>(base), s);
+                           reinterpret_cast<int*>(base + kSelSchedOffset), reinterpret_cast<DevError*>(base), s);
   return cuda_result(e);
 }

@@ -29,6 +29,15 @@
 // partial (max, sum, unnormalised O); the CTA whose atomic ticket completes the
 // segment (no waiting) merges the partials and writes bf16.
 //
+// Small batches (few segments) take a second launch shape: one thread-block
+// cluster of C = 2, 4 or 8 CTAs per segment, each CTA a contiguous share of
+// its units, the C states merged by the cluster's first CTA over distributed
+// shared memory.  The stream-K merge costs a CTA an fp32 partial store, a
+// fence, an atomic and dependent L2 reads of the other partials (6-9 us at
+// the end of a small decode step, more than the streaming itself for a few
+// requests); the cluster merge is two cluster barriers and one read of the
+// peers' shared memory.
+//
 // FP8 main K/V cache (TensorRT-LLM field fuse_qkv_index_projection: the M3 path
 // uses "an FP8 main KV cache"): the caches hold E4M3 bytes standing for
 // k_scale * k and v_scale * v.  A chunk is then 64 keys x 128 bytes of K and of
@@ -38,6 +47,8 @@
 // same MMA code in fp16 (q rounded to fp16 once per segment, P rounded to fp16).
 // k_scale is folded into the softmax scale and v_scale into the normalisation.
 #include <cuda_fp8.h>
+
+#include <mutex>
 
 #include "launch.h"
 
@@ -260,22 +271,104 @@ __device__ __forceinline__ void fp8_stage_to_f16(const uint8_t* src, uint8_t* ds
   }
 }
 
+constexpr int kMaxCluster = 8;
+
+// Cluster split (kSplit): the CTAs of one cluster each hold their share of a
+// (query, KV head) segment as an unnormalised state (m, l, O) in comb slot 0
+// of their own shared memory.  Every thread of the cluster calls this once.
+// After the first cluster barrier the CTA of rank 0 reads the other CTAs'
+// states through distributed shared memory, merges them and stores the
+// output rows; the second barrier keeps the other CTAs (and their shared
+// memory) alive until it has read them.
+template <int kFp8, class Smem>
+__device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int lane, float v_scale,
+                                             __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
+                                             uint8_t* __restrict__ out_scale) {
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (blockIdx.x % csize == 0 && warp == 0) {
+    const int seg = blockIdx.x / csize, qi = seg / kKvHeads, g = seg % kKvHeads;
+    const int row = lane >> 1, d0 = (lane & 1) * 64;
+    float mc[kMaxCluster], lc[kMaxCluster];
+#pragma unroll
+    for (int x = 0; x < kMaxCluster; ++x) {
+      mc[x] = x < csize ? ld_dsmem_f32(dsmem_addr(&sm.comb_m[0][row], x)) : -INFINITY;
+      lc[x] = x < csize ? ld_dsmem_f32(dsmem_addr(&sm.comb_l[0][row], x)) : 0.f;
+    }
+    float Mg = -INFINITY;
+#pragma unroll
+    for (int x = 0; x < kMaxCluster; ++x) Mg = fmaxf(Mg, mc[x]);
+    const float Mgu = Mg == -INFINITY ? 0.f : Mg;
+    float Lg = 0.f, ag[64];
+#pragma unroll
+    for (int d = 0; d < 64; ++d) ag[d] = 0.f;
+#pragma unroll
+    for (int x = 0; x < kMaxCluster; ++x) {
+      mc[x] = exp2f(mc[x] - Mgu);  // the CTA's weight (0 for an empty state and past csize)
+      Lg += lc[x] * mc[x];
+    }
+#pragma unroll 2
+    for (int x = 0; x < csize; ++x) {
+      const uint32_t src = dsmem_addr(&sm.comb[0][row][d0], x);
+      float4 xs[16];
+#pragma unroll
+      for (int d = 0; d < 16; ++d) xs[d] = ld_dsmem_v4(src + 16 * d);
+      const float f = mc[x];
+#pragma unroll
+      for (int d = 0; d < 16; ++d) {
+        ag[4 * d] += xs[d].x * f;
+        ag[4 * d + 1] += xs[d].y * f;
+        ag[4 * d + 2] += xs[d].z * f;
+        ag[4 * d + 3] += xs[d].w * f;
+      }
+    }
+    const float inv = Lg > 0.f ? (kFp8 ? v_scale : 1.f) / Lg : 0.f;
+    const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+    if (out_q) {
+      store_mxfp8_64(ag, inv, out_q + oelem, out_scale + oelem / 32);
+    } else {
+      __nv_bfloat16* orow = out + oelem;
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        reinterpret_cast<uint4*>(orow)[v] = make_uint4(
+            pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
+            pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
+    }
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+}
+
 // out_q / out_scale: when non-null, the output is emitted as MXFP8 there
 // instead of bf16 in `out`.  kFp8: the K / V caches hold E4M3 bytes;
 // scale_log2 then includes k_scale, and v_scale multiplies the output.
-template <int kFp8>
+// kSplit: launched in clusters of csize CTAs, one cluster per (query, KV
+// head) segment; CTA rank r takes units [r topk / csize, (r + 1) topk / csize)
+// of it, and the cluster merges on chip (split_finish).  Otherwise stream-K:
+// the units are split evenly over the grid and cut segments are merged
+// through fp32 partials in global memory and a ticket per segment.
+template <int kFp8, int kSplit>
 __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
     float scale_log2, float v_scale, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
-    uint8_t* __restrict__ out_scale, float* __restrict__ partials, int* __restrict__ tickets, DevError* err) {
+    uint8_t* __restrict__ out_scale, float* __restrict__ partials, int* __restrict__ tickets, int csize,
+    DevError* err) {
   extern __shared__ uint8_t smem_raw[];
   AttSmem<kFp8>& sm =
       *reinterpret_cast<AttSmem<kFp8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
-  const long long lo = seg_begin(blockIdx.x, N, G), hi = seg_begin(blockIdx.x + 1, N, G);
+  long long lo, hi;
+  if constexpr (kSplit != 0) {
+    const long long seg = blockIdx.x / csize, rank = blockIdx.x % csize;
+    lo = seg * topk + rank * topk / csize;
+    hi = seg * topk + (rank + 1) * topk / csize;
+  } else {
+    lo = seg_begin(blockIdx.x, N, G);
+    hi = seg_begin(blockIdx.x + 1, N, G);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < kAttStages; ++s) {
@@ -308,7 +401,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   // written before that grid has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
-  if (lo >= hi) return;
+  if (lo >= hi) {
+    if constexpr (kSplit != 0) {
+      // no unit (csize > topk, never chosen by the host): an empty state
+      if (warp == 0)
+        for (int i = lane; i < kGroup * kDim; i += 32) sm.comb[0][i / kDim][i % kDim] = 0.f;
+      if (warp == 0 && lane < kGroup) {
+        sm.comb_m[0][lane] = -INFINITY;
+        sm.comb_l[0][lane] = 0.f;
+      }
+      split_finish<kFp8>(sm, csize, warp, lane, v_scale, out, out_q, out_scale);
+    }
+    return;
+  }
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
@@ -393,6 +498,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         if (f > 0) mbar_wait(&sm.seg_full[s], (f - 1) & 1, err, 221);
       }
     }
+    __syncwarp();
+    if constexpr (kSplit != 0) split_finish<kFp8>(sm, csize, warp, lane, v_scale, out, out_q, out_scale);
     return;
   }
 
@@ -553,6 +660,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     __syncwarp();
     state_to_smem(st, sm, 0, g8, t4);  // staging for coalesced stores (slot 0 is read only by warp 0)
     __syncwarp();
+    if constexpr (kSplit != 0) continue;  // the cluster merges slot 0 (split_finish)
     // ---- warp 0 writes: lane -> row lane/2, 64 dims ----
     const int row = lane >> 1, d0 = (lane & 1) * 64;
     const float M = sm.comb_m[0][row], Lsum = sm.comb_l[0][row];
@@ -653,6 +761,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       }
     }
   }
+  if constexpr (kSplit != 0) split_finish<kFp8>(sm, csize, warp, lane, v_scale, out, out_q, out_scale);
 }
 
 // ---- host side --------------------------------------------------------------------
@@ -705,6 +814,41 @@ size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof
 // one merge counter per CTA of the persistent grid (at most kNumSMs CTAs)
 size_t attend_tickets_bytes() { return static_cast<size_t>(kNumSMs) * sizeof(int); }
 
+// How many clusters of c CTAs of the split kernel can be resident at once
+// (cudaOccupancyMaxActiveClusters, asked once per device, K/V type and c; 0
+// when the query fails, which keeps the stream-K kernel).
+static int max_active_clusters(int kv_fp8, int c) {
+  static std::mutex mu;
+  static int cache[64][2][kMaxCluster + 1];
+  static bool done[64][2][kMaxCluster + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][kv_fp8][c]) return cache[dev][kv_fp8][c];
+  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
+  auto kern = kv_fp8 ? sparse_attend_kernel<1, 1> : sparse_attend_kernel<0, 1>;
+  int n = 0;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(c * 16));
+  lc.blockDim = dim3(kAttThreads);
+  lc.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess) {
+    cudaGetLastError();  // a failed query leaves no error behind for the launch that follows
+    n = 0;
+  }
+  cache[dev][kv_fp8][c] = n;
+  done[dev][kv_fp8][c] = true;
+  return n;
+}
+
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,
                                  const int32_t* q2k, int topk, float scale, void* out, uint8_t* out_q,
                                  uint8_t* out_scale, float* partials, int* tickets, DevError* err,
@@ -714,33 +858,56 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   const bool maps = kv_fp8 ? make_kv_map8(&kmap, k, geo.num_rows) && make_kv_map8(&vmap, v, geo.num_rows)
                            : make_kv_map(&kmap, k, geo.num_rows) && make_kv_map(&vmap, v, geo.num_rows);
   if (!maps || !make_q_map(&qmap, q, geo.nq)) return cudaErrorInvalidValue;
-  // At least 4 units per CTA: a segment is then shared by at most ~topk/4 + 1
-  // CTAs, which bounds the partials its last CTA has to merge.
-  const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
-  long long grid_l = (N + 3) / 4;
-  if (grid_l > kNumSMs) grid_l = kNumSMs;
-  if (grid_l < 1) grid_l = 1;
-  const int grid = static_cast<int>(grid_l);
-  auto kern = kv_fp8 ? sparse_attend_kernel<1> : sparse_attend_kernel<0>;
-  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  // an FP8 cache holds k / k_scale: the scores are scaled by k_scale as well
   const float scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
+  const long long S = static_cast<long long>(geo.nq) * kKvHeads;  // (query, KV head) segments
+  const long long N = S * topk;
+  // Few segments (small batches): one cluster of C CTAs per segment, merged
+  // on chip -- the largest C in {8, 4, 2} with C <= topk (every CTA gets a
+  // unit), at most one CTA per SM, and every cluster resident at once.
+  // Otherwise stream-K over the whole grid.
+  int C = 0;
+  for (int c = kMaxCluster; c >= 2 && !C; c >>= 1) {
+    if (c > topk || S * c > kNumSMs) continue;
+    const int fit = max_active_clusters(kv_fp8, c);
+    if (fit > 0 && S <= fit) C = c;
+  }
+  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
   // a programmatic dependent of the previous kernel in the stream (the kernel
   // waits for that grid before touching memory), so its launch and prologue
   // overlap the decode top-k
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(grid));
   lc.blockDim = dim3(kAttThreads);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kern, kmap, vmap, qmap, q2k, geo, topk, scale_log2, kv_fp8 ? v_scale : 1.f,
-                            static_cast<__nv_bfloat16*>(out), out_q, out_scale, partials, tickets, err);
+  const float vs = kv_fp8 ? v_scale : 1.f;
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if (C) {
+    lc.gridDim = dim3(static_cast<unsigned>(S * C));
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.numAttrs = 2;
+    auto kern = kv_fp8 ? sparse_attend_kernel<1, 1> : sparse_attend_kernel<0, 1>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    return cudaLaunchKernelEx(&lc, kern, kmap, vmap, qmap, q2k, geo, topk, scale_log2, vs, o, out_q, out_scale,
+                              static_cast<float*>(nullptr), static_cast<int*>(nullptr), C, err);
+  }
+  // At least 4 units per CTA: a segment is then shared by at most ~topk/4 + 1
+  // CTAs, which bounds the partials its last CTA has to merge.
+  long long grid_l = (N + 3) / 4;
+  if (grid_l > kNumSMs) grid_l = kNumSMs;
+  if (grid_l < 1) grid_l = 1;
+  lc.gridDim = dim3(static_cast<unsigned>(grid_l));
+  auto kern = kv_fp8 ? sparse_attend_kernel<1, 0> : sparse_attend_kernel<0, 0>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  return cudaLaunchKernelEx(&lc, kern, kmap, vmap, qmap, q2k, geo, topk, scale_log2, vs, o, out_q, out_scale,
+                            partials, tickets, 1, err);
 }
 
 }  // namespace msa

@@ -111,8 +111,9 @@ msa_status msa_config_check(const msa_config* cfg);
  *   MSA_MODE_PACK   : n = batch * seq of the document map, max_blocks = batch.
  *   MSA_MODE_PREFILL_BWD: as MSA_MODE_PREFILL, for msa_sparse_attend_prefill_backward.
  * The workspace must be zero-filled once before its first use (see
- * msa_workspace_init), which clears the device error word in its first 256
- * bytes and the completion counters.  Every call that completes leaves its
+ * msa_workspace_init), which clears the device error word and the decode
+ * scorer's two page-claim counters in its first 256 bytes, and the
+ * completion counters.  Every call that completes leaves its
  * counters at zero again (the decode calls enqueue no memset; the prefill
  * calls clear theirs with a cudaMemsetAsync on `stream`), and the scorer
  * stores rather than accumulates (NeMo _score_scratch).  In the decode layout
@@ -223,6 +224,11 @@ msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, const void* i
  * top-k).  Before that kernel has completed it reads no input and writes no
  * output; it only issues L2 prefetch hints for its requests' page-table rows,
  * which change no memory, so stream order is kept whatever precedes it.
+ * Up to 19 requests, each (request, KV head) segment is shared by a cluster
+ * of 2-8 CTAs that merges on chip; larger batches are split evenly over one
+ * CTA per SM with merges through the workspace.  The first call on a device
+ * asks the runtime how many clusters can be resident at once
+ * (cudaOccupancyMaxActiveClusters, once per cluster size and K/V type).
  */
 msa_status msa_sparse_attend_decode(const msa_config* cfg, const void* q, const void* k_cache,
                                     const void* v_cache, const int32_t* q2k,

@@ -49,6 +49,40 @@ def test_decode_many_requests():
     _run(d, 16, 1, 1)
 
 
+@pytest.mark.parametrize("n_req,topk", [(1, 16), (3, 16), (4, 16), (2, 3), (4, 5), (6, 16), (9, 16), (12, 16),
+                                        (19, 16), (20, 16), (40, 16), (5, 1)])
+def test_decode_request_counts(n_req, topk):
+    """Small batches run the attention as one cluster of CTAs per (request, KV
+    head) segment, merged through distributed shared memory: clusters of 8 for
+    up to 4 requests, of 4 up to 9, of 2 up to 19, never more CTAs per cluster
+    than topk (so topk 3 takes clusters of 2, topk 5 of 4 with shares 1, 1, 1, 2,
+    topk 1 none).  From 20 requests on, stream-K with merges through global
+    memory.  Every size against the oracle."""
+    lens = np.random.default_rng(100 + n_req).integers(1, 20000, size=n_req).tolist()
+    d = msa_synth.decode_inputs(lens, paged=True, seed=100 + n_req, device="cuda")
+    _run(d, topk, 0, 1 if topk > 1 else 0, f"decode {n_req} requests")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_small_batch_mxfp8_and_fp8_kv(paged):
+    # the cluster-merged attention (3 requests: clusters of 8) with both output
+    # and cache variants: MXFP8 equal to the quantised bf16 output, FP8 K/V against the oracle
+    d = msa_synth.decode_inputs([9000, 300, 20000], paged=paged, seed=13, device="cuda")
+    kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+    q2k, out = _run(d, 16, 0, 1, "decode 3 requests")
+    oq, osc = msa.msa_sparse_attend_decode_mxfp8(d.q, d.k_cache, d.v_cache, q2k, d.seq_lens, scale=SCALE, **kw)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_quantize(out.reshape(out.shape[0], -1))
+    assert np.array_equal(oq.cpu().numpy(), rq) and np.array_equal(osc.cpu().numpy(), rs)
+    k8, v8 = _fp8_caches(d, 0.25, 0.5)
+    out8 = msa.msa_sparse_attend_decode_fp8kv(d.q, k8, v8, q2k, d.seq_lens, k_scale=0.25, v_scale=0.5, scale=SCALE,
+                                              **kw)
+    torch.cuda.synchronize()
+    ref = oracle.attend_decode_fp8(d.q, k8, v8, d.seq_lens, q2k.cpu().numpy(), SCALE, k_scale=0.25, v_scale=0.5,
+                                   page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k)
+    check_out(out8, ref, f"decode attention, FP8 K/V, 3 requests ({'paged' if paged else 'contiguous'})")
+
+
 def test_decode_e4m3_small():
     d = msa_synth.decode_inputs(SMALL_LENS, paged=True, index_dtype="e4m3", seed=3, device="cuda")
     _run(d, 16, 0, 1)
@@ -106,6 +140,17 @@ def test_decode_workspace_shared_across_batch_sizes():
     q2k_b, out_b = _run(big, 16, 0, 1, "decode 64 requests, after the 4-request call", workspace=ws)
     assert torch.equal(q2k_a, q2k_b) and torch.equal(out_a, out_b)
     assert ws.read_device_error() == (0, 0)
+    # the scorer's two page-claim counters (header bytes 128-135) are back at zero
+    assert not ws.buf[128:136].any().item()
+
+
+def test_decode_select_walks_past_unscored_requests():
+    """Scored requests (more than topk blocks) between long runs of short
+    requests that need no scoring: the scorer's page claims walk past 150
+    requests at a time, and a claim's pages cross from one request to the next."""
+    lens = [100] * 150 + [40000] + [90] * 170 + [30000, 5000, 2100, 2200, 2177]
+    d = msa_synth.decode_inputs(lens, paged=True, seed=91, device="cuda")
+    _run(d, 16, 1, 1, "decode, long runs of unscored requests")
 
 
 def test_decode_bad_page_is_reported_not_faulted():
