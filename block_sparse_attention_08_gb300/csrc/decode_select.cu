@@ -81,14 +81,15 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 }
 
 // Exact top-`need` by (score desc, id asc) over the non-forced blocks of one
-// (request, head) row, then the ascending q2k row.  One warp.  Rows of up to
-// 32 x 32 candidates are read once into registers with independent loads.
-// The need-th largest of the 32 lane maxima is a threshold that at least
-// `need` candidates reach, so it keeps every one of the top `need`; those
-// candidates (a few more than `need` as a rule) go to shared memory, where
-// each lane ranks its own against all of them.  Ranks, not rounds of a
-// warp-wide argmax: no step waits on a chain of dependent shuffles.
-constexpr int kTopkRegs = 32;
+// (request, head) row, then the ascending q2k row.  One warp.  The row's
+// scores are staged in shared memory first (rows of up to kTopkStage blocks;
+// longer rows are read from global memory as they go).  The need-th largest
+// of the 32 lane maxima is a threshold that at least `need` candidates reach,
+// so it keeps every one of the top `need`; those candidates (a few more than
+// `need` as a rule) go to shared memory, where each lane ranks its own
+// against all of them.  Ranks, not rounds of a warp-wide argmax, and no loop
+// waits on a global load per step.
+constexpr int kTopkStage = 1024;
 
 __device__ __forceinline__ unsigned long long score_key(float v, int b) {
   return (static_cast<unsigned long long>(float_key(v)) << 32) | (0xffffffffu - static_cast<uint32_t>(b));
@@ -97,8 +98,10 @@ __device__ __forceinline__ int key_block(unsigned long long key) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
 }
 
-// cand: kCandCap keys of shared memory; ids: kMaxTopk ints of shared memory.
-__device__ void topk_row(const float* s, int nb, int topk, int init, int local, int32_t* out,
+// s: the row in global memory; stage: the same row in shared memory when
+// nb <= kTopkStage (else unused); cand: kCandCap keys and ids: kMaxTopk ints
+// of shared memory.
+__device__ void topk_row(const float* s, const float* stage, int nb, int topk, int init, int local, int32_t* out,
                          unsigned long long* cand, int* ids) {
   const int lane = threadIdx.x & 31;
   if (nb <= topk) {
@@ -107,27 +110,13 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
   }
   const int need = topk - init - local;
   const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi), more than `need` of them
+  const bool staged = nb <= kTopkStage;
+  auto key_at = [&](int b) { return score_key(staged ? stage[b] : __ldcg(s + b), b); };
   if (need > 0) {
-    const bool in_regs = c_hi - c_lo <= 32 * kTopkRegs;
-    float v[kTopkRegs];
     unsigned long long best = 0;  // real keys are nonzero; a lane without candidates keeps 0
-    if (in_regs) {
-#pragma unroll
-      for (int k = 0; k < kTopkRegs; ++k) {
-        const int b = c_lo + lane + 32 * k;
-        v[k] = b < c_hi ? __ldcg(s + b) : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < kTopkRegs; ++k) {
-        const int b = c_lo + lane + 32 * k;
-        const unsigned long long key = b < c_hi ? score_key(v[k], b) : 0ull;
-        best = key > best ? key : best;
-      }
-    } else {
-      for (int b = c_lo + lane; b < c_hi; b += 32) {
-        const unsigned long long key = score_key(__ldcg(s + b), b);
-        best = key > best ? key : best;
-      }
+    for (int b = c_lo + lane; b < c_hi; b += 32) {
+      const unsigned long long key = key_at(b);
+      best = key > best ? key : best;
     }
     // rank of this lane's maximum among the 32 (real keys are distinct and
     // at least need + 1 lanes hold one, so exactly one lane has rank need - 1)
@@ -137,7 +126,9 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
     const unsigned who = __ballot_sync(0xffffffffu, rk == need - 1);
     const unsigned long long theta = __shfl_sync(0xffffffffu, best, who ? __ffs(who) - 1 : 0);
     int count = 0;
-    auto consider = [&](unsigned long long key) {
+    for (int b0 = c_lo; b0 < c_hi; b0 += 32) {
+      const int b = b0 + lane;
+      const unsigned long long key = b < c_hi ? key_at(b) : 0ull;
       const bool c = key >= theta && key != 0ull;
       const unsigned m = __ballot_sync(0xffffffffu, c);
       if (c) {
@@ -145,18 +136,6 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
         if (slot < kCandCap) cand[slot] = key;
       }
       count += __popc(m);
-    };
-    if (in_regs) {
-#pragma unroll
-      for (int k = 0; k < kTopkRegs; ++k) {
-        const int b = c_lo + lane + 32 * k;
-        consider(b < c_hi ? score_key(v[k], b) : 0ull);
-      }
-    } else {
-      for (int b0 = c_lo; b0 < c_hi; b0 += 32) {
-        const int b = b0 + lane;
-        consider(b < c_hi ? score_key(__ldcg(s + b), b) : 0ull);
-      }
     }
     __syncwarp();
     if (count <= kCandCap) {
@@ -164,6 +143,7 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
       const unsigned long long e0 = lane < count ? cand[lane] : 0ull;
       const unsigned long long e1 = lane + 32 < count ? cand[lane + 32] : 0ull;
       int r0 = 0, r1 = 0;
+#pragma unroll 8
       for (int j = 0; j < count; ++j) {
         const unsigned long long c = cand[j];
         r0 += c > e0 ? 1 : 0;
@@ -177,7 +157,7 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
       for (int i = 0; i < need; ++i) {
         unsigned long long m = 0;
         for (int b = c_lo + lane; b < c_hi; b += 32) {
-          const unsigned long long key = score_key(__ldcg(s + b), b);
+          const unsigned long long key = key_at(b);
           if (key < prev && key > m) m = key;
         }
         for (int o = 16; o > 0; o >>= 1) {
@@ -196,7 +176,8 @@ __device__ void topk_row(const float* s, int nb, int topk, int init, int local, 
   if (lane < topk) {
     const int id = ids[lane];
     int pos = 0;
-    for (int j = 0; j < topk; ++j) pos += ids[j] < id ? 1 : 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) pos += j < topk && ids[j] < id ? 1 : 0;
     out[pos] = id;
   }
 }
@@ -559,6 +540,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
 __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
                                                           int32_t* __restrict__ q2k, int topk, int init, int local,
                                                           DevError* err) {
+  __shared__ float stage[kKvHeads][kTopkStage];
   __shared__ unsigned long long cand[kKvHeads][kCandCap];
   __shared__ int ids[kKvHeads][kMaxTopk];
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -566,13 +548,24 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
   // may now be scheduled and run its prologue; it waits for this grid to end
   // before it reads q2k
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int r = blockIdx.x, h = threadIdx.x >> 5;
+  const int r = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* row = scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks;
+  // stage the row's first min(max_blocks, kTopkStage) scores -- all loads in
+  // flight together, and together with the length; entries past the
+  // request's blocks are never used
+  const int ns = min(geo.max_blocks, kTopkStage);
+#pragma unroll
+  for (int k = 0; k < kTopkStage / 32; ++k) {
+    const int b = lane + 32 * k;
+    if (b < ns) cp_async_4(&stage[h][b], row + b);
+  }
   const int L = geo.seq_lens[r];
+  cp_async_wait_all();
+  __syncwarp();
   if (threadIdx.x == 0 && (L < 1 || L > geo.max_blocks * kBlock)) record_error(err, MSA_DEVERR_LENGTH, r);
-  int nb;
-  scored_blocks(geo, r, topk, &nb);
-  topk_row(scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks, nb, topk, init, local,
-           q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h], ids[h]);
+  const int nb = L < 1 ? 0 : min((L + kBlock - 1) / kBlock, geo.max_blocks);
+  topk_row(row, stage[h], nb, topk, init, local, q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h],
+           ids[h]);
 }
 
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,

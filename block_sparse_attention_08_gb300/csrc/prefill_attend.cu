@@ -23,16 +23,29 @@
 // schedules the tiles (descriptors and entries read ahead from global memory,
 // published in a shared-memory ring) and issues TMA (Q rows gathered with a
 // 3-D tensor map, one 16-head box per entry; K and V blocks as 128-row boxes);
-// warp 17 issues the MMAs from one thread.  Two softmax warpgroups (warps 0-7)
-// and two epilogue warpgroups (warps 8-15) take the even and the odd tiles, so
-// two tiles are in their softmax and two in their epilogue at a time; in each,
-// a thread owns one tensor-memory lane (query row).  Each entry's result is
-// written as a partial: row max (log2 units) and row sum of p in fp32, and the
-// unnormalised O / 128 in fp16; a merge kernel combines the <= topk partials
-// of a (query, KV head) pair into the bf16 output.  Tiles are handed out in
-// chunks of 16, round-robin over the persistent grid, so all CTAs move through
-// the (KV head, window) buckets together and the window's Q rows and K / V
-// blocks stay in L2.
+// warps 17 and 18 issue the S and O MMAs from one thread each.  Two softmax
+// warpgroups (warps 0-7) and two epilogue warpgroups (warps 8-15) take the
+// even and the odd tiles, so two tiles are in their softmax and two in their
+// epilogue at a time; in each, a thread owns one tensor-memory lane (query row).
+//
+// The entries of one (query, KV head) row land in up to topk different tiles,
+// so their results are summed in memory, in two launches against one fixed
+// exponent reference per row:
+//   phase 0: each row's reference entry (its highest valid block, first
+//            occurrence) -- a two-pass softmax stores the reference exponent
+//            mref = rowmax * scale * log2 e, the row sum lacc and the fp32 O
+//            into acc [T][64][128] (tensor-engine stores of 16-row boxes);
+//   phase 1: every other entry -- a one-pass softmax against mref, fp32 O
+//            added into acc by the tensor engine (cp.reduce.async.bulk .add),
+//            the row sum added into lacc;
+// then bm_norm_kernel writes out = acc / lacc in bf16 (and the log-sum-exp
+// mref + log2 lacc for the backward).  A key that exceeds the reference by
+// 2^64 or more leaves fp32's range for the row sum and is reported
+// (MSA_DEVERR_RANGE).  The adds run in whatever order the tiles finish, so
+// repeated calls agree within fp32 rounding, not bit for bit.  Tiles are
+// handed out in chunks of 16, round-robin over the persistent grid, so all
+// CTAs move through the (KV head, window) buckets together and the window's
+// Q rows, K / V blocks and accumulator rows stay in L2.
 #include <cuda_fp16.h>
 
 #include <type_traits>

@@ -276,67 +276,86 @@ constexpr int kMaxCluster = 8;
 // Cluster split (kSplit): the CTAs of one cluster each hold their share of a
 // (query, KV head) segment as an unnormalised state (m, l, O) in comb slot 0
 // of their own shared memory.  Every thread of the cluster calls this once.
-// After the first cluster barrier the CTA of rank 0 reads the other CTAs'
-// states through distributed shared memory, merges them and stores the
-// output rows; the second barrier keeps the other CTAs (and their shared
-// memory) alive until it has read them.
+// After the first cluster barrier every CTA's pipeline is done, so the chunk
+// ring of the CTA of rank 0 is free: each other CTA stores its state into
+// slot rank - 1 there (remote stores, nothing waited on), and after the second
+// barrier rank 0 merges the states from its own shared memory and stores the
+// output rows.
+constexpr int kPushFloats = 2 * kGroup + kGroup * kDim;  // m[16], l[16], O[16][128]
+
 template <int kFp8, class Smem>
 __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int lane, float v_scale,
                                              __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
                                              uint8_t* __restrict__ out_scale) {
+  static_assert(sizeof(sm.t.stage) >= (kMaxCluster - 1) * kPushFloats * sizeof(float), "push slots");
+  const int rank = blockIdx.x % csize;
+  const int row = lane >> 1, d0 = (lane & 1) * 64;
+  float* slots = reinterpret_cast<float*>(&sm.t.stage[0][0]);
   cluster_arrive_release();
   cluster_wait_acquire();
-  if (blockIdx.x % csize == 0 && warp == 0) {
-    const int seg = blockIdx.x / csize, qi = seg / kKvHeads, g = seg % kKvHeads;
-    const int row = lane >> 1, d0 = (lane & 1) * 64;
-    float mc[kMaxCluster], lc[kMaxCluster];
-#pragma unroll
-    for (int x = 0; x < kMaxCluster; ++x) {
-      mc[x] = x < csize ? ld_dsmem_f32(dsmem_addr(&sm.comb_m[0][row], x)) : -INFINITY;
-      lc[x] = x < csize ? ld_dsmem_f32(dsmem_addr(&sm.comb_l[0][row], x)) : 0.f;
+  if (rank != 0 && warp == 0) {
+    float* dst = slots + (rank - 1) * kPushFloats;
+    if ((lane & 1) == 0) {
+      st_dsmem_f32(dsmem_addr(dst + row, 0), sm.comb_m[0][row]);
+      st_dsmem_f32(dsmem_addr(dst + kGroup + row, 0), sm.comb_l[0][row]);
     }
-    float Mg = -INFINITY;
+    const uint32_t o = dsmem_addr(dst + 2 * kGroup + row * kDim + d0, 0);
+    const float* src = &sm.comb[0][row][d0];
 #pragma unroll
-    for (int x = 0; x < kMaxCluster; ++x) Mg = fmaxf(Mg, mc[x]);
-    const float Mgu = Mg == -INFINITY ? 0.f : Mg;
-    float Lg = 0.f, ag[64];
-#pragma unroll
-    for (int d = 0; d < 64; ++d) ag[d] = 0.f;
-#pragma unroll
-    for (int x = 0; x < kMaxCluster; ++x) {
-      mc[x] = exp2f(mc[x] - Mgu);  // the CTA's weight (0 for an empty state and past csize)
-      Lg += lc[x] * mc[x];
-    }
-#pragma unroll 2
-    for (int x = 0; x < csize; ++x) {
-      const uint32_t src = dsmem_addr(&sm.comb[0][row][d0], x);
-      float4 xs[16];
-#pragma unroll
-      for (int d = 0; d < 16; ++d) xs[d] = ld_dsmem_v4(src + 16 * d);
-      const float f = mc[x];
-#pragma unroll
-      for (int d = 0; d < 16; ++d) {
-        ag[4 * d] += xs[d].x * f;
-        ag[4 * d + 1] += xs[d].y * f;
-        ag[4 * d + 2] += xs[d].z * f;
-        ag[4 * d + 3] += xs[d].w * f;
-      }
-    }
-    const float inv = Lg > 0.f ? (kFp8 ? v_scale : 1.f) / Lg : 0.f;
-    const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
-    if (out_q) {
-      store_mxfp8_64(ag, inv, out_q + oelem, out_scale + oelem / 32);
-    } else {
-      __nv_bfloat16* orow = out + oelem;
-#pragma unroll
-      for (int v = 0; v < 8; ++v)
-        reinterpret_cast<uint4*>(orow)[v] = make_uint4(
-            pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
-            pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
-    }
+    for (int d = 0; d < 16; ++d) st_dsmem_v4(o + 16 * d, *reinterpret_cast<const float4*>(src + 4 * d));
   }
   cluster_arrive_release();
   cluster_wait_acquire();
+  if (rank != 0 || warp != 0) return;
+  const int qi = (blockIdx.x / csize) / kKvHeads, g = (blockIdx.x / csize) % kKvHeads;
+  // contributor 0 is this CTA (comb slot 0), contributor x > 0 the ring slot x - 1
+  auto m_of = [&](int x) { return x == 0 ? sm.comb_m[0][row] : slots[(x - 1) * kPushFloats + row]; };
+  auto l_of = [&](int x) { return x == 0 ? sm.comb_l[0][row] : slots[(x - 1) * kPushFloats + kGroup + row]; };
+  auto o_of = [&](int x) {
+    return x == 0 ? &sm.comb[0][row][d0] : slots + (x - 1) * kPushFloats + 2 * kGroup + row * kDim + d0;
+  };
+  float mc[kMaxCluster], lc[kMaxCluster];
+#pragma unroll
+  for (int x = 0; x < kMaxCluster; ++x) {
+    mc[x] = x < csize ? m_of(x) : -INFINITY;
+    lc[x] = x < csize ? l_of(x) : 0.f;
+  }
+  float Mg = -INFINITY;
+#pragma unroll
+  for (int x = 0; x < kMaxCluster; ++x) Mg = fmaxf(Mg, mc[x]);
+  const float Mgu = Mg == -INFINITY ? 0.f : Mg;
+  float Lg = 0.f, ag[64];
+#pragma unroll
+  for (int d = 0; d < 64; ++d) ag[d] = 0.f;
+#pragma unroll
+  for (int x = 0; x < kMaxCluster; ++x) {
+    mc[x] = exp2f(mc[x] - Mgu);  // the CTA's weight (0 for an empty state and past csize)
+    Lg += lc[x] * mc[x];
+  }
+  for (int x = 0; x < csize; ++x) {
+    const float* src = o_of(x);
+    const float f = mc[x];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) {
+      const float4 v = *reinterpret_cast<const float4*>(src + 4 * d);
+      ag[4 * d] += v.x * f;
+      ag[4 * d + 1] += v.y * f;
+      ag[4 * d + 2] += v.z * f;
+      ag[4 * d + 3] += v.w * f;
+    }
+  }
+  const float inv = Lg > 0.f ? (kFp8 ? v_scale : 1.f) / Lg : 0.f;
+  const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
+  if (out_q) {
+    store_mxfp8_64(ag, inv, out_q + oelem, out_scale + oelem / 32);
+  } else {
+    __nv_bfloat16* orow = out + oelem;
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      reinterpret_cast<uint4*>(orow)[v] = make_uint4(
+          pack_bf16(ag[8 * v] * inv, ag[8 * v + 1] * inv), pack_bf16(ag[8 * v + 2] * inv, ag[8 * v + 3] * inv),
+          pack_bf16(ag[8 * v + 4] * inv, ag[8 * v + 5] * inv), pack_bf16(ag[8 * v + 6] * inv, ag[8 * v + 7] * inv));
+  }
 }
 
 // out_q / out_scale: when non-null, the output is emitted as MXFP8 there
