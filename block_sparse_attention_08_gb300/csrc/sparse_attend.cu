@@ -41,20 +41,24 @@
 // FP8 main K/V cache (TensorRT-LLM field fuse_qkv_index_projection: the M3 path
 // uses "an FP8 main KV cache"): the caches hold E4M3 bytes standing for
 // k_scale * k and v_scale * v.  A chunk is then 64 keys x 128 bytes of K and of
-// V (one 128-byte-swizzled box each, 16 KB a stage); the consumer warp that owns
-// the stage converts it into its own fp16 tile with the bf16 stage's layout
-// (every E4M3 value is exact in fp16), releases the stage at once, and runs the
-// same MMA code in fp16 (q rounded to fp16 once per segment, P rounded to fp16).
-// k_scale is folded into the softmax scale and v_scale into the normalisation.
-#include <cuda_fp8.h>
-
+// V (one 128-byte-swizzled box each, 16 KB a stage; 12 stages keep the bf16
+// path's 192 KB in flight).  The consumers read the E4M3 bytes straight into
+// MMA fragments and convert them in registers (every E4M3 value is exact in
+// fp16): K through ldmatrix, with the k slots of the fp16 Q fragments permuted
+// to match; V through the transposing ldmatrix on byte pairs, each 16-dim
+// block feeding an even-dim and an odd-dim n-tile.  q is rounded to fp16 once
+// per segment, P to fp16.  k_scale is folded into the softmax scale and
+// v_scale into the normalisation.
 #include <mutex>
 
 #include "launch.h"
 
 namespace msa {
 
-constexpr int kAttStages = 6;
+constexpr int kAttStages = 6;        // 32 KB stages of a bf16 cache
+constexpr int kAttStages8 = 12;      // 16 KB stages of an FP8 cache: the same 192 KB in flight
+template <int kFp8>
+__host__ __device__ constexpr int att_stages() { return kFp8 ? kAttStages8 : kAttStages; }
 constexpr int kChunkKeys = 64;
 constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 bf16 dims, or 128 E4M3 dims)
 constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
@@ -68,7 +72,8 @@ constexpr int kCombStride = kDim + 8;               // padded fp32 row of the me
 constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
 // stage s is always consumed by warp s % kConsumerWarps, so a warp never waits
 // on a stage more than one mbarrier phase ahead
-static_assert(kAttStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
+static_assert(kAttStages % kConsumerWarps == 0 && kAttStages8 % kConsumerWarps == 0,
+              "stages must be a multiple of the consumer warps");
 
 struct QueryGeo {
   int pos;         // position of the query (keys 0..pos are causal)
@@ -105,15 +110,15 @@ struct SegInfo {
   int nk[kMaxTopk];  // causal keys of each of the segment's units (0 = nothing to do)
 };
 
-// The chunk ring; with an FP8 cache also one fp16 tile per consumer warp.
+// The chunk ring: 64-key chunks of K and V (bf16: 4 boxes of 64 dims; FP8: one
+// 128-byte box each).
 template <int kFp8>
 struct AttTiles {
   alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
 };
 template <>
 struct AttTiles<1> {
-  alignas(1024) uint8_t stage[kAttStages][kAttStage8Bytes];
-  alignas(1024) uint8_t wtile[kConsumerWarps][kAttStageBytes];
+  alignas(1024) uint8_t stage[kAttStages8][kAttStage8Bytes];
 };
 
 template <int kFp8>
@@ -124,8 +129,8 @@ struct AttSmem {
   float comb_m[kConsumerWarps - 1][kGroup];
   float comb_l[kConsumerWarps - 1][kGroup];
   SegInfo seg[kSegSlots];
-  uint64_t full[kAttStages];
-  uint64_t empty[kAttStages];
+  uint64_t full[kAttStages8];
+  uint64_t empty[kAttStages8];
   uint64_t seg_full[kSegSlots];
   uint64_t seg_empty[kSegSlots];
   int bcast;
@@ -147,7 +152,14 @@ struct WarpState {
   float o[16][4];
 };
 
-template <class Smem>
+// Where accumulator column e of n-tile nd of a lane lies.  bf16: n-tile nd is
+// dims 8 nd .. 8 nd + 7 and the lane holds dims 8 nd + 2 t4 + e.  FP8: the V
+// fragments come from byte pairs (see the PV product), so n-tiles 2c and 2c + 1
+// are the even and the odd dims of the 16-dim block c, and the lane's four
+// values of the pair are the consecutive dims 16 c + 4 t4 .. + 3 -- stored and
+// loaded as one float4, in the natural order, so everything that reads the
+// states back (the merges, the output) sees plain rows.
+template <int kFp8, class Smem>
 __device__ __forceinline__ void state_to_smem(const WarpState& st, Smem& sm, int slot, int g8, int t4) {
   if (t4 == 0) {
     sm.comb_m[slot][g8] = st.m0;
@@ -155,14 +167,24 @@ __device__ __forceinline__ void state_to_smem(const WarpState& st, Smem& sm, int
     sm.comb_l[slot][g8] = st.l0;
     sm.comb_l[slot][g8 + 8] = st.l1;
   }
+  if constexpr (kFp8 != 0) {
 #pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    *reinterpret_cast<float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]) = make_float2(st.o[nd][0], st.o[nd][1]);
-    *reinterpret_cast<float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]) = make_float2(st.o[nd][2], st.o[nd][3]);
+    for (int c = 0; c < 8; ++c) {
+      *reinterpret_cast<float4*>(&sm.comb[slot][g8][16 * c + 4 * t4]) =
+          make_float4(st.o[2 * c][0], st.o[2 * c + 1][0], st.o[2 * c][1], st.o[2 * c + 1][1]);
+      *reinterpret_cast<float4*>(&sm.comb[slot][g8 + 8][16 * c + 4 * t4]) =
+          make_float4(st.o[2 * c][2], st.o[2 * c + 1][2], st.o[2 * c][3], st.o[2 * c + 1][3]);
+    }
+  } else {
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      *reinterpret_cast<float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]) = make_float2(st.o[nd][0], st.o[nd][1]);
+      *reinterpret_cast<float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]) = make_float2(st.o[nd][2], st.o[nd][3]);
+    }
   }
 }
 
-template <class Smem>
+template <int kFp8, class Smem>
 __device__ __forceinline__ void merge_from_smem(WarpState& st, const Smem& sm, int slot, int g8, int t4) {
   const float mb0 = sm.comb_m[slot][g8], mb1 = sm.comb_m[slot][g8 + 8];
   const float M0 = fmaxf(st.m0, mb0), M1 = fmaxf(st.m1, mb1);
@@ -173,14 +195,30 @@ __device__ __forceinline__ void merge_from_smem(WarpState& st, const Smem& sm, i
   st.l1 = st.l1 * fa1 + sm.comb_l[slot][g8 + 8] * fb1;
   st.m0 = M0;
   st.m1 = M1;
+  if constexpr (kFp8 != 0) {
 #pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    const float2 x = *reinterpret_cast<const float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]);
-    const float2 y = *reinterpret_cast<const float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]);
-    st.o[nd][0] = st.o[nd][0] * fa0 + x.x * fb0;
-    st.o[nd][1] = st.o[nd][1] * fa0 + x.y * fb0;
-    st.o[nd][2] = st.o[nd][2] * fa1 + y.x * fb1;
-    st.o[nd][3] = st.o[nd][3] * fa1 + y.y * fb1;
+    for (int c = 0; c < 8; ++c) {
+      const float4 x = *reinterpret_cast<const float4*>(&sm.comb[slot][g8][16 * c + 4 * t4]);
+      const float4 y = *reinterpret_cast<const float4*>(&sm.comb[slot][g8 + 8][16 * c + 4 * t4]);
+      st.o[2 * c][0] = st.o[2 * c][0] * fa0 + x.x * fb0;
+      st.o[2 * c + 1][0] = st.o[2 * c + 1][0] * fa0 + x.y * fb0;
+      st.o[2 * c][1] = st.o[2 * c][1] * fa0 + x.z * fb0;
+      st.o[2 * c + 1][1] = st.o[2 * c + 1][1] * fa0 + x.w * fb0;
+      st.o[2 * c][2] = st.o[2 * c][2] * fa1 + y.x * fb1;
+      st.o[2 * c + 1][2] = st.o[2 * c + 1][2] * fa1 + y.y * fb1;
+      st.o[2 * c][3] = st.o[2 * c][3] * fa1 + y.z * fb1;
+      st.o[2 * c + 1][3] = st.o[2 * c + 1][3] * fa1 + y.w * fb1;
+    }
+  } else {
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      const float2 x = *reinterpret_cast<const float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]);
+      const float2 y = *reinterpret_cast<const float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]);
+      st.o[nd][0] = st.o[nd][0] * fa0 + x.x * fb0;
+      st.o[nd][1] = st.o[nd][1] * fa0 + x.y * fb0;
+      st.o[nd][2] = st.o[nd][2] * fa1 + y.x * fb1;
+      st.o[nd][3] = st.o[nd][3] * fa1 + y.y * fb1;
+    }
   }
 }
 
@@ -221,13 +259,8 @@ __device__ __forceinline__ void store_mxfp8_64(const float* v, float inv, uint8_
   }
 }
 
-// The 16-bit MMA type of the attention: bf16 (a bf16 K/V cache) or fp16 (an
-// FP8 K/V cache, converted to fp16 on chip).
-template <int kFp8>
-__device__ __forceinline__ void mma16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  if (kFp8) mma_f16(c, a, b0, b1);
-  else mma_bf16(c, a, b0, b1);
-}
+// The 16-bit type of P: bf16 (a bf16 K/V cache) or fp16 (an FP8 K/V cache,
+// converted to fp16 on chip).
 template <int kFp8>
 __device__ __forceinline__ float round16(float x) {
   return kFp8 ? __half2float(__float2half_rn(x)) : bf16_round(x);
@@ -245,31 +278,25 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   return *reinterpret_cast<uint32_t*>(&h);
 }
-// Two E4M3 bytes (low byte first) -> fp16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
 
-// One FP8 stage (K and V: 64 rows x 128 E4M3 bytes each, 128-byte swizzle) into
-// an fp16 tile laid out like a bf16 stage (K lo, K hi, V lo, V hi: 64 rows x 64
-// dims each, 128-byte swizzle).  Lane work: 16 E4M3 bytes -> two 16-byte fp16 chunks.
-__device__ __forceinline__ void fp8_stage_to_f16(const uint8_t* src, uint8_t* dst, int lane) {
-#pragma unroll 4
-  for (int i = 0; i < 2 * kChunkKeys * 8 / 32; ++i) {
-    const int idx = i * 32 + lane;
-    const int which = idx >> 9, rr = (idx >> 3) & (kChunkKeys - 1), c = idx & 7;  // K / V, row, 16-dim chunk
-    const uint4 x = *reinterpret_cast<const uint4*>(src + which * kBoxBytes + sw128(rr, c));
-    const uint4 lo = make_uint4(e4m3x2_to_f16x2(x.x & 0xffffu), e4m3x2_to_f16x2(x.x >> 16),
-                                e4m3x2_to_f16x2(x.y & 0xffffu), e4m3x2_to_f16x2(x.y >> 16));
-    const uint4 hi = make_uint4(e4m3x2_to_f16x2(x.z & 0xffffu), e4m3x2_to_f16x2(x.z >> 16),
-                                e4m3x2_to_f16x2(x.w & 0xffffu), e4m3x2_to_f16x2(x.w >> 16));
-    const int cc = 2 * c;  // first fp16 chunk of the 256-byte row; chunks 8.. are the hi half
-    uint8_t* base = dst + (2 * which + (cc >> 3)) * kBoxBytes;
-    *reinterpret_cast<uint4*>(base + sw128(rr, cc & 7)) = lo;
-    *reinterpret_cast<uint4*>(base + sw128(rr, (cc + 1) & 7)) = hi;
-  }
+// Two E4M3 values -> fp16x2 holding each value times 2^-8, exactly, with
+// integer operations only.  The bytes come in as the high byte of each 16-bit
+// half (h = [0, b0, 0, b1]): the sign stays in bit 15, and exponent and
+// mantissa (eeee mmm) move down one bit into bits 14..7, so the fp16 exponent
+// field reads eeee with its top bit 0 and the mantissa's top bits mmm.  For
+// e > 0 that is 2^(e-15) (1 + m/8) = 2^-8 2^(e-7) (1 + m/8); for e = 0 the
+// fp16 subnormal 2^-14 m/8 = 2^-8 2^-6 m/8; so every finite E4M3 value maps to
+// its value times 2^-8 (its NaN encodings to finite numbers: an FP8 cache holds
+// finite values).  The 2^8 is folded into the score scale (K) and into the
+// output scale (V) by the host.
+__device__ __forceinline__ uint32_t e4m3_hb_to_f16x2_s8(uint32_t h) {
+  return ((h >> 1) & 0x3f803f80u) | (h & 0x80008000u);
 }
+// Bytes 0 and 1 / 2 and 3 / 0 and 2 / 1 and 3 of a word, as above.
+__device__ __forceinline__ uint32_t e4m3_lo2(uint32_t w) { return e4m3_hb_to_f16x2_s8(__byte_perm(w, 0u, 0x1404)); }
+__device__ __forceinline__ uint32_t e4m3_hi2(uint32_t w) { return e4m3_hb_to_f16x2_s8(__byte_perm(w, 0u, 0x3424)); }
+__device__ __forceinline__ uint32_t e4m3_even2(uint32_t w) { return e4m3_hb_to_f16x2_s8(__byte_perm(w, 0u, 0x2404)); }
+__device__ __forceinline__ uint32_t e4m3_odd2(uint32_t w) { return e4m3_hb_to_f16x2_s8(__byte_perm(w, 0u, 0x3414)); }
 
 constexpr int kMaxCluster = 8;
 
@@ -360,7 +387,7 @@ __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int 
 
 // out_q / out_scale: when non-null, the output is emitted as MXFP8 there
 // instead of bf16 in `out`.  kFp8: the K / V caches hold E4M3 bytes;
-// scale_log2 then includes k_scale, and v_scale multiplies the output.
+// scale_log2 then includes 2^8 k_scale, and v_scale (2^8 times the cache's) multiplies the output.
 // kSplit: launched in clusters of csize CTAs, one cluster per (query, KV
 // head) segment; CTA rank r takes units [r topk / csize, (r + 1) topk / csize)
 // of it, and the cluster merges on chip (split_finish).  Otherwise stream-K:
@@ -377,6 +404,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   AttSmem<kFp8>& sm =
       *reinterpret_cast<AttSmem<kFp8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kStg = att_stages<kFp8>();
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
   long long lo, hi;
@@ -390,7 +418,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   }
 
   if (tid == 0) {
-    for (int s = 0; s < kAttStages; ++s) {
+    for (int s = 0; s < kStg; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
@@ -482,8 +510,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
         for (int ch = 0; ch < nch; ++ch, ++sc) {
           if (lane == 0) {
-            const int s = static_cast<int>(sc % kAttStages);
-            mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kAttStages) & 1) ^ 1), err, 200);
+            const int s = static_cast<int>(sc % kStg);
+            mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kStg) & 1) ^ 1), err, 200);
             const int row = static_cast<int>(r0 + ch * kChunkKeys);
             uint8_t* st = sm.t.stage[s];
             if (kFp8) {
@@ -508,8 +536,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     // slot.  Only this thread arms those barriers, so that phase cannot have
     // been passed.
     if (lane == 0) {
-      for (int s = 0; s < kAttStages; ++s) {
-        const long long f = (sc - s + kAttStages - 1) / kAttStages;  // fills of stage s
+      for (int s = 0; s < kStg; ++s) {
+        const long long f = (sc - s + kStg - 1) / kStg;  // fills of stage s
         if (f > 0) mbar_wait(&sm.full[s], static_cast<uint32_t>((f - 1) & 1), err, 220);
       }
       for (int s = 0; s < kSegSlots; ++s) {
@@ -541,14 +569,27 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     uint32_t qa[8][4];
     {
       const uint32_t qt = smem_u32(sm.qtile[ss]);
-      const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+      if constexpr (kFp8 != 0) {
+        // fp16, k slots permuted as the K fragments are (S = Q K^T below):
+        // slots 2t, 2t+1, 2t+8, 2t+9 of k-step s hold dims 16s + 4t .. + 3
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int chunk = 2 * kk + (lane >> 4);
-        ldsm_x4(qa[kk], qt + (chunk >> 3) * kQBoxBytes + sw128(qrow, chunk & 7));
-        if (kFp8)
+        for (int kk = 0; kk < 8; ++kk) {
+          const int chunk = 2 * (kk & 3) + (t4 >> 1);  // 16-byte chunk of 8 dims in the box of 64
+          const uint32_t off = (kk >> 2) * kQBoxBytes + 8 * (t4 & 1);
+          const uint2 a = lds64(qt + off + sw128(g8, chunk));
+          const uint2 b = lds64(qt + off + sw128(g8 + 8, chunk));
+          qa[kk][0] = bf16x2_to_f16x2(a.x);
+          qa[kk][1] = bf16x2_to_f16x2(b.x);
+          qa[kk][2] = bf16x2_to_f16x2(a.y);
+          qa[kk][3] = bf16x2_to_f16x2(b.y);
+        }
+      } else {
+        const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) qa[kk][j] = bf16x2_to_f16x2(qa[kk][j]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const int chunk = 2 * kk + (lane >> 4);
+          ldsm_x4(qa[kk], qt + (chunk >> 3) * kQBoxBytes + sw128(qrow, chunk & 7));
+        }
       }
     }
     __syncwarp();
@@ -566,36 +607,48 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
       if (nk == 0) continue;
       const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
       for (int ch = 0; ch < nch; ++ch, ++sc) {
-        const int s = static_cast<int>(sc % kAttStages);
+        const int s = static_cast<int>(sc % kStg);
         if (s % kConsumerWarps != warp) continue;
         const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
-        mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kAttStages) & 1), err, 300);
-        uint32_t stg;
-        if constexpr (kFp8 != 0) {
-          // to this warp's fp16 tile; the stage is free again at once
-          fp8_stage_to_f16(sm.t.stage[s], sm.t.wtile[warp], lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.empty[s]);
-          stg = smem_u32(sm.t.wtile[warp]);
-        } else {
-          stg = smem_u32(sm.t.stage[s]);
-        }
+        mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kStg) & 1), err, 300);
+        const uint32_t stg = smem_u32(sm.t.stage[s]);
         const int mi = lane >> 3;
         // ---- S = Q K^T over the chunk's keys (n-tiles of 8 keys, in pairs) ----
         float sacc[8][4];
 #pragma unroll
         for (int p = 0; p < 8; ++p) sacc[p][0] = sacc[p][1] = sacc[p][2] = sacc[p][3] = 0.f;
+        if constexpr (kFp8 != 0) {
+          // E4M3 K rows are 128 bytes: a 16-byte chunk is one k-step of 16 dims.
+          // ldmatrix (16-bit view) gives a lane 4 consecutive bytes, dims
+          // 16s + 4t .. + 3 of one key, converted in registers into the B
+          // fragment whose slots the Q fragments above were permuted to match.
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          if (16 * kp >= valid) break;
-          const int krow = 16 * kp + 8 * (mi >> 1) + (lane & 7);
+          for (int kp = 0; kp < 4; ++kp) {
+            if (16 * kp >= valid) break;
+            const int krow = 16 * kp + 8 * (mi & 1) + (lane & 7);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
-            uint32_t kb[4];
-            ldsm_x4(kb, stg + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7));
-            mma16<kFp8>(sacc[2 * kp], qa[kk], kb[0], kb[1]);
-            mma16<kFp8>(sacc[2 * kp + 1], qa[kk], kb[2], kb[3]);
+            for (int kk = 0; kk < 8; kk += 2) {
+              uint32_t kr[4];  // keys lo / hi of k-step kk, then of k-step kk + 1
+              ldsm_x4(kr, stg + sw128(krow, kk + (mi >> 1)));
+              mma_f16(sacc[2 * kp], qa[kk], e4m3_lo2(kr[0]), e4m3_hi2(kr[0]));
+              mma_f16(sacc[2 * kp + 1], qa[kk], e4m3_lo2(kr[1]), e4m3_hi2(kr[1]));
+              mma_f16(sacc[2 * kp], qa[kk + 1], e4m3_lo2(kr[2]), e4m3_hi2(kr[2]));
+              mma_f16(sacc[2 * kp + 1], qa[kk + 1], e4m3_lo2(kr[3]), e4m3_hi2(kr[3]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kp = 0; kp < 4; ++kp) {
+            if (16 * kp >= valid) break;
+            const int krow = 16 * kp + 8 * (mi >> 1) + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int chunk = 2 * kk + (mi & 1);  // 16-byte chunk of the 256-byte row
+              uint32_t kb[4];
+              ldsm_x4(kb, stg + (chunk >> 3) * kBoxBytes + sw128(krow, chunk & 7));
+              mma_bf16(sacc[2 * kp], qa[kk], kb[0], kb[1]);
+              mma_bf16(sacc[2 * kp + 1], qa[kk], kb[2], kb[3]);
+            }
           }
         }
         // ---- mask, online softmax (base 2, scale folded in) ----
@@ -650,17 +703,33 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
                                   pack16<kFp8>(sacc[2 * kp + 1][0], sacc[2 * kp + 1][1]),
                                   pack16<kFp8>(sacc[2 * kp + 1][2], sacc[2 * kp + 1][3])};
           const int vrow = 16 * kp + 8 * (mi & 1) + (lane & 7);
+          if constexpr (kFp8 != 0) {
+            // The transposing ldmatrix (16-bit view) of E4M3 V gives a lane
+            // keys 2t, 2t+1 of dims 2g, 2g+1 of a 16-dim block: bytes 0 / 2 are
+            // the pair of the even dim, 1 / 3 that of the odd one, so the block
+            // feeds two n-tiles, its even and its odd dims (st.o[2c], [2c+1]).
 #pragma unroll
-          for (int nd = 0; nd < 16; nd += 2) {
-            const int chunk = nd + (mi >> 1);
-            uint32_t vb[4];
-            ldsm_x4_t(vb, stg + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7));
-            mma16<kFp8>(st.o[nd], pa, vb[0], vb[1]);
-            mma16<kFp8>(st.o[nd + 1], pa, vb[2], vb[3]);
+            for (int c = 0; c < 8; c += 2) {
+              uint32_t vr[4];  // keys lo / hi of block c, then of block c + 1
+              ldsm_x4_t(vr, stg + kBoxBytes + sw128(vrow, c + (mi >> 1)));
+              mma_f16(st.o[2 * c], pa, e4m3_even2(vr[0]), e4m3_even2(vr[1]));
+              mma_f16(st.o[2 * c + 1], pa, e4m3_odd2(vr[0]), e4m3_odd2(vr[1]));
+              mma_f16(st.o[2 * c + 2], pa, e4m3_even2(vr[2]), e4m3_even2(vr[3]));
+              mma_f16(st.o[2 * c + 3], pa, e4m3_odd2(vr[2]), e4m3_odd2(vr[3]));
+            }
+          } else {
+#pragma unroll
+            for (int nd = 0; nd < 16; nd += 2) {
+              const int chunk = nd + (mi >> 1);
+              uint32_t vb[4];
+              ldsm_x4_t(vb, stg + (2 + (chunk >> 3)) * kBoxBytes + sw128(vrow, chunk & 7));
+              mma_bf16(st.o[nd], pa, vb[0], vb[1]);
+              mma_bf16(st.o[nd + 1], pa, vb[2], vb[3]);
+            }
           }
         }
         __syncwarp();
-        if (!kFp8 && lane == 0) mbar_arrive(&sm.empty[s]);
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
       }
     }
     it = seg_end;
@@ -671,13 +740,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
     consumer_sync();
-    if (warp > 0) state_to_smem(st, sm, warp - 1, g8, t4);
+    if (warp > 0) state_to_smem<kFp8>(st, sm, warp - 1, g8, t4);
     consumer_sync();
     if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps - 1; ++w) merge_from_smem(st, sm, w, g8, t4);
+    for (int w = 0; w < kConsumerWarps - 1; ++w) merge_from_smem<kFp8>(st, sm, w, g8, t4);
     __syncwarp();
-    state_to_smem(st, sm, 0, g8, t4);  // staging for coalesced stores (slot 0 is read only by warp 0)
+    state_to_smem<kFp8>(st, sm, 0, g8, t4);  // staging for coalesced stores (slot 0 is read only by warp 0)
     __syncwarp();
     if constexpr (kSplit != 0) continue;  // the cluster merges slot 0 (split_finish)
     // ---- warp 0 writes: lane -> row lane/2, 64 dims ----
@@ -877,7 +946,9 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   const bool maps = kv_fp8 ? make_kv_map8(&kmap, k, geo.num_rows) && make_kv_map8(&vmap, v, geo.num_rows)
                            : make_kv_map(&kmap, k, geo.num_rows) && make_kv_map(&vmap, v, geo.num_rows);
   if (!maps || !make_q_map(&qmap, q, geo.nq)) return cudaErrorInvalidValue;
-  const float scale_log2 = scale * (kv_fp8 ? k_scale : 1.f) * 1.4426950408889634f;
+  // An FP8 cache holds k / k_scale and v / v_scale, and the kernel reads its
+  // bytes as fp16 values times 2^-8 (e4m3_hb_to_f16x2_s8): 2^8 goes into both scales.
+  const float scale_log2 = scale * (kv_fp8 ? 256.f * k_scale : 1.f) * 1.4426950408889634f;
   const long long S = static_cast<long long>(geo.nq) * kKvHeads;  // (query, KV head) segments
   const long long N = S * topk;
   // Few segments (small batches): one cluster of C CTAs per segment, merged
@@ -903,7 +974,7 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const float vs = kv_fp8 ? v_scale : 1.f;
+  const float vs = kv_fp8 ? 256.f * v_scale : 1.f;
   auto* o = static_cast<__nv_bfloat16*>(out);
   if (C) {
     lc.gridDim = dim3(static_cast<unsigned>(S * C));
