@@ -25,7 +25,12 @@ import random
 
 import pytest
 
-INFO, SLOTS, MATH = 4, 3, 8
+from _kernel_consts import kconst, mbar_count
+
+# the kernel's own values (prefill_attend.cu, bw_attend_kernel)
+INFO, SLOTS, MATH = (kconst(n, "prefill_attend.cu") for n in ("kBwInfo", "kBwSlots", "kBwMath"))
+INFO_EMPTY, P_FULL, DQ_FREE, ACC_FREE = (mbar_count(b, "prefill_attend.cu", after="bw_attend_kernel(")
+                                         for b in ("info_empty", "p_full", "dq_free", "acc_free"))
 
 
 class Bar:
@@ -52,18 +57,18 @@ class Sim:
             b[name] = Bar(name, count)
         for i in range(INFO):
             bar(f"info_full{i}")
-            bar(f"info_empty{i}", MATH + 2)
+            bar(f"info_empty{i}", INFO_EMPTY)
         bar("kv_full")
         bar("kv_empty")
         for i in range(SLOTS):
             bar(f"qd_full{i}")
             bar(f"qd_empty{i}")
         bar("s_full")
-        bar("p_full", MATH)
+        bar("p_full", P_FULL)
         bar("dq_full")
-        bar("dq_free", MATH)
+        bar("dq_free", DQ_FREE)
         bar("acc_full")
-        bar("acc_free", MATH)
+        bar("acc_free", ACC_FREE)
         # buffer state: pending asynchronous readers / writers, and active
         # readers in the math warps (tensor memory)
         self.pend_r = {}  # buffer -> count of pending async readers

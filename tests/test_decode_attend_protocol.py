@@ -23,7 +23,17 @@ import random
 
 import pytest
 
-SEG_SLOTS, CHUNK_KEYS = 2, 64
+from _kernel_consts import kconst, mbar_count
+
+# the kernels' own values (sparse_attend.cu, decode_select.cu)
+SEG_SLOTS = kconst("kSegSlots", "sparse_attend.cu")
+CHUNK_KEYS = kconst("kChunkKeys", "sparse_attend.cu")
+STAGES = kconst("kAttStages", "sparse_attend.cu")
+CONSUMERS = kconst("kConsumerWarps", "sparse_attend.cu")
+SEG_EMPTY = mbar_count("seg_empty", "sparse_attend.cu")  # every consumer warp releases a segment slot
+SEL_CONSUMERS = kconst("kSelConsumers", "decode_select.cu")
+SEL_STAGES = (kconst("kSelRingBytes", "decode_select.cu") // (128 * 256),  # bf16 pages
+              kconst("kSelRingBytes", "decode_select.cu") // (128 * 128))  # E4M3 pages
 
 
 class Bar:
@@ -39,7 +49,7 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, segments, rng, stages=6, consumers=3, by_chunk=False, segment_ring=True):
+    def __init__(self, segments, rng, stages=STAGES, consumers=CONSUMERS, by_chunk=False, segment_ring=True):
         # segments: list of lists of key counts (0 = an empty / padded entry).
         # Without the segment ring (and its end-of-segment meetings) this is the
         # decode scorer's page ring: one stage per item, item i to a warp.
@@ -48,7 +58,7 @@ class Sim:
         self.bars = {}
         for i in range(SEG_SLOTS):
             self.bars[f"seg_full{i}"] = Bar(f"seg_full{i}", 1)
-            self.bars[f"seg_empty{i}"] = Bar(f"seg_empty{i}", consumers)
+            self.bars[f"seg_empty{i}"] = Bar(f"seg_empty{i}", SEG_EMPTY if consumers == CONSUMERS else consumers)
         for s in range(stages):
             self.bars[f"full{s}"] = Bar(f"full{s}", 1)
             self.bars[f"empty{s}"] = Bar(f"empty{s}", 1)
@@ -164,11 +174,12 @@ def test_decode_attend_protocol_random_schedules(seed):
     Sim(segment_list(rng, rng.randint(1, 6)), rng).run()
 
 
-def test_decode_attend_protocol_twelve_stages():
+def test_decode_attend_protocol_twice_the_stages():
     # the stage count only has to be a multiple of the consumer warps
+    assert STAGES % CONSUMERS == 0
     for seed in range(5):
         rng = random.Random(100 + seed)
-        Sim(segment_list(rng, 4), rng, stages=12).run()
+        Sim(segment_list(rng, 4), rng, stages=2 * STAGES).run()
 
 
 def test_model_catches_round_robin_chunks():
@@ -184,14 +195,16 @@ def test_model_catches_round_robin_chunks():
     assert failed > 0
 
 
-@pytest.mark.parametrize("stages", [6, 12])
+@pytest.mark.parametrize("stages", SEL_STAGES)
 def test_decode_scorer_page_ring(stages):
-    # the decode scorer: item (page) i to warp i mod 6 through 6 (bf16) or 12
-    # (E4M3) stages -- round-robin, safe because the stage count is a multiple
-    # of the warps
+    # the decode scorer: item (page) i to warp i mod kSelConsumers through the
+    # bf16 or the E4M3 ring (6 or 12 stages as compiled) -- round-robin, safe
+    # because the stage count is a multiple of the warps
+    assert stages % SEL_CONSUMERS == 0
     for seed in range(10):
         rng = random.Random(200 + seed)
-        Sim(segment_list(rng, 4), rng, stages=stages, consumers=6, by_chunk=True, segment_ring=False).run()
+        Sim(segment_list(rng, 4), rng, stages=stages, consumers=SEL_CONSUMERS, by_chunk=True,
+            segment_ring=False).run()
 
 
 def test_model_reports_the_eight_warp_scorer_ring():

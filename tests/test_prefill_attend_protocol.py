@@ -24,7 +24,12 @@ import random
 
 import pytest
 
-INFO, QST, KST, VST = 8, 2, 2, 1
+from _kernel_consts import kconst, mbar_count
+
+# the kernel's own values (prefill_attend.cu, bm_attend_kernel)
+INFO, QST, KST, VST = (kconst(n, "prefill_attend.cu") for n in ("kBmInfo", "kBmQStages", "kBmKStages", "kBmVStages"))
+O_FREE, P_FULL, INFO_EMPTY = (mbar_count(b, "prefill_attend.cu", after="bm_attend_kernel(")
+                              for b in ("o_free", "p_full", "info_empty"))
 
 
 class Bar:
@@ -60,11 +65,11 @@ class Sim:
             bar(f"s_full{b}")
             bar(f"s_free{b}")
             bar(f"o_full{b}")
-            bar(f"o_free{b}", 4)
-            bar(f"p_full{b}", 4)
+            bar(f"o_free{b}", O_FREE)
+            bar(f"p_full{b}", P_FULL)
         for i in range(INFO):
             bar(f"info_full{i}")
-            bar(f"info_empty{i}", 10)
+            bar(f"info_empty{i}", INFO_EMPTY)
         self.tag, self.pend_r, self.pend_w, self.warp_r = {}, {}, {}, {}
         self.pipe = {"S": [], "O": []}  # per MMA thread, in issue order
         self.loads = []

@@ -17,7 +17,11 @@ import random
 
 import pytest
 
-EPI = 4
+from _kernel_consts import kconst, mbar_count
+
+# the kernel's own values (prefill_select.cu): epilogue warps = arrivals that free a tensor-memory buffer
+EPI = mbar_count("t_empty", "prefill_select.cu")
+STAGES = kconst("kPsStages", "prefill_select.cu")
 
 
 class Bar:
@@ -33,7 +37,7 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, units, topk, rng, stages=3, skew=False):
+    def __init__(self, units, topk, rng, stages=STAGES, skew=False):
         # units: block counts nb (qb + 1) of this CTA's units, in order
         self.units, self.topk, self.rng, self.S, self.skew = units, topk, rng, stages, skew
         self.bars = {"a_full": Bar("a_full", 1), "a_empty": Bar("a_empty", 1)}
