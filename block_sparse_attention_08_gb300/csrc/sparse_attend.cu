@@ -41,8 +41,7 @@
 // FP8 main K/V cache (TensorRT-LLM field fuse_qkv_index_projection: the M3 path
 // uses "an FP8 main KV cache"): the caches hold E4M3 bytes standing for
 // k_scale * k and v_scale * v.  A chunk is then 64 keys x 128 bytes of K and of
-// V (one 128-byte-swizzled box each, 16 KB a stage; 12 stages keep the bf16
-// path's 192 KB in flight).  The consumers read the E4M3 bytes straight into
+// V (one 128-byte-swizzled box each, 16 KB a stage).  The consumers read the E4M3 bytes straight into
 // MMA fragments and convert them in registers (every E4M3 value is exact in
 // fp16): K through ldmatrix, with the k slots of the fp16 Q fragments permuted
 // to match; V through the transposing ldmatrix on byte pairs, each 16-dim
@@ -55,10 +54,7 @@
 
 namespace msa {
 
-constexpr int kAttStages = 6;        // 32 KB stages of a bf16 cache
-constexpr int kAttStages8 = 12;      // 16 KB stages of an FP8 cache: the same 192 KB in flight
-template <int kFp8>
-__host__ __device__ constexpr int att_stages() { return kFp8 ? kAttStages8 : kAttStages; }
+constexpr int kAttStages = 6;
 constexpr int kChunkKeys = 64;
 constexpr int kBoxBytes = kChunkKeys * 128;        // 64 rows x 128 bytes (64 bf16 dims, or 128 E4M3 dims)
 constexpr int kAttStageBytes = 4 * kBoxBytes;      // K lo/hi + V lo/hi
@@ -72,8 +68,7 @@ constexpr int kCombStride = kDim + 8;               // padded fp32 row of the me
 constexpr int kPartialFloats = 32 + kGroup * kDim;  // m[16], l[16], O[16][128]
 // stage s is always consumed by warp s % kConsumerWarps, so a warp never waits
 // on a stage more than one mbarrier phase ahead
-static_assert(kAttStages % kConsumerWarps == 0 && kAttStages8 % kConsumerWarps == 0,
-              "stages must be a multiple of the consumer warps");
+static_assert(kAttStages % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
 
 struct QueryGeo {
   int pos;         // position of the query (keys 0..pos are causal)
@@ -118,7 +113,7 @@ struct AttTiles {
 };
 template <>
 struct AttTiles<1> {
-  alignas(1024) uint8_t stage[kAttStages8][kAttStage8Bytes];
+  alignas(1024) uint8_t stage[kAttStages][kAttStage8Bytes];
 };
 
 template <int kFp8>
@@ -129,8 +124,8 @@ struct AttSmem {
   float comb_m[kConsumerWarps - 1][kGroup];
   float comb_l[kConsumerWarps - 1][kGroup];
   SegInfo seg[kSegSlots];
-  uint64_t full[kAttStages8];
-  uint64_t empty[kAttStages8];
+  uint64_t full[kAttStages];
+  uint64_t empty[kAttStages];
   uint64_t seg_full[kSegSlots];
   uint64_t seg_empty[kSegSlots];
   int bcast;
@@ -404,7 +399,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   AttSmem<kFp8>& sm =
       *reinterpret_cast<AttSmem<kFp8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kStg = att_stages<kFp8>();
+  constexpr int kStg = kAttStages;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
   long long lo, hi;
