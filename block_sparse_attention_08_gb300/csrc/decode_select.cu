@@ -238,9 +238,9 @@ __device__ __forceinline__ bool walk_to(const DecodeGeom& geo, int topk, long lo
 
 constexpr int kSelEnd = -2;  // meta.r of the stage that ends a consumer warp's loop
 
-// sched: two ints in the workspace header, zero between calls -- [0] claims
-// past the first wave, [1] CTAs that have finished claiming (the last one
-// puts both back to zero).
+// sched: the claim counter in the workspace header, zero when the kernel
+// starts (the top-k kernel that follows puts it back to zero once this grid
+// has completed).
 template <int kE4M3>
 __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
     const uint8_t* __restrict__ index_q, const uint8_t* __restrict__ index_k, DecodeGeom geo,
@@ -424,13 +424,6 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
         const int f = (i - s + kStages - 1) / kStages;  // fills of stage s
         if (f > 0) mbar_wait(&sm.full[s], (f - 1) & 1, err, 102);
       }
-      // This CTA claims nothing more (its claims are ordered before the count
-      // by the fence): the last CTA to be counted puts both counters back to 0.
-      __threadfence();
-      if (atomicAdd(&sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
-        atomicExch(&sched[0], 0);
-        atomicExch(&sched[1], 0);
-      }
     }
     return;
   }
@@ -539,7 +532,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
 // start while the scorer drains, and wait for the scores to be complete.
 __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
                                                           int32_t* __restrict__ q2k, int topk, int init, int local,
-                                                          DevError* err) {
+                                                          int* __restrict__ sched, DevError* err) {
   __shared__ float stage[kKvHeads][kTopkStage];
   __shared__ unsigned long long cand[kKvHeads][kCandCap];
   __shared__ int ids[kKvHeads][kMaxTopk];
@@ -548,6 +541,9 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
   // may now be scheduled and run its prologue; it waits for this grid to end
   // before it reads q2k
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the scorer grid has completed and claims nothing more: its claim counter
+  // goes back to zero for the next call (no work of this call reads it)
+  if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
   const int r = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* row = scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks;
   // stage the row's first min(max_blocks, kTopkStage) scores -- all loads in
@@ -604,7 +600,8 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
   lc.attrs = attr;
   lc.numAttrs = 1;
   const float* sc = scores;
-  return cudaLaunchKernelEx(&lc, decode_topk_kernel, sc, geo, q2k, cfg.topk, cfg.init_blocks, cfg.local_blocks, err);
+  return cudaLaunchKernelEx(&lc, decode_topk_kernel, sc, geo, q2k, cfg.topk, cfg.init_blocks, cfg.local_blocks, sched,
+                            err);
 }
 
 }  // namespace msa
@@ -669,7 +666,7 @@ extern "C" msa_status msa_select_blocks_decode_noalloc(const msa_config* cfg, co
   auto* base = static_cast<uint8_t*>(noalloc_scratch(&e));
   if (!base) return cuda_fail(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the error word and the scorer's claim counters (both in the header) must
+  // the error word and the scorer's claim counter (both in the header) must
   // start at zero; the scores are stored before they are read
   if (const cudaError_t ce = cudaMemsetAsync(base, 0, off_scores, s); ce != cudaSuccess) return cuda_fail(ce);
   e = launch_decode_select(*cfg, index_q, index_k_cache, seq_lens, page_table, cu_seqlens_k, batch, max_blocks,

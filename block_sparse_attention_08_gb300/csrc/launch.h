@@ -24,8 +24,9 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
                                  const int32_t* seq_lens, const int32_t* page_table, const int64_t* cu_k,
                                  int batch, int max_blocks, long long num_slots, int32_t* q2k, float* scores,
                                  int* sched, DevError* err, cudaStream_t stream);
-// Offset in the workspace header of the decode scorer's two claim counters
-// (zero between calls; the last CTA of each call puts them back to zero).
+// Offset in the workspace header of the decode scorer's page-claim counter
+// (zero between calls: the top-k kernel puts it back once the scorer grid has
+// completed).
 constexpr size_t kSelSchedOffset = 128;
 // kv_fp8: the K / V caches hold E4M3 bytes standing for k_scale * k and v_scale * v.
 cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void* k, const void* v,

@@ -303,7 +303,11 @@ constexpr int kMaxCluster = 8;
 // slot rank - 1 there (remote stores, nothing waited on), and after the second
 // barrier rank 0 merges the states from its own shared memory and stores the
 // output rows.
-constexpr int kPushFloats = 2 * kGroup + kGroup * kDim;  // m[16], l[16], O[16][128]
+// A slot: m[16], l[16], then O[16] rows of kPushStride floats (128 used): the
+// 4 padding floats put the 16-byte pieces a warp reads at once (rows lane / 2,
+// halves lane % 2) in all 8 bank groups instead of one.
+constexpr int kPushStride = kDim + 4;
+constexpr int kPushFloats = 2 * kGroup + kGroup * kPushStride;
 
 template <int kFp8, class Smem>
 __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int lane, float v_scale,
@@ -321,7 +325,7 @@ __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int 
       st_dsmem_f32(dsmem_addr(dst + row, 0), sm.comb_m[0][row]);
       st_dsmem_f32(dsmem_addr(dst + kGroup + row, 0), sm.comb_l[0][row]);
     }
-    const uint32_t o = dsmem_addr(dst + 2 * kGroup + row * kDim + d0, 0);
+    const uint32_t o = dsmem_addr(dst + 2 * kGroup + row * kPushStride + d0, 0);
     const float* src = &sm.comb[0][row][d0];
 #pragma unroll
     for (int d = 0; d < 16; ++d) st_dsmem_v4(o + 16 * d, *reinterpret_cast<const float4*>(src + 4 * d));
@@ -334,7 +338,7 @@ __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int 
   auto m_of = [&](int x) { return x == 0 ? sm.comb_m[0][row] : slots[(x - 1) * kPushFloats + row]; };
   auto l_of = [&](int x) { return x == 0 ? sm.comb_l[0][row] : slots[(x - 1) * kPushFloats + kGroup + row]; };
   auto o_of = [&](int x) {
-    return x == 0 ? &sm.comb[0][row][d0] : slots + (x - 1) * kPushFloats + 2 * kGroup + row * kDim + d0;
+    return x == 0 ? &sm.comb[0][row][d0] : slots + (x - 1) * kPushFloats + 2 * kGroup + row * kPushStride + d0;
   };
   float mc[kMaxCluster], lc[kMaxCluster];
 #pragma unroll

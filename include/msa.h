@@ -112,8 +112,8 @@ msa_status msa_config_check(const msa_config* cfg);
  *   MSA_MODE_PREFILL_BWD: as MSA_MODE_PREFILL, for msa_sparse_attend_prefill_backward.
  * The workspace must be zero-filled once before its first use (see
  * msa_workspace_init), which clears the device error word and the decode
- * scorer's two page-claim counters in its first 256 bytes, and the
- * completion counters.  Every call that completes leaves its
+ * scorer's page-claim counter in its first 256 bytes, and the completion
+ * counters.  Every call that completes leaves its
  * counters at zero again (the decode calls enqueue no memset; the prefill
  * calls clear theirs with a cudaMemsetAsync on `stream`), and the scorer
  * stores rather than accumulates (NeMo _score_scratch).  In the decode layout

@@ -140,8 +140,8 @@ def test_decode_workspace_shared_across_batch_sizes():
     q2k_b, out_b = _run(big, 16, 0, 1, "decode 64 requests, after the 4-request call", workspace=ws)
     assert torch.equal(q2k_a, q2k_b) and torch.equal(out_a, out_b)
     assert ws.read_device_error() == (0, 0)
-    # the scorer's two page-claim counters (header bytes 128-135) are back at zero
-    assert not ws.buf[128:136].any().item()
+    # the scorer's page-claim counter (header bytes 128-131) is back at zero
+    assert not ws.buf[128:132].any().item()
 
 
 def test_decode_select_walks_past_unscored_requests():
