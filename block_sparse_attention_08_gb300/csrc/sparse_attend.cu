@@ -105,31 +105,66 @@ struct SegInfo {
   int nk[kMaxTopk];  // causal keys of each of the segment's units (0 = nothing to do)
 };
 
-// The chunk ring: 64-key chunks of K and V (bf16: 4 boxes of 64 dims; FP8: one
-// 128-byte box each).
-template <int kFp8>
-struct AttTiles {
-  alignas(1024) uint8_t stage[kAttStages][kAttStageBytes];
-};
-template <>
-struct AttTiles<1> {
-  alignas(1024) uint8_t stage[kAttStages][kAttStage8Bytes];
+// The chunk ring: 64-key chunks of K and V (bf16: 4 boxes of 64 dims, 32 KB;
+// FP8: one 128-byte box each, 16 KB), 6 stages.  The cluster form keeps no
+// separate buffer for the warps' states (each warp leaves its state in its own
+// stage, idle once the CTA's one segment is done); with an FP8 cache its 96 KB
+// of stages then let two CTAs share an SM, six consumer warps per SM, which
+// the FP8 attention (bound by its warps' issue) gains from (the 16-request
+// workload 31.4 -> 27.2 us).  A bf16 ring of 96 KB would leave each warp a
+// single stage, nothing landing while it computes: slower (18.4 -> 20.9 us on
+// the 4-request workload), so the bf16 cluster form stays at one CTA per SM.
+template <int kFp8, int kSplit>
+struct AttShape {
+  static constexpr int kStageBytes = kFp8 ? kAttStage8Bytes : kAttStageBytes;
+  static constexpr int kStages = kAttStages;
+  static constexpr int kCtasPerSm = kSplit && kFp8 ? 2 : 1;
 };
 
-template <int kFp8>
-struct AttSmem {
-  AttTiles<kFp8> t;
-  alignas(1024) uint8_t qtile[kSegSlots][2 * kQBoxBytes];
+// Where the consumer warps' states meet (stream-K only).
+template <int kSplit>
+struct AttComb {
   float comb[kConsumerWarps - 1][kGroup][kCombStride];
   float comb_m[kConsumerWarps - 1][kGroup];
   float comb_l[kConsumerWarps - 1][kGroup];
+};
+template <>
+struct AttComb<1> {};
+
+template <int kFp8, int kSplit>
+struct AttSmem {
+  alignas(1024) uint8_t stage[AttShape<kFp8, kSplit>::kStages][AttShape<kFp8, kSplit>::kStageBytes];
+  alignas(1024) uint8_t qtile[kSegSlots][2 * kQBoxBytes];
+  AttComb<kSplit> c;
   SegInfo seg[kSegSlots];
-  uint64_t full[kAttStages];
-  uint64_t empty[kAttStages];
+  uint64_t full[AttShape<kFp8, kSplit>::kStages];
+  uint64_t empty[AttShape<kFp8, kSplit>::kStages];
   uint64_t seg_full[kSegSlots];
   uint64_t seg_empty[kSegSlots];
   int bcast;
 };
+
+// One warp state in shared memory: O as 16 rows of kCombStride floats, m[16], l[16].
+struct CombRef {
+  float* o;
+  float* m;
+  float* l;
+  __device__ float* row(int r) const { return o + r * kCombStride; }
+};
+// who = 0: the CTA's merged state; who = w in 1, 2: the state of consumer warp w.
+// Stream-K: the shared buffer (the merged state over warp 1's slot, which warp
+// 0 has read by then); cluster form: stage `who`, which belongs to warp `who`.
+template <int kFp8, int kSplit>
+__device__ __forceinline__ CombRef comb_ref(AttSmem<kFp8, kSplit>& sm, int who) {
+  if constexpr (kSplit != 0) {
+    float* base = reinterpret_cast<float*>(&sm.stage[who][0]);
+    return CombRef{base, base + kGroup * kCombStride, base + kGroup * kCombStride + kGroup};
+  } else {
+    const int slot = who > 0 ? who - 1 : 0;
+    return CombRef{&sm.c.comb[slot][0][0], sm.c.comb_m[slot], sm.c.comb_l[slot]};
+  }
+}
+static_assert((kGroup * kCombStride + 2 * kGroup) * sizeof(float) <= kAttStage8Bytes, "a warp state fits in a stage");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
 
@@ -154,61 +189,61 @@ struct WarpState {
 // values of the pair are the consecutive dims 16 c + 4 t4 .. + 3 -- stored and
 // loaded as one float4, in the natural order, so everything that reads the
 // states back (the merges, the output) sees plain rows.
-template <int kFp8, class Smem>
-__device__ __forceinline__ void state_to_smem(const WarpState& st, Smem& sm, int slot, int g8, int t4) {
+template <int kFp8>
+__device__ __forceinline__ void state_to_smem(const WarpState& st, const CombRef& c, int g8, int t4) {
   if (t4 == 0) {
-    sm.comb_m[slot][g8] = st.m0;
-    sm.comb_m[slot][g8 + 8] = st.m1;
-    sm.comb_l[slot][g8] = st.l0;
-    sm.comb_l[slot][g8 + 8] = st.l1;
+    c.m[g8] = st.m0;
+    c.m[g8 + 8] = st.m1;
+    c.l[g8] = st.l0;
+    c.l[g8 + 8] = st.l1;
   }
   if constexpr (kFp8 != 0) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      *reinterpret_cast<float4*>(&sm.comb[slot][g8][16 * c + 4 * t4]) =
-          make_float4(st.o[2 * c][0], st.o[2 * c + 1][0], st.o[2 * c][1], st.o[2 * c + 1][1]);
-      *reinterpret_cast<float4*>(&sm.comb[slot][g8 + 8][16 * c + 4 * t4]) =
-          make_float4(st.o[2 * c][2], st.o[2 * c + 1][2], st.o[2 * c][3], st.o[2 * c + 1][3]);
+    for (int k = 0; k < 8; ++k) {
+      *reinterpret_cast<float4*>(c.row(g8) + 16 * k + 4 * t4) =
+          make_float4(st.o[2 * k][0], st.o[2 * k + 1][0], st.o[2 * k][1], st.o[2 * k + 1][1]);
+      *reinterpret_cast<float4*>(c.row(g8 + 8) + 16 * k + 4 * t4) =
+          make_float4(st.o[2 * k][2], st.o[2 * k + 1][2], st.o[2 * k][3], st.o[2 * k + 1][3]);
     }
   } else {
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
-      *reinterpret_cast<float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]) = make_float2(st.o[nd][0], st.o[nd][1]);
-      *reinterpret_cast<float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]) = make_float2(st.o[nd][2], st.o[nd][3]);
+      *reinterpret_cast<float2*>(c.row(g8) + 8 * nd + 2 * t4) = make_float2(st.o[nd][0], st.o[nd][1]);
+      *reinterpret_cast<float2*>(c.row(g8 + 8) + 8 * nd + 2 * t4) = make_float2(st.o[nd][2], st.o[nd][3]);
     }
   }
 }
 
-template <int kFp8, class Smem>
-__device__ __forceinline__ void merge_from_smem(WarpState& st, const Smem& sm, int slot, int g8, int t4) {
-  const float mb0 = sm.comb_m[slot][g8], mb1 = sm.comb_m[slot][g8 + 8];
+template <int kFp8>
+__device__ __forceinline__ void merge_from_smem(WarpState& st, const CombRef& c, int g8, int t4) {
+  const float mb0 = c.m[g8], mb1 = c.m[g8 + 8];
   const float M0 = fmaxf(st.m0, mb0), M1 = fmaxf(st.m1, mb1);
   const float u0 = M0 == -INFINITY ? 0.f : M0, u1 = M1 == -INFINITY ? 0.f : M1;
   const float fa0 = exp2f(st.m0 - u0), fb0 = exp2f(mb0 - u0);
   const float fa1 = exp2f(st.m1 - u1), fb1 = exp2f(mb1 - u1);
-  st.l0 = st.l0 * fa0 + sm.comb_l[slot][g8] * fb0;
-  st.l1 = st.l1 * fa1 + sm.comb_l[slot][g8 + 8] * fb1;
+  st.l0 = st.l0 * fa0 + c.l[g8] * fb0;
+  st.l1 = st.l1 * fa1 + c.l[g8 + 8] * fb1;
   st.m0 = M0;
   st.m1 = M1;
   if constexpr (kFp8 != 0) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 x = *reinterpret_cast<const float4*>(&sm.comb[slot][g8][16 * c + 4 * t4]);
-      const float4 y = *reinterpret_cast<const float4*>(&sm.comb[slot][g8 + 8][16 * c + 4 * t4]);
-      st.o[2 * c][0] = st.o[2 * c][0] * fa0 + x.x * fb0;
-      st.o[2 * c + 1][0] = st.o[2 * c + 1][0] * fa0 + x.y * fb0;
-      st.o[2 * c][1] = st.o[2 * c][1] * fa0 + x.z * fb0;
-      st.o[2 * c + 1][1] = st.o[2 * c + 1][1] * fa0 + x.w * fb0;
-      st.o[2 * c][2] = st.o[2 * c][2] * fa1 + y.x * fb1;
-      st.o[2 * c + 1][2] = st.o[2 * c + 1][2] * fa1 + y.y * fb1;
-      st.o[2 * c][3] = st.o[2 * c][3] * fa1 + y.z * fb1;
-      st.o[2 * c + 1][3] = st.o[2 * c + 1][3] * fa1 + y.w * fb1;
+    for (int k = 0; k < 8; ++k) {
+      const float4 x = *reinterpret_cast<const float4*>(c.row(g8) + 16 * k + 4 * t4);
+      const float4 y = *reinterpret_cast<const float4*>(c.row(g8 + 8) + 16 * k + 4 * t4);
+      st.o[2 * k][0] = st.o[2 * k][0] * fa0 + x.x * fb0;
+      st.o[2 * k + 1][0] = st.o[2 * k + 1][0] * fa0 + x.y * fb0;
+      st.o[2 * k][1] = st.o[2 * k][1] * fa0 + x.z * fb0;
+      st.o[2 * k + 1][1] = st.o[2 * k + 1][1] * fa0 + x.w * fb0;
+      st.o[2 * k][2] = st.o[2 * k][2] * fa1 + y.x * fb1;
+      st.o[2 * k + 1][2] = st.o[2 * k + 1][2] * fa1 + y.y * fb1;
+      st.o[2 * k][3] = st.o[2 * k][3] * fa1 + y.z * fb1;
+      st.o[2 * k + 1][3] = st.o[2 * k + 1][3] * fa1 + y.w * fb1;
     }
   } else {
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
-      const float2 x = *reinterpret_cast<const float2*>(&sm.comb[slot][g8][8 * nd + 2 * t4]);
-      const float2 y = *reinterpret_cast<const float2*>(&sm.comb[slot][g8 + 8][8 * nd + 2 * t4]);
+      const float2 x = *reinterpret_cast<const float2*>(c.row(g8) + 8 * nd + 2 * t4);
+      const float2 y = *reinterpret_cast<const float2*>(c.row(g8 + 8) + 8 * nd + 2 * t4);
       st.o[nd][0] = st.o[nd][0] * fa0 + x.x * fb0;
       st.o[nd][1] = st.o[nd][1] * fa0 + x.y * fb0;
       st.o[nd][2] = st.o[nd][2] * fa1 + y.x * fb1;
@@ -313,20 +348,23 @@ template <int kFp8, class Smem>
 __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int lane, float v_scale,
                                              __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
                                              uint8_t* __restrict__ out_scale) {
-  static_assert(sizeof(sm.t.stage) >= (kMaxCluster - 1) * kPushFloats * sizeof(float), "push slots");
+  // the slots start at stage 1: stage 0 holds this CTA's merged state
+  static_assert(sizeof(sm.stage) - sizeof(sm.stage[0]) >= (kMaxCluster - 1) * kPushFloats * sizeof(float),
+                "push slots");
   const int rank = blockIdx.x % csize;
   const int row = lane >> 1, d0 = (lane & 1) * 64;
-  float* slots = reinterpret_cast<float*>(&sm.t.stage[0][0]);
+  float* slots = reinterpret_cast<float*>(&sm.stage[1][0]);
+  const CombRef mine = comb_ref(sm, 0);
   cluster_arrive_release();
   cluster_wait_acquire();
   if (rank != 0 && warp == 0) {
     float* dst = slots + (rank - 1) * kPushFloats;
     if ((lane & 1) == 0) {
-      st_dsmem_f32(dsmem_addr(dst + row, 0), sm.comb_m[0][row]);
-      st_dsmem_f32(dsmem_addr(dst + kGroup + row, 0), sm.comb_l[0][row]);
+      st_dsmem_f32(dsmem_addr(dst + row, 0), mine.m[row]);
+      st_dsmem_f32(dsmem_addr(dst + kGroup + row, 0), mine.l[row]);
     }
     const uint32_t o = dsmem_addr(dst + 2 * kGroup + row * kPushStride + d0, 0);
-    const float* src = &sm.comb[0][row][d0];
+    const float* src = mine.row(row) + d0;
 #pragma unroll
     for (int d = 0; d < 16; ++d) st_dsmem_v4(o + 16 * d, *reinterpret_cast<const float4*>(src + 4 * d));
   }
@@ -335,10 +373,10 @@ __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int 
   if (rank != 0 || warp != 0) return;
   const int qi = (blockIdx.x / csize) / kKvHeads, g = (blockIdx.x / csize) % kKvHeads;
   // contributor 0 is this CTA (comb slot 0), contributor x > 0 the ring slot x - 1
-  auto m_of = [&](int x) { return x == 0 ? sm.comb_m[0][row] : slots[(x - 1) * kPushFloats + row]; };
-  auto l_of = [&](int x) { return x == 0 ? sm.comb_l[0][row] : slots[(x - 1) * kPushFloats + kGroup + row]; };
+  auto m_of = [&](int x) { return x == 0 ? mine.m[row] : slots[(x - 1) * kPushFloats + row]; };
+  auto l_of = [&](int x) { return x == 0 ? mine.l[row] : slots[(x - 1) * kPushFloats + kGroup + row]; };
   auto o_of = [&](int x) {
-    return x == 0 ? &sm.comb[0][row][d0] : slots + (x - 1) * kPushFloats + 2 * kGroup + row * kPushStride + d0;
+    return x == 0 ? mine.row(row) + d0 : slots + (x - 1) * kPushFloats + 2 * kGroup + row * kPushStride + d0;
   };
   float mc[kMaxCluster], lc[kMaxCluster];
 #pragma unroll
@@ -393,17 +431,17 @@ __device__ __forceinline__ void split_finish(Smem& sm, int csize, int warp, int 
 // the units are split evenly over the grid and cut segments are merged
 // through fp32 partials in global memory and a ticket per segment.
 template <int kFp8, int kSplit>
-__global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
+__global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerSm) sparse_attend_kernel(
     const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
     const __grid_constant__ CUtensorMap qmap, const int32_t* __restrict__ q2k, AttnGeom geo, int topk,
     float scale_log2, float v_scale, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ out_q,
     uint8_t* __restrict__ out_scale, float* __restrict__ partials, int* __restrict__ tickets, int csize,
     DevError* err) {
   extern __shared__ uint8_t smem_raw[];
-  AttSmem<kFp8>& sm =
-      *reinterpret_cast<AttSmem<kFp8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  AttSmem<kFp8, kSplit>& sm = *reinterpret_cast<AttSmem<kFp8, kSplit>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kStg = kAttStages;
+  constexpr int kStg = AttShape<kFp8, kSplit>::kStages;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
   long long lo, hi;
@@ -450,11 +488,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
   if (lo >= hi) {
     if constexpr (kSplit != 0) {
       // no unit (csize > topk, never chosen by the host): an empty state
+      const CombRef c0 = comb_ref(sm, 0);
       if (warp == 0)
-        for (int i = lane; i < kGroup * kDim; i += 32) sm.comb[0][i / kDim][i % kDim] = 0.f;
+        for (int i = lane; i < kGroup * kDim; i += 32) c0.row(i / kDim)[i % kDim] = 0.f;
       if (warp == 0 && lane < kGroup) {
-        sm.comb_m[0][lane] = -INFINITY;
-        sm.comb_l[0][lane] = 0.f;
+        c0.m[lane] = -INFINITY;
+        c0.l[lane] = 0.f;
       }
       split_finish<kFp8>(sm, csize, warp, lane, v_scale, out, out_q, out_scale);
     }
@@ -512,7 +551,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
             const int s = static_cast<int>(sc % kStg);
             mbar_wait(&sm.empty[s], static_cast<uint32_t>(((sc / kStg) & 1) ^ 1), err, 200);
             const int row = static_cast<int>(r0 + ch * kChunkKeys);
-            uint8_t* st = sm.t.stage[s];
+            uint8_t* st = sm.stage[s];
             if (kFp8) {
               mbar_expect_tx(&sm.full[s], kAttStage8Bytes);
               tma_load_3d(st, &kmap, 0, g, row, &sm.full[s]);
@@ -610,7 +649,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
         if (s % kConsumerWarps != warp) continue;
         const int valid = min(kChunkKeys, nk - ch * kChunkKeys);  // keys of this chunk
         mbar_wait(&sm.full[s], static_cast<uint32_t>((sc / kStg) & 1), err, 300);
-        const uint32_t stg = smem_u32(sm.t.stage[s]);
+        const uint32_t stg = smem_u32(sm.stage[s]);
         const int mi = lane >> 3;
         // ---- S = Q K^T over the chunk's keys (n-tiles of 8 keys, in pairs) ----
         float sacc[8][4];
@@ -739,19 +778,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) sparse_attend_kernel(
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
     consumer_sync();
-    if (warp > 0) state_to_smem<kFp8>(st, sm, warp - 1, g8, t4);
+    if (warp > 0) state_to_smem<kFp8>(st, comb_ref(sm, warp), g8, t4);
     consumer_sync();
     if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps - 1; ++w) merge_from_smem<kFp8>(st, sm, w, g8, t4);
+    for (int w = 1; w < kConsumerWarps; ++w) merge_from_smem<kFp8>(st, comb_ref(sm, w), g8, t4);
     __syncwarp();
-    state_to_smem<kFp8>(st, sm, 0, g8, t4);  // staging for coalesced stores (slot 0 is read only by warp 0)
+    state_to_smem<kFp8>(st, comb_ref(sm, 0), g8, t4);  // staging for coalesced stores (read only by warp 0)
     __syncwarp();
     if constexpr (kSplit != 0) continue;  // the cluster merges slot 0 (split_finish)
     // ---- warp 0 writes: lane -> row lane/2, 64 dims ----
     const int row = lane >> 1, d0 = (lane & 1) * 64;
-    const float M = sm.comb_m[0][row], Lsum = sm.comb_l[0][row];
-    const float* src = &sm.comb[0][row][d0];
+    const CombRef c0 = comb_ref(sm, 0);
+    const float M = c0.m[row], Lsum = c0.l[row];
+    const float* src = c0.row(row) + d0;
     const bool complete = (seg_lo == range0) && (seg_end == range0 + topk);
     const long long oelem = (static_cast<long long>(qi) * kHeads + g * kGroup + row) * kDim + d0;
     __nv_bfloat16* orow = out_q ? nullptr : out + oelem;
@@ -894,8 +934,12 @@ static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static_assert(sizeof(AttSmem<0>) + 1024 <= 227 * 1024, "shared memory of the decode attention");
-static_assert(sizeof(AttSmem<1>) + 1024 <= 227 * 1024, "shared memory of the decode attention, FP8 K/V");
+template <int kFp8, int kSplit>
+constexpr size_t att_smem() { return sizeof(AttSmem<kFp8, kSplit>) + 1024; }
+static_assert(att_smem<0, 0>() <= 227 * 1024 && att_smem<1, 0>() <= 227 * 1024, "shared memory of the decode attention");
+static_assert(att_smem<0, 1>() <= 227 * 1024, "shared memory of the decode attention, cluster form");
+// two CTAs of the FP8 cluster form per SM (228 KB of shared memory per SM, 1 KB of it per CTA reserved)
+static_assert(2 * (att_smem<1, 1>() + 1024) <= 228 * 1024, "shared memory of the decode attention, FP8 cluster form");
 
 size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
 // one merge counter per CTA of the persistent grid (at most kNumSMs CTAs)
@@ -912,7 +956,7 @@ static int max_active_clusters(int kv_fp8, int c) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev][kv_fp8][c]) return cache[dev][kv_fp8][c];
-  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
+  const size_t smem = kv_fp8 ? att_smem<1, 1>() : att_smem<0, 1>();
   auto kern = kv_fp8 ? sparse_attend_kernel<1, 1> : sparse_attend_kernel<0, 1>;
   int n = 0;
   cudaLaunchConfig_t lc = {};
@@ -952,15 +996,16 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   const long long N = S * topk;
   // Few segments (small batches): one cluster of C CTAs per segment, merged
   // on chip -- the largest C in {8, 4, 2} with C <= topk (every CTA gets a
-  // unit), at most one CTA per SM, and every cluster resident at once.
-  // Otherwise stream-K over the whole grid.
+  // unit), at most one CTA per SM (two with an FP8 cache), and every cluster
+  // resident at once.  Otherwise stream-K over the whole grid, one CTA per SM.
+  const long long per_sm = kv_fp8 ? AttShape<1, 1>::kCtasPerSm : AttShape<0, 1>::kCtasPerSm;
   int C = 0;
   for (int c = kMaxCluster; c >= 2 && !C; c >>= 1) {
-    if (c > topk || S * c > kNumSMs) continue;
+    if (c > topk || S * c > per_sm * kNumSMs) continue;
     const int fit = max_active_clusters(kv_fp8, c);
     if (fit > 0 && S <= fit) C = c;
   }
-  const size_t smem = (kv_fp8 ? sizeof(AttSmem<1>) : sizeof(AttSmem<0>)) + 1024;
+  const size_t smem = C ? (kv_fp8 ? att_smem<1, 1>() : att_smem<0, 1>()) : (kv_fp8 ? att_smem<1, 0>() : att_smem<0, 0>());
   // a programmatic dependent of the previous kernel in the stream (the kernel
   // waits for that grid before touching memory), so its launch and prologue
   // overlap the decode top-k
