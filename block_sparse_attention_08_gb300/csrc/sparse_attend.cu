@@ -106,41 +106,48 @@ struct SegInfo {
 };
 
 // The chunk ring: 64-key chunks of K and V (bf16: 4 boxes of 64 dims, 32 KB;
-// FP8: one 128-byte box each, 16 KB), 6 stages.  The cluster form keeps no
-// separate buffer for the warps' states (each warp leaves its state in its own
-// stage, idle once the CTA's one segment is done); with an FP8 cache its 96 KB
-// of stages then let two CTAs share an SM, six consumer warps per SM, which
-// the FP8 attention (bound by its warps' issue) gains from (the 16-request
-// workload 31.4 -> 27.2 us).  A bf16 ring of 96 KB would leave each warp a
-// single stage, nothing landing while it computes: slower (18.4 -> 20.9 us on
-// the 4-request workload), so the bf16 cluster form stays at one CTA per SM.
+// FP8: one 128-byte box each, 16 KB), 6 stages.
+//
+// With an FP8 cache the attention is bound by its consumer warps' issue, not
+// by bytes, so two CTAs share an SM (six consumer warps per SM) on its 96 KB of
+// stages: one Q slot in the segment ring (the consumers free it as soon as
+// they hold their Q fragments) and, in the stream-K form, one slot where the
+// three warps' states meet one after the other.  The cluster form needs no such
+// slot at all: each warp leaves its state in its own stage, idle once the
+// CTA's one segment is done.  Measured: the 16-request workload's cluster form
+// 31.4 -> 27.2 us.  A bf16 ring of 96 KB would leave each warp a single stage,
+// nothing landing while it computes: slower (18.4 -> 20.9 us on the 4-request
+// workload), so bf16 stays at one CTA per SM.
 template <int kFp8, int kSplit>
 struct AttShape {
   static constexpr int kStageBytes = kFp8 ? kAttStage8Bytes : kAttStageBytes;
   static constexpr int kStages = kAttStages;
-  static constexpr int kCtasPerSm = kSplit && kFp8 ? 2 : 1;
+  static constexpr int kCtasPerSm = kFp8 ? 2 : 1;
+  static constexpr int kQSlots = kFp8 ? 1 : kSegSlots;             // Q tiles in the segment ring
+  static constexpr int kCombSlots = kFp8 ? 1 : kConsumerWarps - 1;  // stream-K: where states meet
 };
 
 // Where the consumer warps' states meet (stream-K only).
-template <int kSplit>
+template <int kSplit, int kSlots>
 struct AttComb {
-  float comb[kConsumerWarps - 1][kGroup][kCombStride];
-  float comb_m[kConsumerWarps - 1][kGroup];
-  float comb_l[kConsumerWarps - 1][kGroup];
+  float comb[kSlots][kGroup][kCombStride];
+  float comb_m[kSlots][kGroup];
+  float comb_l[kSlots][kGroup];
 };
-template <>
-struct AttComb<1> {};
+template <int kSlots>
+struct AttComb<1, kSlots> {};
 
 template <int kFp8, int kSplit>
 struct AttSmem {
-  alignas(1024) uint8_t stage[AttShape<kFp8, kSplit>::kStages][AttShape<kFp8, kSplit>::kStageBytes];
-  alignas(1024) uint8_t qtile[kSegSlots][2 * kQBoxBytes];
-  AttComb<kSplit> c;
-  SegInfo seg[kSegSlots];
-  uint64_t full[AttShape<kFp8, kSplit>::kStages];
-  uint64_t empty[AttShape<kFp8, kSplit>::kStages];
-  uint64_t seg_full[kSegSlots];
-  uint64_t seg_empty[kSegSlots];
+  using Shape = AttShape<kFp8, kSplit>;
+  alignas(1024) uint8_t stage[Shape::kStages][Shape::kStageBytes];
+  alignas(1024) uint8_t qtile[Shape::kQSlots][2 * kQBoxBytes];
+  AttComb<kSplit, Shape::kCombSlots> c;
+  SegInfo seg[Shape::kQSlots];
+  uint64_t full[Shape::kStages];
+  uint64_t empty[Shape::kStages];
+  uint64_t seg_full[Shape::kQSlots];
+  uint64_t seg_empty[Shape::kQSlots];
   int bcast;
 };
 
@@ -153,14 +160,15 @@ struct CombRef {
 };
 // who = 0: the CTA's merged state; who = w in 1, 2: the state of consumer warp w.
 // Stream-K: the shared buffer (the merged state over warp 1's slot, which warp
-// 0 has read by then); cluster form: stage `who`, which belongs to warp `who`.
+// 0 has read by then; with one slot the warps take turns); cluster form: stage
+// `who`, which belongs to warp `who`.
 template <int kFp8, int kSplit>
 __device__ __forceinline__ CombRef comb_ref(AttSmem<kFp8, kSplit>& sm, int who) {
   if constexpr (kSplit != 0) {
     float* base = reinterpret_cast<float*>(&sm.stage[who][0]);
     return CombRef{base, base + kGroup * kCombStride, base + kGroup * kCombStride + kGroup};
   } else {
-    const int slot = who > 0 ? who - 1 : 0;
+    const int slot = who > 0 ? (who - 1) % AttShape<kFp8, kSplit>::kCombSlots : 0;
     return CombRef{&sm.c.comb[slot][0][0], sm.c.comb_m[slot], sm.c.comb_l[slot]};
   }
 }
@@ -442,6 +450,7 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kStg = AttShape<kFp8, kSplit>::kStages;
+  constexpr int kQS = AttShape<kFp8, kSplit>::kQSlots;
   const long long N = static_cast<long long>(geo.nq) * kKvHeads * topk;
   const long long G = gridDim.x;
   long long lo, hi;
@@ -459,7 +468,7 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    for (int s = 0; s < kSegSlots; ++s) {
+    for (int s = 0; s < kQS; ++s) {
       mbar_init(&sm.seg_full[s], 1);
       mbar_init(&sm.seg_empty[s], kConsumerWarps);
     }
@@ -527,8 +536,8 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
         }
       }
       // segment slot: key counts + the Q tile of the 16 heads
-      const int ss = nseg % kSegSlots;
-      if (lane == 0) mbar_wait(&sm.seg_empty[ss], ((nseg / kSegSlots) & 1) ^ 1, err, 210);
+      const int ss = nseg % kQS;
+      if (lane == 0) mbar_wait(&sm.seg_empty[ss], ((nseg / kQS) & 1) ^ 1, err, 210);
       for (int j = 0; j < kMaxTopk; ++j) {
         const int v = __shfl_sync(0xffffffffu, nk_l, j);
         if (lane == 0) sm.seg[ss].nk[j] = j < jn ? v : 0;
@@ -578,8 +587,8 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
         const long long f = (sc - s + kStg - 1) / kStg;  // fills of stage s
         if (f > 0) mbar_wait(&sm.full[s], static_cast<uint32_t>((f - 1) & 1), err, 220);
       }
-      for (int s = 0; s < kSegSlots; ++s) {
-        const int f = (nseg - s + kSegSlots - 1) / kSegSlots;
+      for (int s = 0; s < kQS; ++s) {
+        const int f = (nseg - s + kQS - 1) / kQS;
         if (f > 0) mbar_wait(&sm.seg_full[s], (f - 1) & 1, err, 221);
       }
     }
@@ -600,8 +609,8 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
     const long long range0 = (static_cast<long long>(qi) * kKvHeads + g) * topk;
     const long long seg_end = min(hi, range0 + topk);
     const int jn = static_cast<int>(seg_end - it);
-    const int ss = nseg % kSegSlots;
-    mbar_wait(&sm.seg_full[ss], (nseg / kSegSlots) & 1, err, 310);
+    const int ss = nseg % kQS;
+    mbar_wait(&sm.seg_full[ss], (nseg / kQS) & 1, err, 310);
     const int nk_l = lane < kMaxTopk ? sm.seg[ss].nk[lane] : 0;
     // Q fragments of the 16 heads (A operand, 8 k-steps) from the swizzled Q tile
     uint32_t qa[8][4];
@@ -777,12 +786,27 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
     st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
-    consumer_sync();
-    if (warp > 0) state_to_smem<kFp8>(st, comb_ref(sm, warp), g8, t4);
-    consumer_sync();
-    if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
+    if constexpr (kSplit == 0 && AttShape<kFp8, kSplit>::kCombSlots == 1) {
+      // one slot: warp 2, then warp 1, hands its state to warp 0 (warp 0 has
+      // read it before it reaches the next segment's first meeting, the only
+      // place the slot is written again)
+      consumer_sync();
+      if (warp == 2) state_to_smem<kFp8>(st, comb_ref(sm, 1), g8, t4);
+      consumer_sync();
+      if (warp == 0) merge_from_smem<kFp8>(st, comb_ref(sm, 1), g8, t4);
+      consumer_sync();
+      if (warp == 1) state_to_smem<kFp8>(st, comb_ref(sm, 1), g8, t4);
+      consumer_sync();
+      if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
+      merge_from_smem<kFp8>(st, comb_ref(sm, 1), g8, t4);
+    } else {
+      consumer_sync();
+      if (warp > 0) state_to_smem<kFp8>(st, comb_ref(sm, warp), g8, t4);
+      consumer_sync();
+      if (warp > 0) continue;  // warps 1 and 2 go on to the next segment
 #pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) merge_from_smem<kFp8>(st, comb_ref(sm, w), g8, t4);
+      for (int w = 1; w < kConsumerWarps; ++w) merge_from_smem<kFp8>(st, comb_ref(sm, w), g8, t4);
+    }
     __syncwarp();
     state_to_smem<kFp8>(st, comb_ref(sm, 0), g8, t4);  // staging for coalesced stores (read only by warp 0)
     __syncwarp();
@@ -936,14 +960,16 @@ static bool make_q_map(CUtensorMap* map, const void* base, long long nq) {
 
 template <int kFp8, int kSplit>
 constexpr size_t att_smem() { return sizeof(AttSmem<kFp8, kSplit>) + 1024; }
-static_assert(att_smem<0, 0>() <= 227 * 1024 && att_smem<1, 0>() <= 227 * 1024, "shared memory of the decode attention");
-static_assert(att_smem<0, 1>() <= 227 * 1024, "shared memory of the decode attention, cluster form");
-// two CTAs of the FP8 cluster form per SM (228 KB of shared memory per SM, 1 KB of it per CTA reserved)
-static_assert(2 * (att_smem<1, 1>() + 1024) <= 228 * 1024, "shared memory of the decode attention, FP8 cluster form");
+static_assert(att_smem<0, 0>() <= 227 * 1024 && att_smem<0, 1>() <= 227 * 1024, "shared memory of the decode attention");
+// two CTAs of the FP8 forms per SM (228 KB of shared memory per SM, 1 KB of it per CTA reserved)
+static_assert(2 * (att_smem<1, 0>() + 1024) <= 228 * 1024 && 2 * (att_smem<1, 1>() + 1024) <= 228 * 1024,
+              "shared memory of the decode attention, FP8 K/V");
 
-size_t attend_partials_bytes() { return 2ull * kNumSMs * kPartialFloats * sizeof(float); }
-// one merge counter per CTA of the persistent grid (at most kNumSMs CTAs)
-size_t attend_tickets_bytes() { return static_cast<size_t>(kNumSMs) * sizeof(int); }
+// The stream-K grid: at most kCtasPerSm CTAs per SM (2 with an FP8 cache).
+constexpr int kMaxStreamKCtas = 2 * kNumSMs;
+size_t attend_partials_bytes() { return 2ull * kMaxStreamKCtas * kPartialFloats * sizeof(float); }
+// one merge counter per CTA of the persistent grid
+size_t attend_tickets_bytes() { return static_cast<size_t>(kMaxStreamKCtas) * sizeof(int); }
 
 // How many clusters of c CTAs of the split kernel can be resident at once
 // (cudaOccupancyMaxActiveClusters, asked once per device, K/V type and c; 0
@@ -1035,7 +1061,9 @@ cudaError_t launch_sparse_attend(const AttnGeom& geo, const void* q, const void*
   // At least 4 units per CTA: a segment is then shared by at most ~topk/4 + 1
   // CTAs, which bounds the partials its last CTA has to merge.
   long long grid_l = (N + 3) / 4;
-  if (grid_l > kNumSMs) grid_l = kNumSMs;
+  const long long max_ctas = static_cast<long long>(kv_fp8 ? AttShape<1, 0>::kCtasPerSm : AttShape<0, 0>::kCtasPerSm) *
+                             kNumSMs;
+  if (grid_l > max_ctas) grid_l = max_ctas;
   if (grid_l < 1) grid_l = 1;
   lc.gridDim = dim3(static_cast<unsigned>(grid_l));
   auto kern = kv_fp8 ? sparse_attend_kernel<1, 0> : sparse_attend_kernel<0, 0>;

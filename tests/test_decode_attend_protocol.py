@@ -49,14 +49,16 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, segments, rng, stages=STAGES, consumers=CONSUMERS, by_chunk=False, segment_ring=True):
+    def __init__(self, segments, rng, stages=STAGES, consumers=CONSUMERS, by_chunk=False, segment_ring=True,
+                 seg_slots=SEG_SLOTS):
         # segments: list of lists of key counts (0 = an empty / padded entry).
         # Without the segment ring (and its end-of-segment meetings) this is the
         # decode scorer's page ring: one stage per item, item i to a warp.
         self.segs, self.rng = segments, rng
         self.S, self.C, self.by_chunk, self.seg_ring = stages, consumers, by_chunk, segment_ring
+        self.Q = seg_slots
         self.bars = {}
-        for i in range(SEG_SLOTS):
+        for i in range(seg_slots):
             self.bars[f"seg_full{i}"] = Bar(f"seg_full{i}", 1)
             self.bars[f"seg_empty{i}"] = Bar(f"seg_empty{i}", SEG_EMPTY if consumers == CONSUMERS else consumers)
         for s in range(stages):
@@ -94,9 +96,9 @@ class Sim:
     def producer(self):
         sc = 0
         for nseg, keys in enumerate(self.segs):
-            ss = nseg % SEG_SLOTS
+            ss = nseg % self.Q
             if self.seg_ring:
-                yield self.wait(f"seg_empty{ss}", ((nseg // SEG_SLOTS) & 1) ^ 1, nseg // SEG_SLOTS)
+                yield self.wait(f"seg_empty{ss}", ((nseg // self.Q) & 1) ^ 1, nseg // self.Q)
                 self.load(f"seg{ss}", ("seg", nseg), f"seg_full{ss}")
             for nch in self.chunks(keys):
                 for _ in range(nch):
@@ -108,9 +110,9 @@ class Sim:
     def consumer(self, w):
         sc = 0
         for nseg, keys in enumerate(self.segs):
-            ss = nseg % SEG_SLOTS
+            ss = nseg % self.Q
             if self.seg_ring:
-                yield self.wait(f"seg_full{ss}", (nseg // SEG_SLOTS) & 1, nseg // SEG_SLOTS + 1)
+                yield self.wait(f"seg_full{ss}", (nseg // self.Q) & 1, nseg // self.Q + 1)
                 self.read(f"seg{ss}", ("seg", nseg))
                 self.reading[f"seg{ss}"] = self.reading.get(f"seg{ss}", 0) + 1
                 yield None  # the Q fragments are loaded
@@ -172,6 +174,13 @@ def segment_list(rng, n):
 def test_decode_attend_protocol_random_schedules(seed):
     rng = random.Random(seed)
     Sim(segment_list(rng, rng.randint(1, 6)), rng).run()
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_decode_attend_protocol_one_q_slot(seed):
+    # the FP8 cache's form: one Q tile in the segment ring (two CTAs per SM)
+    rng = random.Random(300 + seed)
+    Sim(segment_list(rng, rng.randint(1, 6)), rng, seg_slots=1).run()
 
 
 def test_decode_attend_protocol_twice_the_stages():
