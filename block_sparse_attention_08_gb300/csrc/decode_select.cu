@@ -81,14 +81,15 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 }
 
 // Exact top-`need` by (score desc, id asc) over the non-forced blocks of one
-// (request, head) row, then the ascending q2k row.  One warp.  The row's
-// scores are staged in shared memory first (rows of up to kTopkStage blocks;
-// longer rows are read from global memory as they go).  The need-th largest
-// of the 32 lane maxima is a threshold that at least `need` candidates reach,
-// so it keeps every one of the top `need`; those candidates (a few more than
-// `need` as a rule) go to shared memory, where each lane ranks its own
-// against all of them.  Ranks, not rounds of a warp-wide argmax, and no loop
-// waits on a global load per step.
+// (request, head) row, then the ascending q2k row.  One CTA of 128 threads per
+// row: the row's scores are staged in shared memory first (rows of up to
+// kTopkStage blocks; longer rows are read from global memory as they go), each
+// thread takes every 128th candidate, the need-th largest of the 128 thread
+// maxima is a threshold that at least `need` candidates reach (so it keeps all
+// of the top `need`), those candidates (a few more than `need` as a rule) are
+// gathered in shared memory, and each is ranked against the others by its own
+// thread.  (One warp per row took 2-7 us on rows of 64-1024 candidates.)
+constexpr int kTopkThreads = 128;
 constexpr int kTopkStage = 1024;
 
 __device__ __forceinline__ unsigned long long score_key(float v, int b) {
@@ -96,90 +97,6 @@ __device__ __forceinline__ unsigned long long score_key(float v, int b) {
 }
 __device__ __forceinline__ int key_block(unsigned long long key) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
-}
-
-// s: the row in global memory; stage: the same row in shared memory when
-// nb <= kTopkStage (else unused); cand: kCandCap keys and ids: kMaxTopk ints
-// of shared memory.
-__device__ void topk_row(const float* s, const float* stage, int nb, int topk, int init, int local, int32_t* out,
-                         unsigned long long* cand, int* ids) {
-  const int lane = threadIdx.x & 31;
-  if (nb <= topk) {
-    for (int i = lane; i < topk; i += 32) out[i] = i < nb ? i : -1;
-    return;
-  }
-  const int need = topk - init - local;
-  const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi), more than `need` of them
-  const bool staged = nb <= kTopkStage;
-  auto key_at = [&](int b) { return score_key(staged ? stage[b] : __ldcg(s + b), b); };
-  if (need > 0) {
-    unsigned long long best = 0;  // real keys are nonzero; a lane without candidates keeps 0
-    for (int b = c_lo + lane; b < c_hi; b += 32) {
-      const unsigned long long key = key_at(b);
-      best = key > best ? key : best;
-    }
-    // rank of this lane's maximum among the 32 (real keys are distinct and
-    // at least need + 1 lanes hold one, so exactly one lane has rank need - 1)
-    int rk = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) rk += __shfl_sync(0xffffffffu, best, j) > best ? 1 : 0;
-    const unsigned who = __ballot_sync(0xffffffffu, rk == need - 1);
-    const unsigned long long theta = __shfl_sync(0xffffffffu, best, who ? __ffs(who) - 1 : 0);
-    int count = 0;
-    for (int b0 = c_lo; b0 < c_hi; b0 += 32) {
-      const int b = b0 + lane;
-      const unsigned long long key = b < c_hi ? key_at(b) : 0ull;
-      const bool c = key >= theta && key != 0ull;
-      const unsigned m = __ballot_sync(0xffffffffu, c);
-      if (c) {
-        const int slot = count + __popc(m & ((1u << lane) - 1));
-        if (slot < kCandCap) cand[slot] = key;
-      }
-      count += __popc(m);
-    }
-    __syncwarp();
-    if (count <= kCandCap) {
-      // candidate j's rank = how many candidates are larger; ranks 0 .. need-1 are picked
-      const unsigned long long e0 = lane < count ? cand[lane] : 0ull;
-      const unsigned long long e1 = lane + 32 < count ? cand[lane + 32] : 0ull;
-      int r0 = 0, r1 = 0;
-#pragma unroll 8
-      for (int j = 0; j < count; ++j) {
-        const unsigned long long c = cand[j];
-        r0 += c > e0 ? 1 : 0;
-        r1 += c > e1 ? 1 : 0;
-      }
-      if (lane < count && r0 < need) ids[r0] = key_block(e0);
-      if (lane + 32 < count && r1 < need) ids[r1] = key_block(e1);
-    } else {
-      // rare: too many candidates at or above the threshold -- exact rounds
-      unsigned long long prev = ~0ull;
-      for (int i = 0; i < need; ++i) {
-        unsigned long long m = 0;
-        for (int b = c_lo + lane; b < c_hi; b += 32) {
-          const unsigned long long key = key_at(b);
-          if (key < prev && key > m) m = key;
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
-          m = x > m ? x : m;
-        }
-        prev = m;
-        if (lane == 0) ids[i] = key_block(m);
-      }
-    }
-  }
-  // forced ids after the picks; then each id's place in the ascending row
-  if (lane < init) ids[need + lane] = lane;
-  if (lane < local) ids[need + init + lane] = nb - local + lane;
-  __syncwarp();
-  if (lane < topk) {
-    const int id = ids[lane];
-    int pos = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxTopk; ++j) pos += j < topk && ids[j] < id ? 1 : 0;
-    out[pos] = id;
-  }
 }
 
 // How the page items [0, total) are shared out.  Each CTA first streams a
@@ -530,12 +447,15 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
 // Top-k per (request, head): one warp each, four per CTA (one request).
 // Launched right behind the scorer as a programmatic dependent: its CTAs may
 // start while the scorer drains, and wait for the scores to be complete.
-__global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
-                                                          int32_t* __restrict__ q2k, int topk, int init, int local,
-                                                          int* __restrict__ sched, DevError* err) {
-  __shared__ float stage[kKvHeads][kTopkStage];
-  __shared__ unsigned long long cand[kKvHeads][kCandCap];
-  __shared__ int ids[kKvHeads][kMaxTopk];
+__global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
+                                                                   int32_t* __restrict__ q2k, int topk, int init,
+                                                                   int local, int* __restrict__ sched, DevError* err) {
+  __shared__ float stage[kTopkStage];
+  __shared__ unsigned long long tmax[kTopkThreads];
+  __shared__ unsigned long long cand[kCandCap];
+  __shared__ int ids[kMaxTopk];
+  __shared__ unsigned long long theta_s;
+  __shared__ int count_s;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the scores are complete: a programmatic dependent (the decode attention)
   // may now be scheduled and run its prologue; it waits for this grid to end
@@ -544,24 +464,92 @@ __global__ void __launch_bounds__(128) decode_topk_kernel(const float* __restric
   // the scorer grid has completed and claims nothing more: its claim counter
   // goes back to zero for the next call (no work of this call reads it)
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
-  const int r = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x, lane = t & 31;
+  const int r = blockIdx.x / kKvHeads, h = blockIdx.x % kKvHeads;
   const float* row = scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks;
-  // stage the row's first min(max_blocks, kTopkStage) scores -- all loads in
+  int32_t* out = q2k + (static_cast<long long>(h) * geo.batch + r) * topk;
+  // stage the row's first min(max_blocks, kTopkStage) scores -- all copies in
   // flight together, and together with the length; entries past the
   // request's blocks are never used
   const int ns = min(geo.max_blocks, kTopkStage);
-#pragma unroll
-  for (int k = 0; k < kTopkStage / 32; ++k) {
-    const int b = lane + 32 * k;
-    if (b < ns) cp_async_4(&stage[h][b], row + b);
-  }
+  for (int b = t; b < ns; b += kTopkThreads) cp_async_4(&stage[b], row + b);
   const int L = geo.seq_lens[r];
+  if (t == 0) count_s = 0;
   cp_async_wait_all();
-  __syncwarp();
-  if (threadIdx.x == 0 && (L < 1 || L > geo.max_blocks * kBlock)) record_error(err, MSA_DEVERR_LENGTH, r);
+  __syncthreads();
+  if (t == 0 && h == 0 && (L < 1 || L > geo.max_blocks * kBlock)) record_error(err, MSA_DEVERR_LENGTH, r);
   const int nb = L < 1 ? 0 : min((L + kBlock - 1) / kBlock, geo.max_blocks);
-  topk_row(row, stage[h], nb, topk, init, local, q2k + (static_cast<long long>(h) * geo.batch + r) * topk, cand[h],
-           ids[h]);
+  if (nb <= topk) {
+    for (int i = t; i < topk; i += kTopkThreads) out[i] = i < nb ? i : -1;
+    return;
+  }
+  const int need = topk - init - local;
+  const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi), more than `need` of them
+  const bool staged = nb <= kTopkStage;
+  auto key_at = [&](int b) { return score_key(staged ? stage[b] : __ldcg(row + b), b); };
+  if (need > 0) {
+    unsigned long long best = 0;  // real keys are nonzero; a thread without candidates keeps 0
+    for (int b = c_lo + t; b < c_hi; b += kTopkThreads) {
+      const unsigned long long key = key_at(b);
+      best = key > best ? key : best;
+    }
+    tmax[t] = best;
+    __syncthreads();
+    // the rank of this thread's maximum among the 128 (real keys are distinct
+    // and at least need + 1 threads hold one, so exactly one has rank need - 1)
+    int rk = 0;
+#pragma unroll 8
+    for (int j = 0; j < kTopkThreads; ++j) rk += tmax[j] > best ? 1 : 0;
+    if (rk == need - 1 && best != 0ull) theta_s = best;
+    __syncthreads();
+    const unsigned long long theta = theta_s;
+    for (int b = c_lo + t; b < c_hi; b += kTopkThreads) {
+      const unsigned long long key = key_at(b);
+      if (key >= theta) {
+        const int slot = atomicAdd(&count_s, 1);
+        if (slot < kCandCap) cand[slot] = key;
+      }
+    }
+    __syncthreads();
+    const int count = count_s;
+    if (count <= kCandCap) {
+      // candidate t's rank = how many candidates are larger; ranks 0 .. need-1 are picked
+      if (t < count) {
+        const unsigned long long e = cand[t];
+        int rank = 0;
+#pragma unroll 8
+        for (int j = 0; j < count; ++j) rank += cand[j] > e ? 1 : 0;
+        if (rank < need) ids[rank] = key_block(e);
+      }
+    } else if (t < 32) {
+      // rare: too many candidates at or above the threshold -- exact rounds by one warp
+      unsigned long long prev = ~0ull;
+      for (int i = 0; i < need; ++i) {
+        unsigned long long m = 0;
+        for (int b = c_lo + lane; b < c_hi; b += 32) {
+          const unsigned long long key = key_at(b);
+          if (key < prev && key > m) m = key;
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          const unsigned long long x = __shfl_xor_sync(0xffffffffu, m, o);
+          m = x > m ? x : m;
+        }
+        prev = m;
+        if (lane == 0) ids[i] = key_block(m);
+      }
+    }
+  }
+  // forced ids after the picks; then each id's place in the ascending row
+  if (t < init) ids[need + t] = t;
+  if (t < local) ids[need + init + t] = nb - local + t;
+  __syncthreads();
+  if (t < topk) {
+    const int id = ids[t];
+    int pos = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) pos += j < topk && ids[j] < id ? 1 : 0;
+    out[pos] = id;
+  }
 }
 
 cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, const void* index_k,
@@ -590,8 +578,8 @@ cudaError_t launch_decode_select(const msa_config& cfg, const void* index_q, con
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(batch));
-  lc.blockDim = dim3(128);
+  lc.gridDim = dim3(static_cast<unsigned>(batch) * kKvHeads);  // one CTA per (request, head) row
+  lc.blockDim = dim3(kTopkThreads);
   lc.dynamicSmemBytes = 0;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
