@@ -63,6 +63,23 @@ def test_decode_request_counts(n_req, topk):
     _run(d, topk, 0, 1 if topk > 1 else 0, f"decode {n_req} requests")
 
 
+def test_decode_no_request_needs_scoring():
+    # every context within topk blocks: the scorer has no page to score (its
+    # claims and groups are all empty) and the top-k writes every row itself
+    lens = [1, 2, 127, 128, 129, 1000, 2047, 2048, 300, 5]
+    d = msa_synth.decode_inputs(lens, paged=True, seed=19, device="cuda")
+    _run(d, 16, 0, 1, "decode, no request above topk blocks")
+
+
+def test_decode_rows_longer_than_the_topk_stage():
+    # a context of 1200 blocks: its score rows are longer than the 1024 the
+    # top-k stages in shared memory, so they are read from global memory as
+    # they go; the others are staged
+    lens = [1200 * 128 - 5, 3000, 70000]
+    d = msa_synth.decode_inputs(lens, paged=True, seed=23, device="cuda")
+    _run(d, 16, 1, 1, "decode, a 153 k-token context")
+
+
 @pytest.mark.parametrize("paged", [False, True])
 def test_decode_small_batch_mxfp8_and_fp8_kv(paged):
     # the cluster-merged attention (3 requests: clusters of 8) with both output
