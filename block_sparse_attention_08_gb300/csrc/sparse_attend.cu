@@ -973,7 +973,7 @@ size_t attend_tickets_bytes() { return static_cast<size_t>(kMaxStreamKCtas) * si
 
 // How many clusters of c CTAs of the split kernel can be resident at once
 // (cudaOccupancyMaxActiveClusters, asked once per device, K/V type and c; 0
-// when the query fails, which keeps the stream-K kernel).
+// when the query fails, which keeps the stream-K kernel for that call).
 static int max_active_clusters(int kv_fp8, int c) {
   static std::mutex mu;
   static int cache[64][2][kMaxCluster + 1];
@@ -999,7 +999,7 @@ static int max_active_clusters(int kv_fp8, int c) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess ||
       cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess) {
     cudaGetLastError();  // a failed query leaves no error behind for the launch that follows
-    n = 0;
+    return 0;            // and is asked again next time (it is not kept)
   }
   cache[dev][kv_fp8][c] = n;
   done[dev][kv_fp8][c] = true;
