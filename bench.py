@@ -488,7 +488,21 @@ def run_gpu(args, rank, world, device, name=None, steps=None):
         torch.distributed.barrier()
     t_sel = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     t_att = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
-    ms = sum(evs[i][0].elapsed_time(evs[i][1]) for i in range(steps)) / steps
+    step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(steps)]
+    ms = sum(step_ms) / steps
+
+    # the same step as eager C-ABI calls (no graph), same L2 flush between steps
+    eager_ms = None
+    if not args.no_graph:
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush_l2(i)
+            ee[i][0].record(stream)
+            sel()
+            att()
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        eager_ms = sum(ee[i][0].elapsed_time(ee[i][1]) for i in range(steps)) / steps
 
     # end to end through the public API with host buffers (pinned), per step:
     # H2D of the step's inputs, D2H of the output.  Decode: the new queries,
@@ -567,7 +581,7 @@ def run_gpu(args, rank, world, device, name=None, steps=None):
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    return dict(ms=ms, sel_ms=sum(t_sel) / len(t_sel), att_ms=sum(t_att) / len(t_att),
+    return dict(ms=ms, step_ms=step_ms, eager_ms=eager_ms, sel_ms=sum(t_sel) / len(t_sel), att_ms=sum(t_att) / len(t_att),
                 e2e_ms=sum(e_ms) / len(e_ms), n_queries=n_queries, work=work, entries=entries, h2d=h2d, d2h=d2h,
                 clocks=clk.summary(), decode=decode, hbm_peak=hbm_peak, tf_peak=tf_peak, peak_src=peak_src,
                 inputs=inp, q2k=q2k, steps=steps, name=name)
@@ -760,7 +774,9 @@ def main():
                    "l2": "flushed between steps (256 MiB write + 256 MiB read, outside the timed events)",
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu"})
     line = {"metric": METRIC, "value": summ["value"], "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "step_ms_percentiles": _percentiles(res["step_ms"]),
+            "eager_ms_per_step": round(res["eager_ms"], 4) if res["eager_ms"] is not None else None,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": summ["dtype"], "data": "synthetic", "config": config,
             "roofline": summ["roofline"], "e2e": summ["e2e"],
             "gpu_launches": launches_per_step(res["decode"]) * args.steps, "clocks": res["clocks"]}
@@ -788,6 +804,13 @@ def main():
         line["cpu_baseline"] = cpu_baseline(args.workload, args.seed, inputs=inputs, gpu_q2k=gpu_q2k)
         del inputs
     print(json.dumps(line))
+
+
+def _percentiles(xs):
+    """p10 / p50 / p90 of the timed steps (ms), nearest rank."""
+    v = sorted(xs)
+    pick = lambda q: round(v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))], 4)
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9)}
 
 
 def launches_per_step(decode):
