@@ -196,6 +196,14 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 // This thread's bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// A 32-bit load with acquire semantics at GPU scope: the writes that preceded
+// a release (or a fence and the store or atomic) that produced the value are
+// visible after it.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }

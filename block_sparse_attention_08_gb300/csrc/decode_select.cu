@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) decode_select_kernel(
   }
 }
 
-// Top-k per (request, head): one warp each, four per CTA (one request).
+// Top-k per (request, head): one CTA of kTopkThreads threads per row.
 // Launched right behind the scorer as a programmatic dependent: its CTAs may
 // start while the scorer drains, and wait for the scores to be complete.
 __global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* __restrict__ scores, DecodeGeom geo,
@@ -456,6 +456,12 @@ __global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* 
   __shared__ int ids[kMaxTopk];
   __shared__ unsigned long long theta_s;
   __shared__ int count_s;
+  const int r = blockIdx.x / kKvHeads, h = blockIdx.x % kKvHeads;
+  // The request's length is an input of the call, not a result of the scorer,
+  // and the scorer is an ordinary launch (it starts after all earlier work in
+  // the stream, and this grid after it), so it is read before the wait: its
+  // load (often a DRAM miss after the scorer's stream) overlaps the scorer's end.
+  const int L = geo.seq_lens[r];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the scores are complete: a programmatic dependent (the decode attention)
   // may now be scheduled and run its prologue; it waits for this grid to end
@@ -465,15 +471,12 @@ __global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* 
   // goes back to zero for the next call (no work of this call reads it)
   if (blockIdx.x == 0 && threadIdx.x == 0) sched[0] = 0;
   const int t = threadIdx.x, lane = t & 31;
-  const int r = blockIdx.x / kKvHeads, h = blockIdx.x % kKvHeads;
   const float* row = scores + (static_cast<long long>(r) * kKvHeads + h) * geo.max_blocks;
   int32_t* out = q2k + (static_cast<long long>(h) * geo.batch + r) * topk;
   // stage the row's first min(max_blocks, kTopkStage) scores -- all copies in
-  // flight together, and together with the length; entries past the
-  // request's blocks are never used
+  // flight together; entries past the request's blocks are never used
   const int ns = min(geo.max_blocks, kTopkStage);
   for (int b = t; b < ns; b += kTopkThreads) cp_async_4(&stage[b], row + b);
-  const int L = geo.seq_lens[r];
   if (t == 0) count_s = 0;
   cp_async_wait_all();
   __syncthreads();

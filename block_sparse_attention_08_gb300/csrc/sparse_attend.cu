@@ -643,6 +643,13 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
     if (lane == 0) mbar_arrive(&sm.seg_empty[ss]);  // the slot may be refilled
     ++nseg;
 
+    // This CTA holds the end of a segment whose start lies in earlier CTAs: it
+    // is then, in all likelihood, the one that merges it (the others took it
+    // at the start of their ranges), so warp 0 brings their partials back into
+    // L2 two units before the end (the streaming may have evicted them).
+    const bool pf = kSplit == 0 && warp == 0 && seg_end == range0 + topk && seg_lo > range0;
+    const int pf_k = jn > 2 ? jn - 2 : 0;
+
     WarpState st;
     st.m0 = st.m1 = -INFINITY;
     st.l0 = st.l1 = 0.f;
@@ -653,6 +660,14 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
       const int nk = __shfl_sync(0xffffffffu, nk_l, k);
       if (nk == 0) continue;
       const int nch = (nk + kChunkKeys - 1) / kChunkKeys;
+      if (pf && k == pf_k) {
+        const long long c0 = cta_of(range0, N, G);
+        for (long long c = c0; c < blockIdx.x; ++c) {
+          const long long slot = 2 * c + (c == c0 && seg_begin(c0, N, G) < range0 ? 1 : 0);
+          const char* pp = reinterpret_cast<const char*>(partials + slot * kPartialFloats);
+          for (int o = lane * 128; o < kPartialFloats * 4; o += 32 * 128) prefetch_l2(pp + o);
+        }
+      }
       for (int ch = 0; ch < nch; ++ch, ++sc) {
         const int s = static_cast<int>(sc % kStg);
         if (s % kConsumerWarps != warp) continue;
@@ -831,36 +846,46 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
               pack_bf16(src[8 * v + 4] * inv, src[8 * v + 5] * inv), pack_bf16(src[8 * v + 6] * inv, src[8 * v + 7] * inv));
       }
     } else {
-      // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
-      const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
-      float* pp = partials + slot * kPartialFloats;
-      if ((lane & 1) == 0) {
-        pp[row] = M;
-        pp[16 + row] = Lsum;
-      }
-#pragma unroll
-      for (int v = 0; v < 16; ++v)
-        *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + 4 * v) =
-            make_float4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
-      __threadfence();
-      __syncwarp();
       // The contributors are the consecutive CTAs c_first .. c_last (at most
       // topk: each holds at least one unit of the segment).  The segment's
       // counter is the one of c_first: a CTA is the first contributor of a cut
       // segment only for its last segment, so each counter serves one segment.
       const long long c_first = cta_of(range0, N, G);
+      const int cnt = static_cast<int>(seg_end - seg_lo);
+      // If every other contributor has already counted its units, this CTA
+      // completes the segment and merges it at once from its own state, without
+      // publishing a partial.  (They write their partial, fence, then add; the
+      // acquire load that sees their counts also sees their partials.  No
+      // contributor adds after that, so no other CTA merges the segment.)
       int last = 0;
-      if (lane == 0) {
-        const int cnt = static_cast<int>(seg_end - seg_lo);
-        last = (atomicAdd(&tickets[c_first], cnt) + cnt == topk) ? 1 : 0;
-      }
+      if (lane == 0) last = (ld_acquire_gpu(&tickets[c_first]) + cnt == topk) ? 1 : 0;
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
+      if (!last) {
+        // partial slot: the CTA's first segment -> 2c, its last -> 2c+1
+        const long long slot = 2LL * blockIdx.x + (range0 <= lo ? 0 : 1);
+        float* pp = partials + slot * kPartialFloats;
+        if ((lane & 1) == 0) {
+          pp[row] = M;
+          pp[16 + row] = Lsum;
+        }
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+          *reinterpret_cast<float4*>(pp + 32 + row * kDim + d0 + 4 * v) =
+              make_float4(src[4 * v], src[4 * v + 1], src[4 * v + 2], src[4 * v + 3]);
         __threadfence();
-        // Every contributor but the first wrote this segment as its first
-        // partial.  All loads of a pass are issued before any is used.
+        __syncwarp();
+        if (lane == 0) last = (atomicAdd(&tickets[c_first], cnt) + cnt == topk) ? 1 : 0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) __threadfence();
+      }
+      if (last) {
+        // This CTA's own share comes from its staged state (shared memory), the
+        // others' from their partials.  Every contributor but the first wrote
+        // this segment as its first partial.  All loads of a pass are issued
+        // before any is used.
         const long long c_last = cta_of(range0 + topk - 1, N, G);
         const int nc = static_cast<int>(c_last - c_first + 1);
+        const int xs = static_cast<int>(blockIdx.x - c_first);
         const long long slot0 = 2 * c_first + (seg_begin(c_first, N, G) < range0 ? 1 : 0);
         auto part_of = [&](int x) {
           return partials + (x == 0 ? slot0 : 2 * (c_first + x)) * kPartialFloats;
@@ -868,34 +893,36 @@ __global__ void __launch_bounds__(kAttThreads, AttShape<kFp8, kSplit>::kCtasPerS
         float mc[kMaxTopk], lc[kMaxTopk];
 #pragma unroll
         for (int x = 0; x < kMaxTopk; ++x) {
-          mc[x] = x < nc ? __ldcg(part_of(x) + row) : -INFINITY;
-          lc[x] = x < nc ? __ldcg(part_of(x) + 16 + row) : 0.f;
+          mc[x] = x < nc && x != xs ? __ldcg(part_of(x) + row) : -INFINITY;
+          lc[x] = x < nc && x != xs ? __ldcg(part_of(x) + 16 + row) : 0.f;
         }
-        float Mg = -INFINITY;
+        float Mg = M;
 #pragma unroll
         for (int x = 0; x < kMaxTopk; ++x) Mg = fmaxf(Mg, mc[x]);
         const float Mgu = Mg == -INFINITY ? 0.f : Mg;
-        float Lg = 0.f, ag[64];
+        const float fs = exp2f(M - Mgu);  // this CTA's weight
+        float Lg = Lsum * fs, ag[64];
 #pragma unroll
-        for (int d = 0; d < 64; ++d) ag[d] = 0.f;
+        for (int d = 0; d < 64; ++d) ag[d] = src[d] * fs;
 #pragma unroll
         for (int x = 0; x < kMaxTopk; ++x) {
-          mc[x] = exp2f(mc[x] - Mgu);  // the contributor's weight (0 past nc)
+          mc[x] = exp2f(mc[x] - Mgu);  // the contributor's weight (0 past nc and for this CTA)
           Lg += lc[x] * mc[x];
         }
 #pragma unroll 2
         for (int x = 0; x < nc; ++x) {
+          if (x == xs) continue;
           const float* pc = part_of(x) + 32 + row * kDim + d0;
-          float4 xs[16];
+          float4 xv[16];
 #pragma unroll
-          for (int d = 0; d < 16; ++d) xs[d] = __ldcg(reinterpret_cast<const float4*>(pc) + d);
+          for (int d = 0; d < 16; ++d) xv[d] = __ldcg(reinterpret_cast<const float4*>(pc) + d);
           const float f = mc[x];
 #pragma unroll
           for (int d = 0; d < 16; ++d) {
-            ag[4 * d] += xs[d].x * f;
-            ag[4 * d + 1] += xs[d].y * f;
-            ag[4 * d + 2] += xs[d].z * f;
-            ag[4 * d + 3] += xs[d].w * f;
+            ag[4 * d] += xv[d].x * f;
+            ag[4 * d + 1] += xv[d].y * f;
+            ag[4 * d + 2] += xv[d].z * f;
+            ag[4 * d + 3] += xv[d].w * f;
           }
         }
         const float inv = Lg > 0.f ? (kFp8 ? v_scale : 1.f) / Lg : 0.f;
