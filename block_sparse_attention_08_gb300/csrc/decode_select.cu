@@ -84,11 +84,14 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 // (request, head) row, then the ascending q2k row.  One CTA of 128 threads per
 // row: the row's scores are staged in shared memory first (rows of up to
 // kTopkStage blocks; longer rows are read from global memory as they go), each
-// thread takes every 128th candidate, the need-th largest of the 128 thread
-// maxima is a threshold that at least `need` candidates reach (so it keeps all
-// of the top `need`), those candidates (a few more than `need` as a rule) are
-// gathered in shared memory, and each is ranked against the others by its own
-// thread.  (One warp per row took 2-7 us on rows of 64-1024 candidates.)
+// thread takes every 128th candidate, the first warp reduces the 128 thread
+// maxima to 32 (the maxima of every 32nd candidate) and sorts them with a
+// bitonic network over its lanes; the need-th largest of the 32 is a threshold
+// that at least `need` candidates reach (so it keeps all of the top `need`),
+// those candidates (a few more than `need` as a rule) are gathered in shared
+// memory, and each is ranked against the others by its own thread.  (One warp
+// per row took 2-7 us on rows of 64-1024 candidates; ranking each of the 128
+// thread maxima against the others, 1200-4400 cycles.)
 constexpr int kTopkThreads = 128;
 constexpr int kTopkStage = 1024;
 
@@ -498,12 +501,29 @@ __global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* 
     }
     tmax[t] = best;
     __syncthreads();
-    // the rank of this thread's maximum among the 128 (real keys are distinct
-    // and at least need + 1 threads hold one, so exactly one has rank need - 1)
-    int rk = 0;
-#pragma unroll 8
-    for (int j = 0; j < kTopkThreads; ++j) rk += tmax[j] > best ? 1 : 0;
-    if (rk == need - 1 && best != 0ull) theta_s = best;
+    if (t < 32) {
+      // lane l: the largest key of threads l, l + 32, l + 64, l + 96, i.e. of
+      // every 32nd candidate.  At least need + 1 lanes hold a real key (there
+      // are more than need candidates and need < 32), so the need-th largest of
+      // the 32 lane maxima is a score that at least need candidates reach.  The
+      // 32 are sorted in descending order by a bitonic network over the lanes.
+      // Only the score half of a key (its upper 32 bits) takes part: a
+      // threshold on the score alone keeps every key of an equal score.
+      uint32_t v = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkThreads / 32; ++w) v = max(v, static_cast<uint32_t>(tmax[lane + 32 * w] >> 32));
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const uint32_t o = __shfl_xor_sync(0xffffffffu, v, j);
+          // the lower lane of a pair keeps the larger value in a descending run
+          const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+          v = keep_max ? max(v, o) : min(v, o);
+        }
+      }
+      if (lane == need - 1) theta_s = static_cast<unsigned long long>(v) << 32;
+    }
     __syncthreads();
     const unsigned long long theta = theta_s;
     for (int b = c_lo + t; b < c_hi; b += kTopkThreads) {

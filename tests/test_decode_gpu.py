@@ -80,6 +80,36 @@ def test_decode_rows_longer_than_the_topk_stage():
     _run(d, 16, 1, 1, "decode, a 153 k-token context")
 
 
+@pytest.mark.parametrize("pattern", ["all equal", "two levels"])
+def test_decode_tied_scores(pattern):
+    # Exact ties: every key of a context the same vector ("all equal": every
+    # block scores the same), or blocks alternating between two vectors ("two
+    # levels": half the blocks tie at the higher score).  Ties are broken by the
+    # lower block id on both sides, so q2k must match the oracle bit for bit,
+    # near-tie exemption or not.  Rows of 301 and 547 blocks put more than 64
+    # candidates at the top-k's threshold (its exact fallback path).
+    lens = [300 * 128 + 7, 5000, 70000]
+    d = msa_synth.decode_inputs(lens, paged=False, seed=31, device="cuda")
+    ik = d.index_k_cache
+    cu = d.cu_seqlens_k.cpu().tolist()
+    for r, L in enumerate(lens):
+        a, b = ik[cu[r]].clone(), ik[cu[r] + 1].clone()
+        rows = ik[cu[r]:cu[r] + L]
+        rows[:] = a
+        if pattern == "two levels":
+            blk = torch.arange(L, device="cuda") // 128
+            rows[blk % 2 == 1] = b
+    for topk, init, local in [(16, 0, 1), (16, 2, 3), (5, 1, 0)]:
+        kw = dict(page_table=d.page_table, cu_seqlens_k=d.cu_seqlens_k, max_blocks=d.max_blocks)
+        q2k = msa.msa_select_blocks_decode(d.index_q, ik, d.seq_lens, topk=topk, init_blocks=init,
+                                           local_blocks=local, **kw)
+        torch.cuda.synchronize()
+        ref, _, _ = oracle.select_decode(d.index_q, ik, d.seq_lens, page_table=d.page_table,
+                                         cu_seqlens_k=d.cu_seqlens_k, topk=topk, init=init, local=local,
+                                         return_scores=True)
+        assert np.array_equal(q2k.cpu().numpy(), ref), (pattern, topk, init, local)
+
+
 @pytest.mark.parametrize("paged", [False, True])
 def test_decode_small_batch_mxfp8_and_fp8_kv(paged):
     # the cluster-merged attention (3 requests: clusters of 8) with both output
