@@ -56,6 +56,42 @@ def test_prefill_e4m3_small(topk, init, local):
            label="prefill small documents, E4M3 index")
 
 
+@pytest.mark.parametrize("pattern", ["all equal", "two levels"])
+def test_prefill_tied_scores(pattern):
+    # Exact ties: every index key of a document the same vector a ("all
+    # equal": every block of a query scores the same), or blocks alternating
+    # between a and -a ("two levels": the scores of a query are +s and -s).
+    # Ties are broken by the lower block id on both sides, so q2k must match
+    # the oracle bit for bit, near-tie exemption or not.
+    p = msa_synth.prefill_inputs([3000, 700, 2049], seed=41, device="cuda")
+    cu = p.cu_seqlens.cpu().tolist()
+    ik = p.index_k
+    for d in range(len(cu) - 1):
+        rows = ik[cu[d]:cu[d + 1]]
+        a = rows[0].clone()
+        rows[:] = a
+        if pattern == "two levels":
+            blk = torch.arange(cu[d + 1] - cu[d], device="cuda") // 128
+            rows[blk % 2 == 1] = -a
+    T = p.total_tokens
+    every = np.arange(T, dtype=np.int64)
+    for topk, init, local in [(16, 0, 1), (16, 2, 3), (5, 1, 0)]:
+        q2k = msa.msa_select_blocks_prefill(p.index_q, ik, p.cu_seqlens, p.max_seqlen, topk=topk, init_blocks=init,
+                                            local_blocks=local)
+        torch.cuda.synchronize()
+        ref, _, _ = oracle.select_prefill(p.index_q, ik, p.cu_seqlens, every, topk=topk, init=init, local=local,
+                                          return_scores=True)
+        assert np.array_equal(q2k.cpu().numpy(), ref), (pattern, topk, init, local)
+
+
+def test_prefill_many_tiny_documents():
+    # 400 documents of 1..40 tokens around two longer ones: many documents per
+    # bucketing window, most of them a single partial block
+    lens = np.random.default_rng(8).integers(1, 41, size=400).tolist()
+    p = msa_synth.prefill_inputs(lens[:200] + [2500] + lens[200:] + [700], seed=9, device="cuda")
+    _check(p, label="prefill, 402 documents")
+
+
 def test_prefill_e4m3_repeated_calls_are_identical():
     p = msa_synth.prefill_inputs([2500, 300], seed=6, device="cuda", index_dtype="e4m3")
     a = msa.msa_select_blocks_prefill(p.index_q, p.index_k, p.cu_seqlens, p.max_seqlen)
