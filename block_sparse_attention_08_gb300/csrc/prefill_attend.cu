@@ -16,10 +16,13 @@
 // tensor cores see full 128 x 128 x 128 products:
 //
 //   S = Q K^T   (A = gathered Q rows, B = K block; both K-major, 128-byte swizzle)
-//   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 back into S's columns)
+//   P = exp2(S * scale * log2 e - rowmax)   (fp32 in registers, bf16 into a P buffer)
 //   O = P V     (A = P read from tensor memory, B = V read MN-major from the TMA tile)
 //
-// with S and O in tensor memory (double-buffered, 4 x 128 columns).  Warp 16
+// with S (twice), P (twice) and O (once) in tensor memory: a softmax warpgroup
+// frees its S buffer as soon as it has read it, so the next S product into it
+// waits for no O product, and the two epilogue warpgroups take turns on the
+// one O buffer.  Warp 16
 // schedules the tiles (descriptors and entries read ahead from global memory,
 // published in a shared-memory ring) and issues TMA (Q rows gathered with a
 // 3-D tensor map, one 16-head box per entry; K and V blocks as 128-row boxes);
@@ -65,6 +68,10 @@ constexpr int kBmProducerWarp = 16;
 constexpr int kBmMmaSWarp = 17;
 constexpr int kBmMmaOWarp = 18;
 constexpr int kBmChunk = 16;                      // tiles per scheduling chunk
+// Tensor-memory columns: S twice (fp32, 128 columns each), P twice (bf16
+// pairs, 64 columns each), O once (fp32, 128 columns).
+constexpr uint32_t kBmPCol = 256;
+constexpr uint32_t kBmOCol = 384;
 constexpr uint32_t kBmIdescS = tc::idesc_bf16_f32(128, 128);
 constexpr uint32_t kBmIdescO = tc::idesc_bf16_f32(128, 128) | (1u << 16);  // B (V) MN-major
 
@@ -97,7 +104,7 @@ struct BmSmem {
   uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full[kBmKStages], k_empty[kBmKStages];
   uint64_t v_full[kBmVStages], v_empty[kBmVStages];
   uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
-  uint64_t p_full[2], done_s, done_o;
+  uint64_t p_full[2], p_free[2], done_s, done_o;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
   uint32_t tmem_base;
@@ -496,10 +503,11 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 1);  // committed by the O MMAs that read P from the same columns
+      mbar_init(&sm.s_free[i], 4);  // the softmax warpgroup's four warps, once they have read S
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 4);
       mbar_init(&sm.p_full[i], 4);
+      mbar_init(&sm.p_free[i], 1);  // committed by the O MMAs that read P
     }
     for (int i = 0; i < kBmKStages; ++i) {
       mbar_init(&sm.k_full[i], 1);
@@ -657,9 +665,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       mbar_wait(&sm.done_s, 0, err, 716);
     }
   } else if (warp == kBmMmaOWarp) {
-    // ---------------- O MMAs: O(i) = P(i) V into tensor-memory buffer 2 + i % 2 ----------------
-    // A = P from tensor memory (written by the softmax over the S it came from),
-    // B = V from shared memory; their completion also frees the S / P columns.
+    // ---------------- O MMAs: O(i) = P(i) V into the one O buffer ----------------
+    // A = P from tensor memory (P buffer i % 2, written by the softmax of the
+    // tile), B = V from shared memory; their completion frees the P buffer.
+    // The O buffer is free once the epilogue of tile i - 1 has read it.
     if (lane == 0) {
       int nv = 0, vs = 0;
       for (int i = 0; i < n; ++i) {
@@ -675,17 +684,17 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         }
         const int b = i & 1;
         if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, err, 714) ||
-            !mbar_wait(&sm.o_free[b], ((i >> 1) & 1) ^ 1, err, 715))
+            (i > 0 && !mbar_wait(&sm.o_free[(i - 1) & 1], ((i - 1) >> 1) & 1, err, 715)))
           break;
         tc::fence_after();
         const uint32_t va = smem_u32(sm.v[vs]);
-        const uint32_t pt = tmem + b * 128;  // P over the first 64 columns of the S buffer
-        const uint32_t dt = tmem + 256 + b * 128;
+        const uint32_t pt = tmem + kBmPCol + b * 64;
+        const uint32_t dt = tmem + kBmOCol;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc::mma_bf16_ts(dt, pt + kk * 8, desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
         tc::commit(&sm.o_full[b]);
-        tc::commit(&sm.s_free[b]);
+        tc::commit(&sm.p_free[b]);
       }
       tc::commit(&sm.done_o);
       mbar_wait(&sm.done_o, 0, err, 719);
@@ -696,6 +705,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     const int wg = warp >> 2, quarter = warp & 3;
     const int r = quarter * 32 + lane, e = r >> 4, h = r & 15;
     const uint32_t srow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 128;
+    const uint32_t prow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kBmPCol + wg * 64;
     for (int i = wg; i < n; i += 2) {
       const int is = i % kBmInfo, k = i >> 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 723))) break;
@@ -710,6 +720,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       // phase 1: the row's exponent reference, requested before the wait for S
       const float mr = phase && valid ? __ldcg(p.mref + row) : 0.f;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, 720))) break;
+      // the P buffer: read by the O MMA of this warpgroup's previous tile
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_free[wg], (k & 1) ^ 1, err, 725))) break;
       tc::fence_after();
       // Rows whose keys are all causal (every block but the diagonal one) skip
       // the per-key mask.
@@ -744,11 +756,10 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         } else {
           mu = mr;
         }
-        // p = 2^(s * scale * log2 e - mu) in bf16 over the S columns already
-        // read (P chunk ch, 16 columns, lands in S chunk ch / 2); the fp32 row
-        // sum adds the same bf16-rounded values, so the normalisation matches
-        // the weights the PV product applies (which matters when one key
-        // dominates a row and its p is not a power of two)
+        // p = 2^(s * scale * log2 e - mu) in bf16 (P chunk ch: 16 columns of
+        // the P buffer); the fp32 row sum adds the same bf16-rounded values, so
+        // the normalisation matches the weights the PV product applies (which
+        // matters when one key dominates a row and its p is not a power of two)
         float2 l4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) l4[q] = make_float2(0.f, 0.f);
@@ -771,12 +782,16 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
             pk[q] = pp;
             l4[q & 3] = add2(l4[q & 3].x, l4[q & 3].y, __uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u));
           }
-          tc::st_32x32b_x16(srow + ch * 16, pk);
+          tc::st_32x32b_x16(prow + ch * 16, pk);
         }
         l = ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
       };
       if (masked) softmax_rows(std::true_type{});
       else softmax_rows(std::false_type{});
+      // every S column has been read: the next S of this buffer may be issued
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[wg]);
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
@@ -802,7 +817,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     // the tensor engine store (phase 0) or add (phase 1) the two 16-row boxes
     // into the fp32 accumulators [T][64][128].
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
-    const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 256 + wg * 128;
+    const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kBmOCol;
     uint8_t* own = &sm.ostage[0][0] + (warp - 8) * 8192;
     if (lane == 0) prefetch_tmap(&amap);
     for (int i = wg; i < n; i += 2) {

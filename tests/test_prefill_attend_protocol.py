@@ -3,7 +3,10 @@
 Roles as in the kernel: the scheduler / TMA warp (K of a new block, the
 tile's Q rows, V of a new block), the S-MMA thread, the O-MMA thread, two
 softmax warpgroups and two epilogue warpgroups taking the even and the odd
-tiles (four warps each).  Tensor memory holds S (then P over it) and O twice;
+tiles (four warps each).  Tensor memory holds S twice, P (bf16) twice in
+columns of its own, and O once: a softmax warpgroup frees its S buffer as
+soon as it has read it, and the two epilogue warpgroups take turns on the one
+O buffer (each frees it through its own barrier);
 shared memory holds Q twice, K twice, V once, and per epilogue warp two 4 KB
 staging halves: per 32-column quarter of its rows the warp waits until the
 bulk group of two quarters ago has read the half it is about to fill
@@ -28,8 +31,8 @@ from _kernel_consts import kconst, mbar_count
 
 # the kernel's own values (prefill_attend.cu, bm_attend_kernel)
 INFO, QST, KST, VST = (kconst(n, "prefill_attend.cu") for n in ("kBmInfo", "kBmQStages", "kBmKStages", "kBmVStages"))
-O_FREE, P_FULL, INFO_EMPTY = (mbar_count(b, "prefill_attend.cu", after="bm_attend_kernel(")
-                              for b in ("o_free", "p_full", "info_empty"))
+O_FREE, P_FULL, S_FREE, INFO_EMPTY = (mbar_count(b, "prefill_attend.cu", after="bm_attend_kernel(")
+                                      for b in ("o_free", "p_full", "s_free", "info_empty"))
 
 
 class Bar:
@@ -63,10 +66,11 @@ class Sim:
             bar(f"v_empty{i}")
         for b in range(2):
             bar(f"s_full{b}")
-            bar(f"s_free{b}")
+            bar(f"s_free{b}", S_FREE)
             bar(f"o_full{b}")
             bar(f"o_free{b}", O_FREE)
             bar(f"p_full{b}", P_FULL)
+            bar(f"p_free{b}")
         for i in range(INFO):
             bar(f"info_full{i}")
             bar(f"info_empty{i}", INFO_EMPTY)
@@ -185,12 +189,14 @@ class Sim:
                 first = i
             b = i & 1
             yield self.wait(f"p_full{b}", (i >> 1) & 1, (i >> 1) + 1)
-            if not self.skip_o_free:
-                yield self.wait(f"o_free{b}", ((i >> 1) & 1) ^ 1, i >> 1)
-            self.mma("O", [(f"S{b}_{q}", ("P", i)) for q in range(4)] + [(f"V{vs}", ("V", first))],
-                     [(f"O{b}_{q}", ("O", i)) for q in range(4)])
+            if i > 0 and not self.skip_o_free:
+                # the one O buffer: the epilogue of tile i - 1 has read it
+                c = (i - 1) >> 1
+                yield self.wait(f"o_free{(i - 1) & 1}", c & 1, c + 1)
+            self.mma("O", [(f"P{b}_{q}", ("P", i)) for q in range(4)] + [(f"V{vs}", ("V", first))],
+                     [(f"O_{q}", ("O", i)) for q in range(4)])
             self.commit("O", f"o_full{b}")
-            self.commit("O", f"s_free{b}")
+            self.commit("O", f"p_free{b}")
 
     def softmax(self, wg, q):
         for i in range(wg, len(self.tiles), 2):
@@ -198,11 +204,14 @@ class Sim:
             yield self.wait(f"info_full{s}", u & 1, u + 1)
             self.bars[f"info_empty{s}"].arrive()
             yield self.wait(f"s_full{wg}", k & 1, k + 1)
+            yield self.wait(f"p_free{wg}", (k & 1) ^ 1, k)  # the O MMA of its previous tile has read P
             buf = f"S{wg}_{q}"
             self.warp_read(buf, ("S", i))
-            yield None  # two passes over the row
+            yield None  # the passes over the row, P written as it goes
+            self.warp_write(f"P{wg}_{q}", ("P", i))
             self.warp_read_end(buf)
-            self.warp_write(buf, ("P", i))  # P over the S columns this warp read
+            self.bars[f"s_free{wg}"].arrive()
+            yield None
             self.bars[f"p_full{wg}"].arrive()
 
     def epilogue(self, wg, q):
@@ -212,12 +221,12 @@ class Sim:
             yield self.wait(f"info_full{s}", u & 1, u + 1)
             self.bars[f"info_empty{s}"].arrive()
             yield self.wait(f"o_full{wg}", k & 1, k + 1)
-            self.warp_read(f"O{wg}_{q}", ("O", i))  # the warp's rows, one 32-column quarter at a time
+            self.warp_read(f"O_{q}", ("O", i))  # the warp's rows, one 32-column quarter at a time
             for qq in range(4):
                 yield None
-                assert self.tag.get(f"O{wg}_{q}") == ("O", i), f"O{wg}_{q} changed under the epilogue's reads"
+                assert self.tag.get(f"O_{q}") == ("O", i), f"O_{q} changed under the epilogue's reads"
                 if qq == 3:
-                    self.warp_read_end(f"O{wg}_{q}")
+                    self.warp_read_end(f"O_{q}")
                     self.bars[f"o_free{wg}"].arrive()
                 if not self.skip_bulk_wait:
                     # cp.async.bulk.wait_group.read 1: every group but the newest has read its half
