@@ -159,6 +159,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+      "[%7];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
 // Tiled tensor copy shared -> global (bulk group); the coordinates must be >= 0.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
@@ -336,6 +344,11 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;            // descriptor version
   d |= static_cast<uint64_t>(2) << 61;            // SWIZZLE_128B
   return d;
+}
+
+// The same with another distance between 8-row groups (a multiple of 1024).
+__device__ __forceinline__ uint64_t desc_k_sw128_sbo(uint32_t saddr, uint32_t sbo) {
+  return (desc_k_sw128(saddr) & ~(static_cast<uint64_t>(0x3FFF) << 32)) | (static_cast<uint64_t>(sbo >> 4) << 32);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.

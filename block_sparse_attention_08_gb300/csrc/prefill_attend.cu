@@ -61,6 +61,7 @@ constexpr int kBmEntries = 8;                     // entries per tile (8 x 16 he
 constexpr int kBmHalf = 128 * 128;                // 128 rows x 128 bytes (64 bf16) = 16 KB
 constexpr int kBmTile = 2 * kBmHalf;              // a 128 x 128 bf16 operand
 constexpr int kBmQBox = kGroup * 128;             // one entry's 16 rows x 64 dims = 2 KB
+constexpr int kBmQEntry = 2 * kBmQBox;            // one entry's Q rows, both halves: one 4 KB box
 // warps 0-7 softmax (two warpgroups, even / odd tiles), 8-15 epilogue (two
 // warpgroups), 16 TMA and scheduling, 17 the S MMAs, 18 the O MMAs
 constexpr int kBmThreads = 608;
@@ -589,11 +590,11 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         if (ok) mbar_expect_tx(&sm.q_full[qs], d.cnt * 2 * kBmQBox);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (lane < d.cnt) {
-        const int t = ent / topk;
-        tma_load_3d(sm.q[qs] + lane * kBmQBox, &qmap, 0, d.g * kGroup, t, &sm.q_full[qs]);
-        tma_load_3d(sm.q[qs] + kBmHalf + lane * kBmQBox, &qmap, 64, d.g * kGroup, t, &sm.q_full[qs]);
-      }
+      // one 4 KB box per entry: its 16 heads x 128 dims as four 8-row
+      // swizzle atoms (heads 0-7 dims 0-63, heads 0-7 dims 64-127, heads 8-15
+      // dims 0-63, heads 8-15 dims 64-127), so each half of the tile's rows
+      // has its atoms 2048 bytes apart
+      if (lane < d.cnt) tma_load_5d(sm.q[qs] + lane * kBmQEntry, &qmap, 0, 0, 0, 2 * d.g, ent / topk, &sm.q_full[qs]);
       __syncwarp();
       if (fresh) {
         prow = d.row0;
@@ -654,8 +655,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
         const uint32_t qa = smem_u32(sm.q[qs]), ka = smem_u32(sm.k[ks]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kBmHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + b * 128, tc::desc_k_sw128(qa + off), tc::desc_k_sw128(ka + off), kBmIdescS, kk > 0);
+          const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32, koff = (kk >> 2) * kBmHalf + (kk & 3) * 32;
+          tc::mma_bf16(tmem + b * 128, tc::desc_k_sw128_sbo(qa + qoff, 2048), tc::desc_k_sw128(ka + koff), kBmIdescS,
+                       kk > 0);
         }
         tc::commit(&sm.s_full[b]);
         tc::commit(&sm.q_empty[qs]);
@@ -897,6 +899,21 @@ __global__ void __launch_bounds__(256) bm_norm_kernel(BmPlan p, long long rows, 
 
 // ---- host side --------------------------------------------------------------------
 
+// q [T, 64 heads, 128] bf16 as (dims 0-63, head % 8, dims / 64, head / 8, token) with
+// a (64, 8, 2, 2, 1) box: one entry's 16 heads of a KV head as four 8-row
+// 128-byte-swizzled atoms, heads 0-7 then 8-15, each both halves of the dims.
+static bool encode_q_entry(CUtensorMap* map, const void* base, cuuint64_t T) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[5] = {64, 8, 2, kHeads / 8, T};
+  cuuint64_t strides[4] = {kDim * 2, 128, 8 * kDim * 2, kHeads * kDim * 2};
+  cuuint32_t box[5] = {64, 8, 2, 2, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool encode3d(CUtensorMap* map, const void* base, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
                      cuuint32_t b0, cuuint32_t b1, cuuint32_t b2) {
   EncodeTiledFn enc = get_encode_tiled();
@@ -940,7 +957,7 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   bm_carve(dims, region, &p);
   CUtensorMap qmap, kmap, vmap, amap;
   if (!encode3d_f32(&amap, p.acc, kDim, kHeads, total_tokens, 32, kGroup, 1) ||
-      !encode3d(&qmap, q, kDim, kHeads, total_tokens, 64, kGroup, 1) ||
+      !encode_q_entry(&qmap, q, total_tokens) ||
       !encode3d(&kmap, k, kDim, kKvHeads, total_tokens, 64, 1, kBlock) ||
       !encode3d(&vmap, v, kDim, kKvHeads, total_tokens, 64, 1, kBlock))
     return cudaErrorInvalidValue;
