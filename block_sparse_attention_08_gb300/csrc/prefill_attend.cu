@@ -21,15 +21,17 @@
 //
 // with S (twice), P (twice) and O (once) in tensor memory: a softmax warpgroup
 // frees its S buffer as soon as it has read it, so the next S product into it
-// waits for no O product, and the two epilogue warpgroups take turns on the
-// one O buffer.  Warp 16
+// waits for no O product, and both epilogue warpgroups read every tile's O
+// (half of its columns each), so the one O buffer is freed soon after its
+// product.  Warp 16
 // schedules the tiles (descriptors and entries read ahead from global memory,
 // published in a shared-memory ring) and issues TMA (Q rows gathered with a
-// 3-D tensor map, one 16-head box per entry; K and V blocks as 128-row boxes);
+// 5-D tensor map, one 4 KB box per entry; K and V blocks as 128-row boxes);
 // warps 17 and 18 issue the S and O MMAs from one thread each.  Two softmax
-// warpgroups (warps 0-7) and two epilogue warpgroups (warps 8-15) take the
-// even and the odd tiles, so two tiles are in their softmax and two in their
-// epilogue at a time; in each, a thread owns one tensor-memory lane (query row).
+// warpgroups (warps 0-7) take the even and the odd tiles, so two tiles are in
+// their softmax at a time; the two epilogue warpgroups (warps 8-15) take the
+// two halves of every tile's O; in each, a thread owns one tensor-memory lane
+// (query row).
 //
 // The entries of one (query, KV head) row land in up to topk different tiles,
 // so their results are summed in memory, in two launches against one fixed
@@ -104,7 +106,7 @@ struct BmSmem {
   alignas(1024) uint8_t ostage[2][kBmTile];  // 8 KB of fp32 staging per epilogue warp (two 4 KB halves)
   uint64_t q_full[kBmQStages], q_empty[kBmQStages], k_full[kBmKStages], k_empty[kBmKStages];
   uint64_t v_full[kBmVStages], v_empty[kBmVStages];
-  uint64_t s_full[2], s_free[2], o_full[2], o_free[2];
+  uint64_t s_full[2], s_free[2], o_full, o_free;
   uint64_t p_full[2], p_free[2], done_s, done_o;
   uint64_t info_full[kBmInfo], info_empty[kBmInfo];
   BmInfo info[kBmInfo];
@@ -505,8 +507,6 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 4);  // the softmax warpgroup's four warps, once they have read S
-      mbar_init(&sm.o_full[i], 1);
-      mbar_init(&sm.o_free[i], 4);
       mbar_init(&sm.p_full[i], 4);
       mbar_init(&sm.p_free[i], 1);  // committed by the O MMAs that read P
     }
@@ -514,9 +514,11 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
     }
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.o_free, 8);  // both epilogue warpgroups, once they have read their columns
     for (int i = 0; i < kBmInfo; ++i) {
       mbar_init(&sm.info_full[i], 1);
-      mbar_init(&sm.info_empty[i], 10);  // the tile's softmax and epilogue warpgroups, both MMA threads
+      mbar_init(&sm.info_empty[i], 14);  // the tile's softmax warpgroup, both epilogue warpgroups, both MMA threads
     }
     mbar_init(&sm.done_s, 1);
     mbar_init(&sm.done_o, 1);
@@ -685,8 +687,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
           ++nv;
         }
         const int b = i & 1;
-        if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, err, 714) ||
-            (i > 0 && !mbar_wait(&sm.o_free[(i - 1) & 1], ((i - 1) >> 1) & 1, err, 715)))
+        if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, err, 714) || !mbar_wait(&sm.o_free, (i & 1) ^ 1, err, 715))
           break;
         tc::fence_after();
         const uint32_t va = smem_u32(sm.v[vs]);
@@ -695,7 +696,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc::mma_bf16_ts(dt, pt + kk * 8, desc_v_mn_sw128(va + kk * 2048), kBmIdescO, kk > 0);
-        tc::commit(&sm.o_full[b]);
+        tc::commit(&sm.o_full);
         tc::commit(&sm.p_free[b]);
       }
       tc::commit(&sm.done_o);
@@ -812,18 +813,20 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
     }
   } else {
     // ---------------- warps 8-15: epilogue, fp32 O into the row accumulators ----------------
-    // Warpgroup wg takes the tiles i = wg, wg + 2, ... (O buffer wg).  Warp w
-    // owns 32 rows of the tile (entries 2 (w % 4) and 2 (w % 4) + 1): per
-    // 32-column quarter it copies its rows from tensor memory into one 4 KB
-    // half of its own 8 KB of staging (128-byte swizzle), and its lane 0 has
-    // the tensor engine store (phase 0) or add (phase 1) the two 16-row boxes
-    // into the fp32 accumulators [T][64][128].
+    // Both warpgroups take every tile, warpgroup wg the 32-column quarters 2 wg
+    // and 2 wg + 1 of O, so the O buffer is read (and freed for the next tile's
+    // product) in half the time one warpgroup would take.  Warp w owns 32 rows
+    // of the tile (entries 2 (w % 4) and 2 (w % 4) + 1): per quarter it copies
+    // its rows from tensor memory into one 4 KB half of its own 8 KB of staging
+    // (128-byte swizzle), and its lane 0 has the tensor engine store (phase 0)
+    // or add (phase 1) the two 16-row boxes into the fp32 accumulators
+    // [T][64][128].
     const int wg = (warp - 8) >> 2, quarter = warp & 3;
     const uint32_t orow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kBmOCol;
     uint8_t* own = &sm.ostage[0][0] + (warp - 8) * 8192;
     if (lane == 0) prefetch_tmap(&amap);
-    for (int i = wg; i < n; i += 2) {
-      const int is = i % kBmInfo, k = i >> 1;
+    for (int i = 0; i < n; ++i) {
+      const int is = i % kBmInfo;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.info_full[is], (i / kBmInfo) & 1, err, 724))) break;
       const int cnt = sm.info[is].cnt, g = sm.info[is].g;
       const int ea = 2 * quarter;
@@ -831,17 +834,17 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       const int tb = ea + 1 < cnt ? static_cast<int>(sm.info[is].ent[ea + 1] / topk) : -1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, 722))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, i & 1, err, 722))) break;
       tc::fence_after();
 #pragma unroll 1
-      for (int qq = 0; qq < 4; ++qq) {
+      for (int qq = 2 * wg; qq < 2 * wg + 2; ++qq) {
         uint32_t v[32];
         tc::ld_32x32b_x32(orow + qq * 32, v);
         tc::wait_ld();
-        if (qq == 3) {  // every column of the O buffer has been read
+        if (qq & 1) {  // this warp's columns of the O buffer have been read
           tc::fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.o_free[wg]);
+          if (lane == 0) mbar_arrive(&sm.o_free);
         }
         // this half was last read by the bulk group of two quarters ago
         if (lane == 0) bulk_wait_read_1();

@@ -2,11 +2,12 @@
 
 Roles as in the kernel: the scheduler / TMA warp (K of a new block, the
 tile's Q rows, V of a new block), the S-MMA thread, the O-MMA thread, two
-softmax warpgroups and two epilogue warpgroups taking the even and the odd
-tiles (four warps each).  Tensor memory holds S twice, P (bf16) twice in
-columns of its own, and O once: a softmax warpgroup frees its S buffer as
-soon as it has read it, and the two epilogue warpgroups take turns on the one
-O buffer (each frees it through its own barrier);
+softmax warpgroups taking the even and the odd tiles and two epilogue
+warpgroups taking every tile, half of its O columns each (four warps each).
+Tensor memory holds S twice, P (bf16) twice in columns of its own, and O
+once: a softmax warpgroup frees its S buffer as soon as it has read it, and
+both epilogue warpgroups have read a tile's O before the next O product may
+overwrite it;
 shared memory holds Q twice, K twice, V once, and per epilogue warp two 4 KB
 staging halves: per 32-column quarter of its rows the warp waits until the
 bulk group of two quarters ago has read the half it is about to fill
@@ -33,6 +34,7 @@ from _kernel_consts import kconst, mbar_count
 INFO, QST, KST, VST = (kconst(n, "prefill_attend.cu") for n in ("kBmInfo", "kBmQStages", "kBmKStages", "kBmVStages"))
 O_FREE, P_FULL, S_FREE, INFO_EMPTY = (mbar_count(b, "prefill_attend.cu", after="bm_attend_kernel(")
                                       for b in ("o_free", "p_full", "s_free", "info_empty"))
+assert O_FREE == 8 and INFO_EMPTY == 14
 
 
 class Bar:
@@ -67,10 +69,10 @@ class Sim:
         for b in range(2):
             bar(f"s_full{b}")
             bar(f"s_free{b}", S_FREE)
-            bar(f"o_full{b}")
-            bar(f"o_free{b}", O_FREE)
             bar(f"p_full{b}", P_FULL)
             bar(f"p_free{b}")
+        bar("o_full")
+        bar("o_free", O_FREE)
         for i in range(INFO):
             bar(f"info_full{i}")
             bar(f"info_empty{i}", INFO_EMPTY)
@@ -189,13 +191,12 @@ class Sim:
                 first = i
             b = i & 1
             yield self.wait(f"p_full{b}", (i >> 1) & 1, (i >> 1) + 1)
-            if i > 0 and not self.skip_o_free:
-                # the one O buffer: the epilogue of tile i - 1 has read it
-                c = (i - 1) >> 1
-                yield self.wait(f"o_free{(i - 1) & 1}", c & 1, c + 1)
+            if not self.skip_o_free:
+                # the one O buffer: both epilogue warpgroups have read tile i - 1's
+                yield self.wait("o_free", (i & 1) ^ 1, i)
             self.mma("O", [(f"P{b}_{q}", ("P", i)) for q in range(4)] + [(f"V{vs}", ("V", first))],
-                     [(f"O_{q}", ("O", i)) for q in range(4)])
-            self.commit("O", f"o_full{b}")
+                     [(f"O_{q}_{h}", ("O", i)) for q in range(4) for h in range(2)])
+            self.commit("O", "o_full")
             self.commit("O", f"p_free{b}")
 
     def softmax(self, wg, q):
@@ -216,18 +217,19 @@ class Sim:
 
     def epilogue(self, wg, q):
         w = (wg, q)
-        for i in range(wg, len(self.tiles), 2):
-            s, u, k = i % INFO, i // INFO, i >> 1
+        buf = f"O_{q}_{wg}"  # the warp's rows, the warpgroup's half of the columns
+        for i in range(len(self.tiles)):
+            s, u = i % INFO, i // INFO
             yield self.wait(f"info_full{s}", u & 1, u + 1)
             self.bars[f"info_empty{s}"].arrive()
-            yield self.wait(f"o_full{wg}", k & 1, k + 1)
-            self.warp_read(f"O_{q}", ("O", i))  # the warp's rows, one 32-column quarter at a time
-            for qq in range(4):
+            yield self.wait("o_full", i & 1, i + 1)
+            self.warp_read(buf, ("O", i))  # one 32-column quarter at a time
+            for qq in range(2):
                 yield None
-                assert self.tag.get(f"O_{q}") == ("O", i), f"O_{q} changed under the epilogue's reads"
-                if qq == 3:
-                    self.warp_read_end(f"O_{q}")
-                    self.bars[f"o_free{wg}"].arrive()
+                assert self.tag.get(buf) == ("O", i), f"{buf} changed under the epilogue's reads"
+                if qq == 1:
+                    self.warp_read_end(buf)
+                    self.bars["o_free"].arrive()
                 if not self.skip_bulk_wait:
                     # cp.async.bulk.wait_group.read 1: every group but the newest has read its half
                     newest = self.issued[w] - 1
