@@ -836,20 +836,23 @@ __global__ void __launch_bounds__(kBmThreads, 1) bm_attend_kernel(
       if (lane == 0) mbar_arrive(&sm.info_empty[is]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, i & 1, err, 722))) break;
       tc::fence_after();
-#pragma unroll 1
-      for (int qq = 2 * wg; qq < 2 * wg + 2; ++qq) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(orow + qq * 32, v);
-        tc::wait_ld();
-        if (qq & 1) {  // this warp's columns of the O buffer have been read
-          tc::fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.o_free);
-        }
+      // both quarters into registers first: the O buffer is freed before any
+      // staging waits on the tensor engine
+      uint32_t v2[2][32];
+      tc::ld_32x32b_x32(orow + 2 * wg * 32, v2[0]);
+      tc::ld_32x32b_x32(orow + (2 * wg + 1) * 32, v2[1]);
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int qq = 2 * wg + h2;
+        const uint32_t* v = v2[h2];
         // this half was last read by the bulk group of two quarters ago
         if (lane == 0) bulk_wait_read_1();
         __syncwarp();
-        uint8_t* half = own + (qq & 1) * 4096;
+        uint8_t* half = own + h2 * 4096;
         const uint32_t hs = smem_u32(half);
 #pragma unroll
         for (int j = 0; j < 8; ++j) sts128(hs + sw128(lane, j), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);

@@ -223,13 +223,12 @@ class Sim:
             yield self.wait(f"info_full{s}", u & 1, u + 1)
             self.bars[f"info_empty{s}"].arrive()
             yield self.wait("o_full", i & 1, i + 1)
-            self.warp_read(buf, ("O", i))  # one 32-column quarter at a time
+            self.warp_read(buf, ("O", i))  # both of its 32-column quarters into registers
+            yield None
+            assert self.tag.get(buf) == ("O", i), f"{buf} changed under the epilogue's reads"
+            self.warp_read_end(buf)
+            self.bars["o_free"].arrive()
             for qq in range(2):
-                yield None
-                assert self.tag.get(buf) == ("O", i), f"{buf} changed under the epilogue's reads"
-                if qq == 1:
-                    self.warp_read_end(buf)
-                    self.bars["o_free"].arrive()
                 if not self.skip_bulk_wait:
                     # cp.async.bulk.wait_group.read 1: every group but the newest has read its half
                     newest = self.issued[w] - 1
