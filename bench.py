@@ -820,6 +820,11 @@ def launches_per_step(decode):
     return 3 if decode else 10
 
 
+# Nominal figures of the part, reported beside the measured peaks (the fractions
+# against the measured copy and GEMM rates are the ones the roofline uses).
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
 def summarize(res, args, ms, e2e_ms, world):
     """value, dtype, roofline (the dominant call) and e2e of one measured workload."""
     unit = "query tokens/s"
@@ -845,6 +850,8 @@ def summarize(res, args, ms, e2e_ms, world):
                 "frac": round(ach / res["hbm_peak"], 4), "traffic": traffic,
                 "traffic_source": tr["capture"] + " (scaled by algorithmic bytes)" if traffic else None,
                 "peak_source": res["peak_src"] + " hbm_gbs (copy, burst)",
+                "nominal": {"peak": NOMINAL_HBM_GBS, "frac": round(ach / NOMINAL_HBM_GBS, 4),
+                            "source": "GB300 HBM3e nominal bandwidth"},
                 "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "bytes": b_sel, "GB/s": round(sel_r, 1)},
                                "attend": {"ms": round(res["att_ms"], 4), "bytes": b_att, "GB/s": round(att_r, 1)},
                                "step_GB/s": round((b_sel + b_att) / (ms * 1e-3) / 1e9, 1),
@@ -869,6 +876,8 @@ def summarize(res, args, ms, e2e_ms, world):
                 "frac": round(ach / res["tf_peak"], 4), "traffic": traffic,
                 "traffic_source": tr["capture"] + " (scaled by entries)" if traffic else None,
                 "peak_source": res["peak_src"] + " bf16_tflops (burst)",
+                "nominal": {"peak": NOMINAL_BF16_TFLOPS, "frac": round(ach / NOMINAL_BF16_TFLOPS, 4),
+                            "source": "GB300 dense bf16 nominal rate"},
                 "per_kernel": {"select": {"ms": round(res["sel_ms"], 4), "flop": f_sel, "TFLOP/s": round(sel_r, 2),
                                           # an E4M3 index runs the scorer's MMAs on the fp8 pipe: its peak is
                                           # the measured bf16 one times the nominal dense ratio (4.5 / 2.25)
