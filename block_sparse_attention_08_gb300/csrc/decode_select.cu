@@ -89,9 +89,11 @@ __device__ __forceinline__ int block_sum(int v, int* scan) {
 // bitonic network over its lanes; the need-th largest of the 32 is a threshold
 // that at least `need` candidates reach (so it keeps all of the top `need`),
 // those candidates (a few more than `need` as a rule) are gathered in shared
-// memory, and each is ranked against the others by its own thread.  (One warp
-// per row took 2-7 us on rows of 64-1024 candidates; ranking each of the 128
-// thread maxima against the others, 1200-4400 cycles.)
+// memory, and each is ranked against the others by its own thread.  A row of
+// at most 128 candidates skips the threshold: each candidate is ranked against
+// all of them at once.  (One warp per row took 2-7 us on rows of 64-1024
+// candidates; ranking each of the 128 thread maxima against the others,
+// 1200-4400 cycles.)
 constexpr int kTopkThreads = 128;
 constexpr int kTopkStage = 1024;
 
@@ -493,7 +495,20 @@ __global__ void __launch_bounds__(kTopkThreads) decode_topk_kernel(const float* 
   const int c_lo = init, c_hi = nb - local;  // non-forced candidates [c_lo, c_hi), more than `need` of them
   const bool staged = nb <= kTopkStage;
   auto key_at = [&](int b) { return score_key(staged ? stage[b] : __ldcg(row + b), b); };
-  if (need > 0) {
+  if (need > 0 && c_hi - c_lo <= kTopkThreads) {
+    // a short row: every candidate's key in shared memory, each ranked against
+    // all of them by its own thread (keys are distinct: ranks 0 .. need-1 are picked)
+    const int nc = c_hi - c_lo;
+    if (t < nc) tmax[t] = key_at(c_lo + t);
+    __syncthreads();
+    if (t < nc) {
+      const unsigned long long e = tmax[t];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < nc; ++j) rank += tmax[j] > e ? 1 : 0;
+      if (rank < need) ids[rank] = c_lo + t;
+    }
+  } else if (need > 0) {
     unsigned long long best = 0;  // real keys are nonzero; a thread without candidates keeps 0
     for (int b = c_lo + t; b < c_hi; b += kTopkThreads) {
       const unsigned long long key = key_at(b);
