@@ -24,9 +24,8 @@
 // max in registers and store one fp32 score per (request, head, page).  No
 // CTA-wide barrier sits in the loop.  A second kernel, launched as a
 // programmatic dependent so its launch overlaps the scorer's tail, runs the
-// top-k with one warp per (request, head): the need-th largest of the 32 lane
-// maxima is a threshold that filters the candidates, then an exact
-// (score desc, id asc) pick.
+// top-k with one CTA per (request, head) row: a threshold from 32 maxima of
+// the row filters the candidates, then an exact (score desc, id asc) pick.
 #include "launch.h"
 
 namespace msa {
@@ -34,7 +33,7 @@ namespace msa {
 constexpr int kSelConsumers = 6;  // a divisor of the stage counts (6 bf16, 12 E4M3)
 constexpr int kSelThreads = 32 * (kSelConsumers + 1);
 constexpr int kSelRingBytes = 192 * 1024;
-constexpr int kCandCap = 64;  // per-warp candidate list of the top-k filter
+constexpr int kCandCap = 64;  // the top-k's candidate list (a larger count takes its exact fallback)
 
 struct DecodeGeom {
   const int32_t* seq_lens;
