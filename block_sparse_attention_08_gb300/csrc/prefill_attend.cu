@@ -405,24 +405,26 @@ __global__ void __launch_bounds__(1024) bm_scan_kernel(BmPlan p) {
   }
 }
 
-// One thread per key: the tile descriptors of the key (K / V rows, KV head,
-// entry range).
+// One thread per tile: its key (the last whose first tile is at or before
+// it: keys without entries own no tile), then the tile's descriptor (K / V
+// rows, KV head, entry range).  (One thread per key, writing the key's tiles
+// in turn, left a few threads with dozens of tiles each.)
 __global__ void __launch_bounds__(256) bm_tiles_kernel(const int32_t* __restrict__ cu, int num_docs, int nw,
                                                        BmPlan p) {
-  const long long key = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= p.meta[1]) return;
   const int Kg = p.meta[0];
-  if (key >= static_cast<long long>(p.phases) * kKvHeads * Kg) return;
+  const int nkeys = p.phases * kKvHeads * Kg;
+  const int key = last_le(p.toff, nkeys, t);
   const int c = p.counts[key];
-  if (c == 0) return;
-  const long long kh = key % (static_cast<long long>(kKvHeads) * Kg);  // the key within its phase
-  const int g = static_cast<int>(kh / Kg), kk = static_cast<int>(kh - static_cast<long long>(g) * Kg);
+  const int i = static_cast<int>(t - p.toff[key]);
+  const int kh = key % (kKvHeads * Kg);  // the key within its phase
+  const int g = kh / Kg, kk = kh - g * Kg;
   const int w = last_le(p.wbase, nw, kk);
   const int gb = p.wlo[w] + kk - p.wbase[w];
   const int d = last_le(p.blk_base, num_docs, gb);
   const int row0 = cu[d] + (gb - p.blk_base[d]) * kBlock;
-  const int t0 = p.toff[key], o0 = p.offs[key];
-  for (int i = 0; i * kBmEntries < c; ++i)
-    p.tiles[t0 + i] = BmTile{row0, g, o0 + i * kBmEntries, min(kBmEntries, c - i * kBmEntries)};
+  p.tiles[t] = BmTile{row0, g, p.offs[key] + i * kBmEntries, min(kBmEntries, c - i * kBmEntries)};
 }
 
 // One thread per q2k entry: its place in the bucketed list.
@@ -978,7 +980,8 @@ cudaError_t launch_prefill_attend(const void* q, const void* k, const void* v, c
   bm_count_kernel<<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, stream>>>(q2k, cu_seqlens, num_docs,
                                                                                  total_tokens, topk, dims.W, p, err);
   bm_scan_kernel<<<1, 1024, 0, stream>>>(p);
-  bm_tiles_kernel<<<static_cast<unsigned>((keys + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs, dims.nw, p);
+  bm_tiles_kernel<<<static_cast<unsigned>((dims.tiles_max + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs,
+                                                                                          dims.nw, p);
   bm_scatter_kernel<<<static_cast<unsigned>((dims.entries + 255) / 256), 256, 0, stream>>>(
       dims.entries, total_tokens * topk, p);
   const size_t smem = sizeof(BmSmem) + 1024;
@@ -1545,7 +1548,8 @@ cudaError_t launch_prefill_backward(const void* q, const void* k, const void* v,
   bm_count_kernel<<<static_cast<unsigned>((kKvHeads * T + 255) / 256), 256, 0, stream>>>(
       q2k, cu_seqlens, num_docs, T, topk, dims.W, p, err);
   bm_scan_kernel<<<1, 1024, 0, stream>>>(p);
-  bm_tiles_kernel<<<static_cast<unsigned>((keys + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs, dims.nw, p);
+  bm_tiles_kernel<<<static_cast<unsigned>((dims.tiles_max + 255) / 256), 256, 0, stream>>>(cu_seqlens, num_docs,
+                                                                                          dims.nw, p);
   bm_scatter_kernel<<<static_cast<unsigned>((dims.entries + 255) / 256), 256, 0, stream>>>(dims.entries, T * topk,
                                                                                            p);
   bw_rowdot_kernel<<<static_cast<unsigned>((T * kHeads + 7) / 8), 256, 0, stream>>>(
