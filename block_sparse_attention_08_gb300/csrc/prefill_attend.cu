@@ -94,8 +94,8 @@ constexpr int kBmInfo = 8;  // info ring slots
 
 // Two Q stages, two K stages (the next block's K loads while the current one
 // is in use), one V stage (a block's V is needed a tile later than its K), and
-// one fp16 O staging tile per epilogue warpgroup for the TMA stores.  P lives
-// in tensor memory.
+// 8 KB of fp32 O staging per epilogue warp for the tensor engine's stores and
+// adds.  S, P and O live in tensor memory.
 constexpr int kBmQStages = 2;
 constexpr int kBmKStages = 2;
 constexpr int kBmVStages = 1;
